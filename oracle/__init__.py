@@ -1,0 +1,181 @@
+"""fp64 CPU oracle for block-sparse GQA decode attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py``
+may import this package.  The product path (``block_sparse_long_pool_gb300``) never
+does, and the two share no code: the oracle is plain C (``oracle.c``) built with gcc
+and called through ctypes on numpy arrays.
+
+Arrays of bf16 values travel as ``numpy.uint16`` holding the bf16 bit patterns, so
+the oracle sees the exact input values.  Every routine computes in double precision.
+What each routine follows on the pages is stated in ``oracle.c``:
+
+* ``pool``    -- SparDA notes, eq.(4): mean of each 64-token block's keys.
+* ``select``  -- SparDA notes, eq.(6) and Alg.1 step 2: Forecast scores, top-k
+  outside init/local blocks (ties to the lower index), union, ascending.
+* ``attn``    -- SparDA notes, eq.(7), scale 1/sqrt(d) from the SSV notes' NSA step 3.
+* ``verify``  -- SSV notes, mechanism 1, mode A (per-query sets plus window).
+* ``gather``  -- SparDA notes, §4.5: staging is a plain copy.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+D = 128
+BLK = 64
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``_build/liboracle.so`` with gcc (OpenMP, -O2, IEEE math)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-std=c11", "-O2", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def load_library(path: str):
+    """Load an oracle build from ``path`` and declare its C signatures."""
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    i32, i64, f64 = ctypes.c_int, ctypes.c_longlong, ctypes.c_double
+    lib.oracle_set_threads.argtypes = [i32]
+    lib.oracle_get_threads.restype = i32
+    lib.oracle_pool.argtypes = [P, i64, i32, P, i32, P]
+    lib.oracle_select.argtypes = [P, P, i32, i32, P, i32, i32, i32, i32, P, P, P]
+    lib.oracle_select.restype = i32
+    lib.oracle_attn.argtypes = [P, i32, P, P, i64, i32, P, P, i32, P, f64, P, P]
+    lib.oracle_verify.argtypes = [P, P, P, i64, i32, i32, i32, i32, P, i32, i32, i32, P,
+                                  f64, P, P, P]
+    lib.oracle_gather.argtypes = [P, i64, i32, P, P, i32, P]
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = load_library(build())
+        return _lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data) if a is not None else None
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError(f"bf16 inputs travel as uint16 bit patterns, got {a.dtype}")
+    return a
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _i64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int64))
+
+
+def set_threads(n: int) -> None:
+    _load().oracle_set_threads(int(n))
+
+
+def threads() -> int:
+    return int(_load().oracle_get_threads())
+
+
+def pool(K, lens, n_blocks_cap: int) -> np.ndarray:
+    """Compressed keys [P][n_blocks_cap][128] (fp64) from K [P][T_cap][128] (bf16 bits)."""
+    K = _u16(K)
+    lens = _i64(lens)
+    P, T_cap, d = K.shape
+    assert d == D and lens.shape == (P,)
+    out = np.empty((P, n_blocks_cap, D), dtype=np.float64)
+    _load().oracle_pool(_ptr(K), T_cap, P, _ptr(lens), n_blocks_cap, _ptr(out))
+    return out
+
+
+def select(F, ktil, lens, n_init: int, n_local: int, k: int, k_tot: int | None = None):
+    """Block selection.  Returns (idx [P][k_tot] int32, count [P] int32, scores [P][N] fp64)."""
+    F = _u16(F)
+    ktil = np.ascontiguousarray(ktil, dtype=np.float64)
+    lens = _i64(lens)
+    P, n_cap, d = ktil.shape
+    assert d == D and F.shape == (P, D) and lens.shape == (P,)
+    if k_tot is None:
+        k_tot = n_init + n_local + k
+    idx = np.empty((P, k_tot), dtype=np.int32)
+    count = np.empty((P,), dtype=np.int32)
+    scores = np.empty((P, n_cap), dtype=np.float64)
+    rc = _load().oracle_select(_ptr(F), _ptr(ktil), n_cap, P, _ptr(lens), n_init, n_local, k,
+                               k_tot, _ptr(idx), _ptr(count), _ptr(scores))
+    if rc != 0:
+        raise ValueError("oracle_select: a pair needs more than k_tot or n_blocks_cap entries")
+    return idx, count, scores
+
+
+def attn(Q, K, V, blocks, count, lens, scale: float | None = None):
+    """Attention of Q [P][G][128] over the listed blocks of K/V [P][T][128].
+
+    Returns (O [P][G][128] fp64, lse [P][G] fp64)."""
+    Q, K, V = _u16(Q), _u16(K), _u16(V)
+    blocks, count, lens = _i32(blocks), _i32(count), _i64(lens)
+    P, G, d = Q.shape
+    assert d == D and K.shape == V.shape and K.shape[0] == P and K.shape[2] == D
+    k_tot = blocks.shape[1]
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    O = np.empty((P, G, D), dtype=np.float64)
+    lse = np.empty((P, G), dtype=np.float64)
+    _load().oracle_attn(_ptr(Q), G, _ptr(K), _ptr(V), K.shape[1], P, _ptr(blocks), _ptr(count),
+                        k_tot, _ptr(lens), float(scale), _ptr(O), _ptr(lse))
+    return O, lse
+
+
+def verify(Q, K, V, I, C: int, window_blocks: int, lens, scale: float | None = None):
+    """Mode-A grouped verification.  Q [B][N_q][H_q][128], K/V [B][H_kv][T][128],
+    I [B][H_kv][N_q][n_sel].  Returns (O [B][N_q][H_q][128], union_blocks, per_query_blocks)."""
+    Q, K, V = _u16(Q), _u16(K), _u16(V)
+    I, lens = _i32(I), _i64(lens)
+    B, N_q, H_q, d = Q.shape
+    _, H_kv, T_cap, _ = K.shape
+    n_sel = I.shape[3]
+    assert d == D and I.shape[:3] == (B, H_kv, N_q) and lens.shape == (B,)
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    O = np.empty((B, N_q, H_q, D), dtype=np.float64)
+    u = np.zeros(1, dtype=np.int64)
+    pq = np.zeros(1, dtype=np.int64)
+    _load().oracle_verify(_ptr(Q), _ptr(K), _ptr(V), T_cap, B, H_q, H_kv, N_q, _ptr(I), n_sel,
+                          C, window_blocks, _ptr(lens), float(scale), _ptr(O), _ptr(u), _ptr(pq))
+    return O, int(u[0]), int(pq[0])
+
+
+def gather(src, idx, count, ring=None):
+    """Staging copy: src [P][T_host][128] bf16 bits -> ring [P][k_tot][64][128]."""
+    src = _u16(src)
+    idx, count = _i32(idx), _i32(count)
+    P, T_host, d = src.shape
+    k_tot = idx.shape[1]
+    if ring is None:
+        ring = np.zeros((P, k_tot, BLK, D), dtype=np.uint16)
+    assert ring.shape == (P, k_tot, BLK, D) and ring.dtype == np.uint16 and ring.flags.c_contiguous
+    _load().oracle_gather(_ptr(src), T_host, P, _ptr(idx), _ptr(count), k_tot, _ptr(ring))
+    return ring

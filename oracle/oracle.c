@@ -1,0 +1,388 @@
+/*
+ * oracle.c -- the plain, slow, double-precision CPU oracle for block-sparse GQA
+ * decode attention with learned block selection.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg load the library built from this file.  The product (the CUDA
+ * library under block_sparse_long_pool_gb300/csrc) never calls it, and the two
+ * share no code, header, table or helper.
+ *
+ * Every routine is the plain definition of one step, written as loops in double
+ * precision over the exact bf16 input values.  Sources (three web pages):
+ *   [SparDA] "SparDA: sparse decoupled attention" reading notes,
+ *            zhongzhuzhou.org/blog/2026-06-24 (Chinese).
+ *   [SSV]    "SSV: sparse speculative verification" reading notes,
+ *            zhongzhuzhou.org/blog/2026-07-01 (Chinese).
+ *
+ *   oracle_pool    [SparDA] background §3 eq.(4): a compressed key is the mean of
+ *                  the keys it covers; here one mean per non-overlapping 64-token
+ *                  block, over the tokens present (t < len).
+ *   oracle_select  [SparDA] §4.1 eq.(6) and §4.2 Alg.1 step 2: score the Forecast
+ *                  vector against every compressed key (one head per GQA group,
+ *                  §4.3 eq.(9)), take the k best blocks outside the init and local
+ *                  blocks, and return init ∪ local ∪ top-k in ascending order.
+ *   oracle_attn    [SparDA] §4.1 eq.(7): attention of each query head of the group
+ *                  over the tokens of the selected blocks, with the 1/sqrt(d) scale
+ *                  of [SSV] "NSA three-branch math" step 3.
+ *   oracle_verify  [SSV] mechanism 1, mode A: every (query, head) attends over its
+ *                  own block set I_q plus the sliding-window blocks; the group's
+ *                  merged union is what a grouped kernel has to load.
+ *   oracle_gather  [SparDA] §4.5: staging selected blocks is a plain copy.
+ *
+ * Readings where the pages are silent are stated at each routine.
+ * Fixed sizes: head dimension D = 128, block size BLK = 64 tokens.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define D 128
+#define BLK 64
+
+/* bf16 is the upper half of an IEEE-754 binary32: widen the bits, then the value. */
+static double bf16_value(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Number of 64-token blocks that hold at least one of the first len tokens. */
+static int blocks_of(long long len)
+{
+    return len <= 0 ? 0 : (int)((len + BLK - 1) / BLK);
+}
+
+void oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+int oracle_get_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Pooling, [SparDA] eq.(4).  K is [n_pairs][pair_stride][D] bf16 bits, len[p] the
+ * tokens present for pair p.  ktil is [n_pairs][n_blocks_cap][D]:
+ *   ktil[p][j][d] = (1/n_j) * sum_{t = 64j}^{min(64j+64, len)-1} K[p][t][d],
+ * n_j the number of those tokens.  Blocks with no token are written as zero.
+ */
+void oracle_pool(const uint16_t *K, long long pair_stride, int n_pairs,
+                 const long long *len, int n_blocks_cap, double *ktil)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int p = 0; p < n_pairs; ++p) {
+        const uint16_t *Kp = K + (size_t)p * (size_t)pair_stride * D;
+        double *out = ktil + (size_t)p * (size_t)n_blocks_cap * D;
+        int nb = blocks_of(len[p]);
+        for (int j = 0; j < n_blocks_cap; ++j) {
+            double sum[D];
+            long long n = 0;
+            for (int d = 0; d < D; ++d)
+                sum[d] = 0.0;
+            if (j < nb) {
+                long long end = (long long)(j + 1) * BLK;
+                if (end > len[p])
+                    end = len[p];
+                for (long long t = (long long)j * BLK; t < end; ++t) {
+                    for (int d = 0; d < D; ++d)
+                        sum[d] += bf16_value(Kp[(size_t)t * D + d]);
+                    ++n;
+                }
+            }
+            for (int d = 0; d < D; ++d)
+                out[(size_t)j * D + d] = n > 0 ? sum[d] / (double)n : 0.0;
+        }
+    }
+}
+
+typedef struct {
+    double s;
+    int j;
+} cand_t;
+
+/* Descending score; equal scores keep the lower block index first. */
+static int cand_order(const void *a, const void *b)
+{
+    const cand_t *x = (const cand_t *)a, *y = (const cand_t *)b;
+    if (x->s > y->s)
+        return -1;
+    if (x->s < y->s)
+        return 1;
+    return (x->j > y->j) - (x->j < y->j);
+}
+
+/*
+ * Selection, [SparDA] eq.(6) + Alg.1 step 2.
+ *   F     [n_pairs][D]  bf16 bits: one Forecast vector per (batch, KV head).
+ *   ktil  [n_pairs][n_blocks_cap][D] compressed keys of the layer being selected for.
+ *   len   tokens present per pair; N_b = ceil(len / 64).
+ * B_init  = blocks [0, n_init); B_local = the last n_local blocks [N_b-n_local, N_b)
+ * (the block holding token len-1 and the ones before it).  Candidates are all other
+ * blocks; s_j = sum_d F[d] * ktil[j][d]; the k candidates of largest score are taken,
+ * a full sort deciding ties towards the lower index (Alg.1 step 2 excludes init and
+ * local from the top-k, so the union has min(N_b, n_init+n_local+k) distinct blocks).
+ * Output idx[p][0..count) ascending, padded with -1 up to k_tot.  scores (nullable)
+ * receives s_j for every block j < N_b (the rest zero).
+ * Returns 0, or -1 when a pair needs more than k_tot or n_blocks_cap entries.
+ */
+int oracle_select(const uint16_t *F, const double *ktil, int n_blocks_cap, int n_pairs,
+                  const long long *len, int n_init, int n_local, int k, int k_tot,
+                  int *idx, int *count, double *scores)
+{
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int p = 0; p < n_pairs; ++p) {
+        int nb = blocks_of(len[p]);
+        int *out = idx + (size_t)p * k_tot;
+        if (nb > n_blocks_cap) {
+            bad |= 1;
+            count[p] = 0;
+            continue;
+        }
+        double Fp[D];
+        for (int d = 0; d < D; ++d)
+            Fp[d] = bf16_value(F[(size_t)p * D + d]);
+        char *chosen = (char *)calloc((size_t)nb + 1, 1);
+        cand_t *cand = (cand_t *)malloc(sizeof(cand_t) * ((size_t)nb + 1));
+        for (int j = 0; j < nb && j < n_init; ++j)
+            chosen[j] = 1;
+        for (int j = nb - n_local; j < nb; ++j)
+            if (j >= 0)
+                chosen[j] = 1;
+        int nc = 0;
+        for (int j = 0; j < nb; ++j) {
+            const double *kj = ktil + ((size_t)p * n_blocks_cap + j) * D;
+            double s = 0.0;
+            for (int d = 0; d < D; ++d)
+                s += Fp[d] * kj[d];
+            if (scores)
+                scores[(size_t)p * n_blocks_cap + j] = s;
+            if (!chosen[j]) {
+                cand[nc].s = s;
+                cand[nc].j = j;
+                ++nc;
+            }
+        }
+        if (scores)
+            for (int j = nb; j < n_blocks_cap; ++j)
+                scores[(size_t)p * n_blocks_cap + j] = 0.0;
+        qsort(cand, (size_t)nc, sizeof(cand_t), cand_order);
+        for (int r = 0; r < nc && r < k; ++r)
+            chosen[cand[r].j] = 1;
+        int c = 0;
+        for (int j = 0; j < nb; ++j) {
+            if (!chosen[j])
+                continue;
+            if (c < k_tot)
+                out[c] = j;
+            ++c;
+        }
+        if (c > k_tot) {
+            bad |= 1;
+            c = k_tot;
+        }
+        count[p] = c;
+        for (int r = c; r < k_tot; ++r)
+            out[r] = -1;
+        free(cand);
+        free(chosen);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * One query row q over the token set { t : block(t) in set, t < len }:
+ *   a_t = scale * <q, k_t>,  o = sum_t softmax(a)_t v_t,  lse = log sum_t exp(a_t).
+ * member[j] != 0 marks block j as part of the set (a set: each block counts once).
+ * An empty token set gives o = 0 and lse = -inf.
+ */
+static void attend_set(const uint16_t *q, const uint16_t *Kp, const uint16_t *Vp,
+                       const char *member, int nb, long long len, double scale,
+                       double *o, double *lse)
+{
+    double qd[D];
+    for (int d = 0; d < D; ++d)
+        qd[d] = bf16_value(q[d]);
+    long long ntok = 0;
+    for (int j = 0; j < nb; ++j)
+        if (member[j])
+            ntok += BLK;
+    double *a = (double *)malloc(sizeof(double) * (size_t)(ntok > 0 ? ntok : 1));
+    long long *tok = (long long *)malloc(sizeof(long long) * (size_t)(ntok > 0 ? ntok : 1));
+    long long n = 0;
+    double m = -INFINITY;
+    for (int j = 0; j < nb; ++j) {
+        if (!member[j])
+            continue;
+        for (long long t = (long long)j * BLK; t < (long long)(j + 1) * BLK && t < len; ++t) {
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d)
+                dot += qd[d] * bf16_value(Kp[(size_t)t * D + d]);
+            a[n] = scale * dot;
+            tok[n] = t;
+            if (a[n] > m)
+                m = a[n];
+            ++n;
+        }
+    }
+    for (int d = 0; d < D; ++d)
+        o[d] = 0.0;
+    if (n == 0) {
+        *lse = -INFINITY;
+    } else {
+        double L = 0.0;
+        for (long long i = 0; i < n; ++i) {
+            double w = exp(a[i] - m);
+            L += w;
+            for (int d = 0; d < D; ++d)
+                o[d] += w * bf16_value(Vp[(size_t)tok[i] * D + d]);
+        }
+        for (int d = 0; d < D; ++d)
+            o[d] /= L;
+        *lse = m + log(L);
+    }
+    free(tok);
+    free(a);
+}
+
+/*
+ * Sparse decode attention, [SparDA] eq.(7).
+ *   Q       [n_pairs][G][D] bf16 bits: the G query heads of KV head g of batch b
+ *           (query head h belongs to group floor(h / G), so [B][H_q][D] reshapes
+ *           to [B*H_kv][G][D] unchanged).
+ *   K, V    [n_pairs][pair_stride][D] bf16 bits, token t of a pair at row t.
+ *   blocks  [n_pairs][k_tot] logical block ids, count[p] of them valid.  The set
+ *           is what counts: a repeated id is one block; ids outside [0, N_b) hold
+ *           no token t < len and add nothing.
+ *   scale   multiplies q.k before the softmax; 1/sqrt(128) per the NSA formula.
+ *   O       [n_pairs][G][D];  lse [n_pairs][G] (nullable), natural log.
+ */
+void oracle_attn(const uint16_t *Q, int G, const uint16_t *K, const uint16_t *V,
+                 long long pair_stride, int n_pairs, const int *blocks, const int *count,
+                 int k_tot, const long long *len, double scale, double *O, double *lse)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int p = 0; p < n_pairs; ++p) {
+        int nb = blocks_of(len[p]);
+        char *member = (char *)calloc((size_t)nb + 1, 1);
+        for (int i = 0; i < count[p] && i < k_tot; ++i) {
+            int j = blocks[(size_t)p * k_tot + i];
+            if (j >= 0 && j < nb)
+                member[j] = 1;
+        }
+        const uint16_t *Kp = K + (size_t)p * (size_t)pair_stride * D;
+        const uint16_t *Vp = V + (size_t)p * (size_t)pair_stride * D;
+        for (int h = 0; h < G; ++h) {
+            double l;
+            attend_set(Q + ((size_t)p * G + h) * D, Kp, Vp, member, nb, len[p], scale,
+                       O + ((size_t)p * G + h) * D, &l);
+            if (lse)
+                lse[(size_t)p * G + h] = l;
+        }
+        free(member);
+    }
+}
+
+/*
+ * Grouped speculative verification, mode A, [SSV] mechanism 1.
+ *   Q   [B][N_q][H_q][D] bf16 bits: N_q verification queries per sequence, already in
+ *       the flattened (BFS) order; groups are queries [gC, gC+C).
+ *   K,V [B][H_kv][T_cap][D] bf16 bits (committed tokens only; draft tokens are not
+ *       in the cache and are not attended).
+ *   I   [B][H_kv][N_q][n_sel] per-query selected block ids.
+ *   The sliding window is the last window_blocks blocks of the committed sequence
+ *   (block-granular reading of "the last w tokens").  Query q, head h attends over
+ *   the set I_q ∪ W with the plain softmax of oracle_attn.
+ *   O   [B][N_q][H_q][D].
+ *   union_blocks     += |∪_{q in group} (I_q ∪ W)| summed over (b, KV head, group)
+ *   per_query_blocks += sum_q |I_q ∪ W| over the same: the loads without grouping.
+ */
+void oracle_verify(const uint16_t *Q, const uint16_t *K, const uint16_t *V, long long T_cap,
+                   int B, int H_q, int H_kv, int N_q, const int *I, int n_sel, int C,
+                   int window_blocks, const long long *len, double scale, double *O,
+                   long long *union_blocks, long long *per_query_blocks)
+{
+    int G = H_q / H_kv;
+    long long tot_union = 0, tot_query = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) reduction(+ : tot_union, tot_query)
+    for (int b = 0; b < B; ++b) {
+        for (int g = 0; g < H_kv; ++g) {
+            int nb = blocks_of(len[b]);
+            const uint16_t *Kp = K + ((size_t)b * H_kv + g) * (size_t)T_cap * D;
+            const uint16_t *Vp = V + ((size_t)b * H_kv + g) * (size_t)T_cap * D;
+            char *merged = (char *)calloc((size_t)nb + 1, 1);
+            char *member = (char *)calloc((size_t)nb + 1, 1);
+            for (int q0 = 0; q0 < N_q; q0 += C) {
+                memset(merged, 0, (size_t)nb + 1);
+                for (int q = q0; q < q0 + C && q < N_q; ++q) {
+                    memset(member, 0, (size_t)nb + 1);
+                    const int *Iq = I + (((size_t)b * H_kv + g) * N_q + q) * n_sel;
+                    for (int i = 0; i < n_sel; ++i)
+                        if (Iq[i] >= 0 && Iq[i] < nb)
+                            member[Iq[i]] = 1;
+                    for (int j = nb - window_blocks; j < nb; ++j)
+                        if (j >= 0)
+                            member[j] = 1;
+                    for (int j = 0; j < nb; ++j) {
+                        tot_query += member[j];
+                        merged[j] |= member[j];
+                    }
+                    for (int hh = 0; hh < G; ++hh) {
+                        int h = g * G + hh;
+                        double l;
+                        attend_set(Q + (((size_t)b * N_q + q) * H_q + h) * D, Kp, Vp, member, nb,
+                                   len[b], scale, O + (((size_t)b * N_q + q) * H_q + h) * D, &l);
+                    }
+                }
+                for (int j = 0; j < nb; ++j)
+                    tot_union += merged[j];
+            }
+            free(member);
+            free(merged);
+        }
+    }
+    if (union_blocks)
+        *union_blocks = tot_union;
+    if (per_query_blocks)
+        *per_query_blocks = tot_query;
+}
+
+/*
+ * Offload staging, [SparDA] §4.5: copy the K (or V) rows of the selected blocks from
+ * the host cache [n_pairs][T_host][D] into the staging layout [n_pairs][k_tot][64][D]:
+ * slot i of pair p holds block idx[p][i].  Rows past T_host are zero; slots at or
+ * beyond count[p] are left untouched.
+ */
+void oracle_gather(const uint16_t *src, long long T_host, int n_pairs, const int *idx,
+                   const int *count, int k_tot, uint16_t *ring)
+{
+    for (int p = 0; p < n_pairs; ++p) {
+        for (int i = 0; i < count[p] && i < k_tot; ++i) {
+            int j = idx[(size_t)p * k_tot + i];
+            uint16_t *dst = ring + (((size_t)p * k_tot + i) * BLK) * D;
+            for (int r = 0; r < BLK; ++r) {
+                long long t = (long long)j * BLK + r;
+                for (int d = 0; d < D; ++d)
+                    dst[(size_t)r * D + d] =
+                        (j >= 0 && t < T_host) ? src[((size_t)p * T_host + t) * D + d] : 0;
+            }
+        }
+    }
+}

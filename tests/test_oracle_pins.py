@@ -1,0 +1,421 @@
+"""Pins of the fp64 oracle against what the pages and mathematics fix (CPU, no GPU).
+
+Each pin checks the oracle against something other than itself: closed forms, a
+brute-force enumeration, a textbook/library routine (numpy mean, torch fp64 SDPA,
+logsumexp), the SSV page's worked example, or the SSV saving formula on inputs
+whose overlap is exact.  The mutation test at the end plants plausible mistakes in
+a copy of the oracle's C source and checks that the pins catch every one.
+"""
+import itertools
+import json
+import math
+import os
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_long_pool_gb300 import workloads as wl
+
+D, BLK = 128, 64
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bits(x) -> np.ndarray:
+    """Float values that bf16 represents exactly -> uint16 bf16 bit patterns."""
+    f = torch.as_tensor(np.asarray(x, dtype=np.float32))
+    t = f.to(torch.bfloat16)
+    assert torch.equal(t.float(), f), "test value not exact in bf16"
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def rand_bits(shape, seed) -> np.ndarray:
+    return wl.bf16_bits(wl.randn_bf16(shape, seed))
+
+
+def values(b: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def unit_forecast(P, dims_weights):
+    F = np.zeros((P, D), dtype=np.float32)
+    for d, w in dims_weights:
+        F[:, d] = w
+    return bits(F)
+
+
+# ----------------------------------------------------------------------------- pooling
+
+
+def test_pool_single_token_is_the_bf16_value():
+    K = rand_bits((3, 64, D), 1)
+    out = oracle.pool(K, [1, 1, 1], 1)
+    assert np.array_equal(out[:, 0], values(K)[:, 0])
+
+
+def test_pool_constant_keys():
+    K = bits(np.full((2, 256, D), 0.375))
+    out = oracle.pool(K, [200, 130], 4)
+    assert np.all(out[0] == 0.375)
+    assert np.all(out[1, :3] == 0.375) and np.all(out[1, 3] == 0.0)
+
+
+def test_pool_ramp_full_and_partial_blocks():
+    # K[t][d] = ((t mod 64) + 64 (d mod 2)) / 128: a full block averages to
+    # (31.5 + 64 (d mod 2)) / 128; a block holding r tokens to ((r-1)/2 + 64 (d mod 2)) / 128.
+    T = 5 * BLK
+    t = np.arange(T)[:, None]
+    d = np.arange(D)[None, :]
+    K = bits(((t % 64) + 64 * (d % 2)) / 128.0)[None]
+    for r in (1, 17, 63, 64):
+        length = 4 * BLK + r
+        out = oracle.pool(K, [length], 5)[0]
+        full = (31.5 + 64 * (np.arange(D) % 2)) / 128.0
+        part = ((r - 1) / 2.0 + 64 * (np.arange(D) % 2)) / 128.0
+        assert np.array_equal(out[:4], np.broadcast_to(full, (4, D)))
+        assert np.allclose(out[4], part, rtol=0, atol=1e-15)
+
+
+def test_pool_matches_numpy_block_means_ragged():
+    K = rand_bits((3, 7 * BLK, D), 2)
+    lens = [7 * BLK, 3 * BLK + 5, 1]
+    out = oracle.pool(K, lens, 7)
+    Kv = values(K)
+    for p, n in enumerate(lens):
+        for j in range(7):
+            rows = Kv[p, j * BLK: min((j + 1) * BLK, n)]
+            ref = rows.mean(axis=0) if len(rows) else np.zeros(D)
+            assert np.allclose(out[p, j], ref, rtol=1e-13, atol=1e-15)
+
+
+# ----------------------------------------------------------------------------- scores
+
+
+def test_scores_unit_vector_reads_one_dimension():
+    ktil = np.random.default_rng(3).standard_normal((2, 20, D))
+    _, _, s = oracle.select(unit_forecast(2, [(5, 1.0)]), ktil, [20 * BLK] * 2, 1, 2, 4)
+    assert np.array_equal(s, ktil[:, :, 5])
+
+
+def test_scores_two_term_combination():
+    ktil = np.random.default_rng(4).standard_normal((2, 9, D))
+    _, _, s = oracle.select(unit_forecast(2, [(3, 2.0), (100, -0.5)]), ktil, [9 * BLK] * 2, 1, 2, 2)
+    assert np.array_equal(s, 2.0 * ktil[:, :, 3] + (-0.5) * ktil[:, :, 100])
+
+
+def test_scores_match_matrix_product():
+    rng = np.random.default_rng(5)
+    F = rand_bits((3, D), 5)
+    ktil = rng.standard_normal((3, 33, D))
+    _, _, s = oracle.select(F, ktil, [33 * BLK] * 3, 1, 2, 8)
+    ref = np.einsum("pd,pjd->pj", values(F), ktil)
+    assert np.allclose(s, ref, rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- top-k
+
+
+def _brute_topk(s, cands, k):
+    """Best k-subset by exact total score; among equal totals the lexicographically
+    smallest ascending tuple (equivalently: ties go to the lower block index)."""
+    if len(cands) <= k:
+        return tuple(sorted(cands))
+    best = None
+    for sub in itertools.combinations(sorted(cands), k):
+        tot = sum(s[j] for j in sub)
+        if best is None or tot > best[0] or (tot == best[0] and sub < best[1]):
+            best = (tot, sub)
+    return best[1]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_topk_equals_brute_force_with_ties(seed):
+    rng = np.random.default_rng(100 + seed)
+    N, n_init, n_local, k = 13, 1, 2, 4
+    ktil = np.zeros((1, N, D))
+    ktil[0, :, 0] = rng.integers(-3, 4, size=N)      # small integers: many exact ties
+    idx, count, s = oracle.select(unit_forecast(1, [(0, 1.0)]), ktil, [N * BLK], n_init, n_local, k)
+    forced = set(range(n_init)) | set(range(N - n_local, N))
+    cands = [j for j in range(N) if j not in forced]
+    expect = sorted(forced | set(_brute_topk(s[0], cands, k)))
+    assert count[0] == n_init + n_local + k
+    assert list(idx[0, :count[0]]) == expect
+
+
+def test_topk_all_equal_scores_take_lowest_indices():
+    N = 40
+    idx, count, _ = oracle.select(unit_forecast(1, [(7, 1.0)]), np.zeros((1, N, D)), [N * BLK], 1, 2, 5)
+    assert list(idx[0, :count[0]]) == [0, 1, 2, 3, 4, 5, 38, 39]
+
+
+def test_topk_excludes_init_and_local_blocks():
+    N, k = 30, 6
+    ktil = np.zeros((1, N, D))
+    ktil[0, :, 0] = np.arange(N) * 0.25
+    ktil[0, 0, 0] = 1e6          # init block scores highest ...
+    ktil[0, N - 1, 0] = 1e6      # ... and so do the local blocks,
+    ktil[0, N - 2, 0] = 1e6      # yet they must not take top-k slots
+    idx, count, _ = oracle.select(unit_forecast(1, [(0, 1.0)]), ktil, [N * BLK], 1, 2, k)
+    assert count[0] == 1 + 2 + k
+    assert list(idx[0, :count[0]]) == [0] + list(range(N - 2 - k, N - 2)) + [N - 2, N - 1]
+
+
+def test_local_blocks_follow_the_partial_last_block():
+    # len = 10 blocks + 1 token: N_b = 11, local = blocks 9 and 10.
+    N = 11
+    ktil = np.zeros((1, 12, D))
+    ktil[0, :N, 0] = -np.arange(N)   # candidate 1 scores best
+    idx, count, _ = oracle.select(unit_forecast(1, [(0, 1.0)]), ktil, [10 * BLK + 1], 1, 2, 1)
+    assert list(idx[0, :count[0]]) == [0, 1, 9, 10]
+
+
+@pytest.mark.parametrize("N,expect", [(7, list(range(7))), (2, [0, 1]), (1, [0])])
+def test_select_takes_every_block_when_few(N, expect):
+    ktil = np.random.default_rng(6).standard_normal((1, 8, D))
+    idx, count, _ = oracle.select(rand_bits((1, D), 6), ktil, [N * BLK], 1, 2, 8)
+    assert list(idx[0, :count[0]]) == expect
+    assert np.all(idx[0, count[0]:] == -1)
+
+
+def test_select_empty_sequence():
+    idx, count, _ = oracle.select(rand_bits((1, D), 7), np.zeros((1, 4, D)), [0], 1, 2, 3)
+    assert count[0] == 0 and np.all(idx == -1)
+
+
+def test_select_invariants_on_single_layer_workload():
+    sh = wl.SINGLE_4K
+    inp = wl.single_layer(sh)
+    K = wl.bf16_bits(inp["K"]).reshape(sh.pairs, sh.T_cap, D)
+    ktil = oracle.pool(K, [sh.T] * sh.pairs, sh.N_b)
+    F = wl.bf16_bits(inp["F"]).reshape(sh.pairs, D)
+    idx, count, _ = oracle.select(F, ktil, [sh.T] * sh.pairs, sh.n_init, sh.n_local, sh.k)
+    for p in range(sh.pairs):
+        sel = list(idx[p, :count[p]])
+        assert count[p] == sh.k_tot == 11
+        assert sel == sorted(set(sel))
+        assert {0, sh.N_b - 2, sh.N_b - 1} <= set(sel)
+        # sanity of the generator, not a pin: most planted blocks are the ones found
+        assert len(set(inp["planted"][p].tolist()) & set(sel)) >= sh.n_planted - 2
+
+
+# ----------------------------------------------------------------------------- attention
+
+
+def _sdpa(Qv, Kv, Vv, token_mask, scale=None):
+    """torch fp64 scaled_dot_product_attention; Qv [G][D], Kv/Vv [T][D], mask [T]."""
+    q = torch.from_numpy(Qv)[None, :, None, :]                 # [1][G][1][D]
+    k = torch.from_numpy(Kv)[None, None].expand(1, Qv.shape[0], -1, -1)
+    v = torch.from_numpy(Vv)[None, None].expand(1, Qv.shape[0], -1, -1)
+    m = torch.from_numpy(token_mask)[None, None, None, :]
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=m, scale=scale)
+    return o[0, :, 0].numpy()
+
+
+def _lse(Qv, Kv, token_mask, scale):
+    a = torch.from_numpy(Qv @ Kv[token_mask].T * scale)
+    return torch.logsumexp(a, dim=-1).numpy()
+
+
+def test_attn_all_blocks_equals_dense_sdpa():
+    P, G, T = 3, 4, 5 * BLK + 17
+    Q, K, V = rand_bits((P, G, D), 10), rand_bits((P, T, D), 11), rand_bits((P, T, D), 12)
+    lens = [T, T - 40, 3 * BLK]
+    nb = (T + BLK - 1) // BLK
+    blocks = np.tile(np.arange(nb, dtype=np.int32), (P, 1))
+    O, lse = oracle.attn(Q, K, V, blocks, [nb] * P, lens)
+    for p in range(P):
+        mask = np.arange(T) < lens[p]
+        ref = _sdpa(values(Q[p]), values(K[p]), values(V[p]), mask)
+        assert np.allclose(O[p], ref, rtol=1e-11, atol=1e-12)
+        assert np.allclose(lse[p], _lse(values(Q[p]), values(K[p]), mask, 1 / math.sqrt(D)),
+                           rtol=1e-12, atol=1e-12)
+
+
+def test_attn_block_subset_equals_masked_sdpa_and_ignores_order_and_repeats():
+    P, G, T = 2, 8, 9 * BLK
+    Q, K, V = rand_bits((P, G, D), 13), rand_bits((P, T, D), 14), rand_bits((P, T, D), 15)
+    blocks = np.array([[7, 2, 5, 2, -1], [8, 0, 3, 3, 6]], dtype=np.int32)
+    O, _ = oracle.attn(Q, K, V, blocks, [5, 5], [T, T - 30])
+    for p, n in enumerate([T, T - 30]):
+        chosen = {j for j in blocks[p] if j >= 0}
+        mask = np.array([(t // BLK) in chosen and t < n for t in range(T)])
+        assert np.allclose(O[p], _sdpa(values(Q[p]), values(K[p]), values(V[p]), mask),
+                           rtol=1e-11, atol=1e-12)
+
+
+def test_attn_scale_argument_is_applied():
+    Q, K, V = rand_bits((1, 2, D), 16), rand_bits((1, BLK, D), 17), rand_bits((1, BLK, D), 18)
+    O, _ = oracle.attn(Q, K, V, np.zeros((1, 1), np.int32), [1], [BLK], scale=0.3)
+    ref = _sdpa(values(Q[0]), values(K[0]), values(V[0]), np.ones(BLK, bool), scale=0.3)
+    assert np.allclose(O[0], ref, rtol=1e-11, atol=1e-12)
+
+
+def test_attn_equal_keys_give_mean_of_values():
+    T = 4 * BLK
+    K = np.repeat(rand_bits((1, 1, D), 19), T, axis=1)
+    Q, V = rand_bits((1, 3, D), 20), rand_bits((1, T, D), 21)
+    blocks = np.array([[1, 3]], dtype=np.int32)
+    O, _ = oracle.attn(Q, K, V, blocks, [2], [T - 10])
+    rows = [t for t in range(T) if t // BLK in (1, 3) and t < T - 10]
+    assert np.allclose(O[0], np.broadcast_to(values(V[0, rows]).mean(axis=0), (3, D)),
+                       rtol=1e-12, atol=1e-13)
+
+
+def test_attn_constant_values_and_single_token():
+    T = 2 * BLK
+    Q, K = rand_bits((1, 4, D), 22), rand_bits((1, T, D), 23)
+    V = bits(np.full((1, T, D), -1.25))
+    O, _ = oracle.attn(Q, K, V, np.array([[0, 1]], np.int32), [2], [T])
+    assert np.allclose(O, -1.25, rtol=0, atol=1e-14)
+    V = rand_bits((1, T, D), 24)
+    O, lse = oracle.attn(Q, K, V, np.array([[0, 1]], np.int32), [2], [1])
+    assert np.array_equal(O[0], np.broadcast_to(values(V[0, 0]), (4, D)))
+    assert np.allclose(lse[0], values(Q[0]) @ values(K[0, 0]) / math.sqrt(D), rtol=1e-13)
+
+
+def test_attn_empty_set_gives_zero_and_minus_inf():
+    Q, K, V = rand_bits((1, 2, D), 25), rand_bits((1, BLK, D), 26), rand_bits((1, BLK, D), 27)
+    O, lse = oracle.attn(Q, K, V, np.full((1, 3), -1, np.int32), [0], [BLK])
+    assert np.all(O == 0) and np.all(np.isneginf(lse))
+
+
+# ----------------------------------------------------------------------------- verification
+
+
+def test_verify_worked_example_of_the_ssv_page():
+    ex = json.load(open(os.path.join(GOLDEN, "ssv_worked_example.json")))
+    sets = ex["queries"]
+    loads = {}
+    for s in sets:
+        for j in s:
+            loads[j] = loads.get(j, 0) + 1
+    for j, n in ex["printed_load_counts"].items():
+        assert loads[int(j)] == n
+    T = 24 * BLK
+    Q, K, V = rand_bits((1, 4, 1, D), 30), rand_bits((1, 1, T, D), 31), rand_bits((1, 1, T, D), 32)
+    I = np.array(sets, dtype=np.int32)[None, None]
+    O, union, per_query = oracle.verify(Q, K, V, I, C=4, window_blocks=0, lens=[T])
+    assert union == len(ex["derived"]["merged_union"]) == 10
+    assert per_query == ex["derived"]["ungrouped_loads"] == 16
+
+
+@pytest.mark.parametrize("gamma,n_sel,window", [(0.75, 16, 0), (0.75, 16, 512), (0.5, 8, 0),
+                                                (0.875, 16, 0)])
+def test_verify_saving_formula_on_core_private_overlap(gamma, n_sel, window):
+    # SSV notes, grouping saving: merged / ungrouped = (1 + (C-1)(1-gamma)) / C.
+    sh = wl.VerifyShape("t", B=2, H_q=4, H_kv=2, T=64 * BLK, N_q=8, n_sel=n_sel, gamma=gamma,
+                        window_tokens=window, C=4)
+    T = sh.T
+    I = wl.verify_sets(sh).numpy()
+    Q = rand_bits((sh.B, sh.N_q, sh.H_q, D), 33)
+    K = rand_bits((sh.B, sh.H_kv, T, D), 34)
+    _, union, per_query = oracle.verify(Q, K, K, I, sh.C, sh.window_blocks, [T] * sh.B)
+    groups = sh.B * sh.H_kv * (sh.N_q // sh.C)
+    w = sh.window_blocks
+    assert union == groups * (n_sel * (1 + (sh.C - 1) * (1 - gamma)) + w)
+    assert per_query == groups * sh.C * (n_sel + w)
+    if w == 0:
+        assert union / per_query == pytest.approx((1 + (sh.C - 1) * (1 - gamma)) / sh.C, abs=1e-15)
+    if (gamma, n_sel, window) == (0.75, 16, 512):
+        assert union / per_query == 36 / 96
+
+
+def test_verify_equals_masked_sdpa_per_query():
+    B, N_q, H_q, H_kv, T, C, wb = 1, 4, 4, 2, 12 * BLK, 2, 2
+    G = H_q // H_kv
+    Q, K, V = rand_bits((B, N_q, H_q, D), 35), rand_bits((B, H_kv, T, D), 36), rand_bits((B, H_kv, T, D), 37)
+    I = np.array([[[[1, 4], [1, 5], [2, 4], [0, 9]], [[3, 6], [3, 7], [0, 6], [5, 8]]]], np.int32)
+    O, union, per_query = oracle.verify(Q, K, V, I, C, wb, [T - 20])
+    n = T - 20
+    for g in range(H_kv):
+        for q in range(N_q):
+            chosen = set(I[0, g, q].tolist()) | {10, 11}
+            mask = np.array([(t // BLK) in chosen and t < n for t in range(T)])
+            ref = _sdpa(values(Q[0, q, g * G:(g + 1) * G]), values(K[0, g]), values(V[0, g]), mask)
+            assert np.allclose(O[0, q, g * G:(g + 1) * G], ref, rtol=1e-11, atol=1e-12)
+    assert per_query == 2 * 4 * 4
+
+
+# ----------------------------------------------------------------------------- gather
+
+
+def test_gather_is_a_plain_copy():
+    P, T_host = 2, 5 * BLK + 9
+    src = rand_bits((P, T_host, D), 40)
+    idx = np.array([[4, 0, 5, -1], [2, 5, 1, 3]], dtype=np.int32)
+    count = np.array([3, 4], np.int32)
+    ring = oracle.gather(src, idx, count)
+    for p in range(P):
+        for i in range(count[p]):
+            j = idx[p, i]
+            rows = src[p, j * BLK: min((j + 1) * BLK, T_host)]
+            assert np.array_equal(ring[p, i, :len(rows)], rows)
+            assert np.all(ring[p, i, len(rows):] == 0)
+    assert np.all(ring[0, 3] == 0)
+
+
+# ----------------------------------------------------------------------------- mutants
+
+MUTANTS = [
+    # pooling divides by the full block size instead of the tokens present
+    ("sum[d] / (double)n", "sum[d] / (double)BLK"),
+    # score reads the wrong operand dimension
+    ("s += Fp[d] * kj[d];", "s += Fp[d] * kj[(d + 1) % D];"),
+    # ties go to the higher block index
+    ("return (x->j > y->j) - (x->j < y->j);", "return (x->j < y->j) - (x->j > y->j);"),
+    # the local window is one block short
+    ("for (int j = nb - n_local; j < nb; ++j)\n            if (j >= 0)\n                chosen[j] = 1;",
+     "for (int j = nb - n_local + 1; j < nb; ++j)\n            if (j >= 0)\n                chosen[j] = 1;"),
+    # the softmax scale is dropped
+    ("a[n] = scale * dot;", "a[n] = dot;"),
+    # values read from the key cache
+    ("o[d] += w * bf16_value(Vp[", "o[d] += w * bf16_value(Kp["),
+    # the length mask is off by one
+    ("t < (long long)(j + 1) * BLK && t < len;", "t < (long long)(j + 1) * BLK && t <= len;"),
+    # the verification window forgets its first block
+    ("for (int j = nb - window_blocks; j < nb; ++j)", "for (int j = nb - window_blocks + 1; j < nb; ++j)"),
+    # the bf16 widening uses the wrong half
+    ("uint32_t u = (uint32_t)bits << 16;", "uint32_t u = (uint32_t)bits << 15;"),
+]
+
+PIN_TESTS = [
+    test_pool_single_token_is_the_bf16_value, test_pool_constant_keys, test_pool_ramp_full_and_partial_blocks,
+    test_pool_matches_numpy_block_means_ragged, test_scores_unit_vector_reads_one_dimension,
+    test_scores_two_term_combination, test_scores_match_matrix_product,
+    test_topk_all_equal_scores_take_lowest_indices, test_topk_excludes_init_and_local_blocks,
+    test_local_blocks_follow_the_partial_last_block, test_attn_all_blocks_equals_dense_sdpa,
+    test_attn_block_subset_equals_masked_sdpa_and_ignores_order_and_repeats,
+    test_attn_scale_argument_is_applied, test_attn_equal_keys_give_mean_of_values,
+    test_attn_constant_values_and_single_token, test_verify_worked_example_of_the_ssv_page,
+    test_verify_equals_masked_sdpa_per_query,
+]
+
+
+@pytest.mark.parametrize("m", range(len(MUTANTS)))
+def test_pins_catch_planted_oracle_mistakes(m, tmp_path, monkeypatch):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")).read()
+    before, after = MUTANTS[m]
+    assert before in src, f"mutant {m}: pattern not found"
+    c_path, so_path = tmp_path / "mutant.c", tmp_path / "mutant.so"
+    c_path.write_text(src.replace(before, after))
+    subprocess.run(["gcc", "-std=c11", "-O2", "-fopenmp", "-fPIC", "-shared", str(c_path), "-o",
+                    str(so_path), "-lm"], check=True)
+    monkeypatch.setattr(oracle, "_lib", oracle.load_library(str(so_path)))
+    caught = []
+    for t in PIN_TESTS:
+        try:
+            t()
+        except (AssertionError, ValueError):
+            caught.append(t.__name__)
+    try:
+        test_verify_saving_formula_on_core_private_overlap(0.75, 16, 512)
+    except AssertionError:
+        caught.append("saving_formula")
+    for seed in range(3):
+        try:
+            test_topk_equals_brute_force_with_ties(seed)
+        except AssertionError:
+            caught.append("brute_force")
+    assert caught, f"mutant {m} ({after!r}) passed every pin"
