@@ -1,0 +1,495 @@
+#!/usr/bin/env python
+"""Benchmark of the block-sparse GQA decode path on one GB300 (or N replicas).
+
+Default workload: one 128K decode step of a 70B-shaped model (80 layers, B=8,
+H_q=64, H_kv=8, d=128, T=131072, top-64 + 1 init + 2 local blocks).  A step runs, for
+every layer l, the Forecast selection for layer l+1 (sparse_select_topk on a side
+stream, allowed to start once attention of layer l-1 is done) overlapped with the
+block-sparse attention of layer l (sparse_decode_attn on the main stream); layer 0
+first selects with its own current-layer Forecast.  The 80-layer step is one CUDA
+graph.  80 logical layers are backed by 10 physical KV layers (logical l reads
+physical l mod 10): the literal B=8 x 80-layer x 128K cache is 343.6 GB.
+
+Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle instead, on a
+bounded sample per step, and prints the same metric for it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode attn steps/sec and selected-KV HBM GB/s (fraction of 8 TB/s) at 128K"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+D, BLK = 128, 64
+KV_BLOCK_BYTES = 2 * BLK * D * 2      # K + V of one selected block (bf16)
+KTIL_ROW_BYTES = D * 4                # one fp32 compressed key
+
+
+# ----------------------------------------------------------------------------- ranks
+
+
+def dist_env():
+    """(rank, world, local_rank) from the torchrun environment (1 process = 1 GPU)."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a float over all ranks (replicas time independently; the slowest counts)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- helpers
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha1()
+    for f in ("sparse_attn.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "block_sparse_long_pool_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_hash: str):
+    """DRAM bytes per attention launch from the committed ncu summary, if it was taken
+    on the current kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "decode_attn_128k_traffic.txt")
+    try:
+        kv = {}
+        for line in open(path):
+            if ":" in line:
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha1") != kernel_hash:
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- 128K decode workload
+
+
+class Decode128k:
+    """Device state of the 80-layer 128K decode step and its CUDA graph."""
+
+    def __init__(self, device):
+        import torch
+        from block_sparse_long_pool_gb300 import binding
+        from block_sparse_long_pool_gb300 import workloads as wl
+
+        self.torch, self.binding, self.wl = torch, binding, wl
+        sh = self.sh = wl.DECODE_128K
+        self.dev = device
+        B, H_kv, H_q, T = sh.B, sh.H_kv, sh.H_q, sh.T
+        self.k_cap = sh.n_init + sh.n_local + sh.k
+        P = sh.phys_layers
+        planted = wl.planted_sets(sh, P)
+        self.k_cache, self.v_cache, self.ktil = [], [], []
+        for q in range(P):
+            kc = torch.empty((B, H_kv, T, D), dtype=torch.bfloat16, device=device)
+            vc = torch.empty_like(kc)
+            kt = torch.zeros((B, H_kv, sh.N_b, D), dtype=torch.float32, device=device)
+            for b in range(B):
+                kn = torch.empty((1, H_kv, T, D), dtype=torch.bfloat16, device=device)
+                vn = torch.empty_like(kn)
+                for h in range(H_kv):
+                    pr = b * H_kv + h
+                    kn[0, h], vn[0, h] = wl.kv_pair(sh, q, pr, planted[q, pr], device)
+                binding.sparse_pool_append(kc[b:b + 1], vc[b:b + 1], kt[b:b + 1], kn, vn, 0)
+                del kn, vn
+            self.k_cache.append(kc)
+            self.v_cache.append(vc)
+            self.ktil.append(kt)
+        L = sh.layers
+        # per-step inputs: Q_l and F_l (F_l targets layer l+1), F^cur_0; outputs O_l
+        self.Q = torch.stack([wl.queries(sh, l, device) for l in range(L)])            # [L][B][H_q][D]
+        self.F = torch.stack([wl.forecast(sh, (l + 1) % P, l, device) for l in range(L)])  # [L][B][H_kv][D]
+        self.F0 = wl.forecast(sh, 0, -1, device)
+        self.O = torch.zeros((L, B, H_q, D), dtype=torch.bfloat16, device=device)
+        self.idx = torch.full((L, B, H_kv, self.k_cap), -1, dtype=torch.int32, device=device)
+        self.count = torch.zeros((L, B, H_kv), dtype=torch.int32, device=device)
+        self.seq = torch.full((B,), T, dtype=torch.int32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.side = torch.cuda.Stream(device=device)
+        torch.cuda.synchronize(device)
+
+    # bytes the method has to move per step
+    def algorithmic_bytes(self):
+        sh = self.sh
+        attn = sh.layers * sh.pairs * sh.k_tot * KV_BLOCK_BYTES
+        sel = (sh.layers) * sh.pairs * sh.N_b * KTIL_ROW_BYTES     # layer-0 + layers 1..79
+        return attn, sel
+
+    def attn_bytes_per_launch(self):
+        return self.sh.pairs * self.sh.k_tot * KV_BLOCK_BYTES
+
+    def launches_per_step(self):
+        return 2 * self.sh.layers      # 80 selections (incl. layer 0) + 80 attentions
+
+    def _select(self, l_target, F, stream):
+        sh = self.sh
+        self.binding.sparse_select_topk(F, self.ktil[l_target % sh.phys_layers], self.seq, sh.n_init, sh.n_local,
+                                        sh.k, self.idx[l_target], self.count[l_target], status=self.status,
+                                        stream=stream)
+
+    def _attend(self, l, stream, n_split=0):
+        q = l % self.sh.phys_layers
+        self.binding.sparse_decode_attn(self.Q[l], self.k_cache[q], self.v_cache[q], self.idx[l], self.count[l],
+                                        self.seq, self.O[l], status=self.status, n_split=n_split, stream=stream)
+
+    def enqueue_step(self, events=None, n_split=0):
+        """Enqueue one step on the current stream (+ the side stream).  ``events``
+        (list of (start, end) pairs) brackets every attention launch when given."""
+        torch = self.torch
+        main = torch.cuda.current_stream(self.dev)
+        L = self.sh.layers
+        self._select(0, self.F0, main)
+        after_prev_attn = torch.cuda.Event()
+        after_prev_attn.record(main)
+        sel_done = [None] * L
+        for l in range(L):
+            if l + 1 < L:
+                self.side.wait_event(after_prev_attn)
+                self._select(l + 1, self.F[l], self.side)
+                ev = torch.cuda.Event()
+                ev.record(self.side)
+                sel_done[l + 1] = ev
+            if sel_done[l] is not None:
+                main.wait_event(sel_done[l])
+            if events is not None:
+                events[l][0].record(main)
+            self._attend(l, main, n_split)
+            if events is not None:
+                events[l][1].record(main)
+            after_prev_attn = torch.cuda.Event()
+            after_prev_attn.record(main)
+        main.wait_stream(self.side)
+
+    def capture(self):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=self.dev)
+        s.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(s):
+            self.enqueue_step()           # warm the library (tensor maps, attributes) outside capture
+        torch.cuda.synchronize(self.dev)
+        with torch.cuda.graph(g, stream=s):
+            self.enqueue_step()
+        torch.cuda.synchronize(self.dev)
+        return g
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist_init(world, "nccl")
+    import __graft_entry__
+    __graft_entry__.build()
+
+    wk = Decode128k(dev)
+    graph = wk.capture()
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    assert wk.status.item() == 0, f"device status {wk.status.item()}"
+
+    # ---- timed region: K graph replays (inputs resident in HBM, larger than L2)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        start.record()
+        for _ in range(K):
+            graph.replay()
+        end.record()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    ms = max_over_ranks(start.elapsed_time(end), world, dev) / K
+    value = world * 1000.0 / ms
+    attn_b, sel_b = wk.algorithmic_bytes()
+    step_bytes = attn_b + sel_b
+
+    # ---- the dominant kernel: attention launches bracketed by CUDA events on their
+    # stream, in eager steps of the same workload (select overlapped as in the graph)
+    n_ev_steps = max(2, min(10, K // 10))
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(wk.sh.layers)] for _ in range(n_ev_steps)]
+    for e in evs:
+        wk.enqueue_step(events=e)
+    torch.cuda.synchronize(dev)
+    durs = [a.elapsed_time(b) for e in evs for (a, b) in e]
+    attn_ms = statistics.mean(durs)
+    attn_gbs = wk.attn_bytes_per_launch() / (attn_ms * 1e-3) / 1e9
+    peak, peak_src = measured_peaks()
+    khash = kernel_source_hash()
+
+    # ---- end to end through the binding: Q and F from pinned host memory in, O out
+    Qh = wk.Q.cpu().pin_memory()
+    Fh = wk.F.cpu().pin_memory()
+    F0h = wk.F0.cpu().pin_memory()
+    Oh = torch.empty(wk.O.shape, dtype=wk.O.dtype).pin_memory()
+    e_steps = max(3, K // 4)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0.record()
+    for _ in range(e_steps):
+        wk.Q.copy_(Qh, non_blocking=True)
+        wk.F.copy_(Fh, non_blocking=True)
+        wk.F0.copy_(F0h, non_blocking=True)
+        graph.replay()
+        Oh.copy_(wk.O, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / e_steps
+    h2d = Qh.numel() * 2 + Fh.numel() * 2 + F0h.numel() * 2
+    d2h = Oh.numel() * 2
+    assert wk.status.item() == 0, f"device status {wk.status.item()}"
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wk, budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        sh = wk.sh
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "steps/s", "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, planted blocks)",
+            "config": {"workload": sh.name, "B": sh.B, "H_q": sh.H_q, "H_kv": sh.H_kv, "d": D, "T": sh.T,
+                       "layers": sh.layers, "physical_kv_layers": sh.phys_layers, "block": BLK, "k": sh.k,
+                       "n_init": sh.n_init, "n_local": sh.n_local, "blocks_per_pair": sh.k_tot,
+                       "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2: 10 physical layers x 4.3 GB, same layer every 2.1 GB"},
+            "selected_kv_gbs": round(world * step_bytes / (ms * 1e-3) / 1e9, 1),
+            "hbm_frac_of_8tbs": round(step_bytes / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
+            "hbm_frac_of_measured": round(step_bytes / (ms * 1e-3) / 1e9 / peak, 4),
+            "bytes_per_step": {"selected_kv": attn_b, "compressed_keys": sel_b},
+            "roofline": {"bound": "hbm", "achieved": round(attn_gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(attn_gbs / peak, 4), "traffic": profiled_traffic(khash),
+                         "kernel": "sparse_attn_kernel (decode, G=8)", "peak_source": peak_src,
+                         "avg_launch_us": round(attn_ms * 1e3, 2),
+                         "algorithmic_bytes_per_launch": wk.attn_bytes_per_launch(),
+                         "launches_timed": len(durs), "kernel_source_sha1": khash},
+            "e2e": {"value": round(world * 1000.0 / e2e_ms, 3), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": wk.launches_per_step() * K,
+            "clocks": clocks.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- CPU oracle baseline
+
+
+def _oracle_pair_layer_sample(wk, layer: int, batches, threads: int):
+    """Regenerate the sampled batch elements of one logical layer on the GPU, copy them
+    to the host and time the oracle's selection + attention for them (pooling, which
+    the step does not repeat, is prepared outside the timing)."""
+    import numpy as np
+    import torch
+    import oracle
+    wl, sh = wk.wl, wk.sh
+    q_next = (layer + 1) % sh.phys_layers
+    planted = wl.planted_sets(sh, sh.phys_layers)
+    H_kv, G = sh.H_kv, sh.G
+    pairs = [b * H_kv + h for b in batches for h in range(H_kv)]
+    Ks, Vs, Kn = [], [], []
+    for p in pairs:
+        k, v = wl.kv_pair(sh, layer % sh.phys_layers, p, planted[layer % sh.phys_layers, p], wk.dev)
+        Ks.append(wl.bf16_bits(k))
+        Vs.append(wl.bf16_bits(v))
+        kn, _ = wl.kv_pair(sh, q_next, p, planted[q_next, p], wk.dev)
+        Kn.append(wl.bf16_bits(kn))
+    K, V, Knext = np.stack(Ks), np.stack(Vs), np.stack(Kn)
+    lens = [sh.T] * len(pairs)
+    oracle.set_threads(threads)
+    ktil_next = oracle.pool(Knext, lens, sh.N_b)          # resident in the step: not timed
+    ktil_cur = oracle.pool(K, lens, sh.N_b)
+    F = wl.bf16_bits(wl.forecast(sh, q_next, layer, "cpu")).reshape(sh.pairs, D)[pairs]
+    Fc = wl.bf16_bits(wl.forecast(sh, layer % sh.phys_layers, layer - 1, "cpu")).reshape(sh.pairs, D)[pairs]
+    Q = wl.bf16_bits(wl.queries(sh, layer, "cpu")).reshape(sh.pairs, G, D)[pairs]
+    idx, cnt, _ = oracle.select(Fc, ktil_cur, lens, sh.n_init, sh.n_local, sh.k)   # this layer's blocks
+    t0 = time.perf_counter()
+    oracle.select(F, ktil_next, lens, sh.n_init, sh.n_local, sh.k)
+    oracle.attn(Q, K, V, idx, cnt, lens)
+    return time.perf_counter() - t0, len(pairs)
+
+
+def cpu_baseline(wk, budget_s: float = 15.0, max_samples: int = 64):
+    """The oracle on the host cores over a bounded sample of the 128K step: whole
+    layers of B_s batch elements (B_s x 8 pairs, one OpenMP thread per pair), scaled to
+    80 layers x 64 pairs."""
+    cores = len(os.sched_getaffinity(0))
+    per_call = max(1, min(wk.sh.B, cores // wk.sh.H_kv)) if cores >= wk.sh.H_kv else 1
+    threads = min(cores, per_call * wk.sh.H_kv)
+    spent, pair_layers, layers = 0.0, 0, []
+    for i in range(max_samples):
+        layer = (7 * i) % wk.sh.layers
+        batches = [(i * per_call + j) % wk.sh.B for j in range(per_call)]
+        dt, n = _oracle_pair_layer_sample(wk, layer, batches, threads)
+        spent += dt
+        pair_layers += n
+        layers.append(layer)
+        if spent >= budget_s:
+            break
+    per_pair_layer = spent / pair_layers
+    step_s = per_pair_layer * wk.sh.pairs * wk.sh.layers
+    return {"value": round(1.0 / step_s, 6), "unit": "steps/s", "cores": threads, "kind": "oracle",
+            "sample": f"{pair_layers} (pair, layer) units = {len(layers)} layer slices of {per_call} batch "
+                      f"element(s) x 8 KV heads, select(l+1) + attention(l) in fp64, {spent:.1f} s, scaled to "
+                      f"{wk.sh.pairs} pairs x {wk.sh.layers} layers"}
+
+
+def run_reference(args, rank, world, local_rank):
+    """The oracle as the reference arm: every step times a bounded sample (one layer
+    slice of one batch element) and the line reports the extrapolated steps/s."""
+    if rank != 0:
+        return
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", local_rank) if torch.cuda.is_available() else torch.device("cpu")
+
+    class _Shim:  # just the fields the sampler needs; inputs are regenerated per sample
+        pass
+    from block_sparse_long_pool_gb300 import workloads as wl
+    wk = _Shim()
+    wk.wl, wk.sh, wk.dev = wl, wl.DECODE_128K, dev
+    cores = len(os.sched_getaffinity(0))
+    threads = min(cores, wk.sh.H_kv)
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt, n = _oracle_pair_layer_sample(wk, (7 * i) % wk.sh.layers, [i % wk.sh.B], threads)
+        if i >= args.warmup:
+            times.append(dt / n)
+    per_pair_layer = statistics.mean(times)
+    step_s = per_pair_layer * wk.sh.pairs * wk.sh.layers
+    value = 1.0 / step_s
+    sample = (f"per step: one layer slice of one batch element (8 pairs) of {wk.sh.name}, select(l+1) + "
+              f"attention(l) in fp64, scaled to {wk.sh.pairs} pairs x {wk.sh.layers} layers")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "steps/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16, planted blocks)",
+            "config": {"workload": wk.sh.name, "B": wk.sh.B, "H_q": wk.sh.H_q, "H_kv": wk.sh.H_kv, "d": D,
+                       "T": wk.sh.T, "layers": wk.sh.layers, "k": wk.sh.k},
+            "cpu_baseline": {"value": round(value, 6), "unit": "steps/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world, local_rank)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,123 @@
+// pool_append.cu -- append tokens to the K/V caches and keep the compressed keys.
+//
+// SparDA notes §4.2 Alg.1 step 1: new K/V rows are appended and the compressed key
+// cache is updated by mean pooling at O(d) cost per touched block (background
+// eq.(4), one mean per 64-token block).  The running mean of block j becomes
+//     ktil_j <- (n_old * ktil_j + sum of the new keys in j) / n_total.
+//
+// One CTA per (touched block, pair): 16 threads cover the 16 sixteen-byte chunks of
+// a 256-byte token row, 16 rows per pass; each thread copies its rows of K and V
+// with 16-byte loads/stores and sums its 8 key dimensions in fp32.
+#include "common.cuh"
+
+namespace {
+
+using namespace sp;
+
+constexpr int kThreads = 256;
+
+struct AppendParams {
+    uint16_t *k_cache;
+    uint16_t *v_cache;
+    float *ktil;
+    const uint16_t *k_new;
+    const uint16_t *v_new;
+    long long T_cap;
+    long long len_before;
+    int N_cap;
+    int n_new;
+    int first_block;
+};
+
+__global__ void __launch_bounds__(kThreads) pool_append_kernel(const AppendParams p)
+{
+    __shared__ float red[16][kD + 4];
+
+    const int pair = blockIdx.y;
+    const int j = p.first_block + static_cast<int>(blockIdx.x);
+    const long long len_after = p.len_before + p.n_new;
+    const long long blk0 = static_cast<long long>(j) * kBlk;
+    const long long t_begin = blk0 > p.len_before ? blk0 : p.len_before;
+    const long long t_end = (blk0 + kBlk) < len_after ? (blk0 + kBlk) : len_after;
+    long long n_old_ll = p.len_before - blk0;
+    n_old_ll = n_old_ll < 0 ? 0 : (n_old_ll > kBlk ? kBlk : n_old_ll);
+    const int n_old = static_cast<int>(n_old_ll);
+    const int n_total = static_cast<int>(t_end - blk0);
+
+    const int c = threadIdx.x & 15;   // 16-byte chunk: dims 8c .. 8c+7
+    const int r0 = threadIdx.x >> 4;  // row phase 0..15
+
+    const size_t cache_base = static_cast<size_t>(pair) * static_cast<size_t>(p.T_cap) * kD;
+    const size_t new_base = static_cast<size_t>(pair) * static_cast<size_t>(p.n_new) * kD;
+
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        acc[i] = 0.f;
+
+    for (long long t = t_begin + r0; t < t_end; t += 16) {
+        const size_t src = new_base + static_cast<size_t>(t - p.len_before) * kD + c * 8;
+        const size_t dst = cache_base + static_cast<size_t>(t) * kD + c * 8;
+        const uint4 kv = *reinterpret_cast<const uint4 *>(p.k_new + src);
+        const uint4 vv = *reinterpret_cast<const uint4 *>(p.v_new + src);
+        *reinterpret_cast<uint4 *>(p.k_cache + dst) = kv;
+        *reinterpret_cast<uint4 *>(p.v_cache + dst) = vv;
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&kv);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(h[i]);
+            acc[2 * i] += f.x;
+            acc[2 * i + 1] += f.y;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        red[r0][c * 8 + i] = acc[i];
+    __syncthreads();
+
+    if (threadIdx.x < kD) {
+        const int d = threadIdx.x;
+        float s = 0.f;
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            s += red[r][d];
+        float *kt = p.ktil + (static_cast<size_t>(pair) * p.N_cap + j) * kD + d;
+        const float prev = n_old > 0 ? *kt * static_cast<float>(n_old) : 0.f;
+        *kt = (prev + s) / static_cast<float>(n_total);
+    }
+}
+
+}  // namespace
+
+extern "C" SPARSE_API int sparse_pool_append(uint16_t *k_cache, uint16_t *v_cache, float *ktil,
+                                             const uint16_t *k_new, const uint16_t *v_new, int B,
+                                             int H_kv, long long T_cap, int N_cap,
+                                             long long len_before, int n_new, void *stream)
+{
+    using sp_host::aligned16;
+    using sp_host::fail;
+    if (!k_cache || !v_cache || !ktil || !k_new || !v_new)
+        return fail(SPARSE_ERR_INVALID_ARG, "sparse_pool_append: null pointer");
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(ktil) || !aligned16(k_new) ||
+        !aligned16(v_new))
+        return fail(SPARSE_ERR_INVALID_ARG, "sparse_pool_append: buffers must be 16-byte aligned");
+    if (B < 1 || H_kv < 1 || n_new < 1 || len_before < 0 || T_cap < 1 || N_cap < 1)
+        return fail(SPARSE_ERR_INVALID_ARG, "sparse_pool_append: bad size (B=%d H_kv=%d n_new=%d len=%lld)",
+                    B, H_kv, n_new, len_before);
+    const long long len_after = len_before + n_new;
+    if (len_after > T_cap)
+        return fail(SPARSE_ERR_INVALID_ARG, "sparse_pool_append: %lld tokens exceed T_cap=%lld", len_after,
+                    T_cap);
+    if ((len_after + kBlk - 1) / kBlk > N_cap)
+        return fail(SPARSE_ERR_INVALID_ARG, "sparse_pool_append: %lld tokens need more than N_cap=%d blocks",
+                    len_after, N_cap);
+    const long long pairs = static_cast<long long>(B) * H_kv;
+    if (pairs > 65535)
+        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_pool_append: B*H_kv=%lld > 65535", pairs);
+    const int first_block = static_cast<int>(len_before / kBlk);
+    const int last_block = static_cast<int>((len_after - 1) / kBlk);
+    AppendParams p{k_cache, v_cache, ktil, k_new, v_new, T_cap, len_before, N_cap, n_new, first_block};
+    dim3 grid(static_cast<unsigned>(last_block - first_block + 1), static_cast<unsigned>(pairs));
+    pool_append_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    return sp_host::cuda_status(cudaGetLastError(), "sparse_pool_append launch");
+}

@@ -1,0 +1,203 @@
+/*
+ * sparse_pool.h -- C ABI of libsparsepool, block-sparse GQA decode attention with
+ * learned block selection, for one GB300 GPU (sm_103a).
+ *
+ * The method (two reading-note pages on the web):
+ *   [SparDA] "SparDA: sparse decoupled attention" notes, zhongzhuzhou.org/blog/2026-06-24
+ *   [SSV]    "SSV: sparse speculative verification" notes, zhongzhuzhou.org/blog/2026-07-01
+ *
+ * Conventions shared by every entry point
+ *   - Head dimension d = 128 and block size 64 tokens are fixed.
+ *   - bf16 tensors are passed as uint16_t* holding the bf16 bit patterns.
+ *   - "pair" = (batch b, KV head g), flattened as p = b * H_kv + g.  Query head h of a
+ *     batch belongs to KV head floor(h / G), G = H_q / H_kv (contiguous groups).
+ *   - All pointers are device-accessible addresses (device memory, or host memory
+ *     mapped into the device address space where stated), at least 16-byte aligned.
+ *     The caller owns every buffer; the library allocates no device memory.
+ *   - Every call is asynchronous on the given CUDA stream (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream).  Arguments are validated on the host
+ *     before any launch; a rejected call launches nothing and returns a negative
+ *     status.  Errors found on the device (bad block ids, a wait that timed out) are
+ *     written to the optional int32 `status` word in device memory (first error wins,
+ *     0 = OK) and never trap.
+ *   - Calls return SPARSE_OK or a negative SPARSE_ERR_* code; sparse_last_error()
+ *     gives a message for the last failing call on the calling host thread.
+ */
+#ifndef SPARSE_POOL_H
+#define SPARSE_POOL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SPARSE_API __attribute__((visibility("default")))
+#else
+#define SPARSE_API
+#endif
+
+enum {
+    SPARSE_OK = 0,
+    SPARSE_ERR_INVALID_ARG = -1,   /* a null pointer, a bad size or misaligned buffer  */
+    SPARSE_ERR_UNSUPPORTED = -2,   /* a size outside what the kernels handle           */
+    SPARSE_ERR_CUDA = -3,          /* a CUDA runtime call failed                       */
+    SPARSE_ERR_TIMEOUT = -4,       /* device: a bounded wait gave up                   */
+    SPARSE_ERR_NOT_READY = -5,     /* device: a staging slot was not marked ready      */
+    SPARSE_ERR_BAD_INDEX = -6      /* device: a block id outside the cache was skipped */
+};
+
+/* Message for a status code (static storage). */
+SPARSE_API const char *sparse_status_string(int status);
+
+/* Message of the last failing call on this host thread ("" if none). */
+SPARSE_API const char *sparse_last_error(void);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+SPARSE_API int sparse_version(void);
+
+/*
+ * sparse_pool_append -- [SparDA] §4.2 Alg.1 step 1 and background eq.(4).
+ * Appends n_new tokens to every pair's K and V cache at positions
+ * [len_before, len_before + n_new) and updates the compressed key of every block
+ * those tokens touch, at O(d) cost per block:
+ *     ktil[p][j] = (n_old * ktil[p][j] + sum of the new keys in block j) / n_total,
+ * n_old / n_total the tokens of block j before / after the append.  After the call
+ * ktil[p][j] is the mean of the keys present in block j (the last block may be
+ * partial).  Blocks that were empty before are overwritten, not read.
+ *   k_cache, v_cache  [B][H_kv][T_cap][128] bf16, written.
+ *   ktil              [B][H_kv][N_cap][128] fp32, read-modify-written, N_cap >= ceil((len_before+n_new)/64).
+ *   k_new, v_new      [B][H_kv][n_new][128] bf16, read.
+ * Requires len_before >= 0, n_new >= 1, len_before + n_new <= T_cap.  The caches may
+ * be device memory or mapped pinned host memory.
+ */
+SPARSE_API int sparse_pool_append(uint16_t *k_cache, uint16_t *v_cache, float *ktil,
+                                  const uint16_t *k_new, const uint16_t *v_new,
+                                  int B, int H_kv, long long T_cap, int N_cap,
+                                  long long len_before, int n_new, void *stream);
+
+/*
+ * sparse_select_topk -- [SparDA] §4.1 eq.(6), §4.2 Alg.1 step 2, §4.3 eq.(9).
+ * For every pair: N_b = ceil(seq_len[b] / 64); B_init = blocks [0, n_init);
+ * B_local = the last n_local blocks [N_b - n_local, N_b); every other block j is a
+ * candidate with score s_j = sum_d F[p][d] * ktil[p][j][d] (fp32).  The k candidates
+ * of largest score are taken (equal scores: the lower block index wins; the softmax
+ * and temperature of eq.(9) are monotone and do not change the top-k), and
+ * idx_out[p][0 .. count_out[p]) = B_init ∪ B_local ∪ top-k in ascending order, the
+ * rest of the row filled with -1.  count = min(N_b, n_init + n_local + k).
+ *   F          [B][H_kv][128] bf16: one Forecast vector per GQA group.
+ *   ktil       [B][H_kv][N_cap][128] fp32 compressed keys of the layer selected for.
+ *   seq_len    [B] int32 (device): tokens present per batch element.
+ *   idx_out    [B][H_kv][k_tot] int32, k_tot >= n_init + n_local + k.
+ *   count_out  [B][H_kv] int32.
+ *   status     optional int32 device word (a length beyond N_cap*64 is reported).
+ */
+SPARSE_API int sparse_select_topk(const uint16_t *F, const float *ktil, const int *seq_len,
+                                  int B, int H_kv, int N_cap, int n_init, int n_local, int k,
+                                  int *idx_out, int *count_out, int k_tot, int *status,
+                                  void *stream);
+
+/*
+ * sparse_decode_attn -- [SparDA] §4.1 eq.(7), §4.2 Alg.1 step 4; scale 1/sqrt(d) per
+ * the [SSV] NSA selection branch (step 3); split-KV merge by the online-softmax
+ * recurrence of [SSV] "online softmax state merging".
+ * For every query head h of pair p = (b, floor(h/G)):
+ *     O[b][h] = sum_t softmax_t(scale * q_h . k_t) v_t
+ * over the tokens t = 64 * blk_logical[p][i] + r (i < count[p], r < 64) with
+ * t < seq_len[b].  Token rows are read from the pair's region of k_base / v_base at
+ * row 64 * slot + r, slot = blk_slot[p][i]; with blk_slot NULL the slot is the
+ * logical id itself (a resident cache).  A staging ring that holds the selected
+ * blocks in list order passes the slot table slot[p][i] = i.  The listed blocks are
+ * expected to be distinct (a repeated id contributes its tokens once per listing).
+ *   Q            [B][H_q][128] bf16.
+ *   k_base,v_base [B*H_kv][pair_stride_tokens][128] bf16 (a resident cache with
+ *                pair_stride_tokens = T_cap, or a staging ring with k_tot * 64).
+ *   blk_slot     [B*H_kv][k_tot] int32, or NULL for slot = logical id.
+ *   blk_logical  [B*H_kv][k_tot] int32 logical block ids (as sparse_select_topk writes).
+ *   count        [B*H_kv] int32 (device), 0 <= count <= k_tot.
+ *   seq_len      [B] int32 (device).
+ *   scale        0 selects 1/sqrt(128).
+ *   O            [B][H_q][128] bf16;  lse [B][H_q] fp32 natural-log LSE, or NULL.
+ *   n_split      CTAs sharing one pair's list (1, 2, 4 or 8); 0 = chosen from the
+ *                SM count.  The result does not depend on it beyond fp32 rounding.
+ * A row with no valid token gets O = 0 and lse = -inf.  G = H_q / H_kv <= 16.
+ */
+SPARSE_API int sparse_decode_attn(const uint16_t *Q, const uint16_t *k_base,
+                                  const uint16_t *v_base, long long pair_stride_tokens,
+                                  const int *blk_slot, const int *blk_logical, const int *count,
+                                  int k_tot, const int *seq_len, int B, int H_q, int H_kv,
+                                  float scale, uint16_t *O, float *lse, int n_split,
+                                  int *status, void *stream);
+
+/*
+ * sparse_decode_attn_ex -- sparse_decode_attn that first checks a staging-ready word.
+ * Before reading, every CTA polls *ready_flag (device memory, acquire) until it is
+ * >= ready_target, for at most timeout_ns nanoseconds (0 = check once, capped at
+ * 2 s).  If the word does not reach the target, the CTA reads nothing, leaves O and
+ * lse untouched and reports SPARSE_ERR_TIMEOUT (timeout_ns > 0) or
+ * SPARSE_ERR_NOT_READY (timeout_ns == 0) in *status.  Ordering the producer before
+ * this call (same stream, or an event) is the caller's job; the word is an integrity
+ * check, not a substitute for stream order.
+ */
+SPARSE_API int sparse_decode_attn_ex(const uint16_t *Q, const uint16_t *k_base,
+                                     const uint16_t *v_base, long long pair_stride_tokens,
+                                     const int *blk_slot, const int *blk_logical,
+                                     const int *count, int k_tot, const int *seq_len, int B,
+                                     int H_q, int H_kv, float scale, uint16_t *O, float *lse,
+                                     int n_split, const unsigned *ready_flag,
+                                     unsigned ready_target, long long timeout_ns, int *status,
+                                     void *stream);
+
+/*
+ * sparse_verify_attn_grouped -- [SSV] mechanism 1, mode A (exact merged schedule).
+ * N_q verification queries per sequence (already flattened in BFS order) are split
+ * into groups of C consecutive queries.  For group [q0, q0 + C) of pair (b, g) the
+ * merged set U = ∪_q (I_q ∪ W) is loaded once, W = the last window_blocks blocks
+ * [N_b - window_blocks, N_b) of the committed sequence, and every query head h of
+ * every query q of the group attends over its own set I_q ∪ W only:
+ *     O[b][q][h] = sum_t softmax_t(scale * q_{q,h} . k_t) v_t,  t in I_q ∪ W, t < seq_len[b].
+ *   Q        [B][N_q][H_q][128] bf16.
+ *   k_cache, v_cache [B][H_kv][T_cap][128] bf16 (committed tokens).
+ *   idx_q    [B][H_kv][N_q][n_sel] int32 per-query block ids (any order; repeats and
+ *            blocks of W count once; ids outside [0, N_b) are skipped and reported).
+ *   O        [B][N_q][H_q][128] bf16.
+ *   blocks_loaded  optional int64 device counter: += |U| for every group (the blocks
+ *            this call streams from HBM).  Without grouping the count would be
+ *            sum_q |I_q ∪ W|.
+ * Limits: C * G <= 16 rows per group tile; C * n_sel + window_blocks <= 512.
+ */
+SPARSE_API int sparse_verify_attn_grouped(const uint16_t *Q, const uint16_t *k_cache,
+                                          const uint16_t *v_cache, long long T_cap,
+                                          const int *idx_q, int n_sel, int N_q, int C,
+                                          int window_blocks, const int *seq_len, int B,
+                                          int H_q, int H_kv, float scale, uint16_t *O,
+                                          long long *blocks_loaded, int n_split, int *status,
+                                          void *stream);
+
+/*
+ * sparse_gather_offloaded -- [SparDA] §4.5 (persistent prefetch of selected blocks,
+ * re-designed as a gather kernel on the copy stream).  Copies the K and V rows of
+ * block idx[p][i] (i < count[p]) of every pair from the host cache into slot i of the
+ * staging ring: ring[p][i][r][:] = cache[p][64 * idx[p][i] + r][:], rows at or past
+ * T_host written as zero.  After its copies every CTA adds 1 to *ready_flag (release,
+ * device scope), so the word grows by n_ctas per call.
+ *   k_host, v_host  [B][H_kv][T_host][128] bf16 in pinned host memory mapped into the
+ *                   device address space (or any device-accessible memory).
+ *   idx, count      as written by sparse_select_topk ([B*H_kv][k_tot], [B*H_kv]).
+ *   k_ring, v_ring  [B*H_kv][k_tot][64][128] bf16 device memory (one ring slot).
+ *   ready_flag      optional uint32 device word.
+ *   n_ctas          gather CTAs (1..1024); 0 = chosen from the SM count.
+ */
+SPARSE_API int sparse_gather_offloaded(const uint16_t *k_host, const uint16_t *v_host,
+                                       long long T_host, const int *idx, const int *count,
+                                       int k_tot, int B, int H_kv, uint16_t *k_ring,
+                                       uint16_t *v_ring, unsigned *ready_flag, int n_ctas,
+                                       int *status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_POOL_H */

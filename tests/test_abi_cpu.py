@@ -1,0 +1,124 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every declared symbol,
+and rejects bad arguments on the host before anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_sparse_long_pool_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sparse_pool.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"SPARSE_API\s+[\w\s\*]+?\b(sparse_\w+)\s*\(", text)
+
+
+def test_header_declares_the_five_calls():
+    names = set(declared_symbols())
+    assert {"sparse_pool_append", "sparse_select_topk", "sparse_decode_attn", "sparse_verify_attn_grouped",
+            "sparse_gather_offloaded"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(binding.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(raw, name), f"{name} is declared but not exported"
+        assert name in binding.SIGNATURES, f"{name} has no binding signature"
+
+
+def test_only_declared_symbols_are_exported():
+    out = os.popen(f"nm -D --defined-only {binding.LIB_PATH}").read()
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    ours = {s for s in exported if s.startswith("sparse_")}
+    assert ours == set(declared_symbols())
+
+
+def test_status_strings(lib):
+    assert binding.status_string(0) == "ok"
+    for code in range(-6, 0):
+        assert binding.status_string(code) not in ("", "unknown status")
+    assert lib.sparse_version() >= 100
+
+
+FAKE = ctypes.c_void_p(0x10000)      # aligned, never dereferenced: validation fails first
+ODD = ctypes.c_void_p(0x10002)
+
+
+def test_append_rejects_bad_arguments(lib):
+    f = lib.sparse_pool_append
+    assert f(None, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 2, 0, 1, None) == binding.SPARSE_ERR_INVALID_ARG
+    assert f(ODD, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 2, 0, 1, None) == binding.SPARSE_ERR_INVALID_ARG
+    # 100 + 40 tokens do not fit T_cap = 128
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 3, 100, 40, None) == binding.SPARSE_ERR_INVALID_ARG
+    assert "T_cap" in lib.sparse_last_error().decode()
+    # 129 tokens need 3 compressed rows
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 2, 128, 1, None) == binding.SPARSE_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 4, 0, 0, None) == binding.SPARSE_ERR_INVALID_ARG
+
+
+def test_select_rejects_bad_arguments(lib):
+    f = lib.sparse_select_topk
+    # k_tot smaller than n_init + n_local + k
+    assert f(FAKE, FAKE, FAKE, 1, 2, 64, 1, 2, 8, FAKE, FAKE, 10, None, None) == binding.SPARSE_ERR_INVALID_ARG
+    assert f(None, FAKE, FAKE, 1, 2, 64, 1, 2, 8, FAKE, FAKE, 11, None, None) == binding.SPARSE_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, 1, 2, 64, -1, 2, 8, FAKE, FAKE, 11, None, None) == binding.SPARSE_ERR_INVALID_ARG
+
+
+def test_decode_rejects_bad_arguments(lib):
+    f = lib.sparse_decode_attn
+    args = [FAKE, FAKE, FAKE, 4096, None, FAKE, FAKE, 11, FAKE, 1, 8, 2, 0.0, FAKE, None, 0, None, None]
+    bad = list(args)
+    bad[10] = 7                                   # H_q not a multiple of H_kv
+    assert f(*bad) == binding.SPARSE_ERR_INVALID_ARG
+    bad = list(args)
+    bad[10], bad[11] = 34, 2                      # G = 17 > 16
+    assert f(*bad) == binding.SPARSE_ERR_UNSUPPORTED
+    bad = list(args)
+    bad[0] = ODD
+    assert f(*bad) == binding.SPARSE_ERR_INVALID_ARG
+    bad = list(args)
+    bad[12] = float("nan")
+    assert f(*bad) == binding.SPARSE_ERR_INVALID_ARG
+    ex = lib.sparse_decode_attn_ex
+    assert ex(*args[:16], None, 1, 0, None, None) == binding.SPARSE_ERR_INVALID_ARG
+
+
+def test_verify_rejects_bad_arguments(lib):
+    f = lib.sparse_verify_attn_grouped
+    args = [FAKE, FAKE, FAKE, 65536, FAKE, 16, 8, 4, 8, FAKE, 4, 32, 8, 0.0, FAKE, None, 0, None, None]
+    bad = list(args)
+    bad[7] = 5                                    # C*G = 20 rows > 16
+    assert f(*bad) == binding.SPARSE_ERR_UNSUPPORTED
+    bad = list(args)
+    bad[5], bad[7] = 200, 3                       # union bound 3*200+8 > 512
+    bad[11], bad[12] = 8, 8
+    assert f(*bad) == binding.SPARSE_ERR_UNSUPPORTED
+    bad = list(args)
+    bad[4] = None
+    assert f(*bad) == binding.SPARSE_ERR_INVALID_ARG
+
+
+def test_gather_rejects_bad_arguments(lib):
+    f = lib.sparse_gather_offloaded
+    assert f(FAKE, FAKE, 4096, FAKE, FAKE, 11, 1, 2, FAKE, FAKE, None, 2000, None, None) == \
+        binding.SPARSE_ERR_INVALID_ARG
+    assert f(FAKE, ODD, 4096, FAKE, FAKE, 11, 1, 2, FAKE, FAKE, None, 8, None, None) == \
+        binding.SPARSE_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    with pytest.raises(ValueError):
+        binding.sparse_select_topk(torch.zeros(1, 2, 128, dtype=torch.bfloat16),
+                                   torch.zeros(1, 2, 64, 128), torch.zeros(1, dtype=torch.int32), 1, 2, 8,
+                                   torch.zeros(1, 2, 11, dtype=torch.int32), torch.zeros(1, 2, dtype=torch.int32))

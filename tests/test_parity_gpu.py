@@ -1,0 +1,476 @@
+"""GPU parity: every entry point of the C ABI against the fp64 oracle on seeded inputs.
+
+Oracle inputs come only from the seeded generators (never from the CUDA path); the
+CUDA path is called through the ctypes binding of libsparsepool.so.  Tolerances are
+stated in parity_utils.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_long_pool_gb300 import binding, build
+from block_sparse_long_pool_gb300 import workloads as wl
+from parity_utils import (BLK, D, GpuLayer, assert_attn_close, assert_selection_matches, bits,
+                          oracle_layer)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    build.build()
+    binding.load()
+
+
+def _lens_pair(lens_b, H_kv):
+    return np.repeat(np.asarray(lens_b, dtype=np.int64), H_kv)
+
+
+def _seq(lens_b):
+    return torch.tensor(lens_b, dtype=torch.int32, device="cuda")
+
+
+def _check_lse(lse_gpu, lse_ref, mask=None):
+    g = lse_gpu.cpu().double().numpy().reshape(lse_ref.shape)
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(g), fin)
+    assert np.allclose(g[fin], lse_ref[fin], rtol=0, atol=2e-3)
+
+
+# ----------------------------------------------------------------------------- append / pooling
+
+
+def test_append_bulk_then_incremental_matches_oracle():
+    B, H_kv, T_cap = 2, 3, 10 * BLK
+    N_cap = T_cap // BLK
+    K = wl.randn_bf16((B, H_kv, T_cap, D), 501, "cuda")
+    V = wl.randn_bf16((B, H_kv, T_cap, D), 502, "cuda")
+    L = GpuLayer(B, 4 * H_kv, H_kv, T_cap, N_cap, 1, 2, 4)
+    steps = [(0, 5 * BLK + 17), (5 * BLK + 17, 1), (5 * BLK + 18, 100), (5 * BLK + 118, 2 * BLK)]
+    for start, n in steps:
+        L.append(K[:, :, start:start + n], V[:, :, start:start + n], start)
+        torch.cuda.synchronize()
+        end = start + n
+        assert torch.equal(L.k_cache[:, :, :end], K[:, :, :end])
+        assert torch.equal(L.v_cache[:, :, :end], V[:, :, :end])
+        assert not L.k_cache[:, :, end:].any()
+        ref = oracle.pool(bits(K).reshape(B * H_kv, T_cap, D), [end] * (B * H_kv), N_cap)
+        nb = (end + BLK - 1) // BLK
+        got = L.ktil.cpu().double().numpy().reshape(B * H_kv, N_cap, D)
+        assert np.allclose(got[:, :nb], ref[:, :nb], rtol=1e-5, atol=1e-6), f"after append to {end}"
+
+
+# ----------------------------------------------------------------------------- selection
+
+
+def _select_case(lens_b, H_kv, N_cap, n_init, n_local, k, ktil_np, F):
+    B = len(lens_b)
+    P = B * H_kv
+    k_cap = n_init + n_local + k
+    ktil = torch.from_numpy(ktil_np.astype(np.float32)).cuda().view(B, H_kv, N_cap, D)
+    idx = torch.full((B, H_kv, k_cap), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((B, H_kv), -7, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.sparse_select_topk(F, ktil, _seq(lens_b), n_init, n_local, k, idx, cnt, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    lens_p = _lens_pair(lens_b, H_kv)
+    ref = oracle.select(bits(F).reshape(P, D), ktil_np.astype(np.float32).astype(np.float64), lens_p, n_init,
+                        n_local, k, k_cap)
+    return idx, cnt, ref, lens_p
+
+
+@pytest.mark.parametrize("N_cap,lens_b,k", [(64, [4096, 3001, 65, 0], 8), (513, [32769, 32768], 32),
+                                            (2048, [131072, 100000], 64), (16384, [1 << 20], 64),
+                                            (5000, [320000, 319937, 1], 200)])
+def test_select_matches_oracle_random_scores(N_cap, lens_b, k):
+    H_kv = 3
+    P = len(lens_b) * H_kv
+    rng = np.random.default_rng(N_cap)
+    ktil_np = rng.standard_normal((P, N_cap, D)).astype(np.float32)
+    F = wl.randn_bf16((len(lens_b), H_kv, D), N_cap + 1, "cuda")
+    idx, cnt, (ridx, rcnt, rs), lens_p = _select_case(lens_b, H_kv, N_cap, 1, 2, k, ktil_np, F)
+    assert_selection_matches(idx, cnt, ridx, rcnt, rs, lens_p, 1, 2, k)
+
+
+def test_select_ties_go_to_the_lower_index_exactly():
+    # integer scores: fp32 and fp64 agree exactly, so the tie rule alone decides
+    lens_b, H_kv, N_cap, k = [300 * BLK, 77 * BLK + 5], 2, 300, 16
+    P = len(lens_b) * H_kv
+    rng = np.random.default_rng(7)
+    ktil_np = np.zeros((P, N_cap, D), np.float32)
+    ktil_np[:, :, 5] = rng.integers(-4, 5, size=(P, N_cap))
+    F = torch.zeros((len(lens_b), H_kv, D), dtype=torch.bfloat16, device="cuda")
+    F[..., 5] = 1.0
+    idx, cnt, (ridx, rcnt, _), _ = _select_case(lens_b, H_kv, N_cap, 1, 2, k, ktil_np, F)
+    assert np.array_equal(idx.cpu().numpy().reshape(ridx.shape), ridx)
+    assert np.array_equal(cnt.cpu().numpy().reshape(rcnt.shape), rcnt)
+    # all-equal scores: the lowest candidate indices
+    idx, cnt, (ridx, rcnt, _), _ = _select_case(lens_b, H_kv, N_cap, 1, 2, k, np.zeros_like(ktil_np), F)
+    assert np.array_equal(idx.cpu().numpy().reshape(ridx.shape), ridx)
+    assert list(ridx[0, :rcnt[0]]) == list(range(0, k + 1)) + [298, 299]
+
+
+@pytest.mark.parametrize("lens_b", [[7 * BLK, 2 * BLK, 65, 1, 0]])
+def test_select_few_blocks_takes_all(lens_b):
+    H_kv, N_cap = 2, 8
+    P = len(lens_b) * H_kv
+    ktil_np = np.random.default_rng(3).standard_normal((P, N_cap, D)).astype(np.float32)
+    F = wl.randn_bf16((len(lens_b), H_kv, D), 4, "cuda")
+    idx, cnt, (ridx, rcnt, _), _ = _select_case(lens_b, H_kv, N_cap, 1, 2, 8, ktil_np, F)
+    assert np.array_equal(idx.cpu().numpy().reshape(ridx.shape), ridx)
+    assert list(rcnt.reshape(-1, H_kv)[:, 0]) == [7, 2, 2, 1, 0]
+
+
+# ----------------------------------------------------------------------------- decode attention
+
+
+def _decode_direct(B, H_q, H_kv, T_cap, lens_b, k_cap, seed, n_split=0, idx_np=None, cnt_np=None):
+    """sparse_decode_attn on given (or random distinct) block lists vs oracle.attn."""
+    G = H_q // H_kv
+    P = B * H_kv
+    rng = np.random.default_rng(seed)
+    K = wl.randn_bf16((B, H_kv, T_cap, D), seed + 1, "cuda")
+    V = wl.randn_bf16((B, H_kv, T_cap, D), seed + 2, "cuda")
+    Q = wl.randn_bf16((B, H_q, D), seed + 3, "cuda")
+    lens_p = _lens_pair(lens_b, H_kv)
+    if idx_np is None:
+        idx_np = np.full((P, k_cap), -1, np.int32)
+        cnt_np = np.zeros(P, np.int32)
+        for p in range(P):
+            nb = (int(lens_p[p]) + BLK - 1) // BLK
+            c = min(nb, k_cap)
+            idx_np[p, :c] = rng.permutation(nb)[:c]          # distinct, unsorted
+            cnt_np[p] = c
+    O = torch.zeros((B, H_q, D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((B, H_q), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.sparse_decode_attn(Q, K, V, torch.from_numpy(idx_np).cuda().view(B, H_kv, k_cap),
+                               torch.from_numpy(cnt_np).cuda().view(B, H_kv), _seq(lens_b), O, lse,
+                               n_split=n_split, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    Oref, lref = oracle.attn(bits(Q).reshape(P, G, D), bits(K).reshape(P, T_cap, D), bits(V).reshape(P, T_cap, D),
+                             idx_np, cnt_np, lens_p)
+    return O, lse, Oref, lref
+
+
+@pytest.mark.parametrize("H_q,H_kv", [(8, 2), (64, 8), (16, 16), (32, 2), (24, 4)])
+def test_decode_attn_matches_oracle_group_sizes(H_q, H_kv):
+    O, lse, Oref, lref = _decode_direct(2, H_q, H_kv, 40 * BLK, [40 * BLK, 25 * BLK + 11], 19, seed=H_q * 7 + H_kv)
+    assert_attn_close(O, Oref.reshape(2, H_q, D))
+    _check_lse(lse, lref.reshape(2, H_q))
+
+
+def test_decode_attn_split_invariance():
+    outs = {}
+    for n_split in (1, 2, 4, 8):
+        O, lse, Oref, lref = _decode_direct(2, 32, 8, 80 * BLK, [80 * BLK, 79 * BLK + 1], 67, seed=99,
+                                            n_split=n_split)
+        assert_attn_close(O, Oref.reshape(2, 32, D), f"n_split={n_split}")
+        outs[n_split] = O
+    for n_split in (2, 4, 8):
+        diff = (outs[n_split].float() - outs[1].float()).abs().max().item()
+        assert diff <= 2 ** -7, f"split {n_split} changes the output by {diff}"
+
+
+def test_decode_attn_empty_and_tiny_sets():
+    B, H_q, H_kv, T_cap, k_cap = 3, 8, 2, 4 * BLK, 5
+    P = B * H_kv
+    idx_np = np.full((P, k_cap), -1, np.int32)
+    cnt_np = np.zeros(P, np.int32)
+    idx_np[1, 0], cnt_np[1] = 0, 1          # one block, length 1 -> one token
+    idx_np[2, :2], cnt_np[2] = [3, 1], 2
+    idx_np[3, :4], cnt_np[3] = [0, 1, 2, 3], 4
+    O, lse, Oref, lref = _decode_direct(B, H_q, H_kv, T_cap, [4 * BLK, 1, 3 * BLK + 7], k_cap, 5,
+                                        idx_np=idx_np, cnt_np=cnt_np)
+    assert_attn_close(O, Oref.reshape(B, H_q, D))
+    assert not O[0, :4].any()                            # pair 0: empty set -> zeros
+    assert torch.isneginf(lse[0, :4]).all()
+    _check_lse(lse, lref.reshape(B, H_q))
+
+
+def test_decode_attn_is_deterministic():
+    a = _decode_direct(2, 32, 8, 64 * BLK, [64 * BLK, 64 * BLK], 35, seed=3)[0]
+    b = _decode_direct(2, 32, 8, 64 * BLK, [64 * BLK, 64 * BLK], 35, seed=3)[0]
+    assert torch.equal(a, b)
+
+
+def test_decode_attn_reports_bad_block_ids_without_faulting():
+    B, H_q, H_kv, T_cap, k_cap = 1, 8, 2, 8 * BLK, 3
+    K = wl.randn_bf16((B, H_kv, T_cap, D), 1, "cuda")
+    Q = wl.randn_bf16((B, H_q, D), 2, "cuda")
+    idx = torch.tensor([[[0, 1 << 20, 2], [3, -5, 4]]], dtype=torch.int32, device="cuda")
+    cnt = torch.tensor([[3, 3]], dtype=torch.int32, device="cuda")
+    O = torch.zeros((B, H_q, D), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.sparse_decode_attn(Q, K, K, idx, cnt, _seq([T_cap]), O, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == binding.SPARSE_ERR_BAD_INDEX
+    good_idx = torch.tensor([[[0, 2, 2], [3, 4, 4]]], dtype=torch.int32, device="cuda")
+    good_cnt = torch.tensor([[2, 2]], dtype=torch.int32, device="cuda")
+    O2 = torch.zeros_like(O)
+    binding.sparse_decode_attn(Q, K, K, good_idx, good_cnt, _seq([T_cap]), O2)
+    torch.cuda.synchronize()
+    assert (O.float() - O2.float()).abs().max().item() <= 2 ** -8
+
+
+def test_decode_attn_ex_ready_word():
+    B, H_q, H_kv, T_cap, k_cap = 1, 8, 2, 8 * BLK, 3
+    K = wl.randn_bf16((B, H_kv, T_cap, D), 11, "cuda")
+    Q = wl.randn_bf16((B, H_q, D), 12, "cuda")
+    idx = torch.tensor([[[0, 1, 2], [3, 4, 5]]], dtype=torch.int32, device="cuda")
+    cnt = torch.tensor([[3, 3]], dtype=torch.int32, device="cuda")
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sentinel = torch.full((B, H_q, D), 7.0, dtype=torch.bfloat16, device="cuda")
+    # a word that nothing sets: the bounded wait gives up and leaves O untouched
+    O = sentinel.clone()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.sparse_decode_attn_ex(Q, K, K, idx, cnt, _seq([T_cap]), O, flag, 1, 50_000_000, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == binding.SPARSE_ERR_TIMEOUT
+    assert torch.equal(O, sentinel)
+    status.zero_()
+    binding.sparse_decode_attn_ex(Q, K, K, idx, cnt, _seq([T_cap]), O, flag, 1, 0, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == binding.SPARSE_ERR_NOT_READY
+    # once the word reaches the target the call computes the plain result
+    flag.fill_(1)
+    status.zero_()
+    binding.sparse_decode_attn_ex(Q, K, K, idx, cnt, _seq([T_cap]), O, flag, 1, 1_000_000, status=status)
+    ref = torch.zeros_like(O)
+    binding.sparse_decode_attn(Q, K, K, idx, cnt, _seq([T_cap]), ref)
+    torch.cuda.synchronize()
+    assert status.item() == 0 and torch.equal(O, ref)
+
+
+# ----------------------------------------------------------------------------- whole single-layer workloads
+
+
+def _pipeline(sh, lens_b=None):
+    """append -> select -> attend on the GPU; pool -> select -> attend in the oracle."""
+    inp = wl.single_layer(sh, device="cuda")
+    B, H_kv, G, P = sh.B, sh.H_kv, sh.G, sh.pairs
+    L = GpuLayer(B, sh.H_q, H_kv, sh.T_cap, sh.N_b, sh.n_init, sh.n_local, sh.k)
+    K_all, V_all = inp["K"].clone(), inp["V"].clone()
+    if lens_b is None:
+        L.append(inp["K"][:, :, :sh.T], inp["V"][:, :, :sh.T], 0)
+    else:
+        # a ragged batch: element b holds lens_b[b] tokens
+        assert sh.n_new == 0
+        for b, n in enumerate(lens_b):
+            binding.sparse_pool_append(L.k_cache[b:b + 1], L.v_cache[b:b + 1], L.ktil[b:b + 1],
+                                       inp["K"][b:b + 1, :, :n].contiguous(), inp["V"][b:b + 1, :, :n].contiguous(), 0)
+            K_all[b, :, n:] = 0
+            V_all[b, :, n:] = 0
+    if sh.n_new:
+        L.append(inp["k_new"], inp["v_new"], sh.T)
+        K_all[:, :, sh.T:sh.len_after] = inp["k_new"]
+        V_all[:, :, sh.T:sh.len_after] = inp["v_new"]
+    if lens_b is None:
+        lens_b = [sh.len_after] * B
+    seq = _seq(lens_b)
+    L.select(inp["F"], seq)
+    L.attend(inp["Q"], seq)
+    torch.cuda.synchronize()
+    assert L.status.item() == 0
+    assert torch.equal(L.k_cache, K_all) and torch.equal(L.v_cache, V_all)
+    lens_p = _lens_pair(lens_b, H_kv)
+    Kb, Vb = bits(K_all).reshape(P, sh.T_cap, D), bits(V_all).reshape(P, sh.T_cap, D)
+    Qb = bits(inp["Q"])
+    ktil, ridx, rcnt, rs, Oref, lref = oracle_layer(Kb, Vb, Qb, bits(inp["F"]), lens_p, sh.N_b, sh.n_init,
+                                                     sh.n_local, sh.k, G)
+    got = L.ktil.cpu().double().numpy().reshape(P, sh.N_b, D)
+    assert np.allclose(got, ktil, rtol=1e-5, atol=1e-6)
+    exempt = assert_selection_matches(L.idx, L.count, ridx, rcnt, rs, lens_p, sh.n_init, sh.n_local, sh.k)
+    # end-to-end: the GPU's own chain equals the oracle wherever the selections agree
+    same = (L.idx.cpu().numpy().reshape(ridx.shape) == ridx).all(axis=1)
+    Og = L.O.view(B, H_kv, G, D)
+    Oref4 = Oref.reshape(B, H_kv, G, D)
+    for p in np.nonzero(same)[0]:
+        b, g = divmod(int(p), H_kv)
+        assert_attn_close(Og[b, g], Oref4[b, g], f"pair {p}")
+    _check_lse(L.lse.view(P, G)[torch.from_numpy(same)], lref[same])
+    # attention alone over the oracle's selection, all pairs
+    O_gpu_on_ref = torch.zeros_like(L.O)
+    binding.sparse_decode_attn(inp["Q"], L.k_cache, L.v_cache, torch.from_numpy(ridx).cuda().view(B, H_kv, -1),
+                               torch.from_numpy(rcnt).cuda().view(B, H_kv), seq, O_gpu_on_ref)
+    torch.cuda.synchronize()
+    stats = assert_attn_close(O_gpu_on_ref, Oref.reshape(B, sh.H_q, D))
+    return exempt, stats
+
+
+def test_single_layer_4k_workload():
+    _pipeline(wl.SINGLE_4K)
+
+
+def test_llama8b_32k_append_workload():
+    exempt, _ = _pipeline(wl.LLAMA8B_32K)
+    assert exempt <= 2
+
+
+def test_ragged_batch_lengths():
+    sh = wl.DecodeShape("ragged", B=3, H_q=16, H_kv=4, T=8192, n_init=1, n_local=2, k=16, n_planted=12,
+                        seed=77)
+    _pipeline(sh, lens_b=[8192, 5000, 129])
+
+
+def test_decode_128k_layer_sampled_at_full_size():
+    """One physical layer of the 128K, B=8, G=8 workload at full size: append all
+    131072 tokens, select with two Forecast vectors, attend; the oracle checks four
+    sampled pairs one by one."""
+    sh = wl.DECODE_128K
+    B, H_kv, G = sh.B, sh.H_kv, sh.G
+    planted = wl.planted_sets(sh, 2)
+    L = GpuLayer(B, sh.H_q, H_kv, sh.T, sh.N_b, sh.n_init, sh.n_local, sh.k)
+    sample = [0, 13, 38, 63]
+    host = {}
+    for b in range(B):
+        Kb = torch.empty((1, H_kv, sh.T, D), dtype=torch.bfloat16, device="cuda")
+        Vb = torch.empty_like(Kb)
+        for h in range(H_kv):
+            p = b * H_kv + h
+            Kb[0, h], Vb[0, h] = wl.kv_pair(sh, 1, p, planted[1, p], "cuda")
+            if p in sample:
+                host[p] = (bits(Kb[0, h]), bits(Vb[0, h]))
+        binding.sparse_pool_append(L.k_cache[b:b + 1], L.v_cache[b:b + 1], L.ktil[b:b + 1], Kb, Vb, 0)
+    torch.cuda.synchronize()
+    seq = _seq([sh.T] * B)
+    for logical in (0, 10):            # F_0 and F_10 both target physical layer 1
+        F = wl.forecast(sh, 1, logical, "cuda")
+        Q = wl.queries(sh, logical + 1, "cuda")
+        L.select(F, seq)
+        L.attend(Q, seq)
+        torch.cuda.synchronize()
+        assert L.status.item() == 0
+        Fb, Qb = bits(F).reshape(sh.pairs, D), bits(Q).reshape(sh.pairs, G, D)
+        for p in sample:
+            Kp, Vp = host[p]
+            ktil, ridx, rcnt, rs, Oref, lref = oracle_layer(Kp[None], Vp[None], Qb[p][None], Fb[p][None],
+                                                             [sh.T], sh.N_b, sh.n_init, sh.n_local, sh.k, G)
+            gi = L.idx.view(sh.pairs, -1)[p:p + 1]
+            gc = L.count.view(sh.pairs)[p:p + 1]
+            got = L.ktil.view(sh.pairs, sh.N_b, D)[p].cpu().double().numpy()
+            assert np.allclose(got, ktil[0], rtol=1e-5, atol=1e-6)
+            exempt = assert_selection_matches(gi, gc, ridx, rcnt, rs, [sh.T], sh.n_init, sh.n_local, sh.k)
+            assert len(set(planted[1, p].tolist()) & set(ridx[0].tolist())) >= 40   # generator sanity
+            if not exempt:
+                b, h = divmod(p, H_kv)
+                assert_attn_close(L.O.view(B, H_kv, G, D)[b, h], Oref[0], f"pair {p}")
+
+
+# ----------------------------------------------------------------------------- grouped verification
+
+
+def _verify(sh, n_split=0):
+    inp = wl.verify_inputs(sh, device="cuda")
+    O = torch.zeros((sh.B, sh.N_q, sh.H_q, D), dtype=torch.bfloat16, device="cuda")
+    loaded = torch.zeros(1, dtype=torch.int64, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.sparse_verify_attn_grouped(inp["Q"], inp["K"], inp["V"], inp["I"], sh.C, sh.window_blocks,
+                                       inp["seq_len"], O, blocks_loaded=loaded, n_split=n_split, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    return inp, O, int(loaded.item())
+
+
+def test_verify_64k_workload_matches_oracle_and_saves_loads():
+    sh = wl.VERIFY_64K
+    inp, O, loaded = _verify(sh)
+    Oref, union, per_query = oracle.verify(bits(inp["Q"]), bits(inp["K"]), bits(inp["V"]), inp["I"].cpu().numpy(),
+                                           sh.C, sh.window_blocks, [sh.T] * sh.B)
+    assert_attn_close(O, Oref)
+    assert loaded == union
+    bound = (1 + (sh.C - 1) * (1 - sh.gamma)) / sh.C
+    assert loaded / per_query <= bound
+    assert loaded / per_query == pytest.approx(36 / 96)
+
+
+def test_verify_equals_per_query_decode():
+    sh = wl.VerifyShape("small", B=2, H_q=8, H_kv=2, T=3000, N_q=6, n_sel=5, gamma=0.6, window_tokens=3 * BLK, C=3,
+                        seed=31)
+    inp, O, _ = _verify(sh)
+    nb = (sh.T + BLK - 1) // BLK
+    W = list(range(nb - sh.window_blocks, nb))
+    k_cap = sh.n_sel + sh.window_blocks
+    for q in range(sh.N_q):
+        idx = torch.full((sh.B, sh.H_kv, k_cap), -1, dtype=torch.int32)
+        for b in range(sh.B):
+            for h in range(sh.H_kv):
+                s = sorted(set(inp["I"][b, h, q].tolist()) | set(W))
+                idx[b, h, :len(s)] = torch.tensor(s)
+        cnt = (idx >= 0).sum(-1).to(torch.int32)
+        Od = torch.zeros((sh.B, sh.H_q, D), dtype=torch.bfloat16, device="cuda")
+        binding.sparse_decode_attn(inp["Q"][:, q].contiguous(), inp["K"], inp["V"], idx.cuda(), cnt.cuda(),
+                                   inp["seq_len"], Od)
+        torch.cuda.synchronize()
+        assert (Od.float() - O[:, q].float()).abs().max().item() <= 2 ** -7
+
+
+@pytest.mark.parametrize("n_split", [1, 2, 8])
+def test_verify_split_invariance(n_split):
+    sh = wl.VerifyShape("split", B=1, H_q=16, H_kv=4, T=64 * BLK, N_q=8, n_sel=16, gamma=0.75,
+                        window_tokens=8 * BLK, C=4, seed=33)
+    inp, O, loaded = _verify(sh, n_split=n_split)
+    Oref, union, _ = oracle.verify(bits(inp["Q"]), bits(inp["K"]), bits(inp["V"]), inp["I"].cpu().numpy(), sh.C,
+                                   sh.window_blocks, [sh.T] * sh.B)
+    assert_attn_close(O, Oref)
+    assert loaded == union
+
+
+# ----------------------------------------------------------------------------- offloaded gather
+
+
+def test_gather_from_pinned_host_and_attend_over_the_ring():
+    B, H_q, H_kv, T = 2, 16, 4, 96 * BLK + 10
+    P, k_cap = B * H_kv, 15
+    lens_b = [T, T - 700]
+    lens_p = _lens_pair(lens_b, H_kv)
+    K = wl.randn_bf16((B, H_kv, T, D), 61).pin_memory()
+    V = wl.randn_bf16((B, H_kv, T, D), 62).pin_memory()
+    # staged block lists from the generator: ascending, distinct, the last (partial) block included
+    idx_np = np.full((P, k_cap), -1, np.int32)
+    cnt_np = np.zeros(P, np.int32)
+    for p in range(P):
+        nb = (int(lens_p[p]) + BLK - 1) // BLK
+        c = k_cap if p % 3 else k_cap - 4
+        blocks = wl.draw_blocks(c - 1, 0, nb - 1, seed=900 + p).tolist() + [nb - 1]
+        idx_np[p, :c], cnt_np[p] = blocks, c
+    idx = torch.from_numpy(idx_np).cuda().view(B, H_kv, k_cap)
+    cnt = torch.from_numpy(cnt_np).cuda().view(B, H_kv)
+    seq = _seq(lens_b)
+    k_ring = torch.full((B, H_kv, k_cap, BLK, D), 3.0, dtype=torch.bfloat16, device="cuda")
+    v_ring = torch.full_like(k_ring, 3.0)
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    copy = torch.cuda.Stream()
+    copy.wait_stream(torch.cuda.current_stream())
+    binding.sparse_gather_offloaded(K, V, idx, cnt, k_ring, v_ring, ready_flag=flag, n_ctas=24, stream=copy)
+    torch.cuda.current_stream().wait_stream(copy)
+    torch.cuda.synchronize()
+    assert flag.item() == 24
+    ring_ref = np.full((P, k_cap, BLK, D), bits(torch.tensor(3.0, dtype=torch.bfloat16)), np.uint16)
+    oracle.gather(bits(K).reshape(P, T, D), idx_np, cnt_np, ring_ref)
+    assert np.array_equal(bits(k_ring).reshape(ring_ref.shape), ring_ref)
+    oracle.gather(bits(V).reshape(P, T, D), idx_np, cnt_np, ring_ref)
+    assert np.array_equal(bits(v_ring).reshape(ring_ref.shape), ring_ref)
+    # attention over the ring (slot = list position) equals attention over the resident cache
+    Kd, Vd = K.cuda(), V.cuda()
+    Q = wl.randn_bf16((B, H_q, D), 64, "cuda")
+    O_ring = torch.zeros((B, H_q, D), dtype=torch.bfloat16, device="cuda")
+    O_res = torch.zeros_like(O_ring)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots = torch.arange(k_cap, dtype=torch.int32, device="cuda").repeat(B, H_kv, 1).contiguous()
+    binding.sparse_decode_attn_ex(Q, k_ring, v_ring, idx, cnt, seq, O_ring, flag, 24, 1_000_000, blk_slot=slots,
+                                  status=status)
+    binding.sparse_decode_attn(Q, Kd, Vd, idx, cnt, seq, O_res)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert torch.equal(O_ring, O_res)
+    Oref, _ = oracle.attn(bits(Q).reshape(P, H_q // H_kv, D), bits(K).reshape(P, T, D), bits(V).reshape(P, T, D),
+                          idx_np, cnt_np, lens_p)
+    assert_attn_close(O_ring, Oref.reshape(B, H_q, D))
