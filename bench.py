@@ -223,9 +223,12 @@ class Decode128k:
                                         stream=stream)
 
     def _attend(self, l, stream, n_split=0):
+        # the block list of every layer comes from the side stream through an event, so
+        # K/V streaming may start while the previous attention drains
         q = l % self.sh.phys_layers
         self.binding.sparse_decode_attn(self.Q[l], self.k_cache[q], self.v_cache[q], self.idx[l], self.count[l],
-                                        self.seq, self.O[l], status=self.status, n_split=n_split, stream=stream)
+                                        self.seq, self.O[l], status=self.status, n_split=n_split,
+                                        flags=self.binding.SPARSE_ATTN_BLOCKS_READY, stream=stream)
 
     def enqueue_step(self, events=None, n_split=0):
         """Enqueue one step on the current stream (+ the side stream).  ``events``
@@ -233,10 +236,14 @@ class Decode128k:
         torch = self.torch
         main = torch.cuda.current_stream(self.dev)
         L = self.sh.layers
-        self._select(0, self.F0, main)
+        sel_done = [None] * L
+        self.side.wait_stream(main)
+        self._select(0, self.F0, self.side)          # layer 0: its own current-layer Forecast
+        ev0 = torch.cuda.Event()
+        ev0.record(self.side)
+        sel_done[0] = ev0
         after_prev_attn = torch.cuda.Event()
         after_prev_attn.record(main)
-        sel_done = [None] * L
         for l in range(L):
             if l + 1 < L:
                 self.side.wait_event(after_prev_attn)
@@ -375,63 +382,68 @@ def run_ours(args, rank, world, local_rank):
 # ----------------------------------------------------------------------------- CPU oracle baseline
 
 
-def _oracle_pair_layer_sample(wk, layer: int, batches, threads: int):
-    """Regenerate the sampled batch elements of one logical layer on the GPU, copy them
-    to the host and time the oracle's selection + attention for them (pooling, which
-    the step does not repeat, is prepared outside the timing)."""
+def _prepare_oracle_slice(wk, layer: int, batches):
+    """Host copies of the inputs of one layer slice (the sampled batch elements): this
+    layer's K/V and compressed keys, the next layer's compressed keys, Q_l and F_l.
+    Pooling is not part of a decode step (the compressed keys are resident), so it
+    happens here, outside any timing."""
     import numpy as np
-    import torch
     import oracle
     wl, sh = wk.wl, wk.sh
-    q_next = (layer + 1) % sh.phys_layers
+    q_cur, q_next = layer % sh.phys_layers, (layer + 1) % sh.phys_layers
     planted = wl.planted_sets(sh, sh.phys_layers)
-    H_kv, G = sh.H_kv, sh.G
-    pairs = [b * H_kv + h for b in batches for h in range(H_kv)]
+    pairs = [b * sh.H_kv + h for b in batches for h in range(sh.H_kv)]
     Ks, Vs, Kn = [], [], []
     for p in pairs:
-        k, v = wl.kv_pair(sh, layer % sh.phys_layers, p, planted[layer % sh.phys_layers, p], wk.dev)
+        k, v = wl.kv_pair(sh, q_cur, p, planted[q_cur, p], wk.dev)
         Ks.append(wl.bf16_bits(k))
         Vs.append(wl.bf16_bits(v))
         kn, _ = wl.kv_pair(sh, q_next, p, planted[q_next, p], wk.dev)
         Kn.append(wl.bf16_bits(kn))
     K, V, Knext = np.stack(Ks), np.stack(Vs), np.stack(Kn)
     lens = [sh.T] * len(pairs)
-    oracle.set_threads(threads)
-    ktil_next = oracle.pool(Knext, lens, sh.N_b)          # resident in the step: not timed
     ktil_cur = oracle.pool(K, lens, sh.N_b)
+    ktil_next = oracle.pool(Knext, lens, sh.N_b)
     F = wl.bf16_bits(wl.forecast(sh, q_next, layer, "cpu")).reshape(sh.pairs, D)[pairs]
-    Fc = wl.bf16_bits(wl.forecast(sh, layer % sh.phys_layers, layer - 1, "cpu")).reshape(sh.pairs, D)[pairs]
-    Q = wl.bf16_bits(wl.queries(sh, layer, "cpu")).reshape(sh.pairs, G, D)[pairs]
+    Fc = wl.bf16_bits(wl.forecast(sh, q_cur, layer - 1, "cpu")).reshape(sh.pairs, D)[pairs]
+    Q = wl.bf16_bits(wl.queries(sh, layer, "cpu")).reshape(sh.pairs, sh.G, D)[pairs]
     idx, cnt, _ = oracle.select(Fc, ktil_cur, lens, sh.n_init, sh.n_local, sh.k)   # this layer's blocks
+    return dict(K=K, V=V, Q=Q, F=F, ktil_next=ktil_next, idx=idx, cnt=cnt, lens=lens, n=len(pairs), sh=sh)
+
+
+def _time_oracle_slice(sl, threads: int):
+    """Time the oracle's selection for layer l+1 and attention of layer l on a slice."""
+    import oracle
+    sh = sl["sh"]
+    oracle.set_threads(threads)
     t0 = time.perf_counter()
-    oracle.select(F, ktil_next, lens, sh.n_init, sh.n_local, sh.k)
-    oracle.attn(Q, K, V, idx, cnt, lens)
-    return time.perf_counter() - t0, len(pairs)
+    oracle.select(sl["F"], sl["ktil_next"], sl["lens"], sh.n_init, sh.n_local, sh.k)
+    oracle.attn(sl["Q"], sl["K"], sl["V"], sl["idx"], sl["cnt"], sl["lens"])
+    return time.perf_counter() - t0, sl["n"]
 
 
-def cpu_baseline(wk, budget_s: float = 15.0, max_samples: int = 64):
-    """The oracle on the host cores over a bounded sample of the 128K step: whole
-    layers of B_s batch elements (B_s x 8 pairs, one OpenMP thread per pair), scaled to
-    80 layers x 64 pairs."""
+def cpu_baseline(wk, budget_s: float = 15.0, slices: int = 4):
+    """The oracle on the host cores over a bounded sample of the 128K step: layer slices
+    of B_s batch elements (B_s x 8 pairs, one OpenMP thread per pair), repeated until
+    the time budget is spent, scaled to 80 layers x 64 pairs."""
     cores = len(os.sched_getaffinity(0))
-    per_call = max(1, min(wk.sh.B, cores // wk.sh.H_kv)) if cores >= wk.sh.H_kv else 1
+    per_call = max(1, min(wk.sh.B, cores // wk.sh.H_kv))
     threads = min(cores, per_call * wk.sh.H_kv)
-    spent, pair_layers, layers = 0.0, 0, []
-    for i in range(max_samples):
-        layer = (7 * i) % wk.sh.layers
-        batches = [(i * per_call + j) % wk.sh.B for j in range(per_call)]
-        dt, n = _oracle_pair_layer_sample(wk, layer, batches, threads)
+    prepared = [_prepare_oracle_slice(wk, (7 * i) % wk.sh.layers,
+                                      [(i * per_call + j) % wk.sh.B for j in range(per_call)])
+                for i in range(slices)]
+    spent, pair_layers, reps = 0.0, 0, 0
+    while spent < budget_s or reps < len(prepared):
+        dt, n = _time_oracle_slice(prepared[reps % len(prepared)], threads)
         spent += dt
         pair_layers += n
-        layers.append(layer)
-        if spent >= budget_s:
-            break
-    per_pair_layer = spent / pair_layers
-    step_s = per_pair_layer * wk.sh.pairs * wk.sh.layers
+        reps += 1
+    step_s = spent / pair_layers * wk.sh.pairs * wk.sh.layers
     return {"value": round(1.0 / step_s, 6), "unit": "steps/s", "cores": threads, "kind": "oracle",
-            "sample": f"{pair_layers} (pair, layer) units = {len(layers)} layer slices of {per_call} batch "
-                      f"element(s) x 8 KV heads, select(l+1) + attention(l) in fp64, {spent:.1f} s, scaled to "
-                      f"{wk.sh.pairs} pairs x {wk.sh.layers} layers"}
+            "sample": f"{reps} timed layer slices ({len(prepared)} distinct) of {per_call} batch element(s) x "
+                      f"{wk.sh.H_kv} KV heads = {pair_layers} (pair, layer) units of select(l+1) + attention(l) "
+                      f"in fp64 on {threads} threads, {spent:.1f} s, scaled to {wk.sh.pairs} pairs x "
+                      f"{wk.sh.layers} layers"}
 
 
 def run_reference(args, rank, world, local_rank):
@@ -451,9 +463,10 @@ def run_reference(args, rank, world, local_rank):
     wk.wl, wk.sh, wk.dev = wl, wl.DECODE_128K, dev
     cores = len(os.sched_getaffinity(0))
     threads = min(cores, wk.sh.H_kv)
+    prepared = [_prepare_oracle_slice(wk, (7 * i) % wk.sh.layers, [i % wk.sh.B]) for i in range(4)]
     times = []
     for i in range(args.warmup + args.steps):
-        dt, n = _oracle_pair_layer_sample(wk, (7 * i) % wk.sh.layers, [i % wk.sh.B], threads)
+        dt, n = _time_oracle_slice(prepared[i % len(prepared)], threads)
         if i >= args.warmup:
             times.append(dt / n)
     per_pair_layer = statistics.mean(times)
@@ -473,6 +486,75 @@ def run_reference(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_layer_case(args, local_rank):
+    """One physical layer of the 128K workload (4.3 GB of KV): selection then attention,
+    serialised on one stream with a 512 MB L2 flush before each, every launch bracketed
+    by CUDA events.  Used for isolated kernel times and small ncu captures."""
+    import torch
+    from block_sparse_long_pool_gb300 import binding
+    from block_sparse_long_pool_gb300 import workloads as wl
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import dataclasses
+    sh = wl.DECODE_128K
+    if args.tokens:
+        sh = dataclasses.replace(sh, T=args.tokens)
+    B, H_kv, H_q, T = sh.B, sh.H_kv, sh.H_q, sh.T
+    k_cap = sh.n_init + sh.n_local + sh.k
+    planted = wl.planted_sets(sh, 1)
+    select_only = args.case == "select"
+    # the select-only case keeps just the compressed keys resident (KV built per batch element)
+    kc = torch.empty((1 if select_only else B, H_kv, T, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    kt = torch.zeros((B, H_kv, sh.N_b, D), dtype=torch.float32, device=dev)
+    for b in range(B):
+        kn = torch.empty((1, H_kv, T, D), dtype=torch.bfloat16, device=dev)
+        vn = torch.empty_like(kn)
+        for h in range(H_kv):
+            kn[0, h], vn[0, h] = wl.kv_pair(sh, 0, b * H_kv + h, planted[0, b * H_kv + h], dev)
+        cb = 0 if select_only else b
+        binding.sparse_pool_append(kc[cb:cb + 1], vc[cb:cb + 1], kt[b:b + 1], kn, vn, 0)
+    del kn, vn
+    seq = torch.full((B,), T, dtype=torch.int32, device=dev)
+    idx = torch.empty((B, H_kv, k_cap), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B, H_kv), dtype=torch.int32, device=dev)
+    O = torch.empty((B, H_q, D), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(max(1, args.flush_mb) << 20, dtype=torch.uint8, device=dev)
+    sel_ms, att_ms = [], []
+    for i in range(args.warmup + args.steps):
+        F = wl.forecast(sh, 0, i, dev)
+        Q = wl.queries(sh, i, dev)
+        flush.fill_(i & 255)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        binding.sparse_select_topk(F, kt, seq, sh.n_init, sh.n_local, sh.k, idx, cnt, status=status)
+        e[1].record()
+        flush.fill_((i + 1) & 255)
+        e3 = torch.cuda.Event(enable_timing=True)
+        e3.record()
+        if not select_only:
+            binding.sparse_decode_attn(Q, kc, vc, idx, cnt, seq, O, status=status, n_split=args.n_split)
+        e[2].record()
+        torch.cuda.synchronize(dev)
+        if i >= args.warmup:
+            sel_ms.append(e[0].elapsed_time(e[1]))
+            att_ms.append(e3.elapsed_time(e[2]))
+    assert status.item() == 0
+    peak, src = measured_peaks()
+    attn_bytes = sh.pairs * sh.k_tot * KV_BLOCK_BYTES
+    sel_bytes = sh.pairs * sh.N_b * KTIL_ROW_BYTES
+    a, s_ = max(1e-6, statistics.median(att_ms)), statistics.median(sel_ms)
+    print(json.dumps({"case": "decode_128k_one_layer", "T": T, "steps": args.steps, "n_split": args.n_split,
+                      "attn_us": round(a * 1e3, 2), "attn_gbs": round(attn_bytes / a / 1e6, 1),
+                      "attn_frac": round(attn_bytes / a / 1e6 / peak, 4),
+                      "select_us": round(s_ * 1e3, 2), "select_gbs": round(sel_bytes / s_ / 1e6, 1),
+                      "select_frac": round(sel_bytes / s_ / 1e6 / peak, 4), "peak_gbs": peak, "peak_source": src}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -481,11 +563,19 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=["step", "layer", "select"], default="step",
+                    help="step: the 80-layer decode step (the bench line); layer: one physical layer, "
+                         "kernels serialised and timed alone (for profiling); select: selection only")
+    ap.add_argument("--n-split", type=int, default=0)
+    ap.add_argument("--tokens", type=int, default=0, help="layer case: cached tokens (default 131072)")
+    ap.add_argument("--flush-mb", type=int, default=512, help="layer case: L2 flush buffer before each launch")
     args = ap.parse_args()
-    if args.warmup < 3:
+    if args.warmup < 3 and args.case == "step":
         ap.error("--warmup must be >= 3")
     rank, world, local_rank = dist_env()
-    if args.impl == "reference":
+    if args.case in ("layer", "select"):
+        run_layer_case(args, local_rank)
+    elif args.impl == "reference":
         run_reference(args, rank, world, local_rank)
     else:
         run_ours(args, rank, world, local_rank)

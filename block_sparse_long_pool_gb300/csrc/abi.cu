@@ -75,6 +75,22 @@ int device_info(DeviceInfo *out)
     return SPARSE_OK;
 }
 
+int configure_kernel(const void *func, int dyn_smem, int device, int *configured)
+{
+    if (device < 0 || device >= kMaxDevices)
+        return fail(SPARSE_ERR_UNSUPPORTED, "device ordinal %d out of range", device);
+    std::lock_guard<std::mutex> lock(g_info_mu);
+    if (configured[device] >= dyn_smem + 1)
+        return SPARSE_OK;
+    cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess)
+        return cuda_status(e, "cudaFuncSetAttribute");
+    configured[device] = dyn_smem + 1;
+    return SPARSE_OK;
+}
+
 int make_kv_tensor_map(CUtensorMap *map, const void *base, long long rows_per_pair, long long pairs)
 {
     std::call_once(g_encode_once, load_encoder);

@@ -94,6 +94,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     return false;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Wait until the grid that precedes this one on its stream has completed and its
+// memory is visible (a no-op when the launch was not programmatic).
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the grid that follows on the stream to be scheduled once every CTA of this
+// grid has issued this (or exited).
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
@@ -232,6 +248,12 @@ int device_info(DeviceInfo *out);
 // 3-D tiled tensor map over [pairs][rows][128] bf16 with a 64 x 64 box and 128-byte
 // swizzle (the layout the attention kernel reads).  Returns SPARSE_OK or an error.
 int make_kv_tensor_map(CUtensorMap *map, const void *base, long long rows_per_pair, long long pairs);
+
+// Configure a kernel once per device: its dynamic shared memory limit, and the
+// largest shared-memory carveout.  All kernels of the library prefer the same
+// carveout, so their CTAs can share an SM without the SM being reconfigured (a small
+// carveout chosen for one kernel would keep another kernel's CTAs off that SM).
+int configure_kernel(const void *func, int dyn_smem, int device, int *configured);
 
 inline bool aligned16(const void *p)
 {

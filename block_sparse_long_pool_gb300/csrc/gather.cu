@@ -126,6 +126,15 @@ extern "C" SPARSE_API int sparse_gather_offloaded(const uint16_t *k_host, const 
     }
     GatherParams p{src[0], src[1], idx, count, k_ring, v_ring, ready_flag, status, T_host, k_tot,
                    static_cast<int>(pairs)};
+    {
+        sp_host::DeviceInfo dinfo;
+        int rc0 = sp_host::device_info(&dinfo);
+        static int configured[64];
+        if (rc0 == SPARSE_OK)
+            rc0 = sp_host::configure_kernel(reinterpret_cast<const void *>(gather_kernel), 0, dinfo.device, configured);
+        if (rc0 != SPARSE_OK)
+            return rc0;
+    }
     gather_kernel<<<n_ctas, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(p);
     return sp_host::cuda_status(cudaGetLastError(), "sparse_gather_offloaded launch");
 }

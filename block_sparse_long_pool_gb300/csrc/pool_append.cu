@@ -118,6 +118,15 @@ extern "C" SPARSE_API int sparse_pool_append(uint16_t *k_cache, uint16_t *v_cach
     const int last_block = static_cast<int>((len_after - 1) / kBlk);
     AppendParams p{k_cache, v_cache, ktil, k_new, v_new, T_cap, len_before, N_cap, n_new, first_block};
     dim3 grid(static_cast<unsigned>(last_block - first_block + 1), static_cast<unsigned>(pairs));
+    {
+        sp_host::DeviceInfo dinfo;
+        int rc0 = sp_host::device_info(&dinfo);
+        static int configured[64];
+        if (rc0 == SPARSE_OK)
+            rc0 = sp_host::configure_kernel(reinterpret_cast<const void *>(pool_append_kernel), 0, dinfo.device, configured);
+        if (rc0 != SPARSE_OK)
+            return rc0;
+    }
     pool_append_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(p);
     return sp_host::cuda_status(cudaGetLastError(), "sparse_pool_append launch");
 }

@@ -5,14 +5,15 @@
 // the k best blocks outside B_init and B_local are taken, and the union
 // B_init ∪ B_local ∪ top-k is written in ascending block order.
 //
-// GB300 design: one thread-block cluster of S CTAs per (batch, KV head) pair.  CTA r
-// scores a contiguous slice of the pair's blocks (a warp per compressed-key row,
-// 16-byte loads, shuffle reduction) into an order-preserving 32-bit key held in its
-// shared memory.  The k-th largest key is found by an MSB-first radix select over 4
-// byte-digits whose histograms are summed across the cluster through distributed
-// shared memory; equal keys are taken in ascending block order, so ties go to the
-// lower block index.  Every exchange between CTAs goes through DSMEM: the kernel
-// uses no global scratch memory.
+// GB300 design: one thread-block cluster of S CTAs per (batch, KV head) pair.  Every
+// CTA scores a contiguous slice of the pair's compressed keys (a warp per 512-byte
+// row, 16-byte loads, shuffle reduction) and stores each score as an order-preserving
+// 32-bit key straight into CTA 0's shared memory (distributed shared memory stores).
+// After one cluster barrier the other CTAs exit and CTA 0 alone finds the k-th
+// largest candidate key by an MSB-first radix select over 4 byte-digits (histograms
+// built with warp-aggregated shared-memory atomics), takes equal keys in ascending
+// block order (ties go to the lower block index), and compacts the selection in
+// block order with CTA-wide scans.  No global scratch memory.
 #include <limits.h>
 
 #include "common.cuh"
@@ -21,10 +22,13 @@ namespace {
 
 using namespace sp;
 
-constexpr int kThreads = 512;
+// 256 threads and at most ~64 registers per thread (16K registers per CTA): a selection
+// CTA then fits on an SM beside two attention CTAs, so the selection for layer l+1 can
+// run on the SMs that stream layer l's blocks.
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCluster = 8;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 8;
 
 struct SelectParams {
     const uint16_t *F;
@@ -82,12 +86,11 @@ __device__ __forceinline__ int block_inclusive_scan(int v, int *warp_sums, int &
     return v + before;
 }
 
-__global__ void __launch_bounds__(kThreads) select_topk_kernel(const SelectParams p)
+__global__ void __launch_bounds__(kThreads, 3) select_topk_kernel(const SelectParams p)
 {
-    extern __shared__ uint32_t keys[];           // keys of this CTA's block slice
-    __shared__ uint32_t hist[2][256];
+    extern __shared__ uint32_t keys[];           // CTA 0: the keys of all the pair's blocks
+    __shared__ uint32_t hist[256];
     __shared__ int warp_sums[kWarps];
-    __shared__ int xchg[2];                      // [0] = equal-key count, [1] = sure selections
     __shared__ int bcast[4];
 
     const int tid = threadIdx.x;
@@ -97,6 +100,9 @@ __global__ void __launch_bounds__(kThreads) select_topk_kernel(const SelectParam
     const int pair = blockIdx.y;
     const int b = pair / p.H_kv;
 
+    // programmatic dependent launch: every input may come from the kernel before this
+    // one on the stream
+    griddep_wait();
     const long long len = p.seq_len[b];
     long long nb_ll = len <= 0 ? 0 : (len + kBlk - 1) / kBlk;
     if (nb_ll > p.N_cap) {
@@ -108,16 +114,15 @@ __global__ void __launch_bounds__(kThreads) select_topk_kernel(const SelectParam
     const int chunk = (nb + static_cast<int>(S) - 1) / static_cast<int>(S);
     const int j0 = min(nb, static_cast<int>(rank) * chunk);
     const int j1 = min(nb, j0 + chunk);
-    const int my = j1 - j0;
 
     // Candidates: every block that is neither init nor local (Alg.1 step 2).
     const int cand_lo = p.n_init;
     const int cand_hi = nb - p.n_local;
-    const int n_cand = max(0, cand_hi - cand_lo);
-    const bool take_all = n_cand <= p.k;
+    const bool take_all = max(0, cand_hi - cand_lo) <= p.k;
 
-    // ---- 1. scores s_j = F . ktil_j (fp32) as order keys
-    if (!take_all && my > 0) {
+    // ---- 1. scores s_j = F . ktil_j (fp32) as order keys, stored into CTA 0
+    if (!take_all && j1 > j0) {
+        uint32_t *keys0 = static_cast<uint32_t *>(__cluster_map_shared_rank(keys, 0));
         const uint2 fr = *reinterpret_cast<const uint2 *>(p.F + static_cast<size_t>(pair) * kD + 4 * lane);
         const float2 f01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&fr.x));
         const float2 f23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&fr.y));
@@ -141,48 +146,49 @@ __global__ void __launch_bounds__(kThreads) select_topk_kernel(const SelectParam
                     s += __shfl_xor_sync(0xffffffffu, s, o);
                 const int j = jb + u * kWarps;
                 if (lane == 0 && j < j1)
-                    keys[j - j0] = order_key(s);
+                    keys0[j] = order_key(s);
             }
         }
     }
-    __syncthreads();
+    // the keys are in CTA 0 (release/acquire at cluster scope); the next kernel on the
+    // stream may be scheduled, and the scoring CTAs are done
+    cluster_sync();
+    griddep_launch_dependents();
+    if (rank != 0)
+        return;
 
-    // ---- 2. k-th largest key by MSB-first radix select across the cluster
+    // ---- 2. CTA 0: k-th largest candidate key by MSB-first radix select
     uint32_t prefix = 0, pmask = 0;
     int need = p.k;
     if (!take_all) {
         for (int pass = 0; pass < 4; ++pass) {
             const int shift = 24 - 8 * pass;
-            uint32_t *h = hist[pass & 1];
-            for (int i = tid; i < 256; i += kThreads)
-                h[i] = 0;
+            hist[tid] = 0;
             __syncthreads();
-            for (int i = tid; i < my; i += kThreads) {
-                const int j = j0 + i;
-                if (j >= cand_lo && j < cand_hi) {
-                    const uint32_t key = keys[i];
+            for (int jb = cand_lo; jb < cand_hi; jb += kThreads) {
+                const int j = jb + tid;
+                uint32_t digit = 0xFFFFFFFFu;
+                if (j < cand_hi) {
+                    const uint32_t key = keys[j];
                     if ((key & pmask) == prefix)
-                        atomicAdd(&h[(key >> shift) & 255u], 1u);
+                        digit = (key >> shift) & 255u;
                 }
+                // one atomic per distinct digit in the warp
+                const uint32_t same = __match_any_sync(0xffffffffu, digit);
+                if (digit != 0xFFFFFFFFu && lane == __ffs(same) - 1)
+                    atomicAdd(&hist[digit], static_cast<uint32_t>(__popc(same)));
             }
-            cluster_sync();
+            __syncthreads();
             // thread t holds digit d = 255 - t: an inclusive scan gives the number of
-            // keys with a digit >= d.
-            int tot = 0;
+            // matching keys with a digit >= d
             const int d = 255 - tid;
-            if (tid < 256) {
-                const uint32_t local = smem_u32(&h[d]);
-                for (uint32_t c = 0; c < S; ++c)
-                    tot += static_cast<int>(dsmem_ld_u32(dsmem_addr(local, c)));
-            }
+            const int tot = static_cast<int>(hist[d]);
             int all;
-            const int at_or_above = block_inclusive_scan(tid < 256 ? tot : 0, warp_sums, all);
-            if (tid < 256) {
-                const int above = at_or_above - tot;
-                if (at_or_above >= need && above < need) {
-                    bcast[0] = d;
-                    bcast[1] = need - above;
-                }
+            const int at_or_above = block_inclusive_scan(tot, warp_sums, all);
+            const int above = at_or_above - tot;
+            if (at_or_above >= need && above < need) {
+                bcast[0] = d;
+                bcast[1] = need - above;
             }
             __syncthreads();
             prefix |= static_cast<uint32_t>(bcast[0]) << shift;
@@ -194,89 +200,41 @@ __global__ void __launch_bounds__(kThreads) select_topk_kernel(const SelectParam
     const uint32_t thr = prefix;   // the k-th largest candidate key
     const int need_eq = need;      // keys equal to thr to take, lowest block ids first
 
-    // ---- 3. per-thread counts over a contiguous run of this CTA's slice
-    const int ipt = (my + kThreads - 1) / kThreads;
-    const int it0 = min(my, tid * ipt), it1 = min(my, it0 + ipt);
-    int n_eq = 0, n_sure = 0;
-    for (int i = it0; i < it1; ++i) {
-        const int j = j0 + i;
-        const bool forced = j < p.n_init || j >= nb - p.n_local;
-        if (forced) {
-            ++n_sure;
-        } else if (j >= cand_lo && j < cand_hi) {
-            if (take_all) {
-                ++n_sure;
-            } else {
-                const uint32_t key = keys[i];
-                n_sure += key > thr;
-                n_eq += key == thr;
-            }
-        }
-    }
-    int cta_eq, cta_sure;
-    const int eq_incl = block_inclusive_scan(n_eq, warp_sums, cta_eq);
-    block_inclusive_scan(n_sure, warp_sums, cta_sure);
-    if (tid == 0) {
-        xchg[0] = cta_eq;
-        xchg[1] = cta_sure;
-    }
-    cluster_sync();
-    if (tid == 0) {
-        int eq_before = 0, sel_before = 0, total = 0, eq_cum = 0;
-        const uint32_t a0 = smem_u32(&xchg[0]), a1 = smem_u32(&xchg[1]);
-        for (uint32_t c = 0; c < S; ++c) {
-            const int e = static_cast<int>(dsmem_ld_u32(dsmem_addr(a0, c)));
-            const int s = static_cast<int>(dsmem_ld_u32(dsmem_addr(a1, c)));
-            const int take = min(e, max(0, need_eq - eq_cum));
-            if (c < rank) {
-                eq_before += e;
-                sel_before += s + take;
-            }
-            eq_cum += e;
-            total += s + take;
-        }
-        bcast[0] = eq_before;
-        bcast[1] = sel_before;
-        bcast[2] = total;
-    }
-    __syncthreads();
-    const int eq_before = bcast[0], sel_before = bcast[1], total = bcast[2];
-
-    // ---- 4. selection flags and ascending compaction
-    int eq_rank = eq_before + eq_incl - n_eq;   // global rank of this thread's first equal key
+    // ---- 3. selection in block order: this thread's contiguous run of blocks
+    const int ipt = (nb + kThreads - 1) / kThreads;
+    const int it0 = min(nb, tid * ipt), it1 = min(nb, it0 + ipt);
+    int n_eq = 0;
+    if (!take_all)
+        for (int j = it0; j < it1; ++j)
+            n_eq += (j >= cand_lo && j < cand_hi && keys[j] == thr);
+    int total_eq;
+    const int eq_before = block_inclusive_scan(n_eq, warp_sums, total_eq) - n_eq;
     int n_sel = 0;
-    for (int i = it0; i < it1; ++i) {
-        const int j = j0 + i;
-        const bool forced = j < p.n_init || j >= nb - p.n_local;
-        if (forced) {
-            ++n_sel;
-        } else if (j >= cand_lo && j < cand_hi) {
-            if (take_all) {
-                ++n_sel;
-            } else {
-                const uint32_t key = keys[i];
-                if (key > thr)
-                    ++n_sel;
-                else if (key == thr)
-                    n_sel += (eq_rank++ < need_eq);
-            }
-        }
-    }
-    int cta_sel;
-    const int sel_incl = block_inclusive_scan(n_sel, warp_sums, cta_sel);
-    int pos = sel_before + sel_incl - n_sel;
-    eq_rank = eq_before + eq_incl - n_eq;
-    int *out = p.idx_out + static_cast<size_t>(pair) * p.k_tot;
-    bool overflow = false;
-    for (int i = it0; i < it1; ++i) {
-        const int j = j0 + i;
-        const bool forced = j < p.n_init || j >= nb - p.n_local;
-        bool sel = forced;
-        if (!forced && j >= cand_lo && j < cand_hi) {
+    int eq_rank = eq_before;
+    for (int j = it0; j < it1; ++j) {
+        bool sel = j < p.n_init || j >= nb - p.n_local;        // B_init and B_local
+        if (!sel && j >= cand_lo && j < cand_hi) {
             if (take_all) {
                 sel = true;
             } else {
-                const uint32_t key = keys[i];
+                const uint32_t key = keys[j];
+                sel = key > thr || (key == thr && eq_rank++ < need_eq);
+            }
+        }
+        n_sel += sel;
+    }
+    int total;
+    int pos = block_inclusive_scan(n_sel, warp_sums, total) - n_sel;
+    int *out = p.idx_out + static_cast<size_t>(pair) * p.k_tot;
+    eq_rank = eq_before;
+    bool overflow = false;
+    for (int j = it0; j < it1; ++j) {
+        bool sel = j < p.n_init || j >= nb - p.n_local;
+        if (!sel && j >= cand_lo && j < cand_hi) {
+            if (take_all) {
+                sel = true;
+            } else {
+                const uint32_t key = keys[j];
                 sel = key > thr || (key == thr && eq_rank++ < need_eq);
             }
         }
@@ -290,14 +248,10 @@ __global__ void __launch_bounds__(kThreads) select_topk_kernel(const SelectParam
     }
     if (overflow)
         report(p.status, SPARSE_ERR_BAD_INDEX);
-    if (rank == 0) {
-        for (int i = total + tid; i < p.k_tot; i += kThreads)
-            out[i] = -1;
-        if (tid == 0)
-            p.count_out[pair] = min(total, p.k_tot);
-    }
-    // peers may still be reading xchg through DSMEM
-    cluster_sync();
+    for (int i = total + tid; i < p.k_tot; i += kThreads)
+        out[i] = -1;
+    if (tid == 0)
+        p.count_out[pair] = min(total, p.k_tot);
 }
 
 }  // namespace
@@ -328,32 +282,29 @@ extern "C" SPARSE_API int sparse_select_topk(const uint16_t *F, const float *kti
     int S = 1;
     while (S < kMaxCluster && pairs * S * 2 <= 2LL * dev.sm_count && N_cap / (S * 2) >= 256)
         S *= 2;
-    const size_t smem = static_cast<size_t>((N_cap + S - 1) / S) * sizeof(uint32_t);
+    const size_t smem = static_cast<size_t>(N_cap) * sizeof(uint32_t);   // CTA 0 holds every key
     if (smem > static_cast<size_t>(dev.max_smem_optin) - 8192)
         return fail(SPARSE_ERR_UNSUPPORTED, "sparse_select_topk: N_cap=%d too large", N_cap);
-    static thread_local int configured_smem[64];
-    if (dev.device < 64 && configured_smem[dev.device] < static_cast<int>(smem)) {
-        rc = sp_host::cuda_status(cudaFuncSetAttribute(select_topk_kernel,
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       static_cast<int>(smem)),
-                                  "sparse_select_topk smem attribute");
-        if (rc != SPARSE_OK)
-            return rc;
-        configured_smem[dev.device] = static_cast<int>(smem);
-    }
+    static int configured[64];
+    rc = sp_host::configure_kernel(reinterpret_cast<const void *>(select_topk_kernel), static_cast<int>(smem),
+                                   dev.device, configured);
+    if (rc != SPARSE_OK)
+        return rc;
     SelectParams p{F, ktil, seq_len, idx_out, count_out, status, H_kv, N_cap, n_init, n_local, k, k_tot};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(S), static_cast<unsigned>(pairs), 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(S);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     void *args[] = {&p};
     return sp_host::cuda_status(cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(select_topk_kernel), args),
                                 "sparse_select_topk launch");

@@ -54,7 +54,8 @@ constexpr int kOffMask = kOffList + kMaxUnion * 4;       // uint32 umask[kMaxUni
 constexpr int kOffEntV = kOffMask + kMaxUnion * 4;       // union build scratch
 constexpr int kOffEntM = kOffEntV + kMaxUnion * 4;
 constexpr int kOffEntF = kOffEntM + kMaxUnion * 4;
-constexpr int kSmemDecode = kOffList + 1024;
+constexpr int kMaxListCta = kMaxUnion;                   // decode: staged slice of the block list
+constexpr int kSmemDecode = kOffList + 2 * kMaxListCta * 4 + 1024;
 constexpr int kSmemVerify = kOffEntF + kMaxUnion * 4 + 1024;
 
 enum { kCtrlAbort = 0, kCtrlList = 1 };
@@ -83,24 +84,13 @@ struct AttnParams {
     int C;
     int window_blocks;
     int n_groups;
+    unsigned flags;
     float scale_log2;
 };
 
 __device__ __forceinline__ uint32_t ld_b32(const uint16_t *p)
 {
     return *reinterpret_cast<const uint32_t *>(p);
-}
-
-// Block position inside the pair's region whose K/V rows the producer loads: the
-// slot table entry, or the logical block id itself for a resident cache (no table);
-// -1 when it lies outside the region.
-__device__ __forceinline__ int list_slot(const AttnParams &p, int pair, int i)
-{
-    const size_t at = static_cast<size_t>(pair) * p.k_tot + i;
-    const int slot = p.blk_slot != nullptr ? p.blk_slot[at] : p.blk_logical[at];
-    if (slot < 0 || static_cast<long long>(slot) * kBlk >= p.pair_stride)
-        return -1;
-    return slot;
 }
 
 // Merged union of the group's block sets (SSV mode A): ulist ascending, umask[u] the
@@ -193,6 +183,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         rows_valid = p.G;
     }
     const int b = pair / p.H_kv, g = pair % p.H_kv;
+    // Programmatic dependent launch: this grid may start while the kernel before it on
+    // the stream drains.  With SPARSE_ATTN_BLOCKS_READY the block list, lengths and K/V
+    // are already complete (the caller's promise), so only Q and the outputs wait;
+    // otherwise every input may come from that kernel and everything waits.
+    const bool early = !VERIFY && (p.flags & SPARSE_ATTN_BLOCKS_READY) != 0u;
+    if (!early)
+        griddep_wait();
     const long long len = p.seq_len[b];
     const int nb = len <= 0 ? 0 : static_cast<int>((len + kBlk - 1) / kBlk);
 
@@ -244,8 +241,26 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int i0 = min(n_list, static_cast<int>(rank) * per);
     const int i1 = min(n_list, i0 + per);
     const int my_n = i1 - i0;
+    // block ids of this CTA's slice, in shared memory: verification keeps the merged
+    // union (ulist/umask, whole list); decode stages its slice of the block table with
+    // each entry validated (-1 = skip: an out-of-range box is loaded, never a fault)
     const int *ulist = reinterpret_cast<const int *>(base + kOffList);
     const uint32_t *umask = reinterpret_cast<const uint32_t *>(base + kOffMask);
+    int *lslot = reinterpret_cast<int *>(base + kOffList);
+    int *llog = lslot + kMaxListCta;
+    if (!VERIFY) {
+        for (int i = tid; i < my_n; i += kThreads) {
+            const size_t at = static_cast<size_t>(pair) * p.k_tot + i0 + i;
+            const int logical = p.blk_logical[at];
+            const int slot = p.blk_slot != nullptr ? p.blk_slot[at] : logical;
+            const bool ok = logical >= 0 && slot >= 0 && static_cast<long long>(slot) * kBlk < p.pair_stride;
+            if (!ok)
+                report(p.status, SPARSE_ERR_BAD_INDEX);
+            lslot[i] = ok ? slot : -1;
+            llog[i] = ok ? logical : -1;
+        }
+        __syncthreads();
+    }
 
     if (VERIFY && rank == 0 && tid == 0 && p.blocks_loaded != nullptr && !aborted)
         atomicAdd(reinterpret_cast<unsigned long long *>(p.blocks_loaded),
@@ -283,14 +298,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     report(p.status, SPARSE_ERR_TIMEOUT);
                     break;
                 }
-                int slot;
-                if (VERIFY) {
-                    slot = ulist[i0 + it];
-                } else {
-                    slot = list_slot(p, pair, i0 + it);
-                    if (slot < 0)
-                        report(p.status, SPARSE_ERR_BAD_INDEX);
-                }
+                const int slot = VERIFY ? ulist[i0 + it] : lslot[it];
                 // an invalid slot loads an out-of-range box: zeros, never a fault
                 const int row = slot >= 0 ? slot * kBlk : static_cast<int>(min(p.pair_stride, (long long)INT_MAX - kBlk));
                 const uint32_t dst = base_s + s * kStageBytes;
@@ -307,6 +315,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int g8 = lane >> 2, t4 = lane & 3;
         const int jm = lane >> 3, rr = lane & 7;
 
+        if (early)
+            griddep_wait();   // Q may be written by the kernel before this one
         // Q^T fragments (B operand of S^T = K Q^T): row n = g8 of each n-tile
         uint32_t qb[NT][8][2];
         bool row_ok[NT][2];
@@ -354,15 +364,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int li = i0 + it;
             int logical;
             uint32_t qmask = 0xffffffffu;
-            bool ok;
             if (VERIFY) {
                 logical = ulist[li];
                 qmask = umask[li];
-                ok = true;
             } else {
-                logical = p.blk_logical[static_cast<size_t>(pair) * p.k_tot + li];
-                ok = logical >= 0 && list_slot(p, pair, li) >= 0;
+                logical = llog[it];
             }
+            const bool ok = logical >= 0;
             const long long tok0 = static_cast<long long>(logical) * kBlk + w * 16;
             if (ok && tok0 < len) {
                 const uint32_t kst = base_s + s * kStageBytes;
@@ -458,13 +466,22 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // ---------------------------------------------------------------- merge
     // Every stage has been consumed; the ring memory now holds the partial states.
+    // The next kernel on the stream may be scheduled from here on.
+    // (1) each consumer warp's state, (2) merged into this CTA's state in local shared
+    // memory, (3) after one cluster barrier, CTA r merges the S CTA states for its
+    // slice of output dims, reading its peers' shared memory with independent loads.
     __syncthreads();
-    float *part_o = reinterpret_cast<float *>(base);                 // [4][ROWS][128]
-    float *part_m = part_o + kConsumerWarps * ROWS * kD;             // [4][ROWS]
-    float *part_l = part_m + kConsumerWarps * ROWS;                  // [4][ROWS]
-    int *part_abort = reinterpret_cast<int *>(part_l + kConsumerWarps * ROWS);
-    float *fac = reinterpret_cast<float *>(part_abort + 4);          // [S][4][ROWS]
-    float *row_m = fac + kMaxSplit * kConsumerWarps * ROWS;
+    griddep_launch_dependents();
+    float *wo = reinterpret_cast<float *>(base);                     // [4][ROWS][128]
+    float *wm = wo + kConsumerWarps * ROWS * kD;                     // [4][ROWS]
+    float *wl = wm + kConsumerWarps * ROWS;                          // [4][ROWS]
+    float *wf = wl + kConsumerWarps * ROWS;                          // [4][ROWS] warp weights
+    float *co = wf + kConsumerWarps * ROWS;                          // [ROWS][128] CTA state
+    float *cm = co + ROWS * kD;                                      // [ROWS]
+    float *cl = cm + ROWS;                                           // [ROWS]
+    int *cabort = reinterpret_cast<int *>(cl + ROWS);                // [4]
+    float *fac = reinterpret_cast<float *>(cabort + 4);              // [kMaxSplit][ROWS]
+    float *row_m = fac + kMaxSplit * ROWS;
     float *row_l = row_m + ROWS;
     if (warp < kConsumerWarps) {
         const int g8 = lane >> 2, t4 = lane & 3;
@@ -476,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int i = 0; i < 4; ++i) {
                     const int dim = mt * 16 + g8 + (i >> 1) * 8;
                     const int row = nt * 8 + 2 * t4 + (i & 1);
-                    part_o[(warp * ROWS + row) * kD + dim] = acc[mt][nt][i];
+                    wo[(warp * ROWS + row) * kD + dim] = acc[mt][nt][i];
                 }
         if (g8 == 0) {
 #pragma unroll
@@ -484,40 +501,82 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int row = nt * 8 + 2 * t4 + h;
-                    part_m[warp * ROWS + row] = m_r[nt][h];
-                    part_l[warp * ROWS + row] = l_r[nt][h];
+                    wm[warp * ROWS + row] = m_r[nt][h];
+                    wl[warp * ROWS + row] = l_r[nt][h];
                 }
         }
     }
+    __syncthreads();
+    if (tid < ROWS) {
+        const int row = tid;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w4 = 0; w4 < kConsumerWarps; ++w4)
+            M = fmaxf(M, wm[w4 * ROWS + row]);
+        float L = 0.f;
+#pragma unroll
+        for (int w4 = 0; w4 < kConsumerWarps; ++w4) {
+            const float mw = wm[w4 * ROWS + row];
+            const float f = (M == -INFINITY || mw == -INFINITY) ? 0.f : exp2f(mw - M);
+            wf[w4 * ROWS + row] = f;
+            L += f * wl[w4 * ROWS + row];
+        }
+        cm[row] = M;
+        cl[row] = L;
+    }
     if (tid == 0)
-        part_abort[0] = aborted ? 1 : 0;
+        cabort[0] = aborted ? 1 : 0;
+    __syncthreads();
+    for (int item = tid; item < ROWS * kD; item += kThreads) {
+        const int row = item / kD;
+        float o = 0.f;
+#pragma unroll
+        for (int w4 = 0; w4 < kConsumerWarps; ++w4)
+            o = fmaf(wf[w4 * ROWS + row], wo[w4 * ROWS * kD + item], o);
+        co[item] = o;
+    }
     cluster_sync();
 
-    // any CTA of the unit that failed its ready check leaves the output untouched
+    // peers' CTA states (generic pointers into distributed shared memory)
+    const float *peer_co[kMaxSplit];
+    const float *peer_cm[kMaxSplit];
+    const float *peer_cl[kMaxSplit];
     int any_abort = 0;
-    for (uint32_t c = 0; c < S; ++c)
-        any_abort |= static_cast<int>(dsmem_ld_u32(dsmem_addr(smem_u32(part_abort), c)));
+#pragma unroll
+    for (int c = 0; c < kMaxSplit; ++c) {
+        const unsigned r = c < static_cast<int>(S) ? static_cast<unsigned>(c) : 0u;
+        peer_co[c] = static_cast<const float *>(__cluster_map_shared_rank(co, r));
+        peer_cm[c] = static_cast<const float *>(__cluster_map_shared_rank(cm, r));
+        peer_cl[c] = static_cast<const float *>(__cluster_map_shared_rank(cl, r));
+        const int ab = *static_cast<const int *>(__cluster_map_shared_rank(cabort, r));
+        any_abort |= c < static_cast<int>(S) ? ab : 0;
+    }
 
+    // any CTA of the unit that failed its ready check leaves the output untouched
     if (!any_abort) {
-        // per row: global max and normaliser, and each partial's weight 2^(m - M) / L
-        for (int row = tid; row < ROWS; row += kThreads) {
+        if (tid < ROWS) {
+            const int row = tid;
+            float mc[kMaxSplit], lc[kMaxSplit];
+#pragma unroll
+            for (int c = 0; c < kMaxSplit; ++c) {
+                mc[c] = c < static_cast<int>(S) ? peer_cm[c][row] : -INFINITY;
+                lc[c] = c < static_cast<int>(S) ? peer_cl[c][row] : 0.f;
+            }
             float M = -INFINITY;
-            for (uint32_t c = 0; c < S; ++c)
-                for (int w4 = 0; w4 < kConsumerWarps; ++w4)
-                    M = fmaxf(M, dsmem_ld_f32(dsmem_addr(smem_u32(&part_m[w4 * ROWS + row]), c)));
+#pragma unroll
+            for (int c = 0; c < kMaxSplit; ++c)
+                M = fmaxf(M, mc[c]);
             float L = 0.f;
-            for (uint32_t c = 0; c < S; ++c)
-                for (int w4 = 0; w4 < kConsumerWarps; ++w4) {
-                    const float mc = dsmem_ld_f32(dsmem_addr(smem_u32(&part_m[w4 * ROWS + row]), c));
-                    const float lc = dsmem_ld_f32(dsmem_addr(smem_u32(&part_l[w4 * ROWS + row]), c));
-                    const float f = (M == -INFINITY || mc == -INFINITY) ? 0.f : exp2f(mc - M);
-                    fac[(c * kConsumerWarps + w4) * ROWS + row] = f;
-                    L += lc * f;
-                }
+#pragma unroll
+            for (int c = 0; c < kMaxSplit; ++c) {
+                const float f = (M == -INFINITY || mc[c] == -INFINITY) ? 0.f : exp2f(mc[c] - M);
+                fac[c * ROWS + row] = f;
+                L += lc[c] * f;
+            }
             const float inv = L > 0.f ? 1.f / L : 0.f;
-            for (uint32_t c = 0; c < S; ++c)
-                for (int w4 = 0; w4 < kConsumerWarps; ++w4)
-                    fac[(c * kConsumerWarps + w4) * ROWS + row] *= inv;
+#pragma unroll
+            for (int c = 0; c < kMaxSplit; ++c)
+                fac[c * ROWS + row] *= inv;
             row_m[row] = M;
             row_l[row] = L;
         }
@@ -527,13 +586,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int item = tid; item < rows_valid * dims_per; item += kThreads) {
             const int row = item / dims_per;
             const int d = d0 + (item - row * dims_per);
+            float v[kMaxSplit];
+#pragma unroll
+            for (int c = 0; c < kMaxSplit; ++c)
+                v[c] = c < static_cast<int>(S) ? peer_co[c][row * kD + d] : 0.f;
             float o = 0.f;
-            for (uint32_t c = 0; c < S; ++c)
-                for (int w4 = 0; w4 < kConsumerWarps; ++w4) {
-                    const float f = fac[(c * kConsumerWarps + w4) * ROWS + row];
-                    if (f != 0.f)
-                        o = fmaf(f, dsmem_ld_f32(dsmem_addr(smem_u32(&part_o[(w4 * ROWS + row) * kD + d]), c)), o);
-                }
+#pragma unroll
+            for (int c = 0; c < kMaxSplit; ++c)
+                o = fmaf(fac[c * ROWS + row], v[c], o);
             size_t out;
             if (VERIFY) {
                 const int qq = q0 + row / p.G, hh = row % p.G;
@@ -552,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         }
     }
-    // peers may still read this CTA's partial states
+    // peers may still read this CTA's state
     cluster_sync();
 }
 
@@ -562,27 +622,24 @@ int launch(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, in
 {
     auto kern = sparse_attn_kernel<NT, VERIFY>;
     const int smem = (VERIFY ? kSmemVerify : kSmemDecode) + 1024;
-    static bool configured[64];
-    if (device >= 0 && device < 64 && !configured[device]) {
-        int rc = sp_host::cuda_status(
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
-            "sparse attention smem attribute");
-        if (rc != SPARSE_OK)
-            return rc;
-        configured[device] = true;
-    }
+    static int configured[64];
+    int rc = sp_host::configure_kernel(reinterpret_cast<const void *>(kern), smem, device, configured);
+    if (rc != SPARSE_OK)
+        return rc;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(S), static_cast<unsigned>(units), 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(S);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     CUtensorMap kmap = km, vmap = vm;
     AttnParams prm = p;
     void *args[] = {&kmap, &vmap, &prm};
@@ -590,9 +647,9 @@ int launch(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, in
                                 "sparse attention launch");
 }
 
-// The merge scratch (partials, weights) must fit in the ring it reuses.
-static_assert(kConsumerWarps * 16 * kD * 4 + 2 * kConsumerWarps * 16 * 4 + 16 +
-                      kMaxSplit * kConsumerWarps * 16 * 4 + 2 * 16 * 4 <=
+// The merge scratch (warp and CTA states, weights) must fit in the ring it reuses.
+static_assert((3 * kConsumerWarps * 16 + kConsumerWarps * 16 * kD + 16 * kD + 2 * 16 + 4 + kMaxSplit * 16 + 2 * 16) *
+                      4 <=
                   kStages * kStageBytes,
               "merge scratch exceeds the stage ring");
 
@@ -619,7 +676,7 @@ float scale_log2_of(float scale)
 
 int decode_impl(const uint16_t *Q, const uint16_t *k_base, const uint16_t *v_base, long long pair_stride,
                 const int *blk_slot, const int *blk_logical, const int *count, int k_tot, const int *seq_len,
-                int B, int H_q, int H_kv, float scale, uint16_t *O, float *lse, int n_split,
+                int B, int H_q, int H_kv, float scale, uint16_t *O, float *lse, int n_split, unsigned flags,
                 const unsigned *ready_flag, unsigned ready_target, long long timeout_ns, int *status,
                 void *stream)
 {
@@ -648,9 +705,16 @@ int decode_impl(const uint16_t *Q, const uint16_t *k_base, const uint16_t *v_bas
     int rc = sp_host::device_info(&dev);
     if (rc != SPARSE_OK)
         return rc;
+    if ((flags & ~SPARSE_ATTN_BLOCKS_READY) != 0u)
+        return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn: unknown flags 0x%x", flags);
     int S;
     if ((rc = choose_split(n_split, pairs, k_tot, dev.sm_count, &S)) != SPARSE_OK)
         return rc;
+    while ((k_tot + S - 1) / S > kMaxListCta && S < kMaxSplit && n_split == 0)
+        S *= 2;
+    if ((k_tot + S - 1) / S > kMaxListCta)
+        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn: k_tot=%d needs more than %d blocks per CTA", k_tot,
+                    kMaxListCta);
     CUtensorMap km, vm;
     if ((rc = sp_host::make_kv_tensor_map(&km, k_base, pair_stride, pairs)) != SPARSE_OK)
         return rc;
@@ -674,6 +738,7 @@ int decode_impl(const uint16_t *Q, const uint16_t *k_base, const uint16_t *v_bas
     p.H_kv = H_kv;
     p.G = G;
     p.n_groups = 1;
+    p.flags = flags;
     p.scale_log2 = scale_log2_of(scale);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return G <= 8 ? launch<1, false>(p, km, vm, S, pairs, dev.device, st)
@@ -686,24 +751,26 @@ extern "C" SPARSE_API int sparse_decode_attn(const uint16_t *Q, const uint16_t *
                                              long long pair_stride_tokens, const int *blk_slot,
                                              const int *blk_logical, const int *count, int k_tot,
                                              const int *seq_len, int B, int H_q, int H_kv, float scale,
-                                             uint16_t *O, float *lse, int n_split, int *status, void *stream)
+                                             uint16_t *O, float *lse, int n_split, unsigned flags, int *status,
+                                             void *stream)
 {
     return decode_impl(Q, k_base, v_base, pair_stride_tokens, blk_slot, blk_logical, count, k_tot, seq_len, B,
-                       H_q, H_kv, scale, O, lse, n_split, nullptr, 0u, 0, status, stream);
+                       H_q, H_kv, scale, O, lse, n_split, flags, nullptr, 0u, 0, status, stream);
 }
 
 extern "C" SPARSE_API int sparse_decode_attn_ex(const uint16_t *Q, const uint16_t *k_base,
                                                 const uint16_t *v_base, long long pair_stride_tokens,
                                                 const int *blk_slot, const int *blk_logical, const int *count,
                                                 int k_tot, const int *seq_len, int B, int H_q, int H_kv,
-                                                float scale, uint16_t *O, float *lse, int n_split,
+                                                float scale, uint16_t *O, float *lse, int n_split, unsigned flags,
                                                 const unsigned *ready_flag, unsigned ready_target,
                                                 long long timeout_ns, int *status, void *stream)
 {
     if (ready_flag == nullptr)
         return sp_host::fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn_ex: ready_flag is null");
     return decode_impl(Q, k_base, v_base, pair_stride_tokens, blk_slot, blk_logical, count, k_tot, seq_len, B,
-                       H_q, H_kv, scale, O, lse, n_split, ready_flag, ready_target, timeout_ns, status, stream);
+                       H_q, H_kv, scale, O, lse, n_split, flags, ready_flag, ready_target, timeout_ns, status,
+                       stream);
 }
 
 extern "C" SPARSE_API int sparse_verify_attn_grouped(const uint16_t *Q, const uint16_t *k_cache,
@@ -766,6 +833,7 @@ extern "C" SPARSE_API int sparse_verify_attn_grouped(const uint16_t *Q, const ui
     p.C = C;
     p.window_blocks = window_blocks;
     p.n_groups = n_groups;
+    p.flags = 0u;
     p.scale_log2 = scale_log2_of(scale);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return C * G <= 8 ? launch<1, true>(p, km, vm, S, units, dev.device, st)

@@ -122,20 +122,34 @@ SPARSE_API int sparse_select_topk(const uint16_t *F, const float *ktil, const in
  *   O            [B][H_q][128] bf16;  lse [B][H_q] fp32 natural-log LSE, or NULL.
  *   n_split      CTAs sharing one pair's list (1, 2, 4 or 8); 0 = chosen from the
  *                SM count.  The result does not depend on it beyond fp32 rounding.
- * A row with no valid token gets O = 0 and lse = -inf.  G = H_q / H_kv <= 16.
+ *   flags        0 or SPARSE_ATTN_BLOCKS_READY (below).
+ * A row with no valid token gets O = 0 and lse = -inf.  G = H_q / H_kv <= 16,
+ * k_tot <= 4096.
+ *
+ * Launch order.  The kernel is launched with programmatic stream serialization: it
+ * may be scheduled while the kernel before it on the stream is still running, and it
+ * waits for that kernel (griddepcontrol.wait) before reading any input -- unless the
+ * caller passes SPARSE_ATTN_BLOCKS_READY, which promises that the block table,
+ * count, seq_len and the K/V rows are complete before that preceding kernel finishes
+ * (produced earlier, or on another stream ordered by an event).  Then the kernel
+ * stages its block list and starts streaming K/V at once and waits only before
+ * reading Q and writing O and lse.  This is SparDA's decoupling (§4.1): the blocks of
+ * layer l+1 are chosen one layer ahead, so their loads need not wait for Q_{l+1}.
  */
+#define SPARSE_ATTN_BLOCKS_READY 1u
+
 SPARSE_API int sparse_decode_attn(const uint16_t *Q, const uint16_t *k_base,
                                   const uint16_t *v_base, long long pair_stride_tokens,
                                   const int *blk_slot, const int *blk_logical, const int *count,
                                   int k_tot, const int *seq_len, int B, int H_q, int H_kv,
                                   float scale, uint16_t *O, float *lse, int n_split,
-                                  int *status, void *stream);
+                                  unsigned flags, int *status, void *stream);
 
 /*
  * sparse_decode_attn_ex -- sparse_decode_attn that first checks a staging-ready word.
  * Before reading, every CTA polls *ready_flag (device memory, acquire) until it is
  * >= ready_target, for at most timeout_ns nanoseconds (0 = check once, capped at
- * 2 s).  If the word does not reach the target, the CTA reads nothing, leaves O and
+ * 2 s).  If the word does not reach the target, the CTA reads no K/V, leaves O and
  * lse untouched and reports SPARSE_ERR_TIMEOUT (timeout_ns > 0) or
  * SPARSE_ERR_NOT_READY (timeout_ns == 0) in *status.  Ordering the producer before
  * this call (same stream, or an event) is the caller's job; the word is an integrity
@@ -146,7 +160,7 @@ SPARSE_API int sparse_decode_attn_ex(const uint16_t *Q, const uint16_t *k_base,
                                      const int *blk_slot, const int *blk_logical,
                                      const int *count, int k_tot, const int *seq_len, int B,
                                      int H_q, int H_kv, float scale, uint16_t *O, float *lse,
-                                     int n_split, const unsigned *ready_flag,
+                                     int n_split, unsigned flags, const unsigned *ready_flag,
                                      unsigned ready_target, long long timeout_ns, int *status,
                                      void *stream);
 
