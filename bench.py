@@ -162,7 +162,7 @@ class ClockSampler:
 class Decode128k:
     """Device state of the 80-layer 128K decode step and its CUDA graph."""
 
-    def __init__(self, device):
+    def __init__(self, device, use_workspace=True):
         import torch
         from block_sparse_long_pool_gb300 import binding
         from block_sparse_long_pool_gb300 import workloads as wl
@@ -201,6 +201,7 @@ class Decode128k:
         self.seq = torch.full((B,), T, dtype=torch.int32, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.side = torch.cuda.Stream(device=device)
+        self.workspace = binding.decode_workspace(B, H_q, H_kv, self.k_cap, device=device) if use_workspace else None
         torch.cuda.synchronize(device)
 
     # bytes the method has to move per step
@@ -228,7 +229,8 @@ class Decode128k:
         q = l % self.sh.phys_layers
         self.binding.sparse_decode_attn(self.Q[l], self.k_cache[q], self.v_cache[q], self.idx[l], self.count[l],
                                         self.seq, self.O[l], status=self.status, n_split=n_split,
-                                        flags=self.binding.SPARSE_ATTN_BLOCKS_READY, stream=stream)
+                                        flags=self.binding.SPARSE_ATTN_BLOCKS_READY, workspace=self.workspace,
+                                        stream=stream)
 
     def enqueue_step(self, events=None, n_split=0):
         """Enqueue one step on the current stream (+ the side stream).  ``events``
@@ -284,7 +286,7 @@ def run_ours(args, rank, world, local_rank):
     import __graft_entry__
     __graft_entry__.build()
 
-    wk = Decode128k(dev)
+    wk = Decode128k(dev, use_workspace=not args.no_workspace)
     graph = wk.capture()
     K, W = args.steps, args.warmup
     for _ in range(W):
@@ -523,6 +525,7 @@ def run_layer_case(args, local_rank):
     O = torch.empty((B, H_q, D), dtype=torch.bfloat16, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(max(1, args.flush_mb) << 20, dtype=torch.uint8, device=dev)
+    ws = None if args.no_workspace else binding.decode_workspace(B, H_q, H_kv, k_cap, args.n_split, device=dev)
     sel_ms, att_ms = [], []
     for i in range(args.warmup + args.steps):
         F = wl.forecast(sh, 0, i, dev)
@@ -536,7 +539,8 @@ def run_layer_case(args, local_rank):
         e3 = torch.cuda.Event(enable_timing=True)
         e3.record()
         if not select_only:
-            binding.sparse_decode_attn(Q, kc, vc, idx, cnt, seq, O, status=status, n_split=args.n_split)
+            binding.sparse_decode_attn(Q, kc, vc, idx, cnt, seq, O, status=status, n_split=args.n_split,
+                                       workspace=ws)
         e[2].record()
         torch.cuda.synchronize(dev)
         if i >= args.warmup:
@@ -567,6 +571,7 @@ def main():
                     help="step: the 80-layer decode step (the bench line); layer: one physical layer, "
                          "kernels serialised and timed alone (for profiling); select: selection only")
     ap.add_argument("--n-split", type=int, default=0)
+    ap.add_argument("--no-workspace", action="store_true", help="attention without the stream-K workspace (cluster split-KV)")
     ap.add_argument("--tokens", type=int, default=0, help="layer case: cached tokens (default 131072)")
     ap.add_argument("--flush-mb", type=int, default=512, help="layer case: L2 flush buffer before each launch")
     args = ap.parse_args()

@@ -30,18 +30,22 @@ SPARSE_ERR_TIMEOUT = -4
 SPARSE_ERR_NOT_READY = -5
 SPARSE_ERR_BAD_INDEX = -6
 SPARSE_ATTN_BLOCKS_READY = 1
+SPARSE_ATTN_STREAM_K = 2
 
 # (name, restype, argtypes) of every entry point declared in include/sparse_pool.h
 _P, _I, _LL, _F, _U = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float, ctypes.c_uint
+_SZ = ctypes.c_size_t
 SIGNATURES = {
     "sparse_status_string": (ctypes.c_char_p, [_I]),
     "sparse_last_error": (ctypes.c_char_p, []),
     "sparse_version": (_I, []),
     "sparse_pool_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _LL, _I, _LL, _I, _P]),
     "sparse_select_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P]),
-    "sparse_decode_attn": (_I, [_P, _P, _P, _LL, _P, _P, _P, _I, _P, _I, _I, _I, _F, _P, _P, _I, _U, _P, _P]),
-    "sparse_decode_attn_ex": (_I, [_P, _P, _P, _LL, _P, _P, _P, _I, _P, _I, _I, _I, _F, _P, _P, _I, _U, _P, _U,
-                                   _LL, _P, _P]),
+    "sparse_decode_attn": (_I, [_P, _P, _P, _LL, _P, _P, _P, _I, _P, _I, _I, _I, _F, _P, _P, _I, _U, _P, _SZ,
+                                _P, _P]),
+    "sparse_decode_attn_ex": (_I, [_P, _P, _P, _LL, _P, _P, _P, _I, _P, _I, _I, _I, _F, _P, _P, _I, _U, _P, _SZ,
+                                   _P, _U, _LL, _P, _P]),
+    "sparse_decode_attn_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "sparse_verify_attn_grouped": (_I, [_P, _P, _P, _LL, _P, _I, _I, _I, _I, _P, _I, _I, _I, _F, _P, _P, _I,
                                         _P, _P]),
     "sparse_gather_offloaded": (_I, [_P, _P, _LL, _P, _P, _I, _I, _I, _P, _P, _P, _I, _P, _P]),
@@ -157,8 +161,27 @@ def _decode_args(Q, k_base, v_base, blk_logical, count, seq_len, O, lse, blk_slo
     return B, H_q, H_kv, k_tot, pair_stride
 
 
+def sparse_decode_attn_workspace_size(B: int, H_q: int, H_kv: int, k_tot: int, n_split: int = 0) -> int:
+    """Bytes of the stream-K workspace of sparse_decode_attn (0: not used for these sizes)."""
+    return int(load().sparse_decode_attn_workspace_size(B, H_q, H_kv, k_tot, n_split))
+
+
+def decode_workspace(B: int, H_q: int, H_kv: int, k_tot: int, n_split: int = 0, device="cuda"):
+    """A zeroed workspace tensor for sparse_decode_attn, or None when not needed."""
+    n = sparse_decode_attn_workspace_size(B, H_q, H_kv, k_tot, n_split)
+    return torch.zeros(n, dtype=torch.uint8, device=device) if n > 0 else None
+
+
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    _need(workspace, "workspace", torch.uint8)
+    return _ptr(workspace), workspace.numel()
+
+
 def sparse_decode_attn(Q, k_base, v_base, blk_logical, count, seq_len, O, lse=None, blk_slot=None,
-                       scale: float = 0.0, n_split: int = 0, flags: int = 0, status=None, stream=None):
+                       scale: float = 0.0, n_split: int = 0, flags: int = 0, workspace=None, status=None,
+                       stream=None):
     """O [B][H_q][128] = attention of Q over the listed blocks of k_base/v_base.
 
     k_base/v_base hold B*H_kv pair regions of pair_stride x 128 rows (a cache
@@ -167,23 +190,25 @@ def sparse_decode_attn(Q, k_base, v_base, blk_logical, count, seq_len, O, lse=No
     kernel on ``stream`` finishes, so K/V streaming may start while it drains."""
     B, H_q, H_kv, k_tot, pair_stride = _decode_args(Q, k_base, v_base, blk_logical, count, seq_len, O, lse,
                                                     blk_slot)
+    ws, ws_bytes = _ws(workspace)
     rc = load().sparse_decode_attn(_ptr(Q), _ptr(k_base), _ptr(v_base), pair_stride, _ptr(blk_slot),
                                    _ptr(blk_logical), _ptr(count), k_tot, _ptr(seq_len), B, H_q, H_kv,
-                                   float(scale), _ptr(O), _ptr(lse), n_split, int(flags), _ptr(status),
-                                   _stream(stream))
+                                   float(scale), _ptr(O), _ptr(lse), n_split, int(flags), ws, ws_bytes,
+                                   _ptr(status), _stream(stream))
     _check(rc, "sparse_decode_attn")
 
 
 def sparse_decode_attn_ex(Q, k_base, v_base, blk_logical, count, seq_len, O, ready_flag, ready_target: int,
                           timeout_ns: int, lse=None, blk_slot=None, scale: float = 0.0, n_split: int = 0,
-                          flags: int = 0, status=None, stream=None):
+                          flags: int = 0, workspace=None, status=None, stream=None):
     """sparse_decode_attn after a bounded check of a staging-ready word."""
     B, H_q, H_kv, k_tot, pair_stride = _decode_args(Q, k_base, v_base, blk_logical, count, seq_len, O, lse,
                                                     blk_slot)
     _need(ready_flag, "ready_flag", torch.int32)
     rc = load().sparse_decode_attn_ex(_ptr(Q), _ptr(k_base), _ptr(v_base), pair_stride, _ptr(blk_slot),
                                       _ptr(blk_logical), _ptr(count), k_tot, _ptr(seq_len), B, H_q, H_kv,
-                                      float(scale), _ptr(O), _ptr(lse), n_split, int(flags), _ptr(ready_flag),
+                                      float(scale), _ptr(O), _ptr(lse), n_split, int(flags), *_ws(workspace),
+                                      _ptr(ready_flag),
                                       int(ready_target), int(timeout_ns), _ptr(status), _stream(stream))
     _check(rc, "sparse_decode_attn_ex")
 

@@ -176,6 +176,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// ---------------------------------------------------------------- named barriers
+
+// Barrier `id` (1..15) among `count` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Order this thread's generic-proxy shared-memory accesses before later async-proxy
+// (TMA) accesses to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- clusters
 
 // All threads of every CTA of the cluster; the warp is converged first because the

@@ -28,7 +28,7 @@ using namespace sp;
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCluster = 8;
-constexpr int kUnroll = 8;
+constexpr int kUnroll = 16;
 
 struct SelectParams {
     const uint16_t *F;

@@ -120,9 +120,22 @@ SPARSE_API int sparse_select_topk(const uint16_t *F, const float *ktil, const in
  *   seq_len      [B] int32 (device).
  *   scale        0 selects 1/sqrt(128).
  *   O            [B][H_q][128] bf16;  lse [B][H_q] fp32 natural-log LSE, or NULL.
- *   n_split      CTAs sharing one pair's list (1, 2, 4 or 8); 0 = chosen from the
- *                SM count.  The result does not depend on it beyond fp32 rounding.
- *   flags        0 or SPARSE_ATTN_BLOCKS_READY (below).
+ *   n_split      without a workspace: CTAs sharing one pair's list (1, 2, 4 or 8);
+ *                with a workspace: the total CTA count.  0 = chosen from the SM count.
+ *                The result does not depend on it beyond fp32 rounding.
+ *   flags        SPARSE_ATTN_BLOCKS_READY and / or SPARSE_ATTN_STREAM_K (below), or 0.
+ *   workspace    NULL, or device memory of sparse_decode_attn_workspace_size() bytes
+ *                (workspace_bytes gives its size).  By default the CTAs of a pair form a
+ *                thread-block cluster and merge their partial softmax states through
+ *                distributed shared memory (no scratch).  With a workspace and G <= 8,
+ *                the stream-K path runs when SPARSE_ATTN_STREAM_K is set or when the
+ *                pairs are too few for clusters to cover the SMs (B*H_kv*4 < SMs): a
+ *                persistent grid of two CTAs per SM splits the flattened (pair, block)
+ *                list into equal ranges, and pairs split between CTAs are merged
+ *                through the workspace by the CTA finishing last.  The workspace must
+ *                be all zero before the first call that uses it; every call returns its
+ *                arrival counters to zero.  Calls that share a workspace must not run
+ *                at the same time.
  * A row with no valid token gets O = 0 and lse = -inf.  G = H_q / H_kv <= 16,
  * k_tot <= 4096.
  *
@@ -137,20 +150,31 @@ SPARSE_API int sparse_select_topk(const uint16_t *F, const float *ktil, const in
  * layer l+1 are chosen one layer ahead, so their loads need not wait for Q_{l+1}.
  */
 #define SPARSE_ATTN_BLOCKS_READY 1u
+/* Use the stream-K path whenever a workspace is given (see `workspace`). */
+#define SPARSE_ATTN_STREAM_K 2u
 
 SPARSE_API int sparse_decode_attn(const uint16_t *Q, const uint16_t *k_base,
                                   const uint16_t *v_base, long long pair_stride_tokens,
                                   const int *blk_slot, const int *blk_logical, const int *count,
                                   int k_tot, const int *seq_len, int B, int H_q, int H_kv,
                                   float scale, uint16_t *O, float *lse, int n_split,
-                                  unsigned flags, int *status, void *stream);
+                                  unsigned flags, void *workspace, size_t workspace_bytes,
+                                  int *status, void *stream);
+
+/*
+ * Bytes of the sparse_decode_attn workspace for these sizes on the current device
+ * (n_split as for sparse_decode_attn), or 0 when the sizes are invalid or G > 8 (the
+ * workspace-free path serves G > 8).  The SparDA notes have no counterpart: this is
+ * the size of the stream-K partial states and per-pair arrival counters.
+ */
+SPARSE_API size_t sparse_decode_attn_workspace_size(int B, int H_q, int H_kv, int k_tot, int n_split);
 
 /*
  * sparse_decode_attn_ex -- sparse_decode_attn that first checks a staging-ready word.
  * Before reading, every CTA polls *ready_flag (device memory, acquire) until it is
  * >= ready_target, for at most timeout_ns nanoseconds (0 = check once, capped at
- * 2 s).  If the word does not reach the target, the CTA reads no K/V, leaves O and
- * lse untouched and reports SPARSE_ERR_TIMEOUT (timeout_ns > 0) or
+ * 2 s).  If the word does not reach the target, the call reads no K/V, leaves the
+ * O and lse rows it could not complete untouched and reports SPARSE_ERR_TIMEOUT (timeout_ns > 0) or
  * SPARSE_ERR_NOT_READY (timeout_ns == 0) in *status.  Ordering the producer before
  * this call (same stream, or an event) is the caller's job; the word is an integrity
  * check, not a substitute for stream order.
@@ -160,7 +184,8 @@ SPARSE_API int sparse_decode_attn_ex(const uint16_t *Q, const uint16_t *k_base,
                                      const int *blk_slot, const int *blk_logical,
                                      const int *count, int k_tot, const int *seq_len, int B,
                                      int H_q, int H_kv, float scale, uint16_t *O, float *lse,
-                                     int n_split, unsigned flags, const unsigned *ready_flag,
+                                     int n_split, unsigned flags, void *workspace,
+                                     size_t workspace_bytes, const unsigned *ready_flag,
                                      unsigned ready_target, long long timeout_ns, int *status,
                                      void *stream);
 

@@ -78,6 +78,7 @@ class GpuLayer:
         self.O = torch.zeros((B, H_q, D), dtype=torch.bfloat16, device=dev)
         self.lse = torch.zeros((B, H_q), dtype=torch.float32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.workspace = binding.decode_workspace(B, H_q, H_kv, self.k_cap)
 
     def append(self, k_new, v_new, len_before):
         binding.sparse_pool_append(self.k_cache, self.v_cache, self.ktil, k_new.contiguous(), v_new.contiguous(),
@@ -90,7 +91,7 @@ class GpuLayer:
     def attend(self, Q, seq_len, n_split=0, idx=None, count=None):
         binding.sparse_decode_attn(Q, self.k_cache, self.v_cache, self.idx if idx is None else idx,
                                    self.count if count is None else count, seq_len, self.O, self.lse,
-                                   n_split=n_split, status=self.status)
+                                   n_split=n_split, workspace=self.workspace, status=self.status)
 
 
 def oracle_layer(K_bits, V_bits, Q_bits, F_bits, lens_pair, N_cap, n_init, n_local, k, G):

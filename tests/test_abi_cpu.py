@@ -76,7 +76,7 @@ def test_select_rejects_bad_arguments(lib):
 
 def test_decode_rejects_bad_arguments(lib):
     f = lib.sparse_decode_attn
-    args = [FAKE, FAKE, FAKE, 4096, None, FAKE, FAKE, 11, FAKE, 1, 8, 2, 0.0, FAKE, None, 0, 0, None, None]
+    args = [FAKE, FAKE, FAKE, 4096, None, FAKE, FAKE, 11, FAKE, 1, 8, 2, 0.0, FAKE, None, 0, 0, None, 0, None, None]
     bad = list(args)
     bad[10] = 7                                   # H_q not a multiple of H_kv
     assert f(*bad) == binding.SPARSE_ERR_INVALID_ARG
@@ -90,7 +90,7 @@ def test_decode_rejects_bad_arguments(lib):
     bad[12] = float("nan")
     assert f(*bad) == binding.SPARSE_ERR_INVALID_ARG
     ex = lib.sparse_decode_attn_ex
-    assert ex(*args[:17], None, 1, 0, None, None) == binding.SPARSE_ERR_INVALID_ARG
+    assert ex(*args[:19], None, 1, 0, None, None) == binding.SPARSE_ERR_INVALID_ARG
 
 
 def test_verify_rejects_bad_arguments(lib):

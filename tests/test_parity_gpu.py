@@ -130,8 +130,10 @@ def test_select_few_blocks_takes_all(lens_b):
 # ----------------------------------------------------------------------------- decode attention
 
 
-def _decode_direct(B, H_q, H_kv, T_cap, lens_b, k_cap, seed, n_split=0, idx_np=None, cnt_np=None):
-    """sparse_decode_attn on given (or random distinct) block lists vs oracle.attn."""
+def _decode_direct(B, H_q, H_kv, T_cap, lens_b, k_cap, seed, n_split=0, idx_np=None, cnt_np=None,
+                   workspace=False):
+    """sparse_decode_attn on given (or random distinct) block lists vs oracle.attn.
+    With ``workspace`` the stream-K path runs and its counters must end at zero."""
     G = H_q // H_kv
     P = B * H_kv
     rng = np.random.default_rng(seed)
@@ -150,19 +152,25 @@ def _decode_direct(B, H_q, H_kv, T_cap, lens_b, k_cap, seed, n_split=0, idx_np=N
     O = torch.zeros((B, H_q, D), dtype=torch.bfloat16, device="cuda")
     lse = torch.zeros((B, H_q), dtype=torch.float32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = binding.decode_workspace(B, H_q, H_kv, k_cap, n_split) if workspace else None
     binding.sparse_decode_attn(Q, K, V, torch.from_numpy(idx_np).cuda().view(B, H_kv, k_cap),
                                torch.from_numpy(cnt_np).cuda().view(B, H_kv), _seq(lens_b), O, lse,
-                               n_split=n_split, status=status)
+                               n_split=n_split, workspace=ws, status=status,
+                               flags=binding.SPARSE_ATTN_STREAM_K if workspace else 0)
     torch.cuda.synchronize()
     assert status.item() == 0
+    if ws is not None:
+        assert not ws[:4 * P].any(), "arrival counters not back to zero"
     Oref, lref = oracle.attn(bits(Q).reshape(P, G, D), bits(K).reshape(P, T_cap, D), bits(V).reshape(P, T_cap, D),
                              idx_np, cnt_np, lens_p)
     return O, lse, Oref, lref
 
 
+@pytest.mark.parametrize("workspace", [False, True])
 @pytest.mark.parametrize("H_q,H_kv", [(8, 2), (64, 8), (16, 16), (32, 2), (24, 4)])
-def test_decode_attn_matches_oracle_group_sizes(H_q, H_kv):
-    O, lse, Oref, lref = _decode_direct(2, H_q, H_kv, 40 * BLK, [40 * BLK, 25 * BLK + 11], 19, seed=H_q * 7 + H_kv)
+def test_decode_attn_matches_oracle_group_sizes(H_q, H_kv, workspace):
+    O, lse, Oref, lref = _decode_direct(2, H_q, H_kv, 40 * BLK, [40 * BLK, 25 * BLK + 11], 19, seed=H_q * 7 + H_kv,
+                                        workspace=workspace)
     assert_attn_close(O, Oref.reshape(2, H_q, D))
     _check_lse(lse, lref.reshape(2, H_q))
 
@@ -177,6 +185,37 @@ def test_decode_attn_split_invariance():
     for n_split in (2, 4, 8):
         diff = (outs[n_split].float() - outs[1].float()).abs().max().item()
         assert diff <= 2 ** -7, f"split {n_split} changes the output by {diff}"
+
+
+@pytest.mark.parametrize("n_ctas", [1, 2, 3, 7, 13, 64, 0])
+def test_decode_attn_stream_k_partitions(n_ctas):
+    """Equal ranges of the flattened (pair, block) list: pairs split across 1..many
+    CTAs, ragged and empty pairs, every CTA count gives the oracle's result."""
+    B, H_q, H_kv, T_cap, k_cap = 3, 24, 3, 48 * BLK, 21
+    P = B * H_kv
+    lens_b = [48 * BLK, 30 * BLK + 5, 7 * BLK]
+    lens_p = _lens_pair(lens_b, H_kv)
+    rng = np.random.default_rng(11)
+    idx_np = np.full((P, k_cap), -1, np.int32)
+    cnt_np = np.zeros(P, np.int32)
+    for p in range(P):
+        nb = (int(lens_p[p]) + BLK - 1) // BLK
+        c = [k_cap, 5, 0, min(nb, k_cap)][p % 4]
+        c = min(c, nb)
+        idx_np[p, :c] = rng.permutation(nb)[:c]
+        cnt_np[p] = c
+    O, lse, Oref, lref = _decode_direct(B, H_q, H_kv, T_cap, lens_b, k_cap, 7, n_split=n_ctas, idx_np=idx_np,
+                                        cnt_np=cnt_np, workspace=True)
+    assert_attn_close(O, Oref.reshape(B, H_q, D), f"n_ctas={n_ctas}")
+    _check_lse(lse, lref.reshape(B, H_q))
+
+
+def test_decode_attn_stream_k_matches_cluster_path():
+    a = _decode_direct(2, 64, 8, 80 * BLK, [80 * BLK, 79 * BLK + 1], 67, seed=5)[0]
+    b = _decode_direct(2, 64, 8, 80 * BLK, [80 * BLK, 79 * BLK + 1], 67, seed=5, workspace=True)[0]
+    c = _decode_direct(2, 64, 8, 80 * BLK, [80 * BLK, 79 * BLK + 1], 67, seed=5, workspace=True)[0]
+    assert (a.float() - b.float()).abs().max().item() <= 2 ** -7
+    assert torch.equal(b, c)   # deterministic
 
 
 def test_decode_attn_empty_and_tiny_sets():
@@ -235,6 +274,14 @@ def test_decode_attn_ex_ready_word():
     torch.cuda.synchronize()
     assert status.item() == binding.SPARSE_ERR_TIMEOUT
     assert torch.equal(O, sentinel)
+    # the same through the stream-K path (pairs split across CTAs): untouched, counters zero
+    ws = binding.decode_workspace(B, H_q, H_kv, k_cap, 4)
+    status.zero_()
+    binding.sparse_decode_attn_ex(Q, K, K, idx, cnt, _seq([T_cap]), O, flag, 1, 20_000_000, n_split=4,
+                                  workspace=ws, flags=binding.SPARSE_ATTN_STREAM_K, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == binding.SPARSE_ERR_TIMEOUT
+    assert torch.equal(O, sentinel) and not ws[:8].any()
     status.zero_()
     binding.sparse_decode_attn_ex(Q, K, K, idx, cnt, _seq([T_cap]), O, flag, 1, 0, status=status)
     torch.cuda.synchronize()
