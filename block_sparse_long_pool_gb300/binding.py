@@ -46,6 +46,8 @@ SIGNATURES = {
     "sparse_decode_attn_ex": (_I, [_P, _P, _P, _LL, _P, _P, _P, _I, _P, _I, _I, _I, _F, _P, _P, _I, _U, _P, _SZ,
                                    _P, _U, _LL, _P, _P]),
     "sparse_decode_attn_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "sparse_decode_attn_noalloc": (_I, [_P, _P, _P, _LL, _P, _P, _P, _I, _P, _I, _I, _I, _F, _P, _P, _I, _U, _P,
+                                        _P]),
     "sparse_verify_attn_grouped": (_I, [_P, _P, _P, _LL, _P, _I, _I, _I, _I, _P, _I, _I, _I, _F, _P, _P, _I,
                                         _P, _P]),
     "sparse_gather_offloaded": (_I, [_P, _P, _LL, _P, _P, _I, _I, _I, _P, _P, _P, _I, _P, _P]),
@@ -196,6 +198,21 @@ def sparse_decode_attn(Q, k_base, v_base, blk_logical, count, seq_len, O, lse=No
                                    float(scale), _ptr(O), _ptr(lse), n_split, int(flags), ws, ws_bytes,
                                    _ptr(status), _stream(stream))
     _check(rc, "sparse_decode_attn")
+
+
+def sparse_decode_attn_noalloc(Q, k_base, v_base, blk_logical, count, seq_len, O, lse=None, blk_slot=None,
+                               scale: float = 0.0, n_split: int = 0, flags: int = 0, status=None, stream=None):
+    """sparse_decode_attn without a workspace argument and without allocating: for
+    callers that cannot allocate device memory (a host without a caching allocator, an
+    engine whose device memory is planned up front).  The library's fixed 4 MiB device
+    array serves as scratch; calls sharing it must not overlap on the GPU."""
+    B, H_q, H_kv, k_tot, pair_stride = _decode_args(Q, k_base, v_base, blk_logical, count, seq_len, O, lse,
+                                                    blk_slot)
+    rc = load().sparse_decode_attn_noalloc(_ptr(Q), _ptr(k_base), _ptr(v_base), pair_stride, _ptr(blk_slot),
+                                           _ptr(blk_logical), _ptr(count), k_tot, _ptr(seq_len), B, H_q, H_kv,
+                                           float(scale), _ptr(O), _ptr(lse), n_split, int(flags), _ptr(status),
+                                           _stream(stream))
+    _check(rc, "sparse_decode_attn_noalloc")
 
 
 def sparse_decode_attn_ex(Q, k_base, v_base, blk_logical, count, seq_len, O, ready_flag, ready_target: int,

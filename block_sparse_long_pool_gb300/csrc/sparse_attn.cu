@@ -38,6 +38,8 @@
 #include <limits.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace {
@@ -1302,6 +1304,78 @@ extern "C" SPARSE_API int sparse_decode_attn_ex(const uint16_t *Q, const uint16_
     return decode_impl(Q, k_base, v_base, pair_stride_tokens, blk_slot, blk_logical, count, k_tot, seq_len, B,
                        H_q, H_kv, scale, O, lse, n_split, flags, workspace, workspace_bytes, ready_flag,
                        ready_target, timeout_ns, status, stream);
+}
+
+// ---------------------------------------------------------------- allocation-free decode
+
+// Scratch of sparse_decode_attn_noalloc: a fixed array in device memory, so the call
+// allocates nothing.  Every GPU that loads the library holds these 4 MiB until the
+// process exits.  All calls share it; it keeps the last call's contents.
+constexpr size_t kNoallocScratchBytes = static_cast<size_t>(4) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[64];   // device address of the array, per device
+
+// The device address of g_noalloc_scratch on the current device (the host-side name of
+// the array is only a stand-in, never a device address).  Looked up once per device.
+int noalloc_scratch(int device, void **ptr)
+{
+    if (device < 0 || device >= 64)
+        return sp_host::fail(SPARSE_ERR_UNSUPPORTED, "device ordinal %d out of range", device);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[device] == nullptr) {
+        void *addr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+        if (e != cudaSuccess || addr == nullptr)
+            return sp_host::cuda_status(e != cudaSuccess ? e : cudaErrorInvalidSymbol,
+                                        "sparse_decode_attn_noalloc: cudaGetSymbolAddress");
+        g_noalloc_ptr[device] = addr;
+    }
+    *ptr = g_noalloc_ptr[device];
+    return SPARSE_OK;
+}
+
+}  // namespace
+
+extern "C" SPARSE_API int sparse_decode_attn_noalloc(const uint16_t *Q, const uint16_t *k_base,
+                                                     const uint16_t *v_base, long long pair_stride_tokens,
+                                                     const int *blk_slot, const int *blk_logical, const int *count,
+                                                     int k_tot, const int *seq_len, int B, int H_q, int H_kv,
+                                                     float scale, uint16_t *O, float *lse, int n_split,
+                                                     unsigned flags, int *status, void *stream)
+{
+    using sp_host::fail;
+    if (B < 1 || H_kv < 1 || H_q < H_kv || H_q % H_kv != 0 || k_tot < 1 || n_split < 0)
+        return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn_noalloc: bad size");
+    if (H_q / H_kv > 8)
+        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn_noalloc: G=%d > 8", H_q / H_kv);
+    sp_host::DeviceInfo dev;
+    int rc = sp_host::device_info(&dev);
+    if (rc != SPARSE_OK)
+        return rc;
+    const long long pairs = static_cast<long long>(B) * H_kv;
+    const int n_ctas = streamk_ctas(pairs * k_tot, pairs, n_split, dev.sm_count);
+    const size_t need = streamk_workspace_bytes(pairs, H_q / H_kv, n_ctas);
+    if (need > kNoallocScratchBytes)
+        return fail(SPARSE_ERR_UNSUPPORTED,
+                    "sparse_decode_attn_noalloc: these sizes need %zu bytes of scratch, more than the fixed %zu "
+                    "(use sparse_decode_attn with a workspace)",
+                    need, kNoallocScratchBytes);
+    void *scratch = nullptr;
+    if ((rc = noalloc_scratch(dev.device, &scratch)) != SPARSE_OK)
+        return rc;
+    // the per-pair arrival counters must start at zero: clear them on the call's stream
+    const size_t counters = (static_cast<size_t>(pairs) * sizeof(int) + 255) & ~static_cast<size_t>(255);
+    rc = sp_host::cuda_status(cudaMemsetAsync(scratch, 0, counters, static_cast<cudaStream_t>(stream)),
+                              "sparse_decode_attn_noalloc: clearing the counters");
+    if (rc != SPARSE_OK)
+        return rc;
+    return sparse_decode_attn(Q, k_base, v_base, pair_stride_tokens, blk_slot, blk_logical, count, k_tot, seq_len,
+                              B, H_q, H_kv, scale, O, lse, n_split, flags | SPARSE_ATTN_STREAM_K, scratch,
+                              kNoallocScratchBytes, status, stream);
 }
 
 extern "C" SPARSE_API size_t sparse_decode_attn_workspace_size(int B, int H_q, int H_kv, int k_tot, int n_split)

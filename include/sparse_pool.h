@@ -170,6 +170,33 @@ SPARSE_API int sparse_decode_attn(const uint16_t *Q, const uint16_t *k_base,
 SPARSE_API size_t sparse_decode_attn_workspace_size(int B, int H_q, int H_kv, int k_tot, int n_split);
 
 /*
+ * sparse_decode_attn_noalloc -- sparse_decode_attn for callers that cannot allocate
+ * device memory.  The SparDA and SSV notes have no counterpart to this call.
+ * Some callers have no device allocator to hand or may not use one here: a plain C
+ * host without a caching allocator (a cudaMalloc per call would synchronise the
+ * device), a serving engine whose device memory is planned up front and forbids
+ * ad-hoc allocation, or a runtime that hands this library only the tensors of the
+ * layer.  This call takes the same arguments as sparse_decode_attn without the
+ * workspace and runs the stream-K path (G <= 8) on scratch held in a fixed 4 MiB
+ * array of device memory inside the library; every GPU that loads the library keeps
+ * that array until the process exits.  Sizes whose scratch would exceed 4 MiB are
+ * rejected with SPARSE_ERR_UNSUPPORTED before any launch (B*H_kv = 64 pairs at
+ * k_tot = 67 need about 2.6 MB).  The call allocates nothing: no cudaMalloc or
+ * cudaFree, no allocating library routine.
+ * The first call on a device looks up the array's device address (once per device,
+ * with that device current); make that first call before any stream capture.  Each
+ * call first clears the array's per-pair counters on its stream.  All calls share the
+ * one array, so calls that overlap on the GPU (other streams, other threads) race:
+ * order them on one stream.
+ */
+SPARSE_API int sparse_decode_attn_noalloc(const uint16_t *Q, const uint16_t *k_base,
+                                          const uint16_t *v_base, long long pair_stride_tokens,
+                                          const int *blk_slot, const int *blk_logical,
+                                          const int *count, int k_tot, const int *seq_len, int B,
+                                          int H_q, int H_kv, float scale, uint16_t *O, float *lse,
+                                          int n_split, unsigned flags, int *status, void *stream);
+
+/*
  * sparse_decode_attn_ex -- sparse_decode_attn that first checks a staging-ready word.
  * Before reading, every CTA polls *ready_flag (device memory, acquire) until it is
  * >= ready_target, for at most timeout_ns nanoseconds (0 = check once, capped at
