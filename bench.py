@@ -594,6 +594,309 @@ def run_layer_case(args, local_rank):
           flush=True)
 
 
+# ----------------------------------------------------------------------------- the other workloads
+# One JSON line each (not the bench line): the 4K single layer, the 32K append step,
+# grouped verification at 64K and the offloaded 128K decode.  Every timed iteration
+# follows a 512 MB read that evicts L2 (these working sets fit in L2).
+
+
+def _event_times(fn, steps, warmup, evict=None):
+    """Per-iteration device time of fn() (CUDA events on the current stream), µs."""
+    import torch
+    pairs = []
+    for i in range(warmup + steps):
+        if evict is not None:
+            l2_evict(evict)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        if i >= warmup:
+            pairs.append((a, b))
+    torch.cuda.synchronize()
+    us = sorted(a.elapsed_time(b) * 1e3 for a, b in pairs)
+    q = lambda f: us[min(len(us) - 1, int(f * len(us)))]
+    return {"median_us": round(statistics.median(us), 2), "p10_us": round(q(0.1), 2),
+            "p90_us": round(q(0.9), 2), "iterations": len(us)}
+
+
+def _rate(nbytes, t_us, peak):
+    gbs = nbytes / (t_us * 1e-6) / 1e9
+    return round(gbs, 1), round(gbs / peak, 4)
+
+
+class _Layer:
+    """One decode layer on the device: cache, compressed keys, block lists, output."""
+
+    def __init__(self, sh, dev):
+        import torch
+        from block_sparse_long_pool_gb300 import binding
+        from block_sparse_long_pool_gb300 import workloads as wl
+        self.sh, self.binding = sh, binding
+        x = wl.single_layer(sh, dev)
+        B, H_kv, H_q = sh.B, sh.H_kv, sh.H_q
+        self.k_cache = torch.zeros_like(x["K"])
+        self.v_cache = torch.zeros_like(x["V"])
+        self.ktil = torch.zeros((B, H_kv, sh.N_b, D), dtype=torch.float32, device=dev)
+        # bulk append of the cached tokens builds the compressed keys
+        binding.sparse_pool_append(self.k_cache, self.v_cache, self.ktil, x["K"][:, :, :sh.T].contiguous(),
+                                   x["V"][:, :, :sh.T].contiguous(), 0)
+        self.F, self.Q = x["F"], x["Q"]
+        self.k_new, self.v_new = x.get("k_new"), x.get("v_new")
+        self.len_after = sh.len_after
+        self.seq = torch.full((B,), sh.len_after, dtype=torch.int32, device=dev)
+        self.idx = torch.empty((B, H_kv, sh.k_tot), dtype=torch.int32, device=dev)
+        self.cnt = torch.empty((B, H_kv), dtype=torch.int32, device=dev)
+        self.O = torch.empty((B, H_q, D), dtype=torch.bfloat16, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.ws = binding.decode_workspace(B, H_q, H_kv, sh.k_tot, device=dev)
+
+    def step(self):
+        sh, bd = self.sh, self.binding
+        if sh.n_new > 0:
+            # the same token written at the same position every step: the step is idempotent
+            bd.sparse_pool_append(self.k_cache, self.v_cache, self.ktil, self.k_new, self.v_new, sh.T)
+        bd.sparse_select_topk(self.F, self.ktil, self.seq, sh.n_init, sh.n_local, sh.k, self.idx, self.cnt,
+                              status=self.status)
+        bd.sparse_decode_attn(self.Q, self.k_cache, self.v_cache, self.idx, self.cnt, self.seq, self.O,
+                              workspace=self.ws, status=self.status)
+
+
+def run_single_layer_case(args, dev, sh, name):
+    import torch
+    peak, src = measured_peaks()
+    lay = _Layer(sh, dev)
+    evict = torch.ones(512 << 20 >> 2, dtype=torch.int32, device=dev)
+    t = _event_times(lay.step, args.steps, args.warmup, evict)
+    torch.cuda.synchronize()
+    assert lay.status.item() == 0, f"device status {lay.status.item()}"
+    kv = sh.pairs * sh.k_tot * KV_BLOCK_BYTES
+    sel = sh.pairs * sh.N_b * KTIL_ROW_BYTES
+    # append: new K/V rows read and written, the touched compressed key read and written
+    app = sh.pairs * (sh.n_new * 2 * 2 * D * 2 + 2 * KTIL_ROW_BYTES) if sh.n_new else 0
+    gbs, frac = _rate(kv + sel + app, t["median_us"], peak)
+    launches = 3 if sh.n_new else 2
+    line = {"case": name, "workload": sh.name, "unit_of_work": "one decode step (" +
+            ("append + " if sh.n_new else "") + "select + attention)",
+            "steps_per_s": round(1e6 / t["median_us"], 1), **t, "launches_per_step": launches,
+            "algorithmic_bytes": {"selected_kv": kv, "compressed_keys": sel, "append": app},
+            "achieved_gbs": gbs, "frac_of_measured_hbm": frac, "peak_gbs": peak, "peak_source": src,
+            "l2": "512 MB read evicts L2 before each step"}
+    print(json.dumps(line), flush=True)
+
+
+def run_verify_case(args, dev):
+    import torch
+    from block_sparse_long_pool_gb300 import binding
+    from block_sparse_long_pool_gb300 import workloads as wl
+    sh = wl.VERIFY_64K
+    peak, src = measured_peaks()
+    x = wl.verify_inputs(sh, dev)
+    O = torch.empty_like(x["Q"])
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    evict = torch.ones(512 << 20 >> 2, dtype=torch.int32, device=dev)
+    out = {"case": "verify64k", "workload": sh.name, "unit_of_work": "one verification round "
+           f"({sh.N_q} queries x {sh.B * sh.H_kv} pairs)", "peak_gbs": peak, "peak_source": src,
+           "l2": "512 MB read evicts L2 before each round"}
+    for C, key in ((sh.C, "grouped"), (1, "ungrouped")):
+        loaded = torch.zeros(1, dtype=torch.int64, device=dev)
+
+        def run():
+            binding.sparse_verify_attn_grouped(x["Q"], x["K"], x["V"], x["I"], C, sh.window_blocks, x["seq_len"], O,
+                                               status=status)
+        binding.sparse_verify_attn_grouped(x["Q"], x["K"], x["V"], x["I"], C, sh.window_blocks, x["seq_len"], O,
+                                           blocks_loaded=loaded, status=status)
+        t = _event_times(run, args.steps, args.warmup, evict)
+        nbytes = int(loaded.item()) * KV_BLOCK_BYTES
+        gbs, frac = _rate(nbytes, t["median_us"], peak)
+        out[key] = {"C": C, "blocks_loaded": int(loaded.item()), "bytes_loaded": nbytes, **t,
+                    "achieved_gbs": gbs, "frac_of_measured_hbm": frac}
+    assert status.item() == 0, f"device status {status.item()}"
+    g, u = out["grouped"], out["ungrouped"]
+    out["bytes_ratio"] = round(g["bytes_loaded"] / u["bytes_loaded"], 4)
+    out["bytes_ratio_bound"] = round((1 + (sh.C - 1) * (1 - sh.gamma)) / sh.C, 4)
+    out["time_ratio"] = round(g["median_us"] / u["median_us"], 4)
+    print(json.dumps(out), flush=True)
+
+
+class Offload128k:
+    """The offloaded 128K decode: K/V of every layer in pinned host memory, compressed
+    keys resident, selected blocks gathered one layer ahead into a two-slot HBM ring."""
+
+    def __init__(self, dev):
+        import torch
+        from block_sparse_long_pool_gb300 import binding
+        from block_sparse_long_pool_gb300 import workloads as wl
+        self.torch, self.binding, self.dev = torch, binding, dev
+        sh = self.sh = wl.OFFLOAD_128K
+        B, H_kv, H_q, T, L = sh.B, sh.H_kv, sh.H_q, sh.T, sh.layers
+        planted = wl.planted_sets(sh, L)
+        self.k_host, self.v_host, self.ktil = [], [], []
+        kc = torch.empty((B, H_kv, T, D), dtype=torch.bfloat16, device=dev)
+        vc = torch.empty_like(kc)
+        for l in range(L):
+            kn = torch.empty_like(kc)
+            vn = torch.empty_like(kc)
+            for p in range(sh.pairs):
+                b, h = divmod(p, H_kv)
+                kn[b, h], vn[b, h] = wl.kv_pair(sh, l, p, planted[l, p], dev)
+            kt = torch.zeros((B, H_kv, sh.N_b, D), dtype=torch.float32, device=dev)
+            binding.sparse_pool_append(kc, vc, kt, kn, vn, 0)
+            del kn, vn
+            kh = torch.empty(kc.shape, dtype=torch.bfloat16, pin_memory=True)
+            vh = torch.empty(kc.shape, dtype=torch.bfloat16, pin_memory=True)
+            kh.copy_(kc)
+            vh.copy_(vc)
+            self.k_host.append(kh)
+            self.v_host.append(vh)
+            self.ktil.append(kt)
+        del kc, vc
+        self.Q = torch.stack([wl.queries(sh, l, dev) for l in range(L)])
+        self.F = torch.stack([wl.forecast(sh, (l + 1) % L, l, dev) for l in range(L)])
+        self.F0 = wl.forecast(sh, 0, -1, dev)
+        kt_ = sh.k_tot
+        self.k_ring = torch.zeros((2, B, H_kv, kt_, BLK, D), dtype=torch.bfloat16, device=dev)
+        self.v_ring = torch.zeros_like(self.k_ring)
+        self.slots = torch.arange(kt_, dtype=torch.int32, device=dev).repeat(B, H_kv, 1).contiguous()
+        self.idx = torch.full((L, B, H_kv, kt_), -1, dtype=torch.int32, device=dev)
+        self.count = torch.zeros((L, B, H_kv), dtype=torch.int32, device=dev)
+        self.O = torch.zeros((L, B, H_q, D), dtype=torch.bfloat16, device=dev)
+        self.seq = torch.full((B,), T, dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.side = torch.cuda.Stream(device=dev)
+        self.copy = torch.cuda.Stream(device=dev)
+        self.ws = binding.decode_workspace(B, H_q, H_kv, kt_, device=dev)
+        torch.cuda.synchronize(dev)
+
+    def link_bytes_per_layer(self):
+        return self.sh.pairs * self.sh.k_tot * KV_BLOCK_BYTES
+
+    def _select(self, l, F, stream):
+        sh = self.sh
+        self.binding.sparse_select_topk(F, self.ktil[l], self.seq, sh.n_init, sh.n_local, sh.k, self.idx[l],
+                                        self.count[l], status=self.status, stream=stream)
+
+    def _gather(self, l, stream):
+        s = l % 2
+        self.binding.sparse_gather_offloaded(self.k_host[l], self.v_host[l], self.idx[l], self.count[l],
+                                             self.k_ring[s], self.v_ring[s], status=self.status, stream=stream)
+
+    def _attend(self, l, stream):
+        s = l % 2
+        self.binding.sparse_decode_attn(self.Q[l], self.k_ring[s], self.v_ring[s], self.idx[l], self.count[l],
+                                        self.seq, self.O[l], blk_slot=self.slots, status=self.status,
+                                        flags=self.binding.SPARSE_ATTN_BLOCKS_READY, workspace=self.ws,
+                                        stream=stream)
+
+    def enqueue_step(self):
+        torch = self.torch
+        main = torch.cuda.current_stream(self.dev)
+        L = self.sh.layers
+        ev = lambda st: (lambda e: (e.record(st), e)[1])(torch.cuda.Event())
+        self.side.wait_stream(main)
+        self.copy.wait_stream(main)
+        self._select(0, self.F0, self.side)
+        self.copy.wait_event(ev(self.side))
+        self._gather(0, self.copy)
+        staged = [None] * L
+        staged[0] = ev(self.copy)
+        attn_done = [None] * L
+        for l in range(L):
+            if l + 1 < L:
+                if l >= 1:
+                    self.side.wait_event(attn_done[l - 1])    # F_l exists once layer l runs
+                self._select(l + 1, self.F[l], self.side)
+                self.copy.wait_event(ev(self.side))
+                if l >= 1:
+                    self.copy.wait_event(attn_done[l - 1])    # ring slot (l+1) % 2 is free again
+                self._gather(l + 1, self.copy)
+                staged[l + 1] = ev(self.copy)
+            main.wait_event(staged[l])
+            self._attend(l, main)
+            attn_done[l] = ev(main)
+        main.wait_stream(self.side)
+        main.wait_stream(self.copy)
+
+
+def run_offload_case(args, dev):
+    import torch
+    peak, src = measured_peaks()
+    t0 = time.time()
+    wk = Offload128k(dev)
+    setup_s = time.time() - t0
+    sh = wk.sh
+    # the link: one large pinned host -> device copy, and the gather kernel alone
+    src_h = wk.k_host[0]
+    dst = torch.empty(src_h.shape, dtype=src_h.dtype, device=dev)
+    for _ in range(2):
+        dst.copy_(src_h, non_blocking=True)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    reps = 4
+    for _ in range(reps):
+        dst.copy_(src_h, non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    memcpy_gbs = reps * src_h.numel() * 2 / (a.elapsed_time(b) * 1e-3) / 1e9
+    del dst
+    wk._select(1, wk.F[0], torch.cuda.current_stream())
+    evict = torch.ones(512 << 20 >> 2, dtype=torch.int32, device=dev)   # L2 may hold host lines too
+    g = _event_times(lambda: wk._gather(1, torch.cuda.current_stream()), max(10, args.steps // 4), 3, evict)
+    del evict
+    gather_gbs = wk.link_bytes_per_layer() / (g["median_us"] * 1e-6) / 1e9
+    # the 32-layer step as a CUDA graph
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        wk.enqueue_step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        wk.enqueue_step()
+    steps = max(3, args.steps // 20)
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(steps):
+        graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    assert wk.status.item() == 0, f"device status {wk.status.item()}"
+    ms = a.elapsed_time(b) / steps
+    link_step = sh.layers * wk.link_bytes_per_layer()
+    hbm_step = sh.layers * (sh.pairs * sh.N_b * KTIL_ROW_BYTES + 2 * wk.link_bytes_per_layer())
+    line = {"case": "offload128k", "workload": sh.name, "unit_of_work": f"one decode step ({sh.layers} layers of "
+            "select(l+1) -> gather(l+1) on a copy stream, beside attention(l) over the ring)",
+            "steps_per_s": round(1000.0 / ms, 2), "ms_per_step": round(ms, 3), "steps_timed": steps,
+            "link_bytes_per_step": link_step, "link_gbs": round(link_step / (ms * 1e-3) / 1e9, 1),
+            "measured_h2d_memcpy_gbs": round(memcpy_gbs, 1),
+            "frac_of_measured_link": round(link_step / (ms * 1e-3) / 1e9 / memcpy_gbs, 4),
+            "gather_alone": {**g, "gbs": round(gather_gbs, 1)},
+            "pcie5_x16_nominal_gbs": 64.0, "hbm_bytes_per_step": hbm_step,
+            "hbm_frac_of_measured": round(hbm_step / (ms * 1e-3) / 1e9 / peak, 4), "peak_gbs": peak,
+            "peak_source": src, "host_kv_gb": round(2 * sh.layers * wk.k_host[0].numel() * 2 / 1e9, 1),
+            "setup_s": round(setup_s, 1)}
+    print(json.dumps(line), flush=True)
+
+
+def run_other_case(args, local_rank):
+    import torch
+    from block_sparse_long_pool_gb300 import workloads as wl
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    if args.case == "single4k":
+        run_single_layer_case(args, dev, wl.SINGLE_4K, "single4k")
+    elif args.case == "append32k":
+        run_single_layer_case(args, dev, wl.LLAMA8B_32K, "append32k")
+    elif args.case == "verify64k":
+        run_verify_case(args, dev)
+    else:
+        run_offload_case(args, dev)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -602,9 +905,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["step", "layer", "select"], default="step",
+    ap.add_argument("--case", choices=["step", "layer", "select", "single4k", "append32k", "verify64k",
+                                       "offload128k"], default="step",
                     help="step: the 80-layer decode step (the bench line); layer: one physical layer, "
-                         "kernels serialised and timed alone (for profiling); select: selection only")
+                         "kernels serialised and timed alone (for profiling); select: selection only; "
+                         "single4k / append32k / verify64k / offload128k: the other workloads, one line each")
     ap.add_argument("--n-split", type=int, default=0)
     ap.add_argument("--no-workspace", action="store_true", help="attention without the stream-K workspace (cluster split-KV)")
     ap.add_argument("--tokens", type=int, default=0, help="layer case: cached tokens (default 131072)")
@@ -615,6 +920,8 @@ def main():
     rank, world, local_rank = dist_env()
     if args.case in ("layer", "select"):
         run_layer_case(args, local_rank)
+    elif args.case in ("single4k", "append32k", "verify64k", "offload128k"):
+        run_other_case(args, local_rank)
     elif args.impl == "reference":
         run_reference(args, rank, world, local_rank)
     else:
