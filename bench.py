@@ -88,18 +88,22 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
 
 
-def kernel_source_hash() -> str:
+ATTN_SOURCES = ("sparse_attn.cu", "attn_core.cuh", "common.cuh")
+FUSED_SOURCES = ("decode_forecast.cu", "attn_core.cuh", "common.cuh")
+
+
+def kernel_source_hash(files=ATTN_SOURCES) -> str:
     h = hashlib.sha1()
-    for f in ("sparse_attn.cu", "common.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "block_sparse_long_pool_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_hash: str):
-    """DRAM bytes per attention launch from the committed ncu summary, if it was taken
-    on the current kernel source; otherwise None."""
-    path = os.path.join(ROOT, "profiles", "decode_attn_128k_traffic.txt")
+def profiled_traffic(kernel_hash: str, name: str = "decode_attn_128k_traffic.txt"):
+    """DRAM bytes per launch from a committed ncu summary under profiles/, if it was
+    taken on the current kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", name)
     try:
         kv = {}
         for line in open(path):
@@ -173,9 +177,16 @@ def l2_evict(buf):
 
 
 class Decode128k:
-    """Device state of the 80-layer 128K decode step and its CUDA graph."""
+    """Device state of the 80-layer 128K decode step and its CUDA graph.
 
-    def __init__(self, device, use_workspace=True):
+    mode "fused": layer 0 selects with sparse_select_topk, then every layer l is one
+    sparse_decode_attn_forecast launch (attention of l + Forecast selection of l+1), all
+    on one stream.  mode "separate": sparse_select_topk of layer l+1 on a side stream
+    beside sparse_decode_attn of layer l."""
+
+    def __init__(self, device, use_workspace=True, mode="fused"):
+        assert mode in ("fused", "separate")
+        self.mode = mode
         import torch
         from block_sparse_long_pool_gb300 import binding
         from block_sparse_long_pool_gb300 import workloads as wl
@@ -227,8 +238,25 @@ class Decode128k:
     def attn_bytes_per_launch(self):
         return self.sh.pairs * self.sh.k_tot * KV_BLOCK_BYTES
 
+    def fused_bytes_per_launch(self):
+        return self.attn_bytes_per_launch() + self.sh.pairs * self.sh.N_b * KTIL_ROW_BYTES
+
     def launches_per_step(self):
+        if self.mode == "fused":
+            return 1 + self.sh.layers  # layer-0 selection + 80 fused layers
         return 2 * self.sh.layers      # 80 selections (incl. layer 0) + 80 attentions
+
+    def _fused(self, l, stream):
+        # attention of layer l over the list the previous launch selected, and the
+        # Forecast selection of layer l+1 (none after the last layer)
+        sh = self.sh
+        q = l % sh.phys_layers
+        nxt = l + 1 < sh.layers
+        self.binding.sparse_decode_attn_forecast(
+            self.Q[l], self.k_cache[q], self.v_cache[q], self.idx[l], self.count[l], self.seq, self.O[l],
+            F=self.F[l] if nxt else None, ktil_next=self.ktil[(l + 1) % sh.phys_layers] if nxt else None,
+            n_init=sh.n_init, n_local=sh.n_local, k=sh.k, idx_next=self.idx[l + 1] if nxt else None,
+            count_next=self.count[l + 1] if nxt else None, status=self.status, stream=stream)
 
     def _select(self, l_target, F, stream):
         sh = self.sh
@@ -246,11 +274,20 @@ class Decode128k:
                                         stream=stream)
 
     def enqueue_step(self, events=None, n_split=0):
-        """Enqueue one step on the current stream (+ the side stream).  ``events``
-        (list of (start, end) pairs) brackets every attention launch when given."""
+        """Enqueue one step on the current stream (+ the side stream in separate mode).
+        ``events`` (list of (start, end) pairs) brackets every attention launch when given."""
         torch = self.torch
         main = torch.cuda.current_stream(self.dev)
         L = self.sh.layers
+        if self.mode == "fused":
+            self._select(0, self.F0, main)           # layer 0: its own current-layer Forecast
+            for l in range(L):
+                if events is not None:
+                    events[l][0].record(main)
+                self._fused(l, main)
+                if events is not None:
+                    events[l][1].record(main)
+            return
         sel_done = [None] * L
         self.side.wait_stream(main)
         self._select(0, self.F0, self.side)          # layer 0: its own current-layer Forecast
@@ -299,7 +336,7 @@ def run_ours(args, rank, world, local_rank):
     import __graft_entry__
     __graft_entry__.build()
 
-    wk = Decode128k(dev, use_workspace=not args.no_workspace)
+    wk = Decode128k(dev, use_workspace=args.workspace, mode=args.step_mode)
     graph = wk.capture()
     K, W = args.steps, args.warmup
     for _ in range(W):
@@ -323,37 +360,77 @@ def run_ours(args, rank, world, local_rank):
     attn_b, sel_b = wk.algorithmic_bytes()
     step_bytes = attn_b + sel_b
 
-    # ---- the dominant kernel (attention), per launch, CUDA events on its stream:
-    # (a) timed alone: each launch after a 512 MB read that evicts L2 (a read leaves
-    #     clean lines; a write would leave 129 MB of dirty lines for the timed kernel
-    #     to write back), no selection running beside it (the block lists are the ones
-    #     the step just selected);
-    # (b) inside the step: eager steps where the selection for layer l+1 overlaps.
+    # ---- per-launch kernel times, CUDA events on the launching stream, each launch
+    # after a 512 MB read that evicts L2 (a read leaves clean lines; a write would leave
+    # 129 MB of dirty lines for the timed kernel to write back); the block lists are
+    # the ones the step just selected.
     flush = torch.ones(512 << 20 >> 2, dtype=torch.int32, device=dev)
-    alone = []
-    for rep in range(2):
-        for l in range(wk.sh.layers):
-            l2_evict(flush)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            wk._attend(l, torch.cuda.current_stream(dev))
-            b.record()
-            alone.append((a, b))
-    torch.cuda.synchronize(dev)
-    alone_ms = statistics.mean(a.elapsed_time(b) for a, b in alone)
-    del flush
-    n_ev_steps = max(2, min(10, K // 10))
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(wk.sh.layers)] for _ in range(n_ev_steps)]
-    for e in evs:
-        wk.enqueue_step(events=e)
-    torch.cuda.synchronize(dev)
-    durs = [a.elapsed_time(b) for e in evs for (a, b) in e]
-    attn_ms = statistics.mean(durs)
-    attn_gbs = wk.attn_bytes_per_launch() / (alone_ms * 1e-3) / 1e9
-    in_step_gbs = wk.attn_bytes_per_launch() / (attn_ms * 1e-3) / 1e9
+    cur = torch.cuda.current_stream(dev)
+    L = wk.sh.layers
+
+    def time_alone(fn, reps=2):
+        ev = []
+        for _ in range(reps):
+            for l in range(L):
+                l2_evict(flush)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn(l)
+                b.record()
+                ev.append((a, b))
+        torch.cuda.synchronize(dev)
+        return statistics.mean(a.elapsed_time(b) for a, b in ev), len(ev)
+
+    def time_chain(fn, reps=5):
+        # the L launches back to back in one graph (programmatic dependent launch
+        # overlaps each launch's start with the previous one's end)
+        g = torch.cuda.CUDAGraph()
+        s_ = torch.cuda.Stream(device=dev)
+        s_.wait_stream(cur)
+        with torch.cuda.graph(g, stream=s_):
+            for l in range(L):
+                fn(l, s_)
+        for _ in range(2):
+            g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / (reps * L)
+
     peak, peak_src = measured_peaks()
-    khash = kernel_source_hash()
+    # the standalone decode attention (sparse_decode_attn, resident cache, no workspace)
+    att_alone_ms, att_n = time_alone(lambda l: wk._attend(l, cur))
+    att_chain_ms = time_chain(lambda l, st_: wk._attend(l, st_))
+    att_bytes = wk.attn_bytes_per_launch()
+    att_hash = kernel_source_hash(ATTN_SOURCES)
+    attention = {"kernel": "sparse_attn_kernel (sparse_decode_attn, decode, G=8)",
+                 "algorithmic_bytes_per_launch": att_bytes,
+                 "alone": {"avg_launch_us": round(att_alone_ms * 1e3, 2), "launches_timed": att_n,
+                           "achieved": round(att_bytes / (att_alone_ms * 1e-3) / 1e9, 1),
+                           "frac": round(att_bytes / (att_alone_ms * 1e-3) / 1e9 / peak, 4)},
+                 "chained": {"avg_launch_us": round(att_chain_ms * 1e3, 2), "launches": L,
+                             "achieved": round(att_bytes / (att_chain_ms * 1e-3) / 1e9, 1),
+                             "frac": round(att_bytes / (att_chain_ms * 1e-3) / 1e9 / peak, 4),
+                             "note": "80 launches back to back in a CUDA graph, one per layer"},
+                 "traffic": profiled_traffic(att_hash), "kernel_source_sha1": att_hash}
+    if wk.mode == "fused":
+        dom_alone_ms, dom_n = time_alone(lambda l: wk._fused(l, cur))
+        dom_bytes = wk.fused_bytes_per_launch()
+        dom_hash = kernel_source_hash(FUSED_SOURCES)
+        dom_traffic = profiled_traffic(dom_hash, "decode_forecast_128k_traffic.txt")
+        dom_name = ("decode_forecast_kernel (sparse_decode_attn_forecast: attention of layer l + Forecast "
+                    "selection of layer l+1, G=8)")
+    else:
+        dom_alone_ms, dom_n, dom_bytes = att_alone_ms, att_n, att_bytes
+        dom_hash, dom_traffic = att_hash, attention["traffic"]
+        dom_name = "sparse_attn_kernel (sparse_decode_attn, decode, G=8)"
+    dom_gbs = dom_bytes / (dom_alone_ms * 1e-3) / 1e9
+    in_step_ms = ms / wk.launches_per_step()
+    in_step_gbs = dom_bytes / (in_step_ms * 1e-3) / 1e9
+    del flush
 
     # ---- end to end through the binding: Q and F from pinned host memory in, O out
     Qh = wk.Q.cpu().pin_memory()
@@ -397,16 +474,18 @@ def run_ours(args, rank, world, local_rank):
             "hbm_frac_of_8tbs": round(step_bytes / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
             "hbm_frac_of_measured": round(step_bytes / (ms * 1e-3) / 1e9 / peak, 4),
             "bytes_per_step": {"selected_kv": attn_b, "compressed_keys": sel_b},
-            "roofline": {"bound": "hbm", "achieved": round(attn_gbs, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(attn_gbs / peak, 4), "traffic": profiled_traffic(khash),
-                         "kernel": "sparse_attn_kernel (decode, G=8), timed alone after a 512 MB read that evicts L2",
-                         "peak_source": peak_src + ", burst copy figure", "avg_launch_us": round(alone_ms * 1e3, 2),
-                         "launches_timed": len(alone),
-                         "algorithmic_bytes_per_launch": wk.attn_bytes_per_launch(),
-                         "in_step": {"avg_launch_us": round(attn_ms * 1e3, 2), "achieved": round(in_step_gbs, 1),
-                                     "frac": round(in_step_gbs / peak, 4), "launches_timed": len(durs),
-                                     "note": "selection of layer l+1 streams its compressed keys concurrently"},
-                         "kernel_source_sha1": khash},
+            "roofline": {"bound": "hbm", "achieved": round(dom_gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(dom_gbs / peak, 4), "traffic": dom_traffic,
+                         "kernel": dom_name + ", timed alone after a 512 MB read that evicts L2",
+                         "peak_source": peak_src + ", burst copy figure",
+                         "avg_launch_us": round(dom_alone_ms * 1e3, 2), "launches_timed": dom_n,
+                         "algorithmic_bytes_per_launch": dom_bytes,
+                         "in_step": {"avg_launch_us": round(in_step_ms * 1e3, 2), "achieved": round(in_step_gbs, 1),
+                                     "frac": round(in_step_gbs / peak, 4),
+                                     "note": "timed step / launches per step (the launches overlap)"},
+                         "kernel_source_sha1": dom_hash},
+            "attention_kernel": attention,
+            "step_mode": wk.mode,
             "e2e": {"value": round(world * 1000.0 / e2e_ms, 3), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": wk.launches_per_step() * K,
@@ -561,7 +640,8 @@ def run_layer_case(args, local_rank):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.ones(max(1, args.flush_mb) << 20 >> 2, dtype=torch.int32, device=dev)
     ws = None if args.no_workspace else binding.decode_workspace(B, H_q, H_kv, k_cap, args.n_split, device=dev)
-    sel_ms, att_ms = [], []
+    sel_ms, att_ms, fus_ms = [], [], []
+    idx2, cnt2 = torch.empty_like(idx), torch.empty_like(cnt)
     for i in range(args.warmup + args.steps):
         F = wl.forecast(sh, 0, i, dev)
         Q = wl.queries(sh, i, dev)
@@ -577,20 +657,36 @@ def run_layer_case(args, local_rank):
             binding.sparse_decode_attn(Q, kc, vc, idx, cnt, seq, O, status=status, n_split=args.n_split,
                                        workspace=ws)
         e[2].record()
+        # one fused layer: this layer's attention and the selection from the same keys
+        l2_evict(flush)
+        e4, e5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e4.record()
+        if not select_only:
+            binding.sparse_decode_attn_forecast(Q, kc, vc, idx, cnt, seq, O, F=F, ktil_next=kt, n_init=sh.n_init,
+                                                n_local=sh.n_local, k=sh.k, idx_next=idx2, count_next=cnt2,
+                                                n_split=args.n_split, status=status)
+        e5.record()
         torch.cuda.synchronize(dev)
         if i >= args.warmup:
             sel_ms.append(e[0].elapsed_time(e[1]))
             att_ms.append(e3.elapsed_time(e[2]))
+            fus_ms.append(e4.elapsed_time(e5))
     assert status.item() == 0
     peak, src = measured_peaks()
     attn_bytes = sh.pairs * sh.k_tot * KV_BLOCK_BYTES
     sel_bytes = sh.pairs * sh.N_b * KTIL_ROW_BYTES
     a, s_ = max(1e-6, statistics.median(att_ms)), statistics.median(sel_ms)
+    f_ = max(1e-6, statistics.median(fus_ms))
+    if not select_only:
+        assert torch.equal(idx2, idx) and torch.equal(cnt2, cnt), "fused selection differs from sparse_select_topk"
     print(json.dumps({"case": "decode_128k_one_layer", "T": T, "steps": args.steps, "n_split": args.n_split,
                       "attn_us": round(a * 1e3, 2), "attn_gbs": round(attn_bytes / a / 1e6, 1),
                       "attn_frac": round(attn_bytes / a / 1e6 / peak, 4),
                       "select_us": round(s_ * 1e3, 2), "select_gbs": round(sel_bytes / s_ / 1e6, 1),
-                      "select_frac": round(sel_bytes / s_ / 1e6 / peak, 4), "peak_gbs": peak, "peak_source": src}),
+                      "select_frac": round(sel_bytes / s_ / 1e6 / peak, 4),
+                      "fused_us": round(f_ * 1e3, 2), "fused_gbs": round((attn_bytes + sel_bytes) / f_ / 1e6, 1),
+                      "fused_frac": round((attn_bytes + sel_bytes) / f_ / 1e6 / peak, 4),
+                      "peak_gbs": peak, "peak_source": src}),
           flush=True)
 
 
@@ -911,7 +1007,11 @@ def main():
                          "kernels serialised and timed alone (for profiling); select: selection only; "
                          "single4k / append32k / verify64k / offload128k: the other workloads, one line each")
     ap.add_argument("--n-split", type=int, default=0)
-    ap.add_argument("--no-workspace", action="store_true", help="attention without the stream-K workspace (cluster split-KV)")
+    ap.add_argument("--no-workspace", action="store_true", help="layer case: attention without a workspace (cluster path)")
+    ap.add_argument("--workspace", action="store_true", help="step: attention with a workspace (split path)")
+    ap.add_argument("--step-mode", choices=["fused", "separate"], default="fused",
+                    help="fused: one sparse_decode_attn_forecast launch per layer; separate: sparse_select_topk "
+                         "on a side stream beside sparse_decode_attn")
     ap.add_argument("--tokens", type=int, default=0, help="layer case: cached tokens (default 131072)")
     ap.add_argument("--flush-mb", type=int, default=512, help="layer case: L2 flush buffer before each launch")
     args = ap.parse_args()

@@ -48,6 +48,8 @@ SIGNATURES = {
     "sparse_decode_attn_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "sparse_decode_attn_noalloc": (_I, [_P, _P, _P, _LL, _P, _P, _P, _I, _P, _I, _I, _I, _F, _P, _P, _I, _U, _P,
                                         _P]),
+    "sparse_decode_attn_forecast": (_I, [_P, _P, _P, _LL, _P, _P, _I, _P, _I, _I, _I, _F, _P, _P, _P, _P, _I, _I,
+                                         _I, _I, _P, _P, _I, _I, _U, _P, _P]),
     "sparse_verify_attn_grouped": (_I, [_P, _P, _P, _LL, _P, _I, _I, _I, _I, _P, _I, _I, _I, _F, _P, _P, _I,
                                         _P, _P]),
     "sparse_gather_offloaded": (_I, [_P, _P, _LL, _P, _P, _I, _I, _I, _P, _P, _P, _I, _P, _P]),
@@ -164,7 +166,8 @@ def _decode_args(Q, k_base, v_base, blk_logical, count, seq_len, O, lse, blk_slo
 
 
 def sparse_decode_attn_workspace_size(B: int, H_q: int, H_kv: int, k_tot: int, n_split: int = 0) -> int:
-    """Bytes of the stream-K workspace of sparse_decode_attn (0: not used for these sizes)."""
+    """Bytes of the workspace of sparse_decode_attn (split and stream-K paths; 0: sizes
+    that no workspace path serves)."""
     return int(load().sparse_decode_attn_workspace_size(B, H_q, H_kv, k_tot, n_split))
 
 
@@ -228,6 +231,35 @@ def sparse_decode_attn_ex(Q, k_base, v_base, blk_logical, count, seq_len, O, rea
                                       _ptr(ready_flag),
                                       int(ready_target), int(timeout_ns), _ptr(status), _stream(stream))
     _check(rc, "sparse_decode_attn_ex")
+
+
+def sparse_decode_attn_forecast(Q, k_cache, v_cache, blk_idx, count, seq_len, O, lse=None, F=None, ktil_next=None,
+                                n_init: int = 1, n_local: int = 2, k: int = 0, idx_next=None, count_next=None,
+                                scale: float = 0.0, n_split: int = 0, flags: int = 0, status=None, stream=None):
+    """One decode layer in one kernel: O = attention of Q over blocks blk_idx of the
+    resident cache k_cache / v_cache [B][H_kv][T_cap][128], and (when F is given) the
+    Forecast selection of the next layer from ktil_next [B][H_kv][N_cap][128] into
+    idx_next [B][H_kv][k_tot_next] / count_next [B][H_kv]."""
+    B, H_q, H_kv, k_tot, T_cap = _decode_args(Q, k_cache, v_cache, blk_idx, count, seq_len, O, lse, None)
+    _need(k_cache, "k_cache", torch.bfloat16, shape=(B, H_kv, T_cap, D))
+    N_cap = k_tot_next = 0
+    if F is not None:
+        if ktil_next is None or idx_next is None or count_next is None:
+            raise ValueError("F needs ktil_next, idx_next and count_next")
+        N_cap = ktil_next.shape[2]
+        k_tot_next = idx_next.shape[2]
+        _need(F, "F", torch.bfloat16, shape=(B, H_kv, D))
+        _need(ktil_next, "ktil_next", torch.float32, shape=(B, H_kv, N_cap, D))
+        _need(idx_next, "idx_next", torch.int32, shape=(B, H_kv, k_tot_next))
+        _need(count_next, "count_next", torch.int32, shape=(B, H_kv))
+    if status is not None:
+        _need(status, "status", torch.int32)
+    rc = load().sparse_decode_attn_forecast(_ptr(Q), _ptr(k_cache), _ptr(v_cache), T_cap, _ptr(blk_idx), _ptr(count),
+                                            k_tot, _ptr(seq_len), B, H_q, H_kv, float(scale), _ptr(O), _ptr(lse),
+                                            _ptr(F), _ptr(ktil_next), N_cap, n_init, n_local, k, _ptr(idx_next),
+                                            _ptr(count_next), k_tot_next, n_split, int(flags), _ptr(status),
+                                            _stream(stream))
+    _check(rc, "sparse_decode_attn_forecast")
 
 
 def sparse_verify_attn_grouped(Q, k_cache, v_cache, idx_q, C: int, window_blocks: int, seq_len, O,

@@ -1,0 +1,482 @@
+// attn_core.cuh -- building blocks shared by the attention kernels (decode,
+// grouped verification, and decode fused with the next layer's Forecast selection):
+// the shared-memory ring layout, the per-warp online-softmax state, the tensor-core
+// step over one 64-token block, and the merges of partial softmax states.
+#pragma once
+
+#include <limits.h>
+#include <math.h>
+
+#include "common.cuh"
+
+namespace {
+
+using namespace sp;
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 3;
+constexpr int kHalfBytes = kBlk * 64 * 2;       // 64 tokens x 64 dims of bf16: one TMA box
+constexpr int kTileBytes = 2 * kHalfBytes;      // one block of K (or V): 16 KB
+constexpr int kStageBytes = 2 * kTileBytes;     // K + V of one block: 32 KB
+constexpr int kMaxUnion = 512;
+constexpr int kMaxSplit = 8;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+// Dynamic shared memory layout, offsets from a 1024-byte aligned base.
+constexpr int kOffBars = kStages * kStageBytes;          // full[kStages], empty[kStages]
+constexpr int kOffCtrl = kOffBars + 2 * kStages * 8;     // int ctrl[16]
+constexpr int kOffList = kOffCtrl + 64;                  // verification: int ulist[kMaxUnion]
+constexpr int kOffMask = kOffList + kMaxUnion * 4;       // uint32 umask[kMaxUnion]
+constexpr int kOffEntV = kOffMask + kMaxUnion * 4;       // union build scratch
+constexpr int kOffEntM = kOffEntV + kMaxUnion * 4;
+constexpr int kOffEntF = kOffEntM + kMaxUnion * 4;
+constexpr int kMaxListCta = kMaxUnion;                   // decode: staged slice of the block list
+constexpr int kSmemDecode = kOffList + 2 * kMaxListCta * 4 + 1024;
+constexpr int kSmemVerify = kOffEntF + kMaxUnion * 4 + 1024;
+// stream-K decode: the list of the CTA's range, its segment table and merge rows
+constexpr int kMaxSegs = kMaxListCta + 2;
+constexpr int kOffSegs = kOffList + 2 * kMaxListCta * 4;          // seg_nv[kMaxSegs], seg_start[kMaxSegs]
+constexpr int kMaxMergeSeg = 64;                                  // CTAs sharing one pair, at most
+constexpr int kOffRowML = kOffSegs + 2 * kMaxSegs * 4;            // row max / sum of a pair merge
+constexpr int kOffMergeFac = kOffRowML + 2 * 16 * 4;              // [kMaxMergeSeg][8] weights (NT = 1)
+constexpr int kOffMergeSlot = kOffMergeFac + 2 * kMaxMergeSeg * 8 * 4;   // [kMaxMergeSeg] slot offsets
+constexpr int kSmemStreamK = kOffMergeSlot + kMaxMergeSeg * 4 + 1024;
+enum { kCtrlLast = 2, kCtrlMergeValid = 3 };
+
+enum { kCtrlAbort = 0, kCtrlList = 1 };
+
+struct AttnParams {
+    const uint16_t *Q;
+    uint16_t *O;
+    float *lse;
+    const int *blk_slot;
+    const int *blk_logical;
+    const int *count;
+    const int *seq_len;
+    int *status;
+    const int *idx_q;
+    long long *blocks_loaded;
+    const unsigned *ready_flag;
+    long long pair_stride;
+    long long timeout_ns;
+    unsigned ready_target;
+    int k_tot;
+    int H_q;
+    int H_kv;
+    int G;
+    int n_sel;
+    int N_q;
+    int C;
+    int window_blocks;
+    int n_groups;
+    unsigned flags;
+    float scale_log2;
+    // stream-K decode
+    float *ws_part;        // [2 * n_ctas][ROWS * 128 + 2 * ROWS] partial states
+    int *ws_count;         // [pairs] arrival counters, zero between calls
+    long long n_items;     // pairs * k_tot
+    // decode fused with the next layer's Forecast selection
+    const uint16_t *F;     // [pairs][128] Forecast vectors, or null (no selection)
+    const float *ktil;     // [pairs][N_cap][128] compressed keys of the next layer
+    int *idx_next;         // [pairs][k_tot_next] selected blocks of the next layer
+    int *count_next;       // [pairs]
+    int N_cap;
+    int n_init;
+    int n_local;
+    int k_sel;
+    int k_tot_next;
+};
+
+__device__ __forceinline__ uint32_t ld_b32(const uint16_t *p)
+{
+    return *reinterpret_cast<const uint32_t *>(p);
+}
+
+// Per-warp online-softmax state: the max and sum of rows 2*t4 and 2*t4+1 of every
+// n-tile (log2 units) and the O^T accumulators of the warp's MMA fragments.
+template <int NT>
+struct WarpState {
+    float m[NT][2], l[NT][2], acc[8][NT][4];
+
+    __device__ __forceinline__ void reset()
+    {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                m[nt][h] = -INFINITY;
+                l[nt][h] = 0.f;
+            }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    acc[mt][nt][i] = 0.f;
+    }
+};
+
+// Q^T fragments (the B operand of S^T = K Q^T; row n = lane/4 of each n-tile) and the
+// validity / query index of the two rows this lane's softmax state covers.
+template <int NT>
+struct QueryFrags {
+    uint32_t qb[NT][8][2];
+    bool row_ok[NT][2];
+    int row_q[NT][2];
+};
+
+// Query rows of a unit: decode rows are the G heads of KV head g of batch b;
+// verification rows are (query q0 + r / G, head r % G).
+template <int NT, bool VERIFY>
+__device__ __forceinline__ void load_query(QueryFrags<NT> &q, const AttnParams &p, int b, int g, int q0,
+                                           int rows_valid, int lane)
+{
+    const int g8 = lane >> 2, t4 = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int row = nt * 8 + g8;
+        const uint16_t *qrow = nullptr;
+        if (row < rows_valid) {
+            if (VERIFY) {
+                const int qq = q0 + row / p.G, hh = row % p.G;
+                qrow = p.Q + ((static_cast<size_t>(b) * p.N_q + qq) * p.H_q + g * p.G + hh) * kD;
+            } else {
+                qrow = p.Q + (static_cast<size_t>(b) * p.H_q + g * p.G + row) * kD;
+            }
+        }
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            q.qb[nt][ks][0] = qrow ? ld_b32(qrow + 16 * ks + 2 * t4) : 0u;
+            q.qb[nt][ks][1] = qrow ? ld_b32(qrow + 16 * ks + 2 * t4 + 8) : 0u;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = nt * 8 + 2 * t4 + h;
+            q.row_ok[nt][h] = r < rows_valid;
+            q.row_q[nt][h] = VERIFY ? (r < rows_valid ? r / p.G : 0) : 0;
+        }
+    }
+}
+
+// One consumer warp over tokens [16w, 16w+16) of the block held in ring stage `kst`
+// (K, 2 x 8 KB swizzled boxes) and `kst + kTileBytes` (V).  tok0 is the absolute
+// position of the warp's first token; qmask selects the rows' queries (verification).
+template <int NT, bool VERIFY>
+__device__ __forceinline__ void attend_block(WarpState<NT> &st, const QueryFrags<NT> &q, uint32_t kst, long long tok0,
+                                             long long len, uint32_t qmask, float scale_log2, int w, int lane)
+{
+    const int g8 = lane >> 2;
+    const int jm = lane >> 3, rr = lane & 7;
+    const int a_tok = w * 16 + (jm & 1) * 8 + rr;   // K rows for ldmatrix (QK A operand)
+    const int v_tok = w * 16 + (jm >> 1) * 8 + rr;  // V rows for ldmatrix.trans (PV A operand)
+    const uint32_t a_sw = static_cast<uint32_t>(a_tok & 7);
+    const uint32_t v_sw = static_cast<uint32_t>(v_tok & 7);
+    const uint32_t vst = kst + kTileBytes;
+    float sacc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            sacc[nt][i] = 0.f;
+    // S^T (16 tokens x 8*NT rows) = K (16 x 128) Q^T (128 x 8*NT)
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t chunk = static_cast<uint32_t>(((ks & 3) << 1) + (jm >> 1));
+        const uint32_t addr = kst + (ks >> 2) * kHalfBytes + a_tok * 128 + ((chunk ^ a_sw) << 4);
+        uint32_t a[4];
+        ldsm_x4(addr, a);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+            mma_bf16_16816(sacc[nt], a, q.qb[nt][ks][0], q.qb[nt][ks][1]);
+    }
+    // scale to log2 units, mask tokens past the length and rows not selecting the block
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int h = i & 1;
+            const long long tok = tok0 + g8 + (i >> 1) * 8;
+            bool keep = tok < len && q.row_ok[nt][h];
+            if (VERIFY)
+                keep = keep && ((qmask >> q.row_q[nt][h]) & 1u);
+            sacc[nt][i] = keep ? sacc[nt][i] * scale_log2 : -INFINITY;
+        }
+    // online softmax per row (the 8 lanes sharing t4 hold one row's 16 tokens)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float mx = fmaxf(sacc[nt][h], sacc[nt][h + 2]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float m_new = fmaxf(st.m[nt][h], mx);
+            const float m_use = m_new == -INFINITY ? 0.f : m_new;
+            const float alpha = exp2f(st.m[nt][h] - m_use);
+            const float p0 = exp2f(sacc[nt][h] - m_use);
+            const float p1 = exp2f(sacc[nt][h + 2] - m_use);
+            st.l[nt][h] = st.l[nt][h] * alpha + p0 + p1;
+            st.m[nt][h] = m_new;
+            sacc[nt][h] = p0;
+            sacc[nt][h + 2] = p1;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                st.acc[mt][nt][h] *= alpha;
+                st.acc[mt][nt][h + 2] *= alpha;
+            }
+        }
+    // P^T as the B operand: transpose the bf16 (token, row) 8x8 tiles in registers
+    uint32_t pb[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        pb[nt][0] = movmatrix_trans(pack_bf16x2(sacc[nt][0], sacc[nt][1]));
+        pb[nt][1] = movmatrix_trans(pack_bf16x2(sacc[nt][2], sacc[nt][3]));
+    }
+    // O^T (128 dims x rows) += V^T (128 x 16 tokens) P^T (16 x rows)
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        const uint32_t chunk = static_cast<uint32_t>(((mt & 3) << 1) + (jm & 1));
+        const uint32_t addr = vst + (mt >> 2) * kHalfBytes + v_tok * 128 + ((chunk ^ v_sw) << 4);
+        uint32_t a[4];
+        ldsm_x4_trans(addr, a);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+            mma_bf16_16816(st.acc[mt][nt], a, pb[nt][0], pb[nt][1]);
+    }
+}
+
+// Complete the row sums over the 8 lanes that share a row.
+template <int NT>
+__device__ __forceinline__ void finish_row_sums(WarpState<NT> &st)
+{
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float l = st.l[nt][h];
+            l += __shfl_xor_sync(0xffffffffu, l, 4);
+            l += __shfl_xor_sync(0xffffffffu, l, 8);
+            l += __shfl_xor_sync(0xffffffffu, l, 16);
+            st.l[nt][h] = l;
+        }
+}
+
+// Warp `warp`'s state into shared memory: wo [4][ROWS][128], wm / wl [4][ROWS].
+template <int NT>
+__device__ __forceinline__ void store_warp_state(const WarpState<NT> &st, float *wo, float *wm, float *wl, int warp,
+                                                 int lane)
+{
+    constexpr int ROWS = 8 * NT;
+    const int g8 = lane >> 2, t4 = lane & 3;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int dim = mt * 16 + g8 + (i >> 1) * 8;
+                const int row = nt * 8 + 2 * t4 + (i & 1);
+                wo[(warp * ROWS + row) * kD + dim] = st.acc[mt][nt][i];
+            }
+    if (g8 == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = nt * 8 + 2 * t4 + h;
+                wm[warp * ROWS + row] = st.m[nt][h];
+                wl[warp * ROWS + row] = st.l[nt][h];
+            }
+    }
+}
+
+// Merge the 4 warp states (wo/wm/wl) into one CTA state: co [ROWS][128] unnormalised,
+// cm / cl [ROWS] its max and sum; wf [4][ROWS] scratch.  `t` / `nthreads` name the
+// participating threads; the caller synchronises them between the two phases through
+// `sync()`.
+template <int ROWS, typename Sync>
+__device__ __forceinline__ void merge_warp_states(const float *wo, const float *wm, const float *wl, float *wf,
+                                                  float *co, float *cm, float *cl, int t, int nthreads, Sync sync)
+{
+    if (t < ROWS) {
+        const int row = t;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w4 = 0; w4 < kConsumerWarps; ++w4)
+            M = fmaxf(M, wm[w4 * ROWS + row]);
+        float L = 0.f;
+#pragma unroll
+        for (int w4 = 0; w4 < kConsumerWarps; ++w4) {
+            const float mw = wm[w4 * ROWS + row];
+            const float f = (M == -INFINITY || mw == -INFINITY) ? 0.f : exp2f(mw - M);
+            wf[w4 * ROWS + row] = f;
+            L += f * wl[w4 * ROWS + row];
+        }
+        cm[row] = M;
+        cl[row] = L;
+    }
+    sync();
+    for (int item = t; item < ROWS * kD; item += nthreads) {
+        const int row = item / kD;
+        float o = 0.f;
+#pragma unroll
+        for (int w4 = 0; w4 < kConsumerWarps; ++w4)
+            o = fmaf(wf[w4 * ROWS + row], wo[w4 * ROWS * kD + item], o);
+        co[item] = o;
+    }
+}
+
+__device__ __forceinline__ void store_bf16(uint16_t *dst, float v)
+{
+    const __nv_bfloat16 ob = __float2bfloat16_rn(v);
+    *dst = *reinterpret_cast<const uint16_t *>(&ob);
+}
+
+__device__ __forceinline__ float lse_of(float M, float L)
+{
+    return L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
+}
+
+
+// The merge of a cluster's partial states (split-KV): (1) each consumer warp's state
+// into shared memory, (2) merged into this CTA's state, (3) after one cluster barrier
+// CTA `rank` merges the S CTA states for its slice of output dims, reading its peers'
+// shared memory (distributed shared memory) with independent loads, and writes rows
+// [0, rows_valid) of O (and lse from rank 0).  Every thread of every CTA of the
+// cluster calls it (`nthreads` = blockDim.x); the ring at `base` is reused as scratch,
+// so every stage must have been consumed.  A CTA that failed its ready check
+// (`aborted`) makes the whole unit leave O and lse untouched.
+template <int NT, bool VERIFY>
+__device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uint8_t *base, bool aborted,
+                                                    const AttnParams &p, int b, int g, int q0, int rows_valid,
+                                                    uint32_t rank, uint32_t S, int nthreads)
+{
+    constexpr int ROWS = 8 * NT;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    float *wo = reinterpret_cast<float *>(base);                     // [4][ROWS][128]
+    float *wm = wo + kConsumerWarps * ROWS * kD;                     // [4][ROWS]
+    float *wl = wm + kConsumerWarps * ROWS;                          // [4][ROWS]
+    float *wf = wl + kConsumerWarps * ROWS;                          // [4][ROWS] warp weights
+    float *co = wf + kConsumerWarps * ROWS;                          // [ROWS][128] CTA state
+    float *cm = co + ROWS * kD;                                      // [ROWS]
+    float *cl = cm + ROWS;                                           // [ROWS]
+    int *cabort = reinterpret_cast<int *>(cl + ROWS);                // [4]
+    float *fac = reinterpret_cast<float *>(cabort + 4);              // [kMaxSplit][ROWS]
+    float *row_m = fac + kMaxSplit * ROWS;
+    float *row_l = row_m + ROWS;
+    if (warp < kConsumerWarps)
+        store_warp_state<NT>(st, wo, wm, wl, warp, lane);
+    if (tid == 0)
+        cabort[0] = aborted ? 1 : 0;
+    __syncthreads();
+    merge_warp_states<ROWS>(wo, wm, wl, wf, co, cm, cl, tid, nthreads, [] { __syncthreads(); });
+    cluster_sync();
+
+    // peers' CTA states (generic pointers into distributed shared memory)
+    const float *peer_co[kMaxSplit];
+    const float *peer_cm[kMaxSplit];
+    const float *peer_cl[kMaxSplit];
+    int any_abort = 0;
+#pragma unroll
+    for (int c = 0; c < kMaxSplit; ++c) {
+        const unsigned r = c < static_cast<int>(S) ? static_cast<unsigned>(c) : 0u;
+        peer_co[c] = static_cast<const float *>(__cluster_map_shared_rank(co, r));
+        peer_cm[c] = static_cast<const float *>(__cluster_map_shared_rank(cm, r));
+        peer_cl[c] = static_cast<const float *>(__cluster_map_shared_rank(cl, r));
+        const int ab = *static_cast<const int *>(__cluster_map_shared_rank(cabort, r));
+        any_abort |= c < static_cast<int>(S) ? ab : 0;
+    }
+
+    // any CTA of the unit that failed its ready check leaves the output untouched
+    if (!any_abort) {
+        if (tid < ROWS) {
+            const int row = tid;
+            float mc[kMaxSplit], lc[kMaxSplit];
+#pragma unroll
+            for (int c = 0; c < kMaxSplit; ++c) {
+                mc[c] = c < static_cast<int>(S) ? peer_cm[c][row] : -INFINITY;
+                lc[c] = c < static_cast<int>(S) ? peer_cl[c][row] : 0.f;
+            }
+            float M = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kMaxSplit; ++c)
+                M = fmaxf(M, mc[c]);
+            float L = 0.f;
+#pragma unroll
+            for (int c = 0; c < kMaxSplit; ++c) {
+                const float f = (M == -INFINITY || mc[c] == -INFINITY) ? 0.f : exp2f(mc[c] - M);
+                fac[c * ROWS + row] = f;
+                L += lc[c] * f;
+            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+            for (int c = 0; c < kMaxSplit; ++c)
+                fac[c * ROWS + row] *= inv;
+            row_m[row] = M;
+            row_l[row] = L;
+        }
+        __syncthreads();
+        const int dims_per = kD / static_cast<int>(S);
+        const int d0 = static_cast<int>(rank) * dims_per;
+        for (int item = tid; item < rows_valid * dims_per; item += nthreads) {
+            const int row = item / dims_per;
+            const int d = d0 + (item - row * dims_per);
+            float v[kMaxSplit];
+#pragma unroll
+            for (int c = 0; c < kMaxSplit; ++c)
+                v[c] = c < static_cast<int>(S) ? peer_co[c][row * kD + d] : 0.f;
+            float o = 0.f;
+#pragma unroll
+            for (int c = 0; c < kMaxSplit; ++c)
+                o = fmaf(fac[c * ROWS + row], v[c], o);
+            size_t out;
+            if (VERIFY) {
+                const int qq = q0 + row / p.G, hh = row % p.G;
+                out = ((static_cast<size_t>(b) * p.N_q + qq) * p.H_q + g * p.G + hh) * kD + d;
+            } else {
+                out = (static_cast<size_t>(b) * p.H_q + g * p.G + row) * kD + d;
+            }
+            const __nv_bfloat16 ob = __float2bfloat16_rn(o);
+            p.O[out] = *reinterpret_cast<const uint16_t *>(&ob);
+        }
+        if (!VERIFY && rank == 0 && p.lse != nullptr) {
+            for (int row = tid; row < rows_valid; row += nthreads) {
+                const float L = row_l[row];
+                p.lse[static_cast<size_t>(b) * p.H_q + g * p.G + row] =
+                    L > 0.f ? (row_m[row] + log2f(L)) * 0.69314718055994530942f : -INFINITY;
+            }
+        }
+    }
+    // peers may still read this CTA's state
+    cluster_sync();
+}
+
+// ---------------------------------------------------------------- host helpers
+
+// Cluster size S (CTAs sharing one unit's list) for the cluster kernels: auto = enough
+// units x S to cover the SMs twice, at least two blocks per CTA.
+inline int choose_split(int n_split, long long units, int max_list, int sm_count, int *S)
+{
+    if (n_split == 0) {
+        int s = 1;
+        while (s < kMaxSplit && units * s * 2 <= 2LL * sm_count && s * 2 <= (max_list > 1 ? max_list / 2 : 1))
+            s *= 2;
+        *S = s;
+        return SPARSE_OK;
+    }
+    if (n_split != 1 && n_split != 2 && n_split != 4 && n_split != 8)
+        return sp_host::fail(SPARSE_ERR_INVALID_ARG, "n_split must be 0, 1, 2, 4 or 8 (got %d)", n_split);
+    *S = n_split;
+    return SPARSE_OK;
+}
+
+inline float scale_log2_of(float scale)
+{
+    const float s = scale == 0.f ? 1.f / sqrtf(static_cast<float>(kD)) : scale;
+    return s * 1.44269504088896340736f;   // log2(e): scores are exponentiated base 2
+}
+
+}  // namespace

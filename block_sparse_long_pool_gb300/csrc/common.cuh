@@ -94,6 +94,42 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     return false;
 }
 
+// Wait, with acquire semantics at cluster scope, for a phase of a barrier that threads
+// of other CTAs of the cluster arrive on (mbar_arrive_cluster); bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait_cluster(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 0; it < (1u << 28); ++it) {
+        if (mbar_try_wait_cluster(bar, parity))
+            return true;
+        if ((it & 31u) == 31u && globaltimer() - t0 > limit_ns)
+            return false;
+    }
+    return false;
+}
+
+// Arrive (release at cluster scope) on a barrier given by its shared::cluster address
+// (dsmem_addr), possibly in another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 
 // Wait until the grid that precedes this one on its stream has completed and its
@@ -132,6 +168,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::"
         "cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+
+// Contiguous bulk copy global -> this CTA's shared memory (16-byte aligned addresses,
+// size a multiple of 16), completing on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(policy)
         : "memory");
 }
 
@@ -184,6 +232,13 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Arrive at barrier `id` without waiting: the warp's earlier shared-memory writes are
+// visible to the threads that wait there (named_barrier_sync with the same count).
+__device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Order this thread's generic-proxy shared-memory accesses before later async-proxy
 // (TMA) accesses to the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -201,6 +256,20 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
+}
+
+// The two halves of cluster_sync, for a barrier whose wait comes later than its
+// arrive (every thread of the cluster arrives once, then waits once).
+__device__ __forceinline__ void cluster_arrive()
+{
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    __syncwarp();
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -237,6 +306,18 @@ __device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t addr)
     uint32_t v;
     asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
+}
+
+// ---------------------------------------------------------------- selection keys
+
+// Monotone map of an fp32 score to an unsigned key (larger score -> larger key); -0
+// and +0 share a key.  Top-k selection compares keys, so equal scores tie exactly.
+__device__ __forceinline__ uint32_t order_key(float s)
+{
+    uint32_t u = __float_as_uint(s);
+    if (u == 0x80000000u)
+        u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 }  // namespace sp

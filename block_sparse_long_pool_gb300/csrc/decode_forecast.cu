@@ -1,0 +1,701 @@
+// decode_forecast.cu -- one SparDA decode layer in one kernel: block-sparse GQA
+// attention of layer l fused with the Forecast selection of the blocks of layer l+1.
+//
+// SparDA notes §4.1: the Forecast vector F_l of layer l scores the compressed keys of
+// layer l+1, so the blocks of layer l+1 are chosen while layer l attends (eq.(6)),
+// and layer l attends over the blocks chosen one layer earlier (eq.(7)); §4.2 Alg.1
+// steps 2 and 4 of one layer.  The selection is the one of sparse_select_topk (fp32
+// scores s_j = F . K̃_j, the k largest outside B_init and B_local, equal scores to the
+// lower block index, B_init ∪ B_local ∪ top-k ascending); the attention is the one of
+// sparse_decode_attn (scale 1/sqrt(d), split-KV merged by the online-softmax
+// recurrence).
+//
+// GB300 design.  A cluster of S CTAs per (batch, KV head) pair; 6 warps per CTA.
+//   * Warp 4 (producer): one lane first streams this CTA's slice of the next layer's
+//     compressed keys into the ring (1-D bulk copies, 64 rows = 32 KB per stage).
+//     Nothing the preceding kernel writes is needed for that, so it overlaps the
+//     preceding kernel's tail under programmatic dependent launch.  It then waits for
+//     that kernel (the block list of this layer may be its output), stages the list
+//     slice, and streams the selected K/V blocks with TMA tensor copies.
+//   * Warps 0-3 (consumers): score every key row of a stage (fp32 dot product with F,
+//     shuffle reduction, one warp per 16 rows) and store the order key into CTA 0's
+//     shared memory (distributed shared memory); each warp then arrives on CTA 0's
+//     "scored" barrier; then the attention of the sparse_decode_attn cluster kernel.
+//   * Warp 5 (selector) of CTA 0: waits on the "scored" barrier and runs the exact
+//     top-k (MSB-first radix select over the keys) and the ascending compaction while
+//     the consumers attend; the next layer's list is out before the kernel ends.
+//   * The dependent launch is allowed at once: the next layer's kernel starts streaming
+//     its key slice as SMs free up, and waits for this kernel before reading the list
+//     this kernel writes.
+#include "attn_core.cuh"
+
+namespace {
+
+constexpr int kFThreads = (kConsumerWarps + 2) * 32;
+constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;   // producer + consumers (named barrier 1)
+constexpr int kKtilRowBytes = kD * 4;
+constexpr int kKtilRowsPerStage = kStageBytes / kKtilRowBytes;   // 64
+constexpr int kCtrlScoredBar = 8;                                 // ctrl[8..9]: the "scored" mbarrier
+constexpr int kTopkList = 512;                                    // keys gathered in the threshold bin
+constexpr int kCoarseShift = 22;                                  // coarse bin = key >> 22
+constexpr int kCoarseBins = 1 << (32 - kCoarseShift);             // 1024
+
+// Shared memory after the ring, barriers and ctrl words (offsets from the 1024-byte
+// aligned base): CTA 0's coarse key histogram (reused for the radix digits), the keys
+// gathered in the threshold bin, the list slice (slot, logical) and CTA 0's keys.
+__host__ __device__ constexpr int fused_off_hist()
+{
+    return kOffList;
+}
+__host__ __device__ constexpr int fused_off_topk_list()
+{
+    return kOffList + kCoarseBins * 4;
+}
+__host__ __device__ constexpr int fused_off_slice()
+{
+    return fused_off_topk_list() + kTopkList * 4;
+}
+__host__ __device__ inline int fused_per_pad(int per)
+{
+    return (per + 3) & ~3;
+}
+__host__ __device__ inline int fused_off_keys(int per)
+{
+    return fused_off_slice() + 2 * fused_per_pad(per) * 4;
+}
+inline size_t fused_smem_bytes(int per, int N_cap)
+{
+    return static_cast<size_t>(fused_off_keys(per)) + static_cast<size_t>(N_cap) * 4 + 1024;
+}
+
+// Histogram of byte digit (key >> shift) & 255 over keys[lo, hi) whose bits above the
+// digit equal `prefix` (under `pmask`), by one warp; lanes holding the same digit add
+// once (warp-aggregated shared-memory atomics).
+__device__ __forceinline__ void warp_digit_hist(const uint32_t *keys, int lo, int hi, uint32_t pmask,
+                                                uint32_t prefix, int shift, uint32_t *hist, int lane)
+{
+    for (int d = lane; d < 256; d += 32)
+        hist[d] = 0u;
+    __syncwarp();
+    for (int jb = lo; jb < hi; jb += 32) {
+        const int j = jb + lane;
+        uint32_t digit = 0xFFFFFFFFu;
+        if (j < hi) {
+            const uint32_t key = keys[j];
+            if ((key & pmask) == prefix)
+                digit = (key >> shift) & 255u;
+        }
+        const uint32_t same = __match_any_sync(0xffffffffu, digit);
+        if (digit != 0xFFFFFFFFu && lane == __ffs(same) - 1)
+            atomicAdd(&hist[digit], static_cast<uint32_t>(__popc(same)));
+    }
+    __syncwarp();
+}
+
+// From a digit histogram, the digit that holds the need-th largest key (counting from
+// the top digit) and the number of keys still needed within it.  Returns the count of
+// keys with that digit.
+__device__ __forceinline__ int warp_pick_digit(const uint32_t *hist, int &need, uint32_t &digit, int lane)
+{
+    // lane l holds digits 255 - 8l - i (i = 0..7): lanes run from the top digit down
+    int c[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        c[i] = static_cast<int>(hist[255 - 8 * lane - i]);
+        sum += c[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += n;
+    }
+    const int excl = incl - sum;
+    int dsel = -1, need_new = 0, cnt = 0;
+    if (excl < need && need <= incl) {
+        int acc = excl;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (dsel < 0 && acc + c[i] >= need) {
+                dsel = 255 - 8 * lane - i;
+                need_new = need - acc;
+                cnt = c[i];
+            }
+            acc += c[i];
+        }
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, dsel >= 0);
+    const int src = m != 0u ? __ffs(m) - 1 : 0;
+    dsel = __shfl_sync(0xffffffffu, dsel, src);
+    need_new = __shfl_sync(0xffffffffu, need_new, src);
+    cnt = __shfl_sync(0xffffffffu, cnt, src);
+    if (m == 0u) {   // cannot happen with 1 <= need <= keys counted; keep the state sane
+        dsel = 0;
+        need_new = need;
+        cnt = 0;
+    }
+    digit = static_cast<uint32_t>(dsel);
+    need = need_new;
+    return cnt;
+}
+
+// The exact top-k of one pair by one warp over the order keys of blocks [0, nb):
+// the k largest keys among candidates [n_init, nb - n_local) (equal keys: lower block
+// first), united with B_init and B_local, written ascending to out[0 .. count) and -1
+// after.  `coarse` is the histogram of key >> 22 over the candidates (built while the
+// keys were scored).  The k-th largest key lies in the coarse bin where the count
+// from the top reaches k; the keys of that bin are gathered into `list` (at most
+// kTopkList, else every candidate is scanned again) and the remaining 22 bits come
+// from an MSB-first radix select over byte digits.  `coarse` is reused for the digits.
+__device__ void topk_warp(const uint32_t *keys, uint32_t *coarse, uint32_t *list, int nb, int n_init, int n_local,
+                          int k, int *out, int k_tot, int *count_out, int *status, int lane)
+{
+    const int cand_lo = n_init, cand_hi = nb - n_local;
+    const bool take_all = max(0, cand_hi - cand_lo) <= k;
+    const bool take_none = k <= 0;
+    const unsigned lt = (1u << lane) - 1u;
+    uint32_t prefix = 0, pmask = 0;
+    int need = k;
+    if (!take_all && !take_none) {
+        // coarse bin: lane l sums bins [1023 - 32l - 31, 1023 - 32l]
+        constexpr int kPer = kCoarseBins / 32;
+        const uint32_t *mine = coarse + (kCoarseBins - kPer * (lane + 1));
+        int c = 0;
+#pragma unroll
+        for (int i = 0; i < kPer; i += 4) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(mine + i);
+            c += static_cast<int>(v.x + v.y + v.z + v.w);
+        }
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += n;
+        }
+        const int excl = incl - c;
+        int bsel = -1, need_new = 0, m = 0;
+        if (excl < need && need <= incl) {
+            int acc = excl;
+            for (int i = kPer - 1; i >= 0 && bsel < 0; --i) {
+                const int ci = static_cast<int>(mine[i]);
+                if (acc + ci >= need) {
+                    bsel = kCoarseBins - kPer * (lane + 1) + i;
+                    need_new = need - acc;
+                    m = ci;
+                }
+                acc += ci;
+            }
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, bsel >= 0);
+        const int src_lane = hit != 0u ? __ffs(hit) - 1 : 0;
+        bsel = __shfl_sync(0xffffffffu, bsel, src_lane);
+        need = __shfl_sync(0xffffffffu, need_new, src_lane);
+        m = __shfl_sync(0xffffffffu, m, src_lane);
+        const bool found = hit != 0u;   // always, when the histogram counts every candidate
+        prefix = found ? static_cast<uint32_t>(bsel) << kCoarseShift : 0u;
+        pmask = found ? ~((1u << kCoarseShift) - 1u) : 0u;
+        if (!found)
+            need = k;
+        __syncwarp();
+        const uint32_t *src = keys;
+        int lo = cand_lo, hi = cand_hi;
+        if (found && m <= kTopkList) {
+            // gather the keys of the threshold bin (four chunks of 32 in flight)
+            int n = 0;
+            for (int jb = cand_lo; jb < cand_hi; jb += 128) {
+                uint32_t kv[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int j = jb + 32 * u + lane;
+                    kv[u] = j < cand_hi ? keys[j] : 0u;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int j = jb + 32 * u + lane;
+                    const bool in = j < cand_hi && (kv[u] & pmask) == prefix;
+                    const unsigned bm = __ballot_sync(0xffffffffu, in);
+                    if (in)
+                        list[n + __popc(bm & lt)] = kv[u];
+                    n += __popc(bm);
+                }
+            }
+            __syncwarp();
+            src = list;
+            lo = 0;
+            hi = n;
+        }
+        uint32_t d;
+        if (!found) {
+            warp_digit_hist(src, lo, hi, 0u, 0u, 24, coarse, lane);
+            warp_pick_digit(coarse, need, d, lane);
+            prefix = d << 24;
+            pmask = 0xFF000000u;
+        }
+        // the digits below the coarse bin: bits 23..16 (23 and 22 already fixed), 15..8, 7..0
+        warp_digit_hist(src, lo, hi, pmask, prefix, 16, coarse, lane);
+        warp_pick_digit(coarse, need, d, lane);
+        prefix |= d << 16;
+        pmask = 0xFFFF0000u;
+        warp_digit_hist(src, lo, hi, pmask, prefix, 8, coarse, lane);
+        warp_pick_digit(coarse, need, d, lane);
+        prefix |= d << 8;
+        pmask = 0xFFFFFF00u;
+        warp_digit_hist(src, lo, hi, pmask, prefix, 0, coarse, lane);
+        warp_pick_digit(coarse, need, d, lane);
+        prefix |= d;
+    }
+    // ascending compaction: B_init, B_local, keys above the k-th, and the first `need`
+    // keys equal to it in block order (four chunks of 32 loaded ahead)
+    int pos0 = 0, eq_seen = 0;
+    bool overflow = false;
+    for (int jb = 0; jb < nb; jb += 128) {
+        uint32_t kv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int j = jb + 32 * u + lane;
+            kv[u] = (j < nb && j >= n_init && j < nb - n_local) ? keys[j] : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int j = jb + 32 * u + lane;
+            bool sel = false, eq = false;
+            if (j < nb) {
+                if (j < n_init || j >= nb - n_local)
+                    sel = true;
+                else if (take_all)
+                    sel = true;
+                else if (!take_none) {
+                    sel = kv[u] > prefix;
+                    eq = kv[u] == prefix;
+                }
+            }
+            const unsigned em = __ballot_sync(0xffffffffu, eq);
+            if (eq)
+                sel = eq_seen + __popc(em & lt) < need;
+            eq_seen += __popc(em);
+            const unsigned sm = __ballot_sync(0xffffffffu, sel);
+            if (sel) {
+                const int pos = pos0 + __popc(sm & lt);
+                if (pos < k_tot)
+                    out[pos] = j;
+                else
+                    overflow = true;
+            }
+            pos0 += __popc(sm);
+        }
+    }
+    if (__any_sync(0xffffffffu, overflow) && lane == 0)
+        report(status, SPARSE_ERR_BAD_INDEX);
+    for (int i = pos0 + lane; i < k_tot; i += 32)
+        out[i] = -1;
+    if (lane == 0)
+        *count_out = min(pos0, k_tot);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kFThreads, 2)
+    decode_forecast_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                           const AttnParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t *base = smem_raw + (base_s - raw_s);
+    int *ctrl = reinterpret_cast<int *>(base + kOffCtrl);
+    const uint32_t bar_full = base_s + kOffBars;
+    const uint32_t bar_empty = base_s + kOffBars + 8 * kStages;
+    const uint32_t bar_scored = base_s + kOffCtrl + 4 * kCtrlScoredBar;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const uint32_t S = gridDim.x;       // the cluster spans gridDim.x
+    const uint32_t rank = blockIdx.x;   // == %cluster_ctarank
+    const int pair = blockIdx.y;
+    const int b = pair / p.H_kv, g = pair % p.H_kv;
+    const int per = (p.k_tot + static_cast<int>(S) - 1) / static_cast<int>(S);
+    const int i0 = min(p.k_tot, static_cast<int>(rank) * per);
+    const int cap = min(p.k_tot, i0 + per) - i0;
+    int *lslot = reinterpret_cast<int *>(base + fused_off_slice());
+    int *llog = lslot + fused_per_pad(per);
+    uint32_t *keys = reinterpret_cast<uint32_t *>(base + fused_off_keys(per));
+    uint32_t *hist = reinterpret_cast<uint32_t *>(base + fused_off_hist());
+
+    // The next layer's rows: seq_len and its compressed keys are complete before the
+    // kernel before this one finishes (the caller's promise), so they are read at once.
+    const bool do_sel = p.F != nullptr;
+    const long long len = p.seq_len[b];
+    long long nb_ll = len <= 0 ? 0 : (len + kBlk - 1) / kBlk;
+    const bool len_bad = nb_ll > p.N_cap;
+    if (len_bad)
+        nb_ll = p.N_cap;
+    const int nb = static_cast<int>(nb_ll);
+    const bool take_all = max(0, nb - p.n_local - p.n_init) <= p.k_sel;
+    const bool score = do_sel && !take_all;
+    const int chunk = (nb + static_cast<int>(S) - 1) / static_cast<int>(S);
+    const int r0 = score ? min(nb, static_cast<int>(rank) * chunk) : 0;
+    const int n_krows = score ? min(nb, r0 + chunk) - r0 : 0;
+    const int n_kst = (n_krows + kKtilRowsPerStage - 1) / kKtilRowsPerStage;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, kConsumerWarps);
+        }
+        mbar_init(bar_scored, S * kConsumerWarps);
+        fence_barrier_init();
+    }
+    if (rank == 0 && score)
+        for (int i = tid; i < kCoarseBins; i += kFThreads)
+            hist[i] = 0u;
+    __syncthreads();
+    cluster_arrive();              // every thread; waited before the first access to CTA 0
+    griddep_launch_dependents();   // the next layer may start its key stream as SMs free up
+
+    WarpState<NT> st;
+    st.reset();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        int failed = 0;
+        const uint64_t pol = policy_evict_first();
+        int it = 0;
+        if (lane == 0) {
+            const float *kt = p.ktil + (static_cast<size_t>(pair) * p.N_cap + r0) * kD;
+            for (int ks = 0; ks < n_kst; ++ks, ++it) {
+                const int s = it % kStages;
+                const int use = it / kStages;
+                if (use > 0 && !mbar_wait(bar_empty + 8 * s, (use - 1) & 1, kWaitNs)) {
+                    report(p.status, SPARSE_ERR_TIMEOUT);
+                    failed = 1;
+                    break;
+                }
+                const int rows = min(kKtilRowsPerStage, n_krows - ks * kKtilRowsPerStage);
+                const uint32_t bytes = static_cast<uint32_t>(rows * kKtilRowBytes);
+                mbar_arrive_expect_tx(bar_full + 8 * s, bytes);
+                bulk_load(base_s + s * kStageBytes, kt + static_cast<size_t>(ks) * kKtilRowsPerStage * kD, bytes,
+                          bar_full + 8 * s, pol);
+            }
+        }
+        failed = __shfl_sync(0xffffffffu, failed, 0);
+        it = __shfl_sync(0xffffffffu, it, 0);
+        // this layer's block list may be the previous kernel's output
+        if ((p.flags & SPARSE_ATTN_BLOCKS_READY) == 0u)
+            griddep_wait();
+        int c = lane == 0 ? p.count[pair] : 0;
+        for (int i = lane; i < cap; i += 32) {
+            const int logical = p.blk_logical[static_cast<size_t>(pair) * p.k_tot + i0 + i];
+            llog[i] = logical;
+            lslot[i] = logical;
+        }
+        c = __shfl_sync(0xffffffffu, c, 0);
+        if (c < 0 || c > p.k_tot) {
+            if (lane == 0)
+                report(p.status, SPARSE_ERR_BAD_INDEX);
+            c = c < 0 ? 0 : p.k_tot;
+        }
+        const int my_n = max(0, min(cap, c - i0));
+        for (int i = lane; i < my_n; i += 32) {
+            const int logical = llog[i];
+            const bool ok = logical >= 0 && static_cast<long long>(logical) * kBlk < p.pair_stride;
+            if (!ok) {
+                report(p.status, SPARSE_ERR_BAD_INDEX);
+                llog[i] = -1;
+                lslot[i] = -1;
+            }
+        }
+        const int n_run = failed ? 0 : my_n;
+        if (lane == 0) {
+            ctrl[kCtrlAbort] = 0;
+            ctrl[kCtrlList] = n_run;
+        }
+        __syncwarp();
+        named_barrier_arrive(1, kAttnThreads);
+        if (lane == 0 && n_run > 0) {
+            prefetch_tensormap(&kmap);
+            prefetch_tensormap(&vmap);
+            for (int i = 0; i < n_run; ++i, ++it) {
+                const int s = it % kStages;
+                const int use = it / kStages;
+                if (use > 0 && !mbar_wait(bar_empty + 8 * s, (use - 1) & 1, kWaitNs)) {
+                    report(p.status, SPARSE_ERR_TIMEOUT);
+                    break;
+                }
+                const int slot = lslot[i];
+                const int row = slot >= 0 ? slot * kBlk : static_cast<int>(min(p.pair_stride, (long long)INT_MAX - kBlk));
+                const uint32_t dst = base_s + s * kStageBytes;
+                mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
+                tma_load_3d(dst, &kmap, bar_full + 8 * s, 0, row, pair, pol);
+                tma_load_3d(dst + kHalfBytes, &kmap, bar_full + 8 * s, 64, row, pair, pol);
+                tma_load_3d(dst + kTileBytes, &vmap, bar_full + 8 * s, 0, row, pair, pol);
+                tma_load_3d(dst + kTileBytes + kHalfBytes, &vmap, bar_full + 8 * s, 64, row, pair, pol);
+            }
+        }
+        cluster_wait();
+    } else if (warp < kConsumerWarps) {
+        // ------------------------------------------------------------ consumers
+        griddep_wait();   // Q and F may be written by the kernel before this one
+        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (score) {
+            const uint2 fr = *reinterpret_cast<const uint2 *>(p.F + static_cast<size_t>(pair) * kD + 4 * lane);
+            const float2 f01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&fr.x));
+            const float2 f23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&fr.y));
+            f = make_float4(f01.x, f01.y, f23.x, f23.y);
+        }
+        QueryFrags<NT> q;
+        load_query<NT, false>(q, p, b, g, 0, p.G, lane);
+        cluster_wait();   // CTA 0's "scored" barrier and key array exist
+        uint32_t *keys0 = static_cast<uint32_t *>(__cluster_map_shared_rank(keys, 0));
+        uint32_t *coarse0 = static_cast<uint32_t *>(__cluster_map_shared_rank(hist, 0));
+        // (1) the next layer's scores, order keys into CTA 0
+        int it = 0;
+        bool ok = true;
+        for (int ks = 0; ks < n_kst; ++ks, ++it) {
+            const int s = it % kStages;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8 * s, (it / kStages) & 1, kWaitNs))) {
+                if (lane == 0)
+                    report(p.status, SPARSE_ERR_TIMEOUT);
+                ok = false;
+                break;
+            }
+            const int rows = min(kKtilRowsPerStage, n_krows - ks * kKtilRowsPerStage);
+            const int nrow = min(16, rows - warp * 16);   // this warp's rows of the stage
+            if (nrow > 0) {
+                const float *stage = reinterpret_cast<const float *>(base + s * kStageBytes) + warp * 16 * kD;
+                // lane l's partial dot product (dims 4l .. 4l+3) for each of the 16 rows
+                float acc[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    const float4 v = r < nrow ? reinterpret_cast<const float4 *>(stage + r * kD)[lane]
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                    float sc = f.x * v.x;
+                    sc = fmaf(f.y, v.y, sc);
+                    sc = fmaf(f.z, v.z, sc);
+                    sc = fmaf(f.w, v.w, sc);
+                    acc[r] = sc;
+                }
+                // transposed butterfly: after the exchanges at distances 16, 8, 4, 2 lane l
+                // holds row (l >> 1) & 15 summed over the 16 lanes that differ from it in
+                // bits 1-4; distance 1 completes it (the same pairwise sums, in the same
+                // tree, as a per-row xor reduction over 16, 8, 4, 2, 1)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const bool up = (lane & 16) != 0;
+                    const float give = up ? acc[i] : acc[i + 8];
+                    const float keep = up ? acc[i + 8] : acc[i];
+                    acc[i] = keep + __shfl_xor_sync(0xffffffffu, give, 16);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const bool up = (lane & 8) != 0;
+                    const float give = up ? acc[i] : acc[i + 4];
+                    const float keep = up ? acc[i + 4] : acc[i];
+                    acc[i] = keep + __shfl_xor_sync(0xffffffffu, give, 8);
+                }
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const bool up = (lane & 4) != 0;
+                    const float give = up ? acc[i] : acc[i + 2];
+                    const float keep = up ? acc[i + 2] : acc[i];
+                    acc[i] = keep + __shfl_xor_sync(0xffffffffu, give, 4);
+                }
+                {
+                    const bool up = (lane & 2) != 0;
+                    const float give = up ? acc[0] : acc[1];
+                    const float keep = up ? acc[1] : acc[0];
+                    acc[0] = keep + __shfl_xor_sync(0xffffffffu, give, 2);
+                }
+                acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 1);
+                const int r = (lane >> 1) & 15;
+                const bool own = (lane & 1) == 0 && r < nrow;
+                const int j = r0 + ks * kKtilRowsPerStage + warp * 16 + r;
+                const uint32_t key = order_key(acc[0]);
+                if (own)
+                    keys0[j] = key;
+                // coarse histogram of the candidates, one atomic per distinct bin
+                const bool cand = own && j >= p.n_init && j < nb - p.n_local;
+                const uint32_t bin = cand ? key >> kCoarseShift : 0xFFFFFFFFu;
+                const uint32_t same = __match_any_sync(0xffffffffu, bin);
+                if (cand && lane == __ffs(same) - 1)
+                    atomicAdd(coarse0 + bin, static_cast<uint32_t>(__popc(same)));
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar_empty + 8 * s);
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive_cluster(dsmem_addr(bar_scored, 0));
+        // (2) this layer's attention over the staged slice of its block list
+        named_barrier_sync(1, kAttnThreads);
+        const int n_run = ok ? ctrl[kCtrlList] : 0;
+        for (int i = 0; i < n_run; ++i, ++it) {
+            const int s = it % kStages;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8 * s, (it / kStages) & 1, kWaitNs))) {
+                if (lane == 0)
+                    report(p.status, SPARSE_ERR_TIMEOUT);
+                break;
+            }
+            const int logical = llog[i];
+            const long long tok0 = static_cast<long long>(logical) * kBlk + warp * 16;
+            if (logical >= 0 && tok0 < len)
+                attend_block<NT, false>(st, q, base_s + s * kStageBytes, tok0, len, 0xffffffffu, p.scale_log2, warp,
+                                        lane);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar_empty + 8 * s);
+        }
+        finish_row_sums<NT>(st);
+    } else {
+        // ------------------------------------------------------------ selector (CTA 0)
+        if (rank == 0 && do_sel) {
+            if (len_bad && lane == 0)
+                report(p.status, SPARSE_ERR_BAD_INDEX);
+            bool ready = true;
+            if (score)
+                ready = __all_sync(0xffffffffu, mbar_wait_cluster(bar_scored, 0, kWaitNs));
+            if (ready) {
+                topk_warp(keys, hist, reinterpret_cast<uint32_t *>(base + fused_off_topk_list()), nb, p.n_init,
+                          p.n_local, p.k_sel,
+                          p.idx_next + static_cast<size_t>(pair) * p.k_tot_next, p.k_tot_next, p.count_next + pair,
+                          p.status, lane);
+            } else if (lane == 0) {
+                report(p.status, SPARSE_ERR_TIMEOUT);
+            }
+        }
+        cluster_wait();
+    }
+
+    // ---------------------------------------------------------------- merge
+    __syncthreads();
+    cluster_merge_write<NT, false>(st, base, false, p, b, g, 0, p.G, rank, S, kFThreads);
+}
+
+// The "scored" barrier lives in the ctrl words, 8-byte aligned.
+static_assert((kOffCtrl + 4 * kCtrlScoredBar) % 8 == 0 && 4 * kCtrlScoredBar + 8 <= 64, "ctrl layout");
+
+template <int NT>
+int launch_fused(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, int S, long long pairs,
+                 size_t smem, int device, cudaStream_t stream)
+{
+    auto kern = decode_forecast_kernel<NT>;
+    static int configured[64];
+    int rc = sp_host::configure_kernel(reinterpret_cast<const void *>(kern), static_cast<int>(smem), device,
+                                       configured);
+    if (rc != SPARSE_OK)
+        return rc;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(S), static_cast<unsigned>(pairs), 1);
+    cfg.blockDim = dim3(kFThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    CUtensorMap kmap = km, vmap = vm;
+    AttnParams prm = p;
+    void *args[] = {&kmap, &vmap, &prm};
+    return sp_host::cuda_status(cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(kern), args),
+                                "sparse_decode_attn_forecast launch");
+}
+
+}  // namespace
+
+extern "C" SPARSE_API int sparse_decode_attn_forecast(
+    const uint16_t *Q, const uint16_t *k_cache, const uint16_t *v_cache, long long T_cap, const int *blk_idx,
+    const int *count, int k_tot, const int *seq_len, int B, int H_q, int H_kv, float scale, uint16_t *O, float *lse,
+    const uint16_t *F, const float *ktil_next, int N_cap, int n_init, int n_local, int k, int *idx_next,
+    int *count_next, int k_tot_next, int n_split, unsigned flags, int *status, void *stream)
+{
+    using sp_host::aligned16;
+    using sp_host::fail;
+    if (!Q || !k_cache || !v_cache || !blk_idx || !count || !seq_len || !O)
+        return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn_forecast: null pointer");
+    if (!aligned16(Q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(O))
+        return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn_forecast: Q, K, V and O must be 16-byte aligned");
+    if (B < 1 || H_kv < 1 || H_q < H_kv || H_q % H_kv != 0 || k_tot < 1 || T_cap < 1)
+        return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn_forecast: bad size (B=%d H_q=%d H_kv=%d k_tot=%d)",
+                    B, H_q, H_kv, k_tot);
+    if (T_cap > INT_MAX - 2 * kBlk)
+        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn_forecast: T_cap too large");
+    if (!isfinite(scale))
+        return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn_forecast: scale must be finite");
+    const int G = H_q / H_kv;
+    if (G > 16)
+        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn_forecast: G=%d > 16", G);
+    const long long pairs = static_cast<long long>(B) * H_kv;
+    if (pairs > 65535)
+        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn_forecast: B*H_kv=%lld > 65535", pairs);
+    if ((flags & ~SPARSE_ATTN_BLOCKS_READY) != 0u)
+        return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn_forecast: unknown flags 0x%x", flags);
+    const bool do_sel = F != nullptr;
+    if (do_sel) {
+        if (!ktil_next || !idx_next || !count_next)
+            return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn_forecast: F given without ktil_next, idx_next "
+                        "or count_next");
+        if (!aligned16(F) || !aligned16(ktil_next))
+            return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn_forecast: F and ktil_next must be 16-byte aligned");
+        if (N_cap < 1 || n_init < 0 || n_local < 0 || k < 0)
+            return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn_forecast: bad selection size");
+        if (static_cast<long long>(n_init) + n_local + k > k_tot_next)
+            return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn_forecast: k_tot_next=%d < n_init+n_local+k",
+                        k_tot_next);
+    } else {
+        N_cap = 0;
+    }
+    sp_host::DeviceInfo dev;
+    int rc = sp_host::device_info(&dev);
+    if (rc != SPARSE_OK)
+        return rc;
+    int S;
+    if ((rc = choose_split(n_split, pairs, k_tot, dev.sm_count, &S)) != SPARSE_OK)
+        return rc;
+    const int per = (k_tot + S - 1) / S;
+    if (per > kMaxListCta)
+        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn_forecast: %d blocks per CTA (at most %d)", per,
+                    kMaxListCta);
+    const size_t smem = fused_smem_bytes(per, N_cap);
+    if (smem > static_cast<size_t>(dev.max_smem_optin))
+        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn_forecast: N_cap=%d needs %zu bytes of shared memory",
+                    N_cap, smem);
+    AttnParams p = {};
+    p.Q = Q;
+    p.O = O;
+    p.lse = lse;
+    p.blk_logical = blk_idx;
+    p.count = count;
+    p.seq_len = seq_len;
+    p.status = status;
+    p.pair_stride = T_cap;
+    p.k_tot = k_tot;
+    p.H_q = H_q;
+    p.H_kv = H_kv;
+    p.G = G;
+    p.n_groups = 1;
+    p.flags = flags;
+    p.scale_log2 = scale_log2_of(scale);
+    p.F = F;
+    p.ktil = ktil_next;
+    p.idx_next = idx_next;
+    p.count_next = count_next;
+    p.N_cap = N_cap;
+    p.n_init = n_init;
+    p.n_local = n_local;
+    p.k_sel = k;
+    p.k_tot_next = k_tot_next;
+    CUtensorMap km, vm;
+    if ((rc = sp_host::make_kv_tensor_map(&km, k_cache, T_cap, pairs)) != SPARSE_OK)
+        return rc;
+    if ((rc = sp_host::make_kv_tensor_map(&vm, v_cache, T_cap, pairs)) != SPARSE_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return G <= 8 ? launch_fused<1>(p, km, vm, S, pairs, smem, dev.device, st)
+                  : launch_fused<2>(p, km, vm, S, pairs, smem, dev.device, st);
+}

@@ -45,16 +45,6 @@ struct SelectParams {
     int k_tot;
 };
 
-// Monotone map of a float score to an unsigned key (larger score -> larger key);
-// -0 and +0 share a key.
-__device__ __forceinline__ uint32_t order_key(float s)
-{
-    uint32_t u = __float_as_uint(s);
-    if (u == 0x80000000u)
-        u = 0u;
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
 // Inclusive prefix sum over the CTA's threads (thread order); `total` receives the sum.
 __device__ __forceinline__ int block_inclusive_scan(int v, int *warp_sums, int &total)
 {
@@ -119,9 +109,10 @@ __global__ void __launch_bounds__(kThreads, 3) select_topk_kernel(const SelectPa
     const int cand_lo = p.n_init;
     const int cand_hi = nb - p.n_local;
     const bool take_all = max(0, cand_hi - cand_lo) <= p.k;
+    const bool take_none = p.k <= 0;   // only B_init and B_local
 
     // ---- 1. scores s_j = F . ktil_j (fp32) as order keys, stored into CTA 0
-    if (!take_all && j1 > j0) {
+    if (!take_all && !take_none && j1 > j0) {
         uint32_t *keys0 = static_cast<uint32_t *>(__cluster_map_shared_rank(keys, 0));
         const uint2 fr = *reinterpret_cast<const uint2 *>(p.F + static_cast<size_t>(pair) * kD + 4 * lane);
         const float2 f01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&fr.x));
@@ -160,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 3) select_topk_kernel(const SelectPa
     // ---- 2. CTA 0: k-th largest candidate key by MSB-first radix select
     uint32_t prefix = 0, pmask = 0;
     int need = p.k;
-    if (!take_all) {
+    if (!take_all && !take_none) {
         for (int pass = 0; pass < 4; ++pass) {
             const int shift = 24 - 8 * pass;
             hist[tid] = 0;
@@ -204,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 3) select_topk_kernel(const SelectPa
     const int ipt = (nb + kThreads - 1) / kThreads;
     const int it0 = min(nb, tid * ipt), it1 = min(nb, it0 + ipt);
     int n_eq = 0;
-    if (!take_all)
+    if (!take_all && !take_none)
         for (int j = it0; j < it1; ++j)
             n_eq += (j >= cand_lo && j < cand_hi && keys[j] == thr);
     int total_eq;
@@ -213,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 3) select_topk_kernel(const SelectPa
     int eq_rank = eq_before;
     for (int j = it0; j < it1; ++j) {
         bool sel = j < p.n_init || j >= nb - p.n_local;        // B_init and B_local
-        if (!sel && j >= cand_lo && j < cand_hi) {
+        if (!sel && !take_none && j >= cand_lo && j < cand_hi) {
             if (take_all) {
                 sel = true;
             } else {
@@ -230,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 3) select_topk_kernel(const SelectPa
     bool overflow = false;
     for (int j = it0; j < it1; ++j) {
         bool sel = j < p.n_init || j >= nb - p.n_local;
-        if (!sel && j >= cand_lo && j < cand_hi) {
+        if (!sel && !take_none && j >= cand_lo && j < cand_hi) {
             if (take_all) {
                 sel = true;
             } else {

@@ -42,325 +42,11 @@
 
 #include "common.cuh"
 
+#include "attn_core.cuh"
+
 namespace {
 
 using namespace sp;
-
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 3;
-constexpr int kHalfBytes = kBlk * 64 * 2;       // 64 tokens x 64 dims of bf16: one TMA box
-constexpr int kTileBytes = 2 * kHalfBytes;      // one block of K (or V): 16 KB
-constexpr int kStageBytes = 2 * kTileBytes;     // K + V of one block: 32 KB
-constexpr int kMaxUnion = 512;
-constexpr int kMaxSplit = 8;
-constexpr uint64_t kWaitNs = 2000000000ull;
-
-// Dynamic shared memory layout, offsets from a 1024-byte aligned base.
-constexpr int kOffBars = kStages * kStageBytes;          // full[kStages], empty[kStages]
-constexpr int kOffCtrl = kOffBars + 2 * kStages * 8;     // int ctrl[16]
-constexpr int kOffList = kOffCtrl + 64;                  // verification: int ulist[kMaxUnion]
-constexpr int kOffMask = kOffList + kMaxUnion * 4;       // uint32 umask[kMaxUnion]
-constexpr int kOffEntV = kOffMask + kMaxUnion * 4;       // union build scratch
-constexpr int kOffEntM = kOffEntV + kMaxUnion * 4;
-constexpr int kOffEntF = kOffEntM + kMaxUnion * 4;
-constexpr int kMaxListCta = kMaxUnion;                   // decode: staged slice of the block list
-constexpr int kSmemDecode = kOffList + 2 * kMaxListCta * 4 + 1024;
-constexpr int kSmemVerify = kOffEntF + kMaxUnion * 4 + 1024;
-// stream-K decode: the list of the CTA's range, its segment table and merge rows
-constexpr int kMaxSegs = kMaxListCta + 2;
-constexpr int kOffSegs = kOffList + 2 * kMaxListCta * 4;          // seg_nv[kMaxSegs], seg_start[kMaxSegs]
-constexpr int kMaxMergeSeg = 64;                                  // CTAs sharing one pair, at most
-constexpr int kOffRowML = kOffSegs + 2 * kMaxSegs * 4;            // row max / sum of a pair merge
-constexpr int kOffMergeFac = kOffRowML + 2 * 16 * 4;              // [kMaxMergeSeg][8] weights (NT = 1)
-constexpr int kOffMergeSlot = kOffMergeFac + 2 * kMaxMergeSeg * 8 * 4;   // [kMaxMergeSeg] slot offsets
-constexpr int kSmemStreamK = kOffMergeSlot + kMaxMergeSeg * 4 + 1024;
-enum { kCtrlLast = 2, kCtrlMergeValid = 3 };
-
-enum { kCtrlAbort = 0, kCtrlList = 1 };
-
-struct AttnParams {
-    const uint16_t *Q;
-    uint16_t *O;
-    float *lse;
-    const int *blk_slot;
-    const int *blk_logical;
-    const int *count;
-    const int *seq_len;
-    int *status;
-    const int *idx_q;
-    long long *blocks_loaded;
-    const unsigned *ready_flag;
-    long long pair_stride;
-    long long timeout_ns;
-    unsigned ready_target;
-    int k_tot;
-    int H_q;
-    int H_kv;
-    int G;
-    int n_sel;
-    int N_q;
-    int C;
-    int window_blocks;
-    int n_groups;
-    unsigned flags;
-    float scale_log2;
-    // stream-K decode
-    float *ws_part;        // [2 * n_ctas][ROWS * 128 + 2 * ROWS] partial states
-    int *ws_count;         // [pairs] arrival counters, zero between calls
-    long long n_items;     // pairs * k_tot
-};
-
-__device__ __forceinline__ uint32_t ld_b32(const uint16_t *p)
-{
-    return *reinterpret_cast<const uint32_t *>(p);
-}
-
-// Per-warp online-softmax state: the max and sum of rows 2*t4 and 2*t4+1 of every
-// n-tile (log2 units) and the O^T accumulators of the warp's MMA fragments.
-template <int NT>
-struct WarpState {
-    float m[NT][2], l[NT][2], acc[8][NT][4];
-
-    __device__ __forceinline__ void reset()
-    {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                m[nt][h] = -INFINITY;
-                l[nt][h] = 0.f;
-            }
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    acc[mt][nt][i] = 0.f;
-    }
-};
-
-// Q^T fragments (the B operand of S^T = K Q^T; row n = lane/4 of each n-tile) and the
-// validity / query index of the two rows this lane's softmax state covers.
-template <int NT>
-struct QueryFrags {
-    uint32_t qb[NT][8][2];
-    bool row_ok[NT][2];
-    int row_q[NT][2];
-};
-
-// Query rows of a unit: decode rows are the G heads of KV head g of batch b;
-// verification rows are (query q0 + r / G, head r % G).
-template <int NT, bool VERIFY>
-__device__ __forceinline__ void load_query(QueryFrags<NT> &q, const AttnParams &p, int b, int g, int q0,
-                                           int rows_valid, int lane)
-{
-    const int g8 = lane >> 2, t4 = lane & 3;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int row = nt * 8 + g8;
-        const uint16_t *qrow = nullptr;
-        if (row < rows_valid) {
-            if (VERIFY) {
-                const int qq = q0 + row / p.G, hh = row % p.G;
-                qrow = p.Q + ((static_cast<size_t>(b) * p.N_q + qq) * p.H_q + g * p.G + hh) * kD;
-            } else {
-                qrow = p.Q + (static_cast<size_t>(b) * p.H_q + g * p.G + row) * kD;
-            }
-        }
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            q.qb[nt][ks][0] = qrow ? ld_b32(qrow + 16 * ks + 2 * t4) : 0u;
-            q.qb[nt][ks][1] = qrow ? ld_b32(qrow + 16 * ks + 2 * t4 + 8) : 0u;
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int r = nt * 8 + 2 * t4 + h;
-            q.row_ok[nt][h] = r < rows_valid;
-            q.row_q[nt][h] = VERIFY ? (r < rows_valid ? r / p.G : 0) : 0;
-        }
-    }
-}
-
-// One consumer warp over tokens [16w, 16w+16) of the block held in ring stage `kst`
-// (K, 2 x 8 KB swizzled boxes) and `kst + kTileBytes` (V).  tok0 is the absolute
-// position of the warp's first token; qmask selects the rows' queries (verification).
-template <int NT, bool VERIFY>
-__device__ __forceinline__ void attend_block(WarpState<NT> &st, const QueryFrags<NT> &q, uint32_t kst, long long tok0,
-                                             long long len, uint32_t qmask, float scale_log2, int w, int lane)
-{
-    const int g8 = lane >> 2;
-    const int jm = lane >> 3, rr = lane & 7;
-    const int a_tok = w * 16 + (jm & 1) * 8 + rr;   // K rows for ldmatrix (QK A operand)
-    const int v_tok = w * 16 + (jm >> 1) * 8 + rr;  // V rows for ldmatrix.trans (PV A operand)
-    const uint32_t a_sw = static_cast<uint32_t>(a_tok & 7);
-    const uint32_t v_sw = static_cast<uint32_t>(v_tok & 7);
-    const uint32_t vst = kst + kTileBytes;
-    float sacc[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            sacc[nt][i] = 0.f;
-    // S^T (16 tokens x 8*NT rows) = K (16 x 128) Q^T (128 x 8*NT)
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t chunk = static_cast<uint32_t>(((ks & 3) << 1) + (jm >> 1));
-        const uint32_t addr = kst + (ks >> 2) * kHalfBytes + a_tok * 128 + ((chunk ^ a_sw) << 4);
-        uint32_t a[4];
-        ldsm_x4(addr, a);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-            mma_bf16_16816(sacc[nt], a, q.qb[nt][ks][0], q.qb[nt][ks][1]);
-    }
-    // scale to log2 units, mask tokens past the length and rows not selecting the block
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int h = i & 1;
-            const long long tok = tok0 + g8 + (i >> 1) * 8;
-            bool keep = tok < len && q.row_ok[nt][h];
-            if (VERIFY)
-                keep = keep && ((qmask >> q.row_q[nt][h]) & 1u);
-            sacc[nt][i] = keep ? sacc[nt][i] * scale_log2 : -INFINITY;
-        }
-    // online softmax per row (the 8 lanes sharing t4 hold one row's 16 tokens)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            float mx = fmaxf(sacc[nt][h], sacc[nt][h + 2]);
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float m_new = fmaxf(st.m[nt][h], mx);
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            const float alpha = exp2f(st.m[nt][h] - m_use);
-            const float p0 = exp2f(sacc[nt][h] - m_use);
-            const float p1 = exp2f(sacc[nt][h + 2] - m_use);
-            st.l[nt][h] = st.l[nt][h] * alpha + p0 + p1;
-            st.m[nt][h] = m_new;
-            sacc[nt][h] = p0;
-            sacc[nt][h + 2] = p1;
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                st.acc[mt][nt][h] *= alpha;
-                st.acc[mt][nt][h + 2] *= alpha;
-            }
-        }
-    // P^T as the B operand: transpose the bf16 (token, row) 8x8 tiles in registers
-    uint32_t pb[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        pb[nt][0] = movmatrix_trans(pack_bf16x2(sacc[nt][0], sacc[nt][1]));
-        pb[nt][1] = movmatrix_trans(pack_bf16x2(sacc[nt][2], sacc[nt][3]));
-    }
-    // O^T (128 dims x rows) += V^T (128 x 16 tokens) P^T (16 x rows)
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-        const uint32_t chunk = static_cast<uint32_t>(((mt & 3) << 1) + (jm & 1));
-        const uint32_t addr = vst + (mt >> 2) * kHalfBytes + v_tok * 128 + ((chunk ^ v_sw) << 4);
-        uint32_t a[4];
-        ldsm_x4_trans(addr, a);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-            mma_bf16_16816(st.acc[mt][nt], a, pb[nt][0], pb[nt][1]);
-    }
-}
-
-// Complete the row sums over the 8 lanes that share a row.
-template <int NT>
-__device__ __forceinline__ void finish_row_sums(WarpState<NT> &st)
-{
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            float l = st.l[nt][h];
-            l += __shfl_xor_sync(0xffffffffu, l, 4);
-            l += __shfl_xor_sync(0xffffffffu, l, 8);
-            l += __shfl_xor_sync(0xffffffffu, l, 16);
-            st.l[nt][h] = l;
-        }
-}
-
-// Warp `warp`'s state into shared memory: wo [4][ROWS][128], wm / wl [4][ROWS].
-template <int NT>
-__device__ __forceinline__ void store_warp_state(const WarpState<NT> &st, float *wo, float *wm, float *wl, int warp,
-                                                 int lane)
-{
-    constexpr int ROWS = 8 * NT;
-    const int g8 = lane >> 2, t4 = lane & 3;
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int dim = mt * 16 + g8 + (i >> 1) * 8;
-                const int row = nt * 8 + 2 * t4 + (i & 1);
-                wo[(warp * ROWS + row) * kD + dim] = st.acc[mt][nt][i];
-            }
-    if (g8 == 0) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = nt * 8 + 2 * t4 + h;
-                wm[warp * ROWS + row] = st.m[nt][h];
-                wl[warp * ROWS + row] = st.l[nt][h];
-            }
-    }
-}
-
-// Merge the 4 warp states (wo/wm/wl) into one CTA state: co [ROWS][128] unnormalised,
-// cm / cl [ROWS] its max and sum; wf [4][ROWS] scratch.  `t` / `nthreads` name the
-// participating threads; the caller synchronises them between the two phases through
-// `sync()`.
-template <int ROWS, typename Sync>
-__device__ __forceinline__ void merge_warp_states(const float *wo, const float *wm, const float *wl, float *wf,
-                                                  float *co, float *cm, float *cl, int t, int nthreads, Sync sync)
-{
-    if (t < ROWS) {
-        const int row = t;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w4 = 0; w4 < kConsumerWarps; ++w4)
-            M = fmaxf(M, wm[w4 * ROWS + row]);
-        float L = 0.f;
-#pragma unroll
-        for (int w4 = 0; w4 < kConsumerWarps; ++w4) {
-            const float mw = wm[w4 * ROWS + row];
-            const float f = (M == -INFINITY || mw == -INFINITY) ? 0.f : exp2f(mw - M);
-            wf[w4 * ROWS + row] = f;
-            L += f * wl[w4 * ROWS + row];
-        }
-        cm[row] = M;
-        cl[row] = L;
-    }
-    sync();
-    for (int item = t; item < ROWS * kD; item += nthreads) {
-        const int row = item / kD;
-        float o = 0.f;
-#pragma unroll
-        for (int w4 = 0; w4 < kConsumerWarps; ++w4)
-            o = fmaf(wf[w4 * ROWS + row], wo[w4 * ROWS * kD + item], o);
-        co[item] = o;
-    }
-}
-
-__device__ __forceinline__ void store_bf16(uint16_t *dst, float v)
-{
-    const __nv_bfloat16 ob = __float2bfloat16_rn(v);
-    *dst = *reinterpret_cast<const uint16_t *>(&ob);
-}
-
-__device__ __forceinline__ float lse_of(float M, float L)
-{
-    return L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
-}
 
 // Merged union of the group's block sets (SSV mode A): ulist ascending, umask[u] the
 // queries of the group whose set contains ulist[u].  Returns the union size.
@@ -602,108 +288,299 @@ __global__ void __launch_bounds__(kThreads, 2)
     // ---------------------------------------------------------------- merge
     // Every stage has been consumed; the ring memory now holds the partial states.
     // The next kernel on the stream may be scheduled from here on.
-    // (1) each consumer warp's state, (2) merged into this CTA's state in local shared
-    // memory, (3) after one cluster barrier, CTA r merges the S CTA states for its
-    // slice of output dims, reading its peers' shared memory with independent loads.
+    __syncthreads();
+    griddep_launch_dependents();
+    cluster_merge_write<NT, VERIFY>(st, base, aborted, p, b, g, q0, rows_valid, rank, S, kThreads);
+}
+
+// ---------------------------------------------------------------- split-KV decode, workspace merge
+//
+// CTA (r, p) of a (S, pairs) grid attends over slice r of pair p's block list, a
+// slice of ceil(k_tot / S) entries cut from the k_tot-long table (so the slice is
+// known before `count` arrives).  Its producer warp fetches the slice and the count in
+// one round trip and starts the TMA ring at once.  After the main loop the CTA merges
+// its 4 warp states, writes the CTA state (unnormalised O, row max and sum) to the
+// workspace and leaves; the CTA of the pair that arrives last merges the S states
+// (the online-softmax recurrence, applied to whole partial states) and writes O.
+// Early finishers free their SM for the next kernel instead of waiting on peers.
+
+constexpr int kMaxSplitWs = 64;
+
+template <int NT>
+__host__ __device__ constexpr int split_part_floats()
+{
+    return 8 * NT * kD + 2 * 8 * NT + 4;   // O [ROWS][128], m [ROWS], l [ROWS], header
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                        const AttnParams p)
+{
+    constexpr int ROWS = 8 * NT;
+    constexpr int PART = split_part_floats<NT>();
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t *base = smem_raw + (base_s - raw_s);
+    int *ctrl = reinterpret_cast<int *>(base + kOffCtrl);
+    const uint32_t bar_full = base_s + kOffBars;
+    const uint32_t bar_empty = base_s + kOffBars + 8 * kStages;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int S = static_cast<int>(gridDim.x);
+    const int rank = static_cast<int>(blockIdx.x);
+    const int pair = static_cast<int>(blockIdx.y);
+    const int b = pair / p.H_kv, g = pair % p.H_kv;
+    const bool early = (p.flags & SPARSE_ATTN_BLOCKS_READY) != 0u;
+    if (!early)
+        griddep_wait();
+    const int per = (p.k_tot + S - 1) / S;
+    const int i0 = min(p.k_tot, rank * per);
+    const int cap = min(p.k_tot, i0 + per) - i0;
+    int *lslot = reinterpret_cast<int *>(base + kOffList);
+    int *llog = lslot + kMaxListCta;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, kConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    WarpState<NT> st;
+    st.reset();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        // the count and the slice's entries are independent loads: one round trip
+        int c = lane == 0 ? p.count[pair] : 0;
+        for (int i = lane; i < cap; i += 32) {
+            const size_t at = static_cast<size_t>(pair) * p.k_tot + i0 + i;
+            const int logical = p.blk_logical[at];
+            llog[i] = logical;
+            lslot[i] = p.blk_slot != nullptr ? p.blk_slot[at] : logical;
+        }
+        c = __shfl_sync(0xffffffffu, c, 0);
+        if (c < 0 || c > p.k_tot) {
+            if (lane == 0)
+                report(p.status, SPARSE_ERR_BAD_INDEX);
+            c = c < 0 ? 0 : p.k_tot;
+        }
+        const int my_n = max(0, min(cap, c - i0));
+        // each lane re-checks the entries it wrote; -1 = skip (an out-of-range box is
+        // loaded, never a fault)
+        for (int i = lane; i < my_n; i += 32) {
+            const int logical = llog[i], slot = lslot[i];
+            const bool ok = logical >= 0 && slot >= 0 && static_cast<long long>(slot) * kBlk < p.pair_stride;
+            if (!ok) {
+                report(p.status, SPARSE_ERR_BAD_INDEX);
+                llog[i] = -1;
+                lslot[i] = -1;
+            }
+        }
+        int aborted = 0;
+        if (lane == 0 && p.ready_flag != nullptr) {
+            bool ok = false;
+            const uint64_t t0 = globaltimer();
+            for (uint32_t it = 0; it < (1u << 26); ++it) {
+                unsigned v;
+                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p.ready_flag) : "memory");
+                if (v >= p.ready_target) {
+                    ok = true;
+                    break;
+                }
+                if (p.timeout_ns <= 0 || globaltimer() - t0 > static_cast<uint64_t>(p.timeout_ns))
+                    break;
+                __nanosleep(256);
+            }
+            if (!ok) {
+                aborted = 1;
+                report(p.status, p.timeout_ns > 0 ? SPARSE_ERR_TIMEOUT : SPARSE_ERR_NOT_READY);
+            }
+        }
+        aborted = __shfl_sync(0xffffffffu, aborted, 0);
+        const int n_run = aborted ? 0 : my_n;
+        if (lane == 0) {
+            ctrl[kCtrlAbort] = aborted;
+            ctrl[kCtrlList] = n_run;
+        }
+        __syncwarp();
+        named_barrier_arrive(1, kThreads);   // the list and its length are in shared memory
+        if (lane == 0 && n_run > 0) {
+            prefetch_tensormap(&kmap);
+            prefetch_tensormap(&vmap);
+            const uint64_t pol = policy_evict_first();
+            for (int it = 0; it < n_run; ++it) {
+                const int s = it % kStages;
+                const int use = it / kStages;
+                if (use > 0 && !mbar_wait(bar_empty + 8 * s, (use - 1) & 1, kWaitNs)) {
+                    report(p.status, SPARSE_ERR_TIMEOUT);
+                    break;
+                }
+                const int slot = lslot[it];
+                const int row = slot >= 0 ? slot * kBlk : static_cast<int>(min(p.pair_stride, (long long)INT_MAX - kBlk));
+                const uint32_t dst = base_s + s * kStageBytes;
+                mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
+                tma_load_3d(dst, &kmap, bar_full + 8 * s, 0, row, pair, pol);
+                tma_load_3d(dst + kHalfBytes, &kmap, bar_full + 8 * s, 64, row, pair, pol);
+                tma_load_3d(dst + kTileBytes, &vmap, bar_full + 8 * s, 0, row, pair, pol);
+                tma_load_3d(dst + kTileBytes + kHalfBytes, &vmap, bar_full + 8 * s, 64, row, pair, pol);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ consumers
+        if (early)
+            griddep_wait();   // Q may be written by the kernel before this one
+        QueryFrags<NT> q;
+        load_query<NT, false>(q, p, b, g, 0, p.G, lane);
+        const long long len = p.seq_len[b];
+        named_barrier_sync(1, kThreads);
+        const int n_run = ctrl[kCtrlList];
+        for (int it = 0; it < n_run; ++it) {
+            const int s = it % kStages;
+            const bool landed = __all_sync(0xffffffffu, mbar_wait(bar_full + 8 * s, (it / kStages) & 1, kWaitNs));
+            if (!landed) {
+                if (lane == 0)
+                    report(p.status, SPARSE_ERR_TIMEOUT);
+                break;
+            }
+            const int logical = llog[it];
+            const long long tok0 = static_cast<long long>(logical) * kBlk + warp * 16;
+            if (logical >= 0 && tok0 < len)
+                attend_block<NT, false>(st, q, base_s + s * kStageBytes, tok0, len, 0xffffffffu, p.scale_log2,
+                                        warp, lane);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar_empty + 8 * s);
+        }
+        finish_row_sums<NT>(st);
+    }
+
+    // ---------------------------------------------------------------- merge
     __syncthreads();
     griddep_launch_dependents();
     float *wo = reinterpret_cast<float *>(base);                     // [4][ROWS][128]
     float *wm = wo + kConsumerWarps * ROWS * kD;                     // [4][ROWS]
-    float *wl = wm + kConsumerWarps * ROWS;                          // [4][ROWS]
-    float *wf = wl + kConsumerWarps * ROWS;                          // [4][ROWS] warp weights
+    float *wl = wm + kConsumerWarps * ROWS;
+    float *wf = wl + kConsumerWarps * ROWS;
     float *co = wf + kConsumerWarps * ROWS;                          // [ROWS][128] CTA state
     float *cm = co + ROWS * kD;                                      // [ROWS]
     float *cl = cm + ROWS;                                           // [ROWS]
-    int *cabort = reinterpret_cast<int *>(cl + ROWS);                // [4]
-    float *fac = reinterpret_cast<float *>(cabort + 4);              // [kMaxSplit][ROWS]
-    float *row_m = fac + kMaxSplit * ROWS;
-    float *row_l = row_m + ROWS;
+    float *sm = cl + ROWS;                                           // [kMaxSplitWs][ROWS] partial maxima
+    float *sl = sm + kMaxSplitWs * ROWS;                             // [kMaxSplitWs][ROWS] partial sums -> weights
+    float *rowml = sl + kMaxSplitWs * ROWS;                          // [2][ROWS]
     if (warp < kConsumerWarps)
         store_warp_state<NT>(st, wo, wm, wl, warp, lane);
-    if (tid == 0)
-        cabort[0] = aborted ? 1 : 0;
     __syncthreads();
     merge_warp_states<ROWS>(wo, wm, wl, wf, co, cm, cl, tid, kThreads, [] { __syncthreads(); });
-    cluster_sync();
-
-    // peers' CTA states (generic pointers into distributed shared memory)
-    const float *peer_co[kMaxSplit];
-    const float *peer_cm[kMaxSplit];
-    const float *peer_cl[kMaxSplit];
-    int any_abort = 0;
-#pragma unroll
-    for (int c = 0; c < kMaxSplit; ++c) {
-        const unsigned r = c < static_cast<int>(S) ? static_cast<unsigned>(c) : 0u;
-        peer_co[c] = static_cast<const float *>(__cluster_map_shared_rank(co, r));
-        peer_cm[c] = static_cast<const float *>(__cluster_map_shared_rank(cm, r));
-        peer_cl[c] = static_cast<const float *>(__cluster_map_shared_rank(cl, r));
-        const int ab = *static_cast<const int *>(__cluster_map_shared_rank(cabort, r));
-        any_abort |= c < static_cast<int>(S) ? ab : 0;
-    }
-
-    // any CTA of the unit that failed its ready check leaves the output untouched
-    if (!any_abort) {
+    __syncthreads();
+    const float aborted_f = ctrl[kCtrlAbort] != 0 ? 1.f : 0.f;
+    float *ws_pair = p.ws_part + static_cast<size_t>(pair) * S * PART;
+    if (S > 1) {
+        float *part = ws_pair + static_cast<size_t>(rank) * PART;
+        for (int q4 = tid; q4 < ROWS * kD / 4; q4 += kThreads)
+            __stcg(reinterpret_cast<float4 *>(part) + q4, reinterpret_cast<const float4 *>(co)[q4]);
         if (tid < ROWS) {
-            const int row = tid;
-            float mc[kMaxSplit], lc[kMaxSplit];
-#pragma unroll
-            for (int c = 0; c < kMaxSplit; ++c) {
-                mc[c] = c < static_cast<int>(S) ? peer_cm[c][row] : -INFINITY;
-                lc[c] = c < static_cast<int>(S) ? peer_cl[c][row] : 0.f;
-            }
-            float M = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kMaxSplit; ++c)
-                M = fmaxf(M, mc[c]);
-            float L = 0.f;
-#pragma unroll
-            for (int c = 0; c < kMaxSplit; ++c) {
-                const float f = (M == -INFINITY || mc[c] == -INFINITY) ? 0.f : exp2f(mc[c] - M);
-                fac[c * ROWS + row] = f;
-                L += lc[c] * f;
-            }
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-            for (int c = 0; c < kMaxSplit; ++c)
-                fac[c * ROWS + row] *= inv;
-            row_m[row] = M;
-            row_l[row] = L;
+            __stcg(part + ROWS * kD + tid, cm[tid]);
+            __stcg(part + ROWS * kD + ROWS + tid, cl[tid]);
+        }
+        if (tid == 0)
+            __stcg(part + ROWS * kD + 2 * ROWS, aborted_f);
+        __syncthreads();
+        if (tid == 0) {
+            __threadfence();
+            const int prev = atomicAdd(p.ws_count + pair, 1);
+            const int last = prev == S - 1;
+            if (last)
+                atomicExch(p.ws_count + pair, 0);   // ready for the next call
+            ctrl[kCtrlLast] = last;
         }
         __syncthreads();
-        const int dims_per = kD / static_cast<int>(S);
-        const int d0 = static_cast<int>(rank) * dims_per;
-        for (int item = tid; item < rows_valid * dims_per; item += kThreads) {
-            const int row = item / dims_per;
-            const int d = d0 + (item - row * dims_per);
-            float v[kMaxSplit];
-#pragma unroll
-            for (int c = 0; c < kMaxSplit; ++c)
-                v[c] = c < static_cast<int>(S) ? peer_co[c][row * kD + d] : 0.f;
-            float o = 0.f;
-#pragma unroll
-            for (int c = 0; c < kMaxSplit; ++c)
-                o = fmaf(fac[c * ROWS + row], v[c], o);
-            size_t out;
-            if (VERIFY) {
-                const int qq = q0 + row / p.G, hh = row % p.G;
-                out = ((static_cast<size_t>(b) * p.N_q + qq) * p.H_q + g * p.G + hh) * kD + d;
-            } else {
-                out = (static_cast<size_t>(b) * p.H_q + g * p.G + row) * kD + d;
-            }
-            const __nv_bfloat16 ob = __float2bfloat16_rn(o);
-            p.O[out] = *reinterpret_cast<const uint16_t *>(&ob);
-        }
-        if (!VERIFY && rank == 0 && p.lse != nullptr) {
-            for (int row = tid; row < rows_valid; row += kThreads) {
-                const float L = row_l[row];
-                p.lse[static_cast<size_t>(b) * p.H_q + g * p.G + row] =
-                    L > 0.f ? (row_m[row] + log2f(L)) * 0.69314718055994530942f : -INFINITY;
-            }
+        if (!ctrl[kCtrlLast])
+            return;
+        __threadfence();
+    }
+    // the last CTA of the pair: row statistics of the S states, then the weighted sum
+    int any_abort = 0;
+    for (int t = tid; t < S * ROWS; t += kThreads) {
+        const int c = t / ROWS, row = t - c * ROWS;
+        if (c == rank) {
+            sm[t] = cm[row];
+            sl[t] = cl[row];
+        } else {
+            const float *part = ws_pair + static_cast<size_t>(c) * PART;
+            sm[t] = __ldcg(part + ROWS * kD + row);
+            sl[t] = __ldcg(part + ROWS * kD + ROWS + row);
+            if (row == 0)
+                any_abort |= __ldcg(part + ROWS * kD + 2 * ROWS) != 0.f;
         }
     }
-    // peers may still read this CTA's state
-    cluster_sync();
+    any_abort = __syncthreads_or(any_abort || aborted_f != 0.f);
+    if (any_abort)
+        return;   // a CTA of the pair failed its ready check: O and lse stay untouched
+    if (tid < ROWS) {
+        const int row = tid;
+        float M = -INFINITY;
+        for (int c = 0; c < S; ++c)
+            M = fmaxf(M, sm[c * ROWS + row]);
+        float L = 0.f;
+        for (int c = 0; c < S; ++c) {
+            const float mc = sm[c * ROWS + row];
+            const float f = (M == -INFINITY || mc == -INFINITY) ? 0.f : exp2f(mc - M);
+            L += f * sl[c * ROWS + row];
+            sl[c * ROWS + row] = f;
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        for (int c = 0; c < S; ++c)
+            sl[c * ROWS + row] *= inv;
+        rowml[row] = M;
+        rowml[ROWS + row] = L;
+    }
+    __syncthreads();
+    for (int q4 = tid; q4 < p.G * (kD / 4); q4 += kThreads) {
+        const int row = q4 / (kD / 4);
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c0 = 0; c0 < S; c0 += 4) {
+            float4 v[4];
+            float f[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = c0 + j;
+                f[j] = c < S ? sl[c * ROWS + row] : 0.f;
+                if (c >= S)
+                    v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                else if (c == rank)
+                    v[j] = reinterpret_cast<const float4 *>(co)[q4];
+                else
+                    v[j] = __ldcg(reinterpret_cast<const float4 *>(ws_pair + static_cast<size_t>(c) * PART) + q4);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                o.x = fmaf(f[j], v[j].x, o.x);
+                o.y = fmaf(f[j], v[j].y, o.y);
+                o.z = fmaf(f[j], v[j].z, o.z);
+                o.w = fmaf(f[j], v[j].w, o.w);
+            }
+        }
+        uint2 packed;
+        packed.x = pack_bf16x2(o.x, o.y);
+        packed.y = pack_bf16x2(o.z, o.w);
+        const size_t out = (static_cast<size_t>(b) * p.H_q + g * p.G + row) * kD + 4 * (q4 % (kD / 4));
+        *reinterpret_cast<uint2 *>(p.O + out) = packed;
+    }
+    if (p.lse != nullptr && tid < p.G)
+        p.lse[static_cast<size_t>(b) * p.H_q + g * p.G + tid] = lse_of(rowml[tid], rowml[ROWS + tid]);
 }
+
+// The split path's merge scratch must fit in the stage ring it reuses.
+static_assert((kConsumerWarps * 16 * kD + 3 * kConsumerWarps * 16 + 16 * kD + 2 * 16 + 2 * kMaxSplitWs * 16 + 2 * 16) *
+                      4 <=
+                  kStages * kStageBytes,
+              "split merge scratch exceeds the stage ring");
 
 // ---------------------------------------------------------------- stream-K decode
 
@@ -1118,6 +995,64 @@ size_t streamk_workspace_bytes(long long pairs, int G, int n_ctas)
     return counters + 2ull * static_cast<size_t>(n_ctas) * part * sizeof(float);
 }
 
+template <int NT>
+int launch_split(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, int S, long long pairs,
+                 int device, cudaStream_t stream)
+{
+    auto kern = decode_split_kernel<NT>;
+    const int smem = kSmemDecode + 1024;
+    static int configured[64];
+    int rc = sp_host::configure_kernel(reinterpret_cast<const void *>(kern), smem, device, configured);
+    if (rc != SPARSE_OK)
+        return rc;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(S), static_cast<unsigned>(pairs), 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    CUtensorMap kmap = km, vmap = vm;
+    AttnParams prm = p;
+    void *args[] = {&kmap, &vmap, &prm};
+    return sp_host::cuda_status(cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(kern), args),
+                                "sparse attention (split) launch");
+}
+
+// Split path geometry: CTAs per pair.  Auto: one wave of two CTAs per SM, at least two
+// blocks per CTA; a slice never exceeds the staged list (kMaxListCta).  0 = invalid.
+int split_ctas_per_pair(long long pairs, int k_tot, int n_split, int sm_count)
+{
+    long long s;
+    if (n_split > 0) {
+        s = n_split;
+    } else {
+        s = (2LL * sm_count) / pairs;
+        const long long by_list = k_tot / 2;
+        if (s > by_list)
+            s = by_list;
+        if (s > kMaxSplitWs)
+            s = kMaxSplitWs;
+        if (s < 1)
+            s = 1;
+        while ((k_tot + s - 1) / s > kMaxListCta && s < kMaxSplitWs)
+            ++s;
+    }
+    if (s > kMaxSplitWs || (k_tot + s - 1) / s > kMaxListCta)
+        return 0;
+    return static_cast<int>(s);
+}
+
+size_t split_workspace_bytes(long long pairs, int G, int S)
+{
+    const size_t part = G <= 8 ? split_part_floats<1>() : split_part_floats<2>();
+    const size_t counters = (static_cast<size_t>(pairs) * sizeof(int) + 255) & ~static_cast<size_t>(255);
+    return counters + static_cast<size_t>(pairs) * S * part * sizeof(float);
+}
+
 template <int NT, bool VERIFY>
 int launch(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, int S, long long units,
            int device, cudaStream_t stream)
@@ -1154,27 +1089,6 @@ static_assert((3 * kConsumerWarps * 16 + kConsumerWarps * 16 * kD + 16 * kD + 2 
                       4 <=
                   kStages * kStageBytes,
               "merge scratch exceeds the stage ring");
-
-int choose_split(int n_split, long long units, int max_list, int sm_count, int *S)
-{
-    if (n_split == 0) {
-        int s = 1;
-        while (s < kMaxSplit && units * s * 2 <= 2LL * sm_count && s * 2 <= (max_list > 1 ? max_list / 2 : 1))
-            s *= 2;
-        *S = s;
-        return SPARSE_OK;
-    }
-    if (n_split != 1 && n_split != 2 && n_split != 4 && n_split != 8)
-        return sp_host::fail(SPARSE_ERR_INVALID_ARG, "n_split must be 0, 1, 2, 4 or 8 (got %d)", n_split);
-    *S = n_split;
-    return SPARSE_OK;
-}
-
-float scale_log2_of(float scale)
-{
-    const float s = scale == 0.f ? 1.f / sqrtf(static_cast<float>(kD)) : scale;
-    return s * 1.44269504088896340736f;   // log2(e): scores are exponentiated base 2
-}
 
 int decode_impl(const uint16_t *Q, const uint16_t *k_base, const uint16_t *v_base, long long pair_stride,
                 const int *blk_slot, const int *blk_logical, const int *count, int k_tot, const int *seq_len,
@@ -1232,10 +1146,31 @@ int decode_impl(const uint16_t *Q, const uint16_t *k_base, const uint16_t *v_bas
     p.n_groups = 1;
     p.flags = flags;
     p.scale_log2 = scale_log2_of(scale);
-    // Stream-K when asked, or when the pairs are too few for clusters of CTAs to cover
-    // the SMs; otherwise the cluster path (the faster one once every SM is busy).
-    const bool stream_k = workspace != nullptr && G <= 8 &&
-                          ((flags & SPARSE_ATTN_STREAM_K) != 0u || pairs * 4 < dev.sm_count);
+    // With a workspace: the split path (per-pair slices, merged by the last CTA), or
+    // stream-K when asked.  Without one: thread-block clusters merging through DSMEM.
+    const bool stream_k = workspace != nullptr && G <= 8 && (flags & SPARSE_ATTN_STREAM_K) != 0u;
+    if (workspace != nullptr && !stream_k) {
+        if (!aligned16(workspace))
+            return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn: workspace must be 16-byte aligned");
+        const int S = split_ctas_per_pair(pairs, k_tot, n_split, dev.sm_count);
+        if (S == 0)
+            return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn: n_split=%d (1..%d CTAs per pair, at most %d "
+                        "blocks each)", n_split, kMaxSplitWs, kMaxListCta);
+        const size_t need = split_workspace_bytes(pairs, G, S);
+        if (workspace_bytes < need)
+            return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn: workspace of %zu bytes, %zu needed",
+                        workspace_bytes, need);
+        CUtensorMap km, vm;
+        if ((rc = sp_host::make_kv_tensor_map(&km, k_base, pair_stride, pairs)) != SPARSE_OK)
+            return rc;
+        if ((rc = sp_host::make_kv_tensor_map(&vm, v_base, pair_stride, pairs)) != SPARSE_OK)
+            return rc;
+        p.ws_count = static_cast<int *>(workspace);
+        p.ws_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                              ((static_cast<size_t>(pairs) * sizeof(int) + 255) & ~static_cast<size_t>(255)));
+        return G <= 8 ? launch_split<1>(p, km, vm, S, pairs, dev.device, st)
+                      : launch_split<2>(p, km, vm, S, pairs, dev.device, st);
+    }
     if (stream_k) {
         // stream-K: equal contiguous ranges of the flattened (pair, block) list
         if (!aligned16(workspace))
@@ -1387,9 +1322,15 @@ extern "C" SPARSE_API size_t sparse_decode_attn_workspace_size(int B, int H_q, i
         return 0;
     const long long pairs = static_cast<long long>(B) * H_kv;
     const int G = H_q / H_kv;
-    if (G > 8)
-        return 0;   // the cluster path (no workspace) serves G > 8
-    return streamk_workspace_bytes(pairs, G, streamk_ctas(pairs * k_tot, pairs, n_split, dev.sm_count));
+    if (G > 16)
+        return 0;
+    const int S = split_ctas_per_pair(pairs, k_tot, n_split, dev.sm_count);
+    size_t need = S > 0 ? split_workspace_bytes(pairs, G, S) : 0;
+    if (G <= 8) {
+        const size_t sk = streamk_workspace_bytes(pairs, G, streamk_ctas(pairs * k_tot, pairs, n_split, dev.sm_count));
+        need = sk > need ? sk : need;
+    }
+    return need;
 }
 
 extern "C" SPARSE_API int sparse_verify_attn_grouped(const uint16_t *Q, const uint16_t *k_cache,

@@ -120,22 +120,27 @@ SPARSE_API int sparse_select_topk(const uint16_t *F, const float *ktil, const in
  *   seq_len      [B] int32 (device).
  *   scale        0 selects 1/sqrt(128).
  *   O            [B][H_q][128] bf16;  lse [B][H_q] fp32 natural-log LSE, or NULL.
- *   n_split      without a workspace: CTAs sharing one pair's list (1, 2, 4 or 8);
- *                with a workspace: the total CTA count.  0 = chosen from the SM count.
- *                The result does not depend on it beyond fp32 rounding.
+ *   n_split      CTAs sharing one pair's list.  Without a workspace 1, 2, 4 or 8 (one
+ *                thread-block cluster per pair); with a workspace 1 .. 64; with a
+ *                workspace and SPARSE_ATTN_STREAM_K the total CTA count.  0 = chosen
+ *                from the SM count.  The result does not depend on it beyond fp32
+ *                rounding.
  *   flags        SPARSE_ATTN_BLOCKS_READY and / or SPARSE_ATTN_STREAM_K (below), or 0.
  *   workspace    NULL, or device memory of sparse_decode_attn_workspace_size() bytes
- *                (workspace_bytes gives its size).  By default the CTAs of a pair form a
- *                thread-block cluster and merge their partial softmax states through
- *                distributed shared memory (no scratch).  With a workspace and G <= 8,
- *                the stream-K path runs when SPARSE_ATTN_STREAM_K is set or when the
- *                pairs are too few for clusters to cover the SMs (B*H_kv*4 < SMs): a
- *                persistent grid of two CTAs per SM splits the flattened (pair, block)
- *                list into equal ranges, and pairs split between CTAs are merged
- *                through the workspace by the CTA finishing last.  The workspace must
- *                be all zero before the first call that uses it; every call returns its
- *                arrival counters to zero.  Calls that share a workspace must not run
- *                at the same time.
+ *                (workspace_bytes gives its size).
+ *                Without a workspace the CTAs of a pair form a thread-block cluster and
+ *                merge their partial softmax states through distributed shared memory
+ *                (no scratch; the cluster waits for its slowest CTA).
+ *                With a workspace (the split path) CTA r of a pair attends over entries
+ *                [r * ceil(k_tot / S), (r + 1) * ceil(k_tot / S)) of its list, writes its
+ *                partial state to the workspace and exits; the CTA of the pair that
+ *                arrives last merges the S states and writes O and lse.
+ *                With a workspace, SPARSE_ATTN_STREAM_K and G <= 8, the stream-K path
+ *                runs instead: a persistent grid of two CTAs per SM splits the
+ *                flattened (pair, block) list into equal ranges, merged the same way.
+ *                The workspace must be all zero before the first call that uses it;
+ *                every call returns its arrival counters to zero.  Calls that share a
+ *                workspace must not run at the same time.
  * A row with no valid token gets O = 0 and lse = -inf.  G = H_q / H_kv <= 16,
  * k_tot <= 4096.
  *
@@ -163,9 +168,9 @@ SPARSE_API int sparse_decode_attn(const uint16_t *Q, const uint16_t *k_base,
 
 /*
  * Bytes of the sparse_decode_attn workspace for these sizes on the current device
- * (n_split as for sparse_decode_attn), or 0 when the sizes are invalid or G > 8 (the
- * workspace-free path serves G > 8).  The SparDA notes have no counterpart: this is
- * the size of the stream-K partial states and per-pair arrival counters.
+ * (n_split as for sparse_decode_attn): enough for the split path and, for G <= 8, the
+ * stream-K path; 0 when the sizes are invalid.  The SparDA notes have no counterpart:
+ * this is the size of the per-pair arrival counters and the partial softmax states.
  */
 SPARSE_API size_t sparse_decode_attn_workspace_size(int B, int H_q, int H_kv, int k_tot, int n_split);
 
@@ -215,6 +220,50 @@ SPARSE_API int sparse_decode_attn_ex(const uint16_t *Q, const uint16_t *k_base,
                                      size_t workspace_bytes, const unsigned *ready_flag,
                                      unsigned ready_target, long long timeout_ns, int *status,
                                      void *stream);
+
+/*
+ * sparse_decode_attn_forecast -- one decode layer: the attention of layer l fused with
+ * the Forecast selection for layer l+1.  [SparDA] §4.1 (the Forecast vector F_l of
+ * layer l selects the blocks of layer l+1 from its compressed keys, eq.(6), so that
+ * selection runs while layer l attends, eq.(7)) and §4.2 Alg.1 steps 2 and 4.
+ * It computes exactly what these two calls compute, in one kernel:
+ *     sparse_decode_attn(Q, k_cache, v_cache, T_cap, NULL, blk_idx, count, k_tot,
+ *                        seq_len, B, H_q, H_kv, scale, O, lse, n_split, flags, ...)
+ *     sparse_select_topk(F, ktil_next, seq_len, B, H_kv, N_cap, n_init, n_local, k,
+ *                        idx_next, count_next, k_tot_next, ...)
+ * (the selection scores with the same fp32 arithmetic, so its lists are identical to
+ * sparse_select_topk's).  The attention reads a resident cache (slot = logical id).
+ *   Q, k_cache, v_cache, T_cap, blk_idx, count, k_tot, seq_len, B, H_q, H_kv, scale,
+ *   O, lse       as for sparse_decode_attn (k_cache / v_cache [B][H_kv][T_cap][128]).
+ *   F            [B][H_kv][128] bf16 Forecast vectors of layer l, or NULL: attention
+ *                only (ktil_next .. k_tot_next are then ignored).
+ *   ktil_next    [B][H_kv][N_cap][128] fp32 compressed keys of layer l+1.
+ *   N_cap, n_init, n_local, k, idx_next [B][H_kv][k_tot_next], count_next [B][H_kv]
+ *                as for sparse_select_topk; idx_next / count_next must not alias
+ *                blk_idx / count.
+ *   n_split      CTAs per pair (1, 2, 4 or 8; 0 = chosen from the SM count): each
+ *                takes a slice of the pair's block list and of its compressed keys.
+ *   flags        0 or SPARSE_ATTN_BLOCKS_READY (as for sparse_decode_attn).
+ * Shared memory holds the pair's N_cap keys: N_cap up to about 28000.
+ *
+ * Launch order.  seq_len and ktil_next must be complete before the kernel preceding
+ * this one on the stream finishes (compressed keys are updated by the append of the
+ * previous decode step): each CTA streams its slice of ktil_next at once.  Q and F may
+ * be written by that preceding kernel; so may blk_idx and count unless
+ * SPARSE_ATTN_BLOCKS_READY is passed.  The kernel lets the next kernel on the stream be
+ * scheduled as soon as it has started, so a chain of these calls, layer after layer
+ * (idx_next of one call is blk_idx of the next), overlaps each layer's compressed-key
+ * stream with the end of the layer before.
+ */
+SPARSE_API int sparse_decode_attn_forecast(const uint16_t *Q, const uint16_t *k_cache,
+                                           const uint16_t *v_cache, long long T_cap,
+                                           const int *blk_idx, const int *count, int k_tot,
+                                           const int *seq_len, int B, int H_q, int H_kv,
+                                           float scale, uint16_t *O, float *lse,
+                                           const uint16_t *F, const float *ktil_next, int N_cap,
+                                           int n_init, int n_local, int k, int *idx_next,
+                                           int *count_next, int k_tot_next, int n_split,
+                                           unsigned flags, int *status, void *stream);
 
 /*
  * sparse_verify_attn_grouped -- [SSV] mechanism 1, mode A (exact merged schedule).

@@ -116,6 +116,17 @@ def test_select_ties_go_to_the_lower_index_exactly():
     assert list(ridx[0, :rcnt[0]]) == list(range(0, k + 1)) + [298, 299]
 
 
+def test_select_k_zero_keeps_only_init_and_local():
+    lens_b, H_kv, N_cap = [40 * BLK, 3 * BLK + 1, 65], 2, 40
+    P = len(lens_b) * H_kv
+    ktil_np = np.random.default_rng(9).standard_normal((P, N_cap, D)).astype(np.float32)
+    F = wl.randn_bf16((len(lens_b), H_kv, D), 10, "cuda")
+    idx, cnt, (ridx, rcnt, _), _ = _select_case(lens_b, H_kv, N_cap, 1, 2, 0, ktil_np, F)
+    assert np.array_equal(idx.cpu().numpy().reshape(ridx.shape), ridx)
+    assert np.array_equal(cnt.cpu().numpy().reshape(rcnt.shape), rcnt)
+    assert list(ridx[0]) == [0, 38, 39]
+
+
 @pytest.mark.parametrize("lens_b", [[7 * BLK, 2 * BLK, 65, 1, 0]])
 def test_select_few_blocks_takes_all(lens_b):
     H_kv, N_cap = 2, 8
@@ -130,10 +141,15 @@ def test_select_few_blocks_takes_all(lens_b):
 # ----------------------------------------------------------------------------- decode attention
 
 
+PATHS = ("cluster", "split", "stream_k")
+
+
 def _decode_direct(B, H_q, H_kv, T_cap, lens_b, k_cap, seed, n_split=0, idx_np=None, cnt_np=None,
-                   workspace=False):
+                   path="cluster"):
     """sparse_decode_attn on given (or random distinct) block lists vs oracle.attn.
-    With ``workspace`` the stream-K path runs and its counters must end at zero."""
+    ``path``: "cluster" (no workspace), "split" (workspace: per-pair slices merged by the
+    last CTA) or "stream_k" (workspace and SPARSE_ATTN_STREAM_K); with a workspace the
+    arrival counters must end at zero."""
     G = H_q // H_kv
     P = B * H_kv
     rng = np.random.default_rng(seed)
@@ -152,11 +168,12 @@ def _decode_direct(B, H_q, H_kv, T_cap, lens_b, k_cap, seed, n_split=0, idx_np=N
     O = torch.zeros((B, H_q, D), dtype=torch.bfloat16, device="cuda")
     lse = torch.zeros((B, H_q), dtype=torch.float32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    ws = binding.decode_workspace(B, H_q, H_kv, k_cap, n_split) if workspace else None
+    assert path in PATHS
+    ws = binding.decode_workspace(B, H_q, H_kv, k_cap, n_split) if path != "cluster" else None
     binding.sparse_decode_attn(Q, K, V, torch.from_numpy(idx_np).cuda().view(B, H_kv, k_cap),
                                torch.from_numpy(cnt_np).cuda().view(B, H_kv), _seq(lens_b), O, lse,
                                n_split=n_split, workspace=ws, status=status,
-                               flags=binding.SPARSE_ATTN_STREAM_K if workspace else 0)
+                               flags=binding.SPARSE_ATTN_STREAM_K if path == "stream_k" else 0)
     torch.cuda.synchronize()
     assert status.item() == 0
     if ws is not None:
@@ -166,25 +183,51 @@ def _decode_direct(B, H_q, H_kv, T_cap, lens_b, k_cap, seed, n_split=0, idx_np=N
     return O, lse, Oref, lref
 
 
-@pytest.mark.parametrize("workspace", [False, True])
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("H_q,H_kv", [(8, 2), (64, 8), (16, 16), (32, 2), (24, 4)])
-def test_decode_attn_matches_oracle_group_sizes(H_q, H_kv, workspace):
+def test_decode_attn_matches_oracle_group_sizes(H_q, H_kv, path):
+    # (stream-K serves G <= 8; G = 16 with that flag runs the cluster path)
     O, lse, Oref, lref = _decode_direct(2, H_q, H_kv, 40 * BLK, [40 * BLK, 25 * BLK + 11], 19, seed=H_q * 7 + H_kv,
-                                        workspace=workspace)
+                                        path=path)
     assert_attn_close(O, Oref.reshape(2, H_q, D))
     _check_lse(lse, lref.reshape(2, H_q))
 
 
-def test_decode_attn_split_invariance():
+@pytest.mark.parametrize("path,splits", [("cluster", (1, 2, 4, 8)), ("split", (1, 2, 3, 4, 8, 17, 64))])
+def test_decode_attn_split_invariance(path, splits):
     outs = {}
-    for n_split in (1, 2, 4, 8):
+    for n_split in splits:
         O, lse, Oref, lref = _decode_direct(2, 32, 8, 80 * BLK, [80 * BLK, 79 * BLK + 1], 67, seed=99,
-                                            n_split=n_split)
-        assert_attn_close(O, Oref.reshape(2, 32, D), f"n_split={n_split}")
+                                            n_split=n_split, path=path)
+        assert_attn_close(O, Oref.reshape(2, 32, D), f"{path} n_split={n_split}")
+        _check_lse(lse, lref.reshape(2, 32))
         outs[n_split] = O
-    for n_split in (2, 4, 8):
+    for n_split in splits[1:]:
         diff = (outs[n_split].float() - outs[1].float()).abs().max().item()
-        assert diff <= 2 ** -7, f"split {n_split} changes the output by {diff}"
+        assert diff <= 2 ** -7, f"{path}: split {n_split} changes the output by {diff}"
+
+
+@pytest.mark.parametrize("n_split", [1, 2, 5, 16, 0])
+@pytest.mark.parametrize("H_q", [24, 48])
+def test_decode_attn_split_path_ragged_and_empty_pairs(n_split, H_q):
+    """The split path with ragged, short and empty pairs (count < k_tot: trailing
+    slices empty), for G = 8 and G = 16 (two n-tiles)."""
+    B, H_kv, T_cap, k_cap = 3, 3, 48 * BLK, 21
+    P = B * H_kv
+    lens_b = [48 * BLK, 30 * BLK + 5, 7 * BLK]
+    lens_p = _lens_pair(lens_b, H_kv)
+    rng = np.random.default_rng(13)
+    idx_np = np.full((P, k_cap), -1, np.int32)
+    cnt_np = np.zeros(P, np.int32)
+    for p in range(P):
+        nb = (int(lens_p[p]) + BLK - 1) // BLK
+        c = min([k_cap, 5, 0, 1][p % 4], nb)
+        idx_np[p, :c] = rng.permutation(nb)[:c]
+        cnt_np[p] = c
+    O, lse, Oref, lref = _decode_direct(B, H_q, H_kv, T_cap, lens_b, k_cap, 17, n_split=n_split, idx_np=idx_np,
+                                        cnt_np=cnt_np, path="split")
+    assert_attn_close(O, Oref.reshape(B, H_q, D), f"n_split={n_split}")
+    _check_lse(lse, lref.reshape(B, H_q))
 
 
 @pytest.mark.parametrize("n_ctas", [1, 2, 3, 7, 13, 64, 0])
@@ -205,17 +248,18 @@ def test_decode_attn_stream_k_partitions(n_ctas):
         idx_np[p, :c] = rng.permutation(nb)[:c]
         cnt_np[p] = c
     O, lse, Oref, lref = _decode_direct(B, H_q, H_kv, T_cap, lens_b, k_cap, 7, n_split=n_ctas, idx_np=idx_np,
-                                        cnt_np=cnt_np, workspace=True)
+                                        cnt_np=cnt_np, path="stream_k")
     assert_attn_close(O, Oref.reshape(B, H_q, D), f"n_ctas={n_ctas}")
     _check_lse(lse, lref.reshape(B, H_q))
 
 
-def test_decode_attn_stream_k_matches_cluster_path():
+def test_decode_attn_paths_agree_and_are_deterministic():
     a = _decode_direct(2, 64, 8, 80 * BLK, [80 * BLK, 79 * BLK + 1], 67, seed=5)[0]
-    b = _decode_direct(2, 64, 8, 80 * BLK, [80 * BLK, 79 * BLK + 1], 67, seed=5, workspace=True)[0]
-    c = _decode_direct(2, 64, 8, 80 * BLK, [80 * BLK, 79 * BLK + 1], 67, seed=5, workspace=True)[0]
-    assert (a.float() - b.float()).abs().max().item() <= 2 ** -7
-    assert torch.equal(b, c)   # deterministic
+    for path in ("split", "stream_k"):
+        b = _decode_direct(2, 64, 8, 80 * BLK, [80 * BLK, 79 * BLK + 1], 67, seed=5, path=path)[0]
+        c = _decode_direct(2, 64, 8, 80 * BLK, [80 * BLK, 79 * BLK + 1], 67, seed=5, path=path)[0]
+        assert (a.float() - b.float()).abs().max().item() <= 2 ** -7, path
+        assert torch.equal(b, c), f"{path} is not deterministic"
 
 
 def test_decode_attn_empty_and_tiny_sets():
@@ -240,15 +284,18 @@ def test_decode_attn_is_deterministic():
     assert torch.equal(a, b)
 
 
-def test_decode_attn_reports_bad_block_ids_without_faulting():
+@pytest.mark.parametrize("path", ["cluster", "split"])
+def test_decode_attn_reports_bad_block_ids_without_faulting(path):
     B, H_q, H_kv, T_cap, k_cap = 1, 8, 2, 8 * BLK, 3
+    ws = binding.decode_workspace(B, H_q, H_kv, k_cap, 2) if path == "split" else None
     K = wl.randn_bf16((B, H_kv, T_cap, D), 1, "cuda")
     Q = wl.randn_bf16((B, H_q, D), 2, "cuda")
     idx = torch.tensor([[[0, 1 << 20, 2], [3, -5, 4]]], dtype=torch.int32, device="cuda")
     cnt = torch.tensor([[3, 3]], dtype=torch.int32, device="cuda")
     O = torch.zeros((B, H_q, D), dtype=torch.bfloat16, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    binding.sparse_decode_attn(Q, K, K, idx, cnt, _seq([T_cap]), O, status=status)
+    binding.sparse_decode_attn(Q, K, K, idx, cnt, _seq([T_cap]), O, status=status, workspace=ws,
+                               n_split=2 if ws is not None else 0)
     torch.cuda.synchronize()
     assert status.item() == binding.SPARSE_ERR_BAD_INDEX
     good_idx = torch.tensor([[[0, 2, 2], [3, 4, 4]]], dtype=torch.int32, device="cuda")
@@ -279,6 +326,13 @@ def test_decode_attn_ex_ready_word():
     status.zero_()
     binding.sparse_decode_attn_ex(Q, K, K, idx, cnt, _seq([T_cap]), O, flag, 1, 20_000_000, n_split=4,
                                   workspace=ws, flags=binding.SPARSE_ATTN_STREAM_K, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == binding.SPARSE_ERR_TIMEOUT
+    assert torch.equal(O, sentinel) and not ws[:8].any()
+    # and through the split path
+    status.zero_()
+    binding.sparse_decode_attn_ex(Q, K, K, idx, cnt, _seq([T_cap]), O, flag, 1, 20_000_000, n_split=2,
+                                  workspace=ws, status=status)
     torch.cuda.synchronize()
     assert status.item() == binding.SPARSE_ERR_TIMEOUT
     assert torch.equal(O, sentinel) and not ws[:8].any()
