@@ -724,7 +724,7 @@ def _rate(nbytes, t_us, peak):
 class _Layer:
     """One decode layer on the device: cache, compressed keys, block lists, output."""
 
-    def __init__(self, sh, dev):
+    def __init__(self, sh, dev, use_workspace=False):
         import torch
         from block_sparse_long_pool_gb300 import binding
         from block_sparse_long_pool_gb300 import workloads as wl
@@ -745,7 +745,7 @@ class _Layer:
         self.cnt = torch.empty((B, H_kv), dtype=torch.int32, device=dev)
         self.O = torch.empty((B, H_q, D), dtype=torch.bfloat16, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.ws = binding.decode_workspace(B, H_q, H_kv, sh.k_tot, device=dev)
+        self.ws = binding.decode_workspace(B, H_q, H_kv, sh.k_tot, device=dev) if use_workspace else None
 
     def step(self):
         sh, bd = self.sh, self.binding
@@ -761,7 +761,7 @@ class _Layer:
 def run_single_layer_case(args, dev, sh, name):
     import torch
     peak, src = measured_peaks()
-    lay = _Layer(sh, dev)
+    lay = _Layer(sh, dev, use_workspace=args.workspace)
     evict = torch.ones(512 << 20 >> 2, dtype=torch.int32, device=dev)
     t = _event_times(lay.step, args.steps, args.warmup, evict)
     torch.cuda.synchronize()
@@ -772,7 +772,8 @@ def run_single_layer_case(args, dev, sh, name):
     app = sh.pairs * (sh.n_new * 2 * 2 * D * 2 + 2 * KTIL_ROW_BYTES) if sh.n_new else 0
     gbs, frac = _rate(kv + sel + app, t["median_us"], peak)
     launches = 3 if sh.n_new else 2
-    line = {"case": name, "workload": sh.name, "unit_of_work": "one decode step (" +
+    line = {"case": name, "workload": sh.name, "decode_path": "split (workspace)" if args.workspace else "cluster",
+            "unit_of_work": "one decode step (" +
             ("append + " if sh.n_new else "") + "select + attention)",
             "steps_per_s": round(1e6 / t["median_us"], 1), **t, "launches_per_step": launches,
             "algorithmic_bytes": {"selected_kv": kv, "compressed_keys": sel, "append": app},
@@ -1008,7 +1009,8 @@ def main():
                          "single4k / append32k / verify64k / offload128k: the other workloads, one line each")
     ap.add_argument("--n-split", type=int, default=0)
     ap.add_argument("--no-workspace", action="store_true", help="layer case: attention without a workspace (cluster path)")
-    ap.add_argument("--workspace", action="store_true", help="step: attention with a workspace (split path)")
+    ap.add_argument("--workspace", action="store_true",
+                    help="step / single4k / append32k: attention with a workspace (split path)")
     ap.add_argument("--step-mode", choices=["fused", "separate"], default="fused",
                     help="fused: one sparse_decode_attn_forecast launch per layer; separate: sparse_select_topk "
                          "on a side stream beside sparse_decode_attn")
