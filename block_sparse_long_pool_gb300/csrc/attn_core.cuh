@@ -340,6 +340,68 @@ __device__ __forceinline__ float lse_of(float M, float L)
 }
 
 
+// Producer warp of a decode CTA: the CTA's slice [i0, i0 + cap) of the pair's block
+// table and the pair's count, fetched in one round trip (the slice is cut from k_tot,
+// so it does not wait for the count); entries past the count are dropped and invalid
+// ones become -1 (an out-of-range box is loaded for them: zeros, never a fault).  The
+// ready word, if any, is checked with a bounded wait.  Writes lslot / llog[0 .. n),
+// ctrl[kCtrlList] = n (0 when aborted) and ctrl[kCtrlAbort]; every lane returns n.
+__device__ __forceinline__ int producer_fetch_slice(const AttnParams &p, int pair, int i0, int cap, int *lslot,
+                                                    int *llog, int *ctrl, int lane)
+{
+    int c = lane == 0 ? p.count[pair] : 0;
+    for (int i = lane; i < cap; i += 32) {
+        const size_t at = static_cast<size_t>(pair) * p.k_tot + i0 + i;
+        const int logical = p.blk_logical[at];
+        llog[i] = logical;
+        lslot[i] = p.blk_slot != nullptr ? p.blk_slot[at] : logical;
+    }
+    c = __shfl_sync(0xffffffffu, c, 0);
+    if (c < 0 || c > p.k_tot) {
+        if (lane == 0)
+            report(p.status, SPARSE_ERR_BAD_INDEX);
+        c = c < 0 ? 0 : p.k_tot;
+    }
+    const int my_n = max(0, min(cap, c - i0));
+    for (int i = lane; i < my_n; i += 32) {
+        const int logical = llog[i], slot = lslot[i];
+        const bool ok = logical >= 0 && slot >= 0 && static_cast<long long>(slot) * kBlk < p.pair_stride;
+        if (!ok) {
+            report(p.status, SPARSE_ERR_BAD_INDEX);
+            llog[i] = -1;
+            lslot[i] = -1;
+        }
+    }
+    int aborted = 0;
+    if (lane == 0 && p.ready_flag != nullptr) {
+        bool ok = false;
+        const uint64_t t0 = globaltimer();
+        for (uint32_t it = 0; it < (1u << 26); ++it) {
+            unsigned v;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p.ready_flag) : "memory");
+            if (v >= p.ready_target) {
+                ok = true;
+                break;
+            }
+            if (p.timeout_ns <= 0 || globaltimer() - t0 > static_cast<uint64_t>(p.timeout_ns))
+                break;
+            __nanosleep(256);
+        }
+        if (!ok) {
+            aborted = 1;
+            report(p.status, p.timeout_ns > 0 ? SPARSE_ERR_TIMEOUT : SPARSE_ERR_NOT_READY);
+        }
+    }
+    aborted = __shfl_sync(0xffffffffu, aborted, 0);
+    const int n = aborted ? 0 : my_n;
+    if (lane == 0) {
+        ctrl[kCtrlAbort] = aborted;
+        ctrl[kCtrlList] = n;
+    }
+    __syncwarp();
+    return n;
+}
+
 // The merge of a cluster's partial states (split-KV): (1) each consumer warp's state
 // into shared memory, (2) merged into this CTA's state, (3) after one cluster barrier
 // CTA `rank` merges the S CTA states for its slice of output dims, reading its peers'
@@ -364,9 +426,6 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
     float *cm = co + ROWS * kD;                                      // [ROWS]
     float *cl = cm + ROWS;                                           // [ROWS]
     int *cabort = reinterpret_cast<int *>(cl + ROWS);                // [4]
-    float *fac = reinterpret_cast<float *>(cabort + 4);              // [kMaxSplit][ROWS]
-    float *row_m = fac + kMaxSplit * ROWS;
-    float *row_l = row_m + ROWS;
     if (warp < kConsumerWarps)
         store_warp_state<NT>(st, wo, wm, wl, warp, lane);
     if (tid == 0)
@@ -375,80 +434,75 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
     merge_warp_states<ROWS>(wo, wm, wl, wf, co, cm, cl, tid, nthreads, [] { __syncthreads(); });
     cluster_sync();
 
-    // peers' CTA states (generic pointers into distributed shared memory)
-    const float *peer_co[kMaxSplit];
-    const float *peer_cm[kMaxSplit];
-    const float *peer_cl[kMaxSplit];
-    int any_abort = 0;
+    // Peers' CTA states (generic pointers into distributed shared memory).  Every value
+    // a thread needs for an output pair is loaded before any is used, so the remote
+    // loads of an item overlap (one round trip).
+    const int Si = static_cast<int>(S);
+    const float *pco[kMaxSplit];
+    const float *pcm[kMaxSplit];
+    const float *pcl[kMaxSplit];
+    int ab[kMaxSplit];
 #pragma unroll
     for (int c = 0; c < kMaxSplit; ++c) {
-        const unsigned r = c < static_cast<int>(S) ? static_cast<unsigned>(c) : 0u;
-        peer_co[c] = static_cast<const float *>(__cluster_map_shared_rank(co, r));
-        peer_cm[c] = static_cast<const float *>(__cluster_map_shared_rank(cm, r));
-        peer_cl[c] = static_cast<const float *>(__cluster_map_shared_rank(cl, r));
-        const int ab = *static_cast<const int *>(__cluster_map_shared_rank(cabort, r));
-        any_abort |= c < static_cast<int>(S) ? ab : 0;
+        const unsigned r = c < Si ? static_cast<unsigned>(c) : 0u;
+        pco[c] = static_cast<const float *>(__cluster_map_shared_rank(co, r));
+        pcm[c] = static_cast<const float *>(__cluster_map_shared_rank(cm, r));
+        pcl[c] = static_cast<const float *>(__cluster_map_shared_rank(cl, r));
+        ab[c] = c < Si ? *static_cast<const int *>(__cluster_map_shared_rank(cabort, r)) : 0;
     }
-
-    // any CTA of the unit that failed its ready check leaves the output untouched
-    if (!any_abort) {
-        if (tid < ROWS) {
-            const int row = tid;
-            float mc[kMaxSplit], lc[kMaxSplit];
+    // CTA `rank` writes dims [rank * 128 / S, (rank + 1) * 128 / S) of every row, two
+    // adjacent dims per item
+    const int dims_per = kD / Si;
+    const int d0 = static_cast<int>(rank) * dims_per;
+    const int pairs_per_row = dims_per / 2;
+    const int n_items = rows_valid * pairs_per_row;
+    for (int item = tid; item < n_items; item += nthreads) {
+        const int row = item / pairs_per_row;
+        const int d = d0 + 2 * (item - row * pairs_per_row);
+        float mc[kMaxSplit], lc[kMaxSplit];
+        float2 v[kMaxSplit];
 #pragma unroll
-            for (int c = 0; c < kMaxSplit; ++c) {
-                mc[c] = c < static_cast<int>(S) ? peer_cm[c][row] : -INFINITY;
-                lc[c] = c < static_cast<int>(S) ? peer_cl[c][row] : 0.f;
-            }
-            float M = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kMaxSplit; ++c)
-                M = fmaxf(M, mc[c]);
-            float L = 0.f;
-#pragma unroll
-            for (int c = 0; c < kMaxSplit; ++c) {
-                const float f = (M == -INFINITY || mc[c] == -INFINITY) ? 0.f : exp2f(mc[c] - M);
-                fac[c * ROWS + row] = f;
-                L += lc[c] * f;
-            }
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-            for (int c = 0; c < kMaxSplit; ++c)
-                fac[c * ROWS + row] *= inv;
-            row_m[row] = M;
-            row_l[row] = L;
-        }
-        __syncthreads();
-        const int dims_per = kD / static_cast<int>(S);
-        const int d0 = static_cast<int>(rank) * dims_per;
-        for (int item = tid; item < rows_valid * dims_per; item += nthreads) {
-            const int row = item / dims_per;
-            const int d = d0 + (item - row * dims_per);
-            float v[kMaxSplit];
-#pragma unroll
-            for (int c = 0; c < kMaxSplit; ++c)
-                v[c] = c < static_cast<int>(S) ? peer_co[c][row * kD + d] : 0.f;
-            float o = 0.f;
-#pragma unroll
-            for (int c = 0; c < kMaxSplit; ++c)
-                o = fmaf(fac[c * ROWS + row], v[c], o);
-            size_t out;
-            if (VERIFY) {
-                const int qq = q0 + row / p.G, hh = row % p.G;
-                out = ((static_cast<size_t>(b) * p.N_q + qq) * p.H_q + g * p.G + hh) * kD + d;
+        for (int c = 0; c < kMaxSplit; ++c) {
+            if (c < Si) {
+                mc[c] = pcm[c][row];
+                lc[c] = pcl[c][row];
+                v[c] = *reinterpret_cast<const float2 *>(pco[c] + row * kD + d);
             } else {
-                out = (static_cast<size_t>(b) * p.H_q + g * p.G + row) * kD + d;
-            }
-            const __nv_bfloat16 ob = __float2bfloat16_rn(o);
-            p.O[out] = *reinterpret_cast<const uint16_t *>(&ob);
-        }
-        if (!VERIFY && rank == 0 && p.lse != nullptr) {
-            for (int row = tid; row < rows_valid; row += nthreads) {
-                const float L = row_l[row];
-                p.lse[static_cast<size_t>(b) * p.H_q + g * p.G + row] =
-                    L > 0.f ? (row_m[row] + log2f(L)) * 0.69314718055994530942f : -INFINITY;
+                mc[c] = -INFINITY;
+                lc[c] = 0.f;
+                v[c] = make_float2(0.f, 0.f);
             }
         }
+        int any_abort = 0;
+#pragma unroll
+        for (int c = 0; c < kMaxSplit; ++c)
+            any_abort |= ab[c];
+        // any CTA of the unit that failed its ready check leaves the output untouched
+        if (any_abort)
+            break;
+        float M = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kMaxSplit; ++c)
+            M = fmaxf(M, mc[c]);
+        float L = 0.f, ox = 0.f, oy = 0.f;
+#pragma unroll
+        for (int c = 0; c < kMaxSplit; ++c) {
+            const float f = (M == -INFINITY || mc[c] == -INFINITY) ? 0.f : exp2f(mc[c] - M);
+            L = fmaf(lc[c], f, L);
+            ox = fmaf(f, v[c].x, ox);
+            oy = fmaf(f, v[c].y, oy);
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        size_t out;
+        if (VERIFY) {
+            const int qq = q0 + row / p.G, hh = row % p.G;
+            out = ((static_cast<size_t>(b) * p.N_q + qq) * p.H_q + g * p.G + hh) * kD + d;
+        } else {
+            out = (static_cast<size_t>(b) * p.H_q + g * p.G + row) * kD + d;
+        }
+        *reinterpret_cast<uint32_t *>(p.O + out) = pack_bf16x2(ox * inv, oy * inv);
+        if (!VERIFY && rank == 0 && d == 0 && p.lse != nullptr)
+            p.lse[static_cast<size_t>(b) * p.H_q + g * p.G + row] = lse_of(M, L);
     }
     // peers may still read this CTA's state
     cluster_sync();

@@ -383,34 +383,13 @@ __global__ void __launch_bounds__(kFThreads, 2)
         // this layer's block list may be the previous kernel's output
         if ((p.flags & SPARSE_ATTN_BLOCKS_READY) == 0u)
             griddep_wait();
-        int c = lane == 0 ? p.count[pair] : 0;
-        for (int i = lane; i < cap; i += 32) {
-            const int logical = p.blk_logical[static_cast<size_t>(pair) * p.k_tot + i0 + i];
-            llog[i] = logical;
-            lslot[i] = logical;
-        }
-        c = __shfl_sync(0xffffffffu, c, 0);
-        if (c < 0 || c > p.k_tot) {
+        int n_run = producer_fetch_slice(p, pair, i0, cap, lslot, llog, ctrl, lane);
+        if (failed) {
+            n_run = 0;
             if (lane == 0)
-                report(p.status, SPARSE_ERR_BAD_INDEX);
-            c = c < 0 ? 0 : p.k_tot;
+                ctrl[kCtrlList] = 0;
+            __syncwarp();
         }
-        const int my_n = max(0, min(cap, c - i0));
-        for (int i = lane; i < my_n; i += 32) {
-            const int logical = llog[i];
-            const bool ok = logical >= 0 && static_cast<long long>(logical) * kBlk < p.pair_stride;
-            if (!ok) {
-                report(p.status, SPARSE_ERR_BAD_INDEX);
-                llog[i] = -1;
-                lslot[i] = -1;
-            }
-        }
-        const int n_run = failed ? 0 : my_n;
-        if (lane == 0) {
-            ctrl[kCtrlAbort] = 0;
-            ctrl[kCtrlList] = n_run;
-        }
-        __syncwarp();
         named_barrier_arrive(1, kAttnThreads);
         if (lane == 0 && n_run > 0) {
             prefetch_tensormap(&kmap);

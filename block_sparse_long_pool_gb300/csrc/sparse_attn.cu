@@ -145,8 +145,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     const bool early = !VERIFY && (p.flags & SPARSE_ATTN_BLOCKS_READY) != 0u;
     if (!early)
         griddep_wait();
-    const long long len = p.seq_len[b];
-    const int nb = len <= 0 ? 0 : static_cast<int>((len + kBlk - 1) / kBlk);
 
     if (tid == 0) {
         ctrl[kCtrlAbort] = 0;
@@ -156,81 +154,47 @@ __global__ void __launch_bounds__(kThreads, 2)
             mbar_init(bar_empty + 8 * s, kConsumerWarps);
         }
         fence_barrier_init();
-        if (p.ready_flag != nullptr) {
-            // staging-ready integrity check, bounded
-            bool ok = false;
-            const uint64_t t0 = globaltimer();
-            for (uint32_t it = 0; it < (1u << 26); ++it) {
-                unsigned v;
-                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p.ready_flag) : "memory");
-                if (v >= p.ready_target) {
-                    ok = true;
-                    break;
-                }
-                if (p.timeout_ns <= 0 || globaltimer() - t0 > static_cast<uint64_t>(p.timeout_ns))
-                    break;
-                __nanosleep(256);
-            }
-            if (!ok) {
-                ctrl[kCtrlAbort] = 1;
-                report(p.status, p.timeout_ns > 0 ? SPARSE_ERR_TIMEOUT : SPARSE_ERR_NOT_READY);
-            }
-        }
-        if (!VERIFY) {
-            int c = p.count[pair];
-            if (c < 0 || c > p.k_tot) {
-                report(p.status, SPARSE_ERR_BAD_INDEX);
-                c = c < 0 ? 0 : p.k_tot;
-            }
-            ctrl[kCtrlList] = c;
-        }
     }
     __syncthreads();
-    if (VERIFY) {
-        build_union<VERIFY>(p, base, b, g, q0, nb, ctrl);
-        __syncthreads();
-    }
-    const bool aborted = ctrl[kCtrlAbort] != 0;
-    const int n_list = aborted ? 0 : ctrl[kCtrlList];
-    const int per = (n_list + static_cast<int>(S) - 1) / static_cast<int>(S);
-    const int i0 = min(n_list, static_cast<int>(rank) * per);
-    const int i1 = min(n_list, i0 + per);
-    const int my_n = i1 - i0;
-    // block ids of this CTA's slice, in shared memory: verification keeps the merged
-    // union (ulist/umask, whole list); decode stages its slice of the block table with
-    // each entry validated (-1 = skip: an out-of-range box is loaded, never a fault)
+    // Verification: the merged union of the group's block sets (ulist / umask, whole
+    // list) is built by every thread; CTA r takes a contiguous slice of it.  Decode:
+    // CTA r takes entries [r * ceil(k_tot / S), ...) of the pair's table, which its
+    // producer warp fetches together with the count (one round trip) into lslot / llog.
     const int *ulist = reinterpret_cast<const int *>(base + kOffList);
     const uint32_t *umask = reinterpret_cast<const uint32_t *>(base + kOffMask);
     int *lslot = reinterpret_cast<int *>(base + kOffList);
     int *llog = lslot + kMaxListCta;
-    if (!VERIFY) {
-        for (int i = tid; i < my_n; i += kThreads) {
-            const size_t at = static_cast<size_t>(pair) * p.k_tot + i0 + i;
-            const int logical = p.blk_logical[at];
-            const int slot = p.blk_slot != nullptr ? p.blk_slot[at] : logical;
-            const bool ok = logical >= 0 && slot >= 0 && static_cast<long long>(slot) * kBlk < p.pair_stride;
-            if (!ok)
-                report(p.status, SPARSE_ERR_BAD_INDEX);
-            lslot[i] = ok ? slot : -1;
-            llog[i] = ok ? logical : -1;
-        }
+    long long len = 0;
+    int i0 = 0, my_n = 0, n_list = 0;
+    if (VERIFY) {
+        len = p.seq_len[b];
+        const int nb = len <= 0 ? 0 : static_cast<int>((len + kBlk - 1) / kBlk);
+        build_union<VERIFY>(p, base, b, g, q0, nb, ctrl);
         __syncthreads();
+        n_list = ctrl[kCtrlList];
+        const int per = (n_list + static_cast<int>(S) - 1) / static_cast<int>(S);
+        i0 = min(n_list, static_cast<int>(rank) * per);
+        my_n = min(n_list, i0 + per) - i0;
+        if (rank == 0 && tid == 0 && p.blocks_loaded != nullptr)
+            atomicAdd(reinterpret_cast<unsigned long long *>(p.blocks_loaded),
+                      static_cast<unsigned long long>(n_list));
     }
-
-    if (VERIFY && rank == 0 && tid == 0 && p.blocks_loaded != nullptr && !aborted)
-        atomicAdd(reinterpret_cast<unsigned long long *>(p.blocks_loaded),
-                  static_cast<unsigned long long>(n_list));
 
     WarpState<NT> st;
     st.reset();
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
+        if (!VERIFY) {
+            const int per = (p.k_tot + static_cast<int>(S) - 1) / static_cast<int>(S);
+            i0 = min(p.k_tot, static_cast<int>(rank) * per);
+            my_n = producer_fetch_slice(p, pair, i0, min(p.k_tot, i0 + per) - i0, lslot, llog, ctrl, lane);
+            named_barrier_arrive(1, kThreads);   // the slice and its length are in shared memory
+        }
         if (lane == 0 && my_n > 0) {
             prefetch_tensormap(&kmap);
             prefetch_tensormap(&vmap);
             const uint64_t pol = policy_evict_first();
-            const int map_pair = pair;
             for (int it = 0; it < my_n; ++it) {
                 const int s = it % kStages;
                 const int use = it / kStages;
@@ -243,10 +207,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int row = slot >= 0 ? slot * kBlk : static_cast<int>(min(p.pair_stride, (long long)INT_MAX - kBlk));
                 const uint32_t dst = base_s + s * kStageBytes;
                 mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
-                tma_load_3d(dst, &kmap, bar_full + 8 * s, 0, row, map_pair, pol);
-                tma_load_3d(dst + kHalfBytes, &kmap, bar_full + 8 * s, 64, row, map_pair, pol);
-                tma_load_3d(dst + kTileBytes, &vmap, bar_full + 8 * s, 0, row, map_pair, pol);
-                tma_load_3d(dst + kTileBytes + kHalfBytes, &vmap, bar_full + 8 * s, 64, row, map_pair, pol);
+                tma_load_3d(dst, &kmap, bar_full + 8 * s, 0, row, pair, pol);
+                tma_load_3d(dst + kHalfBytes, &kmap, bar_full + 8 * s, 64, row, pair, pol);
+                tma_load_3d(dst + kTileBytes, &vmap, bar_full + 8 * s, 0, row, pair, pol);
+                tma_load_3d(dst + kTileBytes + kHalfBytes, &vmap, bar_full + 8 * s, 64, row, pair, pol);
             }
         }
     } else {
@@ -255,6 +219,11 @@ __global__ void __launch_bounds__(kThreads, 2)
             griddep_wait();   // Q may be written by the kernel before this one
         QueryFrags<NT> q;
         load_query<NT, VERIFY>(q, p, b, g, q0, rows_valid, lane);
+        if (!VERIFY) {
+            len = p.seq_len[b];
+            named_barrier_sync(1, kThreads);
+            my_n = ctrl[kCtrlList];
+        }
         for (int it = 0; it < my_n; ++it) {
             const int s = it % kStages;
             // the verdict is made warp-uniform: the .aligned tensor-core instructions
@@ -265,12 +234,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                     report(p.status, SPARSE_ERR_TIMEOUT);
                 break;
             }
-            const int li = i0 + it;
             int logical;
             uint32_t qmask = 0xffffffffu;
             if (VERIFY) {
-                logical = ulist[li];
-                qmask = umask[li];
+                logical = ulist[i0 + it];
+                qmask = umask[i0 + it];
             } else {
                 logical = llog[it];
             }
@@ -290,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // The next kernel on the stream may be scheduled from here on.
     __syncthreads();
     griddep_launch_dependents();
-    cluster_merge_write<NT, VERIFY>(st, base, aborted, p, b, g, q0, rows_valid, rank, S, kThreads);
+    cluster_merge_write<NT, VERIFY>(st, base, ctrl[kCtrlAbort] != 0, p, b, g, q0, rows_valid, rank, S, kThreads);
 }
 
 // ---------------------------------------------------------------- split-KV decode, workspace merge
@@ -356,59 +324,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
-        // the count and the slice's entries are independent loads: one round trip
-        int c = lane == 0 ? p.count[pair] : 0;
-        for (int i = lane; i < cap; i += 32) {
-            const size_t at = static_cast<size_t>(pair) * p.k_tot + i0 + i;
-            const int logical = p.blk_logical[at];
-            llog[i] = logical;
-            lslot[i] = p.blk_slot != nullptr ? p.blk_slot[at] : logical;
-        }
-        c = __shfl_sync(0xffffffffu, c, 0);
-        if (c < 0 || c > p.k_tot) {
-            if (lane == 0)
-                report(p.status, SPARSE_ERR_BAD_INDEX);
-            c = c < 0 ? 0 : p.k_tot;
-        }
-        const int my_n = max(0, min(cap, c - i0));
-        // each lane re-checks the entries it wrote; -1 = skip (an out-of-range box is
-        // loaded, never a fault)
-        for (int i = lane; i < my_n; i += 32) {
-            const int logical = llog[i], slot = lslot[i];
-            const bool ok = logical >= 0 && slot >= 0 && static_cast<long long>(slot) * kBlk < p.pair_stride;
-            if (!ok) {
-                report(p.status, SPARSE_ERR_BAD_INDEX);
-                llog[i] = -1;
-                lslot[i] = -1;
-            }
-        }
-        int aborted = 0;
-        if (lane == 0 && p.ready_flag != nullptr) {
-            bool ok = false;
-            const uint64_t t0 = globaltimer();
-            for (uint32_t it = 0; it < (1u << 26); ++it) {
-                unsigned v;
-                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p.ready_flag) : "memory");
-                if (v >= p.ready_target) {
-                    ok = true;
-                    break;
-                }
-                if (p.timeout_ns <= 0 || globaltimer() - t0 > static_cast<uint64_t>(p.timeout_ns))
-                    break;
-                __nanosleep(256);
-            }
-            if (!ok) {
-                aborted = 1;
-                report(p.status, p.timeout_ns > 0 ? SPARSE_ERR_TIMEOUT : SPARSE_ERR_NOT_READY);
-            }
-        }
-        aborted = __shfl_sync(0xffffffffu, aborted, 0);
-        const int n_run = aborted ? 0 : my_n;
-        if (lane == 0) {
-            ctrl[kCtrlAbort] = aborted;
-            ctrl[kCtrlList] = n_run;
-        }
-        __syncwarp();
+        const int n_run = producer_fetch_slice(p, pair, i0, cap, lslot, llog, ctrl, lane);
         named_barrier_arrive(1, kThreads);   // the list and its length are in shared memory
         if (lane == 0 && n_run > 0) {
             prefetch_tensormap(&kmap);

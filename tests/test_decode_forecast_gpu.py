@@ -230,3 +230,54 @@ def test_forecast_chain_of_layers_matches_the_oracle():
             b, h = divmod(int(p), H_kv)
             assert_attn_close(Og[b, h], Oref[p], f"layer {l} pair {p}")
         assert exempt <= 1
+
+
+def test_forecast_128k_layer_sampled_at_full_size():
+    """One physical layer of the 128K, B=8, G=8 workload at full size, in the launch
+    configuration of the 80-layer bench step: sparse_select_topk picks this layer's
+    blocks with F_0, then one sparse_decode_attn_forecast launch attends over them and
+    selects again from the same compressed keys with F_10.  The oracle checks four
+    sampled pairs one by one."""
+    from parity_utils import GpuLayer, oracle_layer
+    sh = wl.DECODE_128K
+    B, H_kv, G = sh.B, sh.H_kv, sh.G
+    planted = wl.planted_sets(sh, 2)
+    L = GpuLayer(B, sh.H_q, H_kv, sh.T, sh.N_b, sh.n_init, sh.n_local, sh.k)
+    sample = [0, 13, 38, 63]
+    host = {}
+    for b in range(B):
+        Kb = torch.empty((1, H_kv, sh.T, D), dtype=torch.bfloat16, device="cuda")
+        Vb = torch.empty_like(Kb)
+        for h in range(H_kv):
+            p = b * H_kv + h
+            Kb[0, h], Vb[0, h] = wl.kv_pair(sh, 1, p, planted[1, p], "cuda")
+            if p in sample:
+                host[p] = (bits(Kb[0, h]), bits(Vb[0, h]))
+        binding.sparse_pool_append(L.k_cache[b:b + 1], L.v_cache[b:b + 1], L.ktil[b:b + 1], Kb, Vb, 0)
+    seq = torch.full((B,), sh.T, dtype=torch.int32, device="cuda")
+    F0, F10 = wl.forecast(sh, 1, 0, "cuda"), wl.forecast(sh, 1, 10, "cuda")
+    Q = wl.queries(sh, 1, "cuda")
+    L.select(F0, seq)
+    idx_next = torch.full_like(L.idx, -7)
+    cnt_next = torch.full_like(L.count, -7)
+    binding.sparse_decode_attn_forecast(Q, L.k_cache, L.v_cache, L.idx, L.count, seq, L.O, L.lse, F=F10,
+                                        ktil_next=L.ktil, n_init=sh.n_init, n_local=sh.n_local, k=sh.k,
+                                        idx_next=idx_next, count_next=cnt_next, status=L.status)
+    torch.cuda.synchronize()
+    assert L.status.item() == 0
+    Qb = bits(Q).reshape(sh.pairs, G, D)
+    for p in sample:
+        Kp, Vp = host[p]
+        _, ridx, rcnt, rs, Oref, _ = oracle_layer(Kp[None], Vp[None], Qb[p][None], bits(F0).reshape(sh.pairs, D)[p][None],
+                                                  [sh.T], sh.N_b, sh.n_init, sh.n_local, sh.k, G)
+        exempt = assert_selection_matches(L.idx.view(sh.pairs, -1)[p:p + 1], L.count.view(sh.pairs)[p:p + 1], ridx,
+                                          rcnt, rs, [sh.T], sh.n_init, sh.n_local, sh.k)
+        if not exempt:
+            b, h = divmod(p, H_kv)
+            assert_attn_close(L.O.view(B, H_kv, G, D)[b, h], Oref[0], f"pair {p}")
+        _, nidx, ncnt, ns, _, _ = oracle_layer(Kp[None], Vp[None], Qb[p][None],
+                                               bits(F10).reshape(sh.pairs, D)[p][None], [sh.T], sh.N_b, sh.n_init,
+                                               sh.n_local, sh.k, G)
+        assert_selection_matches(idx_next.view(sh.pairs, -1)[p:p + 1], cnt_next.view(sh.pairs)[p:p + 1], nidx, ncnt,
+                                 ns, [sh.T], sh.n_init, sh.n_local, sh.k)
+        assert len(set(planted[1, p].tolist()) & set(nidx[0].tolist())) >= 40   # generator sanity
