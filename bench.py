@@ -169,6 +169,15 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- 128K decode workload
 
 
+def step_config(sh, world: int) -> dict:
+    """The workload the bench line is quoted on (both arms)."""
+    return {"workload": sh.name, "B": sh.B, "H_q": sh.H_q, "H_kv": sh.H_kv, "d": D, "T": sh.T,
+            "layers": sh.layers, "physical_kv_layers": sh.phys_layers, "block": BLK, "k": sh.k,
+            "n_init": sh.n_init, "n_local": sh.n_local, "blocks_per_pair": sh.k_tot,
+            "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2: 10 physical layers x 4.3 GB, same layer every 2.1 GB"}
+
+
 def l2_evict(buf):
     """Read a buffer larger than L2 (129 MB) so the next launch starts from a cold,
     clean L2."""
@@ -465,11 +474,7 @@ def run_ours(args, rank, world, local_rank):
             "metric": METRIC, "value": round(value, 3), "unit": "steps/s", "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, planted blocks)",
-            "config": {"workload": sh.name, "B": sh.B, "H_q": sh.H_q, "H_kv": sh.H_kv, "d": D, "T": sh.T,
-                       "layers": sh.layers, "physical_kv_layers": sh.phys_layers, "block": BLK, "k": sh.k,
-                       "n_init": sh.n_init, "n_local": sh.n_local, "blocks_per_pair": sh.k_tot,
-                       "parallelism": f"replicas x{world}",
-                       "l2": "inputs larger than L2: 10 physical layers x 4.3 GB, same layer every 2.1 GB"},
+            "config": step_config(sh, world),
             "selected_kv_gbs": round(world * step_bytes / (ms * 1e-3) / 1e9, 1),
             "hbm_frac_of_8tbs": round(step_bytes / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
             "hbm_frac_of_measured": round(step_bytes / (ms * 1e-3) / 1e9 / peak, 4),
@@ -594,8 +599,7 @@ def run_reference(args, rank, world, local_rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) bf16, planted blocks)",
-            "config": {"workload": wk.sh.name, "B": wk.sh.B, "H_q": wk.sh.H_q, "H_kv": wk.sh.H_kv, "d": D,
-                       "T": wk.sh.T, "layers": wk.sh.layers, "k": wk.sh.k},
+            "config": step_config(wk.sh, world),
             "cpu_baseline": {"value": round(value, 6), "unit": "steps/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

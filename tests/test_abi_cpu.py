@@ -122,3 +122,33 @@ def test_binding_refuses_cpu_tensors(lib):
         binding.sparse_select_topk(torch.zeros(1, 2, 128, dtype=torch.bfloat16),
                                    torch.zeros(1, 2, 64, 128), torch.zeros(1, dtype=torch.int32), 1, 2, 8,
                                    torch.zeros(1, 2, 11, dtype=torch.int32), torch.zeros(1, 2, dtype=torch.int32))
+
+
+def test_decode_attn_forecast_rejects_bad_arguments(lib):
+    f = lib.sparse_decode_attn_forecast
+    #       Q     K     V     T_cap idx   cnt   k_tot seq   B  H_q H_kv scale O     lse
+    args = [FAKE, FAKE, FAKE, 4096, FAKE, FAKE, 11, FAKE, 1, 8, 2, 0.0, FAKE, None,
+            # F   ktil  N_cap n_init n_local k idx_next cnt_next k_tot_next n_split flags status stream
+            FAKE, FAKE, 64, 1, 2, 8, FAKE, FAKE, 11, 0, 0, None, None]
+    assert len(args) == len(binding.SIGNATURES["sparse_decode_attn_forecast"][1])
+
+    def call(**kw):
+        a = list(args)
+        names = ["Q", "K", "V", "T_cap", "idx", "cnt", "k_tot", "seq", "B", "H_q", "H_kv", "scale", "O", "lse",
+                 "F", "ktil", "N_cap", "n_init", "n_local", "k", "idx_next", "cnt_next", "k_tot_next", "n_split",
+                 "flags", "status", "stream"]
+        for k_, v in kw.items():
+            a[names.index(k_)] = v
+        return f(*a)
+
+    assert call(Q=None) == binding.SPARSE_ERR_INVALID_ARG
+    assert call(O=ODD) == binding.SPARSE_ERR_INVALID_ARG
+    assert call(H_q=12, H_kv=8) == binding.SPARSE_ERR_INVALID_ARG              # H_q not a multiple of H_kv
+    assert call(H_q=64, H_kv=2) == binding.SPARSE_ERR_UNSUPPORTED              # G = 32 > 16
+    assert call(flags=binding.SPARSE_ATTN_STREAM_K) == binding.SPARSE_ERR_INVALID_ARG
+    assert call(ktil=None) == binding.SPARSE_ERR_INVALID_ARG                   # F without compressed keys
+    assert "ktil_next" in lib.sparse_last_error().decode()
+    assert call(k_tot_next=10) == binding.SPARSE_ERR_INVALID_ARG               # < n_init + n_local + k
+    assert call(ktil=ODD) == binding.SPARSE_ERR_INVALID_ARG
+    assert call(n_local=-1) == binding.SPARSE_ERR_INVALID_ARG
+    assert call(scale=float("inf")) == binding.SPARSE_ERR_INVALID_ARG
