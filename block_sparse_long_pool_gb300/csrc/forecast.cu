@@ -1,32 +1,36 @@
-// decode_forecast.cu -- one SparDA decode layer in one kernel: block-sparse GQA
-// attention of layer l fused with the Forecast selection of the blocks of layer l+1.
+// forecast.cu -- Forecast block selection, alone or fused with a decode layer's attention.
 //
-// SparDA notes §4.1: the Forecast vector F_l of layer l scores the compressed keys of
-// layer l+1, so the blocks of layer l+1 are chosen while layer l attends (eq.(6)),
-// and layer l attends over the blocks chosen one layer earlier (eq.(7)); §4.2 Alg.1
-// steps 2 and 4 of one layer.  The selection is the one of sparse_select_topk (fp32
-// scores s_j = F . K̃_j, the k largest outside B_init and B_local, equal scores to the
-// lower block index, B_init ∪ B_local ∪ top-k ascending); the attention is the one of
-// sparse_decode_attn (scale 1/sqrt(d), split-KV merged by the online-softmax
-// recurrence).
+// Two entry points share one kernel:
+//   * sparse_select_topk (SparDA notes §4.1 eq.(6), §4.2 Alg.1 step 2, §4.3 eq.(9)):
+//     one Forecast vector per GQA group is scored against every compressed key of the
+//     layer it selects for (fp32 s_j = F . K̃_j), the k largest outside B_init and
+//     B_local are taken (equal scores: the lower block index), and B_init ∪ B_local ∪
+//     top-k is written in ascending block order.
+//   * sparse_decode_attn_forecast: one SparDA decode layer in one launch.  The Forecast
+//     vector F_l of layer l selects the blocks of layer l+1 while layer l attends over
+//     the blocks chosen one layer earlier (§4.1: the decoupling; eq.(7); Alg.1 steps 2
+//     and 4 of one layer).  The attention is the one of sparse_decode_attn (scale
+//     1/sqrt(d), split-KV merged by the online-softmax recurrence).
 //
 // GB300 design.  A cluster of S CTAs per (batch, KV head) pair; 6 warps per CTA.
-//   * Warp 4 (producer): one lane first streams this CTA's slice of the next layer's
-//     compressed keys into the ring (1-D bulk copies, 64 rows = 32 KB per stage).
-//     Nothing the preceding kernel writes is needed for that, so it overlaps the
-//     preceding kernel's tail under programmatic dependent launch.  It then waits for
-//     that kernel (the block list of this layer may be its output), stages the list
-//     slice, and streams the selected K/V blocks with TMA tensor copies.
+//   * Warp 4 (producer): one lane streams this CTA's slice of the compressed keys into
+//     the ring (1-D bulk copies, 64 rows = 32 KB per stage).  In the fused launch that
+//     needs nothing the preceding kernel writes, so it overlaps the preceding kernel's
+//     tail under programmatic dependent launch; then the producer waits for that
+//     kernel (the block list of this layer may be its output), stages the list slice,
+//     and streams the selected K/V blocks with TMA tensor copies.
 //   * Warps 0-3 (consumers): score every key row of a stage (fp32 dot product with F,
-//     shuffle reduction, one warp per 16 rows) and store the order key into CTA 0's
-//     shared memory (distributed shared memory); each warp then arrives on CTA 0's
-//     "scored" barrier; then the attention of the sparse_decode_attn cluster kernel.
-//   * Warp 5 (selector) of CTA 0: waits on the "scored" barrier and runs the exact
-//     top-k (MSB-first radix select over the keys) and the ascending compaction while
-//     the consumers attend; the next layer's list is out before the kernel ends.
-//   * The dependent launch is allowed at once: the next layer's kernel starts streaming
-//     its key slice as SMs free up, and waits for this kernel before reading the list
-//     this kernel writes.
+//     one warp per 16 rows, a transposed butterfly reduction), store the order key into
+//     CTA 0's shared memory and add it to CTA 0's coarse histogram (distributed shared
+//     memory); each warp then arrives on CTA 0's "scored" barrier; in the fused launch
+//     they then attend as the sparse_decode_attn cluster kernel does.
+//   * Warp 5 (selector) of CTA 0: waits on the "scored" barrier, finds the coarse bin
+//     that holds the k-th largest key, radix-selects within it and writes the list,
+//     while (in the fused launch) the consumers attend.
+//   * The dependent launch is allowed at once: a following launch starts streaming its
+//     key slice as SMs free up, and waits for this one before reading what it writes.
+#include <string.h>
+
 #include "attn_core.cuh"
 
 namespace {
@@ -68,40 +72,41 @@ inline size_t fused_smem_bytes(int per, int N_cap)
     return static_cast<size_t>(fused_off_keys(per)) + static_cast<size_t>(N_cap) * 4 + 1024;
 }
 
-// Histogram of byte digit (key >> shift) & 255 over keys[lo, hi) whose bits above the
-// digit equal `prefix` (under `pmask`), by one warp; lanes holding the same digit add
-// once (warp-aggregated shared-memory atomics).
-__device__ __forceinline__ void warp_digit_hist(const uint32_t *keys, int lo, int hi, uint32_t pmask,
-                                                uint32_t prefix, int shift, uint32_t *hist, int lane)
+// Histogram of byte digit (key >> shift) & 255 over the keys whose bits above the digit
+// equal `prefix` (under `pmask`), by one warp: keys[i] for i in [lo, hi), or
+// keys[list[i]] when list_s is non-zero.  Lanes holding the same digit add once
+// (warp-aggregated shared-memory atomics).  All arrays are shared-space addresses.
+__device__ __forceinline__ void warp_digit_hist(uint32_t keys_s, uint32_t list_s, int lo, int hi, uint32_t pmask,
+                                                uint32_t prefix, int shift, uint32_t hist_s, int lane)
 {
     for (int d = lane; d < 256; d += 32)
-        hist[d] = 0u;
+        sts_u32(hist_s + 4 * d, 0u);
     __syncwarp();
-    for (int jb = lo; jb < hi; jb += 32) {
-        const int j = jb + lane;
+    for (int ib = lo; ib < hi; ib += 32) {
+        const int i = ib + lane;
         uint32_t digit = 0xFFFFFFFFu;
-        if (j < hi) {
-            const uint32_t key = keys[j];
+        if (i < hi) {
+            const uint32_t j = list_s != 0u ? lds_u32(list_s + 4 * i) : static_cast<uint32_t>(i);
+            const uint32_t key = lds_u32(keys_s + 4 * j);
             if ((key & pmask) == prefix)
                 digit = (key >> shift) & 255u;
         }
         const uint32_t same = __match_any_sync(0xffffffffu, digit);
         if (digit != 0xFFFFFFFFu && lane == __ffs(same) - 1)
-            atomicAdd(&hist[digit], static_cast<uint32_t>(__popc(same)));
+            asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(hist_s + 4 * digit), "r"(__popc(same)) : "memory");
     }
     __syncwarp();
 }
 
 // From a digit histogram, the digit that holds the need-th largest key (counting from
-// the top digit) and the number of keys still needed within it.  Returns the count of
-// keys with that digit.
-__device__ __forceinline__ int warp_pick_digit(const uint32_t *hist, int &need, uint32_t &digit, int lane)
+// the top digit) and the number of keys still needed within it.
+__device__ __forceinline__ void warp_pick_digit(uint32_t hist_s, int &need, uint32_t &digit, int lane)
 {
     // lane l holds digits 255 - 8l - i (i = 0..7): lanes run from the top digit down
     int c[8], sum = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        c[i] = static_cast<int>(hist[255 - 8 * lane - i]);
+        c[i] = static_cast<int>(lds_u32(hist_s + 4 * (255 - 8 * lane - i)));
         sum += c[i];
     }
     int incl = sum;
@@ -112,7 +117,7 @@ __device__ __forceinline__ int warp_pick_digit(const uint32_t *hist, int &need, 
             incl += n;
     }
     const int excl = incl - sum;
-    int dsel = -1, need_new = 0, cnt = 0;
+    int dsel = -1, need_new = 0;
     if (excl < need && need <= incl) {
         int acc = excl;
 #pragma unroll
@@ -120,7 +125,6 @@ __device__ __forceinline__ int warp_pick_digit(const uint32_t *hist, int &need, 
             if (dsel < 0 && acc + c[i] >= need) {
                 dsel = 255 - 8 * lane - i;
                 need_new = need - acc;
-                cnt = c[i];
             }
             acc += c[i];
         }
@@ -129,44 +133,59 @@ __device__ __forceinline__ int warp_pick_digit(const uint32_t *hist, int &need, 
     const int src = m != 0u ? __ffs(m) - 1 : 0;
     dsel = __shfl_sync(0xffffffffu, dsel, src);
     need_new = __shfl_sync(0xffffffffu, need_new, src);
-    cnt = __shfl_sync(0xffffffffu, cnt, src);
     if (m == 0u) {   // cannot happen with 1 <= need <= keys counted; keep the state sane
         dsel = 0;
         need_new = need;
-        cnt = 0;
     }
     digit = static_cast<uint32_t>(dsel);
     need = need_new;
-    return cnt;
 }
 
-// The exact top-k of one pair by one warp over the order keys of blocks [0, nb):
-// the k largest keys among candidates [n_init, nb - n_local) (equal keys: lower block
-// first), united with B_init and B_local, written ascending to out[0 .. count) and -1
-// after.  `coarse` is the histogram of key >> 22 over the candidates (built while the
-// keys were scored).  The k-th largest key lies in the coarse bin where the count
-// from the top reaches k; the keys of that bin are gathered into `list` (at most
-// kTopkList, else every candidate is scanned again) and the remaining 22 bits come
-// from an MSB-first radix select over byte digits.  `coarse` is reused for the digits.
-__device__ void topk_warp(const uint32_t *keys, uint32_t *coarse, uint32_t *list, int nb, int n_init, int n_local,
-                          int k, int *out, int k_tot, int *count_out, int *status, int lane)
+// The exact top-k of one pair by one warp over the order keys of blocks [0, nb) (shared
+// array at keys_s): the k largest keys among candidates [n_init, nb - n_local) (equal
+// keys: lower block first), united with B_init and B_local, written ascending to
+// out[0 .. count) and -1 after.  coarse_s holds the histogram of key >> 22 over the
+// candidates (built while the keys were scored).
+//   1. The coarse bin where the count from the top reaches k.
+//   2. One pass: each lane tests a contiguous run of candidates against the bin's lower
+//      bound (rotated so the lanes hit distinct banks) and writes the block ids of the
+//      keys at or above it, ascending, into list_s (kTopkList entries at most).
+//   3. The remaining 22 bits of the k-th key by an MSB-first radix select over byte
+//      digits of the listed keys that fall in the threshold bin.
+//   4. B_init, then the listed keys above the k-th key and the first `need` equal to it
+//      (block order), then B_local.
+// More than 2048 candidates, or more than kTopkList keys at or above the bin, take a
+// slower path that scans every candidate for each digit.  coarse_s is reused for the
+// digits.
+__device__ void topk_warp(uint32_t keys_s, uint32_t coarse_s, uint32_t list_s, int nb, int n_init, int n_local, int k,
+                          int *out, int k_tot, int *count_out, int *status, int lane)
 {
     const int cand_lo = n_init, cand_hi = nb - n_local;
-    const bool take_all = max(0, cand_hi - cand_lo) <= k;
+    const int n_cand = max(0, cand_hi - cand_lo);
+    const bool take_all = n_cand <= k;
     const bool take_none = k <= 0;
     const unsigned lt = (1u << lane) - 1u;
     uint32_t prefix = 0, pmask = 0;
     int need = k;
+    bool listed = false;
+    int n_list = 0;
     if (!take_all && !take_none) {
-        // coarse bin: lane l sums bins [1023 - 32l - 31, 1023 - 32l]
+        // 1. the coarse bin: lane l holds bins [1024 - 32(l+1), 1024 - 32l)
         constexpr int kPer = kCoarseBins / 32;
-        const uint32_t *mine = coarse + (kCoarseBins - kPer * (lane + 1));
-        int c = 0;
+        const int bin0 = kCoarseBins - kPer * (lane + 1);
+        uint32_t cb[kPer];
 #pragma unroll
         for (int i = 0; i < kPer; i += 4) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(mine + i);
-            c += static_cast<int>(v.x + v.y + v.z + v.w);
+            const uint4 v = lds_v4(coarse_s + 4 * (bin0 + i));
+            cb[i] = v.x;
+            cb[i + 1] = v.y;
+            cb[i + 2] = v.z;
+            cb[i + 3] = v.w;
         }
+        int c = 0;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i)
+            c += static_cast<int>(cb[i]);
         int incl = c;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -178,10 +197,11 @@ __device__ void topk_warp(const uint32_t *keys, uint32_t *coarse, uint32_t *list
         int bsel = -1, need_new = 0, m = 0;
         if (excl < need && need <= incl) {
             int acc = excl;
-            for (int i = kPer - 1; i >= 0 && bsel < 0; --i) {
-                const int ci = static_cast<int>(mine[i]);
-                if (acc + ci >= need) {
-                    bsel = kCoarseBins - kPer * (lane + 1) + i;
+#pragma unroll
+            for (int i = kPer - 1; i >= 0; --i) {
+                const int ci = static_cast<int>(cb[i]);
+                if (bsel < 0 && acc + ci >= need) {
+                    bsel = bin0 + i;
                     need_new = need - acc;
                     m = ci;
                 }
@@ -191,86 +211,106 @@ __device__ void topk_warp(const uint32_t *keys, uint32_t *coarse, uint32_t *list
         const unsigned hit = __ballot_sync(0xffffffffu, bsel >= 0);
         const int src_lane = hit != 0u ? __ffs(hit) - 1 : 0;
         bsel = __shfl_sync(0xffffffffu, bsel, src_lane);
-        need = __shfl_sync(0xffffffffu, need_new, src_lane);
+        need_new = __shfl_sync(0xffffffffu, need_new, src_lane);
         m = __shfl_sync(0xffffffffu, m, src_lane);
-        const bool found = hit != 0u;   // always, when the histogram counts every candidate
-        prefix = found ? static_cast<uint32_t>(bsel) << kCoarseShift : 0u;
-        pmask = found ? ~((1u << kCoarseShift) - 1u) : 0u;
-        if (!found)
-            need = k;
-        __syncwarp();
-        const uint32_t *src = keys;
-        int lo = cand_lo, hi = cand_hi;
-        if (found && m <= kTopkList) {
-            // gather the keys of the threshold bin (four chunks of 32 in flight)
-            int n = 0;
-            for (int jb = cand_lo; jb < cand_hi; jb += 128) {
-                uint32_t kv[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int j = jb + 32 * u + lane;
-                    kv[u] = j < cand_hi ? keys[j] : 0u;
+        if (hit != 0u) {   // always, when the histogram counts every candidate
+            prefix = static_cast<uint32_t>(bsel) << kCoarseShift;
+            pmask = ~((1u << kCoarseShift) - 1u);
+            // keys strictly above the bin: k - need_new; the list holds them and the bin
+            const int expect = k - need_new + m;
+            need = need_new;
+            if (n_cand <= 32 * 64 && expect <= kTopkList) {
+                // 2. one pass over the candidates
+                const int per = ((n_cand + 31) / 32 + 31) & ~31;   // 32 or 64 (a multiple of 32)
+                const int jb = cand_lo + lane * per;
+                uint64_t hits = 0ull;
+#pragma unroll 8
+                for (int i = 0; i < per; ++i) {
+                    const int ii = (i + lane) & (per - 1);
+                    const int j = jb + ii;
+                    const uint32_t key = j < cand_hi ? lds_u32(keys_s + 4 * j) : 0u;
+                    if (j < cand_hi && key >= prefix)
+                        hits |= 1ull << ii;
                 }
+                const int cnt = __popcll(hits);
+                int off = cnt;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int j = jb + 32 * u + lane;
-                    const bool in = j < cand_hi && (kv[u] & pmask) == prefix;
-                    const unsigned bm = __ballot_sync(0xffffffffu, in);
-                    if (in)
-                        list[n + __popc(bm & lt)] = kv[u];
-                    n += __popc(bm);
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int n = __shfl_up_sync(0xffffffffu, off, o);
+                    if (lane >= o)
+                        off += n;
                 }
+                n_list = __shfl_sync(0xffffffffu, off, 31);
+                off -= cnt;
+                while (hits != 0ull) {
+                    const int bpos = __ffsll(static_cast<long long>(hits)) - 1;
+                    if (off < kTopkList)
+                        sts_u32(list_s + 4 * off, static_cast<uint32_t>(jb + bpos));
+                    ++off;
+                    hits &= hits - 1ull;
+                }
+                __syncwarp();
+                listed = n_list <= kTopkList;   // equal to `expect` unless the histogram was off
             }
-            __syncwarp();
-            src = list;
-            lo = 0;
-            hi = n;
+        } else {
+            need = k;
         }
+        // 3. the digits below the coarse bin (bits 23..16, 15..8, 7..0; 23 and 22 are fixed)
+        const uint32_t src_list = listed ? list_s : 0u;
+        const int lo = listed ? 0 : cand_lo, hi = listed ? n_list : cand_hi;
         uint32_t d;
-        if (!found) {
-            warp_digit_hist(src, lo, hi, 0u, 0u, 24, coarse, lane);
-            warp_pick_digit(coarse, need, d, lane);
+        if (pmask == 0u) {
+            warp_digit_hist(keys_s, src_list, lo, hi, 0u, 0u, 24, coarse_s, lane);
+            warp_pick_digit(coarse_s, need, d, lane);
             prefix = d << 24;
             pmask = 0xFF000000u;
         }
-        // the digits below the coarse bin: bits 23..16 (23 and 22 already fixed), 15..8, 7..0
-        warp_digit_hist(src, lo, hi, pmask, prefix, 16, coarse, lane);
-        warp_pick_digit(coarse, need, d, lane);
+        warp_digit_hist(keys_s, src_list, lo, hi, pmask, prefix, 16, coarse_s, lane);
+        warp_pick_digit(coarse_s, need, d, lane);
         prefix |= d << 16;
         pmask = 0xFFFF0000u;
-        warp_digit_hist(src, lo, hi, pmask, prefix, 8, coarse, lane);
-        warp_pick_digit(coarse, need, d, lane);
+        warp_digit_hist(keys_s, src_list, lo, hi, pmask, prefix, 8, coarse_s, lane);
+        warp_pick_digit(coarse_s, need, d, lane);
         prefix |= d << 8;
         pmask = 0xFFFFFF00u;
-        warp_digit_hist(src, lo, hi, pmask, prefix, 0, coarse, lane);
-        warp_pick_digit(coarse, need, d, lane);
+        warp_digit_hist(keys_s, src_list, lo, hi, pmask, prefix, 0, coarse_s, lane);
+        warp_pick_digit(coarse_s, need, d, lane);
         prefix |= d;
     }
-    // ascending compaction: B_init, B_local, keys above the k-th, and the first `need`
-    // keys equal to it in block order (four chunks of 32 loaded ahead)
+    // 4. ascending output: B_init, the selected candidates, B_local
+    const int n_i = min(n_init, nb);
+    const int l0 = max(nb - n_local, n_i);
     int pos0 = 0, eq_seen = 0;
     bool overflow = false;
-    for (int jb = 0; jb < nb; jb += 128) {
-        uint32_t kv[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int j = jb + 32 * u + lane;
-            kv[u] = (j < nb && j >= n_init && j < nb - n_local) ? keys[j] : 0u;
+    for (int j = lane; j < n_i; j += 32) {
+        if (j < k_tot)
+            out[j] = j;
+        else
+            overflow = true;
+    }
+    pos0 = n_i;
+    if (take_all) {
+        for (int j = cand_lo + lane; j < cand_hi; j += 32) {
+            const int pos = pos0 + (j - cand_lo);
+            if (pos < k_tot)
+                out[pos] = j;
+            else
+                overflow = true;
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int j = jb + 32 * u + lane;
-            bool sel = false, eq = false;
-            if (j < nb) {
-                if (j < n_init || j >= nb - n_local)
-                    sel = true;
-                else if (take_all)
-                    sel = true;
-                else if (!take_none) {
-                    sel = kv[u] > prefix;
-                    eq = kv[u] == prefix;
-                }
+        pos0 += n_cand;
+    } else if (!take_none) {
+        const bool from_list = listed;
+        const int hi = from_list ? n_list : cand_hi;
+        for (int ib = from_list ? 0 : cand_lo; ib < hi; ib += 32) {
+            const int i = ib + lane;
+            int j = -1;
+            uint32_t key = 0u;
+            if (i < hi) {
+                j = from_list ? static_cast<int>(lds_u32(list_s + 4 * i)) : i;
+                key = lds_u32(keys_s + 4 * j);
             }
+            bool sel = i < hi && key > prefix;
+            const bool eq = i < hi && key == prefix;
             const unsigned em = __ballot_sync(0xffffffffu, eq);
             if (eq)
                 sel = eq_seen + __popc(em & lt) < need;
@@ -286,6 +326,14 @@ __device__ void topk_warp(const uint32_t *keys, uint32_t *coarse, uint32_t *list
             pos0 += __popc(sm);
         }
     }
+    for (int j = l0 + lane; j < nb; j += 32) {
+        const int pos = pos0 + (j - l0);
+        if (pos < k_tot)
+            out[pos] = j;
+        else
+            overflow = true;
+    }
+    pos0 += max(0, nb - l0);
     if (__any_sync(0xffffffffu, overflow) && lane == 0)
         report(status, SPARSE_ERR_BAD_INDEX);
     for (int i = pos0 + lane; i < k_tot; i += 32)
@@ -294,11 +342,15 @@ __device__ void topk_warp(const uint32_t *keys, uint32_t *coarse, uint32_t *list
         *count_out = min(pos0, k_tot);
 }
 
-template <int NT>
+// ATTN = false: the Forecast selection alone (sparse_select_topk): no block list, no
+// attention, no merge; every input may be written by the kernel before this one.
+template <int NT, bool ATTN>
 __global__ void __launch_bounds__(kFThreads, 2)
     decode_forecast_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                            const AttnParams p)
 {
+    if (!ATTN)
+        griddep_wait();
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -381,17 +433,18 @@ __global__ void __launch_bounds__(kFThreads, 2)
         failed = __shfl_sync(0xffffffffu, failed, 0);
         it = __shfl_sync(0xffffffffu, it, 0);
         // this layer's block list may be the previous kernel's output
-        if ((p.flags & SPARSE_ATTN_BLOCKS_READY) == 0u)
+        if (ATTN && (p.flags & SPARSE_ATTN_BLOCKS_READY) == 0u)
             griddep_wait();
-        int n_run = producer_fetch_slice(p, pair, i0, cap, lslot, llog, ctrl, lane);
+        int n_run = ATTN ? producer_fetch_slice(p, pair, i0, cap, lslot, llog, ctrl, lane) : 0;
         if (failed) {
             n_run = 0;
             if (lane == 0)
                 ctrl[kCtrlList] = 0;
             __syncwarp();
         }
-        named_barrier_arrive(1, kAttnThreads);
-        if (lane == 0 && n_run > 0) {
+        if (ATTN)
+            named_barrier_arrive(1, kAttnThreads);
+        if (ATTN && lane == 0 && n_run > 0) {
             prefetch_tensormap(&kmap);
             prefetch_tensormap(&vmap);
             for (int i = 0; i < n_run; ++i, ++it) {
@@ -423,7 +476,8 @@ __global__ void __launch_bounds__(kFThreads, 2)
             f = make_float4(f01.x, f01.y, f23.x, f23.y);
         }
         QueryFrags<NT> q;
-        load_query<NT, false>(q, p, b, g, 0, p.G, lane);
+        if (ATTN)
+            load_query<NT, false>(q, p, b, g, 0, p.G, lane);
         cluster_wait();   // CTA 0's "scored" barrier and key array exist
         uint32_t *keys0 = static_cast<uint32_t *>(__cluster_map_shared_rank(keys, 0));
         uint32_t *coarse0 = static_cast<uint32_t *>(__cluster_map_shared_rank(hist, 0));
@@ -507,8 +561,9 @@ __global__ void __launch_bounds__(kFThreads, 2)
         if (lane == 0)
             mbar_arrive_cluster(dsmem_addr(bar_scored, 0));
         // (2) this layer's attention over the staged slice of its block list
-        named_barrier_sync(1, kAttnThreads);
-        const int n_run = ok ? ctrl[kCtrlList] : 0;
+        if (ATTN)
+            named_barrier_sync(1, kAttnThreads);
+        const int n_run = ATTN && ok ? ctrl[kCtrlList] : 0;
         for (int i = 0; i < n_run; ++i, ++it) {
             const int s = it % kStages;
             if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8 * s, (it / kStages) & 1, kWaitNs))) {
@@ -535,8 +590,8 @@ __global__ void __launch_bounds__(kFThreads, 2)
             if (score)
                 ready = __all_sync(0xffffffffu, mbar_wait_cluster(bar_scored, 0, kWaitNs));
             if (ready) {
-                topk_warp(keys, hist, reinterpret_cast<uint32_t *>(base + fused_off_topk_list()), nb, p.n_init,
-                          p.n_local, p.k_sel,
+                topk_warp(base_s + fused_off_keys(per), base_s + fused_off_hist(), base_s + fused_off_topk_list(), nb,
+                          p.n_init, p.n_local, p.k_sel,
                           p.idx_next + static_cast<size_t>(pair) * p.k_tot_next, p.k_tot_next, p.count_next + pair,
                           p.status, lane);
             } else if (lane == 0) {
@@ -547,18 +602,20 @@ __global__ void __launch_bounds__(kFThreads, 2)
     }
 
     // ---------------------------------------------------------------- merge
-    __syncthreads();
-    cluster_merge_write<NT, false>(st, base, false, p, b, g, 0, p.G, rank, S, kFThreads);
+    if (ATTN) {
+        __syncthreads();
+        cluster_merge_write<NT, false>(st, base, false, p, b, g, 0, p.G, rank, S, kFThreads);
+    }
 }
 
 // The "scored" barrier lives in the ctrl words, 8-byte aligned.
 static_assert((kOffCtrl + 4 * kCtrlScoredBar) % 8 == 0 && 4 * kCtrlScoredBar + 8 <= 64, "ctrl layout");
 
-template <int NT>
+template <int NT, bool ATTN>
 int launch_fused(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, int S, long long pairs,
                  size_t smem, int device, cudaStream_t stream)
 {
-    auto kern = decode_forecast_kernel<NT>;
+    auto kern = decode_forecast_kernel<NT, ATTN>;
     static int configured[64];
     int rc = sp_host::configure_kernel(reinterpret_cast<const void *>(kern), static_cast<int>(smem), device,
                                        configured);
@@ -675,6 +732,54 @@ extern "C" SPARSE_API int sparse_decode_attn_forecast(
     if ((rc = sp_host::make_kv_tensor_map(&vm, v_cache, T_cap, pairs)) != SPARSE_OK)
         return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return G <= 8 ? launch_fused<1>(p, km, vm, S, pairs, smem, dev.device, st)
-                  : launch_fused<2>(p, km, vm, S, pairs, smem, dev.device, st);
+    return G <= 8 ? launch_fused<1, true>(p, km, vm, S, pairs, smem, dev.device, st)
+                  : launch_fused<2, true>(p, km, vm, S, pairs, smem, dev.device, st);
+}
+
+extern "C" SPARSE_API int sparse_select_topk(const uint16_t *F, const float *ktil, const int *seq_len, int B,
+                                             int H_kv, int N_cap, int n_init, int n_local, int k, int *idx_out,
+                                             int *count_out, int k_tot, int *status, void *stream)
+{
+    using sp_host::aligned16;
+    using sp_host::fail;
+    if (!F || !ktil || !seq_len || !idx_out || !count_out)
+        return fail(SPARSE_ERR_INVALID_ARG, "sparse_select_topk: null pointer");
+    if (!aligned16(F) || !aligned16(ktil))
+        return fail(SPARSE_ERR_INVALID_ARG, "sparse_select_topk: F and ktil must be 16-byte aligned");
+    if (B < 1 || H_kv < 1 || N_cap < 1 || n_init < 0 || n_local < 0 || k < 0)
+        return fail(SPARSE_ERR_INVALID_ARG, "sparse_select_topk: bad size");
+    if (static_cast<long long>(n_init) + n_local + k > k_tot)
+        return fail(SPARSE_ERR_INVALID_ARG, "sparse_select_topk: k_tot=%d < n_init+n_local+k", k_tot);
+    const long long pairs = static_cast<long long>(B) * H_kv;
+    if (pairs > 65535)
+        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_select_topk: B*H_kv=%lld > 65535", pairs);
+    sp_host::DeviceInfo dev;
+    int rc = sp_host::device_info(&dev);
+    if (rc != SPARSE_OK)
+        return rc;
+    // cluster size: enough CTAs to cover the SMs twice, at least 128 key rows per CTA
+    int S = 1;
+    while (S < kMaxSplit && pairs * S * 2 <= 2LL * dev.sm_count && N_cap / (S * 2) >= 128)
+        S *= 2;
+    const size_t smem = fused_smem_bytes(0, N_cap);
+    if (smem > static_cast<size_t>(dev.max_smem_optin))
+        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_select_topk: N_cap=%d needs %zu bytes of shared memory", N_cap,
+                    smem);
+    AttnParams p = {};
+    p.seq_len = seq_len;
+    p.status = status;
+    p.H_kv = H_kv;
+    p.k_tot = 0;   // no block list of this layer: selection only
+    p.F = F;
+    p.ktil = ktil;
+    p.idx_next = idx_out;
+    p.count_next = count_out;
+    p.N_cap = N_cap;
+    p.n_init = n_init;
+    p.n_local = n_local;
+    p.k_sel = k;
+    p.k_tot_next = k_tot;
+    CUtensorMap unused;
+    memset(&unused, 0, sizeof unused);
+    return launch_fused<1, false>(p, unused, unused, S, pairs, smem, dev.device, static_cast<cudaStream_t>(stream));
 }
