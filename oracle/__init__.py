@@ -59,6 +59,8 @@ def load_library(path: str):
     lib.oracle_pool.argtypes = [P, i64, i32, P, i32, P]
     lib.oracle_select.argtypes = [P, P, i32, i32, P, i32, i32, i32, i32, P, P, P]
     lib.oracle_select.restype = i32
+    lib.oracle_select_heads.argtypes = [P, i32, P, i32, i32, P, ctypes.c_double, i32, i32, i32, i32, P, P, P]
+    lib.oracle_select_heads.restype = i32
     lib.oracle_attn.argtypes = [P, i32, P, P, i64, i32, P, P, i32, P, f64, P, P]
     lib.oracle_verify.argtypes = [P, P, P, i64, i32, i32, i32, i32, P, i32, i32, i32, P,
                                   f64, P, P, P]
@@ -128,6 +130,28 @@ def select(F, ktil, lens, n_init: int, n_local: int, k: int, k_tot: int | None =
                                k_tot, _ptr(idx), _ptr(count), _ptr(scores))
     if rc != 0:
         raise ValueError("oracle_select: a pair needs more than k_tot or n_blocks_cap entries")
+    return idx, count, scores
+
+
+def select_heads(Q, ktil, lens, n_init: int, n_local: int, k: int, k_tot: int | None = None, scale: float = 0.0):
+    """Multi-head (InfLLM-V2) block selection from Q [P][G][128] bf16 bits: per-head
+    softmax of scale * q_h . ktil_j over the blocks, summed over heads, then the top-k.
+    Returns (idx [P][k_tot] int32, count [P] int32, scores [P][N] fp64)."""
+    Q = _u16(Q)
+    ktil = np.ascontiguousarray(ktil, dtype=np.float64)
+    lens = _i64(lens)
+    P, n_cap, d = ktil.shape
+    G = Q.shape[1]
+    assert d == D and Q.shape == (P, G, D) and lens.shape == (P,)
+    if k_tot is None:
+        k_tot = n_init + n_local + k
+    idx = np.empty((P, k_tot), dtype=np.int32)
+    count = np.empty((P,), dtype=np.int32)
+    scores = np.empty((P, n_cap), dtype=np.float64)
+    rc = _load().oracle_select_heads(_ptr(Q), G, _ptr(ktil), n_cap, P, _ptr(lens), float(scale), n_init, n_local,
+                                     k, k_tot, _ptr(idx), _ptr(count), _ptr(scores))
+    if rc != 0:
+        raise ValueError("oracle_select_heads: a pair needs more than k_tot or n_blocks_cap entries")
     return idx, count, scores
 
 

@@ -21,6 +21,9 @@
  *                  vector against every compressed key (one head per GQA group,
  *                  §4.3 eq.(9)), take the k best blocks outside the init and local
  *                  blocks, and return init ∪ local ∪ top-k in ascending order.
+ *   oracle_select_heads  the InfLLM-V2 multi-head selector that [SparDA] §4.3 (eq.(8),
+ *                  Figure 3) compares against: G query heads score, per-head softmax
+ *                  over the blocks, summed over heads, then the same top-k.
  *   oracle_attn    [SparDA] §4.1 eq.(7): attention of each query head of the group
  *                  over the tokens of the selected blocks, with the 1/sqrt(d) scale
  *                  of [SSV] "NSA three-branch math" step 3.
@@ -142,6 +145,53 @@ static int cand_order(const void *a, const void *b)
  * receives s_j for every block j < N_b (the rest zero).
  * Returns 0, or -1 when a pair needs more than k_tot or n_blocks_cap entries.
  */
+/*
+ * The selection of one pair from its block scores s[0 .. nb): B_init = [0, n_init),
+ * B_local = [nb - n_local, nb), and the k candidates (all other blocks) of largest
+ * score, a full sort deciding ties towards the lower index; idx[0 .. count) ascending,
+ * padded with -1 up to k_tot.  Returns 1 when the union needs more than k_tot entries.
+ */
+static int select_from_scores(const double *s, int nb, int n_init, int n_local, int k, int k_tot, int *out,
+                              int *count)
+{
+    char *chosen = (char *)calloc((size_t)nb + 1, 1);
+    cand_t *cand = (cand_t *)malloc(sizeof(cand_t) * ((size_t)nb + 1));
+    for (int j = 0; j < nb && j < n_init; ++j)
+        chosen[j] = 1;
+    for (int j = nb - n_local; j < nb; ++j)
+        if (j >= 0)
+            chosen[j] = 1;
+    int nc = 0;
+    for (int j = 0; j < nb; ++j) {
+        if (!chosen[j]) {
+            cand[nc].s = s[j];
+            cand[nc].j = j;
+            ++nc;
+        }
+    }
+    qsort(cand, (size_t)nc, sizeof(cand_t), cand_order);
+    for (int r = 0; r < nc && r < k; ++r)
+        chosen[cand[r].j] = 1;
+    int c = 0, bad = 0;
+    for (int j = 0; j < nb; ++j) {
+        if (!chosen[j])
+            continue;
+        if (c < k_tot)
+            out[c] = j;
+        ++c;
+    }
+    if (c > k_tot) {
+        bad = 1;
+        c = k_tot;
+    }
+    *count = c;
+    for (int r = c; r < k_tot; ++r)
+        out[r] = -1;
+    free(cand);
+    free(chosen);
+    return bad;
+}
+
 int oracle_select(const uint16_t *F, const double *ktil, int n_blocks_cap, int n_pairs,
                   const long long *len, int n_init, int n_local, int k, int k_tot,
                   int *idx, int *count, double *scores)
@@ -159,50 +209,83 @@ int oracle_select(const uint16_t *F, const double *ktil, int n_blocks_cap, int n
         double Fp[D];
         for (int d = 0; d < D; ++d)
             Fp[d] = bf16_value(F[(size_t)p * D + d]);
-        char *chosen = (char *)calloc((size_t)nb + 1, 1);
-        cand_t *cand = (cand_t *)malloc(sizeof(cand_t) * ((size_t)nb + 1));
-        for (int j = 0; j < nb && j < n_init; ++j)
-            chosen[j] = 1;
-        for (int j = nb - n_local; j < nb; ++j)
-            if (j >= 0)
-                chosen[j] = 1;
-        int nc = 0;
+        double *s = (double *)malloc(sizeof(double) * ((size_t)nb + 1));
         for (int j = 0; j < nb; ++j) {
             const double *kj = ktil + ((size_t)p * n_blocks_cap + j) * D;
-            double s = 0.0;
+            double acc = 0.0;
             for (int d = 0; d < D; ++d)
-                s += Fp[d] * kj[d];
-            if (scores)
-                scores[(size_t)p * n_blocks_cap + j] = s;
-            if (!chosen[j]) {
-                cand[nc].s = s;
-                cand[nc].j = j;
-                ++nc;
-            }
+                acc += Fp[d] * kj[d];
+            s[j] = acc;
         }
-        if (scores)
-            for (int j = nb; j < n_blocks_cap; ++j)
-                scores[(size_t)p * n_blocks_cap + j] = 0.0;
-        qsort(cand, (size_t)nc, sizeof(cand_t), cand_order);
-        for (int r = 0; r < nc && r < k; ++r)
-            chosen[cand[r].j] = 1;
-        int c = 0;
-        for (int j = 0; j < nb; ++j) {
-            if (!chosen[j])
-                continue;
-            if (c < k_tot)
-                out[c] = j;
-            ++c;
+        if (scores) {
+            for (int j = 0; j < n_blocks_cap; ++j)
+                scores[(size_t)p * n_blocks_cap + j] = j < nb ? s[j] : 0.0;
         }
-        if (c > k_tot) {
+        bad |= select_from_scores(s, nb, n_init, n_local, k, k_tot, out, count + p);
+        free(s);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * Multi-head selection of InfLLM-V2, the baseline of [SparDA] §4.3 (eq.(8) and its
+ * Figure 3): every one of the G query heads of the group scores every compressed key,
+ *     a^h_j = scale * <q_h, ktil_j>,   j < N_b,
+ * each head's scores pass through a softmax over the pair's blocks, and the G
+ * distributions are summed,
+ *     s_j = sum_h exp(a^h_j) / sum_i exp(a^h_i);
+ * then the k largest s_j outside the init and local blocks are taken as in
+ * oracle_select.  Readings: the softmax runs over all N_b blocks (init and local
+ * included); the max-pooling of the notes maps overlapping compression windows onto
+ * selection blocks and is the identity for non-overlapping 64-token blocks; scale is
+ * the attention scale (1/sqrt(d) when 0 is passed).
+ *   Q [n_pairs][G][D] bf16 bits.  scores (nullable) receives s_j (the rest zero).
+ */
+int oracle_select_heads(const uint16_t *Q, int G, const double *ktil, int n_blocks_cap, int n_pairs,
+                        const long long *len, double scale, int n_init, int n_local, int k, int k_tot,
+                        int *idx, int *count, double *scores)
+{
+    if (scale == 0.0)
+        scale = 1.0 / sqrt((double)D);
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int p = 0; p < n_pairs; ++p) {
+        int nb = blocks_of(len[p]);
+        int *out = idx + (size_t)p * k_tot;
+        if (nb > n_blocks_cap) {
             bad |= 1;
-            c = k_tot;
+            count[p] = 0;
+            continue;
         }
-        count[p] = c;
-        for (int r = c; r < k_tot; ++r)
-            out[r] = -1;
-        free(cand);
-        free(chosen);
+        double *a = (double *)malloc(sizeof(double) * ((size_t)nb + 1));
+        double *s = (double *)calloc((size_t)nb + 1, sizeof(double));
+        for (int h = 0; h < G; ++h) {
+            double q[D];
+            for (int d = 0; d < D; ++d)
+                q[d] = bf16_value(Q[((size_t)p * G + h) * D + d]);
+            double m = -INFINITY;
+            for (int j = 0; j < nb; ++j) {
+                const double *kj = ktil + ((size_t)p * n_blocks_cap + j) * D;
+                double acc = 0.0;
+                for (int d = 0; d < D; ++d)
+                    acc += q[d] * kj[d];
+                a[j] = scale * acc;
+                if (a[j] > m)
+                    m = a[j];
+            }
+            double z = 0.0;
+            for (int j = 0; j < nb; ++j)
+                z += exp(a[j] - m);
+            for (int j = 0; j < nb; ++j)
+                s[j] += exp(a[j] - m) / z;
+        }
+        if (scores) {
+            for (int j = 0; j < n_blocks_cap; ++j)
+                scores[(size_t)p * n_blocks_cap + j] = j < nb ? s[j] : 0.0;
+        }
+        bad |= select_from_scores(s, nb, n_init, n_local, k, k_tot, out, count + p);
+        free(s);
+        free(a);
     }
     return bad ? -1 : 0;
 }

@@ -356,18 +356,63 @@ def test_gather_is_a_plain_copy():
     assert np.all(ring[0, 3] == 0)
 
 
+# ----------------------------------------------------------------------------- multi-head selection
+
+
+def _heads_case(seed, P=3, G=4, N=40, lens=(40 * 64, 23 * 64 + 5, 3 * 64)):
+    rng = np.random.default_rng(seed)
+    Q = rand_bits((P, G, D), seed + 100)
+    ktil = rng.standard_normal((P, N, D)) * 0.3
+    return Q, ktil, np.asarray(lens, dtype=np.int64)
+
+
+def test_select_heads_with_one_head_is_the_forecast_selection():
+    # softmax is monotone, so one head selects exactly what its raw scores select
+    Q, ktil, lens = _heads_case(1, G=1)
+    idx_h, cnt_h, _ = oracle.select_heads(Q, ktil, lens, 1, 2, 6)
+    idx_f, cnt_f, _ = oracle.select(Q[:, 0], ktil, lens, 1, 2, 6)
+    assert np.array_equal(idx_h, idx_f) and np.array_equal(cnt_h, cnt_f)
+
+
+def test_select_heads_scores_are_a_sum_of_head_distributions():
+    # each head contributes a distribution over the pair's blocks: the sum is G
+    Q, ktil, lens = _heads_case(2, G=4)
+    _, _, s = oracle.select_heads(Q, ktil, lens, 1, 2, 6)
+    for p, n in enumerate(lens):
+        nb = (int(n) + 63) // 64
+        assert abs(s[p, :nb].sum() - 4.0) < 1e-12
+        assert not s[p, nb:].any()
+
+
+def test_select_heads_match_scipy_softmax_and_brute_force_topk():
+    from scipy.special import softmax
+    Q, ktil, lens = _heads_case(3, G=4)
+    scale = 0.37
+    idx, cnt, s = oracle.select_heads(Q, ktil, lens, 1, 2, 6, scale=scale)
+    for p, n in enumerate(lens):
+        nb = (int(n) + 63) // 64
+        q = values(Q[p])                                           # [G][D]
+        a = scale * q @ ktil[p, :nb].T                             # [G][nb]
+        ref = softmax(a, axis=1).sum(axis=0)
+        assert np.allclose(s[p, :nb], ref, rtol=1e-12, atol=1e-15)
+        cand = [j for j in range(nb) if 1 <= j < nb - 2]
+        top = sorted(cand, key=lambda j: (-ref[j], j))[:6]
+        want = sorted(set(range(min(1, nb))) | set(range(max(nb - 2, 0), nb)) | set(top))
+        assert list(idx[p, :cnt[p]]) == want
+
+
 # ----------------------------------------------------------------------------- mutants
 
 MUTANTS = [
     # pooling divides by the full block size instead of the tokens present
     ("sum[d] / (double)n", "sum[d] / (double)BLK"),
     # score reads the wrong operand dimension
-    ("s += Fp[d] * kj[d];", "s += Fp[d] * kj[(d + 1) % D];"),
+    ("acc += Fp[d] * kj[d];", "acc += Fp[d] * kj[(d + 1) % D];"),
     # ties go to the higher block index
     ("return (x->j > y->j) - (x->j < y->j);", "return (x->j < y->j) - (x->j > y->j);"),
     # the local window is one block short
-    ("for (int j = nb - n_local; j < nb; ++j)\n            if (j >= 0)\n                chosen[j] = 1;",
-     "for (int j = nb - n_local + 1; j < nb; ++j)\n            if (j >= 0)\n                chosen[j] = 1;"),
+    ("for (int j = nb - n_local; j < nb; ++j)\n        if (j >= 0)\n            chosen[j] = 1;",
+     "for (int j = nb - n_local + 1; j < nb; ++j)\n        if (j >= 0)\n            chosen[j] = 1;"),
     # the softmax scale is dropped
     ("a[n] = scale * dot;", "a[n] = dot;"),
     # values read from the key cache
@@ -378,6 +423,12 @@ MUTANTS = [
     ("for (int j = nb - window_blocks; j < nb; ++j)", "for (int j = nb - window_blocks + 1; j < nb; ++j)"),
     # the bf16 widening uses the wrong half
     ("uint32_t u = (uint32_t)bits << 16;", "uint32_t u = (uint32_t)bits << 15;"),
+    # multi-head selection sums raw scores instead of per-head distributions
+    ("s[j] += exp(a[j] - m) / z;", "s[j] += a[j];"),
+    # multi-head softmax normalised over the candidates only
+    ("z += exp(a[j] - m);", "z += j >= n_init ? exp(a[j] - m) : 0.0;"),
+    # multi-head scores without the scale
+    ("a[j] = scale * acc;", "a[j] = acc;"),
 ]
 
 PIN_TESTS = [
@@ -389,7 +440,8 @@ PIN_TESTS = [
     test_attn_block_subset_equals_masked_sdpa_and_ignores_order_and_repeats,
     test_attn_scale_argument_is_applied, test_attn_equal_keys_give_mean_of_values,
     test_attn_constant_values_and_single_token, test_verify_worked_example_of_the_ssv_page,
-    test_verify_equals_masked_sdpa_per_query,
+    test_verify_equals_masked_sdpa_per_query, test_select_heads_with_one_head_is_the_forecast_selection,
+    test_select_heads_scores_are_a_sum_of_head_distributions, test_select_heads_match_scipy_softmax_and_brute_force_topk,
 ]
 
 
