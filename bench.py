@@ -644,8 +644,9 @@ def run_layer_case(args, local_rank):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.ones(max(1, args.flush_mb) << 20 >> 2, dtype=torch.int32, device=dev)
     ws = None if args.no_workspace else binding.decode_workspace(B, H_q, H_kv, k_cap, args.n_split, device=dev)
-    sel_ms, att_ms, fus_ms = [], [], []
+    sel_ms, att_ms, fus_ms, hds_ms = [], [], [], []
     idx2, cnt2 = torch.empty_like(idx), torch.empty_like(cnt)
+    idx3, cnt3 = torch.empty_like(idx), torch.empty_like(cnt)
     for i in range(args.warmup + args.steps):
         F = wl.forecast(sh, 0, i, dev)
         Q = wl.queries(sh, i, dev)
@@ -670,8 +671,15 @@ def run_layer_case(args, local_rank):
                                                 n_local=sh.n_local, k=sh.k, idx_next=idx2, count_next=cnt2,
                                                 n_split=args.n_split, status=status)
         e5.record()
+        # the multi-head (InfLLM-V2) selector on the same compressed keys, for comparison
+        l2_evict(flush)
+        e6, e7 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e6.record()
+        binding.sparse_select_topk_heads(Q, kt, seq, sh.n_init, sh.n_local, sh.k, idx3, cnt3, status=status)
+        e7.record()
         torch.cuda.synchronize(dev)
         if i >= args.warmup:
+            hds_ms.append(e6.elapsed_time(e7))
             sel_ms.append(e[0].elapsed_time(e[1]))
             att_ms.append(e3.elapsed_time(e[2]))
             fus_ms.append(e4.elapsed_time(e5))
@@ -680,18 +688,23 @@ def run_layer_case(args, local_rank):
     attn_bytes = sh.pairs * sh.k_tot * KV_BLOCK_BYTES
     sel_bytes = sh.pairs * sh.N_b * KTIL_ROW_BYTES
     a, s_ = max(1e-6, statistics.median(att_ms)), statistics.median(sel_ms)
-    f_ = max(1e-6, statistics.median(fus_ms))
+    f_ = max(1e-6, statistics.median(fus_ms)) if fus_ms else 1e-6
+    h_ = statistics.median(hds_ms)
     if not select_only:
         assert torch.equal(idx2, idx) and torch.equal(cnt2, cnt), "fused selection differs from sparse_select_topk"
-    print(json.dumps({"case": "decode_128k_one_layer", "T": T, "steps": args.steps, "n_split": args.n_split,
-                      "attn_us": round(a * 1e3, 2), "attn_gbs": round(attn_bytes / a / 1e6, 1),
-                      "attn_frac": round(attn_bytes / a / 1e6 / peak, 4),
-                      "select_us": round(s_ * 1e3, 2), "select_gbs": round(sel_bytes / s_ / 1e6, 1),
-                      "select_frac": round(sel_bytes / s_ / 1e6 / peak, 4),
-                      "fused_us": round(f_ * 1e3, 2), "fused_gbs": round((attn_bytes + sel_bytes) / f_ / 1e6, 1),
-                      "fused_frac": round((attn_bytes + sel_bytes) / f_ / 1e6 / peak, 4),
-                      "peak_gbs": peak, "peak_source": src}),
-          flush=True)
+    line = {"case": "decode_128k_one_layer", "T": T, "steps": args.steps, "n_split": args.n_split,
+            "attn_us": round(a * 1e3, 2), "attn_gbs": round(attn_bytes / a / 1e6, 1),
+            "attn_frac": round(attn_bytes / a / 1e6 / peak, 4),
+            "select_us": round(s_ * 1e3, 2), "select_gbs": round(sel_bytes / s_ / 1e6, 1),
+            "select_frac": round(sel_bytes / s_ / 1e6 / peak, 4),
+            "heads_select_us": round(h_ * 1e3, 2), "heads_over_forecast": round(h_ / s_, 3),
+            "fused_us": round(f_ * 1e3, 2), "fused_gbs": round((attn_bytes + sel_bytes) / f_ / 1e6, 1),
+            "fused_frac": round((attn_bytes + sel_bytes) / f_ / 1e6 / peak, 4),
+            "peak_gbs": peak, "peak_source": src}
+    if select_only:   # only the selectors ran
+        for key in ("attn_us", "attn_gbs", "attn_frac", "fused_us", "fused_gbs", "fused_frac"):
+            line.pop(key)
+    print(json.dumps(line), flush=True)
 
 
 # ----------------------------------------------------------------------------- the other workloads

@@ -41,6 +41,7 @@ SIGNATURES = {
     "sparse_version": (_I, []),
     "sparse_pool_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _LL, _I, _LL, _I, _P]),
     "sparse_select_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P]),
+    "sparse_select_topk_heads": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _P, _P, _I, _P, _P]),
     "sparse_decode_attn": (_I, [_P, _P, _P, _LL, _P, _P, _P, _I, _P, _I, _I, _I, _F, _P, _P, _I, _U, _P, _SZ,
                                 _P, _P]),
     "sparse_decode_attn_ex": (_I, [_P, _P, _P, _LL, _P, _P, _P, _I, _P, _I, _I, _I, _F, _P, _P, _I, _U, _P, _SZ,
@@ -142,6 +143,26 @@ def sparse_select_topk(F, ktil, seq_len, n_init: int, n_local: int, k: int, idx_
     rc = load().sparse_select_topk(_ptr(F), _ptr(ktil), _ptr(seq_len), B, H_kv, N_cap, n_init, n_local, k,
                                    _ptr(idx_out), _ptr(count_out), k_tot, _ptr(status), _stream(stream))
     _check(rc, "sparse_select_topk")
+
+
+def sparse_select_topk_heads(Q, ktil, seq_len, n_init: int, n_local: int, k: int, idx_out, count_out,
+                             scale: float = 0.0, status=None, stream=None):
+    """Multi-head (InfLLM-V2) selection: Q [B][H_q][128] bf16, ktil [B][H_kv][N_cap][128]
+    fp32 -> idx_out [B][H_kv][k_tot], count_out [B][H_kv]."""
+    B, H_kv, N_cap, _ = ktil.shape
+    H_q = Q.shape[1]
+    k_tot = idx_out.shape[2]
+    _need(Q, "Q", torch.bfloat16, shape=(B, H_q, D))
+    _need(ktil, "ktil", torch.float32)
+    _need(seq_len, "seq_len", torch.int32, shape=(B,))
+    _need(idx_out, "idx_out", torch.int32, shape=(B, H_kv, k_tot))
+    _need(count_out, "count_out", torch.int32, shape=(B, H_kv))
+    if status is not None:
+        _need(status, "status", torch.int32)
+    rc = load().sparse_select_topk_heads(_ptr(Q), _ptr(ktil), _ptr(seq_len), B, H_q, H_kv, N_cap, float(scale),
+                                         n_init, n_local, k, _ptr(idx_out), _ptr(count_out), k_tot, _ptr(status),
+                                         _stream(stream))
+    _check(rc, "sparse_select_topk_heads")
 
 
 def _decode_args(Q, k_base, v_base, blk_logical, count, seq_len, O, lse, blk_slot):

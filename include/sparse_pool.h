@@ -100,6 +100,28 @@ SPARSE_API int sparse_select_topk(const uint16_t *F, const float *ktil, const in
                                   void *stream);
 
 /*
+ * sparse_select_topk_heads -- the multi-head block selector of InfLLM-V2, the baseline
+ * that [SparDA] §4.3 (eq.(8) and its Figure 3) compares the Forecast selector with:
+ * every one of the G = H_q / H_kv query heads of pair p scores every compressed key,
+ *     a^h_j = scale * q_h . ktil_j,   j < N_b = ceil(seq_len[b] / 64),
+ * each head's scores pass through a softmax over the pair's N_b blocks, and
+ *     s_j = sum_h softmax_j(a^h)
+ * replaces the Forecast score; the k largest s_j outside B_init and B_local are taken
+ * (equal keys: lower block index) and idx_out / count_out are written as by
+ * sparse_select_topk.  (The notes' max-pooling onto selection blocks is the identity
+ * for non-overlapping 64-token blocks.)  Scores and sums are fp32.
+ *   Q          [B][H_q][128] bf16: the query heads of the layer selected for.
+ *   ktil, seq_len, N_cap, n_init, n_local, k, idx_out, count_out, k_tot, status
+ *              as for sparse_select_topk.
+ *   scale      0 selects 1/sqrt(128).  G <= 16.
+ * Launch order as for sparse_select_topk (every input may come from the kernel before).
+ */
+SPARSE_API int sparse_select_topk_heads(const uint16_t *Q, const float *ktil, const int *seq_len,
+                                        int B, int H_q, int H_kv, int N_cap, float scale,
+                                        int n_init, int n_local, int k, int *idx_out,
+                                        int *count_out, int k_tot, int *status, void *stream);
+
+/*
  * sparse_decode_attn -- [SparDA] §4.1 eq.(7), §4.2 Alg.1 step 4; scale 1/sqrt(d) per
  * the [SSV] NSA selection branch (step 3); split-KV merge by the online-softmax
  * recurrence of [SSV] "online softmax state merging".

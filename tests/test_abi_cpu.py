@@ -152,3 +152,22 @@ def test_decode_attn_forecast_rejects_bad_arguments(lib):
     assert call(ktil=ODD) == binding.SPARSE_ERR_INVALID_ARG
     assert call(n_local=-1) == binding.SPARSE_ERR_INVALID_ARG
     assert call(scale=float("inf")) == binding.SPARSE_ERR_INVALID_ARG
+
+
+def test_select_heads_rejects_bad_arguments(lib):
+    f = lib.sparse_select_topk_heads
+    #        Q     ktil  seq   B  H_q H_kv N_cap scale init local k  idx   cnt   k_tot status stream
+    args = [FAKE, FAKE, FAKE, 1, 8, 2, 64, 0.0, 1, 2, 8, FAKE, FAKE, 11, None, None]
+    assert len(args) == len(binding.SIGNATURES["sparse_select_topk_heads"][1])
+
+    def call(i, v):
+        a = list(args)
+        a[i] = v
+        return f(*a)
+
+    assert call(0, None) == binding.SPARSE_ERR_INVALID_ARG                 # no Q
+    assert call(1, ODD) == binding.SPARSE_ERR_INVALID_ARG                  # misaligned keys
+    assert call(4, 9) == binding.SPARSE_ERR_INVALID_ARG                    # H_q not a multiple of H_kv
+    assert call(4, 64) == binding.SPARSE_ERR_UNSUPPORTED                   # G = 32 > 16
+    assert call(7, -1.0) == binding.SPARSE_ERR_INVALID_ARG                 # negative scale
+    assert call(13, 10) == binding.SPARSE_ERR_INVALID_ARG                  # k_tot < n_init + n_local + k
