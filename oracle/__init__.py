@@ -64,6 +64,7 @@ def load_library(path: str):
     lib.oracle_attn.argtypes = [P, i32, P, P, i64, i32, P, P, i32, P, f64, P, P]
     lib.oracle_verify.argtypes = [P, P, P, i64, i32, i32, i32, i32, P, i32, i32, i32, P,
                                   f64, P, P, P]
+    lib.oracle_verify_shared.argtypes = lib.oracle_verify.argtypes
     lib.oracle_gather.argtypes = [P, i64, i32, P, P, i32, P]
     return lib
 
@@ -173,9 +174,11 @@ def attn(Q, K, V, blocks, count, lens, scale: float | None = None):
     return O, lse
 
 
-def verify(Q, K, V, I, C: int, window_blocks: int, lens, scale: float | None = None):
-    """Mode-A grouped verification.  Q [B][N_q][H_q][128], K/V [B][H_kv][T][128],
-    I [B][H_kv][N_q][n_sel].  Returns (O [B][N_q][H_q][128], union_blocks, per_query_blocks)."""
+def verify(Q, K, V, I, C: int, window_blocks: int, lens, scale: float | None = None, shared: bool = False):
+    """Grouped verification, mode A (each query over its own set; the group loads the
+    merged union) or, with ``shared``, mode B (every query over its group's first
+    query's set).  Q [B][N_q][H_q][128], K/V [B][H_kv][T][128], I [B][H_kv][N_q][n_sel].
+    Returns (O [B][N_q][H_q][128], union_blocks, per_query_blocks)."""
     Q, K, V = _u16(Q), _u16(K), _u16(V)
     I, lens = _i32(I), _i64(lens)
     B, N_q, H_q, d = Q.shape
@@ -187,8 +190,9 @@ def verify(Q, K, V, I, C: int, window_blocks: int, lens, scale: float | None = N
     O = np.empty((B, N_q, H_q, D), dtype=np.float64)
     u = np.zeros(1, dtype=np.int64)
     pq = np.zeros(1, dtype=np.int64)
-    _load().oracle_verify(_ptr(Q), _ptr(K), _ptr(V), T_cap, B, H_q, H_kv, N_q, _ptr(I), n_sel,
-                          C, window_blocks, _ptr(lens), float(scale), _ptr(O), _ptr(u), _ptr(pq))
+    fn = _load().oracle_verify_shared if shared else _load().oracle_verify
+    fn(_ptr(Q), _ptr(K), _ptr(V), T_cap, B, H_q, H_kv, N_q, _ptr(I), n_sel, C, window_blocks, _ptr(lens),
+       float(scale), _ptr(O), _ptr(u), _ptr(pq))
     return O, int(u[0]), int(pq[0])
 
 

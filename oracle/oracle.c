@@ -30,6 +30,8 @@
  *   oracle_verify  [SSV] mechanism 1, mode A: every (query, head) attends over its
  *                  own block set I_q plus the sliding-window blocks; the group's
  *                  merged union is what a grouped kernel has to load.
+ *   oracle_verify_shared  [SSV] mechanism 1, mode B: every query of a group attends
+ *                  over the layout of the group's first query (plus the window).
  *   oracle_gather  [SparDA] §4.5: staging selected blocks is a plain copy.
  *
  * Readings where the pages are silent are stated at each routine.
@@ -384,23 +386,26 @@ void oracle_attn(const uint16_t *Q, int G, const uint16_t *K, const uint16_t *V,
 }
 
 /*
- * Grouped speculative verification, mode A, [SSV] mechanism 1.
+ * Grouped speculative verification, [SSV] mechanism 1.
  *   Q   [B][N_q][H_q][D] bf16 bits: N_q verification queries per sequence, already in
  *       the flattened (BFS) order; groups are queries [gC, gC+C).
  *   K,V [B][H_kv][T_cap][D] bf16 bits (committed tokens only; draft tokens are not
  *       in the cache and are not attended).
  *   I   [B][H_kv][N_q][n_sel] per-query selected block ids.
  *   The sliding window is the last window_blocks blocks of the committed sequence
- *   (block-granular reading of "the last w tokens").  Query q, head h attends over
- *   the set I_q ∪ W with the plain softmax of oracle_attn.
+ *   (block-granular reading of "the last w tokens").
+ * Mode A (exact merged schedule, oracle_verify): query q, head h attends over its own
+ * set I_q ∪ W with the plain softmax of oracle_attn; the group loads the merged union.
+ * Mode B (approximate shared layout, oracle_verify_shared): every query of a group
+ * attends over the layout of the group's representative, its first query:
+ * I_{q_rep} ∪ W; the group loads that one layout.
  *   O   [B][N_q][H_q][D].
- *   union_blocks     += |∪_{q in group} (I_q ∪ W)| summed over (b, KV head, group)
+ *   union_blocks     += the blocks a group loads, summed over (b, KV head, group)
  *   per_query_blocks += sum_q |I_q ∪ W| over the same: the loads without grouping.
  */
-void oracle_verify(const uint16_t *Q, const uint16_t *K, const uint16_t *V, long long T_cap,
-                   int B, int H_q, int H_kv, int N_q, const int *I, int n_sel, int C,
-                   int window_blocks, const long long *len, double scale, double *O,
-                   long long *union_blocks, long long *per_query_blocks)
+static void verify_impl(const uint16_t *Q, const uint16_t *K, const uint16_t *V, long long T_cap, int B, int H_q,
+                        int H_kv, int N_q, const int *I, int n_sel, int C, int window_blocks, const long long *len,
+                        double scale, double *O, long long *union_blocks, long long *per_query_blocks, int shared)
 {
     int G = H_q / H_kv;
     long long tot_union = 0, tot_query = 0;
@@ -412,21 +417,32 @@ void oracle_verify(const uint16_t *Q, const uint16_t *K, const uint16_t *V, long
             const uint16_t *Vp = V + ((size_t)b * H_kv + g) * (size_t)T_cap * D;
             char *merged = (char *)calloc((size_t)nb + 1, 1);
             char *member = (char *)calloc((size_t)nb + 1, 1);
+            char *own = (char *)calloc((size_t)nb + 1, 1);
             for (int q0 = 0; q0 < N_q; q0 += C) {
                 memset(merged, 0, (size_t)nb + 1);
                 for (int q = q0; q < q0 + C && q < N_q; ++q) {
-                    memset(member, 0, (size_t)nb + 1);
+                    /* the query's own set I_q ∪ W, for the ungrouped count */
+                    memset(own, 0, (size_t)nb + 1);
                     const int *Iq = I + (((size_t)b * H_kv + g) * N_q + q) * n_sel;
                     for (int i = 0; i < n_sel; ++i)
                         if (Iq[i] >= 0 && Iq[i] < nb)
-                            member[Iq[i]] = 1;
+                            own[Iq[i]] = 1;
+                    for (int j = nb - window_blocks; j < nb; ++j)
+                        if (j >= 0)
+                            own[j] = 1;
+                    for (int j = 0; j < nb; ++j)
+                        tot_query += own[j];
+                    /* the set it attends over: its own (mode A) or the representative's (mode B) */
+                    memset(member, 0, (size_t)nb + 1);
+                    const int *Ia = shared ? I + (((size_t)b * H_kv + g) * N_q + q0) * n_sel : Iq;
+                    for (int i = 0; i < n_sel; ++i)
+                        if (Ia[i] >= 0 && Ia[i] < nb)
+                            member[Ia[i]] = 1;
                     for (int j = nb - window_blocks; j < nb; ++j)
                         if (j >= 0)
                             member[j] = 1;
-                    for (int j = 0; j < nb; ++j) {
-                        tot_query += member[j];
+                    for (int j = 0; j < nb; ++j)
                         merged[j] |= member[j];
-                    }
                     for (int hh = 0; hh < G; ++hh) {
                         int h = g * G + hh;
                         double l;
@@ -437,6 +453,7 @@ void oracle_verify(const uint16_t *Q, const uint16_t *K, const uint16_t *V, long
                 for (int j = 0; j < nb; ++j)
                     tot_union += merged[j];
             }
+            free(own);
             free(member);
             free(merged);
         }
@@ -445,6 +462,24 @@ void oracle_verify(const uint16_t *Q, const uint16_t *K, const uint16_t *V, long
         *union_blocks = tot_union;
     if (per_query_blocks)
         *per_query_blocks = tot_query;
+}
+
+void oracle_verify(const uint16_t *Q, const uint16_t *K, const uint16_t *V, long long T_cap,
+                   int B, int H_q, int H_kv, int N_q, const int *I, int n_sel, int C,
+                   int window_blocks, const long long *len, double scale, double *O,
+                   long long *union_blocks, long long *per_query_blocks)
+{
+    verify_impl(Q, K, V, T_cap, B, H_q, H_kv, N_q, I, n_sel, C, window_blocks, len, scale, O, union_blocks,
+                per_query_blocks, 0);
+}
+
+void oracle_verify_shared(const uint16_t *Q, const uint16_t *K, const uint16_t *V, long long T_cap,
+                          int B, int H_q, int H_kv, int N_q, const int *I, int n_sel, int C,
+                          int window_blocks, const long long *len, double scale, double *O,
+                          long long *union_blocks, long long *per_query_blocks)
+{
+    verify_impl(Q, K, V, T_cap, B, H_q, H_kv, N_q, I, n_sel, C, window_blocks, len, scale, O, union_blocks,
+                per_query_blocks, 1);
 }
 
 /*

@@ -338,6 +338,49 @@ def test_verify_equals_masked_sdpa_per_query():
     assert per_query == 2 * 4 * 4
 
 
+def test_verify_shared_layout_attends_over_the_first_query_set():
+    # SSV notes, mode B: every query of a group uses its first query's layout
+    B, N_q, H_q, H_kv, T, C, wb = 1, 4, 4, 2, 12 * BLK, 2, 2
+    G = H_q // H_kv
+    Q, K, V = rand_bits((B, N_q, H_q, D), 38), rand_bits((B, H_kv, T, D), 39), rand_bits((B, H_kv, T, D), 41)
+    I = np.array([[[[1, 4], [1, 5], [2, 4], [0, 9]], [[3, 6], [3, 7], [0, 6], [5, 8]]]], np.int32)
+    n = T - 20
+    O, union, per_query = oracle.verify(Q, K, V, I, C, wb, [n], shared=True)
+    for g in range(H_kv):
+        for q in range(N_q):
+            rep = (q // C) * C
+            chosen = set(I[0, g, rep].tolist()) | {10, 11}
+            mask = np.array([(t // BLK) in chosen and t < n for t in range(T)])
+            ref = _sdpa(values(Q[0, q, g * G:(g + 1) * G]), values(K[0, g]), values(V[0, g]), mask)
+            assert np.allclose(O[0, q, g * G:(g + 1) * G], ref, rtol=1e-11, atol=1e-12)
+    # every group loads one layout: 2 selected + 2 window blocks
+    assert union == H_kv * (N_q // C) * 4
+    assert per_query == 2 * 4 * 4
+
+
+def test_verify_shared_layout_with_singleton_groups_is_mode_a():
+    sh = wl.VerifyShape("t", B=1, H_q=4, H_kv=2, T=64 * BLK, N_q=8, n_sel=8, gamma=0.5, window_tokens=128, C=4)
+    I = wl.verify_sets(sh).numpy()
+    Q = rand_bits((sh.B, sh.N_q, sh.H_q, D), 42)
+    K, V = rand_bits((sh.B, sh.H_kv, sh.T, D), 43), rand_bits((sh.B, sh.H_kv, sh.T, D), 44)
+    Oa, ua, pa = oracle.verify(Q, K, V, I, 1, sh.window_blocks, [sh.T])
+    Ob, ub, pb = oracle.verify(Q, K, V, I, 1, sh.window_blocks, [sh.T], shared=True)
+    assert np.array_equal(Oa, Ob) and (ua, pa) == (ub, pb)
+    # and with C = 4 the shared layout loads n_sel + window per group
+    _, u4, _ = oracle.verify(Q, K, V, I, 4, sh.window_blocks, [sh.T], shared=True)
+    assert u4 == sh.H_kv * 2 * (sh.n_sel + sh.window_blocks)
+
+
+def test_verify_shared_layout_on_the_worked_example():
+    ex = json.load(open(os.path.join(GOLDEN, "ssv_worked_example.json")))
+    T = 24 * BLK
+    Q, K, V = rand_bits((1, 4, 1, D), 45), rand_bits((1, 1, T, D), 46), rand_bits((1, 1, T, D), 47)
+    I = np.array(ex["queries"], dtype=np.int32)[None, None]
+    _, union, per_query = oracle.verify(Q, K, V, I, C=4, window_blocks=0, lens=[T], shared=True)
+    assert union == len(ex["queries"][0])          # the first query's blocks only
+    assert per_query == ex["derived"]["ungrouped_loads"]
+
+
 # ----------------------------------------------------------------------------- gather
 
 
@@ -429,6 +472,9 @@ MUTANTS = [
     ("z += exp(a[j] - m);", "z += j >= n_init ? exp(a[j] - m) : 0.0;"),
     # multi-head scores without the scale
     ("a[j] = scale * acc;", "a[j] = acc;"),
+    # mode B takes the group's last query as its representative
+    ("const int *Ia = shared ? I + (((size_t)b * H_kv + g) * N_q + q0) * n_sel : Iq;",
+     "const int *Ia = shared ? I + (((size_t)b * H_kv + g) * N_q + (q0 + C - 1 < N_q ? q0 + C - 1 : N_q - 1)) * n_sel : Iq;"),
 ]
 
 PIN_TESTS = [
@@ -442,6 +488,8 @@ PIN_TESTS = [
     test_attn_constant_values_and_single_token, test_verify_worked_example_of_the_ssv_page,
     test_verify_equals_masked_sdpa_per_query, test_select_heads_with_one_head_is_the_forecast_selection,
     test_select_heads_scores_are_a_sum_of_head_distributions, test_select_heads_match_scipy_softmax_and_brute_force_topk,
+    test_verify_shared_layout_attends_over_the_first_query_set, test_verify_shared_layout_with_singleton_groups_is_mode_a,
+    test_verify_shared_layout_on_the_worked_example,
 ]
 
 
