@@ -812,18 +812,19 @@ def run_verify_case(args, dev):
     out = {"case": "verify64k", "workload": sh.name, "unit_of_work": "one verification round "
            f"({sh.N_q} queries x {sh.B * sh.H_kv} pairs)", "peak_gbs": peak, "peak_source": src,
            "l2": "512 MB read evicts L2 before each round"}
-    for C, key in ((sh.C, "grouped"), (1, "ungrouped")):
+    for C, key, shared in ((sh.C, "grouped", False), (1, "ungrouped", False), (sh.C, "shared_layout", True)):
         loaded = torch.zeros(1, dtype=torch.int64, device=dev)
 
         def run():
             binding.sparse_verify_attn_grouped(x["Q"], x["K"], x["V"], x["I"], C, sh.window_blocks, x["seq_len"], O,
-                                               status=status)
+                                               status=status, shared=shared)
         binding.sparse_verify_attn_grouped(x["Q"], x["K"], x["V"], x["I"], C, sh.window_blocks, x["seq_len"], O,
-                                           blocks_loaded=loaded, status=status)
+                                           blocks_loaded=loaded, status=status, shared=shared)
         t = _event_times(run, args.steps, args.warmup, evict)
         nbytes = int(loaded.item()) * KV_BLOCK_BYTES
         gbs, frac = _rate(nbytes, t["median_us"], peak)
-        out[key] = {"C": C, "blocks_loaded": int(loaded.item()), "bytes_loaded": nbytes, **t,
+        out[key] = {"C": C, "mode": "B (first query's layout)" if shared else "A (merged union)",
+                    "blocks_loaded": int(loaded.item()), "bytes_loaded": nbytes, **t,
                     "achieved_gbs": gbs, "frac_of_measured_hbm": frac}
     assert status.item() == 0, f"device status {status.item()}"
     g, u = out["grouped"], out["ungrouped"]

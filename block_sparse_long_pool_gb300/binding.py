@@ -53,6 +53,8 @@ SIGNATURES = {
                                          _I, _I, _P, _P, _I, _I, _U, _P, _P]),
     "sparse_verify_attn_grouped": (_I, [_P, _P, _P, _LL, _P, _I, _I, _I, _I, _P, _I, _I, _I, _F, _P, _P, _I,
                                         _P, _P]),
+    "sparse_verify_attn_shared": (_I, [_P, _P, _P, _LL, _P, _I, _I, _I, _I, _P, _I, _I, _I, _F, _P, _P, _I,
+                                       _P, _P]),
     "sparse_gather_offloaded": (_I, [_P, _P, _LL, _P, _P, _I, _I, _I, _P, _P, _P, _I, _P, _P]),
 }
 
@@ -285,8 +287,10 @@ def sparse_decode_attn_forecast(Q, k_cache, v_cache, blk_idx, count, seq_len, O,
 
 def sparse_verify_attn_grouped(Q, k_cache, v_cache, idx_q, C: int, window_blocks: int, seq_len, O,
                                blocks_loaded=None, scale: float = 0.0, n_split: int = 0, status=None,
-                               stream=None):
-    """Mode-A grouped verification: Q [B][N_q][H_q][128], idx_q [B][H_kv][N_q][n_sel]."""
+                               stream=None, shared: bool = False):
+    """Grouped verification: Q [B][N_q][H_q][128], idx_q [B][H_kv][N_q][n_sel].  Mode A
+    (each query over its own set), or with ``shared`` mode B (sparse_verify_attn_shared:
+    every query over its group's first query's set)."""
     B, N_q, H_q, _ = Q.shape
     _, H_kv, T_cap, _ = k_cache.shape
     n_sel = idx_q.shape[3]
@@ -298,10 +302,10 @@ def sparse_verify_attn_grouped(Q, k_cache, v_cache, idx_q, C: int, window_blocks
     _need(O, "O", torch.bfloat16, shape=(B, N_q, H_q, D))
     if blocks_loaded is not None:
         _need(blocks_loaded, "blocks_loaded", torch.int64)
-    rc = load().sparse_verify_attn_grouped(_ptr(Q), _ptr(k_cache), _ptr(v_cache), T_cap, _ptr(idx_q), n_sel, N_q,
-                                           C, window_blocks, _ptr(seq_len), B, H_q, H_kv, float(scale), _ptr(O),
-                                           _ptr(blocks_loaded), n_split, _ptr(status), _stream(stream))
-    _check(rc, "sparse_verify_attn_grouped")
+    fn = load().sparse_verify_attn_shared if shared else load().sparse_verify_attn_grouped
+    rc = fn(_ptr(Q), _ptr(k_cache), _ptr(v_cache), T_cap, _ptr(idx_q), n_sel, N_q, C, window_blocks, _ptr(seq_len), B,
+            H_q, H_kv, float(scale), _ptr(O), _ptr(blocks_loaded), n_split, _ptr(status), _stream(stream))
+    _check(rc, "sparse_verify_attn_shared" if shared else "sparse_verify_attn_grouped")
 
 
 def sparse_gather_offloaded(k_host, v_host, idx, count, k_ring, v_ring, ready_flag=None, n_ctas: int = 0,

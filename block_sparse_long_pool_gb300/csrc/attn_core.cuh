@@ -46,6 +46,10 @@ enum { kCtrlLast = 2, kCtrlMergeValid = 3 };
 
 enum { kCtrlAbort = 0, kCtrlList = 1 };
 
+// Internal AttnParams::flags bit (not a public flag): grouped verification in SSV mode
+// B, every query of a group on its first query's layout.
+constexpr unsigned kVerifySharedLayout = 0x100u;
+
 struct AttnParams {
     const uint16_t *Q;
     uint16_t *O;

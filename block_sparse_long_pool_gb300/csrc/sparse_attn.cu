@@ -62,7 +62,9 @@ __device__ __forceinline__ void build_union(const AttnParams &p, uint8_t *base, 
     const int tid = threadIdx.x;
     const int nq = min(p.C, p.N_q - q0);
     const int wcount = min(p.window_blocks, nb);
-    const int n_sel_ent = nq * p.n_sel;
+    // mode B (shared layout): only the group's first query's set, marked for every query
+    const bool shared = (p.flags & kVerifySharedLayout) != 0u;
+    const int n_sel_ent = shared ? p.n_sel : nq * p.n_sel;
     const int n_ent = n_sel_ent + wcount;
     const uint32_t all_q = nq >= 32 ? 0xffffffffu : ((1u << nq) - 1u);
     for (int e = tid; e < n_ent; e += kThreads) {
@@ -71,7 +73,7 @@ __device__ __forceinline__ void build_union(const AttnParams &p, uint8_t *base, 
         if (e < n_sel_ent) {
             const int qi = e / p.n_sel;
             v = p.idx_q[((static_cast<size_t>(b) * p.H_kv + g) * p.N_q + q0 + qi) * p.n_sel + (e - qi * p.n_sel)];
-            m = 1u << qi;
+            m = shared ? all_q : 1u << qi;
             if (v < 0 || v >= nb) {
                 report(p.status, SPARSE_ERR_BAD_INDEX);
                 v = INT_MAX;
@@ -1249,36 +1251,36 @@ extern "C" SPARSE_API size_t sparse_decode_attn_workspace_size(int B, int H_q, i
     return need;
 }
 
-extern "C" SPARSE_API int sparse_verify_attn_grouped(const uint16_t *Q, const uint16_t *k_cache,
-                                                     const uint16_t *v_cache, long long T_cap, const int *idx_q,
-                                                     int n_sel, int N_q, int C, int window_blocks,
-                                                     const int *seq_len, int B, int H_q, int H_kv, float scale,
-                                                     uint16_t *O, long long *blocks_loaded, int n_split,
-                                                     int *status, void *stream)
+namespace {
+
+static int verify_impl(const char *name, unsigned mode, const uint16_t *Q, const uint16_t *k_cache,
+                       const uint16_t *v_cache, long long T_cap, const int *idx_q, int n_sel, int N_q, int C,
+                       int window_blocks, const int *seq_len, int B, int H_q, int H_kv, float scale, uint16_t *O,
+                       long long *blocks_loaded, int n_split, int *status, void *stream)
 {
     using sp_host::aligned16;
     using sp_host::fail;
     if (!Q || !k_cache || !v_cache || !seq_len || !O || (n_sel > 0 && !idx_q))
-        return fail(SPARSE_ERR_INVALID_ARG, "sparse_verify_attn_grouped: null pointer");
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: null pointer", name);
     if (!aligned16(Q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(O))
-        return fail(SPARSE_ERR_INVALID_ARG, "sparse_verify_attn_grouped: Q, K, V and O must be 16-byte aligned");
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: Q, K, V and O must be 16-byte aligned", name);
     if (B < 1 || H_kv < 1 || H_q < H_kv || H_q % H_kv != 0 || N_q < 1 || C < 1 || n_sel < 0 ||
         window_blocks < 0 || T_cap < 1)
-        return fail(SPARSE_ERR_INVALID_ARG, "sparse_verify_attn_grouped: bad size");
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: bad size", name);
     if (T_cap > INT_MAX - 2 * kBlk)
-        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_verify_attn_grouped: T_cap too large");
+        return fail(SPARSE_ERR_UNSUPPORTED, "%s: T_cap too large", name);
     if (!isfinite(scale))
-        return fail(SPARSE_ERR_INVALID_ARG, "sparse_verify_attn_grouped: scale must be finite");
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: scale must be finite", name);
     const int G = H_q / H_kv;
     if (C > 32 || static_cast<long long>(C) * G > 16)
-        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_verify_attn_grouped: C*G=%lld rows > 16 per group",
+        return fail(SPARSE_ERR_UNSUPPORTED, "%s: C*G=%lld rows > 16 per group", name,
                     static_cast<long long>(C) * G);
     if (static_cast<long long>(C) * n_sel + window_blocks > kMaxUnion)
-        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_verify_attn_grouped: C*n_sel+window_blocks > %d", kMaxUnion);
+        return fail(SPARSE_ERR_UNSUPPORTED, "%s: C*n_sel+window_blocks > %d", name, kMaxUnion);
     const int n_groups = (N_q + C - 1) / C;
     const long long units = static_cast<long long>(B) * H_kv * n_groups;
     if (units > 65535)
-        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_verify_attn_grouped: too many groups");
+        return fail(SPARSE_ERR_UNSUPPORTED, "%s: too many groups", name);
     sp_host::DeviceInfo dev;
     int rc = sp_host::device_info(&dev);
     if (rc != SPARSE_OK)
@@ -1309,9 +1311,34 @@ extern "C" SPARSE_API int sparse_verify_attn_grouped(const uint16_t *Q, const ui
     p.C = C;
     p.window_blocks = window_blocks;
     p.n_groups = n_groups;
-    p.flags = 0u;
+    p.flags = mode;
     p.scale_log2 = scale_log2_of(scale);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return C * G <= 8 ? launch<1, true>(p, km, vm, S, units, dev.device, st)
                       : launch<2, true>(p, km, vm, S, units, dev.device, st);
+}
+
+}  // namespace
+
+extern "C" SPARSE_API int sparse_verify_attn_grouped(const uint16_t *Q, const uint16_t *k_cache,
+                                                     const uint16_t *v_cache, long long T_cap, const int *idx_q,
+                                                     int n_sel, int N_q, int C, int window_blocks,
+                                                     const int *seq_len, int B, int H_q, int H_kv, float scale,
+                                                     uint16_t *O, long long *blocks_loaded, int n_split,
+                                                     int *status, void *stream)
+{
+    return verify_impl("sparse_verify_attn_grouped", 0u, Q, k_cache, v_cache, T_cap, idx_q, n_sel, N_q, C,
+                       window_blocks, seq_len, B, H_q, H_kv, scale, O, blocks_loaded, n_split, status, stream);
+}
+
+extern "C" SPARSE_API int sparse_verify_attn_shared(const uint16_t *Q, const uint16_t *k_cache,
+                                                    const uint16_t *v_cache, long long T_cap, const int *idx_q,
+                                                    int n_sel, int N_q, int C, int window_blocks,
+                                                    const int *seq_len, int B, int H_q, int H_kv, float scale,
+                                                    uint16_t *O, long long *blocks_loaded, int n_split,
+                                                    int *status, void *stream)
+{
+    return verify_impl("sparse_verify_attn_shared", kVerifySharedLayout, Q, k_cache, v_cache, T_cap, idx_q, n_sel,
+                       N_q, C, window_blocks, seq_len, B, H_q, H_kv, scale, O, blocks_loaded, n_split, status,
+                       stream);
 }

@@ -314,6 +314,23 @@ SPARSE_API int sparse_verify_attn_grouped(const uint16_t *Q, const uint16_t *k_c
                                           void *stream);
 
 /*
+ * sparse_verify_attn_shared -- [SSV] mechanism 1, mode B (approximate shared index
+ * layout).  Same arguments and layouts as sparse_verify_attn_grouped, but every query
+ * of a group attends over the layout of the group's representative, its first query:
+ *     O[b][q][h] = attention over I_{q_rep} ∪ W,   q_rep = the first query of q's group,
+ * so the group loads that one layout (|I_{q_rep} ∪ W| blocks, added to *blocks_loaded)
+ * instead of the merged union.  An approximation of the per-query sets, which the SSV
+ * notes recommend when the overlap is high.
+ */
+SPARSE_API int sparse_verify_attn_shared(const uint16_t *Q, const uint16_t *k_cache,
+                                         const uint16_t *v_cache, long long T_cap,
+                                         const int *idx_q, int n_sel, int N_q, int C,
+                                         int window_blocks, const int *seq_len, int B,
+                                         int H_q, int H_kv, float scale, uint16_t *O,
+                                         long long *blocks_loaded, int n_split, int *status,
+                                         void *stream);
+
+/*
  * sparse_gather_offloaded -- [SparDA] §4.5 (persistent prefetch of selected blocks,
  * re-designed as a gather kernel on the copy stream).  Copies the K and V rows of
  * block idx[p][i] (i < count[p]) of every pair from the host cache into slot i of the

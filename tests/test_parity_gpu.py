@@ -468,13 +468,14 @@ def test_decode_128k_layer_sampled_at_full_size():
 # ----------------------------------------------------------------------------- grouped verification
 
 
-def _verify(sh, n_split=0):
+def _verify(sh, n_split=0, shared=False):
     inp = wl.verify_inputs(sh, device="cuda")
     O = torch.zeros((sh.B, sh.N_q, sh.H_q, D), dtype=torch.bfloat16, device="cuda")
     loaded = torch.zeros(1, dtype=torch.int64, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     binding.sparse_verify_attn_grouped(inp["Q"], inp["K"], inp["V"], inp["I"], sh.C, sh.window_blocks,
-                                       inp["seq_len"], O, blocks_loaded=loaded, n_split=n_split, status=status)
+                                       inp["seq_len"], O, blocks_loaded=loaded, n_split=n_split, status=status,
+                                       shared=shared)
     torch.cuda.synchronize()
     assert status.item() == 0
     return inp, O, int(loaded.item())
@@ -520,6 +521,28 @@ def test_verify_split_invariance(n_split):
     inp, O, loaded = _verify(sh, n_split=n_split)
     Oref, union, _ = oracle.verify(bits(inp["Q"]), bits(inp["K"]), bits(inp["V"]), inp["I"].cpu().numpy(), sh.C,
                                    sh.window_blocks, [sh.T] * sh.B)
+    assert_attn_close(O, Oref)
+    assert loaded == union
+
+
+def test_verify_shared_layout_64k_workload_matches_oracle():
+    """SSV mode B on the 64K verification workload: every query over its group's first
+    query's layout; each group loads n_sel + window blocks."""
+    sh = wl.VERIFY_64K
+    inp, O, loaded = _verify(sh, shared=True)
+    Oref, union, per_query = oracle.verify(bits(inp["Q"]), bits(inp["K"]), bits(inp["V"]), inp["I"].cpu().numpy(),
+                                           sh.C, sh.window_blocks, [sh.T] * sh.B, shared=True)
+    assert_attn_close(O, Oref)
+    assert loaded == union == sh.B * sh.H_kv * (sh.N_q // sh.C) * (sh.n_sel + sh.window_blocks)
+
+
+@pytest.mark.parametrize("n_split,C", [(1, 4), (2, 3), (8, 4), (0, 1)])
+def test_verify_shared_layout_ragged_groups(n_split, C):
+    sh = wl.VerifyShape("shared", B=2, H_q=8, H_kv=2, T=40 * BLK + 17, N_q=7, n_sel=6, gamma=0.5,
+                        window_tokens=2 * BLK, C=C, seed=35)
+    inp, O, loaded = _verify(sh, n_split=n_split, shared=True)
+    Oref, union, _ = oracle.verify(bits(inp["Q"]), bits(inp["K"]), bits(inp["V"]), inp["I"].cpu().numpy(), sh.C,
+                                   sh.window_blocks, [sh.T] * sh.B, shared=True)
     assert_attn_close(O, Oref)
     assert loaded == union
 
