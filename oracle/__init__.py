@@ -66,6 +66,7 @@ def load_library(path: str):
                                   f64, P, P, P]
     lib.oracle_verify_shared.argtypes = lib.oracle_verify.argtypes
     lib.oracle_gather.argtypes = [P, i64, i32, P, P, i32, P]
+    lib.oracle_nsa.argtypes = [P, i32, P, P, i64, i32, P, P, i32, P, P, i32, P, i64, P, f64, P]
     return lib
 
 
@@ -194,6 +195,28 @@ def verify(Q, K, V, I, C: int, window_blocks: int, lens, scale: float | None = N
     fn(_ptr(Q), _ptr(K), _ptr(V), T_cap, B, H_q, H_kv, N_q, _ptr(I), n_sel, C, window_blocks, _ptr(lens),
        float(scale), _ptr(O), _ptr(u), _ptr(pq))
     return O, int(u[0]), int(pq[0])
+
+
+def nsa(Q, K, V, khat, vhat, blocks, count, lens, window_tokens: int, gates, scale: float | None = None):
+    """NSA gated three-branch output: Q [P][G][128] bf16 bits, K/V [P][T][128] bf16 bits,
+    khat/vhat [P][N][128] compressed rows, blocks [P][k_tot] selected, gates [P][G][3]
+    = (g_c, g_s, g_w).  Returns O [P][G][128] fp64."""
+    Q, K, V = _u16(Q), _u16(K), _u16(V)
+    khat = np.ascontiguousarray(khat, dtype=np.float64)
+    vhat = np.ascontiguousarray(vhat, dtype=np.float64)
+    blocks, count, lens = _i32(blocks), _i32(count), _i64(lens)
+    gates = np.ascontiguousarray(gates, dtype=np.float64)
+    P, G, d = Q.shape
+    T = K.shape[1]
+    n_cap = khat.shape[1]
+    assert d == D and K.shape == (P, T, D) and V.shape == K.shape and vhat.shape == khat.shape
+    assert gates.shape == (P, G, 3) and blocks.shape[0] == P and lens.shape == (P,)
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    O = np.empty((P, G, D), dtype=np.float64)
+    _load().oracle_nsa(_ptr(Q), G, _ptr(K), _ptr(V), T, P, _ptr(khat), _ptr(vhat), n_cap, _ptr(blocks), _ptr(count),
+                       blocks.shape[1], _ptr(lens), int(window_tokens), _ptr(gates), float(scale), _ptr(O))
+    return O
 
 
 def gather(src, idx, count, ring=None):

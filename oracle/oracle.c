@@ -32,6 +32,8 @@
  *                  merged union is what a grouped kernel has to load.
  *   oracle_verify_shared  [SSV] mechanism 1, mode B: every query of a group attends
  *                  over the layout of the group's first query (plus the window).
+ *   oracle_nsa     [SSV] "NSA three-branch math": compressed, selected and sliding-window
+ *                  branches, each its own softmax, combined by per-head gates.
  *   oracle_gather  [SparDA] §4.5: staging selected blocks is a plain copy.
  *
  * Readings where the pages are silent are stated at each routine.
@@ -380,6 +382,122 @@ void oracle_attn(const uint16_t *Q, int G, const uint16_t *K, const uint16_t *V,
                        O + ((size_t)p * G + h) * D, &l);
             if (lse)
                 lse[(size_t)p * G + h] = l;
+        }
+        free(member);
+    }
+}
+
+/*
+ * Softmax attention of one query row over explicit rows: tokens [t0, t1) of K / V
+ * (bf16 bits; attend_tokens), or n fp64 rows kr / vr (attend_rows).  o = 0 when empty.
+ */
+static void attend_tokens(const double *qd, const uint16_t *Kp, const uint16_t *Vp, long long t0, long long t1,
+                          double scale, double *o)
+{
+    for (int d = 0; d < D; ++d)
+        o[d] = 0.0;
+    if (t1 <= t0)
+        return;
+    double *a = (double *)malloc(sizeof(double) * (size_t)(t1 - t0));
+    double m = -INFINITY;
+    for (long long t = t0; t < t1; ++t) {
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d)
+            dot += qd[d] * bf16_value(Kp[(size_t)t * D + d]);
+        a[t - t0] = scale * dot;
+        if (a[t - t0] > m)
+            m = a[t - t0];
+    }
+    double L = 0.0;
+    for (long long t = t0; t < t1; ++t) {
+        double w = exp(a[t - t0] - m);
+        L += w;
+        for (int d = 0; d < D; ++d)
+            o[d] += w * bf16_value(Vp[(size_t)t * D + d]);
+    }
+    for (int d = 0; d < D; ++d)
+        o[d] /= L;
+    free(a);
+}
+
+static void attend_rows(const double *qd, const double *kr, const double *vr, int n, double scale, double *o)
+{
+    for (int d = 0; d < D; ++d)
+        o[d] = 0.0;
+    if (n <= 0)
+        return;
+    double *a = (double *)malloc(sizeof(double) * (size_t)n);
+    double m = -INFINITY;
+    for (int j = 0; j < n; ++j) {
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d)
+            dot += qd[d] * kr[(size_t)j * D + d];
+        a[j] = scale * dot;
+        if (a[j] > m)
+            m = a[j];
+    }
+    double L = 0.0;
+    for (int j = 0; j < n; ++j) {
+        double w = exp(a[j] - m);
+        L += w;
+        for (int d = 0; d < D; ++d)
+            o[d] += w * vr[(size_t)j * D + d];
+    }
+    for (int d = 0; d < D; ++d)
+        o[d] /= L;
+    free(a);
+}
+
+/*
+ * NSA's gated three-branch output, [SSV] "NSA three-branch math" steps 3-6, for the
+ * decode query of each pair (len[p] tokens present):
+ *   o^(s) = softmax(q . K_I / sqrt d) V_I over the tokens of the selected blocks I
+ *           (blocks[p][0 .. count[p]), as oracle_attn);
+ *   o^(c) = softmax(q . Khat / sqrt d) Vhat over the compressed rows, one per block
+ *           holding a token (khat, vhat [n_pairs][n_blocks_cap][D], e.g. oracle_pool
+ *           of K and of V);
+ *   o^(w) = softmax over the last window_tokens tokens [len - w, len);
+ *   o     = g_c o^(c) + g_s o^(s) + g_w o^(w),  gates [n_pairs][G][3] = (g_c, g_s, g_w).
+ * Readings: the compressed values are mean-pooled like the keys ([SparDA] eq.(4)), the
+ * compressed branch covers all N_b blocks (the last one the mean of the tokens
+ * present), the window is token-granular, and a branch with no rows contributes zero.
+ *   Q [n_pairs][G][D] bf16 bits; K, V [n_pairs][pair_stride][D] bf16 bits; O [n_pairs][G][D].
+ */
+void oracle_nsa(const uint16_t *Q, int G, const uint16_t *K, const uint16_t *V, long long pair_stride, int n_pairs,
+                const double *khat, const double *vhat, int n_blocks_cap, const int *blocks, const int *count,
+                int k_tot, const long long *len, long long window_tokens, const double *gates, double scale,
+                double *O)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int p = 0; p < n_pairs; ++p) {
+        int nb = blocks_of(len[p]);
+        if (nb > n_blocks_cap)
+            nb = n_blocks_cap;
+        char *member = (char *)calloc((size_t)nb + 1, 1);
+        for (int i = 0; i < count[p] && i < k_tot; ++i) {
+            int j = blocks[(size_t)p * k_tot + i];
+            if (j >= 0 && j < nb)
+                member[j] = 1;
+        }
+        const uint16_t *Kp = K + (size_t)p * (size_t)pair_stride * D;
+        const uint16_t *Vp = V + (size_t)p * (size_t)pair_stride * D;
+        const double *kr = khat + (size_t)p * n_blocks_cap * D;
+        const double *vr = vhat + (size_t)p * n_blocks_cap * D;
+        long long w0 = len[p] - window_tokens;
+        if (w0 < 0)
+            w0 = 0;
+        for (int h = 0; h < G; ++h) {
+            const uint16_t *q = Q + ((size_t)p * G + h) * D;
+            double qd[D], os[D], oc[D], ow[D], l;
+            for (int d = 0; d < D; ++d)
+                qd[d] = bf16_value(q[d]);
+            attend_set(q, Kp, Vp, member, nb, len[p], scale, os, &l);
+            attend_rows(qd, kr, vr, nb, scale, oc);
+            attend_tokens(qd, Kp, Vp, w0, len[p], scale, ow);
+            const double *g = gates + ((size_t)p * G + h) * 3;
+            double *o = O + ((size_t)p * G + h) * D;
+            for (int d = 0; d < D; ++d)
+                o[d] = g[0] * oc[d] + g[1] * os[d] + g[2] * ow[d];
         }
         free(member);
     }

@@ -444,6 +444,59 @@ def test_select_heads_match_scipy_softmax_and_brute_force_topk():
         assert list(idx[p, :cnt[p]]) == want
 
 
+# ----------------------------------------------------------------------------- NSA three-branch output
+
+
+def _nsa_case(seed):
+    P, G, T, w = 2, 3, 10 * BLK + 21, 100
+    lens = np.array([T, 6 * BLK + 3], np.int64)
+    Q, K, V = rand_bits((P, G, D), seed), rand_bits((P, T, D), seed + 1), rand_bits((P, T, D), seed + 2)
+    N = 11
+    khat = oracle.pool(K, lens, N)
+    vhat = oracle.pool(V, lens, N)
+    blocks = np.array([[1, 4, 9, -1], [0, 2, -1, -1]], np.int32)
+    count = np.array([3, 2], np.int32)
+    return Q, K, V, khat, vhat, blocks, count, lens, w, G, N
+
+
+def _nsa_with(gate, seed=50):
+    Q, K, V, khat, vhat, blocks, count, lens, w, G, N = _nsa_case(seed)
+    gates = np.broadcast_to(np.asarray(gate, np.float64), (2, G, 3)).copy()
+    return oracle.nsa(Q, K, V, khat, vhat, blocks, count, lens, w, gates), (Q, K, V, khat, vhat, blocks, count,
+                                                                            lens, w, G, N)
+
+
+def test_nsa_selected_branch_is_sdpa_over_the_selected_tokens():
+    O, (Q, K, V, _, _, blocks, count, lens, _, _, _) = _nsa_with((0.0, 1.0, 0.0))
+    for p in range(2):
+        chosen = set(blocks[p, :count[p]].tolist())
+        mask = np.array([(t // BLK) in chosen and t < lens[p] for t in range(K.shape[1])])
+        assert np.allclose(O[p], _sdpa(values(Q[p]), values(K[p]), values(V[p]), mask), rtol=1e-11, atol=1e-12)
+
+
+def test_nsa_window_branch_is_sdpa_over_the_last_w_tokens():
+    O, (Q, K, V, _, _, _, _, lens, w, _, _) = _nsa_with((0.0, 0.0, 1.0))
+    for p in range(2):
+        mask = np.array([lens[p] - w <= t < lens[p] for t in range(K.shape[1])])
+        assert np.allclose(O[p], _sdpa(values(Q[p]), values(K[p]), values(V[p]), mask), rtol=1e-11, atol=1e-12)
+
+
+def test_nsa_compressed_branch_is_sdpa_over_the_compressed_rows():
+    O, (Q, _, _, khat, vhat, _, _, lens, _, _, _) = _nsa_with((1.0, 0.0, 0.0))
+    for p in range(2):
+        nb = (int(lens[p]) + BLK - 1) // BLK
+        mask = np.arange(khat.shape[1]) < nb
+        assert np.allclose(O[p], _sdpa(values(Q[p]), khat[p], vhat[p], mask), rtol=1e-11, atol=1e-12)
+
+
+def test_nsa_output_is_linear_in_the_gates():
+    Oc, _ = _nsa_with((1.0, 0.0, 0.0))
+    Os, _ = _nsa_with((0.0, 1.0, 0.0))
+    Ow, _ = _nsa_with((0.0, 0.0, 1.0))
+    O, _ = _nsa_with((0.25, -0.5, 1.5))
+    assert np.allclose(O, 0.25 * Oc - 0.5 * Os + 1.5 * Ow, rtol=1e-12, atol=1e-13)
+
+
 # ----------------------------------------------------------------------------- mutants
 
 MUTANTS = [
@@ -472,6 +525,12 @@ MUTANTS = [
     ("z += exp(a[j] - m);", "z += j >= n_init ? exp(a[j] - m) : 0.0;"),
     # multi-head scores without the scale
     ("a[j] = scale * acc;", "a[j] = acc;"),
+    # the NSA window starts one token late
+    ("long long w0 = len[p] - window_tokens;", "long long w0 = len[p] - window_tokens + 1;"),
+    # the NSA gates are swapped between the compressed and the selected branch
+    ("o[d] = g[0] * oc[d] + g[1] * os[d] + g[2] * ow[d];", "o[d] = g[1] * oc[d] + g[0] * os[d] + g[2] * ow[d];"),
+    # the NSA compressed branch forgets the last compressed row
+    ("attend_rows(qd, kr, vr, nb, scale, oc);", "attend_rows(qd, kr, vr, nb - 1, scale, oc);"),
     # mode B takes the group's last query as its representative
     ("const int *Ia = shared ? I + (((size_t)b * H_kv + g) * N_q + q0) * n_sel : Iq;",
      "const int *Ia = shared ? I + (((size_t)b * H_kv + g) * N_q + (q0 + C - 1 < N_q ? q0 + C - 1 : N_q - 1)) * n_sel : Iq;"),
@@ -489,7 +548,9 @@ PIN_TESTS = [
     test_verify_equals_masked_sdpa_per_query, test_select_heads_with_one_head_is_the_forecast_selection,
     test_select_heads_scores_are_a_sum_of_head_distributions, test_select_heads_match_scipy_softmax_and_brute_force_topk,
     test_verify_shared_layout_attends_over_the_first_query_set, test_verify_shared_layout_with_singleton_groups_is_mode_a,
-    test_verify_shared_layout_on_the_worked_example,
+    test_verify_shared_layout_on_the_worked_example, test_nsa_selected_branch_is_sdpa_over_the_selected_tokens,
+    test_nsa_window_branch_is_sdpa_over_the_last_w_tokens, test_nsa_compressed_branch_is_sdpa_over_the_compressed_rows,
+    test_nsa_output_is_linear_in_the_gates,
 ]
 
 
