@@ -995,6 +995,82 @@ def run_offload_case(args, dev):
     print(json.dumps(line), flush=True)
 
 
+NSA_WINDOW_TOKENS = 512
+
+
+def run_nsa_case(args, dev):
+    """NSA's gated three-branch decode on the 128K decode shape (8 x 8 pairs, G = 8,
+    67 selected blocks, a 512-token window, 2048 compressed rows per pair): the
+    multi-head selector over the compressed keys (NSA's routing) and the one-launch
+    three-branch attention, each timed alone and as a layer."""
+    import torch
+    from block_sparse_long_pool_gb300 import binding
+    from block_sparse_long_pool_gb300 import workloads as wl
+    sh = wl.DECODE_128K
+    peak, src = measured_peaks()
+    B, H_q, H_kv, T, N = sh.B, sh.H_q, sh.H_kv, sh.T, sh.N_b
+    k_tot, w = sh.k_tot, NSA_WINDOW_TOKENS
+    kc = torch.empty((B, H_kv, T, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    ktil = torch.zeros((B, H_kv, N, D), dtype=torch.float32, device=dev)
+    vtil = torch.zeros_like(ktil)
+    khat = torch.zeros((B, H_kv, N, D), dtype=torch.bfloat16, device=dev)
+    vhat = torch.zeros_like(khat)
+    for b in range(B):   # one batch element at a time keeps the staging small
+        kn = wl.randn_bf16((1, H_kv, T, D), wl._subseed(sh.seed, 71, b), dev)
+        vn = wl.randn_bf16((1, H_kv, T, D), wl._subseed(sh.seed, 72, b), dev)
+        binding.sparse_pool_append_kv(kc[b:b + 1], vc[b:b + 1], ktil[b:b + 1], vtil[b:b + 1], kn, vn, 0,
+                                      khat=khat[b:b + 1], vhat=vhat[b:b + 1])
+        del kn, vn
+    Q = wl.randn_bf16((B, H_q, D), wl._subseed(sh.seed, 73), dev)
+    gates = torch.rand((B, H_q, 3), generator=wl._gen(dev, wl._subseed(sh.seed, 74)), device=dev)
+    seq = torch.full((B,), T, dtype=torch.int32, device=dev)
+    idx = torch.empty((B, H_kv, k_tot), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B, H_kv), dtype=torch.int32, device=dev)
+    O = torch.empty((B, H_q, D), dtype=torch.bfloat16, device=dev)
+    ws = binding.nsa_workspace(B, H_q, H_kv, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    evict = torch.ones(512 << 20 >> 2, dtype=torch.int32, device=dev)
+
+    def select():
+        binding.sparse_select_topk_heads(Q, ktil, seq, sh.n_init, sh.n_local, sh.k, idx, cnt, status=status)
+
+    def attend():
+        binding.sparse_decode_attn_nsa(Q, kc, vc, khat, vhat, idx, cnt, seq, w, gates, O, ws, n_split=args.n_split,
+                                       status=status)
+
+    def layer():
+        select()
+        attend()
+
+    select()
+    torch.cuda.synchronize()
+    t_attn = _event_times(attend, args.steps, args.warmup, evict)
+    t_sel = _event_times(select, args.steps, args.warmup, evict)
+    t_layer = _event_times(layer, args.steps, args.warmup, evict)
+    torch.cuda.synchronize()
+    assert status.item() == 0, f"device status {status.item()}"
+    pairs = B * H_kv
+    w_blocks = (w + BLK - 1) // BLK
+    nbytes = {"selected_kv": pairs * k_tot * KV_BLOCK_BYTES, "window_kv": pairs * w_blocks * KV_BLOCK_BYTES,
+              "compressed_rows": pairs * N * 2 * D * 2, "q_o_gates": B * H_q * (2 * D * 2 + 12)}
+    attn_bytes = sum(nbytes.values())
+    gbs, frac = _rate(attn_bytes, t_attn["median_us"], peak)
+    sel_bytes = pairs * N * KTIL_ROW_BYTES
+    sgbs, sfrac = _rate(sel_bytes, t_sel["median_us"], peak)
+    lgbs, lfrac = _rate(attn_bytes + sel_bytes, t_layer["median_us"], peak)
+    line = {"case": "nsa128k", "workload": f"nsa_decode_128k_b{B}_hq{H_q}_hkv{H_kv}_w{w}",
+            "unit_of_work": "one NSA decode layer (multi-head routing + gated three-branch attention)",
+            "attention": {"launches": 1, **t_attn, "algorithmic_bytes": nbytes, "achieved_gbs": gbs,
+                          "frac_of_measured_hbm": frac},
+            "routing": {"call": "sparse_select_topk_heads", **t_sel, "algorithmic_bytes": sel_bytes,
+                        "achieved_gbs": sgbs, "frac_of_measured_hbm": sfrac},
+            "layer": {**t_layer, "achieved_gbs": lgbs, "frac_of_measured_hbm": lfrac,
+                      "layers_per_s": round(1e6 / t_layer["median_us"], 1)},
+            "peak_gbs": peak, "peak_source": src, "l2": "512 MB read evicts L2 before each timed call"}
+    print(json.dumps(line), flush=True)
+
+
 def run_other_case(args, local_rank):
     import torch
     from block_sparse_long_pool_gb300 import workloads as wl
@@ -1008,6 +1084,8 @@ def run_other_case(args, local_rank):
         run_single_layer_case(args, dev, wl.LLAMA8B_32K, "append32k")
     elif args.case == "verify64k":
         run_verify_case(args, dev)
+    elif args.case == "nsa128k":
+        run_nsa_case(args, dev)
     else:
         run_offload_case(args, dev)
 
@@ -1021,10 +1099,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", choices=["step", "layer", "select", "single4k", "append32k", "verify64k",
-                                       "offload128k"], default="step",
+                                       "offload128k", "nsa128k"], default="step",
                     help="step: the 80-layer decode step (the bench line); layer: one physical layer, "
                          "kernels serialised and timed alone (for profiling); select: selection only; "
-                         "single4k / append32k / verify64k / offload128k: the other workloads, one line each")
+                         "single4k / append32k / verify64k / offload128k / nsa128k: the other workloads, "
+                         "one line each")
     ap.add_argument("--n-split", type=int, default=0)
     ap.add_argument("--no-workspace", action="store_true", help="layer case: attention without a workspace (cluster path)")
     ap.add_argument("--workspace", action="store_true",
@@ -1040,7 +1119,7 @@ def main():
     rank, world, local_rank = dist_env()
     if args.case in ("layer", "select"):
         run_layer_case(args, local_rank)
-    elif args.case in ("single4k", "append32k", "verify64k", "offload128k"):
+    elif args.case in ("single4k", "append32k", "verify64k", "offload128k", "nsa128k"):
         run_other_case(args, local_rank)
     elif args.impl == "reference":
         run_reference(args, rank, world, local_rank)

@@ -40,6 +40,7 @@ SIGNATURES = {
     "sparse_last_error": (ctypes.c_char_p, []),
     "sparse_version": (_I, []),
     "sparse_pool_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _LL, _I, _LL, _I, _P]),
+    "sparse_pool_append_kv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _LL, _I, _LL, _I, _P]),
     "sparse_select_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P]),
     "sparse_select_topk_heads": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _P, _P, _I, _P, _P]),
     "sparse_decode_attn": (_I, [_P, _P, _P, _LL, _P, _P, _P, _I, _P, _I, _I, _I, _F, _P, _P, _I, _U, _P, _SZ,
@@ -56,6 +57,9 @@ SIGNATURES = {
     "sparse_verify_attn_shared": (_I, [_P, _P, _P, _LL, _P, _I, _I, _I, _I, _P, _I, _I, _I, _F, _P, _P, _I,
                                        _P, _P]),
     "sparse_gather_offloaded": (_I, [_P, _P, _LL, _P, _P, _I, _I, _I, _P, _P, _P, _I, _P, _P]),
+    "sparse_decode_attn_nsa": (_I, [_P, _P, _P, _LL, _P, _P, _I, _P, _P, _I, _P, _I, _I, _I, _LL, _P, _F, _P, _P,
+                                    _SZ, _I, _U, _P, _P]),
+    "sparse_decode_attn_nsa_workspace_size": (_SZ, [_I, _I, _I]),
 }
 
 
@@ -128,6 +132,28 @@ def sparse_pool_append(k_cache, v_cache, ktil, k_new, v_new, len_before: int, st
     rc = load().sparse_pool_append(_ptr(k_cache), _ptr(v_cache), _ptr(ktil), _ptr(k_new), _ptr(v_new), B, H_kv,
                                    T_cap, N_cap, int(len_before), n_new, _stream(stream))
     _check(rc, "sparse_pool_append")
+
+
+def sparse_pool_append_kv(k_cache, v_cache, ktil, vtil, k_new, v_new, len_before: int, khat=None, vhat=None,
+                          stream=None):
+    """Append k_new/v_new [B][H_kv][n_new][128] at len_before, update the pooled keys
+    ktil and values vtil (fp32) and, when given, their bf16 copies khat / vhat."""
+    B, H_kv, T_cap, _ = k_cache.shape
+    n_new = k_new.shape[2]
+    N_cap = ktil.shape[2]
+    _need(k_cache, "k_cache", torch.bfloat16, shape=(B, H_kv, T_cap, D))
+    _need(v_cache, "v_cache", torch.bfloat16, shape=(B, H_kv, T_cap, D))
+    _need(ktil, "ktil", torch.float32, shape=(B, H_kv, N_cap, D))
+    _need(vtil, "vtil", torch.float32, shape=(B, H_kv, N_cap, D))
+    for t, n in ((khat, "khat"), (vhat, "vhat")):
+        if t is not None:
+            _need(t, n, torch.bfloat16, shape=(B, H_kv, N_cap, D))
+    _need(k_new, "k_new", torch.bfloat16, shape=(B, H_kv, n_new, D))
+    _need(v_new, "v_new", torch.bfloat16, shape=(B, H_kv, n_new, D))
+    rc = load().sparse_pool_append_kv(_ptr(k_cache), _ptr(v_cache), _ptr(ktil), _ptr(vtil), _ptr(khat), _ptr(vhat),
+                                      _ptr(k_new), _ptr(v_new), B, H_kv, T_cap, N_cap, int(len_before), n_new,
+                                      _stream(stream))
+    _check(rc, "sparse_pool_append_kv")
 
 
 def sparse_select_topk(F, ktil, seq_len, n_init: int, n_local: int, k: int, idx_out, count_out,
@@ -329,3 +355,42 @@ def sparse_gather_offloaded(k_host, v_host, idx, count, k_ring, v_ring, ready_fl
                                         H_kv, _ptr(k_ring), _ptr(v_ring), _ptr(ready_flag), n_ctas, _ptr(status),
                                         _stream(stream))
     _check(rc, "sparse_gather_offloaded")
+
+
+def sparse_decode_attn_nsa_workspace_size(B: int, H_q: int, H_kv: int) -> int:
+    """Bytes of the sparse_decode_attn_nsa workspace (0: invalid sizes)."""
+    return int(load().sparse_decode_attn_nsa_workspace_size(B, H_q, H_kv))
+
+
+def nsa_workspace(B: int, H_q: int, H_kv: int, device="cuda"):
+    """A zeroed workspace tensor for sparse_decode_attn_nsa."""
+    return torch.zeros(sparse_decode_attn_nsa_workspace_size(B, H_q, H_kv), dtype=torch.uint8, device=device)
+
+
+def sparse_decode_attn_nsa(Q, k_cache, v_cache, khat, vhat, blk_idx, count, seq_len, window_tokens: int, gates, O,
+                           workspace, scale: float = 0.0, n_split: int = 0, flags: int = 0, status=None,
+                           stream=None):
+    """NSA gated three-branch decode: Q [B][H_q][128], K/V [B][H_kv][T_cap][128],
+    compressed rows khat/vhat [B][H_kv][N_cap][128], selected blocks blk_idx
+    [B][H_kv][k_tot] with count [B][H_kv], gates [B][H_q][3] = (g_c, g_s, g_w) fp32;
+    writes O [B][H_q][128] = g_c o_c + g_s o_s + g_w o_w."""
+    B, H_q, _ = Q.shape
+    _, H_kv, T_cap, _ = k_cache.shape
+    N_cap = khat.shape[2]
+    k_tot = blk_idx.shape[2]
+    _need(Q, "Q", torch.bfloat16, shape=(B, H_q, D))
+    _need(k_cache, "k_cache", torch.bfloat16, shape=(B, H_kv, T_cap, D))
+    _need(v_cache, "v_cache", torch.bfloat16, shape=(B, H_kv, T_cap, D))
+    _need(khat, "khat", torch.bfloat16, shape=(B, H_kv, N_cap, D))
+    _need(vhat, "vhat", torch.bfloat16, shape=(B, H_kv, N_cap, D))
+    _need(blk_idx, "blk_idx", torch.int32, shape=(B, H_kv, k_tot))
+    _need(count, "count", torch.int32, shape=(B, H_kv))
+    _need(seq_len, "seq_len", torch.int32, shape=(B,))
+    _need(gates, "gates", torch.float32, shape=(B, H_q, 3))
+    _need(O, "O", torch.bfloat16, shape=(B, H_q, D))
+    ws, ws_bytes = _ws(workspace)
+    rc = load().sparse_decode_attn_nsa(_ptr(Q), _ptr(k_cache), _ptr(v_cache), T_cap, _ptr(khat), _ptr(vhat), N_cap,
+                                       _ptr(blk_idx), _ptr(count), k_tot, _ptr(seq_len), B, H_q, H_kv,
+                                       int(window_tokens), _ptr(gates), float(scale), _ptr(O), ws, ws_bytes,
+                                       n_split, int(flags), _ptr(status), _stream(stream))
+    _check(rc, "sparse_decode_attn_nsa")

@@ -90,6 +90,13 @@ struct AttnParams {
     int n_local;
     int k_sel;
     int k_tot_next;
+    // NSA branches: fp32 output instead of bf16 O, and a block range computed from
+    // seq_len instead of a block table (1: the window of the last win_tokens tokens,
+    // masked token-granularly; 2: the compressed rows, one per 64-token block holding
+    // a token, all of them)
+    float *O32;
+    long long win_tokens;
+    int range_mode;
 };
 
 __device__ __forceinline__ uint32_t ld_b32(const uint16_t *p)
@@ -169,7 +176,8 @@ __device__ __forceinline__ void load_query(QueryFrags<NT> &q, const AttnParams &
 // position of the warp's first token; qmask selects the rows' queries (verification).
 template <int NT, bool VERIFY>
 __device__ __forceinline__ void attend_block(WarpState<NT> &st, const QueryFrags<NT> &q, uint32_t kst, long long tok0,
-                                             long long len, uint32_t qmask, float scale_log2, int w, int lane)
+                                             long long len, uint32_t qmask, float scale_log2, int w, int lane,
+                                             long long tok_lo = 0)
 {
     const int g8 = lane >> 2;
     const int jm = lane >> 3, rr = lane & 7;
@@ -202,7 +210,7 @@ __device__ __forceinline__ void attend_block(WarpState<NT> &st, const QueryFrags
         for (int i = 0; i < 4; ++i) {
             const int h = i & 1;
             const long long tok = tok0 + g8 + (i >> 1) * 8;
-            bool keep = tok < len && q.row_ok[nt][h];
+            bool keep = tok < len && tok >= tok_lo && q.row_ok[nt][h];
             if (VERIFY)
                 keep = keep && ((qmask >> q.row_q[nt][h]) & 1u);
             sacc[nt][i] = keep ? sacc[nt][i] * scale_log2 : -INFINITY;
@@ -350,17 +358,53 @@ __device__ __forceinline__ float lse_of(float M, float L)
 // ones become -1 (an out-of-range box is loaded for them: zeros, never a fault).  The
 // ready word, if any, is checked with a bounded wait.  Writes lslot / llog[0 .. n),
 // ctrl[kCtrlList] = n (0 when aborted) and ctrl[kCtrlAbort]; every lane returns n.
+// Rows a unit of batch element b attends over: its tokens, or for the compressed
+// branch (range_mode 2) its compressed rows, one per 64-token block holding a token.
+// The compressed rows are clamped to the pair_stride rows that exist (the producer
+// reports a length beyond them).
+__device__ __forceinline__ long long unit_len(const AttnParams &p, int b)
+{
+    const long long len = p.seq_len[b];
+    if (p.range_mode == 2) {
+        const long long rows = len <= 0 ? 0 : (len + kBlk - 1) / kBlk;
+        return rows < p.pair_stride ? rows : p.pair_stride;
+    }
+    return len;
+}
+
 __device__ __forceinline__ int producer_fetch_slice(const AttnParams &p, int pair, int i0, int cap, int *lslot,
                                                     int *llog, int *ctrl, int lane)
 {
-    int c = lane == 0 ? p.count[pair] : 0;
-    for (int i = lane; i < cap; i += 32) {
-        const size_t at = static_cast<size_t>(pair) * p.k_tot + i0 + i;
-        const int logical = p.blk_logical[at];
-        llog[i] = logical;
-        lslot[i] = p.blk_slot != nullptr ? p.blk_slot[at] : logical;
+    int c;
+    if (p.range_mode != 0) {
+        // a contiguous block range from the length: the window, or every block
+        const int b = pair / p.H_kv;
+        const long long len = unit_len(p, b);
+        if (p.range_mode == 2 && lane == 0 && p.seq_len[b] > p.pair_stride * kBlk)
+            report(p.status, SPARSE_ERR_BAD_INDEX);
+        const int nb = len <= 0 ? 0 : static_cast<int>((len + kBlk - 1) / kBlk);
+        long long w0 = p.range_mode == 1 ? len - p.win_tokens : 0;
+        w0 = w0 < 0 ? 0 : w0;
+        const int first = static_cast<int>(w0 / kBlk);
+        c = nb > first ? nb - first : 0;
+        if (p.range_mode == 1 && p.win_tokens <= 0)
+            c = 0;
+        for (int i = lane; i < cap; i += 32) {
+            llog[i] = first + i0 + i;
+            lslot[i] = first + i0 + i;
+        }
+        if (c > p.k_tot)
+            c = -1;   // reported below: the range is longer than the table the host sized
+    } else {
+        c = lane == 0 ? p.count[pair] : 0;
+        for (int i = lane; i < cap; i += 32) {
+            const size_t at = static_cast<size_t>(pair) * p.k_tot + i0 + i;
+            const int logical = p.blk_logical[at];
+            llog[i] = logical;
+            lslot[i] = p.blk_slot != nullptr ? p.blk_slot[at] : logical;
+        }
+        c = __shfl_sync(0xffffffffu, c, 0);
     }
-    c = __shfl_sync(0xffffffffu, c, 0);
     if (c < 0 || c > p.k_tot) {
         if (lane == 0)
             report(p.status, SPARSE_ERR_BAD_INDEX);
@@ -504,7 +548,10 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
         } else {
             out = (static_cast<size_t>(b) * p.H_q + g * p.G + row) * kD + d;
         }
-        *reinterpret_cast<uint32_t *>(p.O + out) = pack_bf16x2(ox * inv, oy * inv);
+        if (p.O32 != nullptr)
+            *reinterpret_cast<float2 *>(p.O32 + out) = make_float2(ox * inv, oy * inv);
+        else
+            *reinterpret_cast<uint32_t *>(p.O + out) = pack_bf16x2(ox * inv, oy * inv);
         if (!VERIFY && rank == 0 && d == 0 && p.lse != nullptr)
             p.lse[static_cast<size_t>(b) * p.H_q + g * p.G + row] = lse_of(M, L);
     }

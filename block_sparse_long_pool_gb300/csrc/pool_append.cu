@@ -4,6 +4,10 @@
 // cache is updated by mean pooling at O(d) cost per touched block (background
 // eq.(4), one mean per 64-token block).  The running mean of block j becomes
 //     ktil_j <- (n_old * ktil_j + sum of the new keys in j) / n_total.
+// sparse_pool_append_kv keeps the compressed values the same way (the pooled value
+// rows of NSA's compressed branch, SSV notes' NSA math step 4) and, optionally, bf16
+// copies of the touched compressed key and value rows: the rows that the compressed
+// branch's tensor-core attention reads.
 //
 // One CTA per (touched block, pair): 16 threads cover the 16 sixteen-byte chunks of
 // a 256-byte token row, 16 rows per pass; each thread copies its rows of K and V
@@ -20,6 +24,9 @@ struct AppendParams {
     uint16_t *k_cache;
     uint16_t *v_cache;
     float *ktil;
+    float *vtil;        // pooled values, or null
+    uint16_t *khat;     // bf16 copies of the touched ktil rows, or null
+    uint16_t *vhat;     // bf16 copies of the touched vtil rows, or null
     const uint16_t *k_new;
     const uint16_t *v_new;
     long long T_cap;
@@ -32,6 +39,7 @@ struct AppendParams {
 __global__ void __launch_bounds__(kThreads) pool_append_kernel(const AppendParams p)
 {
     __shared__ float red[16][kD + 4];
+    __shared__ float redv[16][kD + 4];
 
     const int pair = blockIdx.y;
     const int j = p.first_block + static_cast<int>(blockIdx.x);
@@ -50,10 +58,12 @@ __global__ void __launch_bounds__(kThreads) pool_append_kernel(const AppendParam
     const size_t cache_base = static_cast<size_t>(pair) * static_cast<size_t>(p.T_cap) * kD;
     const size_t new_base = static_cast<size_t>(pair) * static_cast<size_t>(p.n_new) * kD;
 
-    float acc[8];
+    float acc[8], accv[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 8; ++i) {
         acc[i] = 0.f;
+        accv[i] = 0.f;
+    }
 
     for (long long t = t_begin + r0; t < t_end; t += 16) {
         const size_t src = new_base + static_cast<size_t>(t - p.len_before) * kD + c * 8;
@@ -63,16 +73,22 @@ __global__ void __launch_bounds__(kThreads) pool_append_kernel(const AppendParam
         *reinterpret_cast<uint4 *>(p.k_cache + dst) = kv;
         *reinterpret_cast<uint4 *>(p.v_cache + dst) = vv;
         const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&kv);
+        const __nv_bfloat162 *hv = reinterpret_cast<const __nv_bfloat162 *>(&vv);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const float2 f = __bfloat1622float2(h[i]);
             acc[2 * i] += f.x;
             acc[2 * i + 1] += f.y;
+            const float2 fv = __bfloat1622float2(hv[i]);
+            accv[2 * i] += fv.x;
+            accv[2 * i + 1] += fv.y;
         }
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 8; ++i) {
         red[r0][c * 8 + i] = acc[i];
+        redv[r0][c * 8 + i] = accv[i];
+    }
     __syncthreads();
 
     if (threadIdx.x < kD) {
@@ -81,42 +97,59 @@ __global__ void __launch_bounds__(kThreads) pool_append_kernel(const AppendParam
 #pragma unroll
         for (int r = 0; r < 16; ++r)
             s += red[r][d];
-        float *kt = p.ktil + (static_cast<size_t>(pair) * p.N_cap + j) * kD + d;
-        const float prev = n_old > 0 ? *kt * static_cast<float>(n_old) : 0.f;
-        *kt = (prev + s) / static_cast<float>(n_total);
+        const size_t at = (static_cast<size_t>(pair) * p.N_cap + j) * kD + d;
+        const float prev = n_old > 0 ? p.ktil[at] * static_cast<float>(n_old) : 0.f;
+        const float mean = (prev + s) / static_cast<float>(n_total);
+        p.ktil[at] = mean;
+        if (p.khat != nullptr)
+            p.khat[at] = __bfloat16_as_ushort(__float2bfloat16_rn(mean));
+    } else if (p.vtil != nullptr && threadIdx.x < 2 * kD) {
+        const int d = threadIdx.x - kD;
+        float s = 0.f;
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            s += redv[r][d];
+        const size_t at = (static_cast<size_t>(pair) * p.N_cap + j) * kD + d;
+        const float prev = n_old > 0 ? p.vtil[at] * static_cast<float>(n_old) : 0.f;
+        const float mean = (prev + s) / static_cast<float>(n_total);
+        p.vtil[at] = mean;
+        if (p.vhat != nullptr)
+            p.vhat[at] = __bfloat16_as_ushort(__float2bfloat16_rn(mean));
     }
 }
 
 }  // namespace
 
-extern "C" SPARSE_API int sparse_pool_append(uint16_t *k_cache, uint16_t *v_cache, float *ktil,
-                                             const uint16_t *k_new, const uint16_t *v_new, int B,
-                                             int H_kv, long long T_cap, int N_cap,
-                                             long long len_before, int n_new, void *stream)
+namespace {
+
+int append_impl(const char *name, uint16_t *k_cache, uint16_t *v_cache, float *ktil, float *vtil,
+                uint16_t *khat, uint16_t *vhat, const uint16_t *k_new, const uint16_t *v_new, int B, int H_kv,
+                long long T_cap, int N_cap, long long len_before, int n_new, void *stream)
 {
     using sp_host::aligned16;
     using sp_host::fail;
     if (!k_cache || !v_cache || !ktil || !k_new || !v_new)
-        return fail(SPARSE_ERR_INVALID_ARG, "sparse_pool_append: null pointer");
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: null pointer", name);
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(ktil) || !aligned16(k_new) ||
-        !aligned16(v_new))
-        return fail(SPARSE_ERR_INVALID_ARG, "sparse_pool_append: buffers must be 16-byte aligned");
+        !aligned16(v_new) || (vtil != nullptr && !aligned16(vtil)) || (khat != nullptr && !aligned16(khat)) ||
+        (vhat != nullptr && !aligned16(vhat)))
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: buffers must be 16-byte aligned", name);
     if (B < 1 || H_kv < 1 || n_new < 1 || len_before < 0 || T_cap < 1 || N_cap < 1)
-        return fail(SPARSE_ERR_INVALID_ARG, "sparse_pool_append: bad size (B=%d H_kv=%d n_new=%d len=%lld)",
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: bad size (B=%d H_kv=%d n_new=%d len=%lld)", name,
                     B, H_kv, n_new, len_before);
     const long long len_after = len_before + n_new;
     if (len_after > T_cap)
-        return fail(SPARSE_ERR_INVALID_ARG, "sparse_pool_append: %lld tokens exceed T_cap=%lld", len_after,
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: %lld tokens exceed T_cap=%lld", name, len_after,
                     T_cap);
     if ((len_after + kBlk - 1) / kBlk > N_cap)
-        return fail(SPARSE_ERR_INVALID_ARG, "sparse_pool_append: %lld tokens need more than N_cap=%d blocks",
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: %lld tokens need more than N_cap=%d blocks", name,
                     len_after, N_cap);
     const long long pairs = static_cast<long long>(B) * H_kv;
     if (pairs > 65535)
-        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_pool_append: B*H_kv=%lld > 65535", pairs);
+        return fail(SPARSE_ERR_UNSUPPORTED, "%s: B*H_kv=%lld > 65535", name, pairs);
     const int first_block = static_cast<int>(len_before / kBlk);
     const int last_block = static_cast<int>((len_after - 1) / kBlk);
-    AppendParams p{k_cache, v_cache, ktil, k_new, v_new, T_cap, len_before, N_cap, n_new, first_block};
+    AppendParams p{k_cache, v_cache, ktil, vtil, khat, vhat, k_new, v_new, T_cap, len_before, N_cap, n_new, first_block};
     dim3 grid(static_cast<unsigned>(last_block - first_block + 1), static_cast<unsigned>(pairs));
     {
         sp_host::DeviceInfo dinfo;
@@ -128,5 +161,27 @@ extern "C" SPARSE_API int sparse_pool_append(uint16_t *k_cache, uint16_t *v_cach
             return rc0;
     }
     pool_append_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(p);
-    return sp_host::cuda_status(cudaGetLastError(), "sparse_pool_append launch");
+    return sp_host::cuda_status(cudaGetLastError(), name);
+}
+
+}  // namespace
+
+extern "C" SPARSE_API int sparse_pool_append(uint16_t *k_cache, uint16_t *v_cache, float *ktil,
+                                             const uint16_t *k_new, const uint16_t *v_new, int B,
+                                             int H_kv, long long T_cap, int N_cap,
+                                             long long len_before, int n_new, void *stream)
+{
+    return append_impl("sparse_pool_append", k_cache, v_cache, ktil, nullptr, nullptr, nullptr, k_new, v_new, B,
+                       H_kv, T_cap, N_cap, len_before, n_new, stream);
+}
+
+extern "C" SPARSE_API int sparse_pool_append_kv(uint16_t *k_cache, uint16_t *v_cache, float *ktil, float *vtil,
+                                                uint16_t *khat, uint16_t *vhat, const uint16_t *k_new,
+                                                const uint16_t *v_new, int B, int H_kv, long long T_cap, int N_cap,
+                                                long long len_before, int n_new, void *stream)
+{
+    if (vtil == nullptr)
+        return sp_host::fail(SPARSE_ERR_INVALID_ARG, "sparse_pool_append_kv: null vtil");
+    return append_impl("sparse_pool_append_kv", k_cache, v_cache, ktil, vtil, khat, vhat, k_new, v_new, B, H_kv,
+                       T_cap, N_cap, len_before, n_new, stream);
 }

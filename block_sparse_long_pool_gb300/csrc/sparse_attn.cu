@@ -38,6 +38,7 @@
 #include <limits.h>
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -111,12 +112,12 @@ __device__ __forceinline__ void build_union(const AttnParams &p, uint8_t *base, 
     }
 }
 
+// One CTA of a cluster: unit `unit` (a pair, or a pair x query group), slice `rank` of
+// its block list; the cluster's S partial states are merged and written.
 template <int NT, bool VERIFY>
-__global__ void __launch_bounds__(kThreads, 2)
-    sparse_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                       const AttnParams p)
+__device__ __forceinline__ void attn_cluster_cta(const CUtensorMap *kmap, const CUtensorMap *vmap,
+                                                 const AttnParams &p, int unit)
 {
-    constexpr int ROWS = 8 * NT;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -132,11 +133,11 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     int pair, q0 = 0, rows_valid;
     if (VERIFY) {
-        pair = blockIdx.y / p.n_groups;
-        q0 = static_cast<int>(blockIdx.y % p.n_groups) * p.C;
+        pair = unit / p.n_groups;
+        q0 = (unit % p.n_groups) * p.C;
         rows_valid = min(p.C, p.N_q - q0) * p.G;
     } else {
-        pair = blockIdx.y;
+        pair = unit;
         rows_valid = p.G;
     }
     const int b = pair / p.H_kv, g = pair % p.H_kv;
@@ -194,8 +195,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             named_barrier_arrive(1, kThreads);   // the slice and its length are in shared memory
         }
         if (lane == 0 && my_n > 0) {
-            prefetch_tensormap(&kmap);
-            prefetch_tensormap(&vmap);
+            prefetch_tensormap(kmap);
+            prefetch_tensormap(vmap);
             const uint64_t pol = policy_evict_first();
             for (int it = 0; it < my_n; ++it) {
                 const int s = it % kStages;
@@ -209,10 +210,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int row = slot >= 0 ? slot * kBlk : static_cast<int>(min(p.pair_stride, (long long)INT_MAX - kBlk));
                 const uint32_t dst = base_s + s * kStageBytes;
                 mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
-                tma_load_3d(dst, &kmap, bar_full + 8 * s, 0, row, pair, pol);
-                tma_load_3d(dst + kHalfBytes, &kmap, bar_full + 8 * s, 64, row, pair, pol);
-                tma_load_3d(dst + kTileBytes, &vmap, bar_full + 8 * s, 0, row, pair, pol);
-                tma_load_3d(dst + kTileBytes + kHalfBytes, &vmap, bar_full + 8 * s, 64, row, pair, pol);
+                tma_load_3d(dst, kmap, bar_full + 8 * s, 0, row, pair, pol);
+                tma_load_3d(dst + kHalfBytes, kmap, bar_full + 8 * s, 64, row, pair, pol);
+                tma_load_3d(dst + kTileBytes, vmap, bar_full + 8 * s, 0, row, pair, pol);
+                tma_load_3d(dst + kTileBytes + kHalfBytes, vmap, bar_full + 8 * s, 64, row, pair, pol);
             }
         }
     } else {
@@ -221,8 +222,11 @@ __global__ void __launch_bounds__(kThreads, 2)
             griddep_wait();   // Q may be written by the kernel before this one
         QueryFrags<NT> q;
         load_query<NT, VERIFY>(q, p, b, g, q0, rows_valid, lane);
+        long long tok_lo = 0;
         if (!VERIFY) {
-            len = p.seq_len[b];
+            len = unit_len(p, b);
+            if (p.range_mode == 1)
+                tok_lo = len - p.win_tokens > 0 ? len - p.win_tokens : 0;
             named_barrier_sync(1, kThreads);
             my_n = ctrl[kCtrlList];
         }
@@ -247,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             const long long tok0 = static_cast<long long>(logical) * kBlk + warp * 16;
             if (logical >= 0 && tok0 < len)
                 attend_block<NT, VERIFY>(st, q, base_s + s * kStageBytes, tok0, len, qmask, p.scale_log2, warp,
-                                         lane);
+                                         lane, tok_lo);
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(bar_empty + 8 * s);
@@ -261,6 +265,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     griddep_launch_dependents();
     cluster_merge_write<NT, VERIFY>(st, base, ctrl[kCtrlAbort] != 0, p, b, g, q0, rows_valid, rank, S, kThreads);
+}
+
+template <int NT, bool VERIFY>
+__global__ void __launch_bounds__(kThreads, 2)
+    sparse_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                       const __grid_constant__ AttnParams p)
+{
+    attn_cluster_cta<NT, VERIFY>(&kmap, &vmap, p, static_cast<int>(blockIdx.y));
 }
 
 // ---------------------------------------------------------------- split-KV decode, workspace merge
@@ -1341,4 +1353,219 @@ extern "C" SPARSE_API int sparse_verify_attn_shared(const uint16_t *Q, const uin
     return verify_impl("sparse_verify_attn_shared", kVerifySharedLayout, Q, k_cache, v_cache, T_cap, idx_q, n_sel,
                        N_q, C, window_blocks, seq_len, B, H_q, H_kv, scale, O, blocks_loaded, n_split, status,
                        stream);
+}
+
+// ---------------------------------------------------------------- NSA gated three-branch decode
+//
+// SSV notes, "NSA three-branch math" steps 3-6: the selected-block branch, the
+// compressed branch and the sliding-window branch each run their own softmax, and the
+// output is the gate-weighted sum g_c o^(c) + g_s o^(s) + g_w o^(w).  The notes take
+// the branches to need separate kernels with intermediate results in HBM.  Here the
+// three are one launch: grid (S, pairs, 3), blockIdx.z the branch, each branch a
+// cluster of S CTAs per pair running the same split-KV attention as the decode path
+// (the selected blocks from the table; the window as the block range of the last w
+// tokens, masked token by token; the compressed rows as one more bf16 "cache" with a
+// row per 64-token block).  Each cluster writes its normalised branch output o^(x) in
+// fp32 to a small workspace (L2-resident: 3 x G x 512 B per pair); the last of the
+// pair's 3 S CTAs to finish applies the gates and writes O.
+
+namespace {
+
+struct NsaParams {
+    AttnParams br[3];      // 0: selected blocks, 1: sliding window, 2: compressed rows
+    const float *gates;    // [B][H_q][3] = (g_c, g_s, g_w)
+    const float *part;     // [3][B * H_q][128] branch outputs (br[x].O32)
+    unsigned *arrivals;    // [pairs] arrival counters, zero between calls
+    uint16_t *O;           // [B][H_q][128]
+    unsigned target;       // 3 * S arrivals per pair
+};
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 2)
+    nsa_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                      const __grid_constant__ CUtensorMap khmap, const __grid_constant__ CUtensorMap vhmap,
+                      const __grid_constant__ NsaParams np)
+{
+    __shared__ int last;
+    const int branch = static_cast<int>(blockIdx.z);
+    const int pair = static_cast<int>(blockIdx.y);
+    const AttnParams &p = np.br[branch];
+    const bool compressed = branch == 2;
+    attn_cluster_cta<NT, false>(compressed ? &khmap : &kmap, compressed ? &vhmap : &vmap, p, pair);
+
+    // this CTA's share of o^(x) is written: publish it, count the arrival
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned prev = atomicAdd(&np.arrivals[pair], 1u);
+        last = prev + 1u == np.target;
+        if (last)
+            np.arrivals[pair] = 0u;   // ready for the next call
+    }
+    __syncthreads();
+    if (!last)
+        return;
+    __threadfence();
+    const int b = pair / p.H_kv, g = pair % p.H_kv;
+    const size_t stride = static_cast<size_t>(gridDim.y / p.H_kv) * p.H_q * kD;   // one branch's outputs
+    for (int item = threadIdx.x; item < p.G * (kD / 2); item += kThreads) {
+        const int row = item / (kD / 2);
+        const int d = 2 * (item - row * (kD / 2));
+        const size_t head = static_cast<size_t>(b) * p.H_q + g * p.G + row;
+        const size_t at = head * kD + d;
+        const float gc = np.gates[head * 3 + 0], gs = np.gates[head * 3 + 1], gw = np.gates[head * 3 + 2];
+        const float2 os = __ldcg(reinterpret_cast<const float2 *>(np.part + at));
+        const float2 ow = __ldcg(reinterpret_cast<const float2 *>(np.part + stride + at));
+        const float2 oc = __ldcg(reinterpret_cast<const float2 *>(np.part + 2 * stride + at));
+        const float x = fmaf(gc, oc.x, fmaf(gs, os.x, gw * ow.x));
+        const float y = fmaf(gc, oc.y, fmaf(gs, os.y, gw * ow.y));
+        *reinterpret_cast<uint32_t *>(np.O + at) = pack_bf16x2(x, y);
+    }
+}
+
+size_t nsa_counter_bytes(long long pairs)
+{
+    return (static_cast<size_t>(pairs) * sizeof(unsigned) + 255) & ~static_cast<size_t>(255);
+}
+
+size_t nsa_workspace_bytes(long long pairs, int H_q_total)
+{
+    return nsa_counter_bytes(pairs) + static_cast<size_t>(3) * H_q_total * kD * sizeof(float);
+}
+
+template <int NT>
+int launch_nsa(const NsaParams &np, const CUtensorMap *maps, int S, long long pairs, int device,
+               cudaStream_t stream)
+{
+    auto kern = nsa_decode_kernel<NT>;
+    const int smem = kSmemDecode + 1024;
+    static int configured[64];
+    int rc = sp_host::configure_kernel(reinterpret_cast<const void *>(kern), smem, device, configured);
+    if (rc != SPARSE_OK)
+        return rc;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(S), static_cast<unsigned>(pairs), 3);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    CUtensorMap m0 = maps[0], m1 = maps[1], m2 = maps[2], m3 = maps[3];
+    NsaParams prm = np;
+    void *args[] = {&m0, &m1, &m2, &m3, &prm};
+    return sp_host::cuda_status(cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(kern), args),
+                                "sparse_decode_attn_nsa launch");
+}
+
+}  // namespace
+
+extern "C" SPARSE_API size_t sparse_decode_attn_nsa_workspace_size(int B, int H_q, int H_kv)
+{
+    if (B < 1 || H_kv < 1 || H_q < H_kv || H_q % H_kv != 0)
+        return 0;
+    return nsa_workspace_bytes(static_cast<long long>(B) * H_kv, B * H_q);
+}
+
+extern "C" SPARSE_API int sparse_decode_attn_nsa(const uint16_t *Q, const uint16_t *k_cache, const uint16_t *v_cache,
+                                                 long long T_cap, const uint16_t *khat, const uint16_t *vhat,
+                                                 int N_cap, const int *blk_idx, const int *count, int k_tot,
+                                                 const int *seq_len, int B, int H_q, int H_kv,
+                                                 long long window_tokens, const float *gates, float scale,
+                                                 uint16_t *O, void *workspace, size_t workspace_bytes, int n_split,
+                                                 unsigned flags, int *status, void *stream)
+{
+    using sp_host::aligned16;
+    using sp_host::fail;
+    const char *name = "sparse_decode_attn_nsa";
+    if (!Q || !k_cache || !v_cache || !khat || !vhat || !blk_idx || !count || !seq_len || !gates || !O ||
+        !workspace)
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: null pointer", name);
+    if (!aligned16(Q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(khat) || !aligned16(vhat) ||
+        !aligned16(O) || !aligned16(workspace))
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: Q, the caches, O and the workspace must be 16-byte aligned", name);
+    if (B < 1 || H_kv < 1 || H_q < H_kv || H_q % H_kv != 0 || k_tot < 1 || T_cap < 1 || N_cap < 1 ||
+        window_tokens < 0)
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: bad size (B=%d H_q=%d H_kv=%d k_tot=%d N_cap=%d w=%lld)", name, B,
+                    H_q, H_kv, k_tot, N_cap, window_tokens);
+    if (T_cap > INT_MAX - 2 * kBlk || window_tokens > T_cap)
+        return fail(SPARSE_ERR_UNSUPPORTED, "%s: T_cap or window_tokens too large", name);
+    if (!isfinite(scale))
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: scale must be finite", name);
+    if ((flags & ~SPARSE_ATTN_BLOCKS_READY) != 0u)
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags);
+    const int G = H_q / H_kv;
+    if (G > 16)
+        return fail(SPARSE_ERR_UNSUPPORTED, "%s: G=%d > 16 query heads per KV head", name, G);
+    const long long pairs = static_cast<long long>(B) * H_kv;
+    if (pairs > 65535)
+        return fail(SPARSE_ERR_UNSUPPORTED, "%s: B*H_kv=%lld > 65535", name, pairs);
+    const size_t need = nsa_workspace_bytes(pairs, B * H_q);
+    if (workspace_bytes < need)
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", name, workspace_bytes, need);
+    sp_host::DeviceInfo dev;
+    int rc = sp_host::device_info(&dev);
+    if (rc != SPARSE_OK)
+        return rc;
+    if (n_split < 0)
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: n_split < 0", name);
+    // block lists: the table, the window's blocks, the compressed rows' 64-row tiles
+    const int k_win = static_cast<int>((window_tokens + kBlk - 1) / kBlk) + 1;
+    const int k_cmp = (N_cap + kBlk - 1) / kBlk;
+    const int k_max = std::max(k_tot, std::max(k_win, k_cmp));
+    int S;
+    if ((rc = choose_split(n_split, pairs, k_max, dev.sm_count, &S)) != SPARSE_OK)
+        return rc;
+    while ((k_max + S - 1) / S > kMaxListCta && S < kMaxSplit && n_split == 0)
+        S *= 2;
+    if ((k_max + S - 1) / S > kMaxListCta)
+        return fail(SPARSE_ERR_UNSUPPORTED, "%s: %d blocks per CTA exceed %d", name, (k_max + S - 1) / S,
+                    kMaxListCta);
+    CUtensorMap maps[4];
+    if ((rc = sp_host::make_kv_tensor_map(&maps[0], k_cache, T_cap, pairs)) != SPARSE_OK ||
+        (rc = sp_host::make_kv_tensor_map(&maps[1], v_cache, T_cap, pairs)) != SPARSE_OK ||
+        (rc = sp_host::make_kv_tensor_map(&maps[2], khat, N_cap, pairs)) != SPARSE_OK ||
+        (rc = sp_host::make_kv_tensor_map(&maps[3], vhat, N_cap, pairs)) != SPARSE_OK)
+        return rc;
+    float *part = reinterpret_cast<float *>(static_cast<char *>(workspace) + nsa_counter_bytes(pairs));
+    const size_t branch_floats = static_cast<size_t>(B) * H_q * kD;
+    NsaParams np = {};
+    for (int x = 0; x < 3; ++x) {
+        AttnParams &p = np.br[x];
+        p.Q = Q;
+        p.seq_len = seq_len;
+        p.status = status;
+        p.H_q = H_q;
+        p.H_kv = H_kv;
+        p.G = G;
+        p.n_groups = 1;
+        p.flags = flags;
+        p.scale_log2 = scale_log2_of(scale);
+        p.O32 = part + x * branch_floats;
+    }
+    np.br[0].blk_logical = blk_idx;
+    np.br[0].count = count;
+    np.br[0].k_tot = k_tot;
+    np.br[0].pair_stride = T_cap;
+    np.br[1].range_mode = 1;
+    np.br[1].win_tokens = window_tokens;
+    np.br[1].k_tot = k_win;
+    np.br[1].pair_stride = T_cap;
+    np.br[2].range_mode = 2;
+    np.br[2].k_tot = k_cmp;
+    np.br[2].pair_stride = N_cap;
+    np.gates = gates;
+    np.part = part;
+    np.arrivals = static_cast<unsigned *>(workspace);
+    np.O = O;
+    np.target = 3u * static_cast<unsigned>(S);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return G <= 8 ? launch_nsa<1>(np, maps, S, pairs, dev.device, st)
+                  : launch_nsa<2>(np, maps, S, pairs, dev.device, st);
 }

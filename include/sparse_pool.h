@@ -79,6 +79,24 @@ SPARSE_API int sparse_pool_append(uint16_t *k_cache, uint16_t *v_cache, float *k
                                   long long len_before, int n_new, void *stream);
 
 /*
+ * sparse_pool_append_kv -- sparse_pool_append that also keeps the compressed values,
+ * the rows of NSA's compressed branch ([SSV] "NSA three-branch math", step 4, read
+ * as mean pooling like the keys, [SparDA] eq.(4)):
+ *     vtil[p][j] = (n_old * vtil[p][j] + sum of the new values in block j) / n_total,
+ * and, when khat / vhat are given, bf16 copies (round to nearest even) of every ktil
+ * and vtil row it writes: the compressed cache that sparse_decode_attn_nsa reads.
+ *   vtil         [B][H_kv][N_cap][128] fp32, read-modify-written (required).
+ *   khat, vhat   [B][H_kv][N_cap][128] bf16, written for the touched rows; either may
+ *                be NULL.
+ * Every other argument and requirement is that of sparse_pool_append.
+ */
+SPARSE_API int sparse_pool_append_kv(uint16_t *k_cache, uint16_t *v_cache, float *ktil,
+                                     float *vtil, uint16_t *khat, uint16_t *vhat,
+                                     const uint16_t *k_new, const uint16_t *v_new,
+                                     int B, int H_kv, long long T_cap, int N_cap,
+                                     long long len_before, int n_new, void *stream);
+
+/*
  * sparse_select_topk -- [SparDA] §4.1 eq.(6), §4.2 Alg.1 step 2, §4.3 eq.(9).
  * For every pair: N_b = ceil(seq_len[b] / 64); B_init = blocks [0, n_init);
  * B_local = the last n_local blocks [N_b - n_local, N_b); every other block j is a
@@ -329,6 +347,48 @@ SPARSE_API int sparse_verify_attn_shared(const uint16_t *Q, const uint16_t *k_ca
                                          int H_q, int H_kv, float scale, uint16_t *O,
                                          long long *blocks_loaded, int n_split, int *status,
                                          void *stream);
+
+/*
+ * sparse_decode_attn_nsa -- NSA's gated three-branch decode output, [SSV] "NSA
+ * three-branch math" steps 3-6 (the three-branch sum of its background section):
+ *     o = g_c o^(c) + g_s o^(s) + g_w o^(w)
+ * for every query head of every pair, each branch its own softmax with scale 1/sqrt(d)
+ * (or `scale`):
+ *   o^(s)  over the tokens of the selected blocks blk_idx[p][0 .. count[p])
+ *          (sparse_decode_attn's table, logical block ids, no slot indirection);
+ *   o^(w)  over the last window_tokens tokens [len - w, len), token-granular;
+ *   o^(c)  over the compressed rows khat / vhat [p][0 .. N_b), N_b = ceil(len / 64),
+ *          one row per block holding a token (sparse_pool_append_kv keeps them);
+ * a branch with no rows contributes zero.  The gates are inputs: NSA learns them.
+ *   Q                 [B][H_q][128] bf16.
+ *   k_cache, v_cache  [B][H_kv][T_cap][128] bf16.
+ *   khat, vhat        [B][H_kv][N_cap][128] bf16 compressed rows, N_cap >= N_b.
+ *   blk_idx, count    [B*H_kv][k_tot] int32 and [B*H_kv] int32, as sparse_select_topk
+ *                     writes them; ids outside [0, T_cap / 64) are skipped and reported.
+ *   seq_len           [B] int32 tokens present.
+ *   window_tokens     w, 0 <= w <= T_cap.
+ *   gates             [B][H_q][3] fp32 = (g_c, g_s, g_w) per query head.
+ *   O                 [B][H_q][128] bf16, written.
+ *   workspace         device memory of sparse_decode_attn_nsa_workspace_size() bytes:
+ *                     per-pair arrival counters, then the three branch outputs (fp32).
+ *                     It must be all zero before the first call; every call returns
+ *                     the counters to zero.  Calls that share it must not overlap.
+ *   n_split           CTAs per branch and pair (1, 2, 4 or 8; 0 = from the SM count).
+ *   flags             0 or SPARSE_ATTN_BLOCKS_READY (as for sparse_decode_attn).
+ * One launch runs the three branches (the notes run three kernels); the last CTA of a
+ * pair to finish applies the gates.  G = H_q / H_kv <= 16.
+ */
+SPARSE_API int sparse_decode_attn_nsa(const uint16_t *Q, const uint16_t *k_cache,
+                                      const uint16_t *v_cache, long long T_cap,
+                                      const uint16_t *khat, const uint16_t *vhat, int N_cap,
+                                      const int *blk_idx, const int *count, int k_tot,
+                                      const int *seq_len, int B, int H_q, int H_kv,
+                                      long long window_tokens, const float *gates, float scale,
+                                      uint16_t *O, void *workspace, size_t workspace_bytes,
+                                      int n_split, unsigned flags, int *status, void *stream);
+
+/* Bytes of the sparse_decode_attn_nsa workspace for these sizes; 0 if they are invalid. */
+SPARSE_API size_t sparse_decode_attn_nsa_workspace_size(int B, int H_q, int H_kv);
 
 /*
  * sparse_gather_offloaded -- [SparDA] §4.5 (persistent prefetch of selected blocks,

@@ -171,3 +171,41 @@ def test_select_heads_rejects_bad_arguments(lib):
     assert call(4, 64) == binding.SPARSE_ERR_UNSUPPORTED                   # G = 32 > 16
     assert call(7, -1.0) == binding.SPARSE_ERR_INVALID_ARG                 # negative scale
     assert call(13, 10) == binding.SPARSE_ERR_INVALID_ARG                  # k_tot < n_init + n_local + k
+
+
+def test_append_kv_rejects_bad_arguments(lib):
+    f = lib.sparse_pool_append_kv
+    ok = (FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, 1, 1, 128, 2, 0, 1, None)
+    bad_vtil = ok[:3] + (None,) + ok[4:]
+    assert f(*bad_vtil) == binding.SPARSE_ERR_INVALID_ARG
+    odd_khat = ok[:4] + (ODD,) + ok[5:]
+    assert f(*odd_khat) == binding.SPARSE_ERR_INVALID_ARG
+    too_long = ok[:12] + (100, 40) + ok[14:]   # 140 tokens do not fit T_cap = 128
+    assert f(*too_long) == binding.SPARSE_ERR_INVALID_ARG
+
+
+def test_nsa_rejects_bad_arguments(lib):
+    f = lib.sparse_decode_attn_nsa
+    # Q, K, V, T_cap, khat, vhat, N_cap, idx, count, k_tot, seq_len, B, H_q, H_kv, w, gates, scale, O, ws,
+    # ws_bytes, n_split, flags, status, stream
+    ok = [FAKE, FAKE, FAKE, 4096, FAKE, FAKE, 64, FAKE, FAKE, 8, FAKE, 1, 8, 1, 512, FAKE, 0.0, FAKE, FAKE,
+          1 << 20, 0, 0, None, None]
+
+    def call(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+
+    assert call(a4=None) == binding.SPARSE_ERR_INVALID_ARG            # no khat
+    assert call(a18=None) == binding.SPARSE_ERR_INVALID_ARG           # no workspace
+    assert call(a5=ODD) == binding.SPARSE_ERR_INVALID_ARG             # misaligned vhat
+    assert call(a12=12, a13=8) == binding.SPARSE_ERR_INVALID_ARG      # H_q not a multiple of H_kv
+    assert call(a14=-1) == binding.SPARSE_ERR_INVALID_ARG             # negative window
+    assert call(a14=5000) == binding.SPARSE_ERR_UNSUPPORTED           # window beyond T_cap
+    assert call(a12=32, a13=1) == binding.SPARSE_ERR_UNSUPPORTED      # G = 32
+    assert call(a19=16) == binding.SPARSE_ERR_INVALID_ARG             # workspace too small
+    assert call(a21=4) == binding.SPARSE_ERR_INVALID_ARG              # unknown flag
+    assert call(a16=float("nan")) == binding.SPARSE_ERR_INVALID_ARG   # scale
+    assert lib.sparse_decode_attn_nsa_workspace_size(0, 8, 1) == 0
+    assert lib.sparse_decode_attn_nsa_workspace_size(8, 64, 8) == 256 + 3 * 8 * 64 * 128 * 4

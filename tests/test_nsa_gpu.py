@@ -1,0 +1,282 @@
+"""GPU parity of NSA's gated three-branch decode (SSV notes, "NSA three-branch math"
+steps 3-6) and of the pooled-value append that feeds its compressed branch.
+
+sparse_decode_attn_nsa is checked against oracle.nsa:
+  * with the compressed rows given to both sides as the same bf16 values (the bf16
+    rounding of the oracle's fp64 pooling), so only the kernel's arithmetic differs;
+  * through the whole chain (sparse_pool_append_kv builds the caches and the bf16
+    compressed rows on the GPU; the oracle pools in fp64), which adds the bf16
+    rounding of the compressed rows (relative 2^-9) to the error budget;
+  * branch by branch (gates (1,0,0), (0,1,0), (0,0,1)) and with random gates.
+Tolerances: those of parity_utils (max abs 2e-2, mean abs 2e-3).  Every input comes
+from the seeded generators or from the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_long_pool_gb300 import binding, build
+from block_sparse_long_pool_gb300 import workloads as wl
+from parity_utils import BLK, D, assert_attn_close, bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    build.build()
+    binding.load()
+
+
+def _to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp64 -> bf16 (round to nearest even, through torch) as uint16 bit patterns."""
+    return wl.bf16_bits(torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16))
+
+
+def _bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _case(B, H_q, H_kv, T_cap, lens_b, k_cap, N_cap, seed, gates_kind="random"):
+    P = B * H_kv
+    G = H_q // H_kv
+    rng = np.random.default_rng(seed)
+    K = wl.randn_bf16((B, H_kv, T_cap, D), seed + 1, "cuda")
+    V = wl.randn_bf16((B, H_kv, T_cap, D), seed + 2, "cuda")
+    Q = wl.randn_bf16((B, H_q, D), seed + 3, "cuda")
+    lens_p = np.repeat(np.asarray(lens_b, dtype=np.int64), H_kv)
+    idx_np = np.full((P, k_cap), -1, np.int32)
+    cnt_np = np.zeros(P, np.int32)
+    for p in range(P):
+        nb = (int(lens_p[p]) + BLK - 1) // BLK
+        c = min(nb, k_cap) if p % 3 else min(nb, max(0, k_cap - 3))
+        idx_np[p, :c] = np.sort(rng.permutation(nb)[:c])
+        cnt_np[p] = c
+    if gates_kind == "random":
+        gates = rng.uniform(0.0, 1.0, (B, H_q, 3))
+    else:
+        gates = np.zeros((B, H_q, 3))
+        gates[..., gates_kind] = 1.0
+    Kb = bits(K).reshape(P, T_cap, D)
+    Vb = bits(V).reshape(P, T_cap, D)
+    return dict(K=K, V=V, Q=Q, Kb=Kb, Vb=Vb, Qb=bits(Q).reshape(P, G, D), lens_p=lens_p, idx_np=idx_np,
+                cnt_np=cnt_np, gates_np=gates,
+                idx=torch.from_numpy(idx_np).cuda().view(B, H_kv, k_cap),
+                cnt=torch.from_numpy(cnt_np).cuda().view(B, H_kv),
+                gates=torch.from_numpy(gates.astype(np.float32)).cuda(),
+                seq=torch.tensor(lens_b, dtype=torch.int32, device="cuda"))
+
+
+def _rows_from_oracle(c, N_cap, B, H_kv):
+    """Compressed rows: the oracle's fp64 means, rounded to bf16 (both sides use these)."""
+    kh = _to_bf16_bits(oracle.pool(c["Kb"], c["lens_p"], N_cap))
+    vh = _to_bf16_bits(oracle.pool(c["Vb"], c["lens_p"], N_cap))
+    to_dev = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda().view(B, H_kv, N_cap, D)
+    return kh, vh, to_dev(kh), to_dev(vh)
+
+
+def _gpu_nsa(c, khat, vhat, window, B, H_q, n_split=0, ws=None, status=None):
+    H_kv = c["K"].shape[1]
+    O = torch.full((B, H_q, D), 7.0, dtype=torch.bfloat16, device="cuda")
+    if ws is None:
+        ws = binding.nsa_workspace(B, H_q, H_kv)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.sparse_decode_attn_nsa(c["Q"], c["K"], c["V"], khat, vhat, c["idx"], c["cnt"], c["seq"], window,
+                                   c["gates"], O, ws, n_split=n_split, status=status)
+    torch.cuda.synchronize()
+    return O, ws, status
+
+
+def _oracle_nsa(c, kh_bits, vh_bits, window):
+    return oracle.nsa(c["Qb"], c["Kb"], c["Vb"], _bits_to_f64(kh_bits), _bits_to_f64(vh_bits), c["idx_np"],
+                      c["cnt_np"], c["lens_p"], window, c["gates_np"].reshape(len(c["lens_p"]), -1, 3))
+
+
+@pytest.mark.parametrize("H_q,H_kv", [(16, 4), (64, 8), (32, 2)])
+@pytest.mark.parametrize("n_split", [0, 1, 2, 4, 8])
+def test_nsa_matches_oracle(H_q, H_kv, n_split):
+    B, T_cap, k_cap, N_cap = 2, 40 * BLK, 9, 40
+    lens_b = [40 * BLK, 27 * BLK + 13]
+    c = _case(B, H_q, H_kv, T_cap, lens_b, k_cap, N_cap, seed=11 + n_split + H_q)
+    kh, vh, khat, vhat = _rows_from_oracle(c, N_cap, B, H_kv)
+    O, ws, status = _gpu_nsa(c, khat, vhat, 200, B, H_q, n_split)
+    assert status.item() == 0
+    ref = _oracle_nsa(c, kh, vh, 200)
+    assert_attn_close(O, ref, "nsa")
+    # the arrival counters are back at zero
+    n_cnt = B * H_kv
+    assert int(ws[: 4 * n_cnt].view(torch.int32).abs().sum().item()) == 0
+
+
+@pytest.mark.parametrize("branch", [0, 1, 2])
+@pytest.mark.parametrize("window", [0, 1, 64, 100, 513])
+def test_nsa_each_branch(branch, window):
+    """Gates (1,0,0) / (0,1,0) / (0,0,1): the compressed, selected and window branch alone."""
+    B, H_q, H_kv, T_cap, k_cap, N_cap = 3, 16, 2, 30 * BLK, 7, 100
+    lens_b = [30 * BLK, 11 * BLK + 1, 5]
+    c = _case(B, H_q, H_kv, T_cap, lens_b, k_cap, N_cap, seed=40 + branch + window, gates_kind=branch)
+    kh, vh, khat, vhat = _rows_from_oracle(c, N_cap, B, H_kv)
+    O, _, status = _gpu_nsa(c, khat, vhat, window, B, H_q)
+    assert status.item() == 0
+    ref = _oracle_nsa(c, kh, vh, window)
+    assert_attn_close(O, ref, f"nsa branch {branch} w={window}")
+    if branch == 2 and window == 0:   # an empty window contributes zero
+        assert float(O.float().abs().max()) == 0.0
+
+
+def test_nsa_degenerate_lengths_and_counts():
+    """Empty sequences, single tokens, empty selections, a window longer than the
+    sequence, G = 16 (two n-tiles)."""
+    B, H_q, H_kv, T_cap, k_cap, N_cap = 4, 32, 2, 20 * BLK, 5, 20
+    lens_b = [0, 1, 65, 20 * BLK]
+    c = _case(B, H_q, H_kv, T_cap, lens_b, k_cap, N_cap, seed=77)
+    c["cnt_np"][2] = 0
+    c["cnt"] = torch.from_numpy(c["cnt_np"]).cuda().view(B, H_kv)
+    kh, vh, khat, vhat = _rows_from_oracle(c, N_cap, B, H_kv)
+    O, _, status = _gpu_nsa(c, khat, vhat, T_cap, B, H_q)
+    assert status.item() == 0
+    ref = _oracle_nsa(c, kh, vh, T_cap)
+    assert_attn_close(O, ref, "nsa degenerate")
+    assert float(O[0].float().abs().max()) == 0.0   # no token: every branch is empty
+
+
+def test_nsa_workspace_reuse_is_deterministic():
+    B, H_q, H_kv, T_cap, k_cap, N_cap = 2, 64, 8, 33 * BLK, 6, 33
+    c = _case(B, H_q, H_kv, T_cap, [33 * BLK, 17 * BLK + 30], k_cap, N_cap, seed=5)
+    _, _, khat, vhat = _rows_from_oracle(c, N_cap, B, H_kv)
+    O1, ws, _ = _gpu_nsa(c, khat, vhat, 256, B, H_q)
+    O2, _, _ = _gpu_nsa(c, khat, vhat, 256, B, H_q, ws=ws)
+    O3, _, _ = _gpu_nsa(c, khat, vhat, 256, B, H_q, ws=ws)
+    assert torch.equal(O1, O2) and torch.equal(O2, O3)
+
+
+def test_nsa_bad_block_ids_are_reported():
+    B, H_q, H_kv, T_cap, k_cap, N_cap = 1, 8, 1, 10 * BLK, 4, 10
+    c = _case(B, H_q, H_kv, T_cap, [10 * BLK], k_cap, N_cap, seed=9)
+    c["idx"][0, 0, 0] = 1 << 20   # far outside the cache: skipped, reported
+    _, _, khat, vhat = _rows_from_oracle(c, N_cap, B, H_kv)
+    O, _, status = _gpu_nsa(c, khat, vhat, 64, B, H_q)
+    assert status.item() == binding.SPARSE_ERR_BAD_INDEX
+    assert torch.isfinite(O.float()).all()
+
+
+def test_nsa_length_beyond_compressed_rows_is_reported():
+    """seq_len needs more compressed rows than N_cap holds: reported, rows clamped."""
+    B, H_q, H_kv, T_cap, k_cap, N_cap = 1, 8, 1, 12 * BLK, 4, 8
+    c = _case(B, H_q, H_kv, T_cap, [12 * BLK], k_cap, N_cap, seed=10)
+    _, _, khat, vhat = _rows_from_oracle(c, N_cap, B, H_kv)
+    O, _, status = _gpu_nsa(c, khat, vhat, 64, B, H_q)
+    assert status.item() == binding.SPARSE_ERR_BAD_INDEX
+    assert torch.isfinite(O.float()).all()
+
+
+@pytest.mark.parametrize("chunks", [[700], [64, 1, 63, 200, 5], [130, 1, 1, 1, 1]])
+def test_append_kv_pools_values_and_rounds_rows(chunks):
+    """sparse_pool_append_kv: caches bit-exact, ktil / vtil the oracle's means within
+    fp32 rounding, khat / vhat the bf16 rounding of ktil / vtil and within one bf16
+    rounding of the oracle's means."""
+    B, H_kv, T_cap, N_cap = 2, 3, 12 * BLK, 12
+    total = sum(chunks)
+    Kall = wl.randn_bf16((B, H_kv, total, D), 501, "cuda")
+    Vall = wl.randn_bf16((B, H_kv, total, D), 502, "cuda")
+    kc = torch.zeros((B, H_kv, T_cap, D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    ktil = torch.zeros((B, H_kv, N_cap, D), dtype=torch.float32, device="cuda")
+    vtil = torch.zeros_like(ktil)
+    khat = torch.zeros((B, H_kv, N_cap, D), dtype=torch.bfloat16, device="cuda")
+    vhat = torch.zeros_like(khat)
+    t = 0
+    for n in chunks:
+        binding.sparse_pool_append_kv(kc, vc, ktil, vtil, Kall[:, :, t:t + n].contiguous(),
+                                      Vall[:, :, t:t + n].contiguous(), t, khat=khat, vhat=vhat)
+        t += n
+    torch.cuda.synchronize()
+    P = B * H_kv
+    assert np.array_equal(bits(kc)[:, :, :total], bits(Kall))
+    assert np.array_equal(bits(vc)[:, :, :total], bits(Vall))
+    lens = np.full(P, total, np.int64)
+    nb = (total + BLK - 1) // BLK
+    for name, cache, til, hat in (("k", kc, ktil, khat), ("v", vc, vtil, vhat)):
+        ref = oracle.pool(bits(cache).reshape(P, T_cap, D), lens, N_cap)[:, :nb]
+        got = til.double().cpu().numpy().reshape(P, N_cap, D)[:, :nb]
+        assert np.all(np.abs(got - ref) <= 1e-5 * (1 + np.abs(ref))), f"{name}til"
+        hat_bits = bits(hat).reshape(P, N_cap, D)[:, :nb]
+        assert np.array_equal(hat_bits, bits(til.to(torch.bfloat16)).reshape(P, N_cap, D)[:, :nb]), f"{name}hat"
+        h = _bits_to_f64(hat_bits)
+        assert np.all(np.abs(h - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6), f"{name}hat vs oracle"
+
+
+def test_nsa_chain_append_then_decode():
+    """The whole chain on the GPU (append_kv builds the caches and the bf16 compressed
+    rows) against the oracle pooling in fp64."""
+    B, H_q, H_kv, T_cap, k_cap, N_cap = 2, 32, 4, 24 * BLK, 8, 24
+    lens_b = [24 * BLK - 5, 24 * BLK - 5]
+    total = lens_b[0]
+    K = wl.randn_bf16((B, H_kv, total, D), 601, "cuda")
+    V = wl.randn_bf16((B, H_kv, total, D), 602, "cuda")
+    kc = torch.zeros((B, H_kv, T_cap, D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    ktil = torch.zeros((B, H_kv, N_cap, D), dtype=torch.float32, device="cuda")
+    vtil = torch.zeros_like(ktil)
+    khat = torch.zeros((B, H_kv, N_cap, D), dtype=torch.bfloat16, device="cuda")
+    vhat = torch.zeros_like(khat)
+    binding.sparse_pool_append_kv(kc, vc, ktil, vtil, K[:, :, :total - 3].contiguous(),
+                                  V[:, :, :total - 3].contiguous(), 0, khat=khat, vhat=vhat)
+    for t in range(total - 3, total):
+        binding.sparse_pool_append_kv(kc, vc, ktil, vtil, K[:, :, t:t + 1].contiguous(), V[:, :, t:t + 1].contiguous(),
+                                      t, khat=khat, vhat=vhat)
+    c = _case(B, H_q, H_kv, T_cap, lens_b, k_cap, N_cap, seed=21)
+    c["K"], c["V"] = kc, vc
+    P = B * H_kv
+    c["Kb"], c["Vb"] = bits(kc).reshape(P, T_cap, D), bits(vc).reshape(P, T_cap, D)
+    O, _, status = _gpu_nsa(c, khat, vhat, 300, B, H_q)
+    assert status.item() == 0
+    kr = oracle.pool(c["Kb"], c["lens_p"], N_cap)
+    vr = oracle.pool(c["Vb"], c["lens_p"], N_cap)
+    ref = oracle.nsa(c["Qb"], c["Kb"], c["Vb"], kr, vr, c["idx_np"], c["cnt_np"], c["lens_p"], 300,
+                     c["gates_np"].reshape(P, -1, 3))
+    assert_attn_close(O, ref, "nsa chain")
+
+
+def test_nsa_full_size_sampled_pairs():
+    """The 128K decode shape (B=8, H_q=64, H_kv=8, 67 selected blocks, 512-token
+    window, 2048 compressed rows) in the launch configuration of the bench; a sample of
+    pairs checked against the oracle."""
+    shape = wl.DECODE_128K
+    B, H_q, H_kv, T = shape.B, shape.H_q, shape.H_kv, shape.T
+    k_cap, N_cap, window = shape.n_init + shape.n_local + shape.k, shape.N_b, 512
+    P = B * H_kv
+    K = wl.randn_bf16((B, H_kv, T, D), 901, "cuda")
+    V = wl.randn_bf16((B, H_kv, T, D), 902, "cuda")
+    Q = wl.randn_bf16((B, H_q, D), 903, "cuda")
+    kc, vc = torch.empty_like(K), torch.empty_like(V)
+    ktil = torch.zeros((B, H_kv, N_cap, D), dtype=torch.float32, device="cuda")
+    vtil = torch.zeros_like(ktil)
+    khat = torch.zeros((B, H_kv, N_cap, D), dtype=torch.bfloat16, device="cuda")
+    vhat = torch.zeros_like(khat)
+    binding.sparse_pool_append_kv(kc, vc, ktil, vtil, K, V, 0, khat=khat, vhat=vhat)
+    del K, V
+    rng = np.random.default_rng(904)
+    idx_np = np.stack([np.sort(rng.permutation(N_cap)[:k_cap]) for _ in range(P)]).astype(np.int32)
+    cnt_np = np.full(P, k_cap, np.int32)
+    gates_np = rng.uniform(0.0, 1.0, (B, H_q, 3))
+    c = dict(Q=Q, K=kc, V=vc, idx=torch.from_numpy(idx_np).cuda().view(B, H_kv, k_cap),
+             cnt=torch.from_numpy(cnt_np).cuda().view(B, H_kv),
+             gates=torch.from_numpy(gates_np.astype(np.float32)).cuda(),
+             seq=torch.full((B,), T, dtype=torch.int32, device="cuda"))
+    O, _, status = _gpu_nsa(c, khat, vhat, window, B, H_q)
+    assert status.item() == 0
+    G = H_q // H_kv
+    Qb = bits(Q).reshape(P, G, D)
+    for p in (0, 9, 37, P - 1):
+        b, g = divmod(p, H_kv)
+        Kb = bits(kc[b, g]).reshape(1, T, D)
+        Vb = bits(vc[b, g]).reshape(1, T, D)
+        lens = np.array([T], np.int64)
+        ref = oracle.nsa(Qb[p:p + 1], Kb, Vb, oracle.pool(Kb, lens, N_cap), oracle.pool(Vb, lens, N_cap),
+                         idx_np[p:p + 1], cnt_np[p:p + 1], lens, window,
+                         gates_np[b, g * G:(g + 1) * G].reshape(1, G, 3))
+        assert_attn_close(O[b, g * G:(g + 1) * G], ref, f"nsa 128k pair {p}")
