@@ -1036,8 +1036,12 @@ def run_nsa_case(args, dev):
         binding.sparse_select_topk_heads(Q, ktil, seq, sh.n_init, sh.n_local, sh.k, idx, cnt, status=status)
 
     def attend():
+        binding.sparse_decode_attn_nsa(Q, kc, vc, khat, vhat, idx, cnt, seq, w, gates, O, None,
+                                       n_split=args.n_split, status=status)
+
+    def attend_grid():
         binding.sparse_decode_attn_nsa(Q, kc, vc, khat, vhat, idx, cnt, seq, w, gates, O, ws, n_split=args.n_split,
-                                       status=status)
+                                       flags=binding.SPARSE_NSA_BRANCH_GRID, status=status)
 
     def layer():
         select()
@@ -1046,6 +1050,7 @@ def run_nsa_case(args, dev):
     select()
     torch.cuda.synchronize()
     t_attn = _event_times(attend, args.steps, args.warmup, evict)
+    t_grid = _event_times(attend_grid, args.steps, args.warmup, evict)
     t_sel = _event_times(select, args.steps, args.warmup, evict)
     t_layer = _event_times(layer, args.steps, args.warmup, evict)
     torch.cuda.synchronize()
@@ -1056,13 +1061,17 @@ def run_nsa_case(args, dev):
               "compressed_rows": pairs * N * 2 * D * 2, "q_o_gates": B * H_q * (2 * D * 2 + 12)}
     attn_bytes = sum(nbytes.values())
     gbs, frac = _rate(attn_bytes, t_attn["median_us"], peak)
+    ggbs, gfrac = _rate(attn_bytes, t_grid["median_us"], peak)
     sel_bytes = pairs * N * KTIL_ROW_BYTES
     sgbs, sfrac = _rate(sel_bytes, t_sel["median_us"], peak)
     lgbs, lfrac = _rate(attn_bytes + sel_bytes, t_layer["median_us"], peak)
     line = {"case": "nsa128k", "workload": f"nsa_decode_128k_b{B}_hq{H_q}_hkv{H_kv}_w{w}",
             "unit_of_work": "one NSA decode layer (multi-head routing + gated three-branch attention)",
-            "attention": {"launches": 1, **t_attn, "algorithmic_bytes": nbytes, "achieved_gbs": gbs,
+            "attention": {"form": "fused (one cluster per pair, three branch states, one DSMEM merge)",
+                          "launches": 1, **t_attn, "algorithmic_bytes": nbytes, "achieved_gbs": gbs,
                           "frac_of_measured_hbm": frac},
+            "attention_branch_grid": {"form": "a cluster per branch and pair, gates from the workspace",
+                                      "launches": 1, **t_grid, "achieved_gbs": ggbs, "frac_of_measured_hbm": gfrac},
             "routing": {"call": "sparse_select_topk_heads", **t_sel, "algorithmic_bytes": sel_bytes,
                         "achieved_gbs": sgbs, "frac_of_measured_hbm": sfrac},
             "layer": {**t_layer, "achieved_gbs": lgbs, "frac_of_measured_hbm": lfrac,

@@ -31,6 +31,7 @@ SPARSE_ERR_NOT_READY = -5
 SPARSE_ERR_BAD_INDEX = -6
 SPARSE_ATTN_BLOCKS_READY = 1
 SPARSE_ATTN_STREAM_K = 2
+SPARSE_NSA_BRANCH_GRID = 4
 
 # (name, restype, argtypes) of every entry point declared in include/sparse_pool.h
 _P, _I, _LL, _F, _U = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float, ctypes.c_uint

@@ -1423,6 +1423,303 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
+// The fused form (G <= 8): one cluster of S CTAs per pair runs all three branches.
+// CTA r takes slice r of each branch's list (the selected table, the compressed-row
+// tiles, the window's blocks); its producer streams the three slices back to back
+// through one TMA ring and its consumer warps keep three online-softmax states in
+// registers, one per branch.  One DSMEM merge then gives every CTA the three
+// normalised branch outputs for its output dims, and the gated sum is formed right
+// there: no intermediate reaches HBM and there is no second pass.
+
+// Slice `rank` of a range branch (x = 1 window, 2 compressed): its first block (tile)
+// and length.
+__device__ __forceinline__ void nsa_range_slice(const AttnParams &p, int b, int rank, int S, int *first_out,
+                                                int *n_out)
+{
+    const long long rows = unit_len(p, b);
+    const int nb = rows <= 0 ? 0 : static_cast<int>((rows + kBlk - 1) / kBlk);
+    long long w0 = p.range_mode == 1 ? rows - p.win_tokens : 0;
+    w0 = w0 < 0 ? 0 : w0;
+    const int first = static_cast<int>(w0 / kBlk);
+    int c = nb > first ? nb - first : 0;
+    if (p.range_mode == 1 && p.win_tokens <= 0)
+        c = 0;
+    const int per = (c + S - 1) / S;
+    const int i0 = min(c, rank * per);
+    *first_out = first + i0;
+    *n_out = min(c, i0 + per) - i0;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    nsa_fused_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                     const __grid_constant__ CUtensorMap khmap, const __grid_constant__ CUtensorMap vhmap,
+                     const __grid_constant__ NsaParams np)
+{
+    constexpr int NT = 1, ROWS = 8;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t *base = smem_raw + (base_s - raw_s);
+    int *ctrl = reinterpret_cast<int *>(base + kOffCtrl);
+    const uint32_t bar_full = base_s + kOffBars;
+    const uint32_t bar_empty = base_s + kOffBars + 8 * kStages;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int S = static_cast<int>(gridDim.x);
+    const int rank = static_cast<int>(blockIdx.x);
+    const int pair = static_cast<int>(blockIdx.y);
+    const AttnParams &ps = np.br[0];
+    const AttnParams &pw = np.br[1];
+    const AttnParams &pc = np.br[2];
+    const int b = pair / ps.H_kv, g = pair % ps.H_kv;
+    const bool early = (ps.flags & SPARSE_ATTN_BLOCKS_READY) != 0u;
+    if (!early)
+        griddep_wait();
+    if (tid == 0) {
+        ctrl[kCtrlAbort] = 0;
+        ctrl[kCtrlList] = 0;
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, kConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    int *lslot = reinterpret_cast<int *>(base + kOffList);
+    int *llog = lslot + kMaxListCta;
+    // the range branches' slices follow from the length alone
+    int w_first, n_w, c_first, n_c;
+    nsa_range_slice(pw, b, rank, S, &w_first, &n_w);
+    nsa_range_slice(pc, b, rank, S, &c_first, &n_c);
+
+    WarpState<NT> st_s, st_w, st_c;
+    st_s.reset();
+    st_w.reset();
+    st_c.reset();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        // Ring order: the compressed tiles, the window's blocks, then the selected
+        // blocks.  The range tiles need no table, so the first ring stages are issued
+        // before the selected slice is fetched and that round trip is hidden.
+        const int n_r = n_c + n_w;
+        const uint64_t pol = policy_evict_first();
+        bool ok = true;
+        auto issue = [&](int it) {
+            const int s = it % kStages;
+            const int use = it / kStages;
+            if (use > 0 && !mbar_wait(bar_empty + 8 * s, (use - 1) & 1, kWaitNs)) {
+                report(ps.status, SPARSE_ERR_TIMEOUT);
+                ok = false;
+                return;
+            }
+            const CUtensorMap *km = &kmap, *vm = &vmap;
+            int row;
+            if (it < n_c) {
+                km = &khmap;
+                vm = &vhmap;
+                row = (c_first + it) * kBlk;
+            } else if (it < n_r) {
+                row = (w_first + it - n_c) * kBlk;
+            } else {
+                const int slot = lslot[it - n_r];
+                row = slot >= 0 ? slot * kBlk : static_cast<int>(min(ps.pair_stride, (long long)INT_MAX - kBlk));
+            }
+            const uint32_t dst = base_s + s * kStageBytes;
+            mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
+            tma_load_3d(dst, km, bar_full + 8 * s, 0, row, pair, pol);
+            tma_load_3d(dst + kHalfBytes, km, bar_full + 8 * s, 64, row, pair, pol);
+            tma_load_3d(dst + kTileBytes, vm, bar_full + 8 * s, 0, row, pair, pol);
+            tma_load_3d(dst + kTileBytes + kHalfBytes, vm, bar_full + 8 * s, 64, row, pair, pol);
+        };
+        const int pre = min(n_r, kStages);
+        if (lane == 0) {
+            prefetch_tensormap(&kmap);
+            prefetch_tensormap(&vmap);
+            prefetch_tensormap(&khmap);
+            prefetch_tensormap(&vhmap);
+            for (int it = 0; it < pre; ++it)
+                issue(it);
+        }
+        __syncwarp();
+        const int per = (ps.k_tot + S - 1) / S;
+        const int i0 = min(ps.k_tot, rank * per);
+        const int n_s = producer_fetch_slice(ps, pair, i0, min(ps.k_tot, i0 + per) - i0, lslot, llog, ctrl, lane);
+        named_barrier_arrive(1, kThreads);   // the selected slice and its length are in shared memory
+        if (lane == 0) {
+            if (pc.seq_len[b] > pc.pair_stride * kBlk)
+                report(pc.status, SPARSE_ERR_BAD_INDEX);
+            for (int it = pre; it < n_r + n_s && ok; ++it)
+                issue(it);
+        }
+    } else {
+        // ------------------------------------------------------------ consumers
+        if (early)
+            griddep_wait();
+        QueryFrags<NT> q;
+        load_query<NT, false>(q, ps, b, g, 0, ps.G, lane);
+        const long long len = ps.seq_len[b];
+        const long long rows_c = unit_len(pc, b);
+        const long long tok_lo = len - pw.win_tokens > 0 ? len - pw.win_tokens : 0;
+        int it = 0;
+        bool ok = true;
+        // wait for ring item `it`, run `body` on its stage, release it
+        auto step = [&](auto body) {
+            const int s = it % kStages;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_full + 8 * s, (it / kStages) & 1, kWaitNs));
+            if (!ok) {
+                if (lane == 0)
+                    report(ps.status, SPARSE_ERR_TIMEOUT);
+                return;
+            }
+            body(base_s + s * kStageBytes);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar_empty + 8 * s);
+            ++it;
+        };
+        for (int i = 0; i < n_c && ok; ++i)
+            step([&](uint32_t stage) {
+                const long long r0 = static_cast<long long>(c_first + i) * kBlk + warp * 16;
+                if (r0 < rows_c)
+                    attend_block<NT, false>(st_c, q, stage, r0, rows_c, 0xffffffffu, ps.scale_log2, warp, lane);
+            });
+        for (int i = 0; i < n_w && ok; ++i)
+            step([&](uint32_t stage) {
+                const long long tok0 = static_cast<long long>(w_first + i) * kBlk + warp * 16;
+                if (tok0 < len)
+                    attend_block<NT, false>(st_w, q, stage, tok0, len, 0xffffffffu, ps.scale_log2, warp, lane,
+                                            tok_lo);
+            });
+        named_barrier_sync(1, kThreads);
+        const int n_s = ctrl[kCtrlList];
+        for (int i = 0; i < n_s && ok; ++i)
+            step([&](uint32_t stage) {
+                const int logical = llog[i];
+                const long long tok0 = static_cast<long long>(logical) * kBlk + warp * 16;
+                if (logical >= 0 && tok0 < len)
+                    attend_block<NT, false>(st_s, q, stage, tok0, len, 0xffffffffu, ps.scale_log2, warp, lane);
+            });
+        finish_row_sums<NT>(st_s);
+        finish_row_sums<NT>(st_c);
+        finish_row_sums<NT>(st_w);
+    }
+
+    // ---------------------------------------------------------------- merge + gates
+    __syncthreads();
+    griddep_launch_dependents();
+    // The three branches' warp states side by side (branch x = s, c, w), merged into
+    // three CTA states in one pass.
+    constexpr int WO = kConsumerWarps * ROWS * kD, WR = kConsumerWarps * ROWS;
+    float *wo = reinterpret_cast<float *>(base);           // [3][4][ROWS][128]
+    float *wm = wo + 3 * WO;                               // [3][4][ROWS]
+    float *wl = wm + 3 * WR;
+    float *wf = wl + 3 * WR;
+    float *co = wf + 3 * WR;                               // [3][ROWS][128]
+    float *cm = co + 3 * ROWS * kD;                        // [3][ROWS]
+    float *cl = cm + 3 * ROWS;                             // [3][ROWS]
+    if (warp < kConsumerWarps) {
+        store_warp_state<NT>(st_s, wo, wm, wl, warp, lane);
+        store_warp_state<NT>(st_c, wo + WO, wm + WR, wl + WR, warp, lane);
+        store_warp_state<NT>(st_w, wo + 2 * WO, wm + 2 * WR, wl + 2 * WR, warp, lane);
+    }
+    __syncthreads();
+    if (tid < 3 * ROWS) {
+        const int x = tid / ROWS, row = tid - x * ROWS;
+        const float *m4 = wm + x * WR, *l4 = wl + x * WR;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w4 = 0; w4 < kConsumerWarps; ++w4)
+            M = fmaxf(M, m4[w4 * ROWS + row]);
+        float L = 0.f;
+#pragma unroll
+        for (int w4 = 0; w4 < kConsumerWarps; ++w4) {
+            const float mw = m4[w4 * ROWS + row];
+            const float f = (M == -INFINITY || mw == -INFINITY) ? 0.f : exp2f(mw - M);
+            wf[x * WR + w4 * ROWS + row] = f;
+            L = fmaf(f, l4[w4 * ROWS + row], L);
+        }
+        cm[x * ROWS + row] = M;
+        cl[x * ROWS + row] = L;
+    }
+    __syncthreads();
+    for (int item = tid; item < 3 * ROWS * kD; item += kThreads) {
+        const int x = item / (ROWS * kD);
+        const int r = item - x * ROWS * kD;
+        const int row = r / kD;
+        float o = 0.f;
+#pragma unroll
+        for (int w4 = 0; w4 < kConsumerWarps; ++w4)
+            o = fmaf(wf[x * WR + w4 * ROWS + row], wo[x * WO + w4 * ROWS * kD + r], o);
+        co[item] = o;
+    }
+    cluster_sync();
+
+    const float *pco[kMaxSplit];
+    const float *pcm[kMaxSplit];
+    const float *pcl[kMaxSplit];
+#pragma unroll
+    for (int c = 0; c < kMaxSplit; ++c) {
+        const unsigned r = c < S ? static_cast<unsigned>(c) : 0u;
+        pco[c] = static_cast<const float *>(__cluster_map_shared_rank(co, r));
+        pcm[c] = static_cast<const float *>(__cluster_map_shared_rank(cm, r));
+        pcl[c] = static_cast<const float *>(__cluster_map_shared_rank(cl, r));
+    }
+    // CTA `rank` writes dims [rank * 128 / S, (rank + 1) * 128 / S) of every head
+    const int dims_per = kD / S;
+    const int d0 = rank * dims_per;
+    const int pairs_per_row = dims_per / 2;
+    const int n_items = ps.G * pairs_per_row;
+    for (int item = tid; item < n_items; item += kThreads) {
+        const int row = item / pairs_per_row;
+        const int d = d0 + 2 * (item - row * pairs_per_row);
+        const size_t head = static_cast<size_t>(b) * ps.H_q + g * ps.G + row;
+        float ox = 0.f, oy = 0.f;
+#pragma unroll
+        for (int x = 0; x < 3; ++x) {   // s, c, w
+            float mc[kMaxSplit], lc[kMaxSplit];
+            float2 v[kMaxSplit];
+#pragma unroll
+            for (int c = 0; c < kMaxSplit; ++c) {
+                if (c < S) {
+                    mc[c] = pcm[c][x * ROWS + row];
+                    lc[c] = pcl[c][x * ROWS + row];
+                    v[c] = *reinterpret_cast<const float2 *>(pco[c] + (x * ROWS + row) * kD + d);
+                } else {
+                    mc[c] = -INFINITY;
+                    lc[c] = 0.f;
+                    v[c] = make_float2(0.f, 0.f);
+                }
+            }
+            float M = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kMaxSplit; ++c)
+                M = fmaxf(M, mc[c]);
+            float L = 0.f, bx = 0.f, by = 0.f;
+#pragma unroll
+            for (int c = 0; c < kMaxSplit; ++c) {
+                const float f = (M == -INFINITY || mc[c] == -INFINITY) ? 0.f : exp2f(mc[c] - M);
+                L = fmaf(lc[c], f, L);
+                bx = fmaf(f, v[c].x, bx);
+                by = fmaf(f, v[c].y, by);
+            }
+            // gates [head][3] = (g_c, g_s, g_w); branch x = s, c, w
+            const float gate = np.gates[head * 3 + (x == 0 ? 1 : x == 1 ? 0 : 2)];
+            const float scl = L > 0.f ? gate / L : 0.f;
+            ox = fmaf(scl, bx, ox);
+            oy = fmaf(scl, by, oy);
+        }
+        *reinterpret_cast<uint32_t *>(np.O + head * kD + d) = pack_bf16x2(ox, oy);
+    }
+    // peers may still read this CTA's states
+    cluster_sync();
+}
+
+// The three-branch merge scratch must fit in the ring it reuses.
+static_assert((3 * kConsumerWarps * 8 * kD + 9 * kConsumerWarps * 8 + 3 * 8 * kD + 6 * 8) * 4 <= kStages * kStageBytes,
+              "NSA merge scratch exceeds the stage ring");
+
 size_t nsa_counter_bytes(long long pairs)
 {
     return (static_cast<size_t>(pairs) * sizeof(unsigned) + 255) & ~static_cast<size_t>(255);
@@ -1464,6 +1761,35 @@ int launch_nsa(const NsaParams &np, const CUtensorMap *maps, int S, long long pa
                                 "sparse_decode_attn_nsa launch");
 }
 
+int launch_nsa_fused(const NsaParams &np, const CUtensorMap *maps, int S, long long pairs, int device,
+                     cudaStream_t stream)
+{
+    const int smem = kSmemDecode + 1024;
+    static int configured[64];
+    int rc = sp_host::configure_kernel(reinterpret_cast<const void *>(nsa_fused_kernel), smem, device, configured);
+    if (rc != SPARSE_OK)
+        return rc;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(S), static_cast<unsigned>(pairs), 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    CUtensorMap m0 = maps[0], m1 = maps[1], m2 = maps[2], m3 = maps[3];
+    NsaParams prm = np;
+    void *args[] = {&m0, &m1, &m2, &m3, &prm};
+    return sp_host::cuda_status(cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(nsa_fused_kernel), args),
+                                "sparse_decode_attn_nsa launch");
+}
+
 }  // namespace
 
 extern "C" SPARSE_API size_t sparse_decode_attn_nsa_workspace_size(int B, int H_q, int H_kv)
@@ -1484,11 +1810,10 @@ extern "C" SPARSE_API int sparse_decode_attn_nsa(const uint16_t *Q, const uint16
     using sp_host::aligned16;
     using sp_host::fail;
     const char *name = "sparse_decode_attn_nsa";
-    if (!Q || !k_cache || !v_cache || !khat || !vhat || !blk_idx || !count || !seq_len || !gates || !O ||
-        !workspace)
+    if (!Q || !k_cache || !v_cache || !khat || !vhat || !blk_idx || !count || !seq_len || !gates || !O)
         return fail(SPARSE_ERR_INVALID_ARG, "%s: null pointer", name);
     if (!aligned16(Q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(khat) || !aligned16(vhat) ||
-        !aligned16(O) || !aligned16(workspace))
+        !aligned16(O) || (workspace != nullptr && !aligned16(workspace)))
         return fail(SPARSE_ERR_INVALID_ARG, "%s: Q, the caches, O and the workspace must be 16-byte aligned", name);
     if (B < 1 || H_kv < 1 || H_q < H_kv || H_q % H_kv != 0 || k_tot < 1 || T_cap < 1 || N_cap < 1 ||
         window_tokens < 0)
@@ -1498,7 +1823,7 @@ extern "C" SPARSE_API int sparse_decode_attn_nsa(const uint16_t *Q, const uint16
         return fail(SPARSE_ERR_UNSUPPORTED, "%s: T_cap or window_tokens too large", name);
     if (!isfinite(scale))
         return fail(SPARSE_ERR_INVALID_ARG, "%s: scale must be finite", name);
-    if ((flags & ~SPARSE_ATTN_BLOCKS_READY) != 0u)
+    if ((flags & ~(SPARSE_ATTN_BLOCKS_READY | SPARSE_NSA_BRANCH_GRID)) != 0u)
         return fail(SPARSE_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags);
     const int G = H_q / H_kv;
     if (G > 16)
@@ -1506,9 +1831,14 @@ extern "C" SPARSE_API int sparse_decode_attn_nsa(const uint16_t *Q, const uint16
     const long long pairs = static_cast<long long>(B) * H_kv;
     if (pairs > 65535)
         return fail(SPARSE_ERR_UNSUPPORTED, "%s: B*H_kv=%lld > 65535", name, pairs);
+    // the fused form holds the three branch states of G <= 8 heads in registers; the
+    // branch grid (three clusters per pair, gates applied from the workspace) serves
+    // the rest, or runs when asked
+    const bool fused = G <= 8 && (flags & SPARSE_NSA_BRANCH_GRID) == 0u;
     const size_t need = nsa_workspace_bytes(pairs, B * H_q);
-    if (workspace_bytes < need)
-        return fail(SPARSE_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", name, workspace_bytes, need);
+    if (!fused && (workspace == nullptr || workspace_bytes < need))
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", name,
+                    workspace == nullptr ? static_cast<size_t>(0) : workspace_bytes, need);
     sp_host::DeviceInfo dev;
     int rc = sp_host::device_info(&dev);
     if (rc != SPARSE_OK)
@@ -1518,14 +1848,16 @@ extern "C" SPARSE_API int sparse_decode_attn_nsa(const uint16_t *Q, const uint16
     // block lists: the table, the window's blocks, the compressed rows' 64-row tiles
     const int k_win = static_cast<int>((window_tokens + kBlk - 1) / kBlk) + 1;
     const int k_cmp = (N_cap + kBlk - 1) / kBlk;
-    const int k_max = std::max(k_tot, std::max(k_win, k_cmp));
+    const int k_max = fused ? k_tot + k_win + k_cmp : std::max(k_tot, std::max(k_win, k_cmp));
     int S;
     if ((rc = choose_split(n_split, pairs, k_max, dev.sm_count, &S)) != SPARSE_OK)
         return rc;
-    while ((k_max + S - 1) / S > kMaxListCta && S < kMaxSplit && n_split == 0)
+    // only the selected slice is staged in shared memory (the ranges are arithmetic)
+    const int k_staged = fused ? k_tot : k_max;
+    while ((k_staged + S - 1) / S > kMaxListCta && S < kMaxSplit && n_split == 0)
         S *= 2;
-    if ((k_max + S - 1) / S > kMaxListCta)
-        return fail(SPARSE_ERR_UNSUPPORTED, "%s: %d blocks per CTA exceed %d", name, (k_max + S - 1) / S,
+    if ((k_staged + S - 1) / S > kMaxListCta)
+        return fail(SPARSE_ERR_UNSUPPORTED, "%s: %d blocks per CTA exceed %d", name, (k_staged + S - 1) / S,
                     kMaxListCta);
     CUtensorMap maps[4];
     if ((rc = sp_host::make_kv_tensor_map(&maps[0], k_cache, T_cap, pairs)) != SPARSE_OK ||
@@ -1533,7 +1865,8 @@ extern "C" SPARSE_API int sparse_decode_attn_nsa(const uint16_t *Q, const uint16
         (rc = sp_host::make_kv_tensor_map(&maps[2], khat, N_cap, pairs)) != SPARSE_OK ||
         (rc = sp_host::make_kv_tensor_map(&maps[3], vhat, N_cap, pairs)) != SPARSE_OK)
         return rc;
-    float *part = reinterpret_cast<float *>(static_cast<char *>(workspace) + nsa_counter_bytes(pairs));
+    float *part = fused ? nullptr
+                        : reinterpret_cast<float *>(static_cast<char *>(workspace) + nsa_counter_bytes(pairs));
     const size_t branch_floats = static_cast<size_t>(B) * H_q * kD;
     NsaParams np = {};
     for (int x = 0; x < 3; ++x) {
@@ -1545,9 +1878,9 @@ extern "C" SPARSE_API int sparse_decode_attn_nsa(const uint16_t *Q, const uint16
         p.H_kv = H_kv;
         p.G = G;
         p.n_groups = 1;
-        p.flags = flags;
+        p.flags = flags & SPARSE_ATTN_BLOCKS_READY;
         p.scale_log2 = scale_log2_of(scale);
-        p.O32 = part + x * branch_floats;
+        p.O32 = fused ? nullptr : part + x * branch_floats;
     }
     np.br[0].blk_logical = blk_idx;
     np.br[0].count = count;
@@ -1562,10 +1895,12 @@ extern "C" SPARSE_API int sparse_decode_attn_nsa(const uint16_t *Q, const uint16
     np.br[2].pair_stride = N_cap;
     np.gates = gates;
     np.part = part;
-    np.arrivals = static_cast<unsigned *>(workspace);
+    np.arrivals = fused ? nullptr : static_cast<unsigned *>(workspace);
     np.O = O;
     np.target = 3u * static_cast<unsigned>(S);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (fused)
+        return launch_nsa_fused(np, maps, S, pairs, dev.device, st);
     return G <= 8 ? launch_nsa<1>(np, maps, S, pairs, dev.device, st)
                   : launch_nsa<2>(np, maps, S, pairs, dev.device, st);
 }

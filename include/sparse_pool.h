@@ -369,14 +369,22 @@ SPARSE_API int sparse_verify_attn_shared(const uint16_t *Q, const uint16_t *k_ca
  *   window_tokens     w, 0 <= w <= T_cap.
  *   gates             [B][H_q][3] fp32 = (g_c, g_s, g_w) per query head.
  *   O                 [B][H_q][128] bf16, written.
- *   workspace         device memory of sparse_decode_attn_nsa_workspace_size() bytes:
- *                     per-pair arrival counters, then the three branch outputs (fp32).
- *                     It must be all zero before the first call; every call returns
- *                     the counters to zero.  Calls that share it must not overlap.
- *   n_split           CTAs per branch and pair (1, 2, 4 or 8; 0 = from the SM count).
- *   flags             0 or SPARSE_ATTN_BLOCKS_READY (as for sparse_decode_attn).
- * One launch runs the three branches (the notes run three kernels); the last CTA of a
- * pair to finish applies the gates.  G = H_q / H_kv <= 16.
+ *   workspace         needed by the branch grid only (NULL is fine otherwise): device
+ *                     memory of sparse_decode_attn_nsa_workspace_size() bytes, per-pair
+ *                     arrival counters, then the three branch outputs (fp32).  It must
+ *                     be all zero before the first call; every call returns the
+ *                     counters to zero.  Calls that share it must not overlap.
+ *   n_split           CTAs per pair (per branch in the branch grid): 1, 2, 4 or 8;
+ *                     0 = chosen from the SM count.
+ *   flags             SPARSE_ATTN_BLOCKS_READY (as for sparse_decode_attn) and / or
+ *                     SPARSE_NSA_BRANCH_GRID, or 0.
+ * One launch runs the three branches (the notes run three kernels).  For G <= 8 the
+ * launch is fully fused: one cluster of CTAs per pair streams the slices of all three
+ * branches, keeps one softmax state per branch and forms the gated sum after one
+ * merge through distributed shared memory; no intermediate reaches HBM.  For G > 8,
+ * or with SPARSE_NSA_BRANCH_GRID, each branch is its own cluster (grid z = branch),
+ * the branch outputs go to the workspace and the last CTA of the pair applies the
+ * gates.  G = H_q / H_kv <= 16.
  */
 SPARSE_API int sparse_decode_attn_nsa(const uint16_t *Q, const uint16_t *k_cache,
                                       const uint16_t *v_cache, long long T_cap,
@@ -386,6 +394,9 @@ SPARSE_API int sparse_decode_attn_nsa(const uint16_t *Q, const uint16_t *k_cache
                                       long long window_tokens, const float *gates, float scale,
                                       uint16_t *O, void *workspace, size_t workspace_bytes,
                                       int n_split, unsigned flags, int *status, void *stream);
+
+/* sparse_decode_attn_nsa: run the branch grid (see `flags`) even when G <= 8. */
+#define SPARSE_NSA_BRANCH_GRID 4u
 
 /* Bytes of the sparse_decode_attn_nsa workspace for these sizes; 0 if they are invalid. */
 SPARSE_API size_t sparse_decode_attn_nsa_workspace_size(int B, int H_q, int H_kv);

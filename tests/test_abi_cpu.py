@@ -198,14 +198,15 @@ def test_nsa_rejects_bad_arguments(lib):
         return f(*a)
 
     assert call(a4=None) == binding.SPARSE_ERR_INVALID_ARG            # no khat
-    assert call(a18=None) == binding.SPARSE_ERR_INVALID_ARG           # no workspace
+    assert call(a18=None, a21=binding.SPARSE_NSA_BRANCH_GRID) == binding.SPARSE_ERR_INVALID_ARG  # no workspace
+    assert call(a18=None, a12=16) == binding.SPARSE_ERR_INVALID_ARG   # G = 16 needs the workspace
     assert call(a5=ODD) == binding.SPARSE_ERR_INVALID_ARG             # misaligned vhat
     assert call(a12=12, a13=8) == binding.SPARSE_ERR_INVALID_ARG      # H_q not a multiple of H_kv
     assert call(a14=-1) == binding.SPARSE_ERR_INVALID_ARG             # negative window
     assert call(a14=5000) == binding.SPARSE_ERR_UNSUPPORTED           # window beyond T_cap
     assert call(a12=32, a13=1) == binding.SPARSE_ERR_UNSUPPORTED      # G = 32
-    assert call(a19=16) == binding.SPARSE_ERR_INVALID_ARG             # workspace too small
-    assert call(a21=4) == binding.SPARSE_ERR_INVALID_ARG              # unknown flag
+    assert call(a19=16, a12=16) == binding.SPARSE_ERR_INVALID_ARG     # workspace too small
+    assert call(a21=8) == binding.SPARSE_ERR_INVALID_ARG              # unknown flag
     assert call(a16=float("nan")) == binding.SPARSE_ERR_INVALID_ARG   # scale
     assert lib.sparse_decode_attn_nsa_workspace_size(0, 8, 1) == 0
     assert lib.sparse_decode_attn_nsa_workspace_size(8, 64, 8) == 256 + 3 * 8 * 64 * 128 * 4

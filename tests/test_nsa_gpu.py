@@ -77,15 +77,17 @@ def _rows_from_oracle(c, N_cap, B, H_kv):
     return kh, vh, to_dev(kh), to_dev(vh)
 
 
-def _gpu_nsa(c, khat, vhat, window, B, H_q, n_split=0, ws=None, status=None):
+def _gpu_nsa(c, khat, vhat, window, B, H_q, n_split=0, ws=None, status=None, flags=0):
+    """The fused form for G <= 8 (no workspace), the branch grid for G > 8 or when asked."""
     H_kv = c["K"].shape[1]
     O = torch.full((B, H_q, D), 7.0, dtype=torch.bfloat16, device="cuda")
-    if ws is None:
+    grid = H_q // H_kv > 8 or flags & binding.SPARSE_NSA_BRANCH_GRID
+    if ws is None and grid:
         ws = binding.nsa_workspace(B, H_q, H_kv)
     if status is None:
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
     binding.sparse_decode_attn_nsa(c["Q"], c["K"], c["V"], khat, vhat, c["idx"], c["cnt"], c["seq"], window,
-                                   c["gates"], O, ws, n_split=n_split, status=status)
+                                   c["gates"], O, ws, n_split=n_split, flags=flags, status=status)
     torch.cuda.synchronize()
     return O, ws, status
 
@@ -95,20 +97,34 @@ def _oracle_nsa(c, kh_bits, vh_bits, window):
                       c["cnt_np"], c["lens_p"], window, c["gates_np"].reshape(len(c["lens_p"]), -1, 3))
 
 
-@pytest.mark.parametrize("H_q,H_kv", [(16, 4), (64, 8), (32, 2)])
+@pytest.mark.parametrize("flags", [0, binding.SPARSE_NSA_BRANCH_GRID])
+@pytest.mark.parametrize("H_q,H_kv", [(16, 4), (64, 8), (32, 2), (6, 6)])
 @pytest.mark.parametrize("n_split", [0, 1, 2, 4, 8])
-def test_nsa_matches_oracle(H_q, H_kv, n_split):
+def test_nsa_matches_oracle(H_q, H_kv, n_split, flags):
     B, T_cap, k_cap, N_cap = 2, 40 * BLK, 9, 40
     lens_b = [40 * BLK, 27 * BLK + 13]
     c = _case(B, H_q, H_kv, T_cap, lens_b, k_cap, N_cap, seed=11 + n_split + H_q)
     kh, vh, khat, vhat = _rows_from_oracle(c, N_cap, B, H_kv)
-    O, ws, status = _gpu_nsa(c, khat, vhat, 200, B, H_q, n_split)
+    O, ws, status = _gpu_nsa(c, khat, vhat, 200, B, H_q, n_split, flags=flags)
     assert status.item() == 0
     ref = _oracle_nsa(c, kh, vh, 200)
     assert_attn_close(O, ref, "nsa")
-    # the arrival counters are back at zero
-    n_cnt = B * H_kv
-    assert int(ws[: 4 * n_cnt].view(torch.int32).abs().sum().item()) == 0
+    if ws is not None:   # the arrival counters are back at zero
+        n_cnt = B * H_kv
+        assert int(ws[: 4 * n_cnt].view(torch.int32).abs().sum().item()) == 0
+
+
+@pytest.mark.parametrize("n_split", [1, 2, 4, 8])
+def test_nsa_fused_and_branch_grid_agree(n_split):
+    """The two forms merge the same per-CTA partial states in different places
+    (DSMEM vs the workspace): equal up to fp32 rounding of the gated sum."""
+    B, H_q, H_kv, T_cap, k_cap, N_cap = 3, 64, 8, 50 * BLK, 12, 50
+    c = _case(B, H_q, H_kv, T_cap, [50 * BLK, 31 * BLK + 7, 2 * BLK], k_cap, N_cap, seed=3 + n_split)
+    _, _, khat, vhat = _rows_from_oracle(c, N_cap, B, H_kv)
+    O1, _, s1 = _gpu_nsa(c, khat, vhat, 300, B, H_q, n_split)
+    O2, _, s2 = _gpu_nsa(c, khat, vhat, 300, B, H_q, n_split, flags=binding.SPARSE_NSA_BRANCH_GRID)
+    assert s1.item() == 0 and s2.item() == 0
+    assert (O1.float() - O2.float()).abs().max().item() <= 1e-2
 
 
 @pytest.mark.parametrize("branch", [0, 1, 2])
@@ -143,13 +159,14 @@ def test_nsa_degenerate_lengths_and_counts():
     assert float(O[0].float().abs().max()) == 0.0   # no token: every branch is empty
 
 
-def test_nsa_workspace_reuse_is_deterministic():
+@pytest.mark.parametrize("flags", [0, binding.SPARSE_NSA_BRANCH_GRID])
+def test_nsa_repeat_calls_are_deterministic(flags):
     B, H_q, H_kv, T_cap, k_cap, N_cap = 2, 64, 8, 33 * BLK, 6, 33
     c = _case(B, H_q, H_kv, T_cap, [33 * BLK, 17 * BLK + 30], k_cap, N_cap, seed=5)
     _, _, khat, vhat = _rows_from_oracle(c, N_cap, B, H_kv)
-    O1, ws, _ = _gpu_nsa(c, khat, vhat, 256, B, H_q)
-    O2, _, _ = _gpu_nsa(c, khat, vhat, 256, B, H_q, ws=ws)
-    O3, _, _ = _gpu_nsa(c, khat, vhat, 256, B, H_q, ws=ws)
+    O1, ws, _ = _gpu_nsa(c, khat, vhat, 256, B, H_q, flags=flags)
+    O2, _, _ = _gpu_nsa(c, khat, vhat, 256, B, H_q, ws=ws, flags=flags)
+    O3, _, _ = _gpu_nsa(c, khat, vhat, 256, B, H_q, ws=ws, flags=flags)
     assert torch.equal(O1, O2) and torch.equal(O2, O3)
 
 
