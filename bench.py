@@ -1008,8 +1008,10 @@ def run_nsa_case(args, dev):
     from block_sparse_long_pool_gb300 import workloads as wl
     sh = wl.DECODE_128K
     peak, src = measured_peaks()
-    B, H_q, H_kv, T, N = sh.B, sh.H_q, sh.H_kv, sh.T, sh.N_b
-    k_tot, w = sh.k_tot, NSA_WINDOW_TOKENS
+    B, H_q, H_kv = sh.B, sh.H_q, sh.H_kv
+    T = args.tokens if args.tokens > 0 else sh.T   # a shorter cache only for small profiling captures
+    N = (T + BLK - 1) // BLK
+    k_tot, w = min(sh.k_tot, N), NSA_WINDOW_TOKENS
     kc = torch.empty((B, H_kv, T, D), dtype=torch.bfloat16, device=dev)
     vc = torch.empty_like(kc)
     ktil = torch.zeros((B, H_kv, N, D), dtype=torch.float32, device=dev)
@@ -1065,7 +1067,7 @@ def run_nsa_case(args, dev):
     sel_bytes = pairs * N * KTIL_ROW_BYTES
     sgbs, sfrac = _rate(sel_bytes, t_sel["median_us"], peak)
     lgbs, lfrac = _rate(attn_bytes + sel_bytes, t_layer["median_us"], peak)
-    line = {"case": "nsa128k", "workload": f"nsa_decode_128k_b{B}_hq{H_q}_hkv{H_kv}_w{w}",
+    line = {"case": "nsa128k", "workload": f"nsa_decode_{T // 1024}k_b{B}_hq{H_q}_hkv{H_kv}_w{w}",
             "unit_of_work": "one NSA decode layer (multi-head routing + gated three-branch attention)",
             "attention": {"form": "fused (one cluster per pair, three branch states, one DSMEM merge)",
                           "launches": 1, **t_attn, "algorithmic_bytes": nbytes, "achieved_gbs": gbs,
@@ -1120,7 +1122,7 @@ def main():
     ap.add_argument("--step-mode", choices=["fused", "separate"], default="fused",
                     help="fused: one sparse_decode_attn_forecast launch per layer; separate: sparse_select_topk "
                          "on a side stream beside sparse_decode_attn")
-    ap.add_argument("--tokens", type=int, default=0, help="layer case: cached tokens (default 131072)")
+    ap.add_argument("--tokens", type=int, default=0, help="layer / nsa128k cases: cached tokens (default 131072)")
     ap.add_argument("--flush-mb", type=int, default=512, help="layer case: L2 flush buffer before each launch")
     args = ap.parse_args()
     if args.warmup < 3 and args.case == "step":
