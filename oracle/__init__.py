@@ -15,6 +15,9 @@ What each routine follows on the pages is stated in ``oracle.c``:
 * ``attn``    -- SparDA notes, eq.(7), scale 1/sqrt(d) from the SSV notes' NSA step 3.
 * ``verify``  -- SSV notes, mechanism 1, mode A (per-query sets plus window).
 * ``gather``  -- SparDA notes, §4.5: staging is a plain copy.
+* ``pool_windows`` / ``select_windows`` / ``nsa(..., cmp=(l, s))`` -- eq.(4) with an
+  overlapping kernel and stride, NSA routing max-pooled onto the 64-token blocks, and
+  NSA's compressed branch over those windows.
 """
 from __future__ import annotations
 
@@ -67,6 +70,11 @@ def load_library(path: str):
     lib.oracle_verify_shared.argtypes = lib.oracle_verify.argtypes
     lib.oracle_gather.argtypes = [P, i64, i32, P, P, i32, P]
     lib.oracle_nsa.argtypes = [P, i32, P, P, i64, i32, P, P, i32, P, P, i32, P, i64, P, f64, P]
+    lib.oracle_nsa_windows.argtypes = [P, i32, P, P, i64, i32, P, P, i32, P, P, i32, P, i64, P, f64, i32, i32, P]
+    lib.oracle_pool_windows.argtypes = [P, i64, i32, P, i32, i32, i32, P]
+    lib.oracle_pool_windows.restype = i32
+    lib.oracle_select_windows.argtypes = [P, i32, P, i32, i32, P, i32, i32, f64, i32, i32, i32, i32, P, P, P, i32]
+    lib.oracle_select_windows.restype = i32
     return lib
 
 
@@ -197,10 +205,59 @@ def verify(Q, K, V, I, C: int, window_blocks: int, lens, scale: float | None = N
     return O, int(u[0]), int(pq[0])
 
 
-def nsa(Q, K, V, khat, vhat, blocks, count, lens, window_tokens: int, gates, scale: float | None = None):
+def windows(lens, l: int, s: int):
+    """Complete compression windows [s*j, s*j + l) within each length."""
+    lens = np.asarray(lens, dtype=np.int64)
+    return np.where(lens < l, 0, (lens - l) // s + 1)
+
+
+def pool_windows(X, lens, l: int, s: int, n_rows_cap: int) -> np.ndarray:
+    """Overlapping compression: rows [P][n_rows_cap][128] (fp64), row j the mean of
+    X[s*j : s*j + l] for the complete windows, zero beyond."""
+    X = _u16(X)
+    lens = _i64(lens)
+    P, T_cap, d = X.shape
+    assert d == D and lens.shape == (P,)
+    out = np.empty((P, n_rows_cap, D), dtype=np.float64)
+    rc = _load().oracle_pool_windows(_ptr(X), T_cap, P, _ptr(lens), int(l), int(s), int(n_rows_cap), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_pool_windows: more windows than n_rows_cap")
+    return out
+
+
+def select_windows(Q, kcmp, lens, l: int, s: int, n_init: int, n_local: int, k: int, k_tot: int | None = None,
+                   scale: float = 0.0, n_blocks_cap: int | None = None):
+    """NSA routing: per-head softmax over the compressed windows kcmp [P][R][128],
+    summed over the G heads of Q [P][G][128], max-pooled onto the 64-token blocks,
+    top-k.  Returns (idx [P][k_tot] int32, count [P] int32, block scores [P][n_blocks_cap])."""
+    Q = _u16(Q)
+    kcmp = np.ascontiguousarray(kcmp, dtype=np.float64)
+    lens = _i64(lens)
+    P, n_rows_cap, d = kcmp.shape
+    G = Q.shape[1]
+    assert d == D and Q.shape == (P, G, D) and lens.shape == (P,)
+    if k_tot is None:
+        k_tot = n_init + n_local + k
+    if n_blocks_cap is None:
+        n_blocks_cap = max(1, int((lens.max() + BLK - 1) // BLK))
+    idx = np.empty((P, k_tot), dtype=np.int32)
+    count = np.empty((P,), dtype=np.int32)
+    scores = np.empty((P, n_blocks_cap), dtype=np.float64)
+    rc = _load().oracle_select_windows(_ptr(Q), G, _ptr(kcmp), n_rows_cap, P, _ptr(lens), int(l), int(s),
+                                       float(scale), n_init, n_local, k, k_tot, _ptr(idx), _ptr(count),
+                                       _ptr(scores), int(n_blocks_cap))
+    if rc != 0:
+        raise ValueError("oracle_select_windows: a pair needs more than k_tot, n_rows_cap or n_blocks_cap entries")
+    return idx, count, scores
+
+
+def nsa(Q, K, V, khat, vhat, blocks, count, lens, window_tokens: int, gates, scale: float | None = None,
+        cmp: tuple[int, int] | None = None):
     """NSA gated three-branch output: Q [P][G][128] bf16 bits, K/V [P][T][128] bf16 bits,
     khat/vhat [P][N][128] compressed rows, blocks [P][k_tot] selected, gates [P][G][3]
-    = (g_c, g_s, g_w).  Returns O [P][G][128] fp64."""
+    = (g_c, g_s, g_w).  The compressed rows are one per 64-token block holding a token,
+    or with ``cmp = (l, s)`` the complete windows of kernel l and stride s.
+    Returns O [P][G][128] fp64."""
     Q, K, V = _u16(Q), _u16(K), _u16(V)
     khat = np.ascontiguousarray(khat, dtype=np.float64)
     vhat = np.ascontiguousarray(vhat, dtype=np.float64)
@@ -214,8 +271,14 @@ def nsa(Q, K, V, khat, vhat, blocks, count, lens, window_tokens: int, gates, sca
     if scale is None:
         scale = 1.0 / np.sqrt(D)
     O = np.empty((P, G, D), dtype=np.float64)
-    _load().oracle_nsa(_ptr(Q), G, _ptr(K), _ptr(V), T, P, _ptr(khat), _ptr(vhat), n_cap, _ptr(blocks), _ptr(count),
-                       blocks.shape[1], _ptr(lens), int(window_tokens), _ptr(gates), float(scale), _ptr(O))
+    if cmp is None:
+        _load().oracle_nsa(_ptr(Q), G, _ptr(K), _ptr(V), T, P, _ptr(khat), _ptr(vhat), n_cap, _ptr(blocks),
+                           _ptr(count), blocks.shape[1], _ptr(lens), int(window_tokens), _ptr(gates), float(scale),
+                           _ptr(O))
+    else:
+        _load().oracle_nsa_windows(_ptr(Q), G, _ptr(K), _ptr(V), T, P, _ptr(khat), _ptr(vhat), n_cap, _ptr(blocks),
+                                   _ptr(count), blocks.shape[1], _ptr(lens), int(window_tokens), _ptr(gates),
+                                   float(scale), int(cmp[0]), int(cmp[1]), _ptr(O))
     return O
 
 

@@ -34,6 +34,14 @@
  *                  over the layout of the group's first query (plus the window).
  *   oracle_nsa     [SSV] "NSA three-branch math": compressed, selected and sliding-window
  *                  branches, each its own softmax, combined by per-head gates.
+ *   oracle_pool_windows  eq.(4) with an overlapping kernel l and stride s (the pages'
+ *                  inference setting l = 32, s = 16): the compressed rows of NSA's
+ *                  compressed branch ([SSV] "NSA", branch 1).
+ *   oracle_select_windows  NSA routing on those rows: each head's softmax over the
+ *                  windows, summed over heads, max-pooled onto the 64-token blocks
+ *                  ([SparDA] §4.4: scores on a finer grid are max-pooled onto the
+ *                  coarse one), then the top-k of oracle_select.
+ *   oracle_nsa_windows  oracle_nsa with the compressed branch over the windows.
  *   oracle_gather  [SparDA] §4.5: staging selected blocks is a plain copy.
  *
  * Readings where the pages are silent are stated at each routine.
@@ -63,6 +71,12 @@ static double bf16_value(uint16_t bits)
 static int blocks_of(long long len)
 {
     return len <= 0 ? 0 : (int)((len + BLK - 1) / BLK);
+}
+
+/* Number of complete compression windows [s*j, s*j + l) within the first len tokens. */
+static int windows_of(long long len, int l, int s)
+{
+    return len < l ? 0 : (int)((len - l) / s + 1);
 }
 
 void oracle_set_threads(int n)
@@ -117,6 +131,43 @@ void oracle_pool(const uint16_t *K, long long pair_stride, int n_pairs,
                 out[(size_t)j * D + d] = n > 0 ? sum[d] / (double)n : 0.0;
         }
     }
+}
+
+/*
+ * Overlapping compression, [SparDA] eq.(4) with kernel l and stride s ([SparDA] §4.4:
+ * l = 32, s = 16 at inference) and [SSV] "NSA" branch 1 (compressed blocks of length
+ * l, stride d).  X is [n_pairs][pair_stride][D] bf16 bits; out [n_pairs][n_rows_cap][D]:
+ *   out[p][j][d] = (1/l) * sum_{t = s*j}^{s*j + l - 1} X[p][t][d],   j < W = floor((len - l)/s) + 1.
+ * Reading: only complete windows are rows (a window is compressed once its last token
+ * is present; the most recent tokens are the sliding window's); rows j >= W are zero.
+ * Returns -1 when some pair has more than n_rows_cap windows (its rows are clipped).
+ */
+int oracle_pool_windows(const uint16_t *X, long long pair_stride, int n_pairs, const long long *len, int l, int s,
+                        int n_rows_cap, double *out)
+{
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int p = 0; p < n_pairs; ++p) {
+        const uint16_t *Xp = X + (size_t)p * (size_t)pair_stride * D;
+        double *o = out + (size_t)p * (size_t)n_rows_cap * D;
+        int W = windows_of(len[p], l, s);
+        if (W > n_rows_cap) {
+            bad |= 1;
+            W = n_rows_cap;
+        }
+        for (int j = 0; j < n_rows_cap; ++j) {
+            double sum[D];
+            for (int d = 0; d < D; ++d)
+                sum[d] = 0.0;
+            if (j < W)
+                for (long long t = (long long)s * j; t < (long long)s * j + l; ++t)
+                    for (int d = 0; d < D; ++d)
+                        sum[d] += bf16_value(Xp[(size_t)t * D + d]);
+            for (int d = 0; d < D; ++d)
+                o[(size_t)j * D + d] = j < W ? sum[d] / (double)l : 0.0;
+        }
+    }
+    return bad ? -1 : 0;
 }
 
 typedef struct {
@@ -295,6 +346,80 @@ int oracle_select_heads(const uint16_t *Q, int G, const double *ktil, int n_bloc
 }
 
 /*
+ * NSA routing over overlapping compression windows (rows of oracle_pool_windows):
+ *   a^h_j = scale * <q_h, kcmp_j>,  j < W(len) complete windows;
+ *   p_j   = sum_h exp(a^h_j) / sum_i exp(a^h_i)    (each head's softmax, summed);
+ *   s_b   = max { p_j : window j shares a token with block b }, 0 when none,
+ * for the N_b = ceil(len / 64) selection blocks, then the top-k of oracle_select.
+ * Readings: "shares a token" = [s*j, s*j + l) meets [64b, 64b + 64) (max-pooling
+ * onto the coarse grid, [SparDA] §4.4); a block no complete window reaches (the
+ * trailing one) scores 0 (the p_j are positive); scale 0 means 1/sqrt(d).
+ *   kcmp [n_pairs][n_rows_cap][D]; scores (nullable) [n_pairs][n_blocks_cap] block scores.
+ * Returns -1 when a pair needs more than k_tot entries, more than n_rows_cap windows
+ * or more than n_blocks_cap blocks.
+ */
+int oracle_select_windows(const uint16_t *Q, int G, const double *kcmp, int n_rows_cap, int n_pairs,
+                          const long long *len, int l, int s, double scale, int n_init, int n_local, int k,
+                          int k_tot, int *idx, int *count, double *scores, int n_blocks_cap)
+{
+    if (scale == 0.0)
+        scale = 1.0 / sqrt((double)D);
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int p = 0; p < n_pairs; ++p) {
+        const int nb = blocks_of(len[p]);
+        const int W = windows_of(len[p], l, s);
+        int *out = idx + (size_t)p * k_tot;
+        if (W > n_rows_cap || nb > n_blocks_cap) {
+            bad |= 1;
+            count[p] = 0;
+            continue;
+        }
+        double *a = (double *)malloc(sizeof(double) * ((size_t)W + 1));
+        double *pj = (double *)calloc((size_t)W + 1, sizeof(double));
+        for (int h = 0; h < G; ++h) {
+            double q[D];
+            for (int d = 0; d < D; ++d)
+                q[d] = bf16_value(Q[((size_t)p * G + h) * D + d]);
+            double m = -INFINITY;
+            for (int j = 0; j < W; ++j) {
+                const double *kj = kcmp + ((size_t)p * n_rows_cap + j) * D;
+                double acc = 0.0;
+                for (int d = 0; d < D; ++d)
+                    acc += q[d] * kj[d];
+                a[j] = scale * acc;
+                if (a[j] > m)
+                    m = a[j];
+            }
+            double z = 0.0;
+            for (int j = 0; j < W; ++j)
+                z += exp(a[j] - m);
+            for (int j = 0; j < W; ++j)
+                pj[j] += exp(a[j] - m) / z;
+        }
+        double *sb = (double *)calloc((size_t)nb + 1, sizeof(double));
+        for (int b = 0; b < nb; ++b) {
+            double best = 0.0;
+            for (int j = 0; j < W; ++j) {
+                const long long w0 = (long long)s * j, w1 = w0 + l;
+                const long long b0 = (long long)b * BLK, b1 = b0 + BLK;
+                if (w0 < b1 && b0 < w1 && pj[j] > best)
+                    best = pj[j];
+            }
+            sb[b] = best;
+        }
+        if (scores)
+            for (int b = 0; b < n_blocks_cap; ++b)
+                scores[(size_t)p * n_blocks_cap + b] = b < nb ? sb[b] : 0.0;
+        bad |= select_from_scores(sb, nb, n_init, n_local, k, k_tot, out, count + p);
+        free(sb);
+        free(pj);
+        free(a);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
  * One query row q over the token set { t : block(t) in set, t < len }:
  *   a_t = scale * <q, k_t>,  o = sum_t softmax(a)_t v_t,  lse = log sum_t exp(a_t).
  * member[j] != 0 marks block j as part of the set (a set: each block counts once).
@@ -463,16 +588,17 @@ static void attend_rows(const double *qd, const double *kr, const double *vr, in
  * present), the window is token-granular, and a branch with no rows contributes zero.
  *   Q [n_pairs][G][D] bf16 bits; K, V [n_pairs][pair_stride][D] bf16 bits; O [n_pairs][G][D].
  */
-void oracle_nsa(const uint16_t *Q, int G, const uint16_t *K, const uint16_t *V, long long pair_stride, int n_pairs,
-                const double *khat, const double *vhat, int n_blocks_cap, const int *blocks, const int *count,
-                int k_tot, const long long *len, long long window_tokens, const double *gates, double scale,
-                double *O)
+static void nsa_impl(const uint16_t *Q, int G, const uint16_t *K, const uint16_t *V, long long pair_stride,
+                     int n_pairs, const double *khat, const double *vhat, int n_rows_cap, const int *blocks,
+                     const int *count, int k_tot, const long long *len, long long window_tokens,
+                     const double *gates, double scale, int cmp_len, int cmp_stride, double *O)
 {
 #pragma omp parallel for schedule(dynamic, 1)
     for (int p = 0; p < n_pairs; ++p) {
         int nb = blocks_of(len[p]);
-        if (nb > n_blocks_cap)
-            nb = n_blocks_cap;
+        int nrows = cmp_len > 0 ? windows_of(len[p], cmp_len, cmp_stride) : nb;
+        if (nrows > n_rows_cap)
+            nrows = n_rows_cap;
         char *member = (char *)calloc((size_t)nb + 1, 1);
         for (int i = 0; i < count[p] && i < k_tot; ++i) {
             int j = blocks[(size_t)p * k_tot + i];
@@ -481,8 +607,8 @@ void oracle_nsa(const uint16_t *Q, int G, const uint16_t *K, const uint16_t *V, 
         }
         const uint16_t *Kp = K + (size_t)p * (size_t)pair_stride * D;
         const uint16_t *Vp = V + (size_t)p * (size_t)pair_stride * D;
-        const double *kr = khat + (size_t)p * n_blocks_cap * D;
-        const double *vr = vhat + (size_t)p * n_blocks_cap * D;
+        const double *kr = khat + (size_t)p * n_rows_cap * D;
+        const double *vr = vhat + (size_t)p * n_rows_cap * D;
         long long w0 = len[p] - window_tokens;
         if (w0 < 0)
             w0 = 0;
@@ -492,7 +618,7 @@ void oracle_nsa(const uint16_t *Q, int G, const uint16_t *K, const uint16_t *V, 
             for (int d = 0; d < D; ++d)
                 qd[d] = bf16_value(q[d]);
             attend_set(q, Kp, Vp, member, nb, len[p], scale, os, &l);
-            attend_rows(qd, kr, vr, nb, scale, oc);
+            attend_rows(qd, kr, vr, nrows, scale, oc);
             attend_tokens(qd, Kp, Vp, w0, len[p], scale, ow);
             const double *g = gates + ((size_t)p * G + h) * 3;
             double *o = O + ((size_t)p * G + h) * D;
@@ -501,6 +627,29 @@ void oracle_nsa(const uint16_t *Q, int G, const uint16_t *K, const uint16_t *V, 
         }
         free(member);
     }
+}
+
+void oracle_nsa(const uint16_t *Q, int G, const uint16_t *K, const uint16_t *V, long long pair_stride, int n_pairs,
+                const double *khat, const double *vhat, int n_blocks_cap, const int *blocks, const int *count,
+                int k_tot, const long long *len, long long window_tokens, const double *gates, double scale,
+                double *O)
+{
+    nsa_impl(Q, G, K, V, pair_stride, n_pairs, khat, vhat, n_blocks_cap, blocks, count, k_tot, len, window_tokens,
+             gates, scale, 0, 0, O);
+}
+
+/*
+ * oracle_nsa with NSA's overlapping compression: the compressed branch attends over the
+ * W(len) complete windows of kernel cmp_len and stride cmp_stride (khat, vhat
+ * [n_pairs][n_rows_cap][D], e.g. oracle_pool_windows of K and of V).
+ */
+void oracle_nsa_windows(const uint16_t *Q, int G, const uint16_t *K, const uint16_t *V, long long pair_stride,
+                        int n_pairs, const double *khat, const double *vhat, int n_rows_cap, const int *blocks,
+                        const int *count, int k_tot, const long long *len, long long window_tokens,
+                        const double *gates, double scale, int cmp_len, int cmp_stride, double *O)
+{
+    nsa_impl(Q, G, K, V, pair_stride, n_pairs, khat, vhat, n_rows_cap, blocks, count, k_tot, len, window_tokens,
+             gates, scale, cmp_len, cmp_stride, O);
 }
 
 /*

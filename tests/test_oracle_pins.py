@@ -497,6 +497,116 @@ def test_nsa_output_is_linear_in_the_gates():
     assert np.allclose(O, 0.25 * Oc - 0.5 * Os + 1.5 * Ow, rtol=1e-12, atol=1e-13)
 
 
+# ----------------------------------------------------------------------------- overlapping compression (NSA)
+
+
+def test_pool_windows_ramp_closed_form():
+    """X[t] = t (exact in bf16 up to 256): window j of kernel 32, stride 16 has mean
+    16 j + 15.5; rows past the complete windows are zero."""
+    T = 200
+    X = bits(np.repeat(np.arange(T, dtype=np.float32)[:, None], D, axis=1)[None])
+    out = oracle.pool_windows(X, [T], 32, 16, 14)
+    W = (T - 32) // 16 + 1
+    for j in range(14):
+        want = 16 * j + 15.5 if j < W else 0.0
+        assert np.all(out[0, j] == want), j
+
+
+def test_pool_windows_match_numpy_slices():
+    P, T = 3, 300
+    X = rand_bits((P, T, D), 71)
+    lens = np.array([300, 47, 31], np.int64)
+    for l, s in ((32, 16), (16, 8), (64, 32)):
+        out = oracle.pool_windows(X, lens, l, s, 40)
+        v = values(X)
+        for p in range(P):
+            W = 0 if lens[p] < l else (lens[p] - l) // s + 1
+            for j in range(40):
+                want = v[p, s * j:s * j + l].mean(axis=0) if j < W else np.zeros(D)
+                assert np.allclose(out[p, j], want, rtol=1e-14, atol=1e-15), (l, s, p, j)
+
+
+def test_pool_windows_with_the_block_kernel_are_the_complete_block_means():
+    X = rand_bits((2, 320, D), 72)
+    lens = np.array([320, 200], np.int64)
+    win = oracle.pool_windows(X, lens, BLK, BLK, 5)
+    blk = oracle.pool(X, lens, 5)
+    for p in range(2):
+        full = int(lens[p]) // BLK
+        assert np.allclose(win[p, :full], blk[p, :full], rtol=1e-14, atol=1e-15)
+        assert np.all(win[p, full:] == 0)
+
+
+def _windows_case(seed, P=3, G=4, T=1000):
+    X = rand_bits((P, T, D), seed)
+    lens = np.array([T, 777, 300][:P], np.int64)
+    kc = oracle.pool_windows(X, lens, 32, 16, (T - 32) // 16 + 1)
+    Q = rand_bits((P, G, D), seed + 1)
+    return Q, kc, lens
+
+
+def test_select_windows_match_brute_force_softmax_and_max_pooling():
+    from scipy.special import softmax
+    Q, kc, lens = _windows_case(81)
+    n_init, n_local, k = 1, 2, 4
+    idx, cnt, sc = oracle.select_windows(Q, kc, lens, 32, 16, n_init, n_local, k, scale=0.1)
+    qv = values(Q)
+    for p in range(len(lens)):
+        W = (int(lens[p]) - 32) // 16 + 1
+        nb = (int(lens[p]) + BLK - 1) // BLK
+        pj = sum(softmax(0.1 * (kc[p, :W] @ qv[p, h]), axis=0) for h in range(Q.shape[1]))
+        sb = np.zeros(nb)
+        for b in range(nb):
+            over = [pj[j] for j in range(W) if 16 * j < 64 * b + 64 and 64 * b < 16 * j + 32]
+            sb[b] = max(over) if over else 0.0
+        assert np.allclose(sc[p, :nb], sb, rtol=1e-12, atol=1e-15)
+        cand = [b for b in range(nb) if n_init <= b < nb - n_local]
+        top = sorted(cand, key=lambda b: (-sb[b], b))[:k]
+        want = sorted(set(range(min(n_init, nb))) | set(range(max(nb - n_local, 0), nb)) | set(top))
+        assert list(idx[p, :cnt[p]]) == want
+
+
+def test_select_windows_with_block_windows_is_the_multi_head_selection():
+    """Kernel = stride = 64 and whole blocks: each block is one window, max-pooling is
+    the identity and the routing is oracle_select_heads."""
+    P, G, T = 2, 3, 64 * 40
+    X = rand_bits((P, T, D), 82)
+    lens = np.array([T, 64 * 23], np.int64)
+    kc = oracle.pool_windows(X, lens, BLK, BLK, 40)
+    Q = rand_bits((P, G, D), 83)
+    a = oracle.select_windows(Q, kc, lens, BLK, BLK, 1, 2, 6, scale=0.2, n_blocks_cap=40)
+    b = oracle.select_heads(Q, kc, lens, 1, 2, 6, scale=0.2)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    assert np.allclose(a[2], b[2], rtol=1e-13, atol=1e-16)
+
+
+def _nsa_windows_with(gate, seed=90):
+    P, G, T, w = 2, 3, 10 * BLK + 21, 100
+    lens = np.array([T, 6 * BLK + 3], np.int64)
+    Q, K, V = rand_bits((P, G, D), seed), rand_bits((P, T, D), seed + 1), rand_bits((P, T, D), seed + 2)
+    R = (T - 32) // 16 + 1
+    kc, vc = oracle.pool_windows(K, lens, 32, 16, R), oracle.pool_windows(V, lens, 32, 16, R)
+    blocks = np.array([[1, 4, 9, -1], [0, 2, -1, -1]], np.int32)
+    count = np.array([3, 2], np.int32)
+    gates = np.broadcast_to(np.asarray(gate, np.float64), (P, G, 3)).copy()
+    O = oracle.nsa(Q, K, V, kc, vc, blocks, count, lens, w, gates, cmp=(32, 16))
+    return O, (Q, K, V, kc, vc, blocks, count, lens, w, gates)
+
+
+def test_nsa_windows_compressed_branch_is_sdpa_over_the_complete_windows():
+    O, (Q, _, _, kc, vc, _, _, lens, _, _) = _nsa_windows_with((1.0, 0.0, 0.0))
+    for p in range(2):
+        W = (int(lens[p]) - 32) // 16 + 1
+        mask = np.arange(kc.shape[1]) < W
+        assert np.allclose(O[p], _sdpa(values(Q[p]), kc[p], vc[p], mask), rtol=1e-11, atol=1e-12)
+
+
+def test_nsa_windows_leave_the_selected_and_window_branches_alone():
+    O, (Q, K, V, kc, vc, blocks, count, lens, w, gates) = _nsa_windows_with((0.0, 0.7, 0.3))
+    ref = oracle.nsa(Q, K, V, np.zeros((2, 11, D)), np.zeros((2, 11, D)), blocks, count, lens, w, gates)
+    assert np.allclose(O, ref, rtol=1e-13, atol=1e-14)
+
+
 # ----------------------------------------------------------------------------- mutants
 
 MUTANTS = [
@@ -530,7 +640,17 @@ MUTANTS = [
     # the NSA gates are swapped between the compressed and the selected branch
     ("o[d] = g[0] * oc[d] + g[1] * os[d] + g[2] * ow[d];", "o[d] = g[1] * oc[d] + g[0] * os[d] + g[2] * ow[d];"),
     # the NSA compressed branch forgets the last compressed row
-    ("attend_rows(qd, kr, vr, nb, scale, oc);", "attend_rows(qd, kr, vr, nb - 1, scale, oc);"),
+    ("attend_rows(qd, kr, vr, nrows, scale, oc);", "attend_rows(qd, kr, vr, nrows - 1, scale, oc);"),
+    # the compression windows start one token late
+    ("for (long long t = (long long)s * j; t < (long long)s * j + l; ++t)",
+     "for (long long t = (long long)s * j + 1; t < (long long)s * j + l; ++t)"),
+    # max-pooling takes only the windows that lie inside the block
+    ("if (w0 < b1 && b0 < w1 && pj[j] > best)", "if (w0 >= b0 && w1 <= b1 && pj[j] > best)"),
+    # the window routing sums raw scores instead of per-head distributions
+    ("pj[j] += exp(a[j] - m) / z;", "pj[j] += a[j];"),
+    # the NSA window form attends over one row per block instead of the windows
+    ("int nrows = cmp_len > 0 ? windows_of(len[p], cmp_len, cmp_stride) : nb;",
+     "int nrows = cmp_len > 0 ? (nb < windows_of(len[p], cmp_len, cmp_stride) ? nb : windows_of(len[p], cmp_len, cmp_stride) - 1) : nb;"),
     # mode B takes the group's last query as its representative
     ("const int *Ia = shared ? I + (((size_t)b * H_kv + g) * N_q + q0) * n_sel : Iq;",
      "const int *Ia = shared ? I + (((size_t)b * H_kv + g) * N_q + (q0 + C - 1 < N_q ? q0 + C - 1 : N_q - 1)) * n_sel : Iq;"),
@@ -550,7 +670,12 @@ PIN_TESTS = [
     test_verify_shared_layout_attends_over_the_first_query_set, test_verify_shared_layout_with_singleton_groups_is_mode_a,
     test_verify_shared_layout_on_the_worked_example, test_nsa_selected_branch_is_sdpa_over_the_selected_tokens,
     test_nsa_window_branch_is_sdpa_over_the_last_w_tokens, test_nsa_compressed_branch_is_sdpa_over_the_compressed_rows,
-    test_nsa_output_is_linear_in_the_gates,
+    test_nsa_output_is_linear_in_the_gates, test_pool_windows_ramp_closed_form, test_pool_windows_match_numpy_slices,
+    test_pool_windows_with_the_block_kernel_are_the_complete_block_means,
+    test_select_windows_match_brute_force_softmax_and_max_pooling,
+    test_select_windows_with_block_windows_is_the_multi_head_selection,
+    test_nsa_windows_compressed_branch_is_sdpa_over_the_complete_windows,
+    test_nsa_windows_leave_the_selected_and_window_branches_alone,
 ]
 
 
