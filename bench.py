@@ -1000,9 +1000,11 @@ NSA_WINDOW_TOKENS = 512
 
 def run_nsa_case(args, dev):
     """NSA's gated three-branch decode on the 128K decode shape (8 x 8 pairs, G = 8,
-    67 selected blocks, a 512-token window, 2048 compressed rows per pair): the
-    multi-head selector over the compressed keys (NSA's routing) and the one-launch
-    three-branch attention, each timed alone and as a layer."""
+    67 selected blocks, a 512-token window): with one compressed row per 64-token block
+    (2048 per pair) and with NSA's overlapping 32/16 windows (8191 per pair).  For each:
+    the routing (tensor-core sparse_nsa_select on the bf16 rows) and the one-launch
+    three-branch attention, timed alone and as a layer; the fp32 multi-head selector
+    (sparse_select_topk_heads) on the block rows for comparison."""
     import torch
     from block_sparse_long_pool_gb300 import binding
     from block_sparse_long_pool_gb300 import workloads as wl
@@ -1045,16 +1047,41 @@ def run_nsa_case(args, dev):
         binding.sparse_decode_attn_nsa(Q, kc, vc, khat, vhat, idx, cnt, seq, w, gates, O, ws, n_split=args.n_split,
                                        flags=binding.SPARSE_NSA_BRANCH_GRID, status=status)
 
+    def route():
+        binding.sparse_nsa_select(Q, khat, seq, sh.n_init, sh.n_local, sh.k, idx, cnt, cmp=(0, 0), status=status)
+
     def layer():
-        select()
+        route()
         attend()
+
+    # NSA's overlapping compression: kernel 32, stride 16
+    wl_, ws_ = 32, 16
+    R = (T - wl_) // ws_ + 1
+    kw = torch.empty((B, H_kv, R, D), dtype=torch.bfloat16, device=dev)
+    vw = torch.empty_like(kw)
+    binding.sparse_nsa_compress(kc, vc, kw, vw, 0, T, cmp=(wl_, ws_))
+
+    def route_w():
+        binding.sparse_nsa_select(Q, kw, seq, sh.n_init, sh.n_local, sh.k, idx, cnt, cmp=(wl_, ws_), status=status)
+
+    def attend_w():
+        binding.sparse_decode_attn_nsa(Q, kc, vc, kw, vw, idx, cnt, seq, w, gates, O, None, n_split=args.n_split,
+                                       status=status, cmp=(wl_, ws_))
+
+    def layer_w():
+        route_w()
+        attend_w()
 
     select()
     torch.cuda.synchronize()
     t_attn = _event_times(attend, args.steps, args.warmup, evict)
     t_grid = _event_times(attend_grid, args.steps, args.warmup, evict)
     t_sel = _event_times(select, args.steps, args.warmup, evict)
+    t_route = _event_times(route, args.steps, args.warmup, evict)
     t_layer = _event_times(layer, args.steps, args.warmup, evict)
+    t_route_w = _event_times(route_w, args.steps, args.warmup, evict)
+    t_attn_w = _event_times(attend_w, args.steps, args.warmup, evict)
+    t_layer_w = _event_times(layer_w, args.steps, args.warmup, evict)
     torch.cuda.synchronize()
     assert status.item() == 0, f"device status {status.item()}"
     pairs = B * H_kv
@@ -1066,7 +1093,15 @@ def run_nsa_case(args, dev):
     ggbs, gfrac = _rate(attn_bytes, t_grid["median_us"], peak)
     sel_bytes = pairs * N * KTIL_ROW_BYTES
     sgbs, sfrac = _rate(sel_bytes, t_sel["median_us"], peak)
-    lgbs, lfrac = _rate(attn_bytes + sel_bytes, t_layer["median_us"], peak)
+    route_bytes = pairs * N * D * 2
+    rgbs, rfrac = _rate(route_bytes, t_route["median_us"], peak)
+    lgbs, lfrac = _rate(attn_bytes + route_bytes, t_layer["median_us"], peak)
+    wbytes = dict(nbytes, compressed_rows=pairs * R * 2 * D * 2)
+    attn_w_bytes = sum(wbytes.values())
+    route_w_bytes = pairs * R * D * 2
+    awgbs, awfrac = _rate(attn_w_bytes, t_attn_w["median_us"], peak)
+    rwgbs, rwfrac = _rate(route_w_bytes, t_route_w["median_us"], peak)
+    lwgbs, lwfrac = _rate(attn_w_bytes + route_w_bytes, t_layer_w["median_us"], peak)
     line = {"case": "nsa128k", "workload": f"nsa_decode_{T // 1024}k_b{B}_hq{H_q}_hkv{H_kv}_w{w}",
             "unit_of_work": "one NSA decode layer (multi-head routing + gated three-branch attention)",
             "attention": {"form": "fused (one cluster per pair, three branch states, one DSMEM merge)",
@@ -1074,10 +1109,21 @@ def run_nsa_case(args, dev):
                           "frac_of_measured_hbm": frac},
             "attention_branch_grid": {"form": "a cluster per branch and pair, gates from the workspace",
                                       "launches": 1, **t_grid, "achieved_gbs": ggbs, "frac_of_measured_hbm": gfrac},
-            "routing": {"call": "sparse_select_topk_heads", **t_sel, "algorithmic_bytes": sel_bytes,
-                        "achieved_gbs": sgbs, "frac_of_measured_hbm": sfrac},
+            "routing": {"call": "sparse_nsa_select (bf16 block rows, tensor cores)", **t_route,
+                        "algorithmic_bytes": route_bytes, "achieved_gbs": rgbs, "frac_of_measured_hbm": rfrac},
+            "routing_fp32_multi_head": {"call": "sparse_select_topk_heads (fp32 block rows)", **t_sel,
+                                        "algorithmic_bytes": sel_bytes, "achieved_gbs": sgbs,
+                                        "frac_of_measured_hbm": sfrac},
             "layer": {**t_layer, "achieved_gbs": lgbs, "frac_of_measured_hbm": lfrac,
                       "layers_per_s": round(1e6 / t_layer["median_us"], 1)},
+            "windows_32_16": {
+                "compressed_rows_per_pair": R,
+                "routing": {**t_route_w, "algorithmic_bytes": route_w_bytes, "achieved_gbs": rwgbs,
+                            "frac_of_measured_hbm": rwfrac},
+                "attention": {**t_attn_w, "algorithmic_bytes": wbytes, "achieved_gbs": awgbs,
+                              "frac_of_measured_hbm": awfrac},
+                "layer": {**t_layer_w, "achieved_gbs": lwgbs, "frac_of_measured_hbm": lwfrac,
+                          "layers_per_s": round(1e6 / t_layer_w["median_us"], 1)}},
             "peak_gbs": peak, "peak_source": src, "l2": "512 MB read evicts L2 before each timed call"}
     print(json.dumps(line), flush=True)
 

@@ -58,8 +58,10 @@ SIGNATURES = {
     "sparse_verify_attn_shared": (_I, [_P, _P, _P, _LL, _P, _I, _I, _I, _I, _P, _I, _I, _I, _F, _P, _P, _I,
                                        _P, _P]),
     "sparse_gather_offloaded": (_I, [_P, _P, _LL, _P, _P, _I, _I, _I, _P, _P, _P, _I, _P, _P]),
-    "sparse_decode_attn_nsa": (_I, [_P, _P, _P, _LL, _P, _P, _I, _P, _P, _I, _P, _I, _I, _I, _LL, _P, _F, _P, _P,
-                                    _SZ, _I, _U, _P, _P]),
+    "sparse_decode_attn_nsa": (_I, [_P, _P, _P, _LL, _P, _P, _I, _I, _I, _P, _P, _I, _P, _I, _I, _I, _LL, _P, _F,
+                                    _P, _P, _SZ, _I, _U, _P, _P]),
+    "sparse_nsa_compress": (_I, [_P, _P, _LL, _I, _I, _LL, _I, _I, _I, _P, _P, _I, _P]),
+    "sparse_nsa_select": (_I, [_P, _P, _I, _I, _I, _P, _I, _I, _I, _F, _I, _I, _I, _P, _P, _I, _P, _P]),
     "sparse_decode_attn_nsa_workspace_size": (_SZ, [_I, _I, _I]),
 }
 
@@ -370,9 +372,10 @@ def nsa_workspace(B: int, H_q: int, H_kv: int, device="cuda"):
 
 def sparse_decode_attn_nsa(Q, k_cache, v_cache, khat, vhat, blk_idx, count, seq_len, window_tokens: int, gates, O,
                            workspace, scale: float = 0.0, n_split: int = 0, flags: int = 0, status=None,
-                           stream=None):
+                           stream=None, cmp: tuple = (0, 0)):
     """NSA gated three-branch decode: Q [B][H_q][128], K/V [B][H_kv][T_cap][128],
-    compressed rows khat/vhat [B][H_kv][N_cap][128], selected blocks blk_idx
+    compressed rows khat/vhat [B][H_kv][N_cap][128] (one per 64-token block, or with
+    ``cmp = (l, s)`` the complete overlapping windows), selected blocks blk_idx
     [B][H_kv][k_tot] with count [B][H_kv], gates [B][H_q][3] = (g_c, g_s, g_w) fp32;
     writes O [B][H_q][128] = g_c o_c + g_s o_s + g_w o_w."""
     B, H_q, _ = Q.shape
@@ -391,7 +394,38 @@ def sparse_decode_attn_nsa(Q, k_cache, v_cache, khat, vhat, blk_idx, count, seq_
     _need(O, "O", torch.bfloat16, shape=(B, H_q, D))
     ws, ws_bytes = _ws(workspace)
     rc = load().sparse_decode_attn_nsa(_ptr(Q), _ptr(k_cache), _ptr(v_cache), T_cap, _ptr(khat), _ptr(vhat), N_cap,
-                                       _ptr(blk_idx), _ptr(count), k_tot, _ptr(seq_len), B, H_q, H_kv,
+                                       int(cmp[0]), int(cmp[1]), _ptr(blk_idx), _ptr(count), k_tot, _ptr(seq_len), B, H_q, H_kv,
                                        int(window_tokens), _ptr(gates), float(scale), _ptr(O), ws, ws_bytes,
                                        n_split, int(flags), _ptr(status), _stream(stream))
     _check(rc, "sparse_decode_attn_nsa")
+
+
+def sparse_nsa_compress(k_cache, v_cache, khat, vhat, len_before: int, n_new: int, cmp=(32, 16), stream=None):
+    """Rows of the overlapping windows completed by tokens [len_before, len_before + n_new)."""
+    B, H_kv, T_cap, _ = k_cache.shape
+    R = khat.shape[2]
+    _need(k_cache, "k_cache", torch.bfloat16, shape=(B, H_kv, T_cap, D))
+    _need(v_cache, "v_cache", torch.bfloat16, shape=(B, H_kv, T_cap, D))
+    _need(khat, "khat", torch.bfloat16, shape=(B, H_kv, R, D))
+    _need(vhat, "vhat", torch.bfloat16, shape=(B, H_kv, R, D))
+    rc = load().sparse_nsa_compress(_ptr(k_cache), _ptr(v_cache), T_cap, B, H_kv, int(len_before), int(n_new),
+                                    int(cmp[0]), int(cmp[1]), _ptr(khat), _ptr(vhat), R, _stream(stream))
+    _check(rc, "sparse_nsa_compress")
+
+
+def sparse_nsa_select(Q, khat, seq_len, n_init: int, n_local: int, k: int, idx_out, count_out, cmp=(32, 16),
+                      scale: float = 0.0, status=None, stream=None):
+    """NSA routing: per-head softmax over the compressed rows khat [B][H_kv][R][128],
+    summed over the group, max-pooled onto the 64-token blocks, top-k."""
+    B, H_q, _ = Q.shape
+    _, H_kv, R, _ = khat.shape
+    k_tot = idx_out.shape[2]
+    _need(Q, "Q", torch.bfloat16, shape=(B, H_q, D))
+    _need(khat, "khat", torch.bfloat16, shape=(B, H_kv, R, D))
+    _need(seq_len, "seq_len", torch.int32, shape=(B,))
+    _need(idx_out, "idx_out", torch.int32, shape=(B, H_kv, k_tot))
+    _need(count_out, "count_out", torch.int32, shape=(B, H_kv))
+    rc = load().sparse_nsa_select(_ptr(Q), _ptr(khat), R, int(cmp[0]), int(cmp[1]), _ptr(seq_len), B, H_q, H_kv,
+                                  float(scale), n_init, n_local, k, _ptr(idx_out), _ptr(count_out), k_tot,
+                                  _ptr(status), _stream(stream))
+    _check(rc, "sparse_nsa_select")

@@ -97,6 +97,10 @@ struct AttnParams {
     float *O32;
     long long win_tokens;
     int range_mode;
+    // compressed rows of range_mode 2: one per 64-token block holding a token
+    // (cmp_len = 0), or the complete windows [cmp_stride * j, cmp_stride * j + cmp_len)
+    int cmp_len;
+    int cmp_stride;
 };
 
 __device__ __forceinline__ uint32_t ld_b32(const uint16_t *p)
@@ -171,28 +175,22 @@ __device__ __forceinline__ void load_query(QueryFrags<NT> &q, const AttnParams &
     }
 }
 
-// One consumer warp over tokens [16w, 16w+16) of the block held in ring stage `kst`
-// (K, 2 x 8 KB swizzled boxes) and `kst + kTileBytes` (V).  tok0 is the absolute
-// position of the warp's first token; qmask selects the rows' queries (verification).
-template <int NT, bool VERIFY>
-__device__ __forceinline__ void attend_block(WarpState<NT> &st, const QueryFrags<NT> &q, uint32_t kst, long long tok0,
-                                             long long len, uint32_t qmask, float scale_log2, int w, int lane,
-                                             long long tok_lo = 0)
+// S^T (16 tokens x 8*NT rows) = K (16 x 128) Q^T (128 x 8*NT) for the tokens
+// [16w, 16w+16) of the 64-row K tile at `kst` (2 x 8 KB boxes, 128-byte swizzle), on
+// the bf16 tensor cores.  sacc[nt][i] holds token g8 + 8 (i >> 1) (g8 = lane / 4) and
+// query row 8 nt + 2 (lane % 4) + (i & 1).
+template <int NT>
+__device__ __forceinline__ void score_rows(float (&sacc)[NT][4], const QueryFrags<NT> &q, uint32_t kst, int w,
+                                           int lane)
 {
-    const int g8 = lane >> 2;
     const int jm = lane >> 3, rr = lane & 7;
     const int a_tok = w * 16 + (jm & 1) * 8 + rr;   // K rows for ldmatrix (QK A operand)
-    const int v_tok = w * 16 + (jm >> 1) * 8 + rr;  // V rows for ldmatrix.trans (PV A operand)
     const uint32_t a_sw = static_cast<uint32_t>(a_tok & 7);
-    const uint32_t v_sw = static_cast<uint32_t>(v_tok & 7);
-    const uint32_t vst = kst + kTileBytes;
-    float sacc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             sacc[nt][i] = 0.f;
-    // S^T (16 tokens x 8*NT rows) = K (16 x 128) Q^T (128 x 8*NT)
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
         const uint32_t chunk = static_cast<uint32_t>(((ks & 3) << 1) + (jm >> 1));
@@ -203,6 +201,23 @@ __device__ __forceinline__ void attend_block(WarpState<NT> &st, const QueryFrags
         for (int nt = 0; nt < NT; ++nt)
             mma_bf16_16816(sacc[nt], a, q.qb[nt][ks][0], q.qb[nt][ks][1]);
     }
+}
+
+// One consumer warp over tokens [16w, 16w+16) of the block held in ring stage `kst`
+// (K, 2 x 8 KB swizzled boxes) and `kst + kTileBytes` (V).  tok0 is the absolute
+// position of the warp's first token; qmask selects the rows' queries (verification).
+template <int NT, bool VERIFY>
+__device__ __forceinline__ void attend_block(WarpState<NT> &st, const QueryFrags<NT> &q, uint32_t kst, long long tok0,
+                                             long long len, uint32_t qmask, float scale_log2, int w, int lane,
+                                             long long tok_lo = 0)
+{
+    const int g8 = lane >> 2;
+    const int jm = lane >> 3, rr = lane & 7;
+    const int v_tok = w * 16 + (jm >> 1) * 8 + rr;  // V rows for ldmatrix.trans (PV A operand)
+    const uint32_t v_sw = static_cast<uint32_t>(v_tok & 7);
+    const uint32_t vst = kst + kTileBytes;
+    float sacc[NT][4];
+    score_rows<NT>(sacc, q, kst, w, lane);
     // scale to log2 units, mask tokens past the length and rows not selecting the block
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -366,7 +381,7 @@ __device__ __forceinline__ long long unit_len(const AttnParams &p, int b)
 {
     const long long len = p.seq_len[b];
     if (p.range_mode == 2) {
-        const long long rows = len <= 0 ? 0 : (len + kBlk - 1) / kBlk;
+        const long long rows = compressed_rows(len, p.cmp_len, p.cmp_stride);
         return rows < p.pair_stride ? rows : p.pair_stride;
     }
     return len;
@@ -380,7 +395,7 @@ __device__ __forceinline__ int producer_fetch_slice(const AttnParams &p, int pai
         // a contiguous block range from the length: the window, or every block
         const int b = pair / p.H_kv;
         const long long len = unit_len(p, b);
-        if (p.range_mode == 2 && lane == 0 && p.seq_len[b] > p.pair_stride * kBlk)
+        if (p.range_mode == 2 && lane == 0 && compressed_rows(p.seq_len[b], p.cmp_len, p.cmp_stride) > p.pair_stride)
             report(p.status, SPARSE_ERR_BAD_INDEX);
         const int nb = len <= 0 ? 0 : static_cast<int>((len + kBlk - 1) / kBlk);
         long long w0 = p.range_mode == 1 ? len - p.win_tokens : 0;

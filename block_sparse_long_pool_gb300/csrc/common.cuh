@@ -341,6 +341,16 @@ __device__ __forceinline__ uint32_t order_key(float s)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Compressed rows of a length: one per 64-token block holding a token (cmp_len = 0), or
+// the complete windows [cmp_stride * j, cmp_stride * j + cmp_len) of NSA's overlapping
+// compression.
+__host__ __device__ __forceinline__ long long compressed_rows(long long len, int cmp_len, int cmp_stride)
+{
+    if (cmp_len <= 0)
+        return len <= 0 ? 0 : (len + kBlk - 1) / kBlk;
+    return len < cmp_len ? 0 : (len - cmp_len) / cmp_stride + 1;
+}
+
 }  // namespace sp
 
 // ---------------------------------------------------------------- host side

@@ -12,6 +12,8 @@
 // One CTA per (touched block, pair): 16 threads cover the 16 sixteen-byte chunks of
 // a 256-byte token row, 16 rows per pass; each thread copies its rows of K and V
 // with 16-byte loads/stores and sums its 8 key dimensions in fp32.
+#include <limits.h>
+
 #include "common.cuh"
 
 namespace {
@@ -184,4 +186,121 @@ extern "C" SPARSE_API int sparse_pool_append_kv(uint16_t *k_cache, uint16_t *v_c
         return sp_host::fail(SPARSE_ERR_INVALID_ARG, "sparse_pool_append_kv: null vtil");
     return append_impl("sparse_pool_append_kv", k_cache, v_cache, ktil, vtil, khat, vhat, k_new, v_new, B, H_kv,
                        T_cap, N_cap, len_before, n_new, stream);
+}
+
+// ---------------------------------------------------------------- overlapping compression
+//
+// NSA's compressed rows with an overlapping kernel (SparDA notes, background eq.(4) with
+// the inference kernel l = 32 and stride s = 16 of §4.4; SSV notes, "NSA" branch 1):
+//     khat[p][j] = mean of K[p][s*j .. s*j + l),  vhat likewise,
+// for every window completed by the tokens [len_before, len_before + n_new) (a window is
+// compressed once its last token is in the cache).  One CTA per (new window, pair):
+// 16 threads per 16-byte chunk of a row, 16 rows per pass, fp32 sums, the mean rounded
+// once to bf16.
+
+namespace {
+
+struct CompressParams {
+    const uint16_t *k_cache;
+    const uint16_t *v_cache;
+    uint16_t *khat;
+    uint16_t *vhat;
+    long long T_cap;
+    int n_rows_cap;
+    int cmp_len;
+    int cmp_stride;
+    int first_row;
+};
+
+__global__ void __launch_bounds__(kThreads) compress_windows_kernel(const CompressParams p)
+{
+    __shared__ float red[2][16][kD + 4];
+    const int pair = blockIdx.y;
+    const int j = p.first_row + static_cast<int>(blockIdx.x);
+    const int c = threadIdx.x & 15;   // dims 8c .. 8c+7
+    const int r0 = threadIdx.x >> 4;  // row phase
+    const size_t base = static_cast<size_t>(pair) * static_cast<size_t>(p.T_cap) * kD;
+    const long long t0 = static_cast<long long>(p.cmp_stride) * j;
+    float ak[8], av[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        ak[i] = av[i] = 0.f;
+    for (long long t = t0 + r0; t < t0 + p.cmp_len; t += 16) {
+        const size_t at = base + static_cast<size_t>(t) * kD + c * 8;
+        const uint4 kv = *reinterpret_cast<const uint4 *>(p.k_cache + at);
+        const uint4 vv = *reinterpret_cast<const uint4 *>(p.v_cache + at);
+        const __nv_bfloat162 *hk = reinterpret_cast<const __nv_bfloat162 *>(&kv);
+        const __nv_bfloat162 *hv = reinterpret_cast<const __nv_bfloat162 *>(&vv);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 fk = __bfloat1622float2(hk[i]);
+            const float2 fv = __bfloat1622float2(hv[i]);
+            ak[2 * i] += fk.x;
+            ak[2 * i + 1] += fk.y;
+            av[2 * i] += fv.x;
+            av[2 * i + 1] += fv.y;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        red[0][r0][c * 8 + i] = ak[i];
+        red[1][r0][c * 8 + i] = av[i];
+    }
+    __syncthreads();
+    const int x = threadIdx.x / kD, d = threadIdx.x % kD;   // x = 0: keys, 1: values
+    if (x < 2) {
+        float sum = 0.f;
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            sum += red[x][r][d];
+        uint16_t *dst = x == 0 ? p.khat : p.vhat;
+        dst[(static_cast<size_t>(pair) * p.n_rows_cap + j) * kD + d] =
+            __bfloat16_as_ushort(__float2bfloat16_rn(sum / static_cast<float>(p.cmp_len)));
+    }
+}
+
+}  // namespace
+
+extern "C" SPARSE_API int sparse_nsa_compress(const uint16_t *k_cache, const uint16_t *v_cache, long long T_cap,
+                                              int B, int H_kv, long long len_before, int n_new, int cmp_len,
+                                              int cmp_stride, uint16_t *khat, uint16_t *vhat, int n_rows_cap,
+                                              void *stream)
+{
+    using sp_host::aligned16;
+    using sp_host::fail;
+    const char *name = "sparse_nsa_compress";
+    if (!k_cache || !v_cache || !khat || !vhat)
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: null pointer", name);
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(khat) || !aligned16(vhat))
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: buffers must be 16-byte aligned", name);
+    if (B < 1 || H_kv < 1 || T_cap < 1 || len_before < 0 || n_new < 0 || n_rows_cap < 1 || cmp_stride < 1 ||
+        cmp_len < cmp_stride || cmp_len > 1024)
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: bad size (B=%d H_kv=%d n_new=%d l=%d s=%d)", name, B, H_kv, n_new,
+                    cmp_len, cmp_stride);
+    const long long len_after = len_before + n_new;
+    if (len_after > T_cap)
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: %lld tokens exceed T_cap=%lld", name, len_after, T_cap);
+    const long long w_before = compressed_rows(len_before, cmp_len, cmp_stride);
+    const long long w_after = compressed_rows(len_after, cmp_len, cmp_stride);
+    if (w_after > n_rows_cap)
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: %lld windows exceed n_rows_cap=%d", name, w_after, n_rows_cap);
+    const long long pairs = static_cast<long long>(B) * H_kv;
+    if (pairs > 65535 || w_after - w_before > INT_MAX)
+        return fail(SPARSE_ERR_UNSUPPORTED, "%s: too many pairs or windows", name);
+    if (w_after == w_before)
+        return SPARSE_OK;   // no window completed
+    CompressParams p{k_cache, v_cache, khat, vhat, T_cap, n_rows_cap, cmp_len, cmp_stride, static_cast<int>(w_before)};
+    dim3 grid(static_cast<unsigned>(w_after - w_before), static_cast<unsigned>(pairs));
+    {
+        sp_host::DeviceInfo dinfo;
+        int rc0 = sp_host::device_info(&dinfo);
+        static int configured[64];
+        if (rc0 == SPARSE_OK)
+            rc0 = sp_host::configure_kernel(reinterpret_cast<const void *>(compress_windows_kernel), 0, dinfo.device,
+                                            configured);
+        if (rc0 != SPARSE_OK)
+            return rc0;
+    }
+    compress_windows_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    return sp_host::cuda_status(cudaGetLastError(), name);
 }

@@ -1548,7 +1548,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int n_s = producer_fetch_slice(ps, pair, i0, min(ps.k_tot, i0 + per) - i0, lslot, llog, ctrl, lane);
         named_barrier_arrive(1, kThreads);   // the selected slice and its length are in shared memory
         if (lane == 0) {
-            if (pc.seq_len[b] > pc.pair_stride * kBlk)
+            if (compressed_rows(pc.seq_len[b], pc.cmp_len, pc.cmp_stride) > pc.pair_stride)
                 report(pc.status, SPARSE_ERR_BAD_INDEX);
             for (int it = pre; it < n_r + n_s && ok; ++it)
                 issue(it);
@@ -1801,7 +1801,7 @@ extern "C" SPARSE_API size_t sparse_decode_attn_nsa_workspace_size(int B, int H_
 
 extern "C" SPARSE_API int sparse_decode_attn_nsa(const uint16_t *Q, const uint16_t *k_cache, const uint16_t *v_cache,
                                                  long long T_cap, const uint16_t *khat, const uint16_t *vhat,
-                                                 int N_cap, const int *blk_idx, const int *count, int k_tot,
+                                                 int N_cap, int cmp_len, int cmp_stride, const int *blk_idx, const int *count, int k_tot,
                                                  const int *seq_len, int B, int H_q, int H_kv,
                                                  long long window_tokens, const float *gates, float scale,
                                                  uint16_t *O, void *workspace, size_t workspace_bytes, int n_split,
@@ -1823,6 +1823,9 @@ extern "C" SPARSE_API int sparse_decode_attn_nsa(const uint16_t *Q, const uint16
         return fail(SPARSE_ERR_UNSUPPORTED, "%s: T_cap or window_tokens too large", name);
     if (!isfinite(scale))
         return fail(SPARSE_ERR_INVALID_ARG, "%s: scale must be finite", name);
+    if (!(cmp_len == 0 && cmp_stride == 0) && !(cmp_stride >= 1 && cmp_stride <= cmp_len && cmp_len <= 1024))
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: cmp_len=%d cmp_stride=%d (0, 0 or 1 <= stride <= len <= 1024)",
+                    name, cmp_len, cmp_stride);
     if ((flags & ~(SPARSE_ATTN_BLOCKS_READY | SPARSE_NSA_BRANCH_GRID)) != 0u)
         return fail(SPARSE_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags);
     const int G = H_q / H_kv;
@@ -1893,6 +1896,8 @@ extern "C" SPARSE_API int sparse_decode_attn_nsa(const uint16_t *Q, const uint16
     np.br[2].range_mode = 2;
     np.br[2].k_tot = k_cmp;
     np.br[2].pair_stride = N_cap;
+    np.br[2].cmp_len = cmp_len;
+    np.br[2].cmp_stride = cmp_stride;
     np.gates = gates;
     np.part = part;
     np.arrivals = fused ? nullptr : static_cast<unsigned *>(workspace);

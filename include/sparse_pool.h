@@ -357,12 +357,17 @@ SPARSE_API int sparse_verify_attn_shared(const uint16_t *Q, const uint16_t *k_ca
  *   o^(s)  over the tokens of the selected blocks blk_idx[p][0 .. count[p])
  *          (sparse_decode_attn's table, logical block ids, no slot indirection);
  *   o^(w)  over the last window_tokens tokens [len - w, len), token-granular;
- *   o^(c)  over the compressed rows khat / vhat [p][0 .. N_b), N_b = ceil(len / 64),
- *          one row per block holding a token (sparse_pool_append_kv keeps them);
+ *   o^(c)  over the compressed rows khat / vhat [p][0 .. R): with cmp_len = cmp_stride
+ *          = 0 one row per 64-token block holding a token, R = ceil(len / 64)
+ *          (sparse_pool_append_kv keeps them); otherwise NSA's overlapping windows
+ *          [cmp_stride * j, cmp_stride * j + cmp_len), complete ones only,
+ *          R = floor((len - cmp_len) / cmp_stride) + 1 (sparse_nsa_compress keeps them);
  * a branch with no rows contributes zero.  The gates are inputs: NSA learns them.
  *   Q                 [B][H_q][128] bf16.
  *   k_cache, v_cache  [B][H_kv][T_cap][128] bf16.
- *   khat, vhat        [B][H_kv][N_cap][128] bf16 compressed rows, N_cap >= N_b.
+ *   khat, vhat        [B][H_kv][N_cap][128] bf16 compressed rows, N_cap >= R (a longer
+ *                     length is reported and its rows clipped).
+ *   cmp_len, cmp_stride  0, 0 or 1 <= cmp_stride <= cmp_len <= 1024 (above).
  *   blk_idx, count    [B*H_kv][k_tot] int32 and [B*H_kv] int32, as sparse_select_topk
  *                     writes them; ids outside [0, T_cap / 64) are skipped and reported.
  *   seq_len           [B] int32 tokens present.
@@ -389,11 +394,48 @@ SPARSE_API int sparse_verify_attn_shared(const uint16_t *Q, const uint16_t *k_ca
 SPARSE_API int sparse_decode_attn_nsa(const uint16_t *Q, const uint16_t *k_cache,
                                       const uint16_t *v_cache, long long T_cap,
                                       const uint16_t *khat, const uint16_t *vhat, int N_cap,
-                                      const int *blk_idx, const int *count, int k_tot,
+                                      int cmp_len, int cmp_stride, const int *blk_idx, const int *count, int k_tot,
                                       const int *seq_len, int B, int H_q, int H_kv,
                                       long long window_tokens, const float *gates, float scale,
                                       uint16_t *O, void *workspace, size_t workspace_bytes,
                                       int n_split, unsigned flags, int *status, void *stream);
+
+/*
+ * sparse_nsa_compress -- NSA's overlapping compression ([SparDA] background eq.(4) with
+ * the inference kernel 32 and stride 16 of its §4.4; [SSV] "NSA" branch 1): after
+ * tokens [len_before, len_before + n_new) are in the caches, writes the rows of every
+ * window they complete,
+ *     khat[p][j] = bf16(mean of k_cache[p][s*j .. s*j + l)),  vhat likewise,
+ * for W(len_before) <= j < W(len_before + n_new), W(len) = floor((len - l) / s) + 1
+ * (0 below l).  Call it after the append of those tokens; n_new = 0 writes nothing.
+ *   k_cache, v_cache  [B][H_kv][T_cap][128] bf16, read.
+ *   khat, vhat        [B][H_kv][n_rows_cap][128] bf16, written (rows j only).
+ *   cmp_len l, cmp_stride s   1 <= s <= l <= 1024.
+ */
+SPARSE_API int sparse_nsa_compress(const uint16_t *k_cache, const uint16_t *v_cache, long long T_cap,
+                                   int B, int H_kv, long long len_before, int n_new, int cmp_len,
+                                   int cmp_stride, uint16_t *khat, uint16_t *vhat, int n_rows_cap,
+                                   void *stream);
+
+/*
+ * sparse_nsa_select -- NSA's routing over its compressed keys ([SSV] "NSA three-branch
+ * math" steps 1-2; the per-head softmax summed over the GQA group and the max-pooling
+ * onto the selection grid of [SparDA] §4.3-§4.4 / InfLLM-V2):
+ *     a^h_j = scale * q_h . khat_j   (j < R compressed rows, as sparse_decode_attn_nsa),
+ *     p_j   = sum_h softmax_j(a^h),
+ *     s_b   = max { p_j : row j's tokens meet block b's [64b, 64b + 64) }, 0 if none,
+ * then B_init ∪ B_local ∪ top-k of the 64-token blocks b < N_b = ceil(len / 64) as
+ * sparse_select_topk writes them (ties to the lower block).  The scores are computed on
+ * the bf16 tensor cores from the bf16 rows, exactly as the compressed branch scores
+ * them; with cmp_len = cmp_stride = 0 the rows are the blocks themselves.
+ *   Q           [B][H_q][128] bf16;  khat [B][H_kv][n_rows_cap][128] bf16.
+ *   idx_out     [B][H_kv][k_tot] int32;  count_out [B][H_kv] int32.
+ * G = H_q / H_kv <= 16.
+ */
+SPARSE_API int sparse_nsa_select(const uint16_t *Q, const uint16_t *khat, int n_rows_cap, int cmp_len,
+                                 int cmp_stride, const int *seq_len, int B, int H_q, int H_kv,
+                                 float scale, int n_init, int n_local, int k, int *idx_out,
+                                 int *count_out, int k_tot, int *status, void *stream);
 
 /* sparse_decode_attn_nsa: run the branch grid (see `flags`) even when G <= 8. */
 #define SPARSE_NSA_BRANCH_GRID 4u

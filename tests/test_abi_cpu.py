@@ -186,9 +186,9 @@ def test_append_kv_rejects_bad_arguments(lib):
 
 def test_nsa_rejects_bad_arguments(lib):
     f = lib.sparse_decode_attn_nsa
-    # Q, K, V, T_cap, khat, vhat, N_cap, idx, count, k_tot, seq_len, B, H_q, H_kv, w, gates, scale, O, ws,
-    # ws_bytes, n_split, flags, status, stream
-    ok = [FAKE, FAKE, FAKE, 4096, FAKE, FAKE, 64, FAKE, FAKE, 8, FAKE, 1, 8, 1, 512, FAKE, 0.0, FAKE, FAKE,
+    # Q, K, V, T_cap, khat, vhat, N_cap, cmp_len, cmp_stride, idx, count, k_tot, seq_len, B, H_q, H_kv, w,
+    # gates, scale, O, ws, ws_bytes, n_split, flags, status, stream
+    ok = [FAKE, FAKE, FAKE, 4096, FAKE, FAKE, 64, 0, 0, FAKE, FAKE, 8, FAKE, 1, 8, 1, 512, FAKE, 0.0, FAKE, FAKE,
           1 << 20, 0, 0, None, None]
 
     def call(**kw):
@@ -198,15 +198,51 @@ def test_nsa_rejects_bad_arguments(lib):
         return f(*a)
 
     assert call(a4=None) == binding.SPARSE_ERR_INVALID_ARG            # no khat
-    assert call(a18=None, a21=binding.SPARSE_NSA_BRANCH_GRID) == binding.SPARSE_ERR_INVALID_ARG  # no workspace
-    assert call(a18=None, a12=16) == binding.SPARSE_ERR_INVALID_ARG   # G = 16 needs the workspace
+    assert call(a20=None, a23=binding.SPARSE_NSA_BRANCH_GRID) == binding.SPARSE_ERR_INVALID_ARG  # no workspace
+    assert call(a20=None, a14=16) == binding.SPARSE_ERR_INVALID_ARG   # G = 16 needs the workspace
     assert call(a5=ODD) == binding.SPARSE_ERR_INVALID_ARG             # misaligned vhat
-    assert call(a12=12, a13=8) == binding.SPARSE_ERR_INVALID_ARG      # H_q not a multiple of H_kv
-    assert call(a14=-1) == binding.SPARSE_ERR_INVALID_ARG             # negative window
-    assert call(a14=5000) == binding.SPARSE_ERR_UNSUPPORTED           # window beyond T_cap
-    assert call(a12=32, a13=1) == binding.SPARSE_ERR_UNSUPPORTED      # G = 32
-    assert call(a19=16, a12=16) == binding.SPARSE_ERR_INVALID_ARG     # workspace too small
-    assert call(a21=8) == binding.SPARSE_ERR_INVALID_ARG              # unknown flag
-    assert call(a16=float("nan")) == binding.SPARSE_ERR_INVALID_ARG   # scale
+    assert call(a14=12, a15=8) == binding.SPARSE_ERR_INVALID_ARG      # H_q not a multiple of H_kv
+    assert call(a16=-1) == binding.SPARSE_ERR_INVALID_ARG             # negative window
+    assert call(a16=5000) == binding.SPARSE_ERR_UNSUPPORTED           # window beyond T_cap
+    assert call(a14=32, a15=1) == binding.SPARSE_ERR_UNSUPPORTED      # G = 32
+    assert call(a21=16, a14=16) == binding.SPARSE_ERR_INVALID_ARG     # workspace too small
+    assert call(a23=8) == binding.SPARSE_ERR_INVALID_ARG              # unknown flag
+    assert call(a18=float("nan")) == binding.SPARSE_ERR_INVALID_ARG   # scale
+    assert call(a7=16, a8=32) == binding.SPARSE_ERR_INVALID_ARG       # stride above the kernel
+    assert call(a7=32, a8=0) == binding.SPARSE_ERR_INVALID_ARG        # zero stride
     assert lib.sparse_decode_attn_nsa_workspace_size(0, 8, 1) == 0
     assert lib.sparse_decode_attn_nsa_workspace_size(8, 64, 8) == 256 + 3 * 8 * 64 * 128 * 4
+
+
+def test_nsa_compress_and_select_reject_bad_arguments(lib):
+    f = lib.sparse_nsa_compress
+    # k_cache, v_cache, T_cap, B, H_kv, len_before, n_new, l, s, khat, vhat, n_rows_cap, stream
+    ok = [FAKE, FAKE, 1024, 1, 1, 0, 100, 32, 16, FAKE, FAKE, 64, None]
+
+    def call_c(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+
+    assert call_c(a9=None) == binding.SPARSE_ERR_INVALID_ARG          # no khat
+    assert call_c(a10=ODD) == binding.SPARSE_ERR_INVALID_ARG          # misaligned vhat
+    assert call_c(a7=8) == binding.SPARSE_ERR_INVALID_ARG             # kernel below the stride
+    assert call_c(a6=2000) == binding.SPARSE_ERR_INVALID_ARG          # beyond T_cap
+    assert call_c(a11=3) == binding.SPARSE_ERR_INVALID_ARG            # more windows than rows
+    assert call_c(a5=0, a6=20) == binding.SPARSE_OK                   # no window completes: nothing to do
+    g = lib.sparse_nsa_select
+    # Q, khat, n_rows_cap, l, s, seq_len, B, H_q, H_kv, scale, n_init, n_local, k, idx, count, k_tot, status, stream
+    ok2 = [FAKE, FAKE, 64, 32, 16, FAKE, 1, 8, 1, 0.0, 1, 2, 4, FAKE, FAKE, 7, None, None]
+
+    def call_s(**kw):
+        a = list(ok2)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return g(*a)
+
+    assert call_s(a1=None) == binding.SPARSE_ERR_INVALID_ARG          # no khat
+    assert call_s(a15=6) == binding.SPARSE_ERR_INVALID_ARG            # k_tot too small
+    assert call_s(a3=16, a4=32) == binding.SPARSE_ERR_INVALID_ARG     # stride above the kernel
+    assert call_s(a7=64, a8=2) == binding.SPARSE_ERR_UNSUPPORTED      # G = 32
+    assert call_s(a9=-1.0) == binding.SPARSE_ERR_INVALID_ARG          # negative scale

@@ -297,3 +297,228 @@ def test_nsa_full_size_sampled_pairs():
                          idx_np[p:p + 1], cnt_np[p:p + 1], lens, window,
                          gates_np[b, g * G:(g + 1) * G].reshape(1, G, 3))
         assert_attn_close(O[b, g * G:(g + 1) * G], ref, f"nsa 128k pair {p}")
+
+
+# ----------------------------------------------------------------------------- overlapping compression
+
+
+def _round_rows(x64: np.ndarray) -> np.ndarray:
+    return _to_bf16_bits(x64)
+
+
+@pytest.mark.parametrize("cmp", [(32, 16), (64, 32), (16, 16), (48, 16)])
+def test_compress_windows_match_the_oracle(cmp):
+    """sparse_nsa_compress, fed in chunks: each completed window's row is the mean of
+    its tokens rounded once to bf16 (within one bf16 rounding of the fp64 mean, nearly
+    always equal to its rounding); rows of incomplete windows stay untouched."""
+    l, s = cmp
+    B, H_kv, T_cap = 2, 3, 700
+    R = (T_cap - l) // s + 1
+    K = wl.randn_bf16((B, H_kv, T_cap, D), 301, "cuda")
+    V = wl.randn_bf16((B, H_kv, T_cap, D), 302, "cuda")
+    khat = torch.full((B, H_kv, R + 2, D), 3.0, dtype=torch.bfloat16, device="cuda")
+    vhat = torch.full_like(khat, 3.0)
+    t = 0
+    for n in (100, 1, 15, 17, 200, 0, 300):
+        n = min(n, 650 - t)
+        binding.sparse_nsa_compress(K, V, khat, vhat, t, n, cmp=cmp)
+        t += n
+    torch.cuda.synchronize()
+    P = B * H_kv
+    W = (t - l) // s + 1
+    for X, hat in ((K, khat), (V, vhat)):
+        ref = oracle.pool_windows(bits(X).reshape(P, T_cap, D), np.full(P, t), l, s, R + 2)
+        got = _bits_to_f64(bits(hat).reshape(P, R + 2, D))
+        assert np.all(np.abs(got[:, :W] - ref[:, :W]) <= 2.0 ** -8 * np.abs(ref[:, :W]) + 1e-7)
+        same = np.mean(bits(hat).reshape(P, R + 2, D)[:, :W] == _round_rows(ref[:, :W]))
+        assert same > 0.999, same
+        assert np.all(got[:, W:] == 3.0)
+
+
+def _route_case(B, H_q, H_kv, T_cap, lens_b, cmp, seed, n_rows=None):
+    l, s = cmp
+    P = B * H_kv
+    G = H_q // H_kv
+    K = wl.randn_bf16((B, H_kv, T_cap, D), seed, "cuda")
+    Q = wl.randn_bf16((B, H_q, D), seed + 1, "cuda")
+    lens_p = np.repeat(np.asarray(lens_b, np.int64), H_kv)
+    if l == 0:
+        R = n_rows or (T_cap + BLK - 1) // BLK
+        rows64 = oracle.pool(bits(K).reshape(P, T_cap, D), lens_p, R)
+    else:
+        R = n_rows or (T_cap - l) // s + 1
+        rows64 = oracle.pool_windows(bits(K).reshape(P, T_cap, D), lens_p, l, s, R)
+    kb = _round_rows(rows64)
+    khat = torch.from_numpy(kb.view(np.int16)).view(torch.bfloat16).cuda().view(B, H_kv, R, D)
+    return dict(K=K, Q=Q, Qb=bits(Q).reshape(P, G, D), lens_p=lens_p, kb=kb, khat=khat, R=R,
+                seq=torch.tensor(lens_b, dtype=torch.int32, device="cuda"))
+
+
+def _assert_route_matches(idx_g, cnt_g, idx_r, cnt_r, sc, lens, n_init, n_local, k, rel=1e-4):
+    """Identical lists except blocks whose oracle score lies within rel * s_k of the
+    oracle's k-th candidate score (fp32 tensor-core scores against fp64)."""
+    idx_g = idx_g.cpu().numpy().reshape(idx_r.shape)
+    cnt_g = cnt_g.cpu().numpy().reshape(cnt_r.shape)
+    exempt = 0
+    for p in range(idx_r.shape[0]):
+        assert cnt_g[p] == cnt_r[p], (p, cnt_g[p], cnt_r[p])
+        c = cnt_r[p]
+        g = idx_g[p, :c]
+        assert np.all(np.diff(g) > 0) and np.all(idx_g[p, c:] == -1)
+        if np.array_equal(g, idx_r[p, :c]):
+            continue
+        nb = (int(lens[p]) + BLK - 1) // BLK
+        cand = [j for j in range(nb) if n_init <= j < nb - n_local]
+        kth = sorted((sc[p, j] for j in cand), reverse=True)[k - 1]
+        for j in set(g.tolist()) ^ set(idx_r[p, :c].tolist()):
+            assert j in cand and abs(sc[p, j] - kth) <= rel * abs(kth), (p, j, sc[p, j], kth)
+        exempt += 1
+    return exempt
+
+
+@pytest.mark.parametrize("cmp", [(32, 16), (0, 0), (64, 32)])
+@pytest.mark.parametrize("H_q,H_kv", [(16, 4), (64, 8), (32, 2), (3, 3)])
+@pytest.mark.parametrize("k", [0, 1, 7, 40])
+def test_nsa_select_matches_oracle(cmp, H_q, H_kv, k):
+    B, T_cap = 2, 60 * BLK
+    lens_b = [60 * BLK, 37 * BLK + 23]
+    c = _route_case(B, H_q, H_kv, T_cap, lens_b, cmp, seed=400 + H_q + k)
+    n_init, n_local = 1, 2
+    k_tot = n_init + n_local + k
+    idx = torch.full((B, H_kv, k_tot), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((B, H_kv), -7, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.sparse_nsa_select(c["Q"], c["khat"], c["seq"], n_init, n_local, k, idx, cnt, cmp=cmp, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    kr = _bits_to_f64(c["kb"])
+    if cmp[0] == 0:
+        ir, cr, sc = oracle.select_heads(c["Qb"], kr, c["lens_p"], n_init, n_local, k, k_tot)
+    else:
+        ir, cr, sc = oracle.select_windows(c["Qb"], kr, c["lens_p"], cmp[0], cmp[1], n_init, n_local, k, k_tot,
+                                           n_blocks_cap=60)
+    _assert_route_matches(idx, cnt, ir, cr, sc, c["lens_p"], n_init, n_local, max(k, 1))
+
+
+def test_nsa_select_short_and_empty_lengths():
+    """No complete window (every block scores 0: ties to the lower index), one token,
+    an empty sequence, n_local = 0."""
+    B, H_q, H_kv, T_cap = 4, 8, 2, 20 * BLK
+    lens_b = [0, 1, 40, 20 * BLK - 1]
+    c = _route_case(B, H_q, H_kv, T_cap, lens_b, (32, 16), seed=430)
+    k, n_init, n_local = 3, 0, 0
+    idx = torch.full((B, H_kv, k), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((B, H_kv), -7, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.sparse_nsa_select(c["Q"], c["khat"], c["seq"], n_init, n_local, k, idx, cnt, cmp=(32, 16), status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    ir, cr, sc = oracle.select_windows(c["Qb"], _bits_to_f64(c["kb"]), c["lens_p"], 32, 16, n_init, n_local, k, k,
+                                       n_blocks_cap=20)
+    _assert_route_matches(idx, cnt, ir, cr, sc, c["lens_p"], n_init, n_local, k)
+
+
+@pytest.mark.parametrize("flags", [0, binding.SPARSE_NSA_BRANCH_GRID])
+@pytest.mark.parametrize("H_q,H_kv", [(16, 4), (32, 2)])
+def test_nsa_over_windows_matches_oracle(flags, H_q, H_kv):
+    B, T_cap, k_cap = 2, 40 * BLK, 9
+    lens_b = [40 * BLK, 27 * BLK + 13]
+    l, s = 32, 16
+    R = (T_cap - l) // s + 1
+    c = _case(B, H_q, H_kv, T_cap, lens_b, k_cap, R, seed=500 + H_q)
+    P = B * H_kv
+    kb = _round_rows(oracle.pool_windows(c["Kb"], c["lens_p"], l, s, R))
+    vb = _round_rows(oracle.pool_windows(c["Vb"], c["lens_p"], l, s, R))
+    dev = lambda x: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda().view(B, H_kv, R, D)
+    O = torch.full((B, H_q, D), 7.0, dtype=torch.bfloat16, device="cuda")
+    ws = binding.nsa_workspace(B, H_q, H_kv)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.sparse_decode_attn_nsa(c["Q"], c["K"], c["V"], dev(kb), dev(vb), c["idx"], c["cnt"], c["seq"], 300,
+                                   c["gates"], O, ws, flags=flags, status=status, cmp=(l, s))
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    ref = oracle.nsa(c["Qb"], c["Kb"], c["Vb"], _bits_to_f64(kb), _bits_to_f64(vb), c["idx_np"], c["cnt_np"],
+                     c["lens_p"], 300, c["gates_np"].reshape(P, -1, 3), cmp=(l, s))
+    assert_attn_close(O, ref, "nsa windows")
+
+
+def test_nsa_windows_chain_append_compress_route_attend():
+    """The decode chain on the GPU: append, compress the completed windows, route,
+    three-branch attention; against the oracle's own chain (its fp64 windows and its
+    selection).  Pairs whose selection differs near a tie are skipped for the output."""
+    B, H_q, H_kv, T_cap = 2, 32, 4, 48 * BLK
+    l, s = 32, 16
+    R = (T_cap - l) // s + 1
+    lens_b = [48 * BLK - 9, 48 * BLK - 9]
+    total = lens_b[0]
+    Kall = wl.randn_bf16((B, H_kv, total, D), 611, "cuda")
+    Vall = wl.randn_bf16((B, H_kv, total, D), 612, "cuda")
+    Q = wl.randn_bf16((B, H_q, D), 613, "cuda")
+    kc = torch.zeros((B, H_kv, T_cap, D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    ktil = torch.zeros((B, H_kv, 48, D), dtype=torch.float32, device="cuda")
+    khat = torch.zeros((B, H_kv, R, D), dtype=torch.bfloat16, device="cuda")
+    vhat = torch.zeros_like(khat)
+    t = 0
+    for n in (total - 40, 7, 1, 32):
+        binding.sparse_pool_append(kc, vc, ktil, Kall[:, :, t:t + n].contiguous(), Vall[:, :, t:t + n].contiguous(), t)
+        binding.sparse_nsa_compress(kc, vc, khat, vhat, t, n, cmp=(l, s))
+        t += n
+    assert t == total
+    n_init, n_local, k = 1, 2, 9
+    k_tot = n_init + n_local + k
+    seq = torch.tensor(lens_b, dtype=torch.int32, device="cuda")
+    idx = torch.empty((B, H_kv, k_tot), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((B, H_kv), dtype=torch.int32, device="cuda")
+    gates_np = np.random.default_rng(614).uniform(0, 1, (B, H_q, 3))
+    gates = torch.from_numpy(gates_np.astype(np.float32)).cuda()
+    O = torch.empty((B, H_q, D), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.sparse_nsa_select(Q, khat, seq, n_init, n_local, k, idx, cnt, cmp=(l, s), status=status)
+    binding.sparse_decode_attn_nsa(Q, kc, vc, khat, vhat, idx, cnt, seq, 256, gates, O, None, status=status,
+                                   cmp=(l, s))
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    P = B * H_kv
+    G = H_q // H_kv
+    Kb, Vb, Qb = bits(kc).reshape(P, T_cap, D), bits(vc).reshape(P, T_cap, D), bits(Q).reshape(P, G, D)
+    lens_p = np.repeat(np.asarray(lens_b, np.int64), H_kv)
+    kr = oracle.pool_windows(Kb, lens_p, l, s, R)
+    vr = oracle.pool_windows(Vb, lens_p, l, s, R)
+    ir, cr, sc = oracle.select_windows(Qb, kr, lens_p, l, s, n_init, n_local, k, k_tot, n_blocks_cap=48)
+    exempt = _assert_route_matches(idx, cnt, ir, cr, sc, lens_p, n_init, n_local, k, rel=2e-2)
+    ref = oracle.nsa(Qb, Kb, Vb, kr, vr, ir, cr, lens_p, 256, gates_np.reshape(P, G, 3), cmp=(l, s))
+    same = [p for p in range(P) if np.array_equal(idx.cpu().numpy().reshape(P, k_tot)[p], ir[p])]
+    assert len(same) >= P - exempt and len(same) > 0
+    Og = O.view(B, H_kv, G, D).reshape(P, G, D)
+    assert_attn_close(Og[same], ref[same], "nsa windows chain")
+
+
+def test_nsa_select_full_size_sampled_pairs():
+    """NSA routing on the 128K decode shape with 32/16 windows (8191 rows per pair) in
+    the launch configuration of the bench; a sample of pairs checked by the oracle."""
+    shape = wl.DECODE_128K
+    B, H_q, H_kv, T = shape.B, shape.H_q, shape.H_kv, shape.T
+    l, s = 32, 16
+    R = (T - l) // s + 1
+    P = B * H_kv
+    G = H_q // H_kv
+    rng = np.random.default_rng(931)
+    kb = rng.standard_normal((P, R, D)).astype(np.float32) * 0.125
+    kb = wl.bf16_bits(torch.from_numpy(kb).to(torch.bfloat16))
+    khat = torch.from_numpy(kb.view(np.int16)).view(torch.bfloat16).cuda().view(B, H_kv, R, D)
+    Q = wl.randn_bf16((B, H_q, D), 932, "cuda")
+    seq = torch.full((B,), T, dtype=torch.int32, device="cuda")
+    k_tot = shape.n_init + shape.n_local + shape.k
+    idx = torch.empty((B, H_kv, k_tot), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((B, H_kv), dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.sparse_nsa_select(Q, khat, seq, shape.n_init, shape.n_local, shape.k, idx, cnt, cmp=(l, s), status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    Qb = bits(Q).reshape(P, G, D)
+    sample = [0, 13, 38, P - 1]
+    ir, cr, sc = oracle.select_windows(Qb[sample], _bits_to_f64(kb[sample]), np.full(len(sample), T), l, s,
+                                       shape.n_init, shape.n_local, shape.k, k_tot, n_blocks_cap=shape.N_b)
+    _assert_route_matches(idx.view(P, k_tot)[sample], cnt.view(P)[sample], ir, cr, sc, np.full(len(sample), T),
+                          shape.n_init, shape.n_local, shape.k)
