@@ -15,6 +15,8 @@ What each routine follows on the pages is stated in ``oracle.c``:
 * ``attn``    -- SparDA notes, eq.(7), scale 1/sqrt(d) from the SSV notes' NSA step 3.
 * ``verify``  -- SSV notes, mechanism 1, mode A (per-query sets plus window).
 * ``gather``  -- SparDA notes, §4.5: staging is a plain copy.
+* ``prefill_select`` -- SparDA notes, eq.(16): the Forecast selection of every prefill
+  position over the blocks it can see.
 * ``pool_windows`` / ``select_windows`` / ``nsa(..., cmp=(l, s))`` -- eq.(4) with an
   overlapping kernel and stride, NSA routing max-pooled onto the 64-token blocks, and
   NSA's compressed branch over those windows.
@@ -75,6 +77,8 @@ def load_library(path: str):
     lib.oracle_pool_windows.restype = i32
     lib.oracle_select_windows.argtypes = [P, i32, P, i32, i32, P, i32, i32, f64, i32, i32, i32, i32, P, P, P, i32]
     lib.oracle_select_windows.restype = i32
+    lib.oracle_prefill_select.argtypes = [P, i64, P, i32, i32, P, P, i32, i32, i32, i32, i32, P, P]
+    lib.oracle_prefill_select.restype = i32
     return lib
 
 
@@ -163,6 +167,29 @@ def select_heads(Q, ktil, lens, n_init: int, n_local: int, k: int, k_tot: int | 
     if rc != 0:
         raise ValueError("oracle_select_heads: a pair needs more than k_tot or n_blocks_cap entries")
     return idx, count, scores
+
+
+def prefill_select(F, ktil, lens, n_init: int, n_local: int, k: int, k_tot: int | None = None, rows=None):
+    """Forecast selection of every prefill position (or of the positions in ``rows``):
+    F [P][T][128] bf16 bits, ktil [P][N][128].  Returns (idx [P][R][k_tot] int32,
+    count [P][R] int32) with R = T or len(rows); rows at or past a pair's length are -1 / -1."""
+    F = _u16(F)
+    ktil = np.ascontiguousarray(ktil, dtype=np.float64)
+    lens = _i64(lens)
+    P, T_cap, d = F.shape
+    n_cap = ktil.shape[1]
+    assert d == D and ktil.shape[0] == P and lens.shape == (P,)
+    if k_tot is None:
+        k_tot = n_init + n_local + k
+    rr = None if rows is None else _i32(rows)
+    R = T_cap if rr is None else len(rr)
+    idx = np.full((P, R, k_tot), -1, dtype=np.int32)
+    count = np.full((P, R), -1, dtype=np.int32)
+    rc = _load().oracle_prefill_select(_ptr(F), T_cap, _ptr(ktil), n_cap, P, _ptr(lens), _ptr(rr), R, n_init, n_local,
+                                       k, k_tot, _ptr(idx), _ptr(count))
+    if rc != 0:
+        raise ValueError("oracle_prefill_select: a position needs more than k_tot or n_blocks_cap entries")
+    return idx, count
 
 
 def attn(Q, K, V, blocks, count, lens, scale: float | None = None):

@@ -42,6 +42,8 @@
  *                  ([SparDA] §4.4: scores on a finer grid are max-pooled onto the
  *                  coarse one), then the top-k of oracle_select.
  *   oracle_nsa_windows  oracle_nsa with the compressed branch over the windows.
+ *   oracle_prefill_select  [SparDA] eq.(16): the Forecast selection of every prefill
+ *                  position, each over the blocks it can see (causal).
  *   oracle_gather  [SparDA] §4.5: staging selected blocks is a plain copy.
  *
  * Readings where the pages are silent are stated at each routine.
@@ -415,6 +417,59 @@ int oracle_select_windows(const uint16_t *Q, int G, const double *kcmp, int n_ro
         free(sb);
         free(pj);
         free(a);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * Prefill selection, [SparDA] §4.3 eq.(16) (the Forecast indexer's prefill cost
+ * H_kv * T * N_b * d: every position scores the compressed keys) with the selection of
+ * eq.(6) / Alg.1 step 2 per position.  Position t of pair p (its Forecast vector
+ * F[p][t]) sees the blocks holding tokens 0..t, N_t = floor(t / 64) + 1, and takes
+ * B_init ∪ B_local ∪ top-k among them exactly as oracle_select does for a sequence of
+ * t + 1 tokens: s_j = F[p][t] . ktil[p][j].  Reading: ktil is the prefill's pooled keys
+ * (the block holding t may include later tokens, but with n_local >= 1 it is a local
+ * block and its score is never used).
+ *   F     [n_pairs][T_cap][D] bf16 bits;  ktil [n_pairs][n_blocks_cap][D].
+ *   rows  the positions to select for (n_rows of them, each < len[p]); NULL = all t < len[p].
+ *   idx   [n_pairs][n_rows or T_cap][k_tot];  count [n_pairs][n_rows or T_cap].
+ * Rows of positions at or past len[p] are left untouched.  Returns -1 when a position
+ * needs more than k_tot entries or more than n_blocks_cap blocks.
+ */
+int oracle_prefill_select(const uint16_t *F, long long T_cap, const double *ktil, int n_blocks_cap, int n_pairs,
+                          const long long *len, const int *rows, int n_rows, int n_init, int n_local, int k,
+                          int k_tot, int *idx, int *count)
+{
+    int bad = 0;
+    const long long per_pair = rows ? n_rows : T_cap;
+#pragma omp parallel for collapse(2) schedule(dynamic, 64) reduction(| : bad)
+    for (int p = 0; p < n_pairs; ++p) {
+        for (long long r = 0; r < per_pair; ++r) {
+            const long long t = rows ? rows[r] : r;
+            if (t < 0 || t >= len[p])
+                continue;
+            const int nb = (int)(t / BLK) + 1;
+            int *out = idx + ((size_t)p * per_pair + r) * k_tot;
+            int *cnt = count + (size_t)p * per_pair + r;
+            if (nb > n_blocks_cap) {
+                bad |= 1;
+                *cnt = 0;
+                continue;
+            }
+            double Fp[D];
+            for (int d = 0; d < D; ++d)
+                Fp[d] = bf16_value(F[((size_t)p * T_cap + t) * D + d]);
+            double *sc = (double *)malloc(sizeof(double) * (size_t)nb);
+            for (int j = 0; j < nb; ++j) {
+                const double *kj = ktil + ((size_t)p * n_blocks_cap + j) * D;
+                double acc = 0.0;
+                for (int d = 0; d < D; ++d)
+                    acc += Fp[d] * kj[d];
+                sc[j] = acc;
+            }
+            bad |= select_from_scores(sc, nb, n_init, n_local, k, k_tot, out, cnt);
+            free(sc);
+        }
     }
     return bad ? -1 : 0;
 }

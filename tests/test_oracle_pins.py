@@ -607,6 +607,67 @@ def test_nsa_windows_leave_the_selected_and_window_branches_alone():
     assert np.allclose(O, ref, rtol=1e-13, atol=1e-14)
 
 
+# ----------------------------------------------------------------------------- prefill selection
+
+
+def _prefill_brute(Fv, kt, lens, n_init, n_local, k, k_tot):
+    P, T, _ = Fv.shape
+    idx = np.full((P, T, k_tot), -1, np.int32)
+    cnt = np.full((P, T), -1, np.int32)
+    for p in range(P):
+        for t in range(int(lens[p])):
+            nb = t // BLK + 1
+            sc = kt[p, :nb] @ Fv[p, t]
+            chosen = set(range(min(n_init, nb))) | set(range(max(nb - n_local, 0), nb))
+            cand = [j for j in range(nb) if j not in chosen]
+            chosen |= set(sorted(cand, key=lambda j: (-sc[j], j))[:k])
+            sel = sorted(chosen)
+            cnt[p, t] = len(sel)
+            idx[p, t, :len(sel)] = sel
+    return idx, cnt
+
+
+def test_prefill_select_matches_brute_force_per_position():
+    P, T, N = 2, 64 * 9 + 17, 10
+    F = rand_bits((P, T, D), 91)
+    kt = np.random.default_rng(92).standard_normal((P, N, D))
+    lens = np.array([T, 64 * 5 + 3], np.int64)
+    for n_init, n_local, k in ((1, 2, 3), (0, 1, 1), (2, 1, 5)):
+        idx, cnt = oracle.prefill_select(F, kt, lens, n_init, n_local, k)
+        bi, bc = _prefill_brute(values(F), kt, lens, n_init, n_local, k, n_init + n_local + k)
+        assert np.array_equal(cnt, bc) and np.array_equal(idx, bi), (n_init, n_local, k)
+
+
+def test_prefill_select_is_causal_and_matches_a_decode_of_the_prefix():
+    """Row t depends only on the keys of blocks <= t // 64; with unit Forecast vectors
+    the ranking is the closed-form order of one key dimension."""
+    P, T, N = 1, 64 * 6, 6
+    Fz = np.zeros((P, T, D), np.float32)
+    Fz[:, :, 5] = 1.0
+    F = bits(Fz)
+    kt = np.zeros((P, N, D))
+    kt[0, :, 5] = [0.5, 3.0, -1.0, 3.0, 2.0, 9.0]   # ties between blocks 1 and 3
+    idx, cnt = oracle.prefill_select(F, kt, [T], 0, 1, 2)
+    assert list(idx[0, 64 * 4 + 7, :cnt[0, 64 * 4 + 7]]) == [1, 3, 4]     # blocks 0..3 candidates, 4 local
+    assert list(idx[0, 64 * 5 + 1, :cnt[0, 64 * 5 + 1]]) == [1, 3, 5]     # block 4 (2.0) below the tie pair
+    kt2 = kt.copy()
+    kt2[0, 5, 5] = -50.0   # a later block changes nothing for earlier rows
+    idx2, _ = oracle.prefill_select(F, kt2, [T], 0, 1, 2)
+    assert np.array_equal(idx[0, :320], idx2[0, :320])
+
+
+def test_prefill_select_sampled_rows_equal_the_full_rows():
+    P, T, N = 2, 500, 8
+    F = rand_bits((P, T, D), 93)
+    kt = np.random.default_rng(94).standard_normal((P, N, D))
+    full_i, full_c = oracle.prefill_select(F, kt, [T, 333], 1, 2, 2)
+    rows = [0, 64, 65, 200, 332, 499]
+    si, sc = oracle.prefill_select(F, kt, [T, 333], 1, 2, 2, rows=rows)
+    for r, t in enumerate(rows):
+        assert np.array_equal(si[0, r], full_i[0, t]) and sc[0, r] == full_c[0, t]
+    assert sc[1, rows.index(499)] == -1   # past the second pair's length
+
+
 # ----------------------------------------------------------------------------- mutants
 
 MUTANTS = [
@@ -651,6 +712,11 @@ MUTANTS = [
     # the NSA window form attends over one row per block instead of the windows
     ("int nrows = cmp_len > 0 ? windows_of(len[p], cmp_len, cmp_stride) : nb;",
      "int nrows = cmp_len > 0 ? (nb < windows_of(len[p], cmp_len, cmp_stride) ? nb : windows_of(len[p], cmp_len, cmp_stride) - 1) : nb;"),
+    # a prefill position sees one block too many (the block after its own)
+    ("const int nb = (int)(t / BLK) + 1;", "const int nb = (int)(t / BLK) + 1 + (t % BLK == BLK - 1);"),
+    # a prefill position reads the previous position's Forecast vector
+    ("Fp[d] = bf16_value(F[((size_t)p * T_cap + t) * D + d]);",
+     "Fp[d] = bf16_value(F[((size_t)p * T_cap + (t > 0 ? t - 1 : 0)) * D + d]);"),
     # mode B takes the group's last query as its representative
     ("const int *Ia = shared ? I + (((size_t)b * H_kv + g) * N_q + q0) * n_sel : Iq;",
      "const int *Ia = shared ? I + (((size_t)b * H_kv + g) * N_q + (q0 + C - 1 < N_q ? q0 + C - 1 : N_q - 1)) * n_sel : Iq;"),
@@ -676,6 +742,8 @@ PIN_TESTS = [
     test_select_windows_with_block_windows_is_the_multi_head_selection,
     test_nsa_windows_compressed_branch_is_sdpa_over_the_complete_windows,
     test_nsa_windows_leave_the_selected_and_window_branches_alone,
+    test_prefill_select_matches_brute_force_per_position, test_prefill_select_is_causal_and_matches_a_decode_of_the_prefix,
+    test_prefill_select_sampled_rows_equal_the_full_rows,
 ]
 
 
