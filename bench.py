@@ -89,7 +89,7 @@ def measured_peaks():
 
 
 ATTN_SOURCES = ("sparse_attn.cu", "attn_core.cuh", "common.cuh")
-FUSED_SOURCES = ("forecast.cu", "attn_core.cuh", "common.cuh")
+FUSED_SOURCES = ("forecast.cu", "attn_core.cuh", "select_core.cuh", "common.cuh")
 
 
 def kernel_source_hash(files=ATTN_SOURCES) -> str:
@@ -1128,6 +1128,48 @@ def run_nsa_case(args, dev):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill_case(args, dev):
+    """The Forecast selection of every prefill position (SparDA notes eq.(16)) on the
+    32K prefill shape: B = 4, H_kv = 8 (G = 4), 32768 positions, 512 compressed keys,
+    k = 32.  One sparse_prefill_select launch per step."""
+    import torch
+    from block_sparse_long_pool_gb300 import binding
+    from block_sparse_long_pool_gb300 import workloads as wl
+    sh = wl.PREFILL_32K
+    peak, src = measured_peaks()
+    x = wl.prefill_inputs(sh, dev)
+    B, H_kv, T, N = sh.B, sh.H_kv, sh.T, sh.N_b
+    idx = torch.empty((B, H_kv, T, sh.k_tot), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B, H_kv, T), dtype=torch.int32, device=dev)
+    seq = torch.full((B,), T, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    evict = torch.ones(512 << 20 >> 2, dtype=torch.int32, device=dev)
+
+    def run():
+        binding.sparse_prefill_select(x["F"], x["ktil"], seq, sh.n_init, sh.n_local, sh.k, idx, cnt, status=status)
+
+    t = _event_times(run, args.steps, args.warmup, evict)
+    torch.cuda.synchronize()
+    assert status.item() == 0, f"device status {status.item()}"
+    pairs = B * H_kv
+    # scores: position t scores the candidates of the blocks it sees (causal)
+    cand = sum(max(0, min(qb + 1 - sh.n_local, qb + 1) - sh.n_init) * min(BLK, T - qb * BLK)
+               for qb in range(N))
+    macs = pairs * cand * D
+    nbytes = pairs * (T * D * 2 + N * D * 4 + T * (sh.k_tot + 1) * 4)
+    sec = t["median_us"] * 1e-6
+    tf = 2 * macs / sec / 1e12
+    line = {"case": "prefill32k", "workload": sh.name, "unit_of_work": "the selection of all 32768 positions of "
+            f"{pairs} (batch, KV head) pairs", **t, "positions_per_s": round(pairs * T / sec, 1),
+            "scores": pairs * cand, "score_tflops": round(tf, 2),
+            "score_tflops_note": "2 x (F . K~ multiply-adds); the kernel issues three bf16 mma per product "
+                                 "(fp32 keys split into three bf16 terms)",
+            "algorithmic_bytes": nbytes, "achieved_gbs": round(nbytes / sec / 1e9, 1),
+            "frac_of_measured_hbm": round(nbytes / sec / 1e9 / peak, 4), "peak_gbs": peak, "peak_source": src,
+            "l2": "512 MB read evicts L2 before each launch"}
+    print(json.dumps(line), flush=True)
+
+
 def run_other_case(args, local_rank):
     import torch
     from block_sparse_long_pool_gb300 import workloads as wl
@@ -1143,6 +1185,8 @@ def run_other_case(args, local_rank):
         run_verify_case(args, dev)
     elif args.case == "nsa128k":
         run_nsa_case(args, dev)
+    elif args.case == "prefill32k":
+        run_prefill_case(args, dev)
     else:
         run_offload_case(args, dev)
 
@@ -1156,10 +1200,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", choices=["step", "layer", "select", "single4k", "append32k", "verify64k",
-                                       "offload128k", "nsa128k"], default="step",
+                                       "offload128k", "nsa128k", "prefill32k"], default="step",
                     help="step: the 80-layer decode step (the bench line); layer: one physical layer, "
                          "kernels serialised and timed alone (for profiling); select: selection only; "
-                         "single4k / append32k / verify64k / offload128k / nsa128k: the other workloads, "
+                         "single4k / append32k / verify64k / offload128k / nsa128k / prefill32k: the other "
+                         "workloads, "
                          "one line each")
     ap.add_argument("--n-split", type=int, default=0)
     ap.add_argument("--no-workspace", action="store_true", help="layer case: attention without a workspace (cluster path)")
@@ -1176,7 +1221,7 @@ def main():
     rank, world, local_rank = dist_env()
     if args.case in ("layer", "select"):
         run_layer_case(args, local_rank)
-    elif args.case in ("single4k", "append32k", "verify64k", "offload128k", "nsa128k"):
+    elif args.case in ("single4k", "append32k", "verify64k", "offload128k", "nsa128k", "prefill32k"):
         run_other_case(args, local_rank)
     elif args.impl == "reference":
         run_reference(args, rank, world, local_rank)

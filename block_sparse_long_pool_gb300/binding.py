@@ -44,6 +44,7 @@ SIGNATURES = {
     "sparse_pool_append_kv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _LL, _I, _LL, _I, _P]),
     "sparse_select_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P]),
     "sparse_select_topk_heads": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _P, _P, _I, _P, _P]),
+    "sparse_prefill_select": (_I, [_P, _LL, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P]),
     "sparse_decode_attn": (_I, [_P, _P, _P, _LL, _P, _P, _P, _I, _P, _I, _I, _I, _F, _P, _P, _I, _U, _P, _SZ,
                                 _P, _P]),
     "sparse_decode_attn_ex": (_I, [_P, _P, _P, _LL, _P, _P, _P, _I, _P, _I, _I, _I, _F, _P, _P, _I, _U, _P, _SZ,
@@ -429,3 +430,20 @@ def sparse_nsa_select(Q, khat, seq_len, n_init: int, n_local: int, k: int, idx_o
                                   float(scale), n_init, n_local, k, _ptr(idx_out), _ptr(count_out), k_tot,
                                   _ptr(status), _stream(stream))
     _check(rc, "sparse_nsa_select")
+
+
+def sparse_prefill_select(F, ktil, seq_len, n_init: int, n_local: int, k: int, idx_out, count_out, status=None,
+                          stream=None):
+    """Forecast selection of every prefill position: F [B][H_kv][T_cap][128] bf16, ktil
+    [B][H_kv][N_cap][128] fp32 -> idx_out [B][H_kv][T_cap][k_tot], count_out [B][H_kv][T_cap]."""
+    B, H_kv, T_cap, _ = F.shape
+    N_cap = ktil.shape[2]
+    k_tot = idx_out.shape[3]
+    _need(F, "F", torch.bfloat16, shape=(B, H_kv, T_cap, D))
+    _need(ktil, "ktil", torch.float32, shape=(B, H_kv, N_cap, D))
+    _need(seq_len, "seq_len", torch.int32, shape=(B,))
+    _need(idx_out, "idx_out", torch.int32, shape=(B, H_kv, T_cap, k_tot))
+    _need(count_out, "count_out", torch.int32, shape=(B, H_kv, T_cap))
+    rc = load().sparse_prefill_select(_ptr(F), T_cap, _ptr(ktil), N_cap, _ptr(seq_len), B, H_kv, n_init, n_local, k,
+                                      _ptr(idx_out), _ptr(count_out), k_tot, _ptr(status), _stream(stream))
+    _check(rc, "sparse_prefill_select")

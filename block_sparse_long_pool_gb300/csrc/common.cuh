@@ -160,6 +160,14 @@ __device__ __forceinline__ uint64_t policy_evict_first()
     return pol;
 }
 
+// For data that many CTAs read again soon (e.g. a pair's compressed keys at prefill).
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // 3-D tiled tensor load into this CTA's shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
                                             int c0, int c1, int c2, uint64_t policy)

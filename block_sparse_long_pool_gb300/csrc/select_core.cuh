@@ -1,0 +1,463 @@
+// select_core.cuh -- exact top-k of order keys in shared memory, shared by the Forecast
+// selection (decode), the NSA routing and the prefill selection.
+//
+// Keys are order_key(score): larger score -> larger key, equal scores -> equal keys.
+// The top-k takes the k largest keys of the candidates [n_init, nb - n_local), equal
+// keys in block order (the lower block first), and writes B_init, the selected
+// candidates and B_local in ascending block order (SparDA notes eq.(6), Alg.1 step 2).
+#pragma once
+
+#include "common.cuh"
+
+namespace {
+
+using namespace sp;
+
+constexpr int kTopkList = 512;                                    // keys gathered in the threshold bin
+constexpr int kCoarseShift = 22;                                  // coarse bin = key >> 22
+constexpr int kCoarseBins = 1 << (32 - kCoarseShift);             // 1024
+
+// Histogram of byte digit (key >> shift) & 255 over the keys whose bits above the digit
+// equal `prefix` (under `pmask`), by one warp: keys[i] for i in [lo, hi), or
+// keys[list[i]] when list_s is non-zero.  Lanes holding the same digit add once
+// (warp-aggregated shared-memory atomics).  All arrays are shared-space addresses.
+__device__ __forceinline__ void warp_digit_hist(uint32_t keys_s, uint32_t list_s, int lo, int hi, uint32_t pmask,
+                                                uint32_t prefix, int shift, uint32_t hist_s, int lane)
+{
+    for (int d = lane; d < 256; d += 32)
+        sts_u32(hist_s + 4 * d, 0u);
+    __syncwarp();
+    for (int ib = lo; ib < hi; ib += 32) {
+        const int i = ib + lane;
+        uint32_t digit = 0xFFFFFFFFu;
+        if (i < hi) {
+            const uint32_t j = list_s != 0u ? lds_u32(list_s + 4 * i) : static_cast<uint32_t>(i);
+            const uint32_t key = lds_u32(keys_s + 4 * j);
+            if ((key & pmask) == prefix)
+                digit = (key >> shift) & 255u;
+        }
+        const uint32_t same = __match_any_sync(0xffffffffu, digit);
+        if (digit != 0xFFFFFFFFu && lane == __ffs(same) - 1)
+            asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(hist_s + 4 * digit), "r"(__popc(same)) : "memory");
+    }
+    __syncwarp();
+}
+
+// From a digit histogram, the digit that holds the need-th largest key (counting from
+// the top digit) and the number of keys still needed within it.
+__device__ __forceinline__ void warp_pick_digit(uint32_t hist_s, int &need, uint32_t &digit, int lane)
+{
+    // lane l holds digits 255 - 8l - i (i = 0..7): lanes run from the top digit down
+    int c[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        c[i] = static_cast<int>(lds_u32(hist_s + 4 * (255 - 8 * lane - i)));
+        sum += c[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += n;
+    }
+    const int excl = incl - sum;
+    int dsel = -1, need_new = 0;
+    if (excl < need && need <= incl) {
+        int acc = excl;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (dsel < 0 && acc + c[i] >= need) {
+                dsel = 255 - 8 * lane - i;
+                need_new = need - acc;
+            }
+            acc += c[i];
+        }
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, dsel >= 0);
+    const int src = m != 0u ? __ffs(m) - 1 : 0;
+    dsel = __shfl_sync(0xffffffffu, dsel, src);
+    need_new = __shfl_sync(0xffffffffu, need_new, src);
+    if (m == 0u) {   // cannot happen with 1 <= need <= keys counted; keep the state sane
+        dsel = 0;
+        need_new = need;
+    }
+    digit = static_cast<uint32_t>(dsel);
+    need = need_new;
+}
+
+// The selection in ascending block order: B_init, the candidates above the threshold
+// key `prefix` plus the first `need` of those equal to it (lower index first; from the
+// list of candidate ids when list_s is non-zero, else from all candidates), B_local;
+// the rest of the row is -1.  One warp.
+__device__ void topk_write_warp(uint32_t keys_s, uint32_t list_s, int n_list, int nb, int n_init, int n_local,
+                                bool take_all, bool take_none, uint32_t prefix, int need, int *out, int k_tot,
+                                int *count_out, int *status, int lane)
+{
+    const int cand_lo = n_init, cand_hi = nb - n_local;
+    const int n_cand = max(0, cand_hi - cand_lo);
+    const unsigned lt = (1u << lane) - 1u;
+    const int n_i = min(n_init, nb);
+    const int l0 = max(nb - n_local, n_i);
+    int pos0 = 0, eq_seen = 0;
+    bool overflow = false;
+    for (int j = lane; j < n_i; j += 32) {
+        if (j < k_tot)
+            out[j] = j;
+        else
+            overflow = true;
+    }
+    pos0 = n_i;
+    if (take_all) {
+        for (int j = cand_lo + lane; j < cand_hi; j += 32) {
+            const int pos = pos0 + (j - cand_lo);
+            if (pos < k_tot)
+                out[pos] = j;
+            else
+                overflow = true;
+        }
+        pos0 += n_cand;
+    } else if (!take_none) {
+        const bool from_list = list_s != 0u;
+        const int hi = from_list ? n_list : cand_hi;
+        for (int ib = from_list ? 0 : cand_lo; ib < hi; ib += 32) {
+            const int i = ib + lane;
+            int j = -1;
+            uint32_t key = 0u;
+            if (i < hi) {
+                j = from_list ? static_cast<int>(lds_u32(list_s + 4 * i)) : i;
+                key = lds_u32(keys_s + 4 * j);
+            }
+            bool sel = i < hi && key > prefix;
+            const bool eq = i < hi && key == prefix;
+            const unsigned em = __ballot_sync(0xffffffffu, eq);
+            if (eq)
+                sel = eq_seen + __popc(em & lt) < need;
+            eq_seen += __popc(em);
+            const unsigned sm = __ballot_sync(0xffffffffu, sel);
+            if (sel) {
+                const int pos = pos0 + __popc(sm & lt);
+                if (pos < k_tot)
+                    out[pos] = j;
+                else
+                    overflow = true;
+            }
+            pos0 += __popc(sm);
+        }
+    }
+    for (int j = l0 + lane; j < nb; j += 32) {
+        const int pos = pos0 + (j - l0);
+        if (pos < k_tot)
+            out[pos] = j;
+        else
+            overflow = true;
+    }
+    pos0 += max(0, nb - l0);
+    if (__any_sync(0xffffffffu, overflow) && lane == 0)
+        report(status, SPARSE_ERR_BAD_INDEX);
+    for (int i = pos0 + lane; i < k_tot; i += 32)
+        out[i] = -1;
+    if (lane == 0)
+        *count_out = min(pos0, k_tot);
+}
+
+// The exact top-k of one pair by one warp over the order keys of blocks [0, nb) (shared
+// array at keys_s): the k largest keys among candidates [n_init, nb - n_local) (equal
+// keys: lower block first), united with B_init and B_local, written ascending to
+// out[0 .. count) and -1 after.  coarse_s holds the histogram of key >> 22 over the
+// candidates (built while the keys were scored).
+//   1. The coarse bin where the count from the top reaches k.
+//   2. One pass: each lane tests a contiguous run of candidates against the bin's lower
+//      bound (rotated so the lanes hit distinct banks) and writes the block ids of the
+//      keys at or above it, ascending, into list_s (kTopkList entries at most).
+//   3. The remaining 22 bits of the k-th key by an MSB-first radix select over byte
+//      digits of the listed keys that fall in the threshold bin.
+//   4. B_init, then the listed keys above the k-th key and the first `need` equal to it
+//      (block order), then B_local.
+// More than 2048 candidates, or more than kTopkList keys at or above the bin, take a
+// slower path that scans every candidate for each digit.  coarse_s is reused for the
+// digits.
+__device__ void topk_warp(uint32_t keys_s, uint32_t coarse_s, uint32_t list_s, int nb, int n_init, int n_local, int k,
+                          int *out, int k_tot, int *count_out, int *status, int lane)
+{
+    const int cand_lo = n_init, cand_hi = nb - n_local;
+    const int n_cand = max(0, cand_hi - cand_lo);
+    const bool take_all = n_cand <= k;
+    const bool take_none = k <= 0;
+    uint32_t prefix = 0, pmask = 0;
+    int need = k;
+    bool listed = false;
+    int n_list = 0;
+    if (!take_all && !take_none) {
+        // 1. the coarse bin: lane l holds bins [1024 - 32(l+1), 1024 - 32l)
+        constexpr int kPer = kCoarseBins / 32;
+        const int bin0 = kCoarseBins - kPer * (lane + 1);
+        uint32_t cb[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; i += 4) {
+            const uint4 v = lds_v4(coarse_s + 4 * (bin0 + i));
+            cb[i] = v.x;
+            cb[i + 1] = v.y;
+            cb[i + 2] = v.z;
+            cb[i + 3] = v.w;
+        }
+        int c = 0;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i)
+            c += static_cast<int>(cb[i]);
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += n;
+        }
+        const int excl = incl - c;
+        int bsel = -1, need_new = 0, m = 0;
+        if (excl < need && need <= incl) {
+            int acc = excl;
+#pragma unroll
+            for (int i = kPer - 1; i >= 0; --i) {
+                const int ci = static_cast<int>(cb[i]);
+                if (bsel < 0 && acc + ci >= need) {
+                    bsel = bin0 + i;
+                    need_new = need - acc;
+                    m = ci;
+                }
+                acc += ci;
+            }
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, bsel >= 0);
+        const int src_lane = hit != 0u ? __ffs(hit) - 1 : 0;
+        bsel = __shfl_sync(0xffffffffu, bsel, src_lane);
+        need_new = __shfl_sync(0xffffffffu, need_new, src_lane);
+        m = __shfl_sync(0xffffffffu, m, src_lane);
+        if (hit != 0u) {   // always, when the histogram counts every candidate
+            prefix = static_cast<uint32_t>(bsel) << kCoarseShift;
+            pmask = ~((1u << kCoarseShift) - 1u);
+            // keys strictly above the bin: k - need_new; the list holds them and the bin
+            const int expect = k - need_new + m;
+            need = need_new;
+            if (n_cand <= 32 * 64 && expect <= kTopkList) {
+                // 2. one pass over the candidates
+                const int per = ((n_cand + 31) / 32 + 31) & ~31;   // 32 or 64 (a multiple of 32)
+                const int jb = cand_lo + lane * per;
+                uint64_t hits = 0ull;
+#pragma unroll 8
+                for (int i = 0; i < per; ++i) {
+                    const int ii = (i + lane) & (per - 1);
+                    const int j = jb + ii;
+                    const uint32_t key = j < cand_hi ? lds_u32(keys_s + 4 * j) : 0u;
+                    if (j < cand_hi && key >= prefix)
+                        hits |= 1ull << ii;
+                }
+                const int cnt = __popcll(hits);
+                int off = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int n = __shfl_up_sync(0xffffffffu, off, o);
+                    if (lane >= o)
+                        off += n;
+                }
+                n_list = __shfl_sync(0xffffffffu, off, 31);
+                off -= cnt;
+                while (hits != 0ull) {
+                    const int bpos = __ffsll(static_cast<long long>(hits)) - 1;
+                    if (off < kTopkList)
+                        sts_u32(list_s + 4 * off, static_cast<uint32_t>(jb + bpos));
+                    ++off;
+                    hits &= hits - 1ull;
+                }
+                __syncwarp();
+                listed = n_list <= kTopkList;   // equal to `expect` unless the histogram was off
+            }
+        } else {
+            need = k;
+        }
+        // 3. the digits below the coarse bin (bits 23..16, 15..8, 7..0; 23 and 22 are fixed)
+        const uint32_t src_list = listed ? list_s : 0u;
+        const int lo = listed ? 0 : cand_lo, hi = listed ? n_list : cand_hi;
+        uint32_t d;
+        if (pmask == 0u) {
+            warp_digit_hist(keys_s, src_list, lo, hi, 0u, 0u, 24, coarse_s, lane);
+            warp_pick_digit(coarse_s, need, d, lane);
+            prefix = d << 24;
+            pmask = 0xFF000000u;
+        }
+        warp_digit_hist(keys_s, src_list, lo, hi, pmask, prefix, 16, coarse_s, lane);
+        warp_pick_digit(coarse_s, need, d, lane);
+        prefix |= d << 16;
+        pmask = 0xFFFF0000u;
+        warp_digit_hist(keys_s, src_list, lo, hi, pmask, prefix, 8, coarse_s, lane);
+        warp_pick_digit(coarse_s, need, d, lane);
+        prefix |= d << 8;
+        pmask = 0xFFFFFF00u;
+        warp_digit_hist(keys_s, src_list, lo, hi, pmask, prefix, 0, coarse_s, lane);
+        warp_pick_digit(coarse_s, need, d, lane);
+        prefix |= d;
+    }
+    // 4. ascending output
+    topk_write_warp(keys_s, listed ? list_s : 0u, n_list, nb, n_init, n_local, take_all, take_none, prefix, need,
+                    out, k_tot, count_out, status, lane);
+}
+
+// The threshold of the top-k among keys[cand_lo, cand_hi) by `nthreads` threads (whole
+// warps, synchronised on named barrier `bar`; the thread with tid 0 is in warp 0): four
+// passes of 8-bit digits from the top, each a histogram in per-warp shared-memory bins
+// (hist_s: [nthreads / 32][256] u32, plain shared atomics, so keys packed into a few
+// values cost no more than spread ones), the digit holding the need-th largest key
+// picked by warp 0.  Gives the k-th largest key and how many keys equal to it are
+// taken.  ctrl_s: two words that broadcast the running prefix and need.  Every
+// participant must call it.
+__device__ __forceinline__ void topk_threshold_cta(uint32_t keys_s, int cand_lo, int cand_hi, int k, uint32_t hist_s,
+                                                   uint32_t ctrl_s, int tid, int nthreads, int bar, uint32_t &prefix_out,
+                                                   int &need_out)
+{
+    const int warp = tid >> 5, lane = tid & 31;
+    const int n_warps = nthreads >> 5;
+    uint32_t prefix = 0u, pmask = 0u;
+    int need = k;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        const uint32_t my_hist = hist_s + 4u * 256u * static_cast<uint32_t>(warp);
+        for (int d = lane; d < 256; d += 32)
+            sts_u32(my_hist + 4 * d, 0u);
+        named_barrier_sync(bar, nthreads);
+        for (int ib = cand_lo + (tid & ~31); ib < cand_hi; ib += nthreads) {
+            const int i = ib + lane;
+            uint32_t digit = 0xFFFFFFFFu;
+            if (i < cand_hi) {
+                const uint32_t key = lds_u32(keys_s + 4 * i);
+                if ((key & pmask) == prefix)
+                    digit = (key >> shift) & 255u;
+            }
+            // keys close in value share their upper digits: one add for a warp that agrees
+            const uint32_t d0 = __shfl_sync(0xffffffffu, digit, 0);
+            const unsigned agree = __ballot_sync(0xffffffffu, digit == d0);
+            if (agree == 0xffffffffu) {
+                if (lane == 0 && d0 != 0xFFFFFFFFu)
+                    asm volatile("red.shared.add.u32 [%0], 32;" ::"r"(my_hist + 4 * d0) : "memory");
+            } else if (digit != 0xFFFFFFFFu) {
+                asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(my_hist + 4 * digit) : "memory");
+            }
+        }
+        named_barrier_sync(bar, nthreads);
+        if (warp == 0) {
+            for (int d = lane; d < 256; d += 32) {
+                uint32_t sum = 0u;
+                for (int w = 0; w < n_warps; ++w)
+                    sum += lds_u32(hist_s + 4u * (256u * w + d));
+                sts_u32(hist_s + 4 * d, sum);
+            }
+            __syncwarp();
+            uint32_t d;
+            warp_pick_digit(hist_s, need, d, lane);
+            if (lane == 0) {
+                sts_u32(ctrl_s, prefix | (d << shift));
+                sts_u32(ctrl_s + 4, static_cast<uint32_t>(need));
+            }
+        }
+        named_barrier_sync(bar, nthreads);
+        prefix = lds_u32(ctrl_s);
+        need = static_cast<int>(lds_u32(ctrl_s + 4));
+        pmask |= 255u << shift;
+    }
+    prefix_out = prefix;
+    need_out = need;
+}
+
+// topk_threshold_cta for one warp alone (no named barrier): the k-th largest key among
+// keys[cand_lo, cand_hi) and how many keys equal to it are taken, by four passes of
+// 8-bit digits over the warp's 256 shared-memory bins at hist_s.
+__device__ __forceinline__ void topk_threshold_warp(uint32_t keys_s, int cand_lo, int cand_hi, int k, uint32_t hist_s,
+                                                    int lane, uint32_t &prefix_out, int &need_out)
+{
+    uint32_t prefix = 0u, pmask = 0u;
+    int need = k;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int d = lane; d < 256; d += 32)
+            sts_u32(hist_s + 4 * d, 0u);
+        __syncwarp();
+        for (int ib = cand_lo; ib < cand_hi; ib += 32) {
+            const int i = ib + lane;
+            uint32_t digit = 0xFFFFFFFFu;
+            if (i < cand_hi) {
+                const uint32_t key = lds_u32(keys_s + 4 * i);
+                if ((key & pmask) == prefix)
+                    digit = (key >> shift) & 255u;
+            }
+            const uint32_t d0 = __shfl_sync(0xffffffffu, digit, 0);
+            const unsigned agree = __ballot_sync(0xffffffffu, digit == d0);
+            if (agree == 0xffffffffu) {
+                if (lane == 0 && d0 != 0xFFFFFFFFu)
+                    asm volatile("red.shared.add.u32 [%0], 32;" ::"r"(hist_s + 4 * d0) : "memory");
+            } else if (digit != 0xFFFFFFFFu) {
+                asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(hist_s + 4 * digit) : "memory");
+            }
+        }
+        __syncwarp();
+        uint32_t d;
+        warp_pick_digit(hist_s, need, d, lane);
+        prefix |= d << shift;
+        pmask |= 255u << shift;
+        __syncwarp();
+    }
+    prefix_out = prefix;
+    need_out = need;
+}
+
+// The k-th largest key among keys[cand_lo, cand_hi) (at most 32 * KPL of them) by one
+// warp with the keys in registers: a binary search over the key bits from the top, each
+// step counting with a warp sum the keys that share the decided bits and have the next
+// bit set.  When every key sharing the decided bits is needed, the threshold is their
+// smallest key and the search stops (random scores: after about log2(n) steps).
+// Gives the threshold and how many keys equal to it are taken, as topk_threshold_warp.
+template <int KPL>
+__device__ __forceinline__ void topk_threshold_regs(uint32_t keys_s, int cand_lo, int cand_hi, int k, int lane,
+                                                    uint32_t &prefix_out, int &need_out)
+{
+    uint32_t key[KPL];
+    const int nv = max(0, (cand_hi - cand_lo - lane + 31) / 32);   // this lane's valid slots
+#pragma unroll
+    for (int m = 0; m < KPL; ++m)
+        key[m] = m < nv ? lds_u32(keys_s + 4 * (cand_lo + lane + 32 * m)) : 0u;
+    uint32_t P = 0u, hmask = 0u;
+    int need = k;
+    int mt = max(0, cand_hi - cand_lo);   // keys sharing the decided bits (all, at first)
+    for (int b = 31; b >= 0; --b) {
+        if (mt == need) {
+            // every key sharing the decided bits is taken: the smallest is the threshold
+            uint32_t mn = 0xFFFFFFFFu;
+#pragma unroll
+            for (int m = 0; m < KPL; ++m)
+                if (m < nv && (key[m] & hmask) == P)
+                    mn = min(mn, key[m]);
+            mn = __reduce_min_sync(0xffffffffu, mn);
+            int eq = 0;
+#pragma unroll
+            for (int m = 0; m < KPL; ++m)
+                eq += (m < nv && key[m] == mn) ? 1 : 0;
+            P = mn;
+            need = __reduce_add_sync(0xffffffffu, eq);
+            break;
+        }
+        const uint32_t bit = 1u << b;
+        const uint32_t m2 = hmask | bit, want = P | bit;
+        int c = 0;   // keys sharing the decided bits with bit b set (an empty slot holds 0: never)
+#pragma unroll
+        for (int m = 0; m < KPL; ++m)
+            c += (key[m] & m2) == want ? 1 : 0;
+        c = __reduce_add_sync(0xffffffffu, c);
+        if (c >= need) {
+            P = want;
+            mt = c;
+        } else {
+            need -= c;
+            mt -= c;
+        }
+        hmask = m2;
+    }
+    prefix_out = P;
+    need_out = need;
+}
+
+}  // namespace

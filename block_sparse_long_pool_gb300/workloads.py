@@ -22,6 +22,11 @@ Recipe (every tensor is seeded; bf16 values are N(0, 1) draws rounded once):
   queries) a core of round(gamma * n_sel) blocks shared by every query of the group
   plus n_sel - core private blocks per query, all distinct and drawn without
   replacement outside the sliding window, each query's list ascending.
+* Prefill selection (SparDA notes §4.3 eq.(16), the 1.25x prefill workload's
+  MiniCPM4.1-8B shape: G = 4): one Forecast vector per (batch, KV head, position)
+  [B][H_kv][T][128] (bf16 N(0, 1)) and the prefill's compressed keys
+  [B][H_kv][N_b][128] drawn directly as fp32 N(0, 1/64), the spread of a 64-token mean
+  of N(0, 1) keys.
 """
 from __future__ import annotations
 
@@ -154,6 +159,34 @@ VERIFY_64K = VerifyShape("ssv_verify_64k_b4_c4", B=4, H_q=32, H_kv=8, T=65536, N
                          gamma=0.75, window_tokens=512, C=4, seed=1238)
 OFFLOAD_128K = OffloadShape("offload_128k_b4_32layers", B=4, H_q=32, H_kv=8, T=131072, layers=32,
                             n_init=1, n_local=2, k=64, n_planted=64, phys_layers=32, seed=1239)
+
+
+@dataclasses.dataclass(frozen=True)
+class PrefillShape:
+    name: str
+    B: int
+    H_q: int
+    H_kv: int
+    T: int
+    n_init: int
+    n_local: int
+    k: int
+    seed: int
+
+    @property
+    def pairs(self) -> int:
+        return self.B * self.H_kv
+
+    @property
+    def N_b(self) -> int:
+        return n_blocks(self.T)
+
+    @property
+    def k_tot(self) -> int:
+        return self.n_init + self.n_local + self.k
+
+
+PREFILL_32K = PrefillShape("prefill_32k_b4_g4", B=4, H_q=32, H_kv=8, T=32768, n_init=1, n_local=2, k=32, seed=1240)
 
 
 def _gen(device, seed: int) -> torch.Generator:
@@ -330,3 +363,11 @@ def bf16_bits(t: torch.Tensor):
     import numpy as np
     assert t.dtype == torch.bfloat16
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def prefill_inputs(shape: PrefillShape, device="cpu"):
+    """Forecast vectors of every position and the prefill's compressed keys."""
+    F = randn_bf16((shape.B, shape.H_kv, shape.T, D), _subseed(shape.seed, 1), device)
+    ktil = torch.randn((shape.B, shape.H_kv, shape.N_b, D), generator=_gen(device, _subseed(shape.seed, 2)),
+                       device=device, dtype=torch.float32) * 0.125
+    return dict(F=F, ktil=ktil)

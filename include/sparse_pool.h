@@ -118,6 +118,27 @@ SPARSE_API int sparse_select_topk(const uint16_t *F, const float *ktil, const in
                                   void *stream);
 
 /*
+ * sparse_prefill_select -- the Forecast selection of every prefill position, [SparDA]
+ * §4.3 eq.(16) (the indexer scores all T positions against the compressed keys,
+ * H_kv * T * N_b * d multiply-adds) with the per-position selection of sparse_select_topk:
+ * position t < seq_len[b] of pair p sees the blocks holding tokens 0..t,
+ * N_t = floor(t / 64) + 1; s_j = F[p][t] . ktil[p][j]; B_init = [0, n_init),
+ * B_local = [N_t - n_local, N_t), and the k candidates of largest score (ties to the
+ * lower block), written ascending, padded with -1.  The scores run on the tensor cores
+ * with the fp32 keys split into three bf16 terms (exact products, fp32 sums).
+ *   F          [B][H_kv][T_cap][128] bf16: the Forecast vector of every position.
+ *   ktil       [B][H_kv][N_cap][128] fp32 compressed keys of the prefill (the block
+ *              holding t may include later tokens: it is local, so n_local >= 1).
+ *   idx_out    [B][H_kv][T_cap][k_tot] int32, count_out [B][H_kv][T_cap] int32; rows at
+ *              or past seq_len[b] are not written.
+ * N_cap <= 2048 (131072 tokens).
+ */
+SPARSE_API int sparse_prefill_select(const uint16_t *F, long long T_cap, const float *ktil, int N_cap,
+                                     const int *seq_len, int B, int H_kv, int n_init, int n_local,
+                                     int k, int *idx_out, int *count_out, int k_tot, int *status,
+                                     void *stream);
+
+/*
  * sparse_select_topk_heads -- the multi-head block selector of InfLLM-V2, the baseline
  * that [SparDA] §4.3 (eq.(8) and its Figure 3) compares the Forecast selector with:
  * every one of the G = H_q / H_kv query heads of pair p scores every compressed key,

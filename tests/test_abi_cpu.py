@@ -246,3 +246,21 @@ def test_nsa_compress_and_select_reject_bad_arguments(lib):
     assert call_s(a3=16, a4=32) == binding.SPARSE_ERR_INVALID_ARG     # stride above the kernel
     assert call_s(a7=64, a8=2) == binding.SPARSE_ERR_UNSUPPORTED      # G = 32
     assert call_s(a9=-1.0) == binding.SPARSE_ERR_INVALID_ARG          # negative scale
+
+
+def test_prefill_select_rejects_bad_arguments(lib):
+    f = lib.sparse_prefill_select
+    # F, T_cap, ktil, N_cap, seq_len, B, H_kv, n_init, n_local, k, idx, count, k_tot, status, stream
+    ok = [FAKE, 4096, FAKE, 64, FAKE, 1, 2, 1, 2, 8, FAKE, FAKE, 11, None, None]
+
+    def call(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+
+    assert call(a0=None) == binding.SPARSE_ERR_INVALID_ARG        # no F
+    assert call(a2=ODD) == binding.SPARSE_ERR_INVALID_ARG         # misaligned keys
+    assert call(a8=0) == binding.SPARSE_ERR_INVALID_ARG           # n_local = 0: the own block must be local
+    assert call(a12=10) == binding.SPARSE_ERR_INVALID_ARG         # k_tot too small
+    assert call(a3=4096) == binding.SPARSE_ERR_UNSUPPORTED        # more than 2048 compressed keys
