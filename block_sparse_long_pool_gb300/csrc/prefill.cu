@@ -232,8 +232,15 @@ __global__ void __launch_bounds__(kPfThreads, KPL <= 32 ? 2 : 1) prefill_select_
             const uint32_t row_keys = keys_s + 4 * r * p.key_stride;
             uint32_t prefix = 0u;
             int need = 0;
-            if (score)
-                topk_threshold_regs<KPL>(row_keys, c_lo, c_hi, p.k, lane, prefix, need);
+            if (score) {
+                // registers for the candidates this tile has (they grow with the position)
+                if (KPL >= 16 && n_cand <= 8 * KPL)
+                    topk_threshold_regs<(KPL >= 16 ? KPL / 4 : KPL)>(row_keys, c_lo, c_hi, p.k, lane, prefix, need);
+                else if (KPL >= 8 && n_cand <= 16 * KPL)
+                    topk_threshold_regs<(KPL >= 8 ? KPL / 2 : KPL)>(row_keys, c_lo, c_hi, p.k, lane, prefix, need);
+                else
+                    topk_threshold_regs<KPL>(row_keys, c_lo, c_hi, p.k, lane, prefix, need);
+            }
             const size_t at = static_cast<size_t>(pair) * p.T_cap + t0 + r;
             topk_write_warp(row_keys, 0u, 0, nb, p.n_init, p.n_local, take_all, take_none, prefix, need,
                             p.idx + at * p.k_tot, p.k_tot, p.count + at, p.status, lane);
