@@ -353,6 +353,8 @@ __global__ void __launch_bounds__(kFThreads, 2)
 constexpr int kMaxHeadsSel = 16;
 constexpr int kCtrlStatsBar = 10;   // ctrl[10..11]
 constexpr int kCtrlNormBar = 12;    // ctrl[12..13]
+constexpr int kCtrlThrWords = 4;    // ctrl[4..5]: the running threshold of the top-k search
+constexpr int kHeadsTopkThreads = (kConsumerWarps + 1) * 32;   // CTA 0's consumers + selector
 
 struct HeadsLayout {
     int off_keys, off_q, off_raw, off_stats, off_norm, total;
@@ -363,7 +365,7 @@ __host__ __device__ inline HeadsLayout heads_layout(int N_cap, int rows_max, int
     HeadsLayout l;
     l.off_keys = fused_off_slice();                       // after the histogram and list
     l.off_q = l.off_keys + ((N_cap * 4 + 15) & ~15);      // [G][128] fp32 queries
-    l.off_raw = l.off_q + G * kD * 4;                     // [rows_max][G] raw scores
+    l.off_raw = l.off_q + G * kD * 4;                     // [G][rows_max] raw scores (head-major)
     l.off_stats = l.off_raw + ((rows_max * G * 4 + 15) & ~15);   // CTA 0: [S][G] (max, sum)
     l.off_norm = l.off_stats + S * G * 8;                 // [G] (max, 1 / sum)
     l.total = l.off_norm + G * 8;
@@ -462,7 +464,6 @@ __global__ void __launch_bounds__(kFThreads, 1) select_heads_kernel(const AttnPa
         named_barrier_sync(2, kConsumerWarps * 32);
         cluster_wait();
         uint32_t *keys0 = static_cast<uint32_t *>(__cluster_map_shared_rank(keys, 0));
-        uint32_t *coarse0 = static_cast<uint32_t *>(__cluster_map_shared_rank(hist, 0));
         float *stats0 = static_cast<float *>(__cluster_map_shared_rank(stats, 0));
         bool ok = true;
         // (1) raw scores of the slice
@@ -524,7 +525,7 @@ __global__ void __launch_bounds__(kFThreads, 1) select_heads_kernel(const AttnPa
                     acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 1);
                     const int r = (lane >> 1) & 15;
                     if ((lane & 1) == 0 && r < nrow)
-                        raw[(ks * kKtilRowsPerStage + warp * 16 + r) * G + h] = acc[0];
+                        raw[h * rows_max + ks * kKtilRowsPerStage + warp * 16 + r] = acc[0];
                 }
             }
             __syncwarp();
@@ -537,14 +538,14 @@ __global__ void __launch_bounds__(kFThreads, 1) select_heads_kernel(const AttnPa
             for (int h = warp; h < G; h += kConsumerWarps) {
                 float m = -INFINITY;
                 for (int i = lane; i < n_krows; i += 32)
-                    m = fmaxf(m, raw[i * G + h]);
+                    m = fmaxf(m, raw[h * rows_max + i]);
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1)
                     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
                 float z = 0.f;
                 if (m != -INFINITY)
                     for (int i = lane; i < n_krows; i += 32)
-                        z += exp2f(raw[i * G + h] - m);
+                        z += exp2f(raw[h * rows_max + i] - m);
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1)
                     z += __shfl_xor_sync(0xffffffffu, z, o);
@@ -568,21 +569,26 @@ __global__ void __launch_bounds__(kFThreads, 1) select_heads_kernel(const AttnPa
                     float sum = 0.f;
                     if (in)
                         for (int h = 0; h < G; ++h)
-                            sum += exp2f(raw[i * G + h] - norm[2 * h]) * norm[2 * h + 1];
+                            sum += exp2f(raw[h * rows_max + i] - norm[2 * h]) * norm[2 * h + 1];
                     const int j = r0 + i;
-                    const uint32_t key = order_key(sum);
                     if (in)
-                        keys0[j] = key;
-                    const bool cand = in && j >= p.n_init && j < nb - p.n_local;
-                    const uint32_t bin = cand ? key >> kCoarseShift : 0xFFFFFFFFu;
-                    const uint32_t same = __match_any_sync(0xffffffffu, bin);
-                    if (cand && lane == __ffs(same) - 1)
-                        atomicAdd(coarse0 + bin, static_cast<uint32_t>(__popc(same)));
+                        keys0[j] = order_key(sum);
                 }
             }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive_cluster(dsmem_addr(bar_scored, 0));
+            if (rank == 0) {
+                // CTA 0's consumers join its selector warp in the threshold search (the
+                // summed probabilities share an exponent: a coarse histogram of the top
+                // key bits would not narrow them)
+                if (!__all_sync(0xffffffffu, mbar_wait_cluster(bar_scored, 0, kWaitNs)) && lane == 0)
+                    report(p.status, SPARSE_ERR_TIMEOUT);
+                uint32_t prefix;
+                int need;
+                topk_threshold_cta(base_s + L.off_keys, p.n_init, nb - p.n_local, p.k_sel, base_s + fused_off_hist(),
+                                   base_s + kOffCtrl + 4 * kCtrlThrWords, tid + 32, kHeadsTopkThreads, 3, prefix, need);
+            }
         }
     } else {
         // ------------------------------------------------------------ selector (CTA 0)
@@ -619,10 +625,16 @@ __global__ void __launch_bounds__(kFThreads, 1) select_heads_kernel(const AttnPa
                 if (ready)
                     ready = __all_sync(0xffffffffu, mbar_wait_cluster(bar_scored, 0, kWaitNs));
             }
+            uint32_t prefix = 0u;
+            int need = 0;
+            if (score)
+                topk_threshold_cta(base_s + L.off_keys, p.n_init, nb - p.n_local, p.k_sel, base_s + fused_off_hist(),
+                                   base_s + kOffCtrl + 4 * kCtrlThrWords, lane, kHeadsTopkThreads, 3, prefix, need);
             if (ready) {
-                topk_warp(base_s + L.off_keys, base_s + fused_off_hist(), base_s + fused_off_topk_list(), nb,
-                          p.n_init, p.n_local, p.k_sel, p.idx_next + static_cast<size_t>(pair) * p.k_tot_next,
-                          p.k_tot_next, p.count_next + pair, p.status, lane);
+                topk_write_warp(base_s + L.off_keys, 0u, 0, nb, p.n_init, p.n_local,
+                                max(0, nb - p.n_local - p.n_init) <= p.k_sel, p.k_sel <= 0, prefix, need,
+                                p.idx_next + static_cast<size_t>(pair) * p.k_tot_next, p.k_tot_next,
+                                p.count_next + pair, p.status, lane);
             } else if (lane == 0) {
                 report(p.status, SPARSE_ERR_TIMEOUT);
             }
@@ -632,6 +644,8 @@ __global__ void __launch_bounds__(kFThreads, 1) select_heads_kernel(const AttnPa
 }
 
 static_assert(4 * kCtrlNormBar + 8 <= 64, "ctrl layout");
+static_assert(kCtrlThrWords >= 4 && 4 * kCtrlThrWords + 8 <= 4 * kCtrlScoredBar, "ctrl layout: threshold words");
+static_assert((kHeadsTopkThreads / 32) * 256 <= kCoarseBins + kTopkList, "multi-head radix bins");
 
 // The "scored" barrier lives in the ctrl words, 8-byte aligned.
 static_assert((kOffCtrl + 4 * kCtrlScoredBar) % 8 == 0 && 4 * kCtrlScoredBar + 8 <= 64, "ctrl layout");
@@ -841,10 +855,11 @@ extern "C" SPARSE_API int sparse_select_topk_heads(const uint16_t *Q, const floa
     int S = 1;
     while (S < kMaxSplit && pairs * S * 2 <= dev.sm_count && N_cap / (S * 2) >= 128)
         S *= 2;
-    HeadsLayout L = heads_layout(N_cap, (N_cap + S - 1) / S, G, S);
+    auto stride_for = [&](int S_) { return ((N_cap + S_ - 1) / S_ + 27) / 32 * 32 + 4; };
+    HeadsLayout L = heads_layout(N_cap, stride_for(S), G, S);
     while (static_cast<size_t>(L.total) + 1024 > static_cast<size_t>(dev.max_smem_optin) && S < kMaxSplit) {
         S *= 2;
-        L = heads_layout(N_cap, (N_cap + S - 1) / S, G, S);
+        L = heads_layout(N_cap, stride_for(S), G, S);
     }
     const size_t smem = static_cast<size_t>(L.total) + 1024;
     if (smem > static_cast<size_t>(dev.max_smem_optin))
@@ -866,7 +881,8 @@ extern "C" SPARSE_API int sparse_select_topk_heads(const uint16_t *Q, const floa
     p.n_local = n_local;
     p.k_sel = k;
     p.k_tot_next = k_tot;
-    const int rows_max = (N_cap + S - 1) / S;
+    // per-head stride of the raw scores: the slice's rows, = 4 mod 32 (no bank conflicts)
+    const int rows_max = ((N_cap + S - 1) / S + 27) / 32 * 32 + 4;
     static int configured[64];
     rc = sp_host::configure_kernel(reinterpret_cast<const void *>(select_heads_kernel), static_cast<int>(smem),
                                    dev.device, configured);
