@@ -89,7 +89,7 @@ def measured_peaks():
 
 
 ATTN_SOURCES = ("sparse_attn.cu", "attn_core.cuh", "common.cuh")
-FUSED_SOURCES = ("forecast.cu", "attn_core.cuh", "select_core.cuh", "common.cuh")
+FUSED_SOURCES = ("forecast.cu", "attn_core.cuh", "select_core.cuh", "select_layout.cuh", "common.cuh")
 
 
 def kernel_source_hash(files=ATTN_SOURCES) -> str:
