@@ -817,15 +817,47 @@ def run_verify_case(args, dev):
 
         def run():
             binding.sparse_verify_attn_grouped(x["Q"], x["K"], x["V"], x["I"], C, sh.window_blocks, x["seq_len"], O,
-                                               status=status, shared=shared)
+                                               status=status, shared=shared, n_split=args.n_split)
         binding.sparse_verify_attn_grouped(x["Q"], x["K"], x["V"], x["I"], C, sh.window_blocks, x["seq_len"], O,
-                                           blocks_loaded=loaded, status=status, shared=shared)
+                                           blocks_loaded=loaded, status=status, shared=shared, n_split=args.n_split)
         t = _event_times(run, args.steps, args.warmup, evict)
         nbytes = int(loaded.item()) * KV_BLOCK_BYTES
         gbs, frac = _rate(nbytes, t["median_us"], peak)
         out[key] = {"C": C, "mode": "B (first query's layout)" if shared else "A (merged union)",
                     "blocks_loaded": int(loaded.item()), "bytes_loaded": nbytes, **t,
                     "achieved_gbs": gbs, "frac_of_measured_hbm": frac}
+    # a model's verification round: 32 layers back to back in one CUDA graph (programmatic
+    # dependent launch overlaps each launch's start with the previous one's end), over
+    # 4 physical KV layers of 1.07 GB each (reuse distance far beyond L2)
+    layers, phys = 32, 4
+    Ks, Vs = [x["K"]], [x["V"]]
+    for q_ in range(1, phys):
+        Ks.append(wl.randn_bf16(tuple(x["K"].shape), wl._subseed(sh.seed, 90, q_), dev))
+        Vs.append(wl.randn_bf16(tuple(x["V"].shape), wl._subseed(sh.seed, 91, q_), dev))
+    cur = torch.cuda.current_stream(dev)
+    for key, shared in (("grouped", False), ("shared_layout", True)):
+        g_ = torch.cuda.CUDAGraph()
+        s_ = torch.cuda.Stream(device=dev)
+        s_.wait_stream(cur)
+        with torch.cuda.graph(g_, stream=s_):
+            for l in range(layers):
+                binding.sparse_verify_attn_grouped(x["Q"], Ks[l % phys], Vs[l % phys], x["I"], sh.C, sh.window_blocks,
+                                                   x["seq_len"], O, status=status, shared=shared, stream=s_,
+                                                   n_split=args.n_split)
+        for _ in range(2):
+            g_.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(3, args.steps // 10)
+        a.record()
+        for _ in range(reps):
+            g_.replay()
+        b.record()
+        torch.cuda.synchronize(dev)
+        us = a.elapsed_time(b) * 1e3 / (reps * layers)
+        gbs, frac = _rate(out[key]["bytes_loaded"], us, peak)
+        out[key]["chained"] = {"layers": layers, "physical_kv_layers": phys, "avg_launch_us": round(us, 2),
+                               "achieved_gbs": gbs, "frac_of_measured_hbm": frac,
+                               "rounds_per_s": round(1e6 / (us * layers), 1)}
     assert status.item() == 0, f"device status {status.item()}"
     g, u = out["grouped"], out["ungrouped"]
     out["bytes_ratio"] = round(g["bytes_loaded"] / u["bytes_loaded"], 4)

@@ -50,7 +50,11 @@ namespace {
 using namespace sp;
 
 // Merged union of the group's block sets (SSV mode A): ulist ascending, umask[u] the
-// queries of the group whose set contains ulist[u].  Returns the union size.
+// queries of the group whose set contains ulist[u]; ctrl[kCtrlList] = the union size.
+// Up to kUnionBitmapBlocks blocks in the sequence the union comes from a bitmap over
+// the blocks (O(entries)); beyond, every entry compares itself with all others.
+constexpr int kUnionBitmapBlocks = 4096;
+static_assert(2 * (kUnionBitmapBlocks / 32) <= kMaxUnion, "union bitmap and prefix fit the entry scratch");
 template <bool VERIFY>
 __device__ __forceinline__ void build_union(const AttnParams &p, uint8_t *base, int b, int g, int q0,
                                             int nb, int *ctrl)
@@ -88,6 +92,58 @@ __device__ __forceinline__ void build_union(const AttnParams &p, uint8_t *base, 
     }
     for (int e = tid; e < kMaxUnion; e += kThreads)
         umask[e] = 0u;
+    if (nb <= kUnionBitmapBlocks) {
+        // a bitmap over the blocks: each entry sets its bit; a block's position in the
+        // ascending union is the number of set bits below it
+        uint32_t *bits = reinterpret_cast<uint32_t *>(base + kOffEntF);   // [kUnionBitmapBlocks / 32]
+        uint32_t *pref = bits + kUnionBitmapBlocks / 32;                  // exclusive popcount prefix
+        const int nw = (nb + 31) / 32;
+        for (int w = tid; w < nw; w += kThreads)
+            bits[w] = 0u;
+        __syncthreads();
+        for (int e = tid; e < n_ent; e += kThreads) {
+            const int v = ent_v[e];
+            if (v != INT_MAX)
+                atomicOr(&bits[v >> 5], 1u << (v & 31));
+        }
+        __syncthreads();
+        if (tid < 32) {
+            constexpr int kPer = kUnionBitmapBlocks / 32 / 32;   // words per lane
+            int c[kPer], sum = 0;
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int w = tid * kPer + i;
+                c[i] = w < nw ? __popc(bits[w]) : 0;
+                sum += c[i];
+            }
+            int incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o)
+                    incl += n;
+            }
+            int run = incl - sum;
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                pref[tid * kPer + i] = static_cast<uint32_t>(run);
+                run += c[i];
+            }
+            if (tid == 31)
+                ctrl[kCtrlList] = incl;
+        }
+        __syncthreads();
+        for (int e = tid; e < n_ent; e += kThreads) {
+            const int v = ent_v[e];
+            if (v == INT_MAX)
+                continue;
+            const uint32_t w = bits[v >> 5];
+            const int pos = static_cast<int>(pref[v >> 5]) + __popc(w & ((1u << (v & 31)) - 1u));
+            ulist[pos] = v;   // equal entries write the same block
+            atomicOr(&umask[pos], ent_m[e]);
+        }
+        return;
+    }
     __syncthreads();
     for (int e = tid; e < n_ent; e += kThreads) {
         const int v = ent_v[e];
