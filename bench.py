@@ -1202,6 +1202,81 @@ def run_prefill_case(args, dev):
     print(json.dumps(line), flush=True)
 
 
+def run_refresh_case(args, dev):
+    """SSV's refresh / reuse schedule (mechanism 2) on the 64K verification shape over a
+    32-layer round: a refresh layer routes the 8 verification queries of every pair on
+    the layer's compressed keys (sparse_nsa_select, NSA routing, the 8 window blocks as
+    the local blocks and 16 routed blocks outside them) and verifies with those lists;
+    a reuse layer verifies with the lists of the last refresh layer.  Each schedule is
+    one CUDA graph of the 32 layers (4 physical KV layers, 1.07 GB each)."""
+    import torch
+    from block_sparse_long_pool_gb300 import binding
+    from block_sparse_long_pool_gb300 import workloads as wl
+    sh = wl.VERIFY_64K
+    peak, src = measured_peaks()
+    x = wl.verify_inputs(sh, dev)
+    B, H_kv, T, N = sh.B, sh.H_kv, sh.T, sh.T // BLK
+    layers, phys = 32, 4
+    Ks, Vs = [x["K"]], [x["V"]]
+    for q_ in range(1, phys):
+        Ks.append(wl.randn_bf16(tuple(x["K"].shape), wl._subseed(sh.seed, 90, q_), dev))
+        Vs.append(wl.randn_bf16(tuple(x["V"].shape), wl._subseed(sh.seed, 91, q_), dev))
+    # compressed keys of each physical layer: one row per 64-token block
+    khs = []
+    for q_ in range(phys):
+        kh = torch.empty((B, H_kv, N, D), dtype=torch.bfloat16, device=dev)
+        vh = torch.empty_like(kh)
+        binding.sparse_nsa_compress(Ks[q_], Vs[q_], kh, vh, 0, T, cmp=(BLK, BLK))
+        khs.append(kh)
+    k_tot = sh.window_blocks + sh.n_sel
+    idx = torch.empty((B, H_kv, sh.N_q, k_tot), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B, H_kv, sh.N_q), dtype=torch.int32, device=dev)
+    O = torch.empty_like(x["Q"])
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    cur = torch.cuda.current_stream(dev)
+
+    def layer(l, refresh, st):
+        if refresh:
+            binding.sparse_nsa_select(x["Q"], khs[l % phys], x["seq_len"], 0, sh.window_blocks, sh.n_sel, idx, cnt,
+                                      cmp=(BLK, BLK), status=status, stream=st)
+        binding.sparse_verify_attn_grouped(x["Q"], Ks[l % phys], Vs[l % phys], idx, sh.C, sh.window_blocks,
+                                           x["seq_len"], O, status=status, stream=st)
+
+    def timed(schedule):
+        g_ = torch.cuda.CUDAGraph()
+        s_ = torch.cuda.Stream(device=dev)
+        s_.wait_stream(cur)
+        with torch.cuda.graph(g_, stream=s_):
+            for l in range(layers):
+                layer(l, schedule(l), s_)
+        for _ in range(2):
+            g_.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(3, args.steps // 10)
+        a.record()
+        for _ in range(reps):
+            g_.replay()
+        b.record()
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) * 1e3 / reps
+
+    t_all = timed(lambda l: True)
+    t_none = timed(lambda l: l == 0)
+    out = {"case": "refresh64k", "workload": sh.name + "_32layers",
+           "unit_of_work": f"one verification round: {layers} layers x {sh.N_q} queries x {B * H_kv} pairs",
+           "routing": "sparse_nsa_select: G heads per group, per-head softmax over the 1024 block rows, summed; "
+                      "top-16 outside the 8 window blocks",
+           "all_refresh_us": round(t_all, 1), "refresh_layer_us": round(t_all / layers, 2),
+           "reuse_layer_us": round((t_none - t_all / layers) / (layers - 1), 2)}
+    for r in (2, 4, 8):
+        t_r = timed(lambda l, r=r: l % r == 0)
+        out[f"refresh_every_{r}"] = {"round_us": round(t_r, 1), "rounds_per_s": round(1e6 / t_r, 1),
+                                     "speedup_vs_all_refresh": round(t_all / t_r, 3)}
+    torch.cuda.synchronize()
+    assert status.item() == 0, f"device status {status.item()}"
+    print(json.dumps(out), flush=True)
+
+
 def run_other_case(args, local_rank):
     import torch
     from block_sparse_long_pool_gb300 import workloads as wl
@@ -1219,6 +1294,8 @@ def run_other_case(args, local_rank):
         run_nsa_case(args, dev)
     elif args.case == "prefill32k":
         run_prefill_case(args, dev)
+    elif args.case == "refresh64k":
+        run_refresh_case(args, dev)
     else:
         run_offload_case(args, dev)
 
@@ -1232,10 +1309,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", choices=["step", "layer", "select", "single4k", "append32k", "verify64k",
-                                       "offload128k", "nsa128k", "prefill32k"], default="step",
+                                       "offload128k", "nsa128k", "prefill32k", "refresh64k"], default="step",
                     help="step: the 80-layer decode step (the bench line); layer: one physical layer, "
                          "kernels serialised and timed alone (for profiling); select: selection only; "
-                         "single4k / append32k / verify64k / offload128k / nsa128k / prefill32k: the other "
+                         "single4k / append32k / verify64k / offload128k / nsa128k / prefill32k / refresh64k: "
+                         "the other "
                          "workloads, "
                          "one line each")
     ap.add_argument("--n-split", type=int, default=0)
@@ -1253,7 +1331,7 @@ def main():
     rank, world, local_rank = dist_env()
     if args.case in ("layer", "select"):
         run_layer_case(args, local_rank)
-    elif args.case in ("single4k", "append32k", "verify64k", "offload128k", "nsa128k", "prefill32k"):
+    elif args.case in ("single4k", "append32k", "verify64k", "offload128k", "nsa128k", "prefill32k", "refresh64k"):
         run_other_case(args, local_rank)
     elif args.impl == "reference":
         run_reference(args, rank, world, local_rank)

@@ -62,7 +62,7 @@ SIGNATURES = {
     "sparse_decode_attn_nsa": (_I, [_P, _P, _P, _LL, _P, _P, _I, _I, _I, _P, _P, _I, _P, _I, _I, _I, _LL, _P, _F,
                                     _P, _P, _SZ, _I, _U, _P, _P]),
     "sparse_nsa_compress": (_I, [_P, _P, _LL, _I, _I, _LL, _I, _I, _I, _P, _P, _I, _P]),
-    "sparse_nsa_select": (_I, [_P, _P, _I, _I, _I, _P, _I, _I, _I, _F, _I, _I, _I, _P, _P, _I, _P, _P]),
+    "sparse_nsa_select": (_I, [_P, _P, _I, _I, _I, _P, _I, _I, _I, _I, _F, _I, _I, _I, _P, _P, _I, _P, _P]),
     "sparse_decode_attn_nsa_workspace_size": (_SZ, [_I, _I, _I]),
 }
 
@@ -417,16 +417,22 @@ def sparse_nsa_compress(k_cache, v_cache, khat, vhat, len_before: int, n_new: in
 def sparse_nsa_select(Q, khat, seq_len, n_init: int, n_local: int, k: int, idx_out, count_out, cmp=(32, 16),
                       scale: float = 0.0, status=None, stream=None):
     """NSA routing: per-head softmax over the compressed rows khat [B][H_kv][R][128],
-    summed over the group, max-pooled onto the 64-token blocks, top-k."""
-    B, H_q, _ = Q.shape
+    summed over the group, max-pooled onto the 64-token blocks, top-k.  Q [B][H_q][128]
+    (idx_out [B][H_kv][k_tot], count_out [B][H_kv]) or, for several queries per batch
+    element, Q [B][N_q][H_q][128] (idx_out [B][H_kv][N_q][k_tot], count_out [B][H_kv][N_q])."""
+    if Q.dim() == 3:
+        B, H_q, _ = Q.shape
+        N_q = 1
+    else:
+        B, N_q, H_q, _ = Q.shape
     _, H_kv, R, _ = khat.shape
-    k_tot = idx_out.shape[2]
-    _need(Q, "Q", torch.bfloat16, shape=(B, H_q, D))
+    k_tot = idx_out.shape[-1]
+    _need(Q, "Q", torch.bfloat16, shape=(B, H_q, D) if Q.dim() == 3 else (B, N_q, H_q, D))
     _need(khat, "khat", torch.bfloat16, shape=(B, H_kv, R, D))
     _need(seq_len, "seq_len", torch.int32, shape=(B,))
-    _need(idx_out, "idx_out", torch.int32, shape=(B, H_kv, k_tot))
-    _need(count_out, "count_out", torch.int32, shape=(B, H_kv))
-    rc = load().sparse_nsa_select(_ptr(Q), _ptr(khat), R, int(cmp[0]), int(cmp[1]), _ptr(seq_len), B, H_q, H_kv,
+    _need(idx_out, "idx_out", torch.int32, shape=(B, H_kv, k_tot) if Q.dim() == 3 else (B, H_kv, N_q, k_tot))
+    _need(count_out, "count_out", torch.int32, shape=(B, H_kv) if Q.dim() == 3 else (B, H_kv, N_q))
+    rc = load().sparse_nsa_select(_ptr(Q), _ptr(khat), R, int(cmp[0]), int(cmp[1]), _ptr(seq_len), B, N_q, H_q, H_kv,
                                   float(scale), n_init, n_local, k, _ptr(idx_out), _ptr(count_out), k_tot,
                                   _ptr(status), _stream(stream))
     _check(rc, "sparse_nsa_select")

@@ -42,6 +42,7 @@ struct RouteParams {
     int *count;
     int *status;
     int H_q, H_kv, G;
+    int N_q;              // queries per batch element (each routed on its own)
     int n_rows_cap;       // rows per pair in khat
     int cmp_len;          // row geometry: [cmp_stride * j, cmp_stride * j + cmp_len)
     int cmp_stride;
@@ -105,7 +106,8 @@ __global__ void __launch_bounds__(kFThreads, 1) nsa_route_kernel(const __grid_co
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int rank = static_cast<int>(blockIdx.x);
-    const int pair = static_cast<int>(blockIdx.y);
+    const int unit = static_cast<int>(blockIdx.y);   // (pair, query)
+    const int pair = unit / p.N_q, qi = unit - pair * p.N_q;
     const int b = pair / p.H_kv, g = pair % p.H_kv;
     const int l = p.block_rows ? kBlk : p.cmp_len;
     const int s = p.block_rows ? kBlk : p.cmp_stride;
@@ -170,7 +172,8 @@ __global__ void __launch_bounds__(kFThreads, 1) nsa_route_kernel(const __grid_co
         QueryFrags<NT> q;
         {
             AttnParams ap = {};
-            ap.Q = p.Q;
+            ap.Q = p.Q + static_cast<size_t>(b) * (p.N_q - 1) * p.H_q * kD +
+                   static_cast<size_t>(qi) * p.H_q * kD;   // query qi of batch element b
             ap.H_q = p.H_q;
             ap.G = G;
             load_query<NT, false>(q, ap, b, g, 0, G, lane);
@@ -321,7 +324,7 @@ __global__ void __launch_bounds__(kFThreads, 1) nsa_route_kernel(const __grid_co
             if (ready) {
                 topk_write_warp(base_s + L.off_keys, 0u, 0, nb, p.n_init, p.n_local,
                                 max(0, nb - p.n_local - p.n_init) <= p.k_sel, p.k_sel <= 0, prefix, need,
-                                p.idx + static_cast<size_t>(pair) * p.k_tot, p.k_tot, p.count + pair, p.status, lane);
+                                p.idx + static_cast<size_t>(unit) * p.k_tot, p.k_tot, p.count + unit, p.status, lane);
             } else if (lane == 0) {
                 report(p.status, SPARSE_ERR_TIMEOUT);
             }
@@ -333,7 +336,7 @@ __global__ void __launch_bounds__(kFThreads, 1) nsa_route_kernel(const __grid_co
 static_assert((kRouteTopkThreads / 32) * 256 <= kCoarseBins + kTopkList, "routing radix bins");
 
 template <int NT>
-int launch_route(const RouteParams &p, const CUtensorMap &km, int S, long long pairs, size_t smem, int device,
+int launch_route(const RouteParams &p, const CUtensorMap &km, int S, long long units, size_t smem, int device,
                  cudaStream_t stream)
 {
     auto kern = nsa_route_kernel<NT>;
@@ -343,7 +346,7 @@ int launch_route(const RouteParams &p, const CUtensorMap &km, int S, long long p
     if (rc != SPARSE_OK)
         return rc;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(S), static_cast<unsigned>(pairs), 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(S), static_cast<unsigned>(units), 1);
     cfg.blockDim = dim3(kFThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -366,7 +369,7 @@ int launch_route(const RouteParams &p, const CUtensorMap &km, int S, long long p
 }  // namespace
 
 extern "C" SPARSE_API int sparse_nsa_select(const uint16_t *Q, const uint16_t *khat, int n_rows_cap, int cmp_len,
-                                            int cmp_stride, const int *seq_len, int B, int H_q, int H_kv,
+                                            int cmp_stride, const int *seq_len, int B, int N_q, int H_q, int H_kv,
                                             float scale, int n_init, int n_local, int k, int *idx_out,
                                             int *count_out, int k_tot, int *status, void *stream)
 {
@@ -377,7 +380,8 @@ extern "C" SPARSE_API int sparse_nsa_select(const uint16_t *Q, const uint16_t *k
         return fail(SPARSE_ERR_INVALID_ARG, "%s: null pointer", name);
     if (!aligned16(Q) || !aligned16(khat))
         return fail(SPARSE_ERR_INVALID_ARG, "%s: Q and khat must be 16-byte aligned", name);
-    if (B < 1 || H_kv < 1 || H_q < H_kv || H_q % H_kv != 0 || n_rows_cap < 1 || n_init < 0 || n_local < 0 || k < 0)
+    if (B < 1 || N_q < 1 || H_kv < 1 || H_q < H_kv || H_q % H_kv != 0 || n_rows_cap < 1 || n_init < 0 ||
+        n_local < 0 || k < 0)
         return fail(SPARSE_ERR_INVALID_ARG, "%s: bad size", name);
     if (!(cmp_len == 0 && cmp_stride == 0) && !(cmp_stride >= 1 && cmp_stride <= cmp_len && cmp_len <= 1024))
         return fail(SPARSE_ERR_INVALID_ARG, "%s: cmp_len=%d cmp_stride=%d", name, cmp_len, cmp_stride);
@@ -389,8 +393,9 @@ extern "C" SPARSE_API int sparse_nsa_select(const uint16_t *Q, const uint16_t *k
     if (G > 16)
         return fail(SPARSE_ERR_UNSUPPORTED, "%s: G=%d > 16", name, G);
     const long long pairs = static_cast<long long>(B) * H_kv;
-    if (pairs > 65535)
-        return fail(SPARSE_ERR_UNSUPPORTED, "%s: B*H_kv=%lld > 65535", name, pairs);
+    const long long units = pairs * N_q;
+    if (units > 65535)
+        return fail(SPARSE_ERR_UNSUPPORTED, "%s: B*H_kv*N_q=%lld > 65535", name, units);
     if (n_rows_cap > INT_MAX / 64)
         return fail(SPARSE_ERR_UNSUPPORTED, "%s: n_rows_cap too large", name);
     sp_host::DeviceInfo dev;
@@ -407,7 +412,7 @@ extern "C" SPARSE_API int sparse_nsa_select(const uint16_t *Q, const uint16_t *k
     // memory): the most with pairs * S <= SMs (one wave), then more if the rows do not
     // fit; stages: as many of 2..6 as fit.
     int S = 1;
-    while (S < kMaxSplit && pairs * S * 2 <= dev.sm_count && n_blocks_cap / (S * 2) >= 16)
+    while (S < kMaxSplit && units * S * 2 <= dev.sm_count && n_blocks_cap / (S * 2) >= 16)
         S *= 2;
     // rows a CTA loads at most (its blocks' rows and the left halo), rounded to 4 mod 32
     auto rows_for = [&](int S_) {
@@ -442,6 +447,7 @@ extern "C" SPARSE_API int sparse_nsa_select(const uint16_t *Q, const uint16_t *k
     p.H_q = H_q;
     p.H_kv = H_kv;
     p.G = G;
+    p.N_q = N_q;
     p.n_rows_cap = n_rows_cap;
     p.cmp_len = cmp_len;
     p.cmp_stride = cmp_stride;
@@ -455,6 +461,6 @@ extern "C" SPARSE_API int sparse_nsa_select(const uint16_t *Q, const uint16_t *k
     p.k_tot = k_tot;
     p.scale_log2 = scale_log2_of(scale);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return G <= 8 ? launch_route<1>(p, km, S, pairs, smem, dev.device, st)
-                  : launch_route<2>(p, km, S, pairs, smem, dev.device, st);
+    return G <= 8 ? launch_route<1>(p, km, S, units, smem, dev.device, st)
+                  : launch_route<2>(p, km, S, units, smem, dev.device, st);
 }

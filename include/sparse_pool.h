@@ -449,12 +449,15 @@ SPARSE_API int sparse_nsa_compress(const uint16_t *k_cache, const uint16_t *v_ca
  * sparse_select_topk writes them (ties to the lower block).  The scores are computed on
  * the bf16 tensor cores from the bf16 rows, exactly as the compressed branch scores
  * them; with cmp_len = cmp_stride = 0 the rows are the blocks themselves.
- *   Q           [B][H_q][128] bf16;  khat [B][H_kv][n_rows_cap][128] bf16.
- *   idx_out     [B][H_kv][k_tot] int32;  count_out [B][H_kv] int32.
- * G = H_q / H_kv <= 16.
+ *   Q           [B][N_q][H_q][128] bf16: N_q queries per batch element, each routed on
+ *               its own (N_q = 1 at decode; the verification queries of [SSV]'s refresh
+ *               layers, whose lists the reuse layers then take as they are).
+ *   khat        [B][H_kv][n_rows_cap][128] bf16.
+ *   idx_out     [B][H_kv][N_q][k_tot] int32;  count_out [B][H_kv][N_q] int32.
+ * G = H_q / H_kv <= 16; B * H_kv * N_q <= 65535.
  */
 SPARSE_API int sparse_nsa_select(const uint16_t *Q, const uint16_t *khat, int n_rows_cap, int cmp_len,
-                                 int cmp_stride, const int *seq_len, int B, int H_q, int H_kv,
+                                 int cmp_stride, const int *seq_len, int B, int N_q, int H_q, int H_kv,
                                  float scale, int n_init, int n_local, int k, int *idx_out,
                                  int *count_out, int k_tot, int *status, void *stream);
 

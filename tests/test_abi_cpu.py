@@ -232,8 +232,9 @@ def test_nsa_compress_and_select_reject_bad_arguments(lib):
     assert call_c(a11=3) == binding.SPARSE_ERR_INVALID_ARG            # more windows than rows
     assert call_c(a5=0, a6=20) == binding.SPARSE_OK                   # no window completes: nothing to do
     g = lib.sparse_nsa_select
-    # Q, khat, n_rows_cap, l, s, seq_len, B, H_q, H_kv, scale, n_init, n_local, k, idx, count, k_tot, status, stream
-    ok2 = [FAKE, FAKE, 64, 32, 16, FAKE, 1, 8, 1, 0.0, 1, 2, 4, FAKE, FAKE, 7, None, None]
+    # Q, khat, n_rows_cap, l, s, seq_len, B, N_q, H_q, H_kv, scale, n_init, n_local, k, idx, count, k_tot,
+    # status, stream
+    ok2 = [FAKE, FAKE, 64, 32, 16, FAKE, 1, 1, 8, 1, 0.0, 1, 2, 4, FAKE, FAKE, 7, None, None]
 
     def call_s(**kw):
         a = list(ok2)
@@ -242,10 +243,12 @@ def test_nsa_compress_and_select_reject_bad_arguments(lib):
         return g(*a)
 
     assert call_s(a1=None) == binding.SPARSE_ERR_INVALID_ARG          # no khat
-    assert call_s(a15=6) == binding.SPARSE_ERR_INVALID_ARG            # k_tot too small
+    assert call_s(a16=6) == binding.SPARSE_ERR_INVALID_ARG            # k_tot too small
     assert call_s(a3=16, a4=32) == binding.SPARSE_ERR_INVALID_ARG     # stride above the kernel
-    assert call_s(a7=64, a8=2) == binding.SPARSE_ERR_UNSUPPORTED      # G = 32
-    assert call_s(a9=-1.0) == binding.SPARSE_ERR_INVALID_ARG          # negative scale
+    assert call_s(a8=64, a9=2) == binding.SPARSE_ERR_UNSUPPORTED      # G = 32
+    assert call_s(a10=-1.0) == binding.SPARSE_ERR_INVALID_ARG         # negative scale
+    assert call_s(a7=0) == binding.SPARSE_ERR_INVALID_ARG             # no query
+    assert call_s(a6=4096, a7=16) == binding.SPARSE_ERR_UNSUPPORTED   # too many (pair, query) units
 
 
 def test_prefill_select_rejects_bad_arguments(lib):

@@ -522,3 +522,28 @@ def test_nsa_select_full_size_sampled_pairs():
                                        shape.n_init, shape.n_local, shape.k, k_tot, n_blocks_cap=shape.N_b)
     _assert_route_matches(idx.view(P, k_tot)[sample], cnt.view(P)[sample], ir, cr, sc, np.full(len(sample), T),
                           shape.n_init, shape.n_local, shape.k)
+
+
+def test_nsa_select_many_queries_per_batch_element():
+    """Routing of N_q verification queries per batch element (each its own lists),
+    query by query against the oracle."""
+    B, N_q, H_q, H_kv, T_cap = 2, 8, 16, 4, 45 * BLK
+    l, s = 32, 16
+    lens_b = [45 * BLK, 30 * BLK + 7]
+    c = _route_case(B, H_q, H_kv, T_cap, lens_b, (l, s), seed=470)
+    Qm = wl.randn_bf16((B, N_q, H_q, D), 471, "cuda")
+    n_init, n_local, k = 1, 2, 6
+    k_tot = n_init + n_local + k
+    idx = torch.full((B, H_kv, N_q, k_tot), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((B, H_kv, N_q), -7, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.sparse_nsa_select(Qm, c["khat"], c["seq"], n_init, n_local, k, idx, cnt, cmp=(l, s), status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    P, G = B * H_kv, H_q // H_kv
+    kr = _bits_to_f64(c["kb"])
+    Qb = bits(Qm)   # [B][N_q][H_q][D]
+    for q in range(N_q):
+        Qq = Qb[:, q].reshape(P, G, D)
+        ir, cr, sc = oracle.select_windows(Qq, kr, c["lens_p"], l, s, n_init, n_local, k, k_tot, n_blocks_cap=45)
+        _assert_route_matches(idx[:, :, q], cnt[:, :, q], ir, cr, sc, c["lens_p"], n_init, n_local, k)
