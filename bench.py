@@ -841,9 +841,11 @@ def run_verify_case(args, dev):
         s_.wait_stream(cur)
         with torch.cuda.graph(g_, stream=s_):
             for l in range(layers):
+                # the lists are the round's own (routed before it): the union and the
+                # K/V stream of layer l overlap the drain of layer l - 1
                 binding.sparse_verify_attn_grouped(x["Q"], Ks[l % phys], Vs[l % phys], x["I"], sh.C, sh.window_blocks,
                                                    x["seq_len"], O, status=status, shared=shared, stream=s_,
-                                                   n_split=args.n_split)
+                                                   n_split=args.n_split, flags=binding.SPARSE_ATTN_BLOCKS_READY)
         for _ in range(2):
             g_.replay()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -1239,8 +1241,13 @@ def run_refresh_case(args, dev):
         if refresh:
             binding.sparse_nsa_select(x["Q"], khs[l % phys], x["seq_len"], 0, sh.window_blocks, sh.n_sel, idx, cnt,
                                       cmp=(BLK, BLK), status=status, stream=st)
+        # a reuse layer's lists were routed at least two launches back (the verification
+        # kernel lets its successor start only after its own wait): its union and K/V
+        # stream may overlap the previous layer's drain; a refresh layer's wait for the
+        # routing just before it
         binding.sparse_verify_attn_grouped(x["Q"], Ks[l % phys], Vs[l % phys], idx, sh.C, sh.window_blocks,
-                                           x["seq_len"], O, status=status, stream=st)
+                                           x["seq_len"], O, status=status, stream=st,
+                                           flags=0 if refresh else binding.SPARSE_ATTN_BLOCKS_READY)
 
     def timed(schedule):
         g_ = torch.cuda.CUDAGraph()

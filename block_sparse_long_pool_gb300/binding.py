@@ -55,9 +55,9 @@ SIGNATURES = {
     "sparse_decode_attn_forecast": (_I, [_P, _P, _P, _LL, _P, _P, _I, _P, _I, _I, _I, _F, _P, _P, _P, _P, _I, _I,
                                          _I, _I, _P, _P, _I, _I, _U, _P, _P]),
     "sparse_verify_attn_grouped": (_I, [_P, _P, _P, _LL, _P, _I, _I, _I, _I, _P, _I, _I, _I, _F, _P, _P, _I,
-                                        _P, _P]),
+                                        _U, _P, _P]),
     "sparse_verify_attn_shared": (_I, [_P, _P, _P, _LL, _P, _I, _I, _I, _I, _P, _I, _I, _I, _F, _P, _P, _I,
-                                       _P, _P]),
+                                       _U, _P, _P]),
     "sparse_gather_offloaded": (_I, [_P, _P, _LL, _P, _P, _I, _I, _I, _P, _P, _P, _I, _P, _P]),
     "sparse_decode_attn_nsa": (_I, [_P, _P, _P, _LL, _P, _P, _I, _I, _I, _P, _P, _I, _P, _I, _I, _I, _LL, _P, _F,
                                     _P, _P, _SZ, _I, _U, _P, _P]),
@@ -244,8 +244,9 @@ def sparse_decode_attn(Q, k_base, v_base, blk_logical, count, seq_len, O, lse=No
 
     k_base/v_base hold B*H_kv pair regions of pair_stride x 128 rows (a cache
     [B][H_kv][T_cap][128] or a ring slot [B][H_kv][k_tot][64][128]).  ``flags`` may be
-    SPARSE_ATTN_BLOCKS_READY: the block list and K/V are complete before the previous
-    kernel on ``stream`` finishes, so K/V streaming may start while it drains."""
+    SPARSE_ATTN_BLOCKS_READY: the block list and K/V are not written by the previous
+    kernel on ``stream`` (they are already complete while it runs), so K/V streaming may
+    start while it drains."""
     B, H_q, H_kv, k_tot, pair_stride = _decode_args(Q, k_base, v_base, blk_logical, count, seq_len, O, lse,
                                                     blk_slot)
     ws, ws_bytes = _ws(workspace)
@@ -317,7 +318,7 @@ def sparse_decode_attn_forecast(Q, k_cache, v_cache, blk_idx, count, seq_len, O,
 
 def sparse_verify_attn_grouped(Q, k_cache, v_cache, idx_q, C: int, window_blocks: int, seq_len, O,
                                blocks_loaded=None, scale: float = 0.0, n_split: int = 0, status=None,
-                               stream=None, shared: bool = False):
+                               stream=None, shared: bool = False, flags: int = 0):
     """Grouped verification: Q [B][N_q][H_q][128], idx_q [B][H_kv][N_q][n_sel].  Mode A
     (each query over its own set), or with ``shared`` mode B (sparse_verify_attn_shared:
     every query over its group's first query's set)."""
@@ -334,7 +335,8 @@ def sparse_verify_attn_grouped(Q, k_cache, v_cache, idx_q, C: int, window_blocks
         _need(blocks_loaded, "blocks_loaded", torch.int64)
     fn = load().sparse_verify_attn_shared if shared else load().sparse_verify_attn_grouped
     rc = fn(_ptr(Q), _ptr(k_cache), _ptr(v_cache), T_cap, _ptr(idx_q), n_sel, N_q, C, window_blocks, _ptr(seq_len), B,
-            H_q, H_kv, float(scale), _ptr(O), _ptr(blocks_loaded), n_split, _ptr(status), _stream(stream))
+            H_q, H_kv, float(scale), _ptr(O), _ptr(blocks_loaded), n_split, int(flags), _ptr(status),
+            _stream(stream))
     _check(rc, "sparse_verify_attn_shared" if shared else "sparse_verify_attn_grouped")
 
 

@@ -201,7 +201,7 @@ __device__ __forceinline__ void attn_cluster_cta(const CUtensorMap *kmap, const 
     // the stream drains.  With SPARSE_ATTN_BLOCKS_READY the block list, lengths and K/V
     // are already complete (the caller's promise), so only Q and the outputs wait;
     // otherwise every input may come from that kernel and everything waits.
-    const bool early = !VERIFY && (p.flags & SPARSE_ATTN_BLOCKS_READY) != 0u;
+    const bool early = (p.flags & SPARSE_ATTN_BLOCKS_READY) != 0u;
     if (!early)
         griddep_wait();
 
@@ -1324,10 +1324,12 @@ namespace {
 static int verify_impl(const char *name, unsigned mode, const uint16_t *Q, const uint16_t *k_cache,
                        const uint16_t *v_cache, long long T_cap, const int *idx_q, int n_sel, int N_q, int C,
                        int window_blocks, const int *seq_len, int B, int H_q, int H_kv, float scale, uint16_t *O,
-                       long long *blocks_loaded, int n_split, int *status, void *stream)
+                       long long *blocks_loaded, int n_split, unsigned flags, int *status, void *stream)
 {
     using sp_host::aligned16;
     using sp_host::fail;
+    if ((flags & ~SPARSE_ATTN_BLOCKS_READY) != 0u)
+        return fail(SPARSE_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags);
     if (!Q || !k_cache || !v_cache || !seq_len || !O || (n_sel > 0 && !idx_q))
         return fail(SPARSE_ERR_INVALID_ARG, "%s: null pointer", name);
     if (!aligned16(Q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(O))
@@ -1379,7 +1381,7 @@ static int verify_impl(const char *name, unsigned mode, const uint16_t *Q, const
     p.C = C;
     p.window_blocks = window_blocks;
     p.n_groups = n_groups;
-    p.flags = mode;
+    p.flags = mode | flags;
     p.scale_log2 = scale_log2_of(scale);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return C * G <= 8 ? launch<1, true>(p, km, vm, S, units, dev.device, st)
@@ -1393,10 +1395,11 @@ extern "C" SPARSE_API int sparse_verify_attn_grouped(const uint16_t *Q, const ui
                                                      int n_sel, int N_q, int C, int window_blocks,
                                                      const int *seq_len, int B, int H_q, int H_kv, float scale,
                                                      uint16_t *O, long long *blocks_loaded, int n_split,
-                                                     int *status, void *stream)
+                                                     unsigned flags, int *status, void *stream)
 {
     return verify_impl("sparse_verify_attn_grouped", 0u, Q, k_cache, v_cache, T_cap, idx_q, n_sel, N_q, C,
-                       window_blocks, seq_len, B, H_q, H_kv, scale, O, blocks_loaded, n_split, status, stream);
+                       window_blocks, seq_len, B, H_q, H_kv, scale, O, blocks_loaded, n_split, flags, status,
+                       stream);
 }
 
 extern "C" SPARSE_API int sparse_verify_attn_shared(const uint16_t *Q, const uint16_t *k_cache,
@@ -1404,11 +1407,11 @@ extern "C" SPARSE_API int sparse_verify_attn_shared(const uint16_t *Q, const uin
                                                     int n_sel, int N_q, int C, int window_blocks,
                                                     const int *seq_len, int B, int H_q, int H_kv, float scale,
                                                     uint16_t *O, long long *blocks_loaded, int n_split,
-                                                    int *status, void *stream)
+                                                    unsigned flags, int *status, void *stream)
 {
     return verify_impl("sparse_verify_attn_shared", kVerifySharedLayout, Q, k_cache, v_cache, T_cap, idx_q, n_sel,
-                       N_q, C, window_blocks, seq_len, B, H_q, H_kv, scale, O, blocks_loaded, n_split, status,
-                       stream);
+                       N_q, C, window_blocks, seq_len, B, H_q, H_kv, scale, O, blocks_loaded, n_split, flags,
+                       status, stream);
 }
 
 // ---------------------------------------------------------------- NSA gated three-branch decode

@@ -209,11 +209,16 @@ SPARSE_API int sparse_select_topk_heads(const uint16_t *Q, const float *ktil, co
  * may be scheduled while the kernel before it on the stream is still running, and it
  * waits for that kernel (griddepcontrol.wait) before reading any input -- unless the
  * caller passes SPARSE_ATTN_BLOCKS_READY, which promises that the block table,
- * count, seq_len and the K/V rows are complete before that preceding kernel finishes
- * (produced earlier, or on another stream ordered by an event).  Then the kernel
- * stages its block list and starts streaming K/V at once and waits only before
- * reading Q and writing O and lse.  This is SparDA's decoupling (§4.1): the blocks of
- * layer l+1 are chosen one layer ahead, so their loads need not wait for Q_{l+1}.
+ * count, seq_len and the K/V rows are already complete while that preceding kernel
+ * runs: none of them is written by it (they come from an earlier kernel on the stream,
+ * or from another stream ordered by an event).  Then the kernel stages its block list
+ * and starts streaming K/V at once and waits only before reading Q and writing O and
+ * lse.  This is SparDA's decoupling (§4.1): the blocks of layer l+1 are chosen one
+ * layer ahead, so their loads need not wait for Q_{l+1}.
+ * Every kernel of this library lets its successor start only after its own wait,
+ * except sparse_decode_attn_forecast, which lets it start at once: an input written
+ * two launches back is complete, unless the launch in between is
+ * sparse_decode_attn_forecast.
  */
 #define SPARSE_ATTN_BLOCKS_READY 1u
 /* Use the stream-K path whenever a workspace is given (see `workspace`). */
@@ -342,6 +347,13 @@ SPARSE_API int sparse_decode_attn_forecast(const uint16_t *Q, const uint16_t *k_
  *   blocks_loaded  optional int64 device counter: += |U| for every group (the blocks
  *            this call streams from HBM).  Without grouping the count would be
  *            sum_q |I_q ∪ W|.
+ *   flags    0 or SPARSE_ATTN_BLOCKS_READY: the caller promises that idx_q, seq_len and
+ *            the K/V rows are not written by the kernel preceding this one on the
+ *            stream (e.g. the lists of a reuse layer, routed layers earlier; the
+ *            launch-order rule of sparse_decode_attn), so the union is built and the
+ *            blocks stream while that kernel drains; only Q and the outputs wait for
+ *            it.  Without the flag every input may be that kernel's output and
+ *            everything waits.
  * Limits: C * G <= 16 rows per group tile; C * n_sel + window_blocks <= 512.
  */
 SPARSE_API int sparse_verify_attn_grouped(const uint16_t *Q, const uint16_t *k_cache,
@@ -349,8 +361,8 @@ SPARSE_API int sparse_verify_attn_grouped(const uint16_t *Q, const uint16_t *k_c
                                           const int *idx_q, int n_sel, int N_q, int C,
                                           int window_blocks, const int *seq_len, int B,
                                           int H_q, int H_kv, float scale, uint16_t *O,
-                                          long long *blocks_loaded, int n_split, int *status,
-                                          void *stream);
+                                          long long *blocks_loaded, int n_split, unsigned flags,
+                                          int *status, void *stream);
 
 /*
  * sparse_verify_attn_shared -- [SSV] mechanism 1, mode B (approximate shared index
@@ -366,8 +378,8 @@ SPARSE_API int sparse_verify_attn_shared(const uint16_t *Q, const uint16_t *k_ca
                                          const int *idx_q, int n_sel, int N_q, int C,
                                          int window_blocks, const int *seq_len, int B,
                                          int H_q, int H_kv, float scale, uint16_t *O,
-                                         long long *blocks_loaded, int n_split, int *status,
-                                         void *stream);
+                                         long long *blocks_loaded, int n_split, unsigned flags,
+                                         int *status, void *stream);
 
 /*
  * sparse_decode_attn_nsa -- NSA's gated three-branch decode output, [SSV] "NSA

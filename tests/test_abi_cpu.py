@@ -95,7 +95,7 @@ def test_decode_rejects_bad_arguments(lib):
 
 def test_verify_rejects_bad_arguments(lib):
     f = lib.sparse_verify_attn_grouped
-    args = [FAKE, FAKE, FAKE, 65536, FAKE, 16, 8, 4, 8, FAKE, 4, 32, 8, 0.0, FAKE, None, 0, None, None]
+    args = [FAKE, FAKE, FAKE, 65536, FAKE, 16, 8, 4, 8, FAKE, 4, 32, 8, 0.0, FAKE, None, 0, 0, None, None]
     bad = list(args)
     bad[7] = 5                                    # C*G = 20 rows > 16
     assert f(*bad) == binding.SPARSE_ERR_UNSUPPORTED
@@ -106,6 +106,10 @@ def test_verify_rejects_bad_arguments(lib):
     bad = list(args)
     bad[4] = None
     assert f(*bad) == binding.SPARSE_ERR_INVALID_ARG
+    bad = list(args)
+    bad[17] = 8                                   # an unknown flag bit
+    assert f(*bad) == binding.SPARSE_ERR_INVALID_ARG
+    assert lib.sparse_verify_attn_shared(*bad) == binding.SPARSE_ERR_INVALID_ARG
 
 
 def test_gather_rejects_bad_arguments(lib):

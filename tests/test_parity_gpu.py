@@ -547,6 +547,39 @@ def test_verify_shared_layout_ragged_groups(n_split, C):
     assert loaded == union
 
 
+@pytest.mark.parametrize("shared", [False, True])
+def test_verify_chain_with_blocks_ready(shared):
+    """A chain of verification launches on one stream where each launch's Q is the
+    previous launch's O: with SPARSE_ATTN_BLOCKS_READY the union and the K/V stream start
+    early but Q still waits, so the chain equals the one without the flag bit for bit,
+    and its first link equals the oracle."""
+    sh = wl.VerifyShape("chain", B=2, H_q=16, H_kv=4, T=48 * BLK + 5, N_q=8, n_sel=12, gamma=0.6,
+                        window_tokens=4 * BLK, C=4, seed=37)
+    inp = wl.verify_inputs(sh, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def chain(flags):
+        outs = [inp["Q"]]
+        for _ in range(4):
+            O = torch.full_like(inp["Q"], 3.0)
+            outs.append(O)
+        for l in range(4):
+            binding.sparse_verify_attn_grouped(outs[l], inp["K"], inp["V"], inp["I"], sh.C, sh.window_blocks,
+                                               inp["seq_len"], outs[l + 1], status=status, shared=shared,
+                                               flags=flags)
+        torch.cuda.synchronize()
+        return outs[1:]
+
+    plain = chain(0)
+    early = chain(binding.SPARSE_ATTN_BLOCKS_READY)
+    assert status.item() == 0
+    for a, b in zip(plain, early):
+        assert torch.equal(a, b)
+    Oref, _, _ = oracle.verify(bits(inp["Q"]), bits(inp["K"]), bits(inp["V"]), inp["I"].cpu().numpy(), sh.C,
+                               sh.window_blocks, [sh.T] * sh.B, shared=shared)
+    assert_attn_close(early[0], Oref)
+
+
 # ----------------------------------------------------------------------------- offloaded gather
 
 
