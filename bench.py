@@ -273,11 +273,12 @@ class Decode128k:
                                         sh.k, self.idx[l_target], self.count[l_target], status=self.status,
                                         stream=stream)
 
-    def _attend(self, l, stream, n_split=0):
+    def _attend(self, l, stream, n_split=0, count=None):
         # the block list of every layer comes from the side stream through an event, so
         # K/V streaming may start while the previous attention drains
         q = l % self.sh.phys_layers
-        self.binding.sparse_decode_attn(self.Q[l], self.k_cache[q], self.v_cache[q], self.idx[l], self.count[l],
+        count = self.count[l] if count is None else count
+        self.binding.sparse_decode_attn(self.Q[l], self.k_cache[q], self.v_cache[q], self.idx[l], count,
                                         self.seq, self.O[l], status=self.status, n_split=n_split,
                                         flags=self.binding.SPARSE_ATTN_BLOCKS_READY, workspace=self.workspace,
                                         stream=stream)
@@ -415,11 +416,26 @@ def run_ours(args, rank, world, local_rank):
     att_chain_ms = time_chain(lambda l, st_: wk._attend(l, st_))
     att_bytes = wk.attn_bytes_per_launch()
     att_hash = kernel_source_hash(ATTN_SOURCES)
+    # what a launch costs without streaming: the same launch with every count 0 (list
+    # fetch, Q load, merge, O write), and a one-element torch kernel timed the same way
+    zero_count = torch.zeros_like(wk.count[0])
+    att_empty_ms, _ = time_alone(lambda l: wk._attend(l, cur, count=zero_count), reps=1)
+    tiny = torch.zeros(1, device=dev)
+    floor_ms, _ = time_alone(lambda l: tiny.add_(1.0), reps=1)
+    stream_ms = att_alone_ms - att_empty_ms
     attention = {"kernel": "sparse_attn_kernel (sparse_decode_attn, decode, G=8)",
                  "algorithmic_bytes_per_launch": att_bytes,
                  "alone": {"avg_launch_us": round(att_alone_ms * 1e3, 2), "launches_timed": att_n,
                            "achieved": round(att_bytes / (att_alone_ms * 1e-3) / 1e9, 1),
-                           "frac": round(att_bytes / (att_alone_ms * 1e-3) / 1e9 / peak, 4)},
+                           "frac": round(att_bytes / (att_alone_ms * 1e-3) / 1e9 / peak, 4),
+                           "empty_launch_us": round(att_empty_ms * 1e3, 2),
+                           "event_floor_us": round(floor_ms * 1e3, 2),
+                           "streaming_gbs": round(att_bytes / (stream_ms * 1e-3) / 1e9, 1) if stream_ms > 0 else None,
+                           "streaming_frac": round(att_bytes / (stream_ms * 1e-3) / 1e9 / peak, 4)
+                           if stream_ms > 0 else None,
+                           "note": "empty_launch_us: the same launches with every count 0; event_floor_us: a "
+                                   "one-element torch kernel timed the same way; streaming = bytes / (alone - "
+                                   "empty)"},
                  "chained": {"avg_launch_us": round(att_chain_ms * 1e3, 2), "launches": L,
                              "achieved": round(att_bytes / (att_chain_ms * 1e-3) / 1e9, 1),
                              "frac": round(att_bytes / (att_chain_ms * 1e-3) / 1e9 / peak, 4),

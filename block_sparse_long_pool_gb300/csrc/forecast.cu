@@ -57,6 +57,10 @@ __global__ void __launch_bounds__(kFThreads, 2)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
+    if (ATTN && tid == kConsumerWarps * 32) {   // fetched while the keys stream
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
     const uint32_t S = gridDim.x;       // the cluster spans gridDim.x
     const uint32_t rank = blockIdx.x;   // == %cluster_ctarank
     const int pair = blockIdx.y;
@@ -140,8 +144,6 @@ __global__ void __launch_bounds__(kFThreads, 2)
         if (ATTN)
             named_barrier_arrive(1, kAttnThreads);
         if (ATTN && lane == 0 && n_run > 0) {
-            prefetch_tensormap(&kmap);
-            prefetch_tensormap(&vmap);
             for (int i = 0; i < n_run; ++i, ++it) {
                 const int s = it % kStages;
                 const int use = it / kStages;

@@ -84,6 +84,8 @@ template <int NT>
 __global__ void __launch_bounds__(kFThreads, 1) nsa_route_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                   const __grid_constant__ RouteParams p)
 {
+    if (threadIdx.x == kConsumerWarps * 32)   // the descriptor is a parameter: fetched while waiting
+        prefetch_tensormap(&kmap);
     griddep_wait();   // every input may be written by the kernel before this one
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -150,7 +152,6 @@ __global__ void __launch_bounds__(kFThreads, 1) nsa_route_kernel(const __grid_co
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && n_tiles > 0) {
-            prefetch_tensormap(&kmap);
             const uint64_t pol = policy_evict_first();
             for (int t = 0; t < n_tiles; ++t) {
                 const int st = t % p.stages;

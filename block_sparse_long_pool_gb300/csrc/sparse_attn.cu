@@ -186,6 +186,10 @@ __device__ __forceinline__ void attn_cluster_cta(const CUtensorMap *kmap, const 
     const int warp = tid >> 5, lane = tid & 31;
     const uint32_t S = gridDim.x;        // the cluster spans gridDim.x
     const uint32_t rank = blockIdx.x;    // == %cluster_ctarank
+    if (tid == kConsumerWarps * 32) {    // the descriptor fetches overlap the list fetch
+        prefetch_tensormap(kmap);
+        prefetch_tensormap(vmap);
+    }
 
     int pair, q0 = 0, rows_valid;
     if (VERIFY) {
@@ -251,8 +255,6 @@ __device__ __forceinline__ void attn_cluster_cta(const CUtensorMap *kmap, const 
             named_barrier_arrive(1, kThreads);   // the slice and its length are in shared memory
         }
         if (lane == 0 && my_n > 0) {
-            prefetch_tensormap(kmap);
-            prefetch_tensormap(vmap);
             const uint64_t pol = policy_evict_first();
             for (int it = 0; it < my_n; ++it) {
                 const int s = it % kStages;
@@ -371,6 +373,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int rank = static_cast<int>(blockIdx.x);
     const int pair = static_cast<int>(blockIdx.y);
     const int b = pair / p.H_kv, g = pair % p.H_kv;
+    if (tid == kConsumerWarps * 32) {   // the descriptor fetches overlap the list fetch
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
     const bool early = (p.flags & SPARSE_ATTN_BLOCKS_READY) != 0u;
     if (!early)
         griddep_wait();
@@ -397,8 +403,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int n_run = producer_fetch_slice(p, pair, i0, cap, lslot, llog, ctrl, lane);
         named_barrier_arrive(1, kThreads);   // the list and its length are in shared memory
         if (lane == 0 && n_run > 0) {
-            prefetch_tensormap(&kmap);
-            prefetch_tensormap(&vmap);
             const uint64_t pol = policy_evict_first();
             for (int it = 0; it < n_run; ++it) {
                 const int s = it % kStages;
@@ -619,6 +623,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     const long long lo = N * c / C, hi = N * (c + 1) / C;
     const long long p_first = lo / K;
     const int n_segs = hi > lo ? static_cast<int>((hi - 1) / K - p_first + 1) : 0;
+    if (tid == kConsumerWarps * 32) {   // the descriptor fetches overlap the list fetch
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
 
     const bool early = (p.flags & SPARSE_ATTN_BLOCKS_READY) != 0u;
     if (!early)
@@ -706,8 +714,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && !aborted) {
-            prefetch_tensormap(&kmap);
-            prefetch_tensormap(&vmap);
             const uint64_t pol = policy_evict_first();
             int it = 0;
             bool stop = false;
@@ -1532,6 +1538,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     const AttnParams &pw = np.br[1];
     const AttnParams &pc = np.br[2];
     const int b = pair / ps.H_kv, g = pair % ps.H_kv;
+    if (tid == kConsumerWarps * 32) {   // the descriptor fetches overlap the barrier set-up
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+        prefetch_tensormap(&khmap);
+        prefetch_tensormap(&vhmap);
+    }
     const bool early = (ps.flags & SPARSE_ATTN_BLOCKS_READY) != 0u;
     if (!early)
         griddep_wait();
@@ -1594,10 +1606,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         };
         const int pre = min(n_r, kStages);
         if (lane == 0) {
-            prefetch_tensormap(&kmap);
-            prefetch_tensormap(&vmap);
-            prefetch_tensormap(&khmap);
-            prefetch_tensormap(&vhmap);
             for (int it = 0; it < pre; ++it)
                 issue(it);
         }
