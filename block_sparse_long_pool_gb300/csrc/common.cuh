@@ -25,6 +25,17 @@ __device__ __forceinline__ void report(int *status, int code)
         atomicCAS(status, 0, code);
 }
 
+// 2^x by the PTX ISA's ex2.approx.ftz.f32 instruction: one branch-free instruction
+// (maximum relative error about 2^-22; results below 2^-126 flush to zero), so the
+// compiler can overlap independent calls.  Used where a few ulp do not matter: the
+// selectors' softmax sums, whose scores are compared with a 1e-4 relative tie band.
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint64_t globaltimer()
 {
     uint64_t t;

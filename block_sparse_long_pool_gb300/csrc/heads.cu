@@ -20,14 +20,17 @@ namespace {
 //   2. per head, the slice's max and sum of exp2 -> CTA 0, which merges them and
 //      sends each CTA the head's max and 1 / sum;
 //   3. s_j = sum_h exp2(a^h_j - M_h) / Z_h -> order key -> CTA 0, whose consumer
-//      warps and selector warp find the top-k threshold together (block-wide radix
-//      select), and the selector writes the list.
+//      warps and selector warp take the top-k together: the keys in registers, the
+//      bits every key shares decided at once, a binary search over the rest with
+//      block-wide counts, the list written through block-wide prefix sums (a radix
+//      threshold and a one-warp write past 2720 candidates).
 
 constexpr int kMaxHeadsSel = 16;
 constexpr int kCtrlStatsBar = 10;   // ctrl[10..11]
 constexpr int kCtrlNormBar = 12;    // ctrl[12..13]
 constexpr int kCtrlThrWords = 4;    // ctrl[4..5]: the running threshold of the top-k search
 constexpr int kHeadsTopkThreads = (kConsumerWarps + 1) * 32;   // CTA 0's consumers + selector
+constexpr int kHeadsKpt = 17;   // candidate keys per thread in the register top-k (2720 blocks)
 
 struct HeadsLayout {
     int off_keys, off_q, off_raw, off_stats, off_norm, total;
@@ -66,7 +69,6 @@ __global__ void __launch_bounds__(kFThreads, 1) select_heads_kernel(const AttnPa
     const int b = pair / p.H_kv, g = pair % p.H_kv;
     const int G = p.G;
     const HeadsLayout L = heads_layout(p.N_cap, rows_max, G, S);
-    uint32_t *hist = reinterpret_cast<uint32_t *>(base + fused_off_hist());
     uint32_t *keys = reinterpret_cast<uint32_t *>(base + L.off_keys);
     float *qf = reinterpret_cast<float *>(base + L.off_q);
     float *raw = reinterpret_cast<float *>(base + L.off_raw);
@@ -81,6 +83,7 @@ __global__ void __launch_bounds__(kFThreads, 1) select_heads_kernel(const AttnPa
     const int nb = static_cast<int>(nb_ll);
     const bool take_all = max(0, nb - p.n_local - p.n_init) <= p.k_sel;
     const bool score = !take_all && p.k_sel > 0;
+    const bool regs_topk = topk_cta_regs_fits<kHeadsKpt>(nb - p.n_local - p.n_init, kHeadsTopkThreads);
     const int chunk = (nb + S - 1) / S;
     const int r0 = score ? min(nb, rank * chunk) : 0;
     const int n_krows = score ? min(nb, r0 + chunk) - r0 : 0;
@@ -96,9 +99,6 @@ __global__ void __launch_bounds__(kFThreads, 1) select_heads_kernel(const AttnPa
         mbar_init(bar_norm, 1);
         fence_barrier_init();
     }
-    if (rank == 0 && score)
-        for (int i = tid; i < kCoarseBins; i += kFThreads)
-            hist[i] = 0u;
     __syncthreads();
     cluster_arrive();
     griddep_launch_dependents();
@@ -208,17 +208,29 @@ __global__ void __launch_bounds__(kFThreads, 1) select_heads_kernel(const AttnPa
         named_barrier_sync(2, kConsumerWarps * 32);   // every raw score of the slice is written
         // (2) per head: the slice's max and sum of exp2, merged by CTA 0
         if (score) {
+            // (one warp per scheduler: four independent accumulators per lane)
             for (int h = warp; h < G; h += kConsumerWarps) {
-                float m = -INFINITY;
-                for (int i = lane; i < n_krows; i += 32)
-                    m = fmaxf(m, raw[h * rows_max + i]);
+                const float *rh = raw + h * rows_max;
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                for (int i = lane; i < n_krows; i += 128)
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {   // branch-free: clamped load, masked value
+                        const float v = rh[min(i + 32 * q4, n_krows - 1)];
+                        m4[q4] = fmaxf(m4[q4], i + 32 * q4 < n_krows ? v : -INFINITY);
+                    }
+                float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1)
                     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                float z = 0.f;
+                float z4[4] = {0.f, 0.f, 0.f, 0.f};
                 if (m != -INFINITY)
-                    for (int i = lane; i < n_krows; i += 32)
-                        z += exp2f(raw[h * rows_max + i] - m);
+                    for (int i = lane; i < n_krows; i += 128)
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const float e = ex2_approx(rh[min(i + 32 * q4, n_krows - 1)] - m);
+                            z4[q4] += i + 32 * q4 < n_krows ? e : 0.f;
+                        }
+                float z = (z4[0] + z4[1]) + (z4[2] + z4[3]);
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1)
                     z += __shfl_xor_sync(0xffffffffu, z, o);
@@ -230,22 +242,39 @@ __global__ void __launch_bounds__(kFThreads, 1) select_heads_kernel(const AttnPa
             __syncwarp();
             if (lane == 0)
                 mbar_arrive_cluster(dsmem_addr(bar_stats, 0));
-            // (3) summed per-head distributions -> keys and coarse histogram in CTA 0
+            // (3) summed per-head distributions -> order keys in CTA 0
             const bool have_norm = __all_sync(0xffffffffu, mbar_wait_cluster(bar_norm, 0, kWaitNs));
             if (!have_norm) {
                 if (lane == 0)
                     report(p.status, SPARSE_ERR_TIMEOUT);
             } else {
-                for (int ib = warp * 32; ib < n_krows; ib += kConsumerWarps * 32) {
-                    const int i = ib + lane;
-                    const bool in = ok && i < n_krows;
-                    float sum = 0.f;
-                    if (in)
-                        for (int h = 0; h < G; ++h)
-                            sum += exp2f(raw[h * rows_max + i] - norm[2 * h]) * norm[2 * h + 1];
-                    const int j = r0 + i;
-                    if (in)
-                        keys0[j] = order_key(sum);
+                // heads past G read head G-1's row and add an exact 0: a branch-free body
+                float nm[kMaxHeadsSel], ni[kMaxHeadsSel];
+                const float *rowh[kMaxHeadsSel];
+#pragma unroll
+                for (int h = 0; h < kMaxHeadsSel; ++h) {
+                    nm[h] = h < G ? norm[2 * h] : INFINITY;
+                    ni[h] = h < G ? norm[2 * h + 1] : 0.f;
+                    rowh[h] = raw + min(h, G - 1) * rows_max;
+                }
+                constexpr int kPass = 2, kStride = kConsumerWarps * 32;
+                for (int ib = warp * 32; ib < n_krows; ib += kPass * kStride) {
+                    float sum[kPass];
+#pragma unroll
+                    for (int q2 = 0; q2 < kPass; ++q2) {
+                        const int i = min(ib + q2 * kStride + lane, n_krows - 1);
+                        float acc = 0.f;
+#pragma unroll
+                        for (int h = 0; h < kMaxHeadsSel; ++h)
+                            acc += ex2_approx(rowh[h][i] - nm[h]) * ni[h];
+                        sum[q2] = acc;
+                    }
+#pragma unroll
+                    for (int q2 = 0; q2 < kPass; ++q2) {
+                        const int i = ib + q2 * kStride + lane;
+                        if (ok && i < n_krows)
+                            keys0[r0 + i] = order_key(sum[q2]);
+                    }
                 }
             }
             __syncwarp();
@@ -255,12 +284,21 @@ __global__ void __launch_bounds__(kFThreads, 1) select_heads_kernel(const AttnPa
                 // CTA 0's consumers join its selector warp in the threshold search (the
                 // summed probabilities share an exponent: a coarse histogram of the top
                 // key bits would not narrow them)
-                if (!__all_sync(0xffffffffu, mbar_wait_cluster(bar_scored, 0, kWaitNs)) && lane == 0)
+                const bool got = __all_sync(0xffffffffu, mbar_wait_cluster(bar_scored, 0, kWaitNs));
+                if (!got && lane == 0)
                     report(p.status, SPARSE_ERR_TIMEOUT);
-                uint32_t prefix;
-                int need;
-                topk_threshold_cta(base_s + L.off_keys, p.n_init, nb - p.n_local, p.k_sel, base_s + fused_off_hist(),
-                                   base_s + kOffCtrl + 4 * kCtrlThrWords, tid + 32, kHeadsTopkThreads, 3, prefix, need);
+                if (regs_topk) {
+                    topk_cta_regs<kHeadsKpt>(base_s + L.off_keys, nb, p.n_init, p.n_local, p.k_sel,
+                                             base_s + fused_off_hist(), tid + 32, kHeadsTopkThreads, 3, got,
+                                             p.idx_next + static_cast<size_t>(pair) * p.k_tot_next, p.k_tot_next,
+                                             p.count_next + pair, p.status);
+                } else {
+                    uint32_t prefix;
+                    int need;
+                    topk_threshold_cta(base_s + L.off_keys, p.n_init, nb - p.n_local, p.k_sel,
+                                       base_s + fused_off_hist(), base_s + kOffCtrl + 4 * kCtrlThrWords, tid + 32,
+                                       kHeadsTopkThreads, 3, prefix, need);
+                }
             }
         }
     } else {
@@ -300,16 +338,24 @@ __global__ void __launch_bounds__(kFThreads, 1) select_heads_kernel(const AttnPa
             }
             uint32_t prefix = 0u;
             int need = 0;
-            if (score)
-                topk_threshold_cta(base_s + L.off_keys, p.n_init, nb - p.n_local, p.k_sel, base_s + fused_off_hist(),
-                                   base_s + kOffCtrl + 4 * kCtrlThrWords, lane, kHeadsTopkThreads, 3, prefix, need);
-            if (ready) {
-                topk_write_warp(base_s + L.off_keys, 0u, 0, nb, p.n_init, p.n_local,
-                                max(0, nb - p.n_local - p.n_init) <= p.k_sel, p.k_sel <= 0, prefix, need,
-                                p.idx_next + static_cast<size_t>(pair) * p.k_tot_next, p.k_tot_next,
-                                p.count_next + pair, p.status, lane);
-            } else if (lane == 0) {
-                report(p.status, SPARSE_ERR_TIMEOUT);
+            if (score && regs_topk) {
+                topk_cta_regs<kHeadsKpt>(base_s + L.off_keys, nb, p.n_init, p.n_local, p.k_sel,
+                                         base_s + fused_off_hist(), lane, kHeadsTopkThreads, 3, ready,
+                                         p.idx_next + static_cast<size_t>(pair) * p.k_tot_next, p.k_tot_next,
+                                         p.count_next + pair, p.status);
+            } else {
+                if (score)
+                    topk_threshold_cta(base_s + L.off_keys, p.n_init, nb - p.n_local, p.k_sel,
+                                       base_s + fused_off_hist(), base_s + kOffCtrl + 4 * kCtrlThrWords, lane,
+                                       kHeadsTopkThreads, 3, prefix, need);
+                if (ready) {
+                    topk_write_warp(base_s + L.off_keys, 0u, 0, nb, p.n_init, p.n_local,
+                                    max(0, nb - p.n_local - p.n_init) <= p.k_sel, p.k_sel <= 0, prefix, need,
+                                    p.idx_next + static_cast<size_t>(pair) * p.k_tot_next, p.k_tot_next,
+                                    p.count_next + pair, p.status, lane);
+                } else if (lane == 0) {
+                    report(p.status, SPARSE_ERR_TIMEOUT);
+                }
             }
         }
         cluster_wait();

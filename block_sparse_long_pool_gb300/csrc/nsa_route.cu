@@ -25,15 +25,18 @@
 //   1. TMA ring of 64-row tiles -> raw scores (log2 units) of the CTA's rows;
 //   2. per head, max and sum of exp2 over the owned rows -> CTA 0, which merges them
 //      and sends every CTA the head's max and 1 / sum;
-//   3. p_j for the CTA's rows and the block maxima as order keys -> CTA 0, whose
-//      consumers and selector warp find the top-k threshold together (block-wide radix
-//      select: the summed probabilities share an exponent, so a coarse histogram of the
-//      top key bits would not narrow them), and the selector writes the list.
+//   3. p_j for the CTA's rows (four rows per thread at a time) and the block maxima as
+//      order keys -> CTA 0, whose consumers and selector warp take the top-k together
+//      (topk_cta_regs: the summed probabilities share an exponent, so the bits every
+//      key shares are decided at once and a binary search with block-wide counts finds
+//      the rest; past 2720 candidates a block-wide radix threshold and a one-warp
+//      write).
 
 namespace {
 
 constexpr int kRouteStageBytes = kTileBytes;   // 64 rows x 128 dims, bf16: two 64 x 64 boxes
 constexpr int kRouteTopkThreads = (kConsumerWarps + 1) * 32;   // CTA 0's consumers + selector
+constexpr int kRouteKpt = 17;   // candidate keys per thread in the register top-k (2720 blocks)
 
 struct RouteParams {
     const uint16_t *Q;
@@ -123,6 +126,7 @@ __global__ void __launch_bounds__(kFThreads, 1) nsa_route_kernel(const __grid_co
     const int nb = static_cast<int>(nb_ll), R = static_cast<int>(R_ll);
     const bool take_all = max(0, nb - p.n_local - p.n_init) <= p.k_sel;
     const bool score = !take_all && p.k_sel > 0;
+    const bool regs_topk = topk_cta_regs_fits<kRouteKpt>(nb - p.n_local - p.n_init, kRouteTopkThreads);
     // this CTA's blocks, its owned rows [o_lo, o_hi) and its loaded rows [j_lo, o_hi)
     const int bpc = (nb + S - 1) / S;
     const int b_lo = min(nb, rank * bpc), b_hi = min(nb, b_lo + bpc);
@@ -210,29 +214,34 @@ __global__ void __launch_bounds__(kFThreads, 1) nsa_route_kernel(const __grid_co
         }
         named_barrier_sync(2, kConsumerWarps * 32);   // every raw score is written
         if (score) {
-            // (2) per head: max and sum of exp2 over the owned rows, merged by CTA 0
+            // (2) per head: max and sum of exp2 over the owned rows, merged by CTA 0 (one
+            // warp per scheduler: four independent accumulators per lane)
             const int own0 = o_lo - j_lo, own1 = b_hi > b_lo ? o_hi - j_lo : own0;
             for (int h = warp; h < G; h += kConsumerWarps) {
-                float m = -INFINITY;
                 const float *rh = raw + h * p.rows_cta_max;
-                float z = 0.f;
-                for (int i = own0 + lane; i < own1; i += 32) {   // one pass: running max and sum
-                    const float a = rh[i];
-                    if (a > m) {
-                        z = z * exp2f(m - a) + 1.f;
-                        m = a;
-                    } else {
-                        z += exp2f(a - m);
-                    }
-                }
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                for (int i = own0 + lane; i < own1; i += 128)
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float mo = __shfl_xor_sync(0xffffffffu, m, o);
-                    const float zo = __shfl_xor_sync(0xffffffffu, z, o);
-                    const float mn = fmaxf(m, mo);
-                    z = (m == -INFINITY ? 0.f : z * exp2f(m - mn)) + (mo == -INFINITY ? 0.f : zo * exp2f(mo - mn));
-                    m = mn;
-                }
+                    for (int q4 = 0; q4 < 4; ++q4) {   // branch-free: clamped load, masked value
+                        const float v = rh[min(i + 32 * q4, own1 - 1)];
+                        m4[q4] = fmaxf(m4[q4], i + 32 * q4 < own1 ? v : -INFINITY);
+                    }
+                float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                float z4[4] = {0.f, 0.f, 0.f, 0.f};
+                if (m != -INFINITY)
+                    for (int i = own0 + lane; i < own1; i += 128)
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const float e = ex2_approx(rh[min(i + 32 * q4, own1 - 1)] - m);
+                            z4[q4] += i + 32 * q4 < own1 ? e : 0.f;
+                        }
+                float z = (z4[0] + z4[1]) + (z4[2] + z4[3]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    z += __shfl_xor_sync(0xffffffffu, z, o);
                 if (lane == 0) {
                     stats0[(rank * G + h) * 2] = m;
                     stats0[(rank * G + h) * 2 + 1] = z;
@@ -246,22 +255,54 @@ __global__ void __launch_bounds__(kFThreads, 1) nsa_route_kernel(const __grid_co
                 report(p.status, SPARSE_ERR_TIMEOUT);
             // (3) p_j of the loaded rows, then the block maxima -> keys of CTA 0 (every
             // consumer warp reaches the barrier, whatever its wait gave)
-            if (have_norm)
-                for (int i = tid; i < n_loc; i += kConsumerWarps * 32) {
-                    float sum = 0.f;
-                    for (int h = 0; h < G; ++h)
-                        sum += exp2f(raw[h * p.rows_cta_max + i] - norm[2 * h]) * norm[2 * h + 1];
-                    prow[i] = sum;   // prow aliases head 0's scores: row i is this thread's alone
+            if (have_norm) {
+                // four rows per pass, every load of a pass before its stores (one warp per
+                // scheduler: the rows' exp2 chains overlap within the thread); heads past G
+                // read head G-1's row and add an exact 0, so the body has no branch
+                constexpr int HM = 8 * NT;
+                float nm[HM], ni[HM];
+                const float *rowh[HM];
+#pragma unroll
+                for (int h = 0; h < HM; ++h) {
+                    nm[h] = h < G ? norm[2 * h] : INFINITY;
+                    ni[h] = h < G ? norm[2 * h + 1] : 0.f;
+                    rowh[h] = raw + min(h, G - 1) * p.rows_cta_max;
                 }
+                constexpr int kPass = 4, kStride = kConsumerWarps * 32;
+                for (int i0 = tid; i0 < n_loc; i0 += kPass * kStride) {
+                    float sum[kPass];
+#pragma unroll
+                    for (int q4 = 0; q4 < kPass; ++q4) {
+                        const int i = min(i0 + q4 * kStride, n_loc - 1);
+                        float acc = 0.f;
+#pragma unroll
+                        for (int h = 0; h < HM; ++h)
+                            acc += ex2_approx(rowh[h][i] - nm[h]) * ni[h];
+                        sum[q4] = acc;
+                    }
+#pragma unroll
+                    for (int q4 = 0; q4 < kPass; ++q4) {
+                        const int i = i0 + q4 * kStride;
+                        if (i < n_loc)
+                            prow[i] = sum[q4];   // prow aliases head 0's scores: row i is this thread's alone
+                    }
+                }
+            }
             named_barrier_sync(2, kConsumerWarps * 32);
             if (have_norm) {
+                // rows meeting block blk: [(64 blk - l) / s + 1, (64 blk + 63) / s] (32-bit; a
+                // shift for a power-of-two stride)
+                const bool pow2 = (s & (s - 1)) == 0;
+                const int sh = __ffs(s) - 1;
+                auto div_s = [&](int x) { return pow2 ? x >> sh : x / s; };
                 for (int bb = b_lo + warp * 32; bb < b_hi; bb += kConsumerWarps * 32) {
                     const int blk = bb + lane;
                     const bool in = ok && blk < b_hi;
                     float best = 0.f;
                     if (in) {
-                        const int r0 = static_cast<int>(route_first_row(blk, l, s));
-                        const int r1 = min(R - 1, static_cast<int>((static_cast<long long>(kBlk) * blk + kBlk - 1) / s));
+                        const int x = kBlk * blk - l;
+                        const int r0 = x < 0 ? 0 : div_s(x) + 1;
+                        const int r1 = min(R - 1, div_s(kBlk * blk + kBlk - 1));
                         for (int j = r0; j <= r1; ++j)
                             best = fmaxf(best, prow[j - j_lo]);
                     }
@@ -273,13 +314,21 @@ __global__ void __launch_bounds__(kFThreads, 1) nsa_route_kernel(const __grid_co
             if (lane == 0)
                 mbar_arrive_cluster(dsmem_addr(bar_scored, 0));
             if (rank == 0) {
-                // CTA 0's consumers join its selector warp in the threshold search
-                if (!__all_sync(0xffffffffu, mbar_wait_cluster(bar_scored, 0, kWaitNs)) && lane == 0)
+                // CTA 0's consumers join its selector warp in the top-k
+                const bool got = __all_sync(0xffffffffu, mbar_wait_cluster(bar_scored, 0, kWaitNs));
+                if (!got && lane == 0)
                     report(p.status, SPARSE_ERR_TIMEOUT);
-                uint32_t prefix;
-                int need;
-                topk_threshold_cta(base_s + L.off_keys, p.n_init, nb - p.n_local, p.k_sel, base_s + L.off_hist,
-                                   base_s + L.off_ctrl + 32, tid + 32, kRouteTopkThreads, 3, prefix, need);
+                if (regs_topk) {
+                    topk_cta_regs<kRouteKpt>(base_s + L.off_keys, nb, p.n_init, p.n_local, p.k_sel,
+                                             base_s + L.off_hist, tid + 32, kRouteTopkThreads, 3, got,
+                                             p.idx + static_cast<size_t>(unit) * p.k_tot, p.k_tot, p.count + unit,
+                                             p.status);
+                } else {
+                    uint32_t prefix;
+                    int need;
+                    topk_threshold_cta(base_s + L.off_keys, p.n_init, nb - p.n_local, p.k_sel, base_s + L.off_hist,
+                                       base_s + L.off_ctrl + 32, tid + 32, kRouteTopkThreads, 3, prefix, need);
+                }
             }
         }
     } else {
@@ -315,19 +364,27 @@ __global__ void __launch_bounds__(kFThreads, 1) nsa_route_kernel(const __grid_co
                 if (ready)
                     ready = __all_sync(0xffffffffu, mbar_wait_cluster(bar_scored, 0, kWaitNs));
             }
-            // the top-k threshold with CTA 0's consumers (this warp is warp 0 of the
-            // group), then the list
+            // the top-k with CTA 0's consumers (this warp is warp 0 of the group): keys in
+            // registers and the list written by the group, or the radix threshold and the
+            // list written by this warp
             uint32_t prefix = 0u;
             int need = 0;
-            if (score)
-                topk_threshold_cta(base_s + L.off_keys, p.n_init, nb - p.n_local, p.k_sel, base_s + L.off_hist,
-                                   base_s + L.off_ctrl + 32, lane, kRouteTopkThreads, 3, prefix, need);
-            if (ready) {
-                topk_write_warp(base_s + L.off_keys, 0u, 0, nb, p.n_init, p.n_local,
-                                max(0, nb - p.n_local - p.n_init) <= p.k_sel, p.k_sel <= 0, prefix, need,
-                                p.idx + static_cast<size_t>(unit) * p.k_tot, p.k_tot, p.count + unit, p.status, lane);
-            } else if (lane == 0) {
-                report(p.status, SPARSE_ERR_TIMEOUT);
+            if (score && regs_topk) {
+                topk_cta_regs<kRouteKpt>(base_s + L.off_keys, nb, p.n_init, p.n_local, p.k_sel, base_s + L.off_hist,
+                                         lane, kRouteTopkThreads, 3, ready, p.idx + static_cast<size_t>(unit) * p.k_tot,
+                                         p.k_tot, p.count + unit, p.status);
+            } else {
+                if (score)
+                    topk_threshold_cta(base_s + L.off_keys, p.n_init, nb - p.n_local, p.k_sel, base_s + L.off_hist,
+                                       base_s + L.off_ctrl + 32, lane, kRouteTopkThreads, 3, prefix, need);
+                if (ready) {
+                    topk_write_warp(base_s + L.off_keys, 0u, 0, nb, p.n_init, p.n_local,
+                                    max(0, nb - p.n_local - p.n_init) <= p.k_sel, p.k_sel <= 0, prefix, need,
+                                    p.idx + static_cast<size_t>(unit) * p.k_tot, p.k_tot, p.count + unit, p.status,
+                                    lane);
+                } else if (lane == 0) {
+                    report(p.status, SPARSE_ERR_TIMEOUT);
+                }
             }
         }
         cluster_wait();

@@ -86,6 +86,41 @@ __device__ __forceinline__ void warp_pick_digit(uint32_t hist_s, int &need, uint
     need = need_new;
 }
 
+// B_init (blocks [0, min(n_init, nb))) at the head of a row; returns how many.  One warp.
+__device__ __forceinline__ int write_init_blocks(int nb, int n_init, int *out, int k_tot, bool &overflow, int lane)
+{
+    const int n_i = min(n_init, nb);
+    for (int j = lane; j < n_i; j += 32) {
+        if (j < k_tot)
+            out[j] = j;
+        else
+            overflow = true;
+    }
+    return n_i;
+}
+
+// B_local (the last n_local blocks, after B_init) from position pos0, -1 in the rest of
+// the row, and the count.  One warp.
+__device__ __forceinline__ void write_local_and_close(int nb, int n_init, int n_local, int pos0, int *out, int k_tot,
+                                                      int *count_out, int *status, bool overflow, int lane)
+{
+    const int l0 = max(nb - n_local, min(n_init, nb));
+    for (int j = l0 + lane; j < nb; j += 32) {
+        const int pos = pos0 + (j - l0);
+        if (pos < k_tot)
+            out[pos] = j;
+        else
+            overflow = true;
+    }
+    pos0 += max(0, nb - l0);
+    if (__any_sync(0xffffffffu, overflow) && lane == 0)
+        report(status, SPARSE_ERR_BAD_INDEX);
+    for (int i = pos0 + lane; i < k_tot; i += 32)
+        out[i] = -1;
+    if (lane == 0)
+        *count_out = min(pos0, k_tot);
+}
+
 // The selection in ascending block order: B_init, the candidates above the threshold
 // key `prefix` plus the first `need` of those equal to it (lower index first; from the
 // list of candidate ids when list_s is non-zero, else from all candidates), B_local;
@@ -97,17 +132,9 @@ __device__ void topk_write_warp(uint32_t keys_s, uint32_t list_s, int n_list, in
     const int cand_lo = n_init, cand_hi = nb - n_local;
     const int n_cand = max(0, cand_hi - cand_lo);
     const unsigned lt = (1u << lane) - 1u;
-    const int n_i = min(n_init, nb);
-    const int l0 = max(nb - n_local, n_i);
-    int pos0 = 0, eq_seen = 0;
+    int eq_seen = 0;
     bool overflow = false;
-    for (int j = lane; j < n_i; j += 32) {
-        if (j < k_tot)
-            out[j] = j;
-        else
-            overflow = true;
-    }
-    pos0 = n_i;
+    int pos0 = write_init_blocks(nb, n_init, out, k_tot, overflow, lane);
     if (take_all) {
         for (int j = cand_lo + lane; j < cand_hi; j += 32) {
             const int pos = pos0 + (j - cand_lo);
@@ -145,20 +172,94 @@ __device__ void topk_write_warp(uint32_t keys_s, uint32_t list_s, int n_list, in
             pos0 += __popc(sm);
         }
     }
-    for (int j = l0 + lane; j < nb; j += 32) {
-        const int pos = pos0 + (j - l0);
-        if (pos < k_tot)
-            out[pos] = j;
-        else
-            overflow = true;
+    write_local_and_close(nb, n_init, n_local, pos0, out, k_tot, count_out, status, overflow, lane);
+}
+
+// Steps 3 and 4 of topk_warp when the keys at or above the coarse bin are listed
+// (n_list <= 32 * KPL, ascending block ids at list_s): lane l holds entries l + 32 m in
+// registers.  The bits below the decided ones (`pmask`, value `prefix`) are found by a
+// binary search from bit low_bits - 1 down, carrying how many listed keys share the
+// decided bits; once all of them are needed their smallest key is the threshold.  The
+// row is then written from the registers: B_init, the listed keys above the threshold
+// and the first `need` equal to it (block order), B_local.
+template <int KPL>
+__device__ __forceinline__ void topk_list_regs(uint32_t keys_s, uint32_t list_s, int n_list, int low_bits,
+                                               uint32_t prefix, uint32_t pmask, int need, int nb, int n_init,
+                                               int n_local, int *out, int k_tot, int *count_out, int *status, int lane)
+{
+    uint32_t key[KPL];
+    int id[KPL];
+    const int nv = max(0, (n_list - lane + 31) / 32);   // this lane's valid entries
+#pragma unroll
+    for (int m = 0; m < KPL; ++m)
+        id[m] = m < nv ? static_cast<int>(lds_u32(list_s + 4 * (lane + 32 * m))) : -1;
+#pragma unroll
+    for (int m = 0; m < KPL; ++m)
+        key[m] = m < nv ? lds_u32(keys_s + 4 * id[m]) : 0u;
+    int mt = 0;   // listed keys sharing the decided bits
+#pragma unroll
+    for (int m = 0; m < KPL; ++m)
+        mt += (m < nv && (key[m] & pmask) == prefix) ? 1 : 0;
+    mt = __reduce_add_sync(0xffffffffu, mt);
+    uint32_t P = prefix, hmask = pmask;
+    for (int b = low_bits - 1; b >= 0; --b) {
+        if (mt == need) {
+            uint32_t mn = 0xFFFFFFFFu;
+#pragma unroll
+            for (int m = 0; m < KPL; ++m)
+                if (m < nv && (key[m] & hmask) == P)
+                    mn = min(mn, key[m]);
+            mn = __reduce_min_sync(0xffffffffu, mn);
+            int eq = 0;
+#pragma unroll
+            for (int m = 0; m < KPL; ++m)
+                eq += (m < nv && key[m] == mn) ? 1 : 0;
+            P = mn;
+            need = __reduce_add_sync(0xffffffffu, eq);
+            break;
+        }
+        const uint32_t bit = 1u << b;
+        const uint32_t m2 = hmask | bit, want = P | bit;
+        int c = 0;
+#pragma unroll
+        for (int m = 0; m < KPL; ++m)
+            c += (m < nv && (key[m] & m2) == want) ? 1 : 0;
+        c = __reduce_add_sync(0xffffffffu, c);
+        if (c >= need) {
+            P = want;
+            mt = c;
+        } else {
+            need -= c;
+            mt -= c;
+        }
+        hmask = m2;
     }
-    pos0 += max(0, nb - l0);
-    if (__any_sync(0xffffffffu, overflow) && lane == 0)
-        report(status, SPARSE_ERR_BAD_INDEX);
-    for (int i = pos0 + lane; i < k_tot; i += 32)
-        out[i] = -1;
-    if (lane == 0)
-        *count_out = min(pos0, k_tot);
+    const unsigned lt = (1u << lane) - 1u;
+    bool overflow = false;
+    int pos0 = write_init_blocks(nb, n_init, out, k_tot, overflow, lane);
+    int eq_seen = 0;
+#pragma unroll
+    for (int m = 0; m < KPL; ++m) {
+        if (32 * m < n_list) {   // warp-uniform
+            const bool valid = m < nv;
+            bool sel = valid && key[m] > P;
+            const bool eq = valid && key[m] == P;
+            const unsigned em = __ballot_sync(0xffffffffu, eq);
+            if (eq)
+                sel = eq_seen + __popc(em & lt) < need;
+            eq_seen += __popc(em);
+            const unsigned sm = __ballot_sync(0xffffffffu, sel);
+            if (sel) {
+                const int pos = pos0 + __popc(sm & lt);
+                if (pos < k_tot)
+                    out[pos] = id[m];
+                else
+                    overflow = true;
+            }
+            pos0 += __popc(sm);
+        }
+    }
+    write_local_and_close(nb, n_init, n_local, pos0, out, k_tot, count_out, status, overflow, lane);
 }
 
 // The exact top-k of one pair by one warp over the order keys of blocks [0, nb) (shared
@@ -170,13 +271,13 @@ __device__ void topk_write_warp(uint32_t keys_s, uint32_t list_s, int n_list, in
 //   2. One pass: each lane tests a contiguous run of candidates against the bin's lower
 //      bound (rotated so the lanes hit distinct banks) and writes the block ids of the
 //      keys at or above it, ascending, into list_s (kTopkList entries at most).
-//   3. The remaining 22 bits of the k-th key by an MSB-first radix select over byte
-//      digits of the listed keys that fall in the threshold bin.
+//   3. The remaining 22 bits of the k-th key by a binary search over the listed keys,
+//      held in registers (topk_list_regs).
 //   4. B_init, then the listed keys above the k-th key and the first `need` equal to it
-//      (block order), then B_local.
+//      (block order), then B_local, written from the same registers.
 // More than 2048 candidates, or more than kTopkList keys at or above the bin, take a
-// slower path that scans every candidate for each digit.  coarse_s is reused for the
-// digits.
+// slower path: an MSB-first radix select over byte digits that scans every candidate
+// for each digit (coarse_s is reused for the digits).
 __device__ void topk_warp(uint32_t keys_s, uint32_t coarse_s, uint32_t list_s, int nb, int n_init, int n_local, int k,
                           int *out, int k_tot, int *count_out, int *status, int lane)
 {
@@ -274,9 +375,15 @@ __device__ void topk_warp(uint32_t keys_s, uint32_t coarse_s, uint32_t list_s, i
         } else {
             need = k;
         }
-        // 3. the digits below the coarse bin (bits 23..16, 15..8, 7..0; 23 and 22 are fixed)
-        const uint32_t src_list = listed ? list_s : 0u;
-        const int lo = listed ? 0 : cand_lo, hi = listed ? n_list : cand_hi;
+        if (listed) {   // 3 and 4 with the listed keys in registers
+            topk_list_regs<kTopkList / 32>(keys_s, list_s, n_list, kCoarseShift, prefix, pmask, need, nb, n_init,
+                                           n_local, out, k_tot, count_out, status, lane);
+            return;
+        }
+        // otherwise 3. the digits below the coarse bin over every candidate (bits 23..16,
+        // 15..8, 7..0; 23 and 22 are fixed), or all four digits without a coarse bin
+        const uint32_t src_list = 0u;
+        const int lo = cand_lo, hi = cand_hi;
         uint32_t d;
         if (pmask == 0u) {
             warp_digit_hist(keys_s, src_list, lo, hi, 0u, 0u, 24, coarse_s, lane);
@@ -297,8 +404,8 @@ __device__ void topk_warp(uint32_t keys_s, uint32_t coarse_s, uint32_t list_s, i
         prefix |= d;
     }
     // 4. ascending output
-    topk_write_warp(keys_s, listed ? list_s : 0u, n_list, nb, n_init, n_local, take_all, take_none, prefix, need,
-                    out, k_tot, count_out, status, lane);
+    topk_write_warp(keys_s, 0u, 0, nb, n_init, n_local, take_all, take_none, prefix, need, out, k_tot, count_out,
+                    status, lane);
 }
 
 // The threshold of the top-k among keys[cand_lo, cand_hi) by `nthreads` threads (whole
@@ -458,6 +565,228 @@ __device__ __forceinline__ void topk_threshold_regs(uint32_t keys_s, int cand_lo
     }
     prefix_out = P;
     need_out = need;
+}
+
+// Whether topk_cta_regs<KPT> holds n_cand candidates with nthreads threads.
+template <int KPT>
+__host__ __device__ constexpr bool topk_cta_regs_fits(int n_cand, int nthreads)
+{
+    return (((n_cand + nthreads - 1) / nthreads) | 1) <= KPT;
+}
+
+// Block-wide reductions for a group of threads (whole warps, t in [0, n_warps * 32),
+// synchronised on named barrier `bar`).  buf_s: 16 words of shared memory; calls must
+// alternate between two such buffers (one barrier per call: a thread may write the next
+// call's buffer while another still reads this one).
+__device__ __forceinline__ int group_sum(int v, uint32_t buf_s, int t, int n_warps, int bar)
+{
+    v = __reduce_add_sync(0xffffffffu, v);
+    if ((t & 31) == 0)
+        sts_u32(buf_s + 4 * (t >> 5), static_cast<uint32_t>(v));
+    named_barrier_sync(bar, n_warps * 32);
+    int sum = 0;
+    for (int w = 0; w < n_warps; ++w)
+        sum += static_cast<int>(lds_u32(buf_s + 4 * w));
+    return sum;
+}
+
+__device__ __forceinline__ uint32_t group_min(uint32_t v, uint32_t buf_s, int t, int n_warps, int bar)
+{
+    v = __reduce_min_sync(0xffffffffu, v);
+    if ((t & 31) == 0)
+        sts_u32(buf_s + 4 * (t >> 5), v);
+    named_barrier_sync(bar, n_warps * 32);
+    uint32_t m = 0xFFFFFFFFu;
+    for (int w = 0; w < n_warps; ++w)
+        m = min(m, lds_u32(buf_s + 4 * w));
+    return m;
+}
+
+// Exclusive prefix sum of v over the group in thread order, and the total.
+__device__ __forceinline__ int group_exclusive_scan(int v, uint32_t buf_s, int t, int n_warps, int bar, int &total)
+{
+    const int lane = t & 31;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += n;
+    }
+    if (lane == 31)
+        sts_u32(buf_s + 4 * (t >> 5), static_cast<uint32_t>(incl));
+    named_barrier_sync(bar, n_warps * 32);
+    int before = 0;
+    total = 0;
+    for (int w = 0; w < n_warps; ++w) {
+        const int c = static_cast<int>(lds_u32(buf_s + 4 * w));
+        if (w < (t >> 5))
+            before += c;
+        total += c;
+    }
+    return before + incl - v;
+}
+
+// The exact top-k of one pair by a group of threads (whole warps, t in [0, nthreads),
+// nthreads <= 256, synchronised on named barrier `bar`) with the candidate keys in
+// registers: thread t holds the run of `per` consecutive candidates starting at
+// n_init + t * per (per odd, so a warp's loads hit distinct banks; per <= KPT).  The k
+// largest keys among candidates [n_init, nb - n_local) (equal keys: the lower block
+// first), united with B_init and B_local, are written ascending to out[0 .. count) and
+// -1 after.  Requires n_init + n_local + k < nb and k >= 1 (else topk_write_warp's
+// take-all / take-none forms apply) and topk_cta_regs_fits<KPT>(n_cand, nthreads).
+//   1. The leading bits that every candidate shares (the AND and the OR of the keys
+//      agree there) are decided at once.
+//   2. The rest by a binary search from the top, each step a group count of the keys
+//      that share the decided bits and have the next bit set; the count of keys sharing
+//      the decided bits is carried, and once all of them are needed their smallest key
+//      is the threshold.
+//   3. Each thread counts its keys above the threshold and equal to it; a group prefix
+//      sum of the equal ones gives each thread its share of the `need` equal keys taken
+//      (block order), a second one its output offset.
+// ok: this thread's view of its inputs is complete; false on any thread: nothing is
+// written and a timeout is reported.  scratch_s: 64 words of shared memory.
+template <int KPT>
+__device__ void topk_cta_regs(uint32_t keys_s, int nb, int n_init, int n_local, int k, uint32_t scratch_s, int t,
+                              int nthreads, int bar, bool ok, int *out, int k_tot, int *count_out, int *status)
+{
+    static_assert(KPT % 2 == 1, "an odd run length keeps a warp's loads on distinct banks");
+    const int n_warps = nthreads >> 5;
+    const int cand_lo = n_init, cand_hi = nb - n_local;
+    const int n_cand = cand_hi - cand_lo;
+    const int per = ((n_cand + nthreads - 1) / nthreads) | 1;
+    const int lo = cand_lo + t * per;
+    const int nv = max(0, min(per, cand_hi - lo));
+    uint32_t key[KPT];
+    uint32_t kand = 0xFFFFFFFFu, kor = 0u;
+#pragma unroll
+    for (int m = 0; m < KPT; ++m) {
+        key[m] = m < nv ? lds_u32(keys_s + 4 * (lo + m)) : 0u;
+        if (m < nv) {
+            kand &= key[m];
+            kor |= key[m];
+        }
+    }
+    // 1. shared leading bits, and whether every thread is ready (three reductions in one
+    //    round: buffers 0 and 1 hold the AND and the OR, buffer 2 the not-ready count)
+    {
+        const uint32_t wa = __reduce_and_sync(0xffffffffu, kand);
+        const uint32_t wo = __reduce_or_sync(0xffffffffu, kor);
+        const int wn = __reduce_add_sync(0xffffffffu, ok ? 0 : 1);
+        if ((t & 31) == 0) {
+            sts_u32(scratch_s + 4 * (t >> 5), wa);
+            sts_u32(scratch_s + 4 * (16 + (t >> 5)), wo);
+            sts_u32(scratch_s + 4 * (32 + (t >> 5)), static_cast<uint32_t>(wn));
+        }
+        named_barrier_sync(bar, nthreads);
+        kand = 0xFFFFFFFFu;
+        kor = 0u;
+        int not_ready = 0;
+        for (int w = 0; w < n_warps; ++w) {
+            kand &= lds_u32(scratch_s + 4 * w);
+            kor |= lds_u32(scratch_s + 4 * (16 + w));
+            not_ready += static_cast<int>(lds_u32(scratch_s + 4 * (32 + w)));
+        }
+        if (not_ready != 0) {
+            if (t == 0)
+                report(status, SPARSE_ERR_TIMEOUT);
+            return;
+        }
+    }
+    const int lead = __clz(kand ^ kor);   // 32 when every key is equal
+    uint32_t hmask = lead >= 32 ? 0xFFFFFFFFu : ~(0xFFFFFFFFu >> lead);
+    uint32_t P = kand & hmask;
+    int need = k, mt = n_cand;
+    int ph = 0;   // alternates the reduction buffers (words 48.. and 56..)
+    auto buf = [&]() { return scratch_s + 4 * (48 + 8 * (ph++ & 1)); };
+    // 2. the remaining bits
+    for (int b = 31 - lead; b >= 0; --b) {
+        if (mt == need)
+            break;
+        const uint32_t bit = 1u << b;
+        const uint32_t m2 = hmask | bit, want = P | bit;
+        int c = 0;
+#pragma unroll
+        for (int m = 0; m < KPT; ++m)
+            c += (m < nv && (key[m] & m2) == want) ? 1 : 0;
+        c = group_sum(c, buf(), t, n_warps, bar);
+        if (c >= need) {
+            P = want;
+            mt = c;
+        } else {
+            need -= c;
+            mt -= c;
+        }
+        hmask = m2;
+    }
+    if (mt == need && hmask != 0xFFFFFFFFu) {
+        // every key sharing the decided bits is taken: the smallest is the threshold
+        uint32_t mn = 0xFFFFFFFFu;
+#pragma unroll
+        for (int m = 0; m < KPT; ++m)
+            if (m < nv && (key[m] & hmask) == P)
+                mn = min(mn, key[m]);
+        mn = group_min(mn, buf(), t, n_warps, bar);
+        int eq = 0;
+#pragma unroll
+        for (int m = 0; m < KPT; ++m)
+            eq += (m < nv && key[m] == mn) ? 1 : 0;
+        P = mn;
+        need = group_sum(eq, buf(), t, n_warps, bar);
+    }
+    // 3. the ascending list
+    int n_gt = 0, n_eq = 0;
+#pragma unroll
+    for (int m = 0; m < KPT; ++m) {
+        n_gt += (m < nv && key[m] > P) ? 1 : 0;
+        n_eq += (m < nv && key[m] == P) ? 1 : 0;
+    }
+    int total_eq, total_sel;
+    const int eq_before = group_exclusive_scan(n_eq, buf(), t, n_warps, bar, total_eq);
+    const int take_eq = max(0, min(n_eq, need - eq_before));
+    const int sel_before = group_exclusive_scan(n_gt + take_eq, buf(), t, n_warps, bar, total_sel);
+    const int n_i = min(n_init, nb);
+    bool overflow = false;
+    int pos = n_i + sel_before, eq_taken = 0;
+#pragma unroll
+    for (int m = 0; m < KPT; ++m) {
+        if (m < nv) {
+            bool sel = key[m] > P;
+            if (key[m] == P && eq_taken < take_eq) {
+                sel = true;
+                ++eq_taken;
+            }
+            if (sel) {
+                if (pos < k_tot)
+                    out[pos] = lo + m;
+                else
+                    overflow = true;
+                ++pos;
+            }
+        }
+    }
+    for (int j = t; j < n_i; j += nthreads) {
+        if (j < k_tot)
+            out[j] = j;
+        else
+            overflow = true;
+    }
+    const int l0 = max(nb - n_local, n_i);
+    const int pos_l = n_i + total_sel;
+    for (int j = l0 + t; j < nb; j += nthreads) {
+        const int q = pos_l + (j - l0);
+        if (q < k_tot)
+            out[q] = j;
+        else
+            overflow = true;
+    }
+    const int end = pos_l + max(0, nb - l0);
+    for (int i = end + t; i < k_tot; i += nthreads)
+        out[i] = -1;
+    if (overflow)
+        report(status, SPARSE_ERR_BAD_INDEX);
+    if (t == 0)
+        *count_out = min(end, k_tot);
 }
 
 }  // namespace
