@@ -234,30 +234,35 @@ __device__ __forceinline__ void topk_list_regs(uint32_t keys_s, uint32_t list_s,
         }
         hmask = m2;
     }
+    // the row: masks over this lane's entries, then a short loop over the list's rows of
+    // 32 (this once-run code stays small; block ids are read back from the list)
+    uint32_t gt_mask = 0u, eq_mask = 0u;
+#pragma unroll
+    for (int m = 0; m < KPL; ++m) {
+        gt_mask |= (m < nv && key[m] > P) ? (1u << m) : 0u;
+        eq_mask |= (m < nv && key[m] == P) ? (1u << m) : 0u;
+    }
     const unsigned lt = (1u << lane) - 1u;
     bool overflow = false;
     int pos0 = write_init_blocks(nb, n_init, out, k_tot, overflow, lane);
     int eq_seen = 0;
-#pragma unroll
-    for (int m = 0; m < KPL; ++m) {
-        if (32 * m < n_list) {   // warp-uniform
-            const bool valid = m < nv;
-            bool sel = valid && key[m] > P;
-            const bool eq = valid && key[m] == P;
-            const unsigned em = __ballot_sync(0xffffffffu, eq);
-            if (eq)
-                sel = eq_seen + __popc(em & lt) < need;
-            eq_seen += __popc(em);
-            const unsigned sm = __ballot_sync(0xffffffffu, sel);
-            if (sel) {
-                const int pos = pos0 + __popc(sm & lt);
-                if (pos < k_tot)
-                    out[pos] = id[m];
-                else
-                    overflow = true;
-            }
-            pos0 += __popc(sm);
+#pragma unroll 1
+    for (int m = 0; 32 * m < n_list; ++m) {
+        const bool eq = (eq_mask >> m) & 1u;
+        bool sel = (gt_mask >> m) & 1u;
+        const unsigned em = __ballot_sync(0xffffffffu, eq);
+        if (eq)
+            sel = eq_seen + __popc(em & lt) < need;
+        eq_seen += __popc(em);
+        const unsigned sm = __ballot_sync(0xffffffffu, sel);
+        if (sel) {
+            const int pos = pos0 + __popc(sm & lt);
+            if (pos < k_tot)
+                out[pos] = static_cast<int>(lds_u32(list_s + 4 * (lane + 32 * m)));
+            else
+                overflow = true;
         }
+        pos0 += __popc(sm);
     }
     write_local_and_close(nb, n_init, n_local, pos0, out, k_tot, count_out, status, overflow, lane);
 }
@@ -651,6 +656,7 @@ __device__ void topk_cta_regs(uint32_t keys_s, int nb, int n_init, int n_local, 
                               int nthreads, int bar, bool ok, int *out, int k_tot, int *count_out, int *status)
 {
     static_assert(KPT % 2 == 1, "an odd run length keeps a warp's loads on distinct banks");
+    static_assert(KPT <= 32, "a thread's keys are bits of one mask");
     const int n_warps = nthreads >> 5;
     const int cand_lo = n_init, cand_hi = nb - n_local;
     const int n_cand = cand_hi - cand_lo;
@@ -734,36 +740,32 @@ __device__ void topk_cta_regs(uint32_t keys_s, int nb, int n_init, int n_local, 
         P = mn;
         need = group_sum(eq, buf(), t, n_warps, bar);
     }
-    // 3. the ascending list
-    int n_gt = 0, n_eq = 0;
+    // 3. the ascending list (bit m of a mask: this thread's key m; the loops below run
+    //    over set bits, so this once-run code stays short)
+    uint32_t gt_mask = 0u, eq_mask = 0u;
 #pragma unroll
     for (int m = 0; m < KPT; ++m) {
-        n_gt += (m < nv && key[m] > P) ? 1 : 0;
-        n_eq += (m < nv && key[m] == P) ? 1 : 0;
+        gt_mask |= (m < nv && key[m] > P) ? (1u << m) : 0u;
+        eq_mask |= (m < nv && key[m] == P) ? (1u << m) : 0u;
     }
+    const int n_eq = __popc(eq_mask);
     int total_eq, total_sel;
     const int eq_before = group_exclusive_scan(n_eq, buf(), t, n_warps, bar, total_eq);
     const int take_eq = max(0, min(n_eq, need - eq_before));
-    const int sel_before = group_exclusive_scan(n_gt + take_eq, buf(), t, n_warps, bar, total_sel);
+    uint32_t sel = gt_mask, rest = eq_mask;
+    for (int c = 0; c < take_eq; ++c) {   // the first take_eq equal keys, in block order
+        sel |= rest & (0u - rest);
+        rest &= rest - 1u;
+    }
+    const int sel_before = group_exclusive_scan(__popc(sel), buf(), t, n_warps, bar, total_sel);
     const int n_i = min(n_init, nb);
     bool overflow = false;
-    int pos = n_i + sel_before, eq_taken = 0;
-#pragma unroll
-    for (int m = 0; m < KPT; ++m) {
-        if (m < nv) {
-            bool sel = key[m] > P;
-            if (key[m] == P && eq_taken < take_eq) {
-                sel = true;
-                ++eq_taken;
-            }
-            if (sel) {
-                if (pos < k_tot)
-                    out[pos] = lo + m;
-                else
-                    overflow = true;
-                ++pos;
-            }
-        }
+    int pos = n_i + sel_before;
+    for (; sel != 0u; sel &= sel - 1u, ++pos) {
+        if (pos < k_tot)
+            out[pos] = lo + __ffs(sel) - 1;
+        else
+            overflow = true;
     }
     for (int j = t; j < n_i; j += nthreads) {
         if (j < k_tot)
