@@ -188,6 +188,13 @@ __global__ void __launch_bounds__(kFThreads, 1) nsa_route_kernel(const __grid_co
         float *stats0 = static_cast<float *>(__cluster_map_shared_rank(stats, 0));
         const int g8 = lane >> 2, t4 = lane & 3;
         bool ok = true;
+        // owned rows in local indices; each lane keeps the running max of its heads
+        // (nt * 8 + 2 * t4 + hb) over the owned rows it scores (two fmaxf per score)
+        const int own0 = o_lo - j_lo, own1 = b_hi > b_lo ? o_hi - j_lo : own0;
+        float mrun[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+            mrun[nt][0] = mrun[nt][1] = -INFINITY;
         // (1) raw scores of the loaded rows
         for (int t = 0; t < n_tiles; ++t) {
             const int st = t % p.stages;
@@ -207,29 +214,38 @@ __global__ void __launch_bounds__(kFThreads, 1) nsa_route_kernel(const __grid_co
                     const int h = nt * 8 + 2 * t4 + (i & 1);
                     if (lr < n_loc && h < G)
                         raw[h * p.rows_cta_max + lr] = sacc[nt][i] * p.scale_log2;
+                    if (lr >= own0 && lr < own1)
+                        mrun[nt][i & 1] = fmaxf(mrun[nt][i & 1], sacc[nt][i] * p.scale_log2);
                 }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(bar_empty + 8 * st);
         }
-        named_barrier_sync(2, kConsumerWarps * 32);   // every raw score is written
+        // the warp's max per head (the 8 lanes that share t4) -> wmax [warp][16 heads],
+        // past CTA 0's top-k scratch in its radix-bin region
+        float *wmax = reinterpret_cast<float *>(base + L.off_hist) + 64;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+                float m = mrun[nt][hb];
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1)
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                const int h = nt * 8 + 2 * t4 + hb;
+                if (g8 == 0 && h < G)
+                    wmax[warp * 16 + h] = m;
+            }
+        named_barrier_sync(2, kConsumerWarps * 32);   // every raw score and warp max is written
         if (score) {
             // (2) per head: max and sum of exp2 over the owned rows, merged by CTA 0 (one
             // warp per scheduler: four independent accumulators per lane)
-            const int own0 = o_lo - j_lo, own1 = b_hi > b_lo ? o_hi - j_lo : own0;
             for (int h = warp; h < G; h += kConsumerWarps) {
                 const float *rh = raw + h * p.rows_cta_max;
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                for (int i = own0 + lane; i < own1; i += 128)
+                float m = -INFINITY;
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {   // branch-free: clamped load, masked value
-                        const float v = rh[min(i + 32 * q4, own1 - 1)];
-                        m4[q4] = fmaxf(m4[q4], i + 32 * q4 < own1 ? v : -INFINITY);
-                    }
-                float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
-                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                for (int w = 0; w < kConsumerWarps; ++w)
+                    m = fmaxf(m, wmax[w * 16 + h]);
                 float z4[4] = {0.f, 0.f, 0.f, 0.f};
                 if (m != -INFINITY)
                     for (int i = own0 + lane; i < own1; i += 128)
@@ -303,8 +319,12 @@ __global__ void __launch_bounds__(kFThreads, 1) nsa_route_kernel(const __grid_co
                         const int x = kBlk * blk - l;
                         const int r0 = x < 0 ? 0 : div_s(x) + 1;
                         const int r1 = min(R - 1, div_s(kBlk * blk + kBlk - 1));
-                        for (int j = r0; j <= r1; ++j)
-                            best = fmaxf(best, prow[j - j_lo]);
+                        for (int j = r0; j <= r1; j += 4)   // four rows a step, clamped and masked
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                const float v = prow[min(j + c, r1) - j_lo];
+                                best = fmaxf(best, j + c <= r1 ? v : 0.f);
+                            }
                     }
                     if (in)
                         keys0[blk] = order_key(best);
