@@ -230,20 +230,23 @@ __global__ void __launch_bounds__(kPfThreads, KPL <= 32 ? 2 : 1) prefill_select_
         named_barrier_sync(2, kPfConsumerWarps * 32);   // every order key is in place
         for (int r = warp; r < rows_valid; r += kPfConsumerWarps) {
             const uint32_t row_keys = keys_s + 4 * r * p.key_stride;
-            uint32_t prefix = 0u;
-            int need = 0;
+            const size_t at = static_cast<size_t>(pair) * p.T_cap + t0 + r;
+            int *row_out = p.idx + at * p.k_tot;
             if (score) {
                 // registers for the candidates this tile has (they grow with the position)
                 if (KPL >= 16 && n_cand <= 8 * KPL)
-                    topk_threshold_regs<(KPL >= 16 ? KPL / 4 : KPL)>(row_keys, c_lo, c_hi, p.k, lane, prefix, need);
+                    topk_range_regs<(KPL >= 16 ? KPL / 4 : KPL)>(row_keys, nb, p.n_init, p.n_local, p.k, row_out,
+                                                                 p.k_tot, p.count + at, p.status, lane);
                 else if (KPL >= 8 && n_cand <= 16 * KPL)
-                    topk_threshold_regs<(KPL >= 8 ? KPL / 2 : KPL)>(row_keys, c_lo, c_hi, p.k, lane, prefix, need);
+                    topk_range_regs<(KPL >= 8 ? KPL / 2 : KPL)>(row_keys, nb, p.n_init, p.n_local, p.k, row_out,
+                                                                p.k_tot, p.count + at, p.status, lane);
                 else
-                    topk_threshold_regs<KPL>(row_keys, c_lo, c_hi, p.k, lane, prefix, need);
+                    topk_range_regs<KPL>(row_keys, nb, p.n_init, p.n_local, p.k, row_out, p.k_tot, p.count + at,
+                                         p.status, lane);
+            } else {
+                topk_write_warp(row_keys, 0u, 0, nb, p.n_init, p.n_local, take_all, take_none, 0u, 0, row_out,
+                                p.k_tot, p.count + at, p.status, lane);
             }
-            const size_t at = static_cast<size_t>(pair) * p.T_cap + t0 + r;
-            topk_write_warp(row_keys, 0u, 0, nb, p.n_init, p.n_local, take_all, take_none, prefix, need,
-                            p.idx + at * p.k_tot, p.k_tot, p.count + at, p.status, lane);
         }
     }
 }

@@ -1,5 +1,5 @@
 // select_core.cuh -- exact top-k of order keys in shared memory, shared by the Forecast
-// selection (decode), the NSA routing and the prefill selection.
+// selection (decode), the multi-head selector, the NSA routing and the prefill selection.
 //
 // Keys are order_key(score): larger score -> larger key, equal scores -> equal keys.
 // The top-k takes the k largest keys of the candidates [n_init, nb - n_local), equal
@@ -267,6 +267,97 @@ __device__ __forceinline__ void topk_list_regs(uint32_t keys_s, uint32_t list_s,
     write_local_and_close(nb, n_init, n_local, pos0, out, k_tot, count_out, status, overflow, lane);
 }
 
+// The exact top-k of one row by one warp with its candidates [n_init, nb - n_local)
+// (at most 32 * KPL of them) in registers, lane l holding candidates l + 32 m, written
+// like topk_write_warp.  The k-th largest key value is the largest T with at least k
+// keys >= T: the leading bits every key shares (a warp AND and OR) are decided at once,
+// then one bit at a time, each step one compare and one add per key (an empty slot
+// holds 0 and is never counted, every probe being nonzero).  A probe that exactly k
+// keys reach ends the search: those k keys are the selection.  The row is written from
+// the registers (bit masks, a short loop over rows of 32).  Requires
+// nb - n_local - n_init > k >= 1.
+template <int KPL>
+__device__ __forceinline__ void topk_range_regs(uint32_t keys_s, int nb, int n_init, int n_local, int k, int *out,
+                                                int k_tot, int *count_out, int *status, int lane)
+{
+    static_assert(KPL <= 64, "a lane's keys are bits of one 64-bit mask");
+    const int cand_lo = n_init, cand_hi = nb - n_local;
+    const int n_cand = cand_hi - cand_lo;
+    const int nv = max(0, (n_cand - lane + 31) / 32);   // this lane's valid slots
+    uint32_t key[KPL];
+    uint32_t kand = 0xFFFFFFFFu, kor = 0u;
+#pragma unroll
+    for (int m = 0; m < KPL; ++m) {
+        key[m] = m < nv ? lds_u32(keys_s + 4 * (cand_lo + lane + 32 * m)) : 0u;
+        if (m < nv) {
+            kand &= key[m];
+            kor |= key[m];
+        }
+    }
+    kand = __reduce_and_sync(0xffffffffu, kand);
+    kor = __reduce_or_sync(0xffffffffu, kor);
+    const int lead = __clz(kand ^ kor);   // 32: every key equal
+    uint32_t T = lead >= 32 ? kand : kand & ~(0xFFFFFFFFu >> lead);
+    bool exact = false;
+    for (int b = 31 - lead; b >= 0; --b) {
+        const uint32_t probe = T | (1u << b);
+        int c = 0;
+#pragma unroll
+        for (int m = 0; m < KPL; ++m)
+            c += key[m] >= probe ? 1 : 0;
+        c = __reduce_add_sync(0xffffffffu, c);
+        if (c >= k) {
+            T = probe;
+            if (c == k) {
+                exact = true;
+                break;
+            }
+        }
+    }
+    // threshold P and how many keys equal to it are taken
+    uint32_t P = T;
+    int need;
+    if (exact) {
+        uint32_t mn = 0xFFFFFFFFu;
+#pragma unroll
+        for (int m = 0; m < KPL; ++m)
+            if (m < nv && key[m] >= T)
+                mn = min(mn, key[m]);
+        P = __reduce_min_sync(0xffffffffu, mn);
+    }
+    uint64_t gt_mask = 0ull, eq_mask = 0ull;
+#pragma unroll
+    for (int m = 0; m < KPL; ++m) {
+        gt_mask |= (m < nv && key[m] > P) ? (1ull << m) : 0ull;
+        eq_mask |= (m < nv && key[m] == P) ? (1ull << m) : 0ull;
+    }
+    need = exact ? __reduce_add_sync(0xffffffffu, __popcll(eq_mask))
+                 : k - __reduce_add_sync(0xffffffffu, __popcll(gt_mask));
+    const unsigned lt = (1u << lane) - 1u;
+    bool overflow = false;
+    int pos0 = write_init_blocks(nb, n_init, out, k_tot, overflow, lane);
+    int eq_seen = 0;
+#pragma unroll 1
+    for (int m = 0; 32 * m < n_cand; ++m) {
+        const bool eq = (eq_mask >> m) & 1ull;
+        bool sel = (gt_mask >> m) & 1ull;
+        const unsigned em = __ballot_sync(0xffffffffu, eq);
+        if (eq)
+            sel = eq_seen + __popc(em & lt) < need;
+        eq_seen += __popc(em);
+        const unsigned sm = __ballot_sync(0xffffffffu, sel);
+        if (sel) {
+            const int pos = pos0 + __popc(sm & lt);
+            if (pos < k_tot)
+                out[pos] = cand_lo + lane + 32 * m;
+            else
+                overflow = true;
+        }
+        pos0 += __popc(sm);
+    }
+    write_local_and_close(nb, n_init, n_local, pos0, out, k_tot, count_out, status, overflow, lane);
+}
+
 // The exact top-k of one pair by one warp over the order keys of blocks [0, nb) (shared
 // array at keys_s): the k largest keys among candidates [n_init, nb - n_local) (equal
 // keys: lower block first), united with B_init and B_local, written ascending to
@@ -474,101 +565,6 @@ __device__ __forceinline__ void topk_threshold_cta(uint32_t keys_s, int cand_lo,
         pmask |= 255u << shift;
     }
     prefix_out = prefix;
-    need_out = need;
-}
-
-// topk_threshold_cta for one warp alone (no named barrier): the k-th largest key among
-// keys[cand_lo, cand_hi) and how many keys equal to it are taken, by four passes of
-// 8-bit digits over the warp's 256 shared-memory bins at hist_s.
-__device__ __forceinline__ void topk_threshold_warp(uint32_t keys_s, int cand_lo, int cand_hi, int k, uint32_t hist_s,
-                                                    int lane, uint32_t &prefix_out, int &need_out)
-{
-    uint32_t prefix = 0u, pmask = 0u;
-    int need = k;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int d = lane; d < 256; d += 32)
-            sts_u32(hist_s + 4 * d, 0u);
-        __syncwarp();
-        for (int ib = cand_lo; ib < cand_hi; ib += 32) {
-            const int i = ib + lane;
-            uint32_t digit = 0xFFFFFFFFu;
-            if (i < cand_hi) {
-                const uint32_t key = lds_u32(keys_s + 4 * i);
-                if ((key & pmask) == prefix)
-                    digit = (key >> shift) & 255u;
-            }
-            const uint32_t d0 = __shfl_sync(0xffffffffu, digit, 0);
-            const unsigned agree = __ballot_sync(0xffffffffu, digit == d0);
-            if (agree == 0xffffffffu) {
-                if (lane == 0 && d0 != 0xFFFFFFFFu)
-                    asm volatile("red.shared.add.u32 [%0], 32;" ::"r"(hist_s + 4 * d0) : "memory");
-            } else if (digit != 0xFFFFFFFFu) {
-                asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(hist_s + 4 * digit) : "memory");
-            }
-        }
-        __syncwarp();
-        uint32_t d;
-        warp_pick_digit(hist_s, need, d, lane);
-        prefix |= d << shift;
-        pmask |= 255u << shift;
-        __syncwarp();
-    }
-    prefix_out = prefix;
-    need_out = need;
-}
-
-// The k-th largest key among keys[cand_lo, cand_hi) (at most 32 * KPL of them) by one
-// warp with the keys in registers: a binary search over the key bits from the top, each
-// step counting with a warp sum the keys that share the decided bits and have the next
-// bit set.  When every key sharing the decided bits is needed, the threshold is their
-// smallest key and the search stops (random scores: after about log2(n) steps).
-// Gives the threshold and how many keys equal to it are taken, as topk_threshold_warp.
-template <int KPL>
-__device__ __forceinline__ void topk_threshold_regs(uint32_t keys_s, int cand_lo, int cand_hi, int k, int lane,
-                                                    uint32_t &prefix_out, int &need_out)
-{
-    uint32_t key[KPL];
-    const int nv = max(0, (cand_hi - cand_lo - lane + 31) / 32);   // this lane's valid slots
-#pragma unroll
-    for (int m = 0; m < KPL; ++m)
-        key[m] = m < nv ? lds_u32(keys_s + 4 * (cand_lo + lane + 32 * m)) : 0u;
-    uint32_t P = 0u, hmask = 0u;
-    int need = k;
-    int mt = max(0, cand_hi - cand_lo);   // keys sharing the decided bits (all, at first)
-    for (int b = 31; b >= 0; --b) {
-        if (mt == need) {
-            // every key sharing the decided bits is taken: the smallest is the threshold
-            uint32_t mn = 0xFFFFFFFFu;
-#pragma unroll
-            for (int m = 0; m < KPL; ++m)
-                if (m < nv && (key[m] & hmask) == P)
-                    mn = min(mn, key[m]);
-            mn = __reduce_min_sync(0xffffffffu, mn);
-            int eq = 0;
-#pragma unroll
-            for (int m = 0; m < KPL; ++m)
-                eq += (m < nv && key[m] == mn) ? 1 : 0;
-            P = mn;
-            need = __reduce_add_sync(0xffffffffu, eq);
-            break;
-        }
-        const uint32_t bit = 1u << b;
-        const uint32_t m2 = hmask | bit, want = P | bit;
-        int c = 0;   // keys sharing the decided bits with bit b set (an empty slot holds 0: never)
-#pragma unroll
-        for (int m = 0; m < KPL; ++m)
-            c += (key[m] & m2) == want ? 1 : 0;
-        c = __reduce_add_sync(0xffffffffu, c);
-        if (c >= need) {
-            P = want;
-            mt = c;
-        } else {
-            need -= c;
-            mt -= c;
-        }
-        hmask = m2;
-    }
-    prefix_out = P;
     need_out = need;
 }
 
