@@ -400,6 +400,25 @@ def test_nsa_select_matches_oracle(cmp, H_q, H_kv, k):
     _assert_route_matches(idx, cnt, ir, cr, sc, c["lens_p"], n_init, n_local, max(k, 1))
 
 
+@pytest.mark.parametrize("n_blocks", [2723, 2724, 3000])
+def test_nsa_select_register_and_radix_topk_boundary(n_blocks):
+    """Block rows: up to 2720 candidates the top-k keeps them in registers across CTA 0's
+    160 threads; 2721 and more take the radix threshold and the one-warp write."""
+    B, H_q, H_kv, T_cap = 1, 8, 2, n_blocks * BLK
+    lens_b = [T_cap]
+    c = _route_case(B, H_q, H_kv, T_cap, lens_b, (0, 0), seed=470 + n_blocks)
+    n_init, n_local, k = 1, 2, 64
+    k_tot = n_init + n_local + k
+    idx = torch.full((B, H_kv, k_tot), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((B, H_kv), -7, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.sparse_nsa_select(c["Q"], c["khat"], c["seq"], n_init, n_local, k, idx, cnt, cmp=(0, 0), status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    ir, cr, sc = oracle.select_heads(c["Qb"], _bits_to_f64(c["kb"]), c["lens_p"], n_init, n_local, k, k_tot)
+    _assert_route_matches(idx, cnt, ir, cr, sc, c["lens_p"], n_init, n_local, k)
+
+
 def test_nsa_select_short_and_empty_lengths():
     """No complete window (every block scores 0: ties to the lower index), one token,
     an empty sequence, n_local = 0."""

@@ -51,6 +51,17 @@ def test_select_heads_matches_oracle(H_q, H_kv, N_cap, lens_b, k):
     assert_selection_matches(idx, cnt, ridx, rcnt, rs, lens_p, 1, 2, k)
 
 
+@pytest.mark.parametrize("N_cap", [2723, 2724, 3500])
+def test_select_heads_register_and_radix_topk_boundary(N_cap):
+    """The block-wide top-k keeps up to 17 candidates a thread in registers (2720 with the
+    group's 160 threads); 2721 and more take the radix threshold and the one-warp write.
+    N_cap = 2723 sits on the boundary (2720 candidates), 2724 just past it."""
+    lens_b = [N_cap * BLK, N_cap * BLK - 100]
+    idx, cnt, (ridx, rcnt, rs), lens_p, st = _run(lens_b, 8, 2, N_cap, 1, 2, 64, seed=N_cap)
+    assert st == 0
+    assert_selection_matches(idx, cnt, ridx, rcnt, rs, lens_p, 1, 2, 64)
+
+
 def test_select_heads_scale_argument_and_sharp_softmax():
     # a large scale makes each head's softmax nearly one-hot: the sum then counts heads
     idx, cnt, (ridx, rcnt, rs), lens_p, st = _run([64 * 300, 64 * 250 + 7], 32, 4, 300, 1, 2, 12, seed=5,
