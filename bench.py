@@ -457,25 +457,66 @@ def run_ours(args, rank, world, local_rank):
     in_step_gbs = dom_bytes / (in_step_ms * 1e-3) / 1e9
     del flush
 
-    # ---- end to end through the binding: Q and F from pinned host memory in, O out
+    # ---- end to end through the binding: Q and F from pinned host memory in, O out.
+    # Double-buffered: a second set of Q / F / O device buffers with its own graph; one
+    # stream moves step s+1's inputs in while step s runs, another moves step s's
+    # outputs out while step s+1 runs.  Every step's copies are inside the timed region.
     Qh = wk.Q.cpu().pin_memory()
     Fh = wk.F.cpu().pin_memory()
     F0h = wk.F0.cpu().pin_memory()
     Oh = torch.empty(wk.O.shape, dtype=wk.O.dtype).pin_memory()
-    e_steps = max(3, K // 4)
+    sets = [(wk.Q, wk.F, wk.F0, wk.O, graph)]
+    wk.Q, wk.F, wk.F0, wk.O = (torch.empty_like(wk.Q), torch.empty_like(wk.F), torch.empty_like(wk.F0),
+                               torch.empty_like(wk.O))
+    wk.Q.copy_(sets[0][0])
+    wk.F.copy_(sets[0][1])
+    wk.F0.copy_(sets[0][2])
+    sets.append((wk.Q, wk.F, wk.F0, wk.O, wk.capture()))
+    main = torch.cuda.current_stream(dev)
+    h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    e_steps = max(4, K // 4)
+    graph_done = [None, None]   # the last step of set i: its graph (inputs read, O written)
+    d2h_done = [None, None]     # ... and the copy that read its O
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
-    e0.record()
-    for _ in range(e_steps):
-        wk.Q.copy_(Qh, non_blocking=True)
-        wk.F.copy_(Fh, non_blocking=True)
-        wk.F0.copy_(F0h, non_blocking=True)
-        graph.replay()
-        Oh.copy_(wk.O, non_blocking=True)
-    e1.record()
+    for st in range(-2, e_steps):   # two untimed steps first: both graphs uploaded and warm
+        if st == 0:
+            main.wait_stream(h2d_s)
+            main.wait_stream(d2h_s)
+            torch.cuda.synchronize(dev)
+            e0.record(main)
+            h2d_s.wait_stream(main)
+            d2h_s.wait_stream(main)
+        i = st % 2
+        Qd, Fd, F0d, Od, g_ = sets[i]
+        with torch.cuda.stream(h2d_s):
+            if graph_done[i] is not None:
+                h2d_s.wait_event(graph_done[i])   # step st-2 has read this set's inputs
+            Qd.copy_(Qh, non_blocking=True)
+            Fd.copy_(Fh, non_blocking=True)
+            F0d.copy_(F0h, non_blocking=True)
+            ready = torch.cuda.Event()
+            ready.record(h2d_s)
+        main.wait_event(ready)
+        if d2h_done[i] is not None:
+            main.wait_event(d2h_done[i])          # step st-2's O has been copied out
+        g_.replay()
+        done = torch.cuda.Event()
+        done.record(main)
+        graph_done[i] = done
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(done)
+            Oh.copy_(Od, non_blocking=True)
+            out = torch.cuda.Event()
+            out.record(d2h_s)
+            d2h_done[i] = out
+    main.wait_stream(h2d_s)
+    main.wait_stream(d2h_s)
+    e1.record(main)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / e_steps
+    wk.Q, wk.F, wk.F0, wk.O = sets[0][:4]
     h2d = Qh.numel() * 2 + Fh.numel() * 2 + F0h.numel() * 2
     d2h = Oh.numel() * 2
     assert wk.status.item() == 0, f"device status {wk.status.item()}"
