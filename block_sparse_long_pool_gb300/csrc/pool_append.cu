@@ -42,6 +42,8 @@ __global__ void __launch_bounds__(kThreads) pool_append_kernel(const AppendParam
 {
     __shared__ float red[16][kD + 4];
     __shared__ float redv[16][kD + 4];
+    griddep_wait();                // the new rows may be the preceding kernel's output
+    griddep_launch_dependents();   // the next kernel may be scheduled now; it waits for this one
 
     const int pair = blockIdx.y;
     const int j = p.first_block + static_cast<int>(blockIdx.x);
@@ -124,6 +126,26 @@ __global__ void __launch_bounds__(kThreads) pool_append_kernel(const AppendParam
 
 namespace {
 
+// One launch of a kThreads-thread kernel taking one parameter struct, with programmatic
+// stream serialization: it may be scheduled while the kernel before it drains (it waits
+// for that kernel itself), and it lets the kernel after it do the same.
+template <typename Params>
+cudaError_t launch_pdl(const void *kern, dim3 grid, const Params *prm, void *stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *args[] = {const_cast<Params *>(prm)};
+    return cudaLaunchKernelExC(&cfg, kern, args);
+}
+
 int append_impl(const char *name, uint16_t *k_cache, uint16_t *v_cache, float *ktil, float *vtil,
                 uint16_t *khat, uint16_t *vhat, const uint16_t *k_new, const uint16_t *v_new, int B, int H_kv,
                 long long T_cap, int N_cap, long long len_before, int n_new, void *stream)
@@ -162,8 +184,8 @@ int append_impl(const char *name, uint16_t *k_cache, uint16_t *v_cache, float *k
         if (rc0 != SPARSE_OK)
             return rc0;
     }
-    pool_append_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(p);
-    return sp_host::cuda_status(cudaGetLastError(), name);
+    return sp_host::cuda_status(launch_pdl(reinterpret_cast<const void *>(pool_append_kernel), grid, &p, stream),
+                                name);
 }
 
 }  // namespace
@@ -215,6 +237,8 @@ struct CompressParams {
 __global__ void __launch_bounds__(kThreads) compress_windows_kernel(const CompressParams p)
 {
     __shared__ float red[2][16][kD + 4];
+    griddep_wait();                // the cache rows may be the preceding kernel's output
+    griddep_launch_dependents();   // the next kernel may be scheduled now; it waits for this one
     const int pair = blockIdx.y;
     const int j = p.first_row + static_cast<int>(blockIdx.x);
     const int c = threadIdx.x & 15;   // dims 8c .. 8c+7
@@ -301,6 +325,6 @@ extern "C" SPARSE_API int sparse_nsa_compress(const uint16_t *k_cache, const uin
         if (rc0 != SPARSE_OK)
             return rc0;
     }
-    compress_windows_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(p);
-    return sp_host::cuda_status(cudaGetLastError(), name);
+    return sp_host::cuda_status(
+        launch_pdl(reinterpret_cast<const void *>(compress_windows_kernel), grid, &p, stream), name);
 }

@@ -72,6 +72,10 @@ SPARSE_API int sparse_version(void);
  *   k_new, v_new      [B][H_kv][n_new][128] bf16, read.
  * Requires len_before >= 0, n_new >= 1, len_before + n_new <= T_cap.  The caches may
  * be device memory or mapped pinned host memory.
+ * Launch order: programmatic stream serialization.  The kernel waits for the kernel
+ * before it on the stream before reading anything, and lets the kernel after it be
+ * scheduled at once; that kernel must wait (as every call of this library does,
+ * unless a flag promises otherwise) before reading what this one writes.
  */
 SPARSE_API int sparse_pool_append(uint16_t *k_cache, uint16_t *v_cache, float *ktil,
                                   const uint16_t *k_new, const uint16_t *v_new,
@@ -312,9 +316,9 @@ SPARSE_API int sparse_decode_attn_ex(const uint16_t *Q, const uint16_t *k_base,
  *   flags        0 or SPARSE_ATTN_BLOCKS_READY (as for sparse_decode_attn).
  * Shared memory holds the pair's N_cap keys: N_cap up to about 28000.
  *
- * Launch order.  seq_len and ktil_next must be complete before the kernel preceding
- * this one on the stream finishes (compressed keys are updated by the append of the
- * previous decode step): each CTA streams its slice of ktil_next at once.  Q and F may
+ * Launch order.  seq_len and ktil_next must not be written by the kernel preceding
+ * this one on the stream (compressed keys are updated by the append of the previous
+ * decode step): each CTA streams its slice of ktil_next at once.  Q and F may
  * be written by that preceding kernel; so may blk_idx and count unless
  * SPARSE_ATTN_BLOCKS_READY is passed.  The kernel lets the next kernel on the stream be
  * scheduled as soon as it has started, so a chain of these calls, layer after layer
