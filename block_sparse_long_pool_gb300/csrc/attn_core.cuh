@@ -467,18 +467,80 @@ __device__ __forceinline__ int producer_fetch_slice(const AttnParams &p, int pai
 
 // The merge of a cluster's partial states (split-KV): (1) each consumer warp's state
 // into shared memory, (2) merged into this CTA's state, (3) after one cluster barrier
-// CTA `rank` merges the S CTA states for its slice of output dims, reading its peers'
-// shared memory (distributed shared memory) with independent loads, and writes rows
-// [0, rows_valid) of O (and lse from rank 0).  Every thread of every CTA of the
-// cluster calls it (`nthreads` = blockDim.x); the ring at `base` is reused as scratch,
-// so every stage must have been consumed.  A CTA that failed its ready check
-// (`aborted`) makes the whole unit leave O and lse untouched.
+// The cluster merge of the S CTA states of a unit (decode pair, or verification group):
+// rows [0, rows_valid) of O (and lse) written once, from every CTA's partial softmax
+// state.  Every thread of every CTA of the cluster calls it (`nthreads` = blockDim.x);
+// the ring at `base` is reused as scratch, so every stage must have been consumed.  A
+// CTA that failed its ready check (`aborted`) makes the whole unit leave O and lse
+// untouched.  The caller has initialised the merge barriers (merge_barriers_init) and
+// arrived on the cluster barrier after that; `wait_cluster`: it has not waited on it yet.
+//   push (when the slots fit): the leader (rank 0) tells each peer once its ring is
+//     free; a peer merges its warps' states and copies its CTA state into the leader's
+//     slot (16-byte distributed-shared-memory stores), arrives on the leader's barrier
+//     and leaves; the leader merges the S states for every output dim.  No cluster-wide
+//     barrier: the peers do not wait for one another, nor for the leader's output.
+//   pull: every CTA waits for all, then merges the S states for its slice of the dims
+//     by reading its peers' shared memory, and all wait again before leaving.
+constexpr int kPushRecvOff = 48 * 1024;   // the leader's slots: past the warp and CTA states
+constexpr int kCtrlGoBar = 10;            // ctrl[10..11]: "the leader's slots are free" (every CTA)
+constexpr int kCtrlRecvBar = 12;          // ctrl[12..13]: the peers' states have landed (leader)
+static_assert(kPushRecvOff >= (kConsumerWarps * 16 * kD + 3 * kConsumerWarps * 16 + 16 * kD + 2 * 16 + 4) * 4,
+              "the slots lie past the warp and CTA states");
+
+template <int NT>
+__host__ __device__ constexpr int push_slot_floats()
+{
+    return 8 * NT * kD + 2 * 8 * NT + 4;   // CTA state: O [ROWS][128], m [ROWS], l [ROWS], abort flag
+}
+
+template <int NT>
+__host__ __device__ constexpr bool merge_pushes(uint32_t S)
+{
+    return S > 1 && kPushRecvOff + (S - 1) * push_slot_floats<NT>() * 4 <= kStages * kStageBytes;
+}
+
+// Thread 0 at kernel start, before fence_barrier_init and the cluster arrive.
+__device__ __forceinline__ void merge_barriers_init(uint32_t ctrl_s, uint32_t S, int nthreads)
+{
+    mbar_init(ctrl_s + 4 * kCtrlGoBar, 1);
+    mbar_init(ctrl_s + 4 * kCtrlRecvBar, (S > 1 ? S - 1 : 1) * static_cast<uint32_t>(nthreads / 32));
+}
+
+__device__ __forceinline__ void dsmem_st_v4(uint32_t addr, float4 v)
+{
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
+
+template <int NT, bool VERIFY>
+__device__ __forceinline__ void merge_write_item(const AttnParams &p, int b, int g, int q0, int row, int d, float M,
+                                                 float L, float ox, float oy, bool write_lse)
+{
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    size_t out;
+    if (VERIFY) {
+        const int qq = q0 + row / p.G, hh = row % p.G;
+        out = ((static_cast<size_t>(b) * p.N_q + qq) * p.H_q + g * p.G + hh) * kD + d;
+    } else {
+        out = (static_cast<size_t>(b) * p.H_q + g * p.G + row) * kD + d;
+    }
+    if (p.O32 != nullptr)
+        *reinterpret_cast<float2 *>(p.O32 + out) = make_float2(ox * inv, oy * inv);
+    else
+        *reinterpret_cast<uint32_t *>(p.O + out) = pack_bf16x2(ox * inv, oy * inv);
+    if (!VERIFY && write_lse && d == 0 && p.lse != nullptr)
+        p.lse[static_cast<size_t>(b) * p.H_q + g * p.G + row] = lse_of(M, L);
+}
+
 template <int NT, bool VERIFY>
 __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uint8_t *base, bool aborted,
                                                     const AttnParams &p, int b, int g, int q0, int rows_valid,
-                                                    uint32_t rank, uint32_t S, int nthreads)
+                                                    uint32_t rank, uint32_t S, int nthreads, uint32_t ctrl_s,
+                                                    bool wait_cluster)
 {
     constexpr int ROWS = 8 * NT;
+    constexpr int SLOT = push_slot_floats<NT>();
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     float *wo = reinterpret_cast<float *>(base);                     // [4][ROWS][128]
@@ -489,12 +551,85 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
     float *cm = co + ROWS * kD;                                      // [ROWS]
     float *cl = cm + ROWS;                                           // [ROWS]
     int *cabort = reinterpret_cast<int *>(cl + ROWS);                // [4]
+    const bool push = merge_pushes<NT>(S);
+    const uint32_t bar_go = ctrl_s + 4 * kCtrlGoBar, bar_recv = ctrl_s + 4 * kCtrlRecvBar;
+    if (wait_cluster)
+        cluster_wait();   // every CTA's merge barriers are initialised
+    if (push && rank == 0 && tid == 0)
+        for (uint32_t r = 1; r < S; ++r)   // this CTA's ring is consumed: the peers may fill its slots
+            mbar_arrive_cluster(dsmem_addr(bar_go, r));
     if (warp < kConsumerWarps)
         store_warp_state<NT>(st, wo, wm, wl, warp, lane);
     if (tid == 0)
         cabort[0] = aborted ? 1 : 0;
     __syncthreads();
     merge_warp_states<ROWS>(wo, wm, wl, wf, co, cm, cl, tid, nthreads, [] { __syncthreads(); });
+    __syncthreads();   // the CTA state (co, cm, cl, cabort) is complete
+    if (push) {
+        const float *slots = reinterpret_cast<const float *>(base + kPushRecvOff);   // [S - 1][SLOT]
+        if (rank != 0) {
+            // a peer: copy the CTA state, contiguous from co, into slot rank - 1 of the leader
+            const bool go = __all_sync(0xffffffffu, mbar_wait_cluster(bar_go, 0, kWaitNs));
+            if (!go) {
+                if (lane == 0)
+                    report(p.status, SPARSE_ERR_TIMEOUT);
+                return;
+            }
+            const uint32_t dst = dsmem_addr(smem_u32(base + kPushRecvOff) + (rank - 1) * SLOT * 4, 0);
+            const float4 *src = reinterpret_cast<const float4 *>(co);
+            for (int q4 = tid; q4 < SLOT / 4; q4 += nthreads)
+                dsmem_st_v4(dst + 16 * q4, src[q4]);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_cluster(dsmem_addr(bar_recv, 0));
+            return;
+        }
+        // the leader: the S states, own first, then the slots in rank order
+        if (!__all_sync(0xffffffffu, mbar_wait_cluster(bar_recv, 0, kWaitNs))) {
+            if (lane == 0)
+                report(p.status, SPARSE_ERR_TIMEOUT);
+            return;
+        }
+        int any_abort = cabort[0];
+        for (uint32_t c = 1; c < S; ++c)
+            any_abort |= reinterpret_cast<const int *>(slots + (c - 1) * SLOT + ROWS * kD + 2 * ROWS)[0];
+        if (any_abort)
+            return;
+        const int n_items = rows_valid * (kD / 2);
+        for (int item = tid; item < n_items; item += nthreads) {
+            const int row = item / (kD / 2);
+            const int d = 2 * (item - row * (kD / 2));
+            float mc[kMaxSplit], lc[kMaxSplit];
+            float2 v[kMaxSplit];
+#pragma unroll
+            for (int c = 0; c < kMaxSplit; ++c) {
+                if (c < static_cast<int>(S)) {
+                    const float *src = c == 0 ? co : slots + (c - 1) * SLOT;
+                    mc[c] = src[ROWS * kD + row];
+                    lc[c] = src[ROWS * kD + ROWS + row];
+                    v[c] = *reinterpret_cast<const float2 *>(src + row * kD + d);
+                } else {
+                    mc[c] = -INFINITY;
+                    lc[c] = 0.f;
+                    v[c] = make_float2(0.f, 0.f);
+                }
+            }
+            float M = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kMaxSplit; ++c)
+                M = fmaxf(M, mc[c]);
+            float L = 0.f, ox = 0.f, oy = 0.f;
+#pragma unroll
+            for (int c = 0; c < kMaxSplit; ++c) {
+                const float f = (M == -INFINITY || mc[c] == -INFINITY) ? 0.f : exp2f(mc[c] - M);
+                L = fmaf(lc[c], f, L);
+                ox = fmaf(f, v[c].x, ox);
+                oy = fmaf(f, v[c].y, oy);
+            }
+            merge_write_item<NT, VERIFY>(p, b, g, q0, row, d, M, L, ox, oy, true);
+        }
+        return;
+    }
     cluster_sync();
 
     // Peers' CTA states (generic pointers into distributed shared memory).  Every value
@@ -555,20 +690,7 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
             ox = fmaf(f, v[c].x, ox);
             oy = fmaf(f, v[c].y, oy);
         }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        size_t out;
-        if (VERIFY) {
-            const int qq = q0 + row / p.G, hh = row % p.G;
-            out = ((static_cast<size_t>(b) * p.N_q + qq) * p.H_q + g * p.G + hh) * kD + d;
-        } else {
-            out = (static_cast<size_t>(b) * p.H_q + g * p.G + row) * kD + d;
-        }
-        if (p.O32 != nullptr)
-            *reinterpret_cast<float2 *>(p.O32 + out) = make_float2(ox * inv, oy * inv);
-        else
-            *reinterpret_cast<uint32_t *>(p.O + out) = pack_bf16x2(ox * inv, oy * inv);
-        if (!VERIFY && rank == 0 && d == 0 && p.lse != nullptr)
-            p.lse[static_cast<size_t>(b) * p.H_q + g * p.G + row] = lse_of(M, L);
+        merge_write_item<NT, VERIFY>(p, b, g, q0, row, d, M, L, ox, oy, rank == 0);
     }
     // peers may still read this CTA's state
     cluster_sync();

@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(kFThreads, 2)
             mbar_init(bar_empty + 8 * s, kConsumerWarps);
         }
         mbar_init(bar_scored, S * kConsumerWarps);
+        if (ATTN)
+            merge_barriers_init(base_s + kOffCtrl, S, kFThreads);
         fence_barrier_init();
     }
     if (rank == 0 && score)
@@ -301,7 +303,8 @@ __global__ void __launch_bounds__(kFThreads, 2)
     // ---------------------------------------------------------------- merge
     if (ATTN) {
         __syncthreads();
-        cluster_merge_write<NT, false>(st, base, false, p, b, g, 0, p.G, rank, S, kFThreads);
+        cluster_merge_write<NT, false>(st, base, false, p, b, g, 0, p.G, rank, S, kFThreads, base_s + kOffCtrl,
+                                       false);
     }
 }
 
