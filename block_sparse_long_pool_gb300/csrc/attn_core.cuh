@@ -472,9 +472,10 @@ __device__ __forceinline__ int producer_fetch_slice(const AttnParams &p, int pai
 // state.  Every thread of every CTA of the cluster calls it (`nthreads` = blockDim.x);
 // the ring at `base` is reused as scratch, so every stage must have been consumed.  A
 // CTA that failed its ready check (`aborted`) makes the whole unit leave O and lse
-// untouched.  The caller has initialised the merge barriers (merge_barriers_init) and
-// arrived on the cluster barrier after that; `wait_cluster`: it has not waited on it yet.
-//   push (when the slots fit): the leader (rank 0) tells each peer once its ring is
+// untouched.  `wait_cluster`: the caller arrived on the cluster barrier at its start
+// and has not waited on it yet.  `allow_push`: the caller initialised the merge barriers
+// (merge_barriers_init) before that arrive, and the push form may run.
+//   push (when allowed and the slots fit): the leader (rank 0) tells each peer once its ring is
 //     free; a peer merges its warps' states and copies its CTA state into the leader's
 //     slot (16-byte distributed-shared-memory stores), arrives on the leader's barrier
 //     and leaves; the leader merges the S states for every output dim.  No cluster-wide
@@ -537,7 +538,7 @@ template <int NT, bool VERIFY>
 __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uint8_t *base, bool aborted,
                                                     const AttnParams &p, int b, int g, int q0, int rows_valid,
                                                     uint32_t rank, uint32_t S, int nthreads, uint32_t ctrl_s,
-                                                    bool wait_cluster)
+                                                    bool wait_cluster, bool allow_push)
 {
     constexpr int ROWS = 8 * NT;
     constexpr int SLOT = push_slot_floats<NT>();
@@ -551,7 +552,7 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
     float *cm = co + ROWS * kD;                                      // [ROWS]
     float *cl = cm + ROWS;                                           // [ROWS]
     int *cabort = reinterpret_cast<int *>(cl + ROWS);                // [4]
-    const bool push = merge_pushes<NT>(S);
+    const bool push = allow_push && merge_pushes<NT>(S);
     const uint32_t bar_go = ctrl_s + 4 * kCtrlGoBar, bar_recv = ctrl_s + 4 * kCtrlRecvBar;
     if (wait_cluster)
         cluster_wait();   // every CTA's merge barriers are initialised

@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(kFThreads, 2)
     if (ATTN) {
         __syncthreads();
         cluster_merge_write<NT, false>(st, base, false, p, b, g, 0, p.G, rank, S, kFThreads, base_s + kOffCtrl,
-                                       false);
+                                       false, true);
     }
 }
 

@@ -216,11 +216,9 @@ __device__ __forceinline__ void attn_cluster_cta(const CUtensorMap *kmap, const 
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, kConsumerWarps);
         }
-        merge_barriers_init(base_s + kOffCtrl, S, kThreads);
         fence_barrier_init();
     }
     __syncthreads();
-    cluster_arrive();   // waited in the merge: every CTA's merge barriers exist by then
     // Verification: the merged union of the group's block sets (ulist / umask, whole
     // list) is built by every thread; CTA r takes a contiguous slice of it.  Decode:
     // CTA r takes entries [r * ceil(k_tot / S), ...) of the pair's table, which its
@@ -325,7 +323,7 @@ __device__ __forceinline__ void attn_cluster_cta(const CUtensorMap *kmap, const 
     __syncthreads();
     griddep_launch_dependents();
     cluster_merge_write<NT, VERIFY>(st, base, ctrl[kCtrlAbort] != 0, p, b, g, q0, rows_valid, rank, S, kThreads,
-                                    base_s + kOffCtrl, true);
+                                    base_s + kOffCtrl, false, false);
 }
 
 template <int NT, bool VERIFY>
