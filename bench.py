@@ -21,6 +21,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -126,7 +127,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        # the raw samples (the JSON line carries their summary); SPARSE_POOL_CLOCKS_DIR moves them
+        out_dir = os.environ.get("SPARSE_POOL_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"sparse_pool_clocks_gpu{gpu_index}.csv")
 
     def __enter__(self):
         try:

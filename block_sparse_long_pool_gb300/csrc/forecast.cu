@@ -25,10 +25,14 @@
 //     memory); each warp then arrives on CTA 0's "scored" barrier; in the fused launch
 //     they then attend as the sparse_decode_attn cluster kernel does.
 //   * Warp 5 (selector) of CTA 0: waits on the "scored" barrier, finds the coarse bin
-//     that holds the k-th largest key, radix-selects within it and writes the list,
-//     while (in the fused launch) the consumers attend.
+//     that holds the k-th largest key, lists the candidates at or above it, finds the
+//     remaining bits by a binary search over that list held in registers and writes the
+//     list from the same registers, while (in the fused launch) the consumers attend.
 //   * The dependent launch is allowed at once: a following launch starts streaming its
 //     key slice as SMs free up, and waits for this one before reading what it writes.
+//   * The CTAs' partial softmax states merge by push (cluster_merge_write): CTA 0 tells
+//     the others when its ring is free, they copy their states into it and leave, and
+//     CTA 0 writes O; no cluster-wide barrier at the end of the layer.
 #include <string.h>
 
 #include "attn_core.cuh"
