@@ -636,7 +636,8 @@ def cpu_baseline(wk, budget_s: float = 15.0, slices: int = 4):
 
 def run_reference(args, rank, world, local_rank):
     """The oracle as the reference arm: every step times a bounded sample (one layer
-    slice of one batch element) and the line reports the extrapolated steps/s."""
+    slice of as many batch elements as keep the host cores busy, one thread per pair, as
+    the main line's cpu_baseline does) and the line reports the extrapolated steps/s."""
     if rank != 0:
         return
     import torch
@@ -650,8 +651,10 @@ def run_reference(args, rank, world, local_rank):
     wk = _Shim()
     wk.wl, wk.sh, wk.dev = wl, wl.DECODE_128K, dev
     cores = len(os.sched_getaffinity(0))
-    threads = min(cores, wk.sh.H_kv)
-    prepared = [_prepare_oracle_slice(wk, (7 * i) % wk.sh.layers, [i % wk.sh.B]) for i in range(4)]
+    per_call = max(1, min(wk.sh.B, cores // wk.sh.H_kv))   # batch elements per sample
+    threads = min(cores, per_call * wk.sh.H_kv)
+    prepared = [_prepare_oracle_slice(wk, (7 * i) % wk.sh.layers, [(i + j) % wk.sh.B for j in range(per_call)])
+                for i in range(4)]
     times = []
     for i in range(args.warmup + args.steps):
         dt, n = _time_oracle_slice(prepared[i % len(prepared)], threads)
@@ -660,8 +663,9 @@ def run_reference(args, rank, world, local_rank):
     per_pair_layer = statistics.mean(times)
     step_s = per_pair_layer * wk.sh.pairs * wk.sh.layers
     value = 1.0 / step_s
-    sample = (f"per step: one layer slice of one batch element (8 pairs) of {wk.sh.name}, select(l+1) + "
-              f"attention(l) in fp64, scaled to {wk.sh.pairs} pairs x {wk.sh.layers} layers")
+    sample = (f"per step: one layer slice of {per_call} batch element(s) ({per_call * wk.sh.H_kv} pairs) of "
+              f"{wk.sh.name}, select(l+1) + attention(l) in fp64 on {threads} threads, scaled to "
+              f"{wk.sh.pairs} pairs x {wk.sh.layers} layers")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "steps/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
