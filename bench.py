@@ -931,6 +931,26 @@ def run_verify_case(args, dev):
         out[key]["chained"] = {"layers": layers, "physical_kv_layers": phys, "avg_launch_us": round(us, 2),
                                "achieved_gbs": gbs, "frac_of_measured_hbm": frac,
                                "rounds_per_s": round(1e6 / (us * layers), 1)}
+    # the baseline of the SSV notes' kernel comparison: one decode-attention launch per
+    # verification query, each over its own blocks and the window (no grouping)
+    nb = (sh.T + BLK - 1) // BLK
+    W = torch.arange(nb - sh.window_blocks, nb, dtype=torch.int32, device=dev)
+    lists = [torch.cat([x["I"][:, :, q], W.expand(sh.B, sh.H_kv, sh.window_blocks)], dim=-1).sort(dim=-1).values
+             .contiguous() for q in range(sh.N_q)]
+    cnt_q = torch.full((sh.B, sh.H_kv), lists[0].shape[-1], dtype=torch.int32, device=dev)
+    Qs = [x["Q"][:, q].contiguous() for q in range(sh.N_q)]
+    Os = [torch.empty_like(Qs[0]) for _ in range(sh.N_q)]
+
+    def per_query():
+        for q in range(sh.N_q):
+            binding.sparse_decode_attn(Qs[q], x["K"], x["V"], lists[q], cnt_q, x["seq_len"], Os[q], status=status)
+    t = _event_times(per_query, args.steps, args.warmup, evict)
+    out["per_query_decode"] = {"launches": sh.N_q, **t,
+                               "blocks_requested": sh.N_q * sh.B * sh.H_kv * int(lists[0].shape[-1]),
+                               "grouped_speedup": round(t["median_us"] / out["grouped"]["median_us"], 3),
+                               "shared_layout_speedup": round(t["median_us"] / out["shared_layout"]["median_us"], 3),
+                               "note": "one sparse_decode_attn launch per verification query over its blocks and "
+                                       "the window, back to back on one stream"}
     assert status.item() == 0, f"device status {status.item()}"
     g, u = out["grouped"], out["ungrouped"]
     out["bytes_ratio"] = round(g["bytes_loaded"] / u["bytes_loaded"], 4)
