@@ -22,6 +22,9 @@ constexpr int kStageBytes = 2 * kTileBytes;     // K + V of one block: 32 KB
 constexpr int kMaxUnion = 512;
 constexpr int kMaxSplit = 8;
 constexpr uint64_t kWaitNs = 2000000000ull;
+// Row stride (floats) of the warp states in shared memory: a fragment store writes 8
+// dims of 4 rows two apart, and the 4 extra floats put those rows in distinct banks.
+constexpr int kWoStride = kD + 4;
 
 // Dynamic shared memory layout, offsets from a 1024-byte aligned base.
 constexpr int kOffBars = kStages * kStageBytes;          // full[kStages], empty[kStages]
@@ -290,7 +293,7 @@ __device__ __forceinline__ void finish_row_sums(WarpState<NT> &st)
         }
 }
 
-// Warp `warp`'s state into shared memory: wo [4][ROWS][128], wm / wl [4][ROWS].
+// Warp `warp`'s state into shared memory: wo [4][ROWS][kWoStride], wm / wl [4][ROWS].
 template <int NT>
 __device__ __forceinline__ void store_warp_state(const WarpState<NT> &st, float *wo, float *wm, float *wl, int warp,
                                                  int lane)
@@ -305,7 +308,7 @@ __device__ __forceinline__ void store_warp_state(const WarpState<NT> &st, float 
             for (int i = 0; i < 4; ++i) {
                 const int dim = mt * 16 + g8 + (i >> 1) * 8;
                 const int row = nt * 8 + 2 * t4 + (i & 1);
-                wo[(warp * ROWS + row) * kD + dim] = st.acc[mt][nt][i];
+                wo[(warp * ROWS + row) * kWoStride + dim] = st.acc[mt][nt][i];
             }
     if (g8 == 0) {
 #pragma unroll
@@ -319,8 +322,9 @@ __device__ __forceinline__ void store_warp_state(const WarpState<NT> &st, float 
     }
 }
 
-// Merge the 4 warp states (wo/wm/wl) into one CTA state: co [ROWS][128] unnormalised,
-// cm / cl [ROWS] its max and sum; wf [4][ROWS] scratch.  `t` / `nthreads` name the
+// Merge the 4 warp states (wo/wm/wl) into one CTA state: co [ROWS][128] unnormalised
+// (16-byte aligned, as are the rows of wo), cm / cl [ROWS] its max and sum; wf [4][ROWS]
+// scratch.  `t` / `nthreads` name the
 // participating threads; the caller synchronises them between the two phases through
 // `sync()`.
 template <int ROWS, typename Sync>
@@ -345,13 +349,21 @@ __device__ __forceinline__ void merge_warp_states(const float *wo, const float *
         cl[row] = L;
     }
     sync();
-    for (int item = t; item < ROWS * kD; item += nthreads) {
-        const int row = item / kD;
-        float o = 0.f;
+    // four adjacent dims per item (16-byte loads and stores)
+    for (int item = t; item < ROWS * (kD / 4); item += nthreads) {
+        const int row = item / (kD / 4);
+        const int d = 4 * (item - row * (kD / 4));
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int w4 = 0; w4 < kConsumerWarps; ++w4)
-            o = fmaf(wf[w4 * ROWS + row], wo[w4 * ROWS * kD + item], o);
-        co[item] = o;
+        for (int w4 = 0; w4 < kConsumerWarps; ++w4) {
+            const float f = wf[w4 * ROWS + row];
+            const float4 v = *reinterpret_cast<const float4 *>(wo + (w4 * ROWS + row) * kWoStride + d);
+            o.x = fmaf(f, v.x, o.x);
+            o.y = fmaf(f, v.y, o.y);
+            o.z = fmaf(f, v.z, o.z);
+            o.w = fmaf(f, v.w, o.w);
+        }
+        *reinterpret_cast<float4 *>(co + row * kD + d) = o;
     }
 }
 
@@ -485,7 +497,7 @@ __device__ __forceinline__ int producer_fetch_slice(const AttnParams &p, int pai
 constexpr int kPushRecvOff = 48 * 1024;   // the leader's slots: past the warp and CTA states
 constexpr int kCtrlGoBar = 10;            // ctrl[10..11]: "the leader's slots are free" (every CTA)
 constexpr int kCtrlRecvBar = 12;          // ctrl[12..13]: the peers' states have landed (leader)
-static_assert(kPushRecvOff >= (kConsumerWarps * 16 * kD + 3 * kConsumerWarps * 16 + 16 * kD + 2 * 16 + 4) * 4,
+static_assert(kPushRecvOff >= (kConsumerWarps * 16 * kWoStride + 3 * kConsumerWarps * 16 + 16 * kD + 2 * 16 + 4) * 4,
               "the slots lie past the warp and CTA states");
 
 template <int NT>
@@ -534,6 +546,28 @@ __device__ __forceinline__ void merge_write_item(const AttnParams &p, int b, int
         p.lse[static_cast<size_t>(b) * p.H_q + g * p.G + row] = lse_of(M, L);
 }
 
+// Four adjacent output dims [d, d + 4) of one row (16-byte aligned: d % 4 == 0).
+template <int NT, bool VERIFY>
+__device__ __forceinline__ void merge_write_item4(const AttnParams &p, int b, int g, int q0, int row, int d, float M,
+                                                  float L, float4 o, bool write_lse)
+{
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    size_t out;
+    if (VERIFY) {
+        const int qq = q0 + row / p.G, hh = row % p.G;
+        out = ((static_cast<size_t>(b) * p.N_q + qq) * p.H_q + g * p.G + hh) * kD + d;
+    } else {
+        out = (static_cast<size_t>(b) * p.H_q + g * p.G + row) * kD + d;
+    }
+    if (p.O32 != nullptr)
+        *reinterpret_cast<float4 *>(p.O32 + out) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+    else
+        *reinterpret_cast<uint2 *>(p.O + out) = make_uint2(pack_bf16x2(o.x * inv, o.y * inv),
+                                                           pack_bf16x2(o.z * inv, o.w * inv));
+    if (!VERIFY && write_lse && d == 0 && p.lse != nullptr)
+        p.lse[static_cast<size_t>(b) * p.H_q + g * p.G + row] = lse_of(M, L);
+}
+
 template <int NT, bool VERIFY>
 __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uint8_t *base, bool aborted,
                                                     const AttnParams &p, int b, int g, int q0, int rows_valid,
@@ -544,8 +578,8 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
     constexpr int SLOT = push_slot_floats<NT>();
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    float *wo = reinterpret_cast<float *>(base);                     // [4][ROWS][128]
-    float *wm = wo + kConsumerWarps * ROWS * kD;                     // [4][ROWS]
+    float *wo = reinterpret_cast<float *>(base);                     // [4][ROWS][kWoStride]
+    float *wm = wo + kConsumerWarps * ROWS * kWoStride;              // [4][ROWS]
     float *wl = wm + kConsumerWarps * ROWS;                          // [4][ROWS]
     float *wf = wl + kConsumerWarps * ROWS;                          // [4][ROWS] warp weights
     float *co = wf + kConsumerWarps * ROWS;                          // [ROWS][128] CTA state
@@ -649,27 +683,28 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
         pcl[c] = static_cast<const float *>(__cluster_map_shared_rank(cl, r));
         ab[c] = c < Si ? *static_cast<const int *>(__cluster_map_shared_rank(cabort, r)) : 0;
     }
-    // CTA `rank` writes dims [rank * 128 / S, (rank + 1) * 128 / S) of every row, two
-    // adjacent dims per item
+    // CTA `rank` writes dims [rank * 128 / S, (rank + 1) * 128 / S) of every row, four
+    // adjacent dims per item: with up to 16 rows and S >= 4, one item per thread, so the
+    // remote loads of the whole slice are one round trip
     const int dims_per = kD / Si;
     const int d0 = static_cast<int>(rank) * dims_per;
-    const int pairs_per_row = dims_per / 2;
-    const int n_items = rows_valid * pairs_per_row;
+    const int quads_per_row = dims_per / 4;
+    const int n_items = rows_valid * quads_per_row;
     for (int item = tid; item < n_items; item += nthreads) {
-        const int row = item / pairs_per_row;
-        const int d = d0 + 2 * (item - row * pairs_per_row);
+        const int row = item / quads_per_row;
+        const int d = d0 + 4 * (item - row * quads_per_row);
         float mc[kMaxSplit], lc[kMaxSplit];
-        float2 v[kMaxSplit];
+        float4 v[kMaxSplit];
 #pragma unroll
         for (int c = 0; c < kMaxSplit; ++c) {
             if (c < Si) {
                 mc[c] = pcm[c][row];
                 lc[c] = pcl[c][row];
-                v[c] = *reinterpret_cast<const float2 *>(pco[c] + row * kD + d);
+                v[c] = *reinterpret_cast<const float4 *>(pco[c] + row * kD + d);
             } else {
                 mc[c] = -INFINITY;
                 lc[c] = 0.f;
-                v[c] = make_float2(0.f, 0.f);
+                v[c] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
         int any_abort = 0;
@@ -683,15 +718,18 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
 #pragma unroll
         for (int c = 0; c < kMaxSplit; ++c)
             M = fmaxf(M, mc[c]);
-        float L = 0.f, ox = 0.f, oy = 0.f;
+        float L = 0.f;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < kMaxSplit; ++c) {
             const float f = (M == -INFINITY || mc[c] == -INFINITY) ? 0.f : exp2f(mc[c] - M);
             L = fmaf(lc[c], f, L);
-            ox = fmaf(f, v[c].x, ox);
-            oy = fmaf(f, v[c].y, oy);
+            o.x = fmaf(f, v[c].x, o.x);
+            o.y = fmaf(f, v[c].y, o.y);
+            o.z = fmaf(f, v[c].z, o.z);
+            o.w = fmaf(f, v[c].w, o.w);
         }
-        merge_write_item<NT, VERIFY>(p, b, g, q0, row, d, M, L, ox, oy, rank == 0);
+        merge_write_item4<NT, VERIFY>(p, b, g, q0, row, d, M, L, o, rank == 0);
     }
     // peers may still read this CTA's state
     cluster_sync();

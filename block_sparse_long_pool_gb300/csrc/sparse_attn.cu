@@ -454,8 +454,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     // ---------------------------------------------------------------- merge
     __syncthreads();
     griddep_launch_dependents();
-    float *wo = reinterpret_cast<float *>(base);                     // [4][ROWS][128]
-    float *wm = wo + kConsumerWarps * ROWS * kD;                     // [4][ROWS]
+    float *wo = reinterpret_cast<float *>(base);                     // [4][ROWS][kWoStride]
+    float *wm = wo + kConsumerWarps * ROWS * kWoStride;              // [4][ROWS]
     float *wl = wm + kConsumerWarps * ROWS;
     float *wf = wl + kConsumerWarps * ROWS;
     float *co = wf + kConsumerWarps * ROWS;                          // [ROWS][128] CTA state
@@ -568,7 +568,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // The split path's merge scratch must fit in the stage ring it reuses.
-static_assert((kConsumerWarps * 16 * kD + 3 * kConsumerWarps * 16 + 16 * kD + 2 * 16 + 2 * kMaxSplitWs * 16 + 2 * 16) *
+static_assert((kConsumerWarps * 16 * kWoStride + 3 * kConsumerWarps * 16 + 16 * kD + 2 * 16 + 2 * kMaxSplitWs * 16 +
+               2 * 16) *
                       4 <=
                   kStages * kStageBytes,
               "split merge scratch exceeds the stage ring");
@@ -601,6 +602,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 {
     constexpr int ROWS = 8 * NT;
     constexpr int PART = ROWS * kD + 2 * ROWS + 1;   // o, max, sum, valid flag
+    static_assert((kConsumerWarps * ROWS * kWoStride + 3 * kConsumerWarps * ROWS + ROWS * kD + 2 * ROWS) * 4 <=
+                      kStageBytes,
+                  "a segment's warp and CTA states fit the one stage it holds");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -797,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         float *co = nullptr, *cm = nullptr, *cl = nullptr;
         if (held >= 0) {
             float *wo = reinterpret_cast<float *>(base + held * kStageBytes);
-            float *wm = wo + kConsumerWarps * ROWS * kD;
+            float *wm = wo + kConsumerWarps * ROWS * kWoStride;
             float *wl = wm + kConsumerWarps * ROWS;
             float *wf = wl + kConsumerWarps * ROWS;
             co = wf + kConsumerWarps * ROWS;
@@ -1078,7 +1082,7 @@ int launch(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, in
 }
 
 // The merge scratch (warp and CTA states, weights) must fit in the ring it reuses.
-static_assert((3 * kConsumerWarps * 16 + kConsumerWarps * 16 * kD + 16 * kD + 2 * 16 + 4 + kMaxSplit * 16 + 2 * 16) *
+static_assert((3 * kConsumerWarps * 16 + kConsumerWarps * 16 * kWoStride + 16 * kD + 2 * 16 + 4 + kMaxSplit * 16 + 2 * 16) *
                       4 <=
                   kStages * kStageBytes,
               "merge scratch exceeds the stage ring");
@@ -1679,8 +1683,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     griddep_launch_dependents();
     // The three branches' warp states side by side (branch x = s, c, w), merged into
     // three CTA states in one pass.
-    constexpr int WO = kConsumerWarps * ROWS * kD, WR = kConsumerWarps * ROWS;
-    float *wo = reinterpret_cast<float *>(base);           // [3][4][ROWS][128]
+    constexpr int WO = kConsumerWarps * ROWS * kWoStride, WR = kConsumerWarps * ROWS;
+    float *wo = reinterpret_cast<float *>(base);           // [3][4][ROWS][kWoStride]
     float *wm = wo + 3 * WO;                               // [3][4][ROWS]
     float *wl = wm + 3 * WR;
     float *wf = wl + 3 * WR;
@@ -1715,11 +1719,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int item = tid; item < 3 * ROWS * kD; item += kThreads) {
         const int x = item / (ROWS * kD);
         const int r = item - x * ROWS * kD;
-        const int row = r / kD;
+        const int row = r / kD, d = r - row * kD;
         float o = 0.f;
 #pragma unroll
         for (int w4 = 0; w4 < kConsumerWarps; ++w4)
-            o = fmaf(wf[x * WR + w4 * ROWS + row], wo[x * WO + w4 * ROWS * kD + r], o);
+            o = fmaf(wf[x * WR + w4 * ROWS + row], wo[x * WO + (w4 * ROWS + row) * kWoStride + d], o);
         co[item] = o;
     }
     cluster_sync();
@@ -1785,7 +1789,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // The three-branch merge scratch must fit in the ring it reuses.
-static_assert((3 * kConsumerWarps * 8 * kD + 9 * kConsumerWarps * 8 + 3 * 8 * kD + 6 * 8) * 4 <= kStages * kStageBytes,
+static_assert((3 * kConsumerWarps * 8 * kWoStride + 9 * kConsumerWarps * 8 + 3 * 8 * kD + 6 * 8) * 4 <=
+                  kStages * kStageBytes,
               "NSA merge scratch exceeds the stage ring");
 
 size_t nsa_counter_bytes(long long pairs)
