@@ -505,6 +505,8 @@ __host__ __device__ constexpr int push_slot_floats()
 {
     return 8 * NT * kD + 2 * 8 * NT + 4;   // CTA state: O [ROWS][128], m [ROWS], l [ROWS], abort flag
 }
+static_assert(push_slot_floats<1>() % 4 == 0 && push_slot_floats<2>() % 4 == 0,
+              "each slot starts 16-byte aligned, so its rows take 16-byte loads");
 
 template <int NT>
 __host__ __device__ constexpr bool merge_pushes(uint32_t S)
@@ -524,26 +526,6 @@ __device__ __forceinline__ void dsmem_st_v4(uint32_t addr, float4 v)
     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
                  "f"(v.w)
                  : "memory");
-}
-
-template <int NT, bool VERIFY>
-__device__ __forceinline__ void merge_write_item(const AttnParams &p, int b, int g, int q0, int row, int d, float M,
-                                                 float L, float ox, float oy, bool write_lse)
-{
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    size_t out;
-    if (VERIFY) {
-        const int qq = q0 + row / p.G, hh = row % p.G;
-        out = ((static_cast<size_t>(b) * p.N_q + qq) * p.H_q + g * p.G + hh) * kD + d;
-    } else {
-        out = (static_cast<size_t>(b) * p.H_q + g * p.G + row) * kD + d;
-    }
-    if (p.O32 != nullptr)
-        *reinterpret_cast<float2 *>(p.O32 + out) = make_float2(ox * inv, oy * inv);
-    else
-        *reinterpret_cast<uint32_t *>(p.O + out) = pack_bf16x2(ox * inv, oy * inv);
-    if (!VERIFY && write_lse && d == 0 && p.lse != nullptr)
-        p.lse[static_cast<size_t>(b) * p.H_q + g * p.G + row] = lse_of(M, L);
 }
 
 // Four adjacent output dims [d, d + 4) of one row (16-byte aligned: d % 4 == 0).
@@ -630,38 +612,42 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
             any_abort |= reinterpret_cast<const int *>(slots + (c - 1) * SLOT + ROWS * kD + 2 * ROWS)[0];
         if (any_abort)
             return;
-        const int n_items = rows_valid * (kD / 2);
+        // four adjacent dims per item (the slots are 16-byte aligned: SLOT % 4 == 0)
+        const int n_items = rows_valid * (kD / 4);
         for (int item = tid; item < n_items; item += nthreads) {
-            const int row = item / (kD / 2);
-            const int d = 2 * (item - row * (kD / 2));
+            const int row = item / (kD / 4);
+            const int d = 4 * (item - row * (kD / 4));
             float mc[kMaxSplit], lc[kMaxSplit];
-            float2 v[kMaxSplit];
+            float4 v[kMaxSplit];
 #pragma unroll
             for (int c = 0; c < kMaxSplit; ++c) {
                 if (c < static_cast<int>(S)) {
                     const float *src = c == 0 ? co : slots + (c - 1) * SLOT;
                     mc[c] = src[ROWS * kD + row];
                     lc[c] = src[ROWS * kD + ROWS + row];
-                    v[c] = *reinterpret_cast<const float2 *>(src + row * kD + d);
+                    v[c] = *reinterpret_cast<const float4 *>(src + row * kD + d);
                 } else {
                     mc[c] = -INFINITY;
                     lc[c] = 0.f;
-                    v[c] = make_float2(0.f, 0.f);
+                    v[c] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
             float M = -INFINITY;
 #pragma unroll
             for (int c = 0; c < kMaxSplit; ++c)
                 M = fmaxf(M, mc[c]);
-            float L = 0.f, ox = 0.f, oy = 0.f;
+            float L = 0.f;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int c = 0; c < kMaxSplit; ++c) {
                 const float f = (M == -INFINITY || mc[c] == -INFINITY) ? 0.f : exp2f(mc[c] - M);
                 L = fmaf(lc[c], f, L);
-                ox = fmaf(f, v[c].x, ox);
-                oy = fmaf(f, v[c].y, oy);
+                o.x = fmaf(f, v[c].x, o.x);
+                o.y = fmaf(f, v[c].y, o.y);
+                o.z = fmaf(f, v[c].z, o.z);
+                o.w = fmaf(f, v[c].w, o.w);
             }
-            merge_write_item<NT, VERIFY>(p, b, g, q0, row, d, M, L, ox, oy, true);
+            merge_write_item4<NT, VERIFY>(p, b, g, q0, row, d, M, L, o, true);
         }
         return;
     }
