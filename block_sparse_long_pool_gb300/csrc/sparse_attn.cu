@@ -1716,15 +1716,23 @@ __global__ void __launch_bounds__(kThreads, 2)
         cl[x * ROWS + row] = L;
     }
     __syncthreads();
-    for (int item = tid; item < 3 * ROWS * kD; item += kThreads) {
-        const int x = item / (ROWS * kD);
-        const int r = item - x * ROWS * kD;
-        const int row = r / kD, d = r - row * kD;
-        float o = 0.f;
+    // four adjacent dims per item (16-byte loads and stores: WO, kWoStride and the offset
+    // of co are multiples of 4 floats)
+    for (int item = tid; item < 3 * ROWS * (kD / 4); item += kThreads) {
+        const int x = item / (ROWS * (kD / 4));
+        const int r = item - x * ROWS * (kD / 4);
+        const int row = r / (kD / 4), d = 4 * (r - row * (kD / 4));
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int w4 = 0; w4 < kConsumerWarps; ++w4)
-            o = fmaf(wf[x * WR + w4 * ROWS + row], wo[x * WO + (w4 * ROWS + row) * kWoStride + d], o);
-        co[item] = o;
+        for (int w4 = 0; w4 < kConsumerWarps; ++w4) {
+            const float f = wf[x * WR + w4 * ROWS + row];
+            const float4 v = *reinterpret_cast<const float4 *>(wo + x * WO + (w4 * ROWS + row) * kWoStride + d);
+            o.x = fmaf(f, v.x, o.x);
+            o.y = fmaf(f, v.y, o.y);
+            o.z = fmaf(f, v.z, o.z);
+            o.w = fmaf(f, v.w, o.w);
+        }
+        *reinterpret_cast<float4 *>(co + (x * ROWS + row) * kD + d) = o;
     }
     cluster_sync();
 
@@ -1792,6 +1800,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 static_assert((3 * kConsumerWarps * 8 * kWoStride + 9 * kConsumerWarps * 8 + 3 * 8 * kD + 6 * 8) * 4 <=
                   kStages * kStageBytes,
               "NSA merge scratch exceeds the stage ring");
+static_assert((3 * kConsumerWarps * 8 * kWoStride + 9 * kConsumerWarps * 8) % 4 == 0,
+              "the NSA CTA states start 16-byte aligned");
 
 size_t nsa_counter_bytes(long long pairs)
 {
