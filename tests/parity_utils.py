@@ -62,6 +62,24 @@ def assert_selection_matches(idx_gpu, cnt_gpu, idx_ref, cnt_ref, scores_ref, len
     return exempt
 
 
+def oracle_attn_on_taken_lists(idx_gpu, cnt_gpu, ridx, rcnt, Oref, Qb, Kb, Vb, lens):
+    """The oracle's attention over the block lists the GPU took, for checking an output
+    the GPU computed over its own selection: Oref (the oracle over its own lists) where
+    the lists agree, recomputed by the oracle over the GPU's list for every pair where
+    they differ.  Call assert_selection_matches first: a differing list is accepted only
+    when every differing block lies within the near-tie band, i.e. it is one of the
+    valid answers, and the attention over it must then be exact."""
+    P = ridx.shape[0]
+    gidx = idx_gpu.cpu().numpy().reshape(ridx.shape)
+    gcnt = cnt_gpu.cpu().numpy().reshape(rcnt.shape)
+    out = np.array(Oref, copy=True)
+    differ = [p for p in range(P) if gcnt[p] != rcnt[p] or not np.array_equal(gidx[p], ridx[p])]
+    if differ:
+        lens = np.asarray(lens)
+        out[differ], _ = oracle.attn(Qb[differ], Kb[differ], Vb[differ], gidx[differ], gcnt[differ], lens[differ])
+    return out, len(differ)
+
+
 class GpuLayer:
     """The CUDA path for one decode layer through the C-ABI binding."""
 

@@ -82,3 +82,41 @@ def test_noalloc_rejects_sizes_beyond_its_fixed_scratch():
     assert "scratch" in str(e.value)
     torch.cuda.synchronize()
     assert not out.any()
+
+
+@pytest.mark.parametrize("n_split", [37, 304])
+def test_noalloc_matches_the_oracle_at_other_splits(n_split):
+    """The allocation-free call with other CTA counts (ranges that cut pairs at other
+    points), against the fp64 oracle directly: the same tolerances as the decode tests."""
+    import oracle
+    Q, K, V, idx, cnt, seq = _inputs(303)
+    B, H_q = Q.shape[:2]
+    H_kv = K.shape[1]
+    P, G, T = B * H_kv, H_q // H_kv, K.shape[2]
+    out = torch.full_like(Q, 5.0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.sparse_decode_attn_noalloc(Q, K, V, idx, cnt, seq, out, n_split=n_split, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    Oref, _ = oracle.attn(wl.bf16_bits(Q).reshape(P, G, D), wl.bf16_bits(K).reshape(P, T, D),
+                          wl.bf16_bits(V).reshape(P, T, D), idx.cpu().numpy().reshape(P, -1),
+                          cnt.cpu().numpy().reshape(P), [T] * P)
+    err = np.abs(out.float().cpu().double().numpy().reshape(Oref.shape) - Oref)
+    assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, f"max {err.max():.3e} mean {err.mean():.3e}"
+
+
+def test_noalloc_rejected_call_leaves_the_scratch_alone():
+    """A call rejected by the argument checks launches nothing: a valid call right after
+    it still gives the right result (its counters were not disturbed half-way)."""
+    Q, K, V, idx, cnt, seq = _inputs(404)
+    out = torch.zeros_like(Q)
+    with pytest.raises(binding.SparsePoolError) as e:
+        binding.sparse_decode_attn_noalloc(Q, K, V, idx, cnt, seq, out, flags=0x80)   # an unknown flag
+    assert e.value.status == binding.SPARSE_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert not out.any()
+    ref = torch.zeros_like(Q)
+    binding.sparse_decode_attn(Q, K, V, idx, cnt, seq, ref)
+    binding.sparse_decode_attn_noalloc(Q, K, V, idx, cnt, seq, out)
+    torch.cuda.synchronize()
+    assert (out.float() - ref.float()).abs().max().item() <= MAX_ABS
