@@ -174,11 +174,14 @@ class ClockSampler:
 
 def step_config(sh, world: int) -> dict:
     """The workload the bench line is quoted on (both arms)."""
+    layer_gb = sh.pairs * sh.T * D * 2 * 2 / 1e9
     return {"workload": sh.name, "B": sh.B, "H_q": sh.H_q, "H_kv": sh.H_kv, "d": D, "T": sh.T,
             "layers": sh.layers, "physical_kv_layers": sh.phys_layers, "block": BLK, "k": sh.k,
             "n_init": sh.n_init, "n_local": sh.n_local, "blocks_per_pair": sh.k_tot,
             "parallelism": f"replicas x{world}",
-            "l2": "inputs larger than L2: 10 physical layers x 4.3 GB, same layer every 2.1 GB"}
+            "l2": f"inputs larger than L2: {sh.phys_layers} physical layers x {layer_gb:.2f} GB, the same layer "
+                  f"again after {sh.phys_layers * sh.pairs * (sh.k_tot * KV_BLOCK_BYTES + sh.N_b * KTIL_ROW_BYTES) / 1e9:.2f}"
+                  " GB of other reads"}
 
 
 def l2_evict(buf):
@@ -188,15 +191,24 @@ def l2_evict(buf):
     torch.sum(buf)
 
 
-class Decode128k:
-    """Device state of the 80-layer 128K decode step and its CUDA graph.
+def step_distribution(per_step_ms):
+    """Median and 10th / 90th percentiles of per-step times (ms)."""
+    xs = sorted(per_step_ms)
+    q = lambda f: xs[min(len(xs) - 1, int(f * len(xs)))]
+    return {"median": round(statistics.median(xs), 4), "p10": round(q(0.1), 4), "p90": round(q(0.9), 4),
+            "min": round(xs[0], 4), "max": round(xs[-1], 4), "steps": len(xs)}
+
+
+class DecodeStep:
+    """Device state of a multi-layer decode step (the 128K, 80-layer workloads) and its
+    CUDA graph.
 
     mode "fused": layer 0 selects with sparse_select_topk, then every layer l is one
     sparse_decode_attn_forecast launch (attention of l + Forecast selection of l+1), all
     on one stream.  mode "separate": sparse_select_topk of layer l+1 on a side stream
-    beside sparse_decode_attn of layer l."""
+    beside sparse_decode_attn of layer l (with a workspace: the split path)."""
 
-    def __init__(self, device, use_workspace=True, mode="fused"):
+    def __init__(self, device, shape=None, use_workspace=True, mode="fused", n_split=0):
         assert mode in ("fused", "separate")
         self.mode = mode
         import torch
@@ -204,7 +216,8 @@ class Decode128k:
         from block_sparse_long_pool_gb300 import workloads as wl
 
         self.torch, self.binding, self.wl = torch, binding, wl
-        sh = self.sh = wl.DECODE_128K
+        sh = self.sh = shape if shape is not None else wl.DECODE_128K
+        self.n_split = n_split
         self.dev = device
         B, H_kv, H_q, T = sh.B, sh.H_kv, sh.H_q, sh.T
         self.k_cap = sh.n_init + sh.n_local + sh.k
@@ -237,7 +250,8 @@ class Decode128k:
         self.seq = torch.full((B,), T, dtype=torch.int32, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.side = torch.cuda.Stream(device=device)
-        self.workspace = binding.decode_workspace(B, H_q, H_kv, self.k_cap, device=device) if use_workspace else None
+        self.workspace = (binding.decode_workspace(B, H_q, H_kv, self.k_cap, n_split, device=device)
+                          if use_workspace else None)
         torch.cuda.synchronize(device)
 
     # bytes the method has to move per step
@@ -250,8 +264,11 @@ class Decode128k:
     def attn_bytes_per_launch(self):
         return self.sh.pairs * self.sh.k_tot * KV_BLOCK_BYTES
 
+    def select_bytes_per_launch(self):
+        return self.sh.pairs * self.sh.N_b * KTIL_ROW_BYTES
+
     def fused_bytes_per_launch(self):
-        return self.attn_bytes_per_launch() + self.sh.pairs * self.sh.N_b * KTIL_ROW_BYTES
+        return self.attn_bytes_per_launch() + self.select_bytes_per_launch()
 
     def launches_per_step(self):
         if self.mode == "fused":
@@ -268,7 +285,8 @@ class Decode128k:
             self.Q[l], self.k_cache[q], self.v_cache[q], self.idx[l], self.count[l], self.seq, self.O[l],
             F=self.F[l] if nxt else None, ktil_next=self.ktil[(l + 1) % sh.phys_layers] if nxt else None,
             n_init=sh.n_init, n_local=sh.n_local, k=sh.k, idx_next=self.idx[l + 1] if nxt else None,
-            count_next=self.count[l + 1] if nxt else None, status=self.status, stream=stream)
+            count_next=self.count[l + 1] if nxt else None, n_split=self.n_split, status=self.status,
+            stream=stream)
 
     def _select(self, l_target, F, stream):
         sh = self.sh
@@ -276,30 +294,26 @@ class Decode128k:
                                         sh.k, self.idx[l_target], self.count[l_target], status=self.status,
                                         stream=stream)
 
-    def _attend(self, l, stream, n_split=0, count=None):
+    def _attend(self, l, stream, count=None, workspace=True):
         # the block list of every layer comes from the side stream through an event, so
         # K/V streaming may start while the previous attention drains
         q = l % self.sh.phys_layers
         count = self.count[l] if count is None else count
+        ws = self.workspace if workspace else None
         self.binding.sparse_decode_attn(self.Q[l], self.k_cache[q], self.v_cache[q], self.idx[l], count,
-                                        self.seq, self.O[l], status=self.status, n_split=n_split,
-                                        flags=self.binding.SPARSE_ATTN_BLOCKS_READY, workspace=self.workspace,
-                                        stream=stream)
+                                        self.seq, self.O[l], status=self.status,
+                                        n_split=self.n_split if ws is not None else 0,
+                                        flags=self.binding.SPARSE_ATTN_BLOCKS_READY, workspace=ws, stream=stream)
 
-    def enqueue_step(self, events=None, n_split=0):
-        """Enqueue one step on the current stream (+ the side stream in separate mode).
-        ``events`` (list of (start, end) pairs) brackets every attention launch when given."""
+    def enqueue_step(self):
+        """Enqueue one step on the current stream (+ the side stream in separate mode)."""
         torch = self.torch
         main = torch.cuda.current_stream(self.dev)
         L = self.sh.layers
         if self.mode == "fused":
             self._select(0, self.F0, main)           # layer 0: its own current-layer Forecast
             for l in range(L):
-                if events is not None:
-                    events[l][0].record(main)
                 self._fused(l, main)
-                if events is not None:
-                    events[l][1].record(main)
             return
         sel_done = [None] * L
         self.side.wait_stream(main)
@@ -318,11 +332,7 @@ class Decode128k:
                 sel_done[l + 1] = ev
             if sel_done[l] is not None:
                 main.wait_event(sel_done[l])
-            if events is not None:
-                events[l][0].record(main)
-            self._attend(l, main, n_split)
-            if events is not None:
-                events[l][1].record(main)
+            self._attend(l, main)
             after_prev_attn = torch.cuda.Event()
             after_prev_attn.record(main)
         main.wait_stream(self.side)
@@ -341,47 +351,42 @@ class Decode128k:
         return g
 
 
-def run_ours(args, rank, world, local_rank):
+Decode128k = DecodeStep
+
+
+def time_graph_steps(graph, K, world, dev, clocks_gpu):
+    """K graph replays, barrier + synchronize on both sides, a CUDA event between
+    consecutive replays (the per-step distribution) and clocks sampled meanwhile.
+    Returns (max-over-ranks ms per step, per-step ms, clock summary)."""
     import torch
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    dist_init(world, "nccl")
-    import __graft_entry__
-    __graft_entry__.build()
-
-    wk = Decode128k(dev, use_workspace=args.workspace, mode=args.step_mode)
-    graph = wk.capture()
-    K, W = args.steps, args.warmup
-    for _ in range(W):
-        graph.replay()
-    torch.cuda.synchronize(dev)
-    assert wk.status.item() == 0, f"device status {wk.status.item()}"
-
-    # ---- timed region: K graph replays (inputs resident in HBM, larger than L2)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local_rank) as clocks:
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    with ClockSampler(clocks_gpu) as clocks:
         barrier(world)
         torch.cuda.synchronize(dev)
-        start.record()
-        for _ in range(K):
+        evs[0].record()
+        for i in range(K):
             graph.replay()
-        end.record()
+            evs[i + 1].record()
         torch.cuda.synchronize(dev)
         barrier(world)
-    ms = max_over_ranks(start.elapsed_time(end), world, dev) / K
-    value = whole_job_steps_per_s(ms, world)
-    attn_b, sel_b = wk.algorithmic_bytes()
-    step_bytes = attn_b + sel_b
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(K)]
+    ms = max_over_ranks(evs[0].elapsed_time(evs[K]), world, dev) / K
+    return ms, per, clocks.summary()
 
-    # ---- per-launch kernel times, CUDA events on the launching stream, each launch
-    # after a 512 MB read that evicts L2 (a read leaves clean lines; a write would leave
-    # 129 MB of dirty lines for the timed kernel to write back); the block lists are
-    # the ones the step just selected.
+
+def kernel_breakdown(wk, dev, peak):
+    """Per-launch kernel times of the step's kernels, CUDA events on the launching
+    stream: each launch alone after a 512 MB read that evicts L2 (a read leaves clean
+    lines; a write would leave 129 MB of dirty lines for the timed kernel to write back),
+    and the layers' launches back to back in one graph.  The block lists are the ones
+    the step just selected."""
+    import torch
     flush = torch.ones(512 << 20 >> 2, dtype=torch.int32, device=dev)
     cur = torch.cuda.current_stream(dev)
     L = wk.sh.layers
+    reps_alone = 2 if L * 2 >= 160 else max(2, 160 // L)
 
-    def time_alone(fn, reps=2):
+    def time_alone(fn, reps=reps_alone):
         ev = []
         for _ in range(reps):
             for l in range(L):
@@ -413,20 +418,19 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize(dev)
         return a.elapsed_time(b) / (reps * L)
 
-    peak, peak_src = measured_peaks()
     # the standalone decode attention (sparse_decode_attn, resident cache, no workspace)
-    att_alone_ms, att_n = time_alone(lambda l: wk._attend(l, cur))
-    att_chain_ms = time_chain(lambda l, st_: wk._attend(l, st_))
+    att_alone_ms, att_n = time_alone(lambda l: wk._attend(l, cur, workspace=False))
+    att_chain_ms = time_chain(lambda l, st_: wk._attend(l, st_, workspace=False))
     att_bytes = wk.attn_bytes_per_launch()
     att_hash = kernel_source_hash(ATTN_SOURCES)
     # what a launch costs without streaming: the same launch with every count 0 (list
     # fetch, Q load, merge, O write), and a one-element torch kernel timed the same way
     zero_count = torch.zeros_like(wk.count[0])
-    att_empty_ms, _ = time_alone(lambda l: wk._attend(l, cur, count=zero_count), reps=1)
+    att_empty_ms, _ = time_alone(lambda l: wk._attend(l, cur, count=zero_count, workspace=False), reps=1)
     tiny = torch.zeros(1, device=dev)
     floor_ms, _ = time_alone(lambda l: tiny.add_(1.0), reps=1)
     stream_ms = att_alone_ms - att_empty_ms
-    attention = {"kernel": "sparse_attn_kernel (sparse_decode_attn, decode, G=8)",
+    attention = {"kernel": f"sparse_attn_kernel (sparse_decode_attn, decode, G={wk.sh.G})",
                  "algorithmic_bytes_per_launch": att_bytes,
                  "alone": {"avg_launch_us": round(att_alone_ms * 1e3, 2), "launches_timed": att_n,
                            "achieved": round(att_bytes / (att_alone_ms * 1e-3) / 1e9, 1),
@@ -442,32 +446,120 @@ def run_ours(args, rank, world, local_rank):
                  "chained": {"avg_launch_us": round(att_chain_ms * 1e3, 2), "launches": L,
                              "achieved": round(att_bytes / (att_chain_ms * 1e-3) / 1e9, 1),
                              "frac": round(att_bytes / (att_chain_ms * 1e-3) / 1e9 / peak, 4),
-                             "note": "80 launches back to back in a CUDA graph, one per layer"},
-                 "traffic": profiled_traffic(att_hash), "kernel_source_sha1": att_hash}
+                             "note": f"{L} launches back to back in a CUDA graph, one per layer"},
+                 "traffic": profiled_traffic(att_hash) if wk.sh.name == "decode_128k_70b_b8_80layers" else None,
+                 "kernel_source_sha1": att_hash}
+    sel_alone_ms, sel_n = time_alone(lambda l: wk._select(l, wk.F[l - 1] if l else wk.F0, cur))
+    sel_bytes = wk.select_bytes_per_launch()
+    selection = {"kernel": "decode_forecast_kernel<1, false> (sparse_select_topk)",
+                 "algorithmic_bytes_per_launch": sel_bytes,
+                 "alone": {"avg_launch_us": round(sel_alone_ms * 1e3, 2), "launches_timed": sel_n,
+                           "achieved": round(sel_bytes / (sel_alone_ms * 1e-3) / 1e9, 1),
+                           "frac": round(sel_bytes / (sel_alone_ms * 1e-3) / 1e9 / peak, 4)}}
+    out = {"attention": attention, "selection": selection}
     if wk.mode == "fused":
         dom_alone_ms, dom_n = time_alone(lambda l: wk._fused(l, cur))
         dom_bytes = wk.fused_bytes_per_launch()
-        dom_hash = kernel_source_hash(FUSED_SOURCES)
-        dom_traffic = profiled_traffic(dom_hash, "decode_forecast_128k_traffic.txt")
-        dom_name = ("decode_forecast_kernel (sparse_decode_attn_forecast: attention of layer l + Forecast "
-                    "selection of layer l+1, G=8)")
+        out["dominant"] = {"kernel": "decode_forecast_kernel (sparse_decode_attn_forecast: attention of layer l + "
+                                     f"Forecast selection of layer l+1, G={wk.sh.G})",
+                           "algorithmic_bytes_per_launch": dom_bytes, "source": FUSED_SOURCES,
+                           "alone_us": dom_alone_ms * 1e3, "alone_n": dom_n}
     else:
-        dom_alone_ms, dom_n, dom_bytes = att_alone_ms, att_n, att_bytes
-        dom_hash, dom_traffic = att_hash, attention["traffic"]
-        dom_name = "sparse_attn_kernel (sparse_decode_attn, decode, G=8)"
-    dom_gbs = dom_bytes / (dom_alone_ms * 1e-3) / 1e9
-    # the dominant kernel's launches in a step: fused, the 80 layers plus layer 0's selection
-    # launch counted with them; separate, the 80 attention launches (the selections run on
-    # a side stream beside them and their bytes are not counted)
-    dom_launches = wk.sh.layers + (1 if wk.mode == "fused" else 0)
-    in_step_ms = ms / dom_launches
-    in_step_gbs = dom_bytes / (in_step_ms * 1e-3) / 1e9
+        out["dominant"] = {"kernel": f"sparse_attn_kernel (sparse_decode_attn, G={wk.sh.G})",
+                           "algorithmic_bytes_per_launch": att_bytes, "source": ATTN_SOURCES,
+                           "alone_us": att_alone_ms * 1e3, "alone_n": att_n}
     del flush
+    return out
 
-    # ---- end to end through the binding: Q and F from pinned host memory in, O out.
-    # Double-buffered: a second set of Q / F / O device buffers with its own graph; one
-    # stream moves step s+1's inputs in while step s runs, another moves step s's
-    # outputs out while step s+1 runs.  Every step's copies are inside the timed region.
+
+def measure_decode_step(args, sh, rank, world, local_rank, with_e2e=True):
+    """The multi-layer decode step of workload ``sh``: its CUDA graph timed over K
+    replays, the roofline of the step, the per-kernel breakdown and (optionally) the
+    end-to-end number with host copies.  Returns the fields of a JSON line."""
+    import torch
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist_init(world, "nccl")
+    import __graft_entry__
+    __graft_entry__.build()
+
+    wk = DecodeStep(dev, sh, use_workspace=args.workspace, mode=args.step_mode, n_split=args.n_split)
+    graph = wk.capture()
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    assert wk.status.item() == 0, f"device status {wk.status.item()}"
+
+    # ---- timed region: K graph replays (inputs resident in HBM, larger than L2)
+    ms, per_step, clocks = time_graph_steps(graph, K, world, dev, local_rank)
+    value = whole_job_steps_per_s(ms, world)
+    attn_b, sel_b = wk.algorithmic_bytes()
+    step_bytes = attn_b + sel_b
+    peak, peak_src = measured_peaks()
+    kb = kernel_breakdown(wk, dev, peak)
+    dom = kb["dominant"]
+    dom_hash = kernel_source_hash(dom["source"])
+    dom_traffic = None
+    if sh.name == "decode_128k_70b_b8_80layers":
+        dom_traffic = (profiled_traffic(dom_hash, "decode_forecast_128k_traffic.txt") if wk.mode == "fused"
+                       else profiled_traffic(dom_hash))
+    launches = wk.launches_per_step()
+    achieved = step_bytes / (ms * 1e-3) / 1e9
+    alone_gbs = dom["algorithmic_bytes_per_launch"] / (dom["alone_us"] * 1e-6) / 1e9
+    roofline = {
+        "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+        "frac": round(achieved / peak, 4), "traffic": dom_traffic,
+        "kernel": dom["kernel"] + ", inside the timed step",
+        "achieved_is": "the step's algorithmic bytes (selected K/V + compressed keys of every launch) / the step's "
+                       "CUDA-event time: per launch, the average algorithmic bytes of the step's launches / their "
+                       "average duration",
+        "peak_source": peak_src + " (the one HBM figure: a burst copy)",
+        "algorithmic_bytes_per_step": step_bytes, "launches_per_step": launches,
+        "avg_launch_us": round(ms * 1e3 / launches, 2),
+        "algorithmic_bytes_per_launch": {"dominant": dom["algorithmic_bytes_per_launch"],
+                                         "layer0_selection": wk.select_bytes_per_launch(),
+                                         "average": round(step_bytes / launches)},
+        "traffic_is": "dram__bytes_read.sum + dram__bytes_write.sum of one dominant launch (ncu), null unless "
+                      "taken on the current kernel source",
+        "alone": {"avg_launch_us": round(dom["alone_us"], 2), "launches_timed": dom["alone_n"],
+                  "achieved": round(alone_gbs, 1), "frac": round(alone_gbs / peak, 4),
+                  "note": "each launch timed by itself after a 512 MB read that evicts L2"},
+        "kernel_source_sha1": dom_hash}
+    line = {
+        "value": round(value, 3), "unit": "steps/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(ms, 4), "step_ms": step_distribution(per_step),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, planted blocks)",
+        "config": dict(step_config(sh, world), step_mode=wk.mode, n_split=args.n_split,
+                       workspace=bool(args.workspace)),
+        "selected_kv_gbs": round(world * step_bytes / (ms * 1e-3) / 1e9, 1),
+        "hbm_frac_of_8tbs": round(step_bytes / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
+        "hbm_frac_of_measured": round(step_bytes / (ms * 1e-3) / 1e9 / peak, 4),
+        "bytes_per_step": {"selected_kv": attn_b, "compressed_keys": sel_b},
+        "roofline": roofline,
+        "attention_kernel": kb["attention"],
+        "selection_kernel": kb["selection"],
+        "gpu_launches": launches * K,
+        "clocks": clocks,
+    }
+    if with_e2e:
+        e2e_ms, h2d, d2h = measure_e2e(wk, graph, K, world, dev)
+        line["e2e"] = {"value": round(world * 1000.0 / e2e_ms, 3), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h}
+    assert wk.status.item() == 0, f"device status {wk.status.item()}"
+    line["cpu_baseline"] = (cpu_baseline(wk, budget_s=args.cpu_seconds)
+                            if rank == 0 and not args.no_cpu_baseline else None)
+    return line
+
+
+def measure_e2e(wk, graph, K, world, dev):
+    """End to end through the binding: Q and F from pinned host memory in, O out, every
+    step inside the timed region.  Double-buffered: a second set of Q / F / O device
+    buffers with its own graph; one stream moves step s+1's inputs in while step s runs,
+    another moves step s's outputs out while step s+1 runs.  Returns (ms per step, H2D
+    bytes per step, D2H bytes per step)."""
+    import torch
     Qh = wk.Q.cpu().pin_memory()
     Fh = wk.F.cpu().pin_memory()
     F0h = wk.F0.cpu().pin_memory()
@@ -526,67 +618,46 @@ def run_ours(args, rank, world, local_rank):
     wk.Q, wk.F, wk.F0, wk.O = sets[0][:4]
     h2d = Qh.numel() * 2 + Fh.numel() * 2 + F0h.numel() * 2
     d2h = Oh.numel() * 2
-    assert wk.status.item() == 0, f"device status {wk.status.item()}"
+    return e2e_ms, h2d, d2h
 
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wk, budget_s=args.cpu_seconds)
 
+def run_ours(args, rank, world, local_rank):
+    from block_sparse_long_pool_gb300 import workloads as wl
+    line = measure_decode_step(args, wl.DECODE_128K, rank, world, local_rank)
     if rank == 0:
-        sh = wk.sh
-        line = {
-            "metric": METRIC, "value": round(value, 3), "unit": "steps/s", "n_gpus": world, "steps": K,
-            "warmup": W, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, planted blocks)",
-            "config": step_config(sh, world),
-            "selected_kv_gbs": round(world * step_bytes / (ms * 1e-3) / 1e9, 1),
-            "hbm_frac_of_8tbs": round(step_bytes / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
-            "hbm_frac_of_measured": round(step_bytes / (ms * 1e-3) / 1e9 / peak, 4),
-            "bytes_per_step": {"selected_kv": attn_b, "compressed_keys": sel_b},
-            # the dominant kernel over the timed region: the step's CUDA-event time over its
-            # launches (they overlap under programmatic dependent launch; the one selection
-            # launch of a step is counted as a fused one); alone: each launch timed by itself
-            "roofline": {"bound": "hbm", "achieved": round(in_step_gbs, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(in_step_gbs / peak, 4), "traffic": dom_traffic,
-                         "kernel": dom_name + ", inside the timed step (step time / its launches per step)",
-                         "peak_source": peak_src + " (the one HBM figure: a burst copy)",
-                         "avg_launch_us": round(in_step_ms * 1e3, 2), "launches_timed": dom_launches * K,
-                         "algorithmic_bytes_per_launch": dom_bytes,
-                         "alone": {"avg_launch_us": round(dom_alone_ms * 1e3, 2), "launches_timed": dom_n,
-                                   "achieved": round(dom_gbs, 1), "frac": round(dom_gbs / peak, 4),
-                                   "note": "each launch timed by itself after a 512 MB read that evicts L2"},
-                         "kernel_source_sha1": dom_hash},
-            "attention_kernel": attention,
-            "step_mode": wk.mode,
-            "e2e": {"value": round(world * 1000.0 / e2e_ms, 3), "unit": "steps/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
-            "gpu_launches": wk.launches_per_step() * K,
-            "clocks": clocks.summary(),
-            "cpu_baseline": cpu,
-        }
-        print(json.dumps(line), flush=True)
+        print(json.dumps(dict({"metric": METRIC}, **line)), flush=True)
+
+
+def run_b1_case(args, local_rank):
+    """The literal B = 1 variant of the 128K step: all 80 layers resident (42.9 GB), 8
+    pairs per layer, so a launch has 8 pairs to spread over the SMs."""
+    from block_sparse_long_pool_gb300 import workloads as wl
+    line = measure_decode_step(args, wl.DECODE_128K_B1, 0, 1, local_rank)
+    print(json.dumps(dict({"case": "decode128k_b1", "metric": METRIC}, **line)), flush=True)
 
 
 # ----------------------------------------------------------------------------- CPU oracle baseline
 
 
-def _prepare_oracle_slice(wk, layer: int, batches):
+def _prepare_oracle_slice(wk, layer: int, batches, device=None):
     """Host copies of the inputs of one layer slice (the sampled batch elements): this
     layer's K/V and compressed keys, the next layer's compressed keys, Q_l and F_l.
     Pooling is not part of a decode step (the compressed keys are resident), so it
-    happens here, outside any timing."""
+    happens here, outside any timing.  ``device`` draws the inputs there (the GPU arm
+    draws them where its own kernels read them, so both see the same bytes)."""
     import numpy as np
     import oracle
     wl, sh = wk.wl, wk.sh
+    dev = wk.dev if device is None else device
     q_cur, q_next = layer % sh.phys_layers, (layer + 1) % sh.phys_layers
     planted = wl.planted_sets(sh, sh.phys_layers)
     pairs = [b * sh.H_kv + h for b in batches for h in range(sh.H_kv)]
     Ks, Vs, Kn = [], [], []
     for p in pairs:
-        k, v = wl.kv_pair(sh, q_cur, p, planted[q_cur, p], wk.dev)
+        k, v = wl.kv_pair(sh, q_cur, p, planted[q_cur, p], dev)
         Ks.append(wl.bf16_bits(k))
         Vs.append(wl.bf16_bits(v))
-        kn, _ = wl.kv_pair(sh, q_next, p, planted[q_next, p], wk.dev)
+        kn, _ = wl.kv_pair(sh, q_next, p, planted[q_next, p], dev)
         Kn.append(wl.bf16_bits(kn))
     K, V, Knext = np.stack(Ks), np.stack(Vs), np.stack(Kn)
     lens = [sh.T] * len(pairs)
@@ -610,13 +681,19 @@ def _time_oracle_slice(sl, threads: int):
     return time.perf_counter() - t0, sl["n"]
 
 
-def cpu_baseline(wk, budget_s: float = 15.0, slices: int = 4):
-    """The oracle on the host cores over a bounded sample of the 128K step: layer slices
-    of B_s batch elements (B_s x 8 pairs, one OpenMP thread per pair), repeated until
-    the time budget is spent, scaled to 80 layers x 64 pairs."""
+def _slice_geometry(sh):
+    """Batch elements per oracle slice and threads: one OpenMP thread per pair, as many
+    pairs as keep the host cores busy."""
     cores = len(os.sched_getaffinity(0))
-    per_call = max(1, min(wk.sh.B, cores // wk.sh.H_kv))
-    threads = min(cores, per_call * wk.sh.H_kv)
+    per_call = max(1, min(sh.B, cores // sh.H_kv))
+    return per_call, min(cores, per_call * sh.H_kv)
+
+
+def cpu_baseline(wk, budget_s: float = 15.0, slices: int = 4):
+    """The oracle on the host cores over a bounded sample of the decode step: layer
+    slices of B_s batch elements (B_s x 8 pairs, one OpenMP thread per pair), repeated
+    until the time budget is spent, scaled to the step's layers x pairs."""
+    per_call, threads = _slice_geometry(wk.sh)
     prepared = [_prepare_oracle_slice(wk, (7 * i) % wk.sh.layers,
                                       [(i * per_call + j) % wk.sh.B for j in range(per_call)])
                 for i in range(slices)]
@@ -635,41 +712,47 @@ def cpu_baseline(wk, budget_s: float = 15.0, slices: int = 4):
 
 
 def run_reference(args, rank, world, local_rank):
-    """The oracle as the reference arm: every step times a bounded sample (one layer
-    slice of as many batch elements as keep the host cores busy, one thread per pair, as
-    the main line's cpu_baseline does) and the line reports the extrapolated steps/s."""
+    """The oracle as the reference arm, on the host cores only (no GPU, no CUDA
+    library): every step is one bounded sample of the 128K step -- one layer slice of
+    as many batch elements as keep the host cores busy (one thread per pair), the
+    selection of layer l+1 and the attention of layer l -- drawn on the CPU.  The line
+    reports the measured time per sample as ms_per_step and, as value, the steps/s of
+    the whole 80-layer, 64-pair step extrapolated from it (the factor is stated)."""
     if rank != 0:
         return
-    import torch
-    import __graft_entry__
-    __graft_entry__.build()
-    dev = torch.device("cuda", local_rank) if torch.cuda.is_available() else torch.device("cpu")
-
-    class _Shim:  # just the fields the sampler needs; inputs are regenerated per sample
-        pass
+    import oracle
     from block_sparse_long_pool_gb300 import workloads as wl
+    oracle.build()
+
+    class _Shim:  # just the fields the sampler needs
+        pass
     wk = _Shim()
-    wk.wl, wk.sh, wk.dev = wl, wl.DECODE_128K, dev
-    cores = len(os.sched_getaffinity(0))
-    per_call = max(1, min(wk.sh.B, cores // wk.sh.H_kv))   # batch elements per sample
-    threads = min(cores, per_call * wk.sh.H_kv)
+    wk.wl, wk.sh, wk.dev = wl, wl.DECODE_128K, "cpu"
+    per_call, threads = _slice_geometry(wk.sh)
+    t0 = time.perf_counter()
     prepared = [_prepare_oracle_slice(wk, (7 * i) % wk.sh.layers, [(i + j) % wk.sh.B for j in range(per_call)])
-                for i in range(4)]
-    times = []
+                for i in range(2)]
+    prep_s = time.perf_counter() - t0
+    times, n_pairs = [], 0
     for i in range(args.warmup + args.steps):
         dt, n = _time_oracle_slice(prepared[i % len(prepared)], threads)
         if i >= args.warmup:
-            times.append(dt / n)
-    per_pair_layer = statistics.mean(times)
-    step_s = per_pair_layer * wk.sh.pairs * wk.sh.layers
-    value = 1.0 / step_s
-    sample = (f"per step: one layer slice of {per_call} batch element(s) ({per_call * wk.sh.H_kv} pairs) of "
-              f"{wk.sh.name}, select(l+1) + attention(l) in fp64 on {threads} threads, scaled to "
-              f"{wk.sh.pairs} pairs x {wk.sh.layers} layers")
+            times.append(dt)
+            n_pairs = n
+    slice_s = statistics.mean(times)
+    factor = wk.sh.pairs * wk.sh.layers / n_pairs
+    value = 1.0 / (slice_s * factor)
+    sample = (f"per step: one layer slice of {per_call} batch element(s) ({n_pairs} pairs) of {wk.sh.name}, "
+              f"select(l+1) + attention(l) in fp64 on {threads} threads; value = 1 / (slice time x "
+              f"{factor:g}), the whole step being {wk.sh.pairs} pairs x {wk.sh.layers} layers")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "steps/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(slice_s * 1e3, 3),
+            "ms_per_step_is": "the measured time of one timed sample (a layer slice), not of a whole step",
+            "extrapolation_factor": factor, "full_step_ms_extrapolated": round(slice_s * factor * 1e3, 1),
+            "timed_slices": len(times), "step_ms": step_distribution([t * 1e3 for t in times]),
+            "input_prep_s": round(prep_s, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded N(0,1) bf16, planted blocks)",
+            "data": "synthetic (seeded N(0,1) bf16, planted blocks; drawn on the CPU)",
             "config": step_config(wk.sh, world),
             "cpu_baseline": {"value": round(value, 6), "unit": "steps/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
@@ -809,6 +892,36 @@ def _rate(nbytes, t_us, peak):
     return round(gbs, 1), round(gbs / peak, 4)
 
 
+def case_roofline(kernel, nbytes, t_us, peak, peak_src, traffic=None, note=None):
+    """The roofline object of a case line: algorithmic bytes of one timed call over its
+    median CUDA-event time, against the measured HBM copy bandwidth."""
+    gbs = nbytes / (t_us * 1e-6) / 1e9
+    out = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
+           "traffic": traffic, "kernel": kernel, "algorithmic_bytes": int(nbytes), "median_us": t_us,
+           "peak_source": peak_src}
+    if note:
+        out["note"] = note
+    return out
+
+
+def oracle_baseline(fn, budget_s, units_per_call, unit, sample, min_reps=2):
+    """The oracle (as it stands) on the host cores: fn() runs one bounded sample of the
+    case's work in fp64, repeated until budget_s is spent; value = units per second,
+    the sample scaled by units_per_call (the part of the case's unit of work it is)."""
+    import oracle
+    threads = len(os.sched_getaffinity(0))
+    oracle.set_threads(threads)
+    spent, reps = 0.0, 0
+    while spent < budget_s or reps < min_reps:
+        t0 = time.perf_counter()
+        fn()
+        spent += time.perf_counter() - t0
+        reps += 1
+    per_call = spent / reps
+    return {"value": round(units_per_call / per_call, 6), "unit": unit, "cores": threads, "kind": "oracle",
+            "sample": f"{sample}; {reps} timed calls, {spent:.1f} s, {per_call * 1e3:.2f} ms per call"}
+
+
 class _Layer:
     """One decode layer on the device: cache, compressed keys, block lists, output."""
 
@@ -817,7 +930,7 @@ class _Layer:
         from block_sparse_long_pool_gb300 import binding
         from block_sparse_long_pool_gb300 import workloads as wl
         self.sh, self.binding = sh, binding
-        x = wl.single_layer(sh, dev)
+        x = self.x = wl.single_layer(sh, dev)
         B, H_kv, H_q = sh.B, sh.H_kv, sh.H_q
         self.k_cache = torch.zeros_like(x["K"])
         self.v_cache = torch.zeros_like(x["V"])
@@ -846,12 +959,44 @@ class _Layer:
                               workspace=self.ws, status=self.status)
 
 
+def single_layer_oracle(lay, budget_s):
+    """The oracle on one decode step of a single-layer workload, all pairs: the
+    compressed key of the block the appended token lands in (when the step appends),
+    the Forecast selection and the attention, in fp64.  The compressed keys of the
+    other blocks are resident (pooled outside the timing)."""
+    import numpy as np
+    import oracle
+    from block_sparse_long_pool_gb300 import workloads as wl
+    sh, x = lay.sh, lay.x
+    P = sh.pairs
+    K = wl.bf16_bits(x["K"]).reshape(P, sh.T_cap, D).copy()
+    V = wl.bf16_bits(x["V"]).reshape(P, sh.T_cap, D).copy()
+    if sh.n_new:
+        K[:, sh.T:sh.len_after] = wl.bf16_bits(x["k_new"]).reshape(P, sh.n_new, D)
+        V[:, sh.T:sh.len_after] = wl.bf16_bits(x["v_new"]).reshape(P, sh.n_new, D)
+    lens = [sh.len_after] * P
+    ktil = oracle.pool(K, lens, sh.N_b)
+    F = wl.bf16_bits(x["F"]).reshape(P, D)
+    Q = wl.bf16_bits(x["Q"]).reshape(P, sh.G, D)
+    j0 = sh.T // BLK                     # the block the appended tokens land in
+    blk = np.ascontiguousarray(K[:, j0 * BLK:(j0 + 1) * BLK]) if sh.n_new else None
+
+    def step():
+        if sh.n_new:
+            oracle.pool(blk, [sh.len_after - j0 * BLK] * P, 1)
+        idx, cnt, _ = oracle.select(F, ktil, lens, sh.n_init, sh.n_local, sh.k)
+        oracle.attn(Q, K, V, idx, cnt, lens)
+    what = ("append (the touched block's mean) + " if sh.n_new else "") + "select + attention"
+    return oracle_baseline(step, budget_s, 1.0, "steps/s", f"the whole step ({what}) of all {P} pairs in fp64")
+
+
 def run_single_layer_case(args, dev, sh, name):
     import torch
     peak, src = measured_peaks()
     lay = _Layer(sh, dev, use_workspace=args.workspace)
     evict = torch.ones(512 << 20 >> 2, dtype=torch.int32, device=dev)
-    t = _event_times(lay.step, args.steps, args.warmup, evict)
+    with ClockSampler(dev.index or 0) as clk:
+        t = _event_times(lay.step, args.steps, args.warmup, evict)
     torch.cuda.synchronize()
     assert lay.status.item() == 0, f"device status {lay.status.item()}"
     kv = sh.pairs * sh.k_tot * KV_BLOCK_BYTES
@@ -866,7 +1011,11 @@ def run_single_layer_case(args, dev, sh, name):
             "steps_per_s": round(1e6 / t["median_us"], 1), **t, "launches_per_step": launches,
             "algorithmic_bytes": {"selected_kv": kv, "compressed_keys": sel, "append": app},
             "achieved_gbs": gbs, "frac_of_measured_hbm": frac, "peak_gbs": peak, "peak_source": src,
-            "l2": "512 MB read evicts L2 before each step"}
+            "roofline": case_roofline(f"the step's {launches} launches (" + ("pool_append_kernel, " if sh.n_new
+                                      else "") + "decode_forecast_kernel<1, false>, sparse_attn_kernel)",
+                                      kv + sel + app, t["median_us"], peak, src),
+            "l2": "512 MB read evicts L2 before each step", "clocks": clk.summary(),
+            "cpu_baseline": None if args.no_cpu_baseline else single_layer_oracle(lay, args.case_cpu_seconds)}
     print(json.dumps(line), flush=True)
 
 
@@ -883,6 +1032,7 @@ def run_verify_case(args, dev):
     out = {"case": "verify64k", "workload": sh.name, "unit_of_work": "one verification round "
            f"({sh.N_q} queries x {sh.B * sh.H_kv} pairs)", "peak_gbs": peak, "peak_source": src,
            "l2": "512 MB read evicts L2 before each round"}
+    clk = ClockSampler(dev.index or 0).__enter__()
     for C, key, shared in ((sh.C, "grouped", False), (1, "ungrouped", False), (sh.C, "shared_layout", True)):
         loaded = torch.zeros(1, dtype=torch.int64, device=dev)
 
@@ -956,6 +1106,20 @@ def run_verify_case(args, dev):
     out["bytes_ratio"] = round(g["bytes_loaded"] / u["bytes_loaded"], 4)
     out["bytes_ratio_bound"] = round((1 + (sh.C - 1) * (1 - sh.gamma)) / sh.C, 4)
     out["time_ratio"] = round(g["median_us"] / u["median_us"], 4)
+    clk.__exit__(None, None, None)
+    out["clocks"] = clk.summary()
+    out["roofline"] = case_roofline("sparse_attn_kernel<2, true> (sparse_verify_attn_grouped, C = 4, G = 4)",
+                                    g["bytes_loaded"], g["median_us"], peak, src,
+                                    note="bytes = the blocks the grouped launch loads (blocks_loaded x 32 KB)")
+    if not args.no_cpu_baseline:
+        import oracle
+        Qb, Kb, Vb = wl.bf16_bits(x["Q"]), wl.bf16_bits(x["K"]), wl.bf16_bits(x["V"])
+        I = x["I"].cpu().numpy()
+        out["cpu_baseline"] = oracle_baseline(
+            lambda: oracle.verify(Qb, Kb, Vb, I, sh.C, sh.window_blocks, [sh.T] * sh.B), args.case_cpu_seconds,
+            1.0, "rounds/s", f"the whole round (mode A, C = {sh.C}: {sh.N_q} queries x {sh.B * sh.H_kv} pairs) in fp64")
+    else:
+        out["cpu_baseline"] = None
     print(json.dumps(out), flush=True)
 
 
@@ -963,12 +1127,14 @@ class Offload128k:
     """The offloaded 128K decode: K/V of every layer in pinned host memory, compressed
     keys resident, selected blocks gathered one layer ahead into a two-slot HBM ring."""
 
-    def __init__(self, dev):
+    def __init__(self, dev, layers=0):
+        import dataclasses
         import torch
         from block_sparse_long_pool_gb300 import binding
         from block_sparse_long_pool_gb300 import workloads as wl
         self.torch, self.binding, self.dev = torch, binding, dev
-        sh = self.sh = wl.OFFLOAD_128K
+        sh = self.sh = (dataclasses.replace(wl.OFFLOAD_128K, layers=layers, phys_layers=layers) if layers > 0
+                        else wl.OFFLOAD_128K)
         B, H_kv, H_q, T, L = sh.B, sh.H_kv, sh.H_q, sh.T, sh.layers
         planted = wl.planted_sets(sh, L)
         self.k_host, self.v_host, self.ktil = [], [], []
@@ -1062,7 +1228,7 @@ def run_offload_case(args, dev):
     import torch
     peak, src = measured_peaks()
     t0 = time.time()
-    wk = Offload128k(dev)
+    wk = Offload128k(dev, args.layers)
     setup_s = time.time() - t0
     sh = wk.sh
     # the link: one large pinned host -> device copy, and the gather kernel alone
@@ -1097,11 +1263,12 @@ def run_offload_case(args, dev):
     for _ in range(max(3, args.warmup)):
         graph.replay()
     torch.cuda.synchronize()
-    a.record()
-    for _ in range(steps):
-        graph.replay()
-    b.record()
-    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as clk:
+        a.record()
+        for _ in range(steps):
+            graph.replay()
+        b.record()
+        torch.cuda.synchronize()
     assert wk.status.item() == 0, f"device status {wk.status.item()}"
     ms = a.elapsed_time(b) / steps
     link_step = sh.layers * wk.link_bytes_per_layer()
@@ -1116,8 +1283,45 @@ def run_offload_case(args, dev):
             "pcie5_x16_nominal_gbs": 64.0, "hbm_bytes_per_step": hbm_step,
             "hbm_frac_of_measured": round(hbm_step / (ms * 1e-3) / 1e9 / peak, 4), "peak_gbs": peak,
             "peak_source": src, "host_kv_gb": round(2 * sh.layers * wk.k_host[0].numel() * 2 / 1e9, 1),
-            "setup_s": round(setup_s, 1)}
+            "setup_s": round(setup_s, 1),
+            "roofline": {"bound": "host link", "achieved": round(link_step / (ms * 1e-3) / 1e9, 1),
+                         "peak": round(memcpy_gbs, 1), "unit": "GB/s",
+                         "frac": round(link_step / (ms * 1e-3) / 1e9 / memcpy_gbs, 4), "traffic": None,
+                         "kernel": "gather_kernel (sparse_gather_offloaded) on the copy stream",
+                         "peak_source": "a pinned host -> device copy of 1 GB measured in this run"},
+            "clocks": clk.summary(),
+            "cpu_baseline": None if args.no_cpu_baseline else offload_oracle(wk, args.case_cpu_seconds)}
     print(json.dumps(line), flush=True)
+
+
+def offload_oracle(wk, budget_s):
+    """The oracle on one layer of the offloaded step, all pairs: the Forecast selection
+    from the resident compressed keys, the staging copy of the selected blocks from the
+    host cache into a ring, and the attention over the ring, in fp64; scaled to the
+    step's layers."""
+    import numpy as np
+    import oracle
+    from block_sparse_long_pool_gb300 import workloads as wl
+    sh = wk.sh
+    P, l = sh.pairs, 1
+    Kh = wl.bf16_bits(wk.k_host[l]).reshape(P, sh.T, D)   # views of the pinned host cache
+    Vh = wl.bf16_bits(wk.v_host[l]).reshape(P, sh.T, D)
+    lens = [sh.T] * P
+    ktil = oracle.pool(Kh, lens, sh.N_b)
+    F = wl.bf16_bits(wk.F[l - 1]).reshape(P, D)
+    Q = wl.bf16_bits(wk.Q[l]).reshape(P, sh.G, D)
+    ring_k = np.zeros((P, sh.k_tot, BLK, D), np.uint16)
+    ring_v = np.zeros_like(ring_k)
+
+    def layer():
+        idx, cnt, _ = oracle.select(F, ktil, lens, sh.n_init, sh.n_local, sh.k)
+        oracle.gather(Kh, idx, cnt, ring_k)
+        oracle.gather(Vh, idx, cnt, ring_v)
+        # the same rows as the ring holds (a staged copy), read where the length mask is defined
+        oracle.attn(Q, Kh, Vh, idx, cnt, lens)
+    return oracle_baseline(layer, budget_s, 1.0 / sh.layers, "steps/s",
+                           f"one layer of all {P} pairs (select + staging copy of K and V + attention) in fp64, "
+                           f"scaled to {sh.layers} layers")
 
 
 NSA_WINDOW_TOKENS = 512
@@ -1199,15 +1403,16 @@ def run_nsa_case(args, dev):
 
     select()
     torch.cuda.synchronize()
-    t_attn = _event_times(attend, args.steps, args.warmup, evict)
-    t_grid = _event_times(attend_grid, args.steps, args.warmup, evict)
-    t_sel = _event_times(select, args.steps, args.warmup, evict)
-    t_route = _event_times(route, args.steps, args.warmup, evict)
-    t_layer = _event_times(layer, args.steps, args.warmup, evict)
-    t_route_w = _event_times(route_w, args.steps, args.warmup, evict)
-    t_attn_w = _event_times(attend_w, args.steps, args.warmup, evict)
-    t_layer_w = _event_times(layer_w, args.steps, args.warmup, evict)
-    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as clk:
+        t_attn = _event_times(attend, args.steps, args.warmup, evict)
+        t_grid = _event_times(attend_grid, args.steps, args.warmup, evict)
+        t_sel = _event_times(select, args.steps, args.warmup, evict)
+        t_route = _event_times(route, args.steps, args.warmup, evict)
+        t_layer = _event_times(layer, args.steps, args.warmup, evict)
+        t_route_w = _event_times(route_w, args.steps, args.warmup, evict)
+        t_attn_w = _event_times(attend_w, args.steps, args.warmup, evict)
+        t_layer_w = _event_times(layer_w, args.steps, args.warmup, evict)
+        torch.cuda.synchronize()
     assert status.item() == 0, f"device status {status.item()}"
     pairs = B * H_kv
     w_blocks = (w + BLK - 1) // BLK
@@ -1249,7 +1454,30 @@ def run_nsa_case(args, dev):
                               "frac_of_measured_hbm": awfrac},
                 "layer": {**t_layer_w, "achieved_gbs": lwgbs, "frac_of_measured_hbm": lwfrac,
                           "layers_per_s": round(1e6 / t_layer_w["median_us"], 1)}},
-            "peak_gbs": peak, "peak_source": src, "l2": "512 MB read evicts L2 before each timed call"}
+            "peak_gbs": peak, "peak_source": src, "l2": "512 MB read evicts L2 before each timed call",
+            "roofline": case_roofline("nsa_fused_kernel (sparse_decode_attn_nsa, block rows, G = 8)", attn_bytes,
+                                      t_attn["median_us"], peak, src),
+            "clocks": clk.summary()}
+    if not args.no_cpu_baseline:
+        import oracle
+        G = H_q // H_kv
+        lens = [T] * H_kv
+        Kb = wl.bf16_bits(kc[0]).reshape(H_kv, T, D)
+        Vb = wl.bf16_bits(vc[0]).reshape(H_kv, T, D)
+        kh64 = khat[0].float().double().cpu().numpy()
+        vh64 = vhat[0].float().double().cpu().numpy()
+        Qb = wl.bf16_bits(Q[0]).reshape(H_kv, G, D)
+        gt = gates[0].double().cpu().numpy().reshape(H_kv, G, 3)
+
+        def nsa_layer():
+            ridx, rcnt, _ = oracle.select_windows(Qb, kh64, lens, BLK, BLK, sh.n_init, sh.n_local, sh.k, k_tot)
+            oracle.nsa(Qb, Kb, Vb, kh64, vh64, ridx, rcnt, lens, w, gt)
+        line["cpu_baseline"] = oracle_baseline(
+            nsa_layer, args.case_cpu_seconds, 1.0 / B, "layers/s",
+            f"batch element 0 ({H_kv} pairs) of one layer with block rows: the routing (per-head softmax over "
+            f"the rows, summed, top-k) and the gated three-branch attention in fp64, scaled to {B} batch elements")
+    else:
+        line["cpu_baseline"] = None
     print(json.dumps(line), flush=True)
 
 
@@ -1273,8 +1501,9 @@ def run_prefill_case(args, dev):
     def run():
         binding.sparse_prefill_select(x["F"], x["ktil"], seq, sh.n_init, sh.n_local, sh.k, idx, cnt, status=status)
 
-    t = _event_times(run, args.steps, args.warmup, evict)
-    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as clk:
+        t = _event_times(run, args.steps, args.warmup, evict)
+        torch.cuda.synchronize()
     assert status.item() == 0, f"device status {status.item()}"
     pairs = B * H_kv
     # scores: position t scores the candidates of the blocks it sees (causal)
@@ -1291,7 +1520,24 @@ def run_prefill_case(args, dev):
                                  "(fp32 keys split into three bf16 terms)",
             "algorithmic_bytes": nbytes, "achieved_gbs": round(nbytes / sec / 1e9, 1),
             "frac_of_measured_hbm": round(nbytes / sec / 1e9 / peak, 4), "peak_gbs": peak, "peak_source": src,
-            "l2": "512 MB read evicts L2 before each launch"}
+            "l2": "512 MB read evicts L2 before each launch",
+            "roofline": case_roofline("prefill_select_kernel (sparse_prefill_select)", nbytes, t["median_us"], peak,
+                                      src, note="the kernel is instruction-bound by the per-position top-k "
+                                                "(ncu: issue active ~60 %), not by its bytes"),
+            "clocks": clk.summary()}
+    if not args.no_cpu_baseline:
+        import oracle
+        n_p, stride = 16, 16                 # 16 pairs (one thread each), every 16th position
+        Fb = wl.bf16_bits(x["F"]).reshape(pairs, T, D)[:n_p]
+        kt = x["ktil"].reshape(pairs, N, D)[:n_p].double().cpu().numpy()
+        rows = list(range(stride - 1, T, stride))
+        line["cpu_baseline"] = oracle_baseline(
+            lambda: oracle.prefill_select(Fb, kt, [T] * n_p, sh.n_init, sh.n_local, sh.k, rows=rows),
+            args.case_cpu_seconds, n_p * len(rows), "positions/s",
+            f"{n_p} pairs x {len(rows)} positions (every {stride}th, spanning the causal range) of the selection "
+            "in fp64; value = positions per second")
+    else:
+        line["cpu_baseline"] = None
     print(json.dumps(line), flush=True)
 
 
@@ -1358,6 +1604,7 @@ def run_refresh_case(args, dev):
         torch.cuda.synchronize(dev)
         return a.elapsed_time(b) * 1e3 / reps
 
+    clk = ClockSampler(dev.index or 0).__enter__()
     t_all = timed(lambda l: True)
     t_none = timed(lambda l: l == 0)
     out = {"case": "refresh64k", "workload": sh.name + "_32layers",
@@ -1371,8 +1618,48 @@ def run_refresh_case(args, dev):
         out[f"refresh_every_{r}"] = {"round_us": round(t_r, 1), "rounds_per_s": round(1e6 / t_r, 1),
                                      "speedup_vs_all_refresh": round(t_all / t_r, 3)}
     torch.cuda.synchronize()
+    clk.__exit__(None, None, None)
     assert status.item() == 0, f"device status {status.item()}"
+    # the bytes of one layer over the last routed lists: the merged unions it loads, plus
+    # (refresh) the bf16 block rows the routing reads
+    loaded = torch.zeros(1, dtype=torch.int64, device=dev)
+    binding.sparse_verify_attn_grouped(x["Q"], Ks[0], Vs[0], idx, sh.C, sh.window_blocks, x["seq_len"], O,
+                                       blocks_loaded=loaded, status=status)
+    torch.cuda.synchronize()
+    reuse_bytes = int(loaded.item()) * KV_BLOCK_BYTES
+    route_bytes = B * H_kv * N * D * 2
+    peak, src = measured_peaks()
+    out["roofline"] = case_roofline("a refresh layer: nsa_route_kernel + sparse_attn_kernel<2, true>, chained",
+                                    reuse_bytes + route_bytes, out["refresh_layer_us"], peak, src,
+                                    note="per layer of the all-refresh round; bytes = the routed lists' merged "
+                                         "unions (blocks_loaded x 32 KB) + the block rows routed over")
+    out["clocks"] = clk.summary()
+    if not args.no_cpu_baseline:
+        import numpy as np
+        import oracle
+        G = sh.G
+        Qb, Kb, Vb = wl.bf16_bits(x["Q"]), wl.bf16_bits(Ks[0]), wl.bf16_bits(Vs[0])
+        kh64 = khs[0].float().double().cpu().numpy().reshape(B * H_kv, N, D)
+        lens_p = [T] * (B * H_kv)
+        Qq = [np.ascontiguousarray(Qb[:, q].reshape(B * H_kv, G, D)) for q in range(sh.N_q)]
+
+        def refresh_layer():
+            I = np.empty((B * H_kv, sh.N_q, k_tot), np.int32)
+            for q in range(sh.N_q):
+                I[:, q], _, _ = oracle.select_windows(Qq[q], kh64, lens_p, BLK, BLK, 0, sh.window_blocks, sh.n_sel,
+                                                      k_tot)
+            oracle.verify(Qb, Kb, Vb, I.reshape(B, H_kv, sh.N_q, k_tot), sh.C, sh.window_blocks, [T] * B)
+        out["cpu_baseline"] = oracle_baseline(
+            refresh_layer, args.case_cpu_seconds, 1.0 / layers, "rounds/s",
+            f"one refresh layer ({sh.N_q} queries x {B * H_kv} pairs routed over the block rows, then verified, "
+            f"mode A) in fp64, scaled to an all-refresh round of {layers} layers")
+    else:
+        out["cpu_baseline"] = None
     print(json.dumps(out), flush=True)
+
+
+OTHER_CASES = ("decode128k_b1", "single4k", "append32k", "verify64k", "offload128k", "nsa128k", "prefill32k",
+               "refresh64k")
 
 
 def run_other_case(args, local_rank):
@@ -1406,14 +1693,15 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["step", "layer", "select", "single4k", "append32k", "verify64k",
-                                       "offload128k", "nsa128k", "prefill32k", "refresh64k"], default="step",
+    ap.add_argument("--case", choices=["step", "layer", "select"] + list(OTHER_CASES), default="step",
                     help="step: the 80-layer decode step (the bench line); layer: one physical layer, "
                          "kernels serialised and timed alone (for profiling); select: selection only; "
+                         "decode128k_b1: the 128K step at B = 1 with all 80 layers resident; "
                          "single4k / append32k / verify64k / offload128k / nsa128k / prefill32k / refresh64k: "
-                         "the other "
-                         "workloads, "
-                         "one line each")
+                         "the other workloads, one line each")
+    ap.add_argument("--case-cpu-seconds", type=float, default=3.0,
+                    help="other cases: host seconds of oracle work for their cpu_baseline")
+    ap.add_argument("--layers", type=int, default=0, help="offload128k: layers (default 32; fewer for profiling)")
     ap.add_argument("--n-split", type=int, default=0)
     ap.add_argument("--no-workspace", action="store_true", help="layer case: attention without a workspace (cluster path)")
     ap.add_argument("--workspace", action="store_true",
@@ -1429,7 +1717,9 @@ def main():
     rank, world, local_rank = dist_env()
     if args.case in ("layer", "select"):
         run_layer_case(args, local_rank)
-    elif args.case in ("single4k", "append32k", "verify64k", "offload128k", "nsa128k", "prefill32k", "refresh64k"):
+    elif args.case == "decode128k_b1":
+        run_b1_case(args, local_rank)
+    elif args.case in OTHER_CASES:
         run_other_case(args, local_rank)
     elif args.impl == "reference":
         run_reference(args, rank, world, local_rank)

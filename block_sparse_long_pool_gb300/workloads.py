@@ -17,7 +17,8 @@ Recipe (every tensor is seeded; bf16 values are N(0, 1) draws rounded once):
   (logical l uses physical l mod 10); each physical layer q has its own direction
   u_q per pair and 64 planted blocks, 38 of them (60 %) shared with physical q-1.
   F_l = u_{(l+1) mod 10} + 0.25 * noise (the Forecast of layer l targets layer l+1,
-  SparDA notes eq.(6)); F^cur_0 = u_0 + 0.25 * noise (SparDA notes §4.6).
+  SparDA notes eq.(6)); F^cur_0 = u_0 + 0.25 * noise (SparDA notes §4.6).  The B = 1
+  variant keeps all 80 layers resident (80 physical layers, same recipe).
 * Grouped verification (SSV notes, mechanism 1): per (batch, KV head, group of C
   queries) a core of round(gamma * n_sel) blocks shared by every query of the group
   plus n_sel - core private blocks per query, all distinct and drawn without
@@ -155,6 +156,11 @@ LLAMA8B_32K = DecodeShape("llama8b_32k_b8_append", B=8, H_q=32, H_kv=8, T=32768,
 DECODE_128K = DecodeShape("decode_128k_70b_b8_80layers", B=8, H_q=64, H_kv=8, T=131072,
                           n_init=1, n_local=2, k=64, n_planted=64, layers=80, phys_layers=10,
                           shared_planted=38, seed=1237)
+# The same 70B-shaped 128K decode at B = 1 with all 80 layers resident (80 x 537 MB =
+# 42.9 GB, the footprint the SparDA notes print in eq.(2)): 8 pairs per layer.
+DECODE_128K_B1 = DecodeShape("decode_128k_70b_b1_80layers_resident", B=1, H_q=64, H_kv=8, T=131072,
+                             n_init=1, n_local=2, k=64, n_planted=64, layers=80, phys_layers=80,
+                             shared_planted=38, seed=1241)
 VERIFY_64K = VerifyShape("ssv_verify_64k_b4_c4", B=4, H_q=32, H_kv=8, T=65536, N_q=8, n_sel=16,
                          gamma=0.75, window_tokens=512, C=4, seed=1238)
 OFFLOAD_128K = OffloadShape("offload_128k_b4_32layers", B=4, H_q=32, H_kv=8, T=131072, layers=32,
