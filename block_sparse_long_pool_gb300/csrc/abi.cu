@@ -22,6 +22,25 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 cudaError_t g_encode_err = cudaSuccess;
 
+// cuCtxGetCurrent / cuCtxGetId, for keying per-context caches (a context's id is unique
+// for the life of the process, unlike its handle or the device ordinal).
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+void load_ctx_queries()
+{
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+}
+
 void load_encoder()
 {
     cudaDriverEntryPointQueryResult q;
@@ -72,6 +91,31 @@ int device_info(DeviceInfo *out)
         g_info_valid[dev] = true;
     }
     *out = g_info[dev];
+    return SPARSE_OK;
+}
+
+int current_context_id(unsigned long long *id)
+{
+    std::call_once(g_ctx_once, load_ctx_queries);
+    if (g_ctx_current == nullptr || g_ctx_id == nullptr)
+        return fail(SPARSE_ERR_CUDA, "cuCtxGetCurrent / cuCtxGetId unavailable");
+    CUcontext ctx = nullptr;
+    CUresult r = g_ctx_current(&ctx);
+    if (r == CUDA_SUCCESS && ctx == nullptr) {
+        // no context current on this host thread yet: the runtime makes the device's
+        // primary context current (a no-op call that initialises it), then look again
+        const cudaError_t e = cudaFree(nullptr);
+        if (e != cudaSuccess)
+            return cuda_status(e, "making the primary context current");
+        r = g_ctx_current(&ctx);
+    }
+    if (r != CUDA_SUCCESS || ctx == nullptr)
+        return fail(SPARSE_ERR_CUDA, "cuCtxGetCurrent failed (CUresult %d)", static_cast<int>(r));
+    unsigned long long v = 0;
+    r = g_ctx_id(ctx, &v);
+    if (r != CUDA_SUCCESS)
+        return fail(SPARSE_ERR_CUDA, "cuCtxGetId failed (CUresult %d)", static_cast<int>(r));
+    *id = v;
     return SPARSE_OK;
 }
 

@@ -491,7 +491,12 @@ __device__ __forceinline__ int producer_fetch_slice(const AttnParams &p, int pai
 //     free; a peer merges its warps' states and copies its CTA state into the leader's
 //     slot (16-byte distributed-shared-memory stores), arrives on the leader's barrier
 //     and leaves; the leader merges the S states for every output dim.  No cluster-wide
-//     barrier: the peers do not wait for one another, nor for the leader's output.
+//     wait on the normal path: the peers do not wait for one another, nor for the
+//     leader's output.  Every thread arrives (relaxed) on the cluster barrier as it
+//     leaves; a warp whose bounded wait ran out waits there too before leaving, so it
+//     stays resident until every CTA of the cluster is past its merge and none can
+//     still reach its shared memory (a late arrive from the leader, late stores from a
+//     peer).
 //   pull: every CTA waits for all, then merges the S states for its slice of the dims
 //     by reading its peers' shared memory, and all wait again before leaving.
 constexpr int kPushRecvOff = 48 * 1024;   // the leader's slots: past the warp and CTA states
@@ -590,6 +595,8 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
             if (!go) {
                 if (lane == 0)
                     report(p.status, SPARSE_ERR_TIMEOUT);
+                cluster_arrive_relaxed();
+                cluster_wait();   // the leader may still arrive on this CTA's barrier
                 return;
             }
             const uint32_t dst = dsmem_addr(smem_u32(base + kPushRecvOff) + (rank - 1) * SLOT * 4, 0);
@@ -599,19 +606,24 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
             __syncwarp();
             if (lane == 0)
                 mbar_arrive_cluster(dsmem_addr(bar_recv, 0));
+            cluster_arrive_relaxed();
             return;
         }
         // the leader: the S states, own first, then the slots in rank order
         if (!__all_sync(0xffffffffu, mbar_wait_cluster(bar_recv, 0, kWaitNs))) {
             if (lane == 0)
                 report(p.status, SPARSE_ERR_TIMEOUT);
+            cluster_arrive_relaxed();
+            cluster_wait();   // late peers may still store into this CTA's slots
             return;
         }
         int any_abort = cabort[0];
         for (uint32_t c = 1; c < S; ++c)
             any_abort |= reinterpret_cast<const int *>(slots + (c - 1) * SLOT + ROWS * kD + 2 * ROWS)[0];
-        if (any_abort)
+        if (any_abort) {
+            cluster_arrive_relaxed();
             return;
+        }
         // four adjacent dims per item (the slots are 16-byte aligned: SLOT % 4 == 0)
         const int n_items = rows_valid * (kD / 4);
         for (int item = tid; item < n_items; item += nthreads) {
@@ -649,6 +661,7 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
             }
             merge_write_item4<NT, VERIFY>(p, b, g, q0, row, d, M, L, o, true);
         }
+        cluster_arrive_relaxed();
         return;
     }
     cluster_sync();

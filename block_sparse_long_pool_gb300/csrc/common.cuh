@@ -306,6 +306,14 @@ __device__ __forceinline__ void cluster_arrive()
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
+// Arrive without ordering this thread's earlier memory accesses (the barrier is used
+// only to know when every thread of the cluster has got past a point).
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_wait()
 {
     __syncwarp();
@@ -390,6 +398,10 @@ struct DeviceInfo {
 
 // Current device's properties (cached per device).
 int device_info(DeviceInfo *out);
+
+// Unique id of the current CUDA context (the device's primary context, made current if
+// needed): keys caches of device addresses that a context reset would invalidate.
+int current_context_id(unsigned long long *id);
 
 // 3-D tiled tensor map over [pairs][rows][128] bf16 with a 64 x 64 box and 128-byte
 // swizzle (the layout the attention kernel reads).  Returns SPARSE_OK or an error.

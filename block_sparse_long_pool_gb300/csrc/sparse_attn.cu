@@ -1087,11 +1087,11 @@ static_assert((3 * kConsumerWarps * 16 + kConsumerWarps * 16 * kWoStride + 16 * 
                   kStages * kStageBytes,
               "merge scratch exceeds the stage ring");
 
-int decode_impl(const uint16_t *Q, const uint16_t *k_base, const uint16_t *v_base, long long pair_stride,
-                const int *blk_slot, const int *blk_logical, const int *count, int k_tot, const int *seq_len,
-                int B, int H_q, int H_kv, float scale, uint16_t *O, float *lse, int n_split, unsigned flags,
-                void *workspace, size_t workspace_bytes, const unsigned *ready_flag, unsigned ready_target,
-                long long timeout_ns, int *status, void *stream)
+// The host-side checks of sparse_decode_attn's arguments that do not depend on the
+// path (cluster, split or stream-K); SPARSE_OK or the error, before anything is launched.
+int decode_check(const uint16_t *Q, const uint16_t *k_base, const uint16_t *v_base, long long pair_stride,
+                 const int *blk_logical, const int *count, int k_tot, const int *seq_len, int B, int H_q, int H_kv,
+                 float scale, const uint16_t *O, int n_split, unsigned flags, long long timeout_ns)
 {
     using sp_host::aligned16;
     using sp_host::fail;
@@ -1108,20 +1108,36 @@ int decode_impl(const uint16_t *Q, const uint16_t *k_base, const uint16_t *v_bas
         return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn: scale must be finite");
     if (timeout_ns < 0)
         return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn_ex: timeout_ns < 0");
-    const int G = H_q / H_kv;
-    if (G > 16)
-        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn: G=%d > 16 query heads per KV head", G);
-    const long long pairs = static_cast<long long>(B) * H_kv;
-    if (pairs > 65535)
-        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn: B*H_kv=%lld > 65535", pairs);
-    sp_host::DeviceInfo dev;
-    int rc = sp_host::device_info(&dev);
-    if (rc != SPARSE_OK)
-        return rc;
+    if (H_q / H_kv > 16)
+        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn: G=%d > 16 query heads per KV head", H_q / H_kv);
+    if (static_cast<long long>(B) * H_kv > 65535)
+        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn: B*H_kv=%lld > 65535",
+                    static_cast<long long>(B) * H_kv);
     if ((flags & ~(SPARSE_ATTN_BLOCKS_READY | SPARSE_ATTN_STREAM_K)) != 0u)
         return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn: unknown flags 0x%x", flags);
     if (n_split < 0)
         return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn: n_split < 0");
+    return SPARSE_OK;
+}
+
+int decode_impl(const uint16_t *Q, const uint16_t *k_base, const uint16_t *v_base, long long pair_stride,
+                const int *blk_slot, const int *blk_logical, const int *count, int k_tot, const int *seq_len,
+                int B, int H_q, int H_kv, float scale, uint16_t *O, float *lse, int n_split, unsigned flags,
+                void *workspace, size_t workspace_bytes, const unsigned *ready_flag, unsigned ready_target,
+                long long timeout_ns, int *status, void *stream)
+{
+    using sp_host::aligned16;
+    using sp_host::fail;
+    int rc = decode_check(Q, k_base, v_base, pair_stride, blk_logical, count, k_tot, seq_len, B, H_q, H_kv, scale,
+                          O, n_split, flags, timeout_ns);
+    if (rc != SPARSE_OK)
+        return rc;
+    const int G = H_q / H_kv;
+    const long long pairs = static_cast<long long>(B) * H_kv;
+    sp_host::DeviceInfo dev;
+    rc = sp_host::device_info(&dev);
+    if (rc != SPARSE_OK)
+        return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     AttnParams p = {};
     p.Q = Q;
@@ -1248,25 +1264,38 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratch
 
 namespace {
 
+// The device address of g_noalloc_scratch in the current context (the host-side name of
+// the array is only a stand-in, never a device address).  Looked up once per context:
+// a context that is destroyed and created again (cudaDeviceReset) loads the module
+// anew, so the cache is keyed on the context's unique id, not on the device ordinal.
+constexpr int kNoallocCacheSlots = 64;
 std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[64];   // device address of the array, per device
+unsigned long long g_noalloc_ctx[kNoallocCacheSlots];   // 0 = empty (context ids are nonzero)
+void *g_noalloc_ptr[kNoallocCacheSlots];
+int g_noalloc_next;
 
-// The device address of g_noalloc_scratch on the current device (the host-side name of
-// the array is only a stand-in, never a device address).  Looked up once per device.
-int noalloc_scratch(int device, void **ptr)
+int noalloc_scratch(void **ptr)
 {
-    if (device < 0 || device >= 64)
-        return sp_host::fail(SPARSE_ERR_UNSUPPORTED, "device ordinal %d out of range", device);
+    unsigned long long ctx = 0;
+    int rc = sp_host::current_context_id(&ctx);
+    if (rc != SPARSE_OK)
+        return rc;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (g_noalloc_ptr[device] == nullptr) {
-        void *addr = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
-        if (e != cudaSuccess || addr == nullptr)
-            return sp_host::cuda_status(e != cudaSuccess ? e : cudaErrorInvalidSymbol,
-                                        "sparse_decode_attn_noalloc: cudaGetSymbolAddress");
-        g_noalloc_ptr[device] = addr;
-    }
-    *ptr = g_noalloc_ptr[device];
+    for (int i = 0; i < kNoallocCacheSlots; ++i)
+        if (g_noalloc_ctx[i] == ctx && ctx != 0) {
+            *ptr = g_noalloc_ptr[i];
+            return SPARSE_OK;
+        }
+    void *addr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+    if (e != cudaSuccess || addr == nullptr)
+        return sp_host::cuda_status(e != cudaSuccess ? e : cudaErrorInvalidSymbol,
+                                    "sparse_decode_attn_noalloc: cudaGetSymbolAddress");
+    const int slot = g_noalloc_next;
+    g_noalloc_next = (g_noalloc_next + 1) % kNoallocCacheSlots;
+    g_noalloc_ctx[slot] = ctx;
+    g_noalloc_ptr[slot] = addr;
+    *ptr = addr;
     return SPARSE_OK;
 }
 
@@ -1280,16 +1309,21 @@ extern "C" SPARSE_API int sparse_decode_attn_noalloc(const uint16_t *Q, const ui
                                                      unsigned flags, int *status, void *stream)
 {
     using sp_host::fail;
-    if (B < 1 || H_kv < 1 || H_q < H_kv || H_q % H_kv != 0 || k_tot < 1 || n_split < 0)
-        return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn_noalloc: bad size");
+    // every argument check first: a rejected call leaves the shared array untouched
+    int rc = decode_check(Q, k_base, v_base, pair_stride_tokens, blk_logical, count, k_tot, seq_len, B, H_q, H_kv,
+                          scale, O, n_split, flags, 0);
+    if (rc != SPARSE_OK)
+        return rc;
     if (H_q / H_kv > 8)
         return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn_noalloc: G=%d > 8", H_q / H_kv);
     sp_host::DeviceInfo dev;
-    int rc = sp_host::device_info(&dev);
-    if (rc != SPARSE_OK)
+    if ((rc = sp_host::device_info(&dev)) != SPARSE_OK)
         return rc;
     const long long pairs = static_cast<long long>(B) * H_kv;
-    const int n_ctas = streamk_ctas(pairs * k_tot, pairs, n_split, dev.sm_count);
+    const long long n_items = pairs * k_tot;
+    const int n_ctas = streamk_ctas(n_items, pairs, n_split, dev.sm_count);
+    if ((n_items + n_ctas - 1) / n_ctas > kMaxListCta)
+        return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn_noalloc: too many blocks per CTA");
     const size_t need = streamk_workspace_bytes(pairs, H_q / H_kv, n_ctas);
     if (need > kNoallocScratchBytes)
         return fail(SPARSE_ERR_UNSUPPORTED,
@@ -1297,7 +1331,7 @@ extern "C" SPARSE_API int sparse_decode_attn_noalloc(const uint16_t *Q, const ui
                     "(use sparse_decode_attn with a workspace)",
                     need, kNoallocScratchBytes);
     void *scratch = nullptr;
-    if ((rc = noalloc_scratch(dev.device, &scratch)) != SPARSE_OK)
+    if ((rc = noalloc_scratch(&scratch)) != SPARSE_OK)
         return rc;
     // the per-pair arrival counters must start at zero: clear them on the call's stream
     const size_t counters = (static_cast<size_t>(pairs) * sizeof(int) + 255) & ~static_cast<size_t>(255);

@@ -258,11 +258,14 @@ SPARSE_API size_t sparse_decode_attn_workspace_size(int B, int H_q, int H_kv, in
  * rejected with SPARSE_ERR_UNSUPPORTED before any launch (B*H_kv = 64 pairs at
  * k_tot = 67 need about 2.6 MB).  The call allocates nothing: no cudaMalloc or
  * cudaFree, no allocating library routine.
- * The first call on a device looks up the array's device address (once per device,
- * with that device current); make that first call before any stream capture.  Each
- * call first clears the array's per-pair counters on its stream.  All calls share the
- * one array, so calls that overlap on the GPU (other streams, other threads) race:
- * order them on one stream.
+ * The first call in a CUDA context looks up the array's device address (once per
+ * context, with the context's device current; a context created again after
+ * cudaDeviceReset holds a new copy of the array and is looked up anew); make that
+ * first call before any stream capture.  Every argument is checked before anything
+ * is queued: a rejected call leaves the array untouched.  Each accepted call first
+ * clears the array's per-pair counters on its stream.  All calls share the one array,
+ * so calls that overlap on the GPU (other streams, other threads) race: order them on
+ * one stream.
  */
 SPARSE_API int sparse_decode_attn_noalloc(const uint16_t *Q, const uint16_t *k_base,
                                           const uint16_t *v_base, long long pair_stride_tokens,
