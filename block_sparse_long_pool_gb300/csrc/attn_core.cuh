@@ -93,6 +93,7 @@ struct AttnParams {
     int n_local;
     int k_sel;
     int k_tot_next;
+    int sel_block;         // 1: CTA 0's consumer warps and selector warp take the top-k together
     // NSA branches: fp32 output instead of bf16 O, and a block range computed from
     // seq_len instead of a block table (1: the window of the last win_tokens tokens,
     // masked token-granularly; 2: the compressed rows, one per 64-token block holding
@@ -555,7 +556,7 @@ __device__ __forceinline__ void merge_write_item4(const AttnParams &p, int b, in
         p.lse[static_cast<size_t>(b) * p.H_q + g * p.G + row] = lse_of(M, L);
 }
 
-template <int NT, bool VERIFY>
+template <int NT, bool VERIFY, int MAXS = kMaxSplit>
 __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uint8_t *base, bool aborted,
                                                     const AttnParams &p, int b, int g, int q0, int rows_valid,
                                                     uint32_t rank, uint32_t S, int nthreads, uint32_t ctrl_s,
@@ -629,10 +630,10 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
         for (int item = tid; item < n_items; item += nthreads) {
             const int row = item / (kD / 4);
             const int d = 4 * (item - row * (kD / 4));
-            float mc[kMaxSplit], lc[kMaxSplit];
-            float4 v[kMaxSplit];
+            float mc[MAXS], lc[MAXS];
+            float4 v[MAXS];
 #pragma unroll
-            for (int c = 0; c < kMaxSplit; ++c) {
+            for (int c = 0; c < MAXS; ++c) {
                 if (c < static_cast<int>(S)) {
                     const float *src = c == 0 ? co : slots + (c - 1) * SLOT;
                     mc[c] = src[ROWS * kD + row];
@@ -646,12 +647,12 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
             }
             float M = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < kMaxSplit; ++c)
+            for (int c = 0; c < MAXS; ++c)
                 M = fmaxf(M, mc[c]);
             float L = 0.f;
             float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < kMaxSplit; ++c) {
+            for (int c = 0; c < MAXS; ++c) {
                 const float f = (M == -INFINITY || mc[c] == -INFINITY) ? 0.f : exp2f(mc[c] - M);
                 L = fmaf(lc[c], f, L);
                 o.x = fmaf(f, v[c].x, o.x);
@@ -670,12 +671,12 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
     // a thread needs for an output pair is loaded before any is used, so the remote
     // loads of an item overlap (one round trip).
     const int Si = static_cast<int>(S);
-    const float *pco[kMaxSplit];
-    const float *pcm[kMaxSplit];
-    const float *pcl[kMaxSplit];
-    int ab[kMaxSplit];
+    const float *pco[MAXS];
+    const float *pcm[MAXS];
+    const float *pcl[MAXS];
+    int ab[MAXS];
 #pragma unroll
-    for (int c = 0; c < kMaxSplit; ++c) {
+    for (int c = 0; c < MAXS; ++c) {
         const unsigned r = c < Si ? static_cast<unsigned>(c) : 0u;
         pco[c] = static_cast<const float *>(__cluster_map_shared_rank(co, r));
         pcm[c] = static_cast<const float *>(__cluster_map_shared_rank(cm, r));
@@ -692,10 +693,10 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
     for (int item = tid; item < n_items; item += nthreads) {
         const int row = item / quads_per_row;
         const int d = d0 + 4 * (item - row * quads_per_row);
-        float mc[kMaxSplit], lc[kMaxSplit];
-        float4 v[kMaxSplit];
+        float mc[MAXS], lc[MAXS];
+        float4 v[MAXS];
 #pragma unroll
-        for (int c = 0; c < kMaxSplit; ++c) {
+        for (int c = 0; c < MAXS; ++c) {
             if (c < Si) {
                 mc[c] = pcm[c][row];
                 lc[c] = pcl[c][row];
@@ -708,19 +709,19 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
         }
         int any_abort = 0;
 #pragma unroll
-        for (int c = 0; c < kMaxSplit; ++c)
+        for (int c = 0; c < MAXS; ++c)
             any_abort |= ab[c];
         // any CTA of the unit that failed its ready check leaves the output untouched
         if (any_abort)
             break;
         float M = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kMaxSplit; ++c)
+        for (int c = 0; c < MAXS; ++c)
             M = fmaxf(M, mc[c]);
         float L = 0.f;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < kMaxSplit; ++c) {
+        for (int c = 0; c < MAXS; ++c) {
             const float f = (M == -INFINITY || mc[c] == -INFINITY) ? 0.f : exp2f(mc[c] - M);
             L = fmaf(lc[c], f, L);
             o.x = fmaf(f, v[c].x, o.x);
@@ -737,18 +738,20 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
 // ---------------------------------------------------------------- host helpers
 
 // Cluster size S (CTAs sharing one unit's list) for the cluster kernels: auto = enough
-// units x S to cover the SMs twice, at least two blocks per CTA.
-inline int choose_split(int n_split, long long units, int max_list, int sm_count, int *S)
+// units x S to cover the SMs twice, at least two blocks per CTA; at most max_s (8, the
+// portable cluster size, or 16 for a kernel that allows the non-portable size).
+inline int choose_split(int n_split, long long units, int max_list, int sm_count, int *S, int max_s = kMaxSplit)
 {
     if (n_split == 0) {
         int s = 1;
-        while (s < kMaxSplit && units * s * 2 <= 2LL * sm_count && s * 2 <= (max_list > 1 ? max_list / 2 : 1))
+        while (s < max_s && units * s * 2 <= 2LL * sm_count && s * 2 <= (max_list > 1 ? max_list / 2 : 1))
             s *= 2;
         *S = s;
         return SPARSE_OK;
     }
-    if (n_split != 1 && n_split != 2 && n_split != 4 && n_split != 8)
-        return sp_host::fail(SPARSE_ERR_INVALID_ARG, "n_split must be 0, 1, 2, 4 or 8 (got %d)", n_split);
+    if (n_split != 1 && n_split != 2 && n_split != 4 && n_split != 8 && !(n_split == 16 && max_s >= 16))
+        return sp_host::fail(SPARSE_ERR_INVALID_ARG, "n_split must be 0, 1, 2, 4 or 8%s (got %d)",
+                             max_s >= 16 ? " or 16" : "", n_split);
     *S = n_split;
     return SPARSE_OK;
 }

@@ -35,6 +35,8 @@
 //     CTA 0 writes O; no cluster-wide barrier at the end of the layer.
 #include <string.h>
 
+#include <mutex>
+
 #include "attn_core.cuh"
 #include "select_core.cuh"
 #include "select_layout.cuh"
@@ -43,7 +45,8 @@ namespace {
 
 // ATTN = false: the Forecast selection alone (sparse_select_topk): no block list, no
 // attention, no merge; every input may be written by the kernel before this one.
-template <int NT, bool ATTN>
+// MAXS: the largest cluster the launch may use (16 for the non-portable size).
+template <int NT, bool ATTN, int MAXS>
 __global__ void __launch_bounds__(kFThreads, 2)
     decode_forecast_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                            const AttnParams p)
@@ -88,6 +91,10 @@ __global__ void __launch_bounds__(kFThreads, 2)
     const int nb = static_cast<int>(nb_ll);
     const bool take_all = max(0, nb - p.n_local - p.n_init) <= p.k_sel;
     const bool score = do_sel && !take_all;
+    // the top-k by CTA 0's consumer and selector warps together (else its selector warp
+    // alone, while the consumers attend)
+    const bool sel_group = rank == 0 && score && p.sel_block != 0 && p.k_sel >= 1 &&
+                           topk_cta_regs_fits<kSelKPT>(nb - p.n_local - p.n_init, kSelThreads);
     const int chunk = (nb + static_cast<int>(S) - 1) / static_cast<int>(S);
     const int r0 = score ? min(nb, static_cast<int>(rank) * chunk) : 0;
     const int n_krows = score ? min(nb, r0 + chunk) - r0 : 0;
@@ -263,6 +270,14 @@ __global__ void __launch_bounds__(kFThreads, 2)
         __syncwarp();
         if (lane == 0)
             mbar_arrive_cluster(dsmem_addr(bar_scored, 0));
+        if (sel_group) {
+            // CTA 0: once every CTA has scored its slice, the top-k with the selector warp
+            const bool ready = __all_sync(0xffffffffu, mbar_wait_cluster(bar_scored, 0, kWaitNs));
+            topk_forecast_cta<kSelKPT, kSelThreads / 32>(
+                base_s + fused_off_keys(per), base_s + fused_off_hist(), base_s + fused_off_hist(), nb, p.n_init,
+                p.n_local, p.k_sel, tid, kSelBar, ready, p.idx_next + static_cast<size_t>(pair) * p.k_tot_next,
+                p.k_tot_next, p.count_next + pair, p.status);
+        }
         // (2) this layer's attention over the staged slice of its block list
         if (ATTN)
             named_barrier_sync(1, kAttnThreads);
@@ -292,7 +307,13 @@ __global__ void __launch_bounds__(kFThreads, 2)
             bool ready = true;
             if (score)
                 ready = __all_sync(0xffffffffu, mbar_wait_cluster(bar_scored, 0, kWaitNs));
-            if (ready) {
+            if (sel_group) {
+                topk_forecast_cta<kSelKPT, kSelThreads / 32>(
+                    base_s + fused_off_keys(per), base_s + fused_off_hist(), base_s + fused_off_hist(), nb, p.n_init,
+                    p.n_local, p.k_sel, kConsumerWarps * 32 + lane, kSelBar, ready,
+                    p.idx_next + static_cast<size_t>(pair) * p.k_tot_next, p.k_tot_next, p.count_next + pair,
+                    p.status);
+            } else if (ready) {
                 topk_warp(base_s + fused_off_keys(per), base_s + fused_off_hist(), base_s + fused_off_topk_list(), nb,
                           p.n_init, p.n_local, p.k_sel,
                           p.idx_next + static_cast<size_t>(pair) * p.k_tot_next, p.k_tot_next, p.count_next + pair,
@@ -307,38 +328,103 @@ __global__ void __launch_bounds__(kFThreads, 2)
     // ---------------------------------------------------------------- merge
     if (ATTN) {
         __syncthreads();
-        cluster_merge_write<NT, false>(st, base, false, p, b, g, 0, p.G, rank, S, kFThreads, base_s + kOffCtrl,
-                                       false, true);
+        cluster_merge_write<NT, false, MAXS>(st, base, false, p, b, g, 0, p.G, rank, S, kFThreads,
+                                             base_s + kOffCtrl, false, true);
     }
 }
 
 // The "scored" barrier lives in the ctrl words, 8-byte aligned.
 static_assert((kOffCtrl + 4 * kCtrlScoredBar) % 8 == 0 && 4 * kCtrlScoredBar + 8 <= 64, "ctrl layout");
 
-template <int NT, bool ATTN>
-int launch_fused(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, int S, long long pairs,
-                 size_t smem, int device, cudaStream_t stream)
+// Blocks per CTA up to which the fused layer's CTA 0 takes its top-k with its consumer
+// warps before attending.
+constexpr int kSelBlockMaxPer = 12;
+
+template <int NT, bool ATTN, int MAXS>
+cudaError_t fused_config(cudaLaunchConfig_t *cfg, cudaLaunchAttribute (&attr)[2], int S, long long pairs, size_t smem,
+                         cudaStream_t stream)
 {
-    auto kern = decode_forecast_kernel<NT, ATTN>;
-    static int configured[64];
-    int rc = sp_host::configure_kernel(reinterpret_cast<const void *>(kern), static_cast<int>(smem), device,
-                                       configured);
-    if (rc != SPARSE_OK)
-        return rc;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(S), static_cast<unsigned>(pairs), 1);
-    cfg.blockDim = dim3(kFThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
+    *cfg = {};
+    cfg->gridDim = dim3(static_cast<unsigned>(S), static_cast<unsigned>(pairs), 1);
+    cfg->blockDim = dim3(kFThreads, 1, 1);
+    cfg->dynamicSmemBytes = smem;
+    cfg->stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(S);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg->attrs = attr;
+    cfg->numAttrs = 2;
+    return cudaSuccess;
+}
+
+// Configure the kernel for this device once (shared memory, carveout and, for MAXS > 8,
+// the non-portable cluster size).
+template <int NT, bool ATTN, int MAXS>
+int configure_fused(size_t smem, int device)
+{
+    auto kern = decode_forecast_kernel<NT, ATTN, MAXS>;
+    static int configured[64];
+    if (MAXS > kMaxSplit && device >= 0 && device < 64 && configured[device] < static_cast<int>(smem) + 1) {
+        const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(kern),
+                                                   cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess)
+            return sp_host::cuda_status(e, "cudaFuncSetAttribute(non-portable cluster size)");
+    }
+    return sp_host::configure_kernel(reinterpret_cast<const void *>(kern), static_cast<int>(smem), device,
+                                     configured);
+}
+
+// Whether clusters of 16 CTAs of the wide kernel fit on this device with this shared
+// memory (the occupancy query, remembered per device for the largest size that fit and
+// the smallest that did not).
+std::mutex g_wide_mu;
+size_t g_wide_fit[64], g_wide_nofit[64];
+
+template <int NT>
+bool wide_clusters_fit(size_t smem, long long pairs, int device, cudaStream_t stream)
+{
+    if (device < 0 || device >= 64)
+        return false;
+    {
+        std::lock_guard<std::mutex> lock(g_wide_mu);
+        if (smem <= g_wide_fit[device])
+            return true;
+        if (g_wide_nofit[device] != 0 && smem >= g_wide_nofit[device])
+            return false;
+    }
+    if (configure_fused<NT, true, 16>(smem, device) != SPARSE_OK)
+        return false;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    fused_config<NT, true, 16>(&cfg, attr, 16, pairs, smem, stream);
+    int n = 0;
+    const cudaError_t e =
+        cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void *>(decode_forecast_kernel<NT, true, 16>), &cfg);
+    if (e != cudaSuccess)
+        (void)cudaGetLastError();   // a failed query leaves a (non-sticky) error behind: clear it
+    const bool fit = e == cudaSuccess && n >= 1;
+    std::lock_guard<std::mutex> lock(g_wide_mu);
+    if (fit && smem > g_wide_fit[device])
+        g_wide_fit[device] = smem;
+    if (!fit && (g_wide_nofit[device] == 0 || smem < g_wide_nofit[device]))
+        g_wide_nofit[device] = smem;
+    return fit;
+}
+
+template <int NT, bool ATTN, int MAXS>
+int launch_fused(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, int S, long long pairs,
+                 size_t smem, int device, cudaStream_t stream)
+{
+    auto kern = decode_forecast_kernel<NT, ATTN, MAXS>;
+    int rc = configure_fused<NT, ATTN, MAXS>(smem, device);
+    if (rc != SPARSE_OK)
+        return rc;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    fused_config<NT, ATTN, MAXS>(&cfg, attr, S, pairs, smem, stream);
     CUtensorMap kmap = km, vmap = vm;
     AttnParams prm = p;
     void *args[] = {&kmap, &vmap, &prm};
@@ -394,9 +480,22 @@ extern "C" SPARSE_API int sparse_decode_attn_forecast(
     int rc = sp_host::device_info(&dev);
     if (rc != SPARSE_OK)
         return rc;
+    // up to 16 CTAs per pair (a non-portable cluster) when few pairs have to fill the GPU
     int S;
-    if ((rc = choose_split(n_split, pairs, k_tot, dev.sm_count, &S)) != SPARSE_OK)
+    if ((rc = choose_split(n_split, pairs, k_tot, dev.sm_count, &S, 16)) != SPARSE_OK)
         return rc;
+    if (S > kMaxSplit && G <= 8 &&
+        !wide_clusters_fit<1>(fused_smem_bytes((k_tot + S - 1) / S, N_cap), pairs, dev.device,
+                              static_cast<cudaStream_t>(stream))) {
+        if (n_split != 0)
+            return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn_forecast: clusters of 16 CTAs do not fit");
+        S = kMaxSplit;
+    }
+    if (S > kMaxSplit && G > 8) {
+        if (n_split != 0)
+            return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn_forecast: n_split = 16 needs G <= 8");
+        S = kMaxSplit;
+    }
     const int per = (k_tot + S - 1) / S;
     if (per > kMaxListCta)
         return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn_forecast: %d blocks per CTA (at most %d)", per,
@@ -430,14 +529,20 @@ extern "C" SPARSE_API int sparse_decode_attn_forecast(
     p.n_local = n_local;
     p.k_sel = k;
     p.k_tot_next = k_tot_next;
+    // few blocks per CTA: the layer's attention is short, so the top-k is on the path to
+    // the next layer and CTA 0's consumers help with it before they attend; many
+    // blocks: the selector warp alone, hidden behind the attention
+    p.sel_block = per <= kSelBlockMaxPer ? 1 : 0;
     CUtensorMap km, vm;
     if ((rc = sp_host::make_kv_tensor_map(&km, k_cache, T_cap, pairs)) != SPARSE_OK)
         return rc;
     if ((rc = sp_host::make_kv_tensor_map(&vm, v_cache, T_cap, pairs)) != SPARSE_OK)
         return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return G <= 8 ? launch_fused<1, true>(p, km, vm, S, pairs, smem, dev.device, st)
-                  : launch_fused<2, true>(p, km, vm, S, pairs, smem, dev.device, st);
+    if (S > kMaxSplit)
+        return launch_fused<1, true, 16>(p, km, vm, S, pairs, smem, dev.device, st);
+    return G <= 8 ? launch_fused<1, true, kMaxSplit>(p, km, vm, S, pairs, smem, dev.device, st)
+                  : launch_fused<2, true, kMaxSplit>(p, km, vm, S, pairs, smem, dev.device, st);
 }
 
 extern "C" SPARSE_API int sparse_select_topk(const uint16_t *F, const float *ktil, const int *seq_len, int B,
@@ -483,7 +588,9 @@ extern "C" SPARSE_API int sparse_select_topk(const uint16_t *F, const float *kti
     p.n_local = n_local;
     p.k_sel = k;
     p.k_tot_next = k_tot;
+    p.sel_block = 1;   // nothing else to do: every warp of CTA 0 takes part
     CUtensorMap unused;
     memset(&unused, 0, sizeof unused);
-    return launch_fused<1, false>(p, unused, unused, S, pairs, smem, dev.device, static_cast<cudaStream_t>(stream));
+    return launch_fused<1, false, kMaxSplit>(p, unused, unused, S, pairs, smem, dev.device,
+                                             static_cast<cudaStream_t>(stream));
 }

@@ -586,8 +586,9 @@ __device__ __forceinline__ int group_sum(int v, uint32_t buf_s, int t, int n_war
         sts_u32(buf_s + 4 * (t >> 5), static_cast<uint32_t>(v));
     named_barrier_sync(bar, n_warps * 32);
     int sum = 0;
-    for (int w = 0; w < n_warps; ++w)
-        sum += static_cast<int>(lds_u32(buf_s + 4 * w));
+#pragma unroll
+    for (int w = 0; w < 16; ++w)   // a fixed trip count: the loads issue together
+        sum += w < n_warps ? static_cast<int>(lds_u32(buf_s + 4 * w)) : 0;
     return sum;
 }
 
@@ -598,8 +599,9 @@ __device__ __forceinline__ uint32_t group_min(uint32_t v, uint32_t buf_s, int t,
         sts_u32(buf_s + 4 * (t >> 5), v);
     named_barrier_sync(bar, n_warps * 32);
     uint32_t m = 0xFFFFFFFFu;
-    for (int w = 0; w < n_warps; ++w)
-        m = min(m, lds_u32(buf_s + 4 * w));
+#pragma unroll
+    for (int w = 0; w < 16; ++w)
+        m = w < n_warps ? min(m, lds_u32(buf_s + 4 * w)) : m;
     return m;
 }
 
@@ -619,13 +621,80 @@ __device__ __forceinline__ int group_exclusive_scan(int v, uint32_t buf_s, int t
     named_barrier_sync(bar, n_warps * 32);
     int before = 0;
     total = 0;
-    for (int w = 0; w < n_warps; ++w) {
-        const int c = static_cast<int>(lds_u32(buf_s + 4 * w));
+#pragma unroll
+    for (int w = 0; w < 16; ++w) {
+        const int c = w < n_warps ? static_cast<int>(lds_u32(buf_s + 4 * w)) : 0;
         if (w < (t >> 5))
             before += c;
         total += c;
     }
     return before + incl - v;
+}
+
+// Step 3 of the group top-k selections: thread t holds keys key[0 .. nv) of the
+// consecutive candidates lo, lo + 1, ...; a key is above the threshold when its bits
+// under hmask exceed P, equal to it when they match P, and of the keys equal to it the
+// first `need` in block order are taken.  Each thread counts its keys above and equal;
+// a group prefix sum of the equal ones gives each thread its share of the `need`, a
+// second one its output offset; B_init, the selection and B_local are written
+// ascending, -1 after, and the count.  buf0_s / buf1_s: two 16-word reduction buffers.
+// (Bit m of a mask stands for the thread's key m; the loops run over set bits, so this
+// once-run code stays short.)
+template <int KPT>
+__device__ __forceinline__ void cta_write_list(const uint32_t (&key)[KPT], int nv, int lo, uint32_t P, uint32_t hmask,
+                                               int need, int nb, int n_init, int n_local, uint32_t buf0_s,
+                                               uint32_t buf1_s, int t, int nthreads, int bar, int *out, int k_tot,
+                                               int *count_out, int *status)
+{
+    const int n_warps = nthreads >> 5;
+    uint32_t gt_mask = 0u, eq_mask = 0u;
+#pragma unroll
+    for (int m = 0; m < KPT; ++m) {
+        const uint32_t km = key[m] & hmask;
+        gt_mask |= (m < nv && km > P) ? (1u << m) : 0u;
+        eq_mask |= (m < nv && km == P) ? (1u << m) : 0u;
+    }
+    const int n_eq = __popc(eq_mask);
+    int total_eq, total_sel;
+    const int eq_before = group_exclusive_scan(n_eq, buf0_s, t, n_warps, bar, total_eq);
+    const int take_eq = max(0, min(n_eq, need - eq_before));
+    uint32_t sel = gt_mask, rest = eq_mask;
+    for (int c = 0; c < take_eq; ++c) {   // the first take_eq equal keys, in block order
+        sel |= rest & (0u - rest);
+        rest &= rest - 1u;
+    }
+    const int sel_before = group_exclusive_scan(__popc(sel), buf1_s, t, n_warps, bar, total_sel);
+    const int n_i = min(n_init, nb);
+    bool overflow = false;
+    int pos = n_i + sel_before;
+    for (; sel != 0u; sel &= sel - 1u, ++pos) {
+        if (pos < k_tot)
+            out[pos] = lo + __ffs(sel) - 1;
+        else
+            overflow = true;
+    }
+    for (int j = t; j < n_i; j += nthreads) {
+        if (j < k_tot)
+            out[j] = j;
+        else
+            overflow = true;
+    }
+    const int l0 = max(nb - n_local, n_i);
+    const int pos_l = n_i + total_sel;
+    for (int j = l0 + t; j < nb; j += nthreads) {
+        const int q = pos_l + (j - l0);
+        if (q < k_tot)
+            out[q] = j;
+        else
+            overflow = true;
+    }
+    const int end = pos_l + max(0, nb - l0);
+    for (int i = end + t; i < k_tot; i += nthreads)
+        out[i] = -1;
+    if (overflow)
+        report(status, SPARSE_ERR_BAD_INDEX);
+    if (t == 0)
+        *count_out = min(end, k_tot);
 }
 
 // The exact top-k of one pair by a group of threads (whole warps, t in [0, nthreads),
@@ -736,55 +805,201 @@ __device__ void topk_cta_regs(uint32_t keys_s, int nb, int n_init, int n_local, 
         P = mn;
         need = group_sum(eq, buf(), t, n_warps, bar);
     }
-    // 3. the ascending list (bit m of a mask: this thread's key m; the loops below run
-    //    over set bits, so this once-run code stays short)
-    uint32_t gt_mask = 0u, eq_mask = 0u;
+    // 3. the ascending list
+    const uint32_t b0 = buf();
+    const uint32_t b1 = buf();
+    cta_write_list<KPT>(key, nv, lo, P, 0xFFFFFFFFu, need, nb, n_init, n_local, b0, b1, t, nthreads, bar, out, k_tot,
+                        count_out, status);
+}
+
+// Shared-memory words that topk_forecast_cta uses at scratch_s for n_warps warps: the
+// warps' digit histograms, then its control words (placed past the coarse histogram, so
+// scratch_s may be the histogram's own address).
+__host__ __device__ constexpr int topk_forecast_scratch_words(int n_warps)
+{
+    return (n_warps * 256 > kCoarseBins ? n_warps * 256 : kCoarseBins) + 56;
+}
+
+// The exact top-k of one pair's Forecast scores by a group of NW warps (t in [0, 32 NW),
+// at most 16 warps, synchronised on named barrier `bar`; t = 0 is in warp 0), with the candidate keys in registers as topk_cta_regs holds them and the coarse
+// histogram of key >> 22 over the candidates at coarse_s (built while the keys were
+// scored).  The k largest keys among candidates [n_init, nb - n_local) (equal keys: the
+// lower block first), united with B_init and B_local, are written ascending to
+// out[0 .. count) and -1 after.
+//   1. Warp 0 finds the coarse bin that holds the k-th largest key: 10 bits decided.
+//   2. The other 22 in passes of 8, 8 and 6 bits: each warp histograms the digit of its
+//      keys that share the decided bits in 256 bins of its own (scratch, over the coarse
+//      histogram once warp 0 has read it), warp 0 adds the warps' bins and picks the
+//      digit that holds the need-th largest.  A bucket that holds exactly the keys still
+//      needed ends the search: every key in it is taken.
+//   3. The list, as topk_cta_regs writes it, above / equal meaning the decided bits.
+// Requires n_init + n_local + k < nb, k >= 1 and topk_cta_regs_fits<KPT>(n_cand,
+// nthreads).  ok: this thread's view of its inputs is complete; false on any thread:
+// nothing is written and a timeout is reported.
+template <int KPT, int NW>
+__device__ void topk_forecast_cta(uint32_t keys_s, uint32_t coarse_s, uint32_t scratch_s, int nb, int n_init,
+                                  int n_local, int k, int t, int bar, bool ok, int *out, int k_tot, int *count_out,
+                                  int *status)
+{
+    static_assert(KPT % 2 == 1, "an odd run length keeps a warp's loads on distinct banks");
+    static_assert(KPT <= 32, "a thread's keys are bits of one mask");
+    static_assert(NW >= 1 && NW <= 16, "at most 16 warps");
+    constexpr int n_warps = NW;
+    constexpr int nthreads = 32 * NW;
+    const int warp = t >> 5, lane = t & 31;
+    const int cand_lo = n_init, cand_hi = nb - n_local;
+    const int n_cand = cand_hi - cand_lo;
+    const int per = ((n_cand + nthreads - 1) / nthreads) | 1;
+    const int lo = cand_lo + t * per;
+    const int nv = max(0, min(per, cand_hi - lo));
+    // control words: [0..2] and [4..6] broadcast slots (prefix, need, bucket count),
+    // [8..23] and [24..39] reduction buffers, [40..55] the warps' not-ready counts
+    const uint32_t ctrl_s = scratch_s + 4u * static_cast<uint32_t>(topk_forecast_scratch_words(n_warps) - 56);
+    uint32_t key[KPT];
 #pragma unroll
-    for (int m = 0; m < KPT; ++m) {
-        gt_mask |= (m < nv && key[m] > P) ? (1u << m) : 0u;
-        eq_mask |= (m < nv && key[m] == P) ? (1u << m) : 0u;
+    for (int m = 0; m < KPT; ++m)
+        key[m] = m < nv ? lds_u32(keys_s + 4 * (lo + m)) : 0u;
+    const int wn = __reduce_add_sync(0xffffffffu, ok ? 0 : 1);
+    if (lane == 0)
+        sts_u32(ctrl_s + 4 * (40 + warp), static_cast<uint32_t>(wn));
+    // 1. the coarse bin: lane l holds bins [1024 - 32(l+1), 1024 - 32l)
+    if (warp == 0) {
+        constexpr int kPer = kCoarseBins / 32;
+        const int bin0 = kCoarseBins - kPer * (lane + 1);
+        uint32_t cb[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; i += 4) {
+            const uint4 v = lds_v4(coarse_s + 4 * (bin0 + i));
+            cb[i] = v.x;
+            cb[i + 1] = v.y;
+            cb[i + 2] = v.z;
+            cb[i + 3] = v.w;
+        }
+        int c = 0;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i)
+            c += static_cast<int>(cb[i]);
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += n;
+        }
+        const int excl = incl - c;
+        int bsel = -1, need_new = 0, cnt = 0;
+        if (excl < k && k <= incl) {
+            int acc = excl;
+#pragma unroll
+            for (int i = kPer - 1; i >= 0; --i) {
+                const int ci = static_cast<int>(cb[i]);
+                if (bsel < 0 && acc + ci >= k) {
+                    bsel = bin0 + i;
+                    need_new = k - acc;
+                    cnt = ci;
+                }
+                acc += ci;
+            }
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, bsel >= 0);
+        if (hit != 0u && lane == __ffs(hit) - 1) {
+            sts_u32(ctrl_s, static_cast<uint32_t>(bsel) << kCoarseShift);
+            sts_u32(ctrl_s + 4, static_cast<uint32_t>(need_new));
+            sts_u32(ctrl_s + 8, static_cast<uint32_t>(cnt));
+            sts_u32(ctrl_s + 12, 1u);
+        } else if (hit == 0u && lane == 0) {   // cannot happen when the histogram counts every candidate
+            sts_u32(ctrl_s, 0u);
+            sts_u32(ctrl_s + 4, static_cast<uint32_t>(k));
+            sts_u32(ctrl_s + 8, static_cast<uint32_t>(n_cand));
+            sts_u32(ctrl_s + 12, 0u);
+        }
     }
-    const int n_eq = __popc(eq_mask);
-    int total_eq, total_sel;
-    const int eq_before = group_exclusive_scan(n_eq, buf(), t, n_warps, bar, total_eq);
-    const int take_eq = max(0, min(n_eq, need - eq_before));
-    uint32_t sel = gt_mask, rest = eq_mask;
-    for (int c = 0; c < take_eq; ++c) {   // the first take_eq equal keys, in block order
-        sel |= rest & (0u - rest);
-        rest &= rest - 1u;
+    named_barrier_sync(bar, nthreads);
+    int not_ready = 0;
+#pragma unroll
+    for (int w = 0; w < n_warps; ++w)
+        not_ready += static_cast<int>(lds_u32(ctrl_s + 4 * (40 + w)));
+    if (not_ready != 0) {
+        if (t == 0)
+            report(status, SPARSE_ERR_TIMEOUT);
+        return;
     }
-    const int sel_before = group_exclusive_scan(__popc(sel), buf(), t, n_warps, bar, total_sel);
-    const int n_i = min(n_init, nb);
-    bool overflow = false;
-    int pos = n_i + sel_before;
-    for (; sel != 0u; sel &= sel - 1u, ++pos) {
-        if (pos < k_tot)
-            out[pos] = lo + __ffs(sel) - 1;
-        else
-            overflow = true;
+    uint32_t P = lds_u32(ctrl_s);
+    int need = static_cast<int>(lds_u32(ctrl_s + 4));
+    int cnt = static_cast<int>(lds_u32(ctrl_s + 8));
+    int top = lds_u32(ctrl_s + 12) != 0u ? kCoarseShift : 32;
+    uint32_t hmask = top == 32 ? 0u : ~((1u << kCoarseShift) - 1u);
+    // 2. the digits below the decided bits
+    int slot = 1;
+    while (top > 0 && cnt != need) {
+        const int w = top < 8 ? top : 8;
+        const int shift = top - w;
+        const uint32_t dmask = (1u << w) - 1u;
+        const uint32_t my_hist = scratch_s + 4u * 256u * static_cast<uint32_t>(warp);
+        for (int d = lane; d < 256; d += 32)
+            sts_u32(my_hist + 4 * d, 0u);
+        __syncwarp();
+#pragma unroll
+        for (int m = 0; m < KPT; ++m)
+            if (m < nv && (key[m] & hmask) == P)
+                asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(my_hist + 4 * ((key[m] >> shift) & dmask)) : "memory");
+        named_barrier_sync(bar, nthreads);
+        if (warp == 0) {
+            // lane l holds digits 255 - 8l - i (i = 0..7), summed over the warps' bins
+            int c[8], sum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t d = static_cast<uint32_t>(255 - 8 * lane - i);
+                int s = 0;
+#pragma unroll
+                for (int ww = 0; ww < n_warps; ++ww)
+                    s += static_cast<int>(lds_u32(scratch_s + 4u * (256u * ww + d)));
+                c[i] = s;
+                sum += s;
+            }
+            int incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o)
+                    incl += n;
+            }
+            const int excl = incl - sum;
+            int dsel = -1, need_new = 0, cdig = 0;
+            if (excl < need && need <= incl) {
+                int acc = excl;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (dsel < 0 && acc + c[i] >= need) {
+                        dsel = 255 - 8 * lane - i;
+                        need_new = need - acc;
+                        cdig = c[i];
+                    }
+                    acc += c[i];
+                }
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, dsel >= 0);
+            // (always found: the bins count exactly the cnt >= need keys sharing the decided bits)
+            const int src = hit != 0u ? __ffs(hit) - 1 : 0;
+            if (lane == src) {
+                const uint32_t so = ctrl_s + 16u * static_cast<uint32_t>(slot);
+                sts_u32(so, P | (static_cast<uint32_t>(dsel < 0 ? 0 : dsel) << shift));
+                sts_u32(so + 4, static_cast<uint32_t>(hit != 0u ? need_new : need));
+                sts_u32(so + 8, static_cast<uint32_t>(hit != 0u ? cdig : need));
+            }
+        }
+        named_barrier_sync(bar, nthreads);
+        const uint32_t so = ctrl_s + 16u * static_cast<uint32_t>(slot);
+        P = lds_u32(so);
+        need = static_cast<int>(lds_u32(so + 4));
+        cnt = static_cast<int>(lds_u32(so + 8));
+        hmask |= dmask << shift;
+        top = shift;
+        slot ^= 1;
     }
-    for (int j = t; j < n_i; j += nthreads) {
-        if (j < k_tot)
-            out[j] = j;
-        else
-            overflow = true;
-    }
-    const int l0 = max(nb - n_local, n_i);
-    const int pos_l = n_i + total_sel;
-    for (int j = l0 + t; j < nb; j += nthreads) {
-        const int q = pos_l + (j - l0);
-        if (q < k_tot)
-            out[q] = j;
-        else
-            overflow = true;
-    }
-    const int end = pos_l + max(0, nb - l0);
-    for (int i = end + t; i < k_tot; i += nthreads)
-        out[i] = -1;
-    if (overflow)
-        report(status, SPARSE_ERR_BAD_INDEX);
-    if (t == 0)
-        *count_out = min(end, k_tot);
+    // 3. the ascending list
+    cta_write_list<KPT>(key, nv, lo, P, hmask, need, nb, n_init, n_local, ctrl_s + 4 * 8, ctrl_s + 4 * 24, t,
+                        nthreads, bar, out, k_tot, count_out, status);
 }
 
 }  // namespace

@@ -42,4 +42,13 @@ inline size_t fused_smem_bytes(int per, int N_cap)
     return static_cast<size_t>(fused_off_keys(per)) + static_cast<size_t>(N_cap) * 4 + 1024;
 }
 
+// The group top-k of CTA 0 (topk_forecast_cta): its 4 consumer warps and the selector
+// warp, on named barrier 2, with up to kSelKPT candidates per thread (2720 in all), its
+// scratch over the coarse histogram and the threshold list.
+constexpr int kSelThreads = (kConsumerWarps + 1) * 32;
+constexpr int kSelKPT = 17;
+constexpr int kSelBar = 2;
+static_assert(topk_forecast_scratch_words(kSelThreads / 32) * 4 <= fused_off_slice() - fused_off_hist(),
+              "the group top-k's scratch fits over the histogram and the list");
+
 }  // namespace

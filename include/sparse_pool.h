@@ -314,8 +314,12 @@ SPARSE_API int sparse_decode_attn_ex(const uint16_t *Q, const uint16_t *k_base,
  *   N_cap, n_init, n_local, k, idx_next [B][H_kv][k_tot_next], count_next [B][H_kv]
  *                as for sparse_select_topk; idx_next / count_next must not alias
  *                blk_idx / count.
- *   n_split      CTAs per pair (1, 2, 4 or 8; 0 = chosen from the SM count): each
- *                takes a slice of the pair's block list and of its compressed keys.
+ *   n_split      CTAs per pair (1, 2, 4, 8 or, for G <= 8, 16; 0 = chosen from the SM
+ *                count): each takes a slice of the pair's block list and of its
+ *                compressed keys.  16 is a non-portable cluster size: it is used (and
+ *                chosen automatically, when few pairs have to fill the GPU) only where
+ *                the device can schedule such clusters; an explicit 16 that cannot be
+ *                scheduled is rejected with SPARSE_ERR_UNSUPPORTED.
  *   flags        0 or SPARSE_ATTN_BLOCKS_READY (as for sparse_decode_attn).
  * Shared memory holds the pair's N_cap keys: N_cap up to about 28000.
  *

@@ -281,7 +281,7 @@ def test_forecast_128k_layer_all_pairs_at_full_size():
         assert len(set(planted[1, p].tolist()) & set(nidx[p].tolist())) >= 40
 
 
-@pytest.mark.parametrize("n_split", [0, 8])
+@pytest.mark.parametrize("n_split", [0, 8, 16])
 def test_b1_80layer_resident_sampled_layers(n_split):
     """The literal B = 1 variant of the 128K step (8 pairs per layer, all 80 layers
     resident in the bench): the bench's chain of launches -- sparse_select_topk for
