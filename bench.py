@@ -387,9 +387,13 @@ def kernel_breakdown(wk, dev, peak):
     reps_alone = 2 if L * 2 >= 160 else max(2, 160 // L)
 
     def time_alone(fn, reps=reps_alone):
+        # synchronize, then the L2-evicting read (~85 us of GPU time), during which the
+        # host enqueues the timed launch: the events bracket GPU work only, never a wait
+        # for the host to submit the launch
         ev = []
         for _ in range(reps):
             for l in range(L):
+                torch.cuda.synchronize(dev)
                 l2_evict(flush)
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record()
@@ -804,11 +808,13 @@ def run_layer_case(args, local_rank):
     for i in range(args.warmup + args.steps):
         F = wl.forecast(sh, 0, i, dev)
         Q = wl.queries(sh, i, dev)
+        torch.cuda.synchronize(dev)
         l2_evict(flush)
         e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         e[0].record()
         binding.sparse_select_topk(F, kt, seq, sh.n_init, sh.n_local, sh.k, idx, cnt, status=status)
         e[1].record()
+        torch.cuda.synchronize(dev)
         l2_evict(flush)
         e3 = torch.cuda.Event(enable_timing=True)
         e3.record()
@@ -817,6 +823,7 @@ def run_layer_case(args, local_rank):
                                        workspace=ws)
         e[2].record()
         # one fused layer: this layer's attention and the selection from the same keys
+        torch.cuda.synchronize(dev)
         l2_evict(flush)
         e4, e5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e4.record()
@@ -826,6 +833,7 @@ def run_layer_case(args, local_rank):
                                                 n_split=args.n_split, status=status)
         e5.record()
         # the multi-head (InfLLM-V2) selector on the same compressed keys, for comparison
+        torch.cuda.synchronize(dev)
         l2_evict(flush)
         e6, e7 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e6.record()
@@ -868,10 +876,13 @@ def run_layer_case(args, local_rank):
 
 
 def _event_times(fn, steps, warmup, evict=None):
-    """Per-iteration device time of fn() (CUDA events on the current stream), µs."""
+    """Per-iteration device time of fn() (CUDA events on the current stream), µs.  Each
+    iteration starts from an idle GPU: synchronize, the L2-evicting read, during which
+    the host enqueues fn's launches, so the events bracket GPU work only."""
     import torch
     pairs = []
     for i in range(warmup + steps):
+        torch.cuda.synchronize()
         if evict is not None:
             l2_evict(evict)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -953,8 +964,11 @@ class _Layer:
         if sh.n_new > 0:
             # the same token written at the same position every step: the step is idempotent
             bd.sparse_pool_append(self.k_cache, self.v_cache, self.ktil, self.k_new, self.v_new, sh.T)
+        # the append writes only the block of the new token, a local block: the selection
+        # streams the candidates' keys while it runs
+        local_only = sh.n_new > 0 and sh.T // BLK >= sh.N_b - sh.n_local
         bd.sparse_select_topk(self.F, self.ktil, self.seq, sh.n_init, sh.n_local, sh.k, self.idx, self.cnt,
-                              status=self.status)
+                              status=self.status, flags=bd.SPARSE_SELECT_KEYS_READY if local_only else 0)
         bd.sparse_decode_attn(self.Q, self.k_cache, self.v_cache, self.idx, self.cnt, self.seq, self.O,
                               workspace=self.ws, status=self.status)
 

@@ -32,6 +32,7 @@ SPARSE_ERR_BAD_INDEX = -6
 SPARSE_ATTN_BLOCKS_READY = 1
 SPARSE_ATTN_STREAM_K = 2
 SPARSE_NSA_BRANCH_GRID = 4
+SPARSE_SELECT_KEYS_READY = 8
 
 # (name, restype, argtypes) of every entry point declared in include/sparse_pool.h
 _P, _I, _LL, _F, _U = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float, ctypes.c_uint
@@ -43,6 +44,7 @@ SIGNATURES = {
     "sparse_pool_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _LL, _I, _LL, _I, _P]),
     "sparse_pool_append_kv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _LL, _I, _LL, _I, _P]),
     "sparse_select_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P]),
+    "sparse_select_topk_ex": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _U, _P, _P]),
     "sparse_select_topk_heads": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _P, _P, _I, _P, _P]),
     "sparse_prefill_select": (_I, [_P, _LL, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P]),
     "sparse_decode_attn": (_I, [_P, _P, _P, _LL, _P, _P, _P, _I, _P, _I, _I, _I, _F, _P, _P, _I, _U, _P, _SZ,
@@ -161,8 +163,9 @@ def sparse_pool_append_kv(k_cache, v_cache, ktil, vtil, k_new, v_new, len_before
 
 
 def sparse_select_topk(F, ktil, seq_len, n_init: int, n_local: int, k: int, idx_out, count_out,
-                       status=None, stream=None):
-    """Fill idx_out [B][H_kv][k_tot] and count_out [B][H_kv] from F [B][H_kv][128] and ktil."""
+                       status=None, stream=None, flags: int = 0):
+    """Fill idx_out [B][H_kv][k_tot] and count_out [B][H_kv] from F [B][H_kv][128] and ktil.
+    flags (SPARSE_SELECT_KEYS_READY) calls sparse_select_topk_ex."""
     B, H_kv, N_cap, _ = ktil.shape
     k_tot = idx_out.shape[2]
     _need(F, "F", torch.bfloat16, shape=(B, H_kv, D))
@@ -172,6 +175,12 @@ def sparse_select_topk(F, ktil, seq_len, n_init: int, n_local: int, k: int, idx_
     _need(count_out, "count_out", torch.int32, shape=(B, H_kv))
     if status is not None:
         _need(status, "status", torch.int32)
+    if flags:
+        rc = load().sparse_select_topk_ex(_ptr(F), _ptr(ktil), _ptr(seq_len), B, H_kv, N_cap, n_init, n_local, k,
+                                          _ptr(idx_out), _ptr(count_out), k_tot, int(flags), _ptr(status),
+                                          _stream(stream))
+        _check(rc, "sparse_select_topk_ex")
+        return
     rc = load().sparse_select_topk(_ptr(F), _ptr(ktil), _ptr(seq_len), B, H_kv, N_cap, n_init, n_local, k,
                                    _ptr(idx_out), _ptr(count_out), k_tot, _ptr(status), _stream(stream))
     _check(rc, "sparse_select_topk")

@@ -51,7 +51,10 @@ __global__ void __launch_bounds__(kFThreads, 2)
     decode_forecast_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                            const AttnParams p)
 {
-    if (!ATTN)
+    // the selection alone waits for the kernel before it unless the caller promised that
+    // the candidates' compressed keys and seq_len are complete (SPARSE_SELECT_KEYS_READY):
+    // then the key stream starts at once and only F waits (consumers, below)
+    if (!ATTN && (p.flags & SPARSE_SELECT_KEYS_READY) == 0u)
         griddep_wait();
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -95,9 +98,12 @@ __global__ void __launch_bounds__(kFThreads, 2)
     // alone, while the consumers attend)
     const bool sel_group = rank == 0 && score && p.sel_block != 0 && p.k_sel >= 1 &&
                            topk_cta_regs_fits<kSelKPT>(nb - p.n_local - p.n_init, kSelThreads);
-    const int chunk = (nb + static_cast<int>(S) - 1) / static_cast<int>(S);
-    const int r0 = score ? min(nb, static_cast<int>(rank) * chunk) : 0;
-    const int n_krows = score ? min(nb, r0 + chunk) - r0 : 0;
+    // CTA r streams its slice of the candidates [n_init, nb - n_local) only: init and
+    // local blocks are never scored (and the local ones may be the ones an append writes)
+    const int n_cand = max(0, nb - p.n_local - p.n_init);
+    const int chunk = (n_cand + static_cast<int>(S) - 1) / static_cast<int>(S);
+    const int r0 = score ? p.n_init + min(n_cand, static_cast<int>(rank) * chunk) : 0;
+    const int n_krows = score ? p.n_init + min(n_cand, static_cast<int>(rank + 1) * chunk) - r0 : 0;
     const int n_kst = (n_krows + kKtilRowsPerStage - 1) / kKtilRowsPerStage;
 
     if (tid == 0) {
@@ -257,7 +263,7 @@ __global__ void __launch_bounds__(kFThreads, 2)
                 if (own)
                     keys0[j] = key;
                 // coarse histogram of the candidates, one atomic per distinct bin
-                const bool cand = own && j >= p.n_init && j < nb - p.n_local;
+                const bool cand = own;   // every streamed row is a candidate
                 const uint32_t bin = cand ? key >> kCoarseShift : 0xFFFFFFFFu;
                 const uint32_t same = __match_any_sync(0xffffffffu, bin);
                 if (cand && lane == __ffs(same) - 1)
@@ -545,12 +551,16 @@ extern "C" SPARSE_API int sparse_decode_attn_forecast(
                   : launch_fused<2, true, kMaxSplit>(p, km, vm, S, pairs, smem, dev.device, st);
 }
 
-extern "C" SPARSE_API int sparse_select_topk(const uint16_t *F, const float *ktil, const int *seq_len, int B,
-                                             int H_kv, int N_cap, int n_init, int n_local, int k, int *idx_out,
-                                             int *count_out, int k_tot, int *status, void *stream)
+namespace {
+
+int select_impl(const uint16_t *F, const float *ktil, const int *seq_len, int B, int H_kv, int N_cap, int n_init,
+                int n_local, int k, int *idx_out, int *count_out, int k_tot, unsigned flags, int *status,
+                void *stream)
 {
     using sp_host::aligned16;
     using sp_host::fail;
+    if ((flags & ~SPARSE_SELECT_KEYS_READY) != 0u)
+        return fail(SPARSE_ERR_INVALID_ARG, "sparse_select_topk_ex: unknown flags 0x%x", flags);
     if (!F || !ktil || !seq_len || !idx_out || !count_out)
         return fail(SPARSE_ERR_INVALID_ARG, "sparse_select_topk: null pointer");
     if (!aligned16(F) || !aligned16(ktil))
@@ -589,8 +599,27 @@ extern "C" SPARSE_API int sparse_select_topk(const uint16_t *F, const float *kti
     p.k_sel = k;
     p.k_tot_next = k_tot;
     p.sel_block = 1;   // nothing else to do: every warp of CTA 0 takes part
+    p.flags = flags;
     CUtensorMap unused;
     memset(&unused, 0, sizeof unused);
     return launch_fused<1, false, kMaxSplit>(p, unused, unused, S, pairs, smem, dev.device,
                                              static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" SPARSE_API int sparse_select_topk(const uint16_t *F, const float *ktil, const int *seq_len, int B,
+                                             int H_kv, int N_cap, int n_init, int n_local, int k, int *idx_out,
+                                             int *count_out, int k_tot, int *status, void *stream)
+{
+    return select_impl(F, ktil, seq_len, B, H_kv, N_cap, n_init, n_local, k, idx_out, count_out, k_tot, 0u, status,
+                       stream);
+}
+
+extern "C" SPARSE_API int sparse_select_topk_ex(const uint16_t *F, const float *ktil, const int *seq_len, int B,
+                                                int H_kv, int N_cap, int n_init, int n_local, int k, int *idx_out,
+                                                int *count_out, int k_tot, unsigned flags, int *status, void *stream)
+{
+    return select_impl(F, ktil, seq_len, B, H_kv, N_cap, n_init, n_local, k, idx_out, count_out, k_tot, flags,
+                       status, stream);
 }

@@ -122,6 +122,24 @@ SPARSE_API int sparse_select_topk(const uint16_t *F, const float *ktil, const in
                                   void *stream);
 
 /*
+ * sparse_select_topk_ex -- sparse_select_topk with launch-order flags (the same
+ * arguments, results and launch order otherwise; flags = 0 is sparse_select_topk).
+ *   flags  0 or SPARSE_SELECT_KEYS_READY: the caller promises that seq_len and the
+ *          compressed keys of the candidate blocks [n_init, N_b - n_local) are not
+ *          written by the kernel before this one on the stream (e.g. a decode step's
+ *          sparse_pool_append, which only touches the block holding the new token: a
+ *          local block).  The selection then streams those keys at once, overlapping
+ *          that kernel, and waits for it only before reading F.  Only candidate keys
+ *          are read in any case.
+ */
+#define SPARSE_SELECT_KEYS_READY 8u
+
+SPARSE_API int sparse_select_topk_ex(const uint16_t *F, const float *ktil, const int *seq_len,
+                                     int B, int H_kv, int N_cap, int n_init, int n_local, int k,
+                                     int *idx_out, int *count_out, int k_tot, unsigned flags,
+                                     int *status, void *stream);
+
+/*
  * sparse_prefill_select -- the Forecast selection of every prefill position, [SparDA]
  * §4.3 eq.(16) (the indexer scores all T positions against the compressed keys,
  * H_kv * T * N_b * d multiply-adds) with the per-position selection of sparse_select_topk:

@@ -74,6 +74,17 @@ def test_select_rejects_bad_arguments(lib):
     assert f(FAKE, FAKE, FAKE, 1, 2, 64, -1, 2, 8, FAKE, FAKE, 11, None, None) == binding.SPARSE_ERR_INVALID_ARG
 
 
+def test_select_ex_rejects_unknown_flags(lib):
+    f = lib.sparse_select_topk_ex
+    ok_flags = binding.SPARSE_SELECT_KEYS_READY
+    assert f(FAKE, FAKE, FAKE, 1, 2, 64, 1, 2, 8, FAKE, FAKE, 11, 0x10, None, None) == binding.SPARSE_ERR_INVALID_ARG
+    assert "flags" in lib.sparse_last_error().decode()
+    # the flag itself is accepted: the call fails later, on the null F
+    assert f(None, FAKE, FAKE, 1, 2, 64, 1, 2, 8, FAKE, FAKE, 11, ok_flags, None, None) == \
+        binding.SPARSE_ERR_INVALID_ARG
+    assert "null" in lib.sparse_last_error().decode()
+
+
 def test_decode_rejects_bad_arguments(lib):
     f = lib.sparse_decode_attn
     args = [FAKE, FAKE, FAKE, 4096, None, FAKE, FAKE, 11, FAKE, 1, 8, 2, 0.0, FAKE, None, 0, 0, None, 0, None, None]

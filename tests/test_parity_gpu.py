@@ -151,6 +151,44 @@ def test_select_matches_oracle_random_scores(N_cap, lens_b, k):
     assert_selection_matches(idx, cnt, ridx, rcnt, rs, lens_p, 1, 2, k)
 
 
+def test_select_keys_ready_overlaps_the_decode_append():
+    """A decode step's append followed on the same stream by sparse_select_topk_ex with
+    SPARSE_SELECT_KEYS_READY (the append writes only the new token's block, a local
+    block, so the selection streams the candidates' keys while the append runs): over
+    40 appends crossing a block boundary the lists equal those of a plain selection
+    issued after the append completed, and the last ones equal the oracle's."""
+    sh = wl.DecodeShape("keys_ready", B=2, H_q=16, H_kv=4, T=40 * BLK - 20, n_init=1, n_local=2, k=12,
+                        n_planted=10, seed=91)
+    B, H_kv, P = sh.B, sh.H_kv, sh.pairs
+    T_end = sh.T + 40
+    N_cap = (T_end + BLK - 1) // BLK
+    planted = wl.planted_sets(sh, 1)[0]
+    K = torch.empty((B, H_kv, T_end, D), dtype=torch.bfloat16, device="cuda")
+    V = torch.empty_like(K)
+    for p in range(P):
+        b, h = divmod(p, H_kv)
+        K[b, h], V[b, h] = wl.kv_pair(sh, 0, p, planted[p], "cuda", tokens=T_end)
+    F = wl.forecast(sh, 0, 0, "cuda")
+    L = GpuLayer(B, sh.H_q, H_kv, T_end, N_cap, sh.n_init, sh.n_local, sh.k)
+    L.append(K[:, :, :sh.T], V[:, :, :sh.T], 0)
+    idx_b, cnt_b = torch.empty_like(L.idx), torch.empty_like(L.count)
+    for i in range(40):
+        pos = sh.T + i
+        seq = _seq([pos + 1] * B)
+        L.append(K[:, :, pos:pos + 1], V[:, :, pos:pos + 1], pos)
+        binding.sparse_select_topk(F, L.ktil, seq, sh.n_init, sh.n_local, sh.k, L.idx, L.count, status=L.status,
+                                   flags=binding.SPARSE_SELECT_KEYS_READY)
+        torch.cuda.synchronize()
+        binding.sparse_select_topk(F, L.ktil, seq, sh.n_init, sh.n_local, sh.k, idx_b, cnt_b, status=L.status)
+        torch.cuda.synchronize()
+        assert L.status.item() == 0
+        assert torch.equal(L.idx, idx_b) and torch.equal(L.count, cnt_b), f"after append {i}"
+    lens_p = [T_end] * P
+    ref = oracle.pool(bits(K).reshape(P, T_end, D), lens_p, N_cap)
+    ridx, rcnt, rs = oracle.select(bits(F).reshape(P, D), ref, lens_p, sh.n_init, sh.n_local, sh.k)
+    assert_selection_matches(L.idx, L.count, ridx, rcnt, rs, lens_p, sh.n_init, sh.n_local, sh.k)
+
+
 def test_select_ties_go_to_the_lower_index_exactly():
     # integer scores: fp32 and fp64 agree exactly, so the tie rule alone decides
     lens_b, H_kv, N_cap, k = [300 * BLK, 77 * BLK + 5], 2, 300, 16
