@@ -358,6 +358,58 @@ __device__ __forceinline__ void topk_range_regs(uint32_t keys_s, int nb, int n_i
     write_local_and_close(nb, n_init, n_local, pos0, out, k_tot, count_out, status, overflow, lane);
 }
 
+// The coarse bin that holds the k-th largest key, from the histogram of key >> 22 at
+// coarse_s (kCoarseBins counts), by one warp: every lane sums its 32 bins [1024 - 32(l+1),
+// 1024 - 32l) read in a rotated order (lane l starts at its bin l, so the 32 lanes hit 32
+// distinct banks), a prefix sum from the top bin finds the lane that holds the k-th key,
+// and that lane alone walks its bins from the top.  Gives the bin (-1 if the histogram
+// counts fewer than k keys), the keys still needed within it and its count, on every lane.
+__device__ __forceinline__ void coarse_pick_warp(uint32_t coarse_s, int k, int lane, int &bsel, int &need_new,
+                                                 int &cnt)
+{
+    constexpr int kPer = kCoarseBins / 32;
+    const int bin0 = kCoarseBins - kPer * (lane + 1);
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+        c += static_cast<int>(lds_u32(coarse_s + 4 * (bin0 + ((j + lane) & (kPer - 1)))));
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += n;
+    }
+    const int excl = incl - c;
+    bsel = -1;
+    need_new = 0;
+    cnt = 0;
+    if (excl < k && k <= incl) {
+        uint32_t cb[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i)
+            cb[i] = lds_u32(coarse_s + 4 * (bin0 + i));
+        int acc = excl;
+#pragma unroll
+        for (int i = kPer - 1; i >= 0; --i) {
+            const int ci = static_cast<int>(cb[i]);
+            if (bsel < 0 && acc + ci >= k) {
+                bsel = bin0 + i;
+                need_new = k - acc;
+                cnt = ci;
+            }
+            acc += ci;
+        }
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, bsel >= 0);
+    const int src = hit != 0u ? __ffs(hit) - 1 : 0;
+    bsel = __shfl_sync(0xffffffffu, bsel, src);
+    need_new = __shfl_sync(0xffffffffu, need_new, src);
+    cnt = __shfl_sync(0xffffffffu, cnt, src);
+    if (hit == 0u)
+        bsel = -1;
+}
+
 // The exact top-k of one pair by one warp over the order keys of blocks [0, nb) (shared
 // array at keys_s): the k largest keys among candidates [n_init, nb - n_local) (equal
 // keys: lower block first), united with B_init and B_local, written ascending to
@@ -386,50 +438,10 @@ __device__ void topk_warp(uint32_t keys_s, uint32_t coarse_s, uint32_t list_s, i
     bool listed = false;
     int n_list = 0;
     if (!take_all && !take_none) {
-        // 1. the coarse bin: lane l holds bins [1024 - 32(l+1), 1024 - 32l)
-        constexpr int kPer = kCoarseBins / 32;
-        const int bin0 = kCoarseBins - kPer * (lane + 1);
-        uint32_t cb[kPer];
-#pragma unroll
-        for (int i = 0; i < kPer; i += 4) {
-            const uint4 v = lds_v4(coarse_s + 4 * (bin0 + i));
-            cb[i] = v.x;
-            cb[i + 1] = v.y;
-            cb[i + 2] = v.z;
-            cb[i + 3] = v.w;
-        }
-        int c = 0;
-#pragma unroll
-        for (int i = 0; i < kPer; ++i)
-            c += static_cast<int>(cb[i]);
-        int incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o)
-                incl += n;
-        }
-        const int excl = incl - c;
-        int bsel = -1, need_new = 0, m = 0;
-        if (excl < need && need <= incl) {
-            int acc = excl;
-#pragma unroll
-            for (int i = kPer - 1; i >= 0; --i) {
-                const int ci = static_cast<int>(cb[i]);
-                if (bsel < 0 && acc + ci >= need) {
-                    bsel = bin0 + i;
-                    need_new = need - acc;
-                    m = ci;
-                }
-                acc += ci;
-            }
-        }
-        const unsigned hit = __ballot_sync(0xffffffffu, bsel >= 0);
-        const int src_lane = hit != 0u ? __ffs(hit) - 1 : 0;
-        bsel = __shfl_sync(0xffffffffu, bsel, src_lane);
-        need_new = __shfl_sync(0xffffffffu, need_new, src_lane);
-        m = __shfl_sync(0xffffffffu, m, src_lane);
-        if (hit != 0u) {   // always, when the histogram counts every candidate
+        // 1. the coarse bin
+        int bsel, need_new, m;
+        coarse_pick_warp(coarse_s, need, lane, bsel, need_new, m);
+        if (bsel >= 0) {   // always, when the histogram counts every candidate
             prefix = static_cast<uint32_t>(bsel) << kCoarseShift;
             pmask = ~((1u << kCoarseShift) - 1u);
             // keys strictly above the bin: k - need_new; the list holds them and the bin
@@ -635,16 +647,15 @@ __device__ __forceinline__ int group_exclusive_scan(int v, uint32_t buf_s, int t
 // consecutive candidates lo, lo + 1, ...; a key is above the threshold when its bits
 // under hmask exceed P, equal to it when they match P, and of the keys equal to it the
 // first `need` in block order are taken.  Each thread counts its keys above and equal;
-// a group prefix sum of the equal ones gives each thread its share of the `need`, a
-// second one its output offset; B_init, the selection and B_local are written
-// ascending, -1 after, and the count.  buf0_s / buf1_s: two 16-word reduction buffers.
-// (Bit m of a mask stands for the thread's key m; the loops run over set bits, so this
-// once-run code stays short.)
+// one group prefix sum of the two counts (packed in one word) gives each thread its
+// share of the `need` equal keys and its output offset; B_init, the selection and
+// B_local are written ascending, -1 after, and the count.  buf_s: a 16-word reduction
+// buffer.  (Bit m of a mask stands for the thread's key m; the loops run over set bits,
+// so this once-run code stays short.)
 template <int KPT>
 __device__ __forceinline__ void cta_write_list(const uint32_t (&key)[KPT], int nv, int lo, uint32_t P, uint32_t hmask,
-                                               int need, int nb, int n_init, int n_local, uint32_t buf0_s,
-                                               uint32_t buf1_s, int t, int nthreads, int bar, int *out, int k_tot,
-                                               int *count_out, int *status)
+                                               int need, int nb, int n_init, int n_local, uint32_t buf_s, int t,
+                                               int nthreads, int bar, int *out, int k_tot, int *count_out, int *status)
 {
     const int n_warps = nthreads >> 5;
     uint32_t gt_mask = 0u, eq_mask = 0u;
@@ -655,15 +666,18 @@ __device__ __forceinline__ void cta_write_list(const uint32_t (&key)[KPT], int n
         eq_mask |= (m < nv && km == P) ? (1u << m) : 0u;
     }
     const int n_eq = __popc(eq_mask);
-    int total_eq, total_sel;
-    const int eq_before = group_exclusive_scan(n_eq, buf0_s, t, n_warps, bar, total_eq);
+    // (equal << 16) | above: both counts stay below 2^16 (at most 16 warps x 32 keys each)
+    int total;
+    const int before = group_exclusive_scan((n_eq << 16) | __popc(gt_mask), buf_s, t, n_warps, bar, total);
+    const int eq_before = before >> 16, gt_before = before & 0xFFFF;
     const int take_eq = max(0, min(n_eq, need - eq_before));
     uint32_t sel = gt_mask, rest = eq_mask;
     for (int c = 0; c < take_eq; ++c) {   // the first take_eq equal keys, in block order
         sel |= rest & (0u - rest);
         rest &= rest - 1u;
     }
-    const int sel_before = group_exclusive_scan(__popc(sel), buf1_s, t, n_warps, bar, total_sel);
+    const int sel_before = gt_before + min(eq_before, need);
+    const int total_sel = (total & 0xFFFF) + min(total >> 16, need);
     const int n_i = min(n_init, nb);
     bool overflow = false;
     int pos = n_i + sel_before;
@@ -806,9 +820,7 @@ __device__ void topk_cta_regs(uint32_t keys_s, int nb, int n_init, int n_local, 
         need = group_sum(eq, buf(), t, n_warps, bar);
     }
     // 3. the ascending list
-    const uint32_t b0 = buf();
-    const uint32_t b1 = buf();
-    cta_write_list<KPT>(key, nv, lo, P, 0xFFFFFFFFu, need, nb, n_init, n_local, b0, b1, t, nthreads, bar, out, k_tot,
+    cta_write_list<KPT>(key, nv, lo, P, 0xFFFFFFFFu, need, nb, n_init, n_local, buf(), t, nthreads, bar, out, k_tot,
                         count_out, status);
 }
 
@@ -864,43 +876,8 @@ __device__ void topk_forecast_cta(uint32_t keys_s, uint32_t coarse_s, uint32_t s
         sts_u32(ctrl_s + 4 * (40 + warp), static_cast<uint32_t>(wn));
     // 1. the coarse bin: lane l holds bins [1024 - 32(l+1), 1024 - 32l)
     if (warp == 0) {
-        constexpr int kPer = kCoarseBins / 32;
-        const int bin0 = kCoarseBins - kPer * (lane + 1);
-        uint32_t cb[kPer];
-#pragma unroll
-        for (int i = 0; i < kPer; i += 4) {
-            const uint4 v = lds_v4(coarse_s + 4 * (bin0 + i));
-            cb[i] = v.x;
-            cb[i + 1] = v.y;
-            cb[i + 2] = v.z;
-            cb[i + 3] = v.w;
-        }
-        int c = 0;
-#pragma unroll
-        for (int i = 0; i < kPer; ++i)
-            c += static_cast<int>(cb[i]);
-        int incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o)
-                incl += n;
-        }
-        const int excl = incl - c;
-        int bsel = -1, need_new = 0, cnt = 0;
-        if (excl < k && k <= incl) {
-            int acc = excl;
-#pragma unroll
-            for (int i = kPer - 1; i >= 0; --i) {
-                const int ci = static_cast<int>(cb[i]);
-                if (bsel < 0 && acc + ci >= k) {
-                    bsel = bin0 + i;
-                    need_new = k - acc;
-                    cnt = ci;
-                }
-                acc += ci;
-            }
-        }
+        int bsel, need_new, cnt;
+        coarse_pick_warp(coarse_s, k, lane, bsel, need_new, cnt);
         const unsigned hit = __ballot_sync(0xffffffffu, bsel >= 0);
         if (hit != 0u && lane == __ffs(hit) - 1) {
             sts_u32(ctrl_s, static_cast<uint32_t>(bsel) << kCoarseShift);
@@ -946,17 +923,24 @@ __device__ void topk_forecast_cta(uint32_t keys_s, uint32_t coarse_s, uint32_t s
         named_barrier_sync(bar, nthreads);
         if (warp == 0) {
             // lane l holds digits 255 - 8l - i (i = 0..7), summed over the warps' bins
-            int c[8], sum = 0;
+            // (two 16-byte reads per warp's bins: digits [248 - 8l, 256 - 8l))
+            int c[8] = {0, 0, 0, 0, 0, 0, 0, 0}, sum = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t d = static_cast<uint32_t>(255 - 8 * lane - i);
-                int s = 0;
-#pragma unroll
-                for (int ww = 0; ww < n_warps; ++ww)
-                    s += static_cast<int>(lds_u32(scratch_s + 4u * (256u * ww + d)));
-                c[i] = s;
-                sum += s;
+            for (int ww = 0; ww < n_warps; ++ww) {
+                const uint32_t wb = scratch_s + 4u * (256u * ww + 248u - 8u * static_cast<uint32_t>(lane));
+                const uint4 d0 = lds_v4(wb), d1 = lds_v4(wb + 16);
+                c[0] += static_cast<int>(d1.w);
+                c[1] += static_cast<int>(d1.z);
+                c[2] += static_cast<int>(d1.y);
+                c[3] += static_cast<int>(d1.x);
+                c[4] += static_cast<int>(d0.w);
+                c[5] += static_cast<int>(d0.z);
+                c[6] += static_cast<int>(d0.y);
+                c[7] += static_cast<int>(d0.x);
             }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                sum += c[i];
             int incl = sum;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -998,8 +982,8 @@ __device__ void topk_forecast_cta(uint32_t keys_s, uint32_t coarse_s, uint32_t s
         slot ^= 1;
     }
     // 3. the ascending list
-    cta_write_list<KPT>(key, nv, lo, P, hmask, need, nb, n_init, n_local, ctrl_s + 4 * 8, ctrl_s + 4 * 24, t,
-                        nthreads, bar, out, k_tot, count_out, status);
+    cta_write_list<KPT>(key, nv, lo, P, hmask, need, nb, n_init, n_local, ctrl_s + 4 * 8, t, nthreads, bar, out,
+                        k_tot, count_out, status);
 }
 
 }  // namespace
