@@ -22,6 +22,8 @@ constexpr int kStageBytes = 2 * kTileBytes;     // K + V of one block: 32 KB
 constexpr int kMaxUnion = 512;
 constexpr int kMaxSplit = 8;
 constexpr uint64_t kWaitNs = 2000000000ull;
+// The push merge's waits on the other CTAs of a cluster (see cluster_merge_write).
+constexpr uint64_t kMergeWaitNs = 4 * kWaitNs;
 // Row stride (floats) of the warp states in shared memory: a fragment store writes 8
 // dims of 4 rows two apart, and the 4 extra floats put those rows in distinct banks.
 constexpr int kWoStride = kD + 4;
@@ -93,7 +95,6 @@ struct AttnParams {
     int n_local;
     int k_sel;
     int k_tot_next;
-    int sel_block;         // 1: CTA 0's consumer warps and selector warp take the top-k together
     // NSA branches: fp32 output instead of bf16 O, and a block range computed from
     // seq_len instead of a block table (1: the window of the last win_tokens tokens,
     // masked token-granularly; 2: the compressed rows, one per 64-token block holding
@@ -492,12 +493,16 @@ __device__ __forceinline__ int producer_fetch_slice(const AttnParams &p, int pai
 //     free; a peer merges its warps' states and copies its CTA state into the leader's
 //     slot (16-byte distributed-shared-memory stores), arrives on the leader's barrier
 //     and leaves; the leader merges the S states for every output dim.  No cluster-wide
-//     wait on the normal path: the peers do not wait for one another, nor for the
-//     leader's output.  Every thread arrives (relaxed) on the cluster barrier as it
-//     leaves; a warp whose bounded wait ran out waits there too before leaving, so it
-//     stays resident until every CTA of the cluster is past its merge and none can
-//     still reach its shared memory (a late arrive from the leader, late stores from a
-//     peer).
+//     barrier: the peers do not wait for one another, nor for the leader's output.
+//     Lifetimes: a peer is alive until it has seen "go" (the leader's only remote access
+//     to it), and the leader until it has received every state (the peers' only remote
+//     accesses to it).  A CTA gives up one of these waits only after kMergeWaitNs,
+//     longer than any CTA of the cluster can take to reach its merge (its pipeline
+//     waits are bounded by kWaitNs and a CTA leaves its loops at the first that runs
+//     out, so a stalled CTA arrives within about two such waits of starting), so a CTA
+//     that gives up has outlived every remote access the others can still make --
+//     unless a pipeline keeps crawling at under one stage per kWaitNs, which no bounded
+//     wait can tell from progress.
 //   pull: every CTA waits for all, then merges the S states for its slice of the dims
 //     by reading its peers' shared memory, and all wait again before leaving.
 constexpr int kPushRecvOff = 48 * 1024;   // the leader's slots: past the warp and CTA states
@@ -592,12 +597,10 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
         const float *slots = reinterpret_cast<const float *>(base + kPushRecvOff);   // [S - 1][SLOT]
         if (rank != 0) {
             // a peer: copy the CTA state, contiguous from co, into slot rank - 1 of the leader
-            const bool go = __all_sync(0xffffffffu, mbar_wait_cluster(bar_go, 0, kWaitNs));
+            const bool go = __all_sync(0xffffffffu, mbar_wait_cluster(bar_go, 0, kMergeWaitNs));
             if (!go) {
                 if (lane == 0)
                     report(p.status, SPARSE_ERR_TIMEOUT);
-                cluster_arrive_relaxed();
-                cluster_wait();   // the leader may still arrive on this CTA's barrier
                 return;
             }
             const uint32_t dst = dsmem_addr(smem_u32(base + kPushRecvOff) + (rank - 1) * SLOT * 4, 0);
@@ -607,24 +610,19 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
             __syncwarp();
             if (lane == 0)
                 mbar_arrive_cluster(dsmem_addr(bar_recv, 0));
-            cluster_arrive_relaxed();
             return;
         }
         // the leader: the S states, own first, then the slots in rank order
-        if (!__all_sync(0xffffffffu, mbar_wait_cluster(bar_recv, 0, kWaitNs))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_cluster(bar_recv, 0, kMergeWaitNs))) {
             if (lane == 0)
                 report(p.status, SPARSE_ERR_TIMEOUT);
-            cluster_arrive_relaxed();
-            cluster_wait();   // late peers may still store into this CTA's slots
             return;
         }
         int any_abort = cabort[0];
         for (uint32_t c = 1; c < S; ++c)
             any_abort |= reinterpret_cast<const int *>(slots + (c - 1) * SLOT + ROWS * kD + 2 * ROWS)[0];
-        if (any_abort) {
-            cluster_arrive_relaxed();
+        if (any_abort)
             return;
-        }
         // four adjacent dims per item (the slots are 16-byte aligned: SLOT % 4 == 0)
         const int n_items = rows_valid * (kD / 4);
         for (int item = tid; item < n_items; item += nthreads) {
@@ -662,7 +660,6 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
             }
             merge_write_item4<NT, VERIFY>(p, b, g, q0, row, d, M, L, o, true);
         }
-        cluster_arrive_relaxed();
         return;
     }
     cluster_sync();

@@ -306,14 +306,6 @@ __device__ __forceinline__ void cluster_arrive()
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
-// Arrive without ordering this thread's earlier memory accesses (the barrier is used
-// only to know when every thread of the cluster has got past a point).
-__device__ __forceinline__ void cluster_arrive_relaxed()
-{
-    __syncwarp();
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-
 __device__ __forceinline__ void cluster_wait()
 {
     __syncwarp();

@@ -45,8 +45,11 @@ namespace {
 
 // ATTN = false: the Forecast selection alone (sparse_select_topk): no block list, no
 // attention, no merge; every input may be written by the kernel before this one.
-// MAXS: the largest cluster the launch may use (16 for the non-portable size).
-template <int NT, bool ATTN, int MAXS>
+// MAXS: the largest cluster the launch may use (16 for the non-portable size).  SELG:
+// CTA 0's consumer warps and its selector warp take the top-k together (else the
+// selector warp alone, while the consumers attend); a separate instantiation, so the
+// kernels that never use the group top-k carry none of its code.
+template <int NT, bool ATTN, int MAXS, bool SELG>
 __global__ void __launch_bounds__(kFThreads, 2)
     decode_forecast_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                            const AttnParams p)
@@ -96,7 +99,7 @@ __global__ void __launch_bounds__(kFThreads, 2)
     const bool score = do_sel && !take_all;
     // the top-k by CTA 0's consumer and selector warps together (else its selector warp
     // alone, while the consumers attend)
-    const bool sel_group = rank == 0 && score && p.sel_block != 0 && p.k_sel >= 1 &&
+    const bool sel_group = SELG && rank == 0 && score && p.k_sel >= 1 &&
                            topk_cta_regs_fits<kSelKPT>(nb - p.n_local - p.n_init, kSelThreads);
     // CTA r streams its slice of the candidates [n_init, nb - n_local) only: init and
     // local blocks are never scored (and the local ones may be the ones an append writes)
@@ -346,7 +349,7 @@ static_assert((kOffCtrl + 4 * kCtrlScoredBar) % 8 == 0 && 4 * kCtrlScoredBar + 8
 // warps before attending.
 constexpr int kSelBlockMaxPer = 12;
 
-template <int NT, bool ATTN, int MAXS>
+template <int NT, bool ATTN, int MAXS, bool SELG>
 cudaError_t fused_config(cudaLaunchConfig_t *cfg, cudaLaunchAttribute (&attr)[2], int S, long long pairs, size_t smem,
                          cudaStream_t stream)
 {
@@ -368,10 +371,10 @@ cudaError_t fused_config(cudaLaunchConfig_t *cfg, cudaLaunchAttribute (&attr)[2]
 
 // Configure the kernel for this device once (shared memory, carveout and, for MAXS > 8,
 // the non-portable cluster size).
-template <int NT, bool ATTN, int MAXS>
+template <int NT, bool ATTN, int MAXS, bool SELG>
 int configure_fused(size_t smem, int device)
 {
-    auto kern = decode_forecast_kernel<NT, ATTN, MAXS>;
+    auto kern = decode_forecast_kernel<NT, ATTN, MAXS, SELG>;
     static int configured[64];
     if (MAXS > kMaxSplit && device >= 0 && device < 64 && configured[device] < static_cast<int>(smem) + 1) {
         const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(kern),
@@ -401,14 +404,14 @@ bool wide_clusters_fit(size_t smem, long long pairs, int device, cudaStream_t st
         if (g_wide_nofit[device] != 0 && smem >= g_wide_nofit[device])
             return false;
     }
-    if (configure_fused<NT, true, 16>(smem, device) != SPARSE_OK)
+    if (configure_fused<NT, true, 16, true>(smem, device) != SPARSE_OK)
         return false;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    fused_config<NT, true, 16>(&cfg, attr, 16, pairs, smem, stream);
+    fused_config<NT, true, 16, true>(&cfg, attr, 16, pairs, smem, stream);
     int n = 0;
-    const cudaError_t e =
-        cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void *>(decode_forecast_kernel<NT, true, 16>), &cfg);
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(
+        &n, reinterpret_cast<const void *>(decode_forecast_kernel<NT, true, 16, true>), &cfg);
     if (e != cudaSuccess)
         (void)cudaGetLastError();   // a failed query leaves a (non-sticky) error behind: clear it
     const bool fit = e == cudaSuccess && n >= 1;
@@ -420,17 +423,17 @@ bool wide_clusters_fit(size_t smem, long long pairs, int device, cudaStream_t st
     return fit;
 }
 
-template <int NT, bool ATTN, int MAXS>
+template <int NT, bool ATTN, int MAXS, bool SELG>
 int launch_fused(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, int S, long long pairs,
                  size_t smem, int device, cudaStream_t stream)
 {
-    auto kern = decode_forecast_kernel<NT, ATTN, MAXS>;
-    int rc = configure_fused<NT, ATTN, MAXS>(smem, device);
+    auto kern = decode_forecast_kernel<NT, ATTN, MAXS, SELG>;
+    int rc = configure_fused<NT, ATTN, MAXS, SELG>(smem, device);
     if (rc != SPARSE_OK)
         return rc;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    fused_config<NT, ATTN, MAXS>(&cfg, attr, S, pairs, smem, stream);
+    fused_config<NT, ATTN, MAXS, SELG>(&cfg, attr, S, pairs, smem, stream);
     CUtensorMap kmap = km, vmap = vm;
     AttnParams prm = p;
     void *args[] = {&kmap, &vmap, &prm};
@@ -538,7 +541,7 @@ extern "C" SPARSE_API int sparse_decode_attn_forecast(
     // few blocks per CTA: the layer's attention is short, so the top-k is on the path to
     // the next layer and CTA 0's consumers help with it before they attend; many
     // blocks: the selector warp alone, hidden behind the attention
-    p.sel_block = per <= kSelBlockMaxPer ? 1 : 0;
+    const bool sel_group = per <= kSelBlockMaxPer && G <= 8;
     CUtensorMap km, vm;
     if ((rc = sp_host::make_kv_tensor_map(&km, k_cache, T_cap, pairs)) != SPARSE_OK)
         return rc;
@@ -546,9 +549,11 @@ extern "C" SPARSE_API int sparse_decode_attn_forecast(
         return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (S > kMaxSplit)
-        return launch_fused<1, true, 16>(p, km, vm, S, pairs, smem, dev.device, st);
-    return G <= 8 ? launch_fused<1, true, kMaxSplit>(p, km, vm, S, pairs, smem, dev.device, st)
-                  : launch_fused<2, true, kMaxSplit>(p, km, vm, S, pairs, smem, dev.device, st);
+        return launch_fused<1, true, 16, true>(p, km, vm, S, pairs, smem, dev.device, st);
+    if (G > 8)
+        return launch_fused<2, true, kMaxSplit, false>(p, km, vm, S, pairs, smem, dev.device, st);
+    return sel_group ? launch_fused<1, true, kMaxSplit, true>(p, km, vm, S, pairs, smem, dev.device, st)
+                     : launch_fused<1, true, kMaxSplit, false>(p, km, vm, S, pairs, smem, dev.device, st);
 }
 
 namespace {
@@ -598,12 +603,12 @@ int select_impl(const uint16_t *F, const float *ktil, const int *seq_len, int B,
     p.n_local = n_local;
     p.k_sel = k;
     p.k_tot_next = k_tot;
-    p.sel_block = 1;   // nothing else to do: every warp of CTA 0 takes part
     p.flags = flags;
     CUtensorMap unused;
     memset(&unused, 0, sizeof unused);
-    return launch_fused<1, false, kMaxSplit>(p, unused, unused, S, pairs, smem, dev.device,
-                                             static_cast<cudaStream_t>(stream));
+    // nothing else to do: every warp of CTA 0 takes part in the top-k
+    return launch_fused<1, false, kMaxSplit, true>(p, unused, unused, S, pairs, smem, dev.device,
+                                                   static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
