@@ -37,6 +37,12 @@ KV_BLOCK_BYTES = 2 * BLK * D * 2      # K + V of one selected block (bf16)
 KTIL_ROW_BYTES = D * 4                # one fp32 compressed key
 
 
+def n_candidates(sh):
+    """Blocks the selection scores: every block but B_init and B_local (the pages' top-k
+    is taken over the others), so the compressed keys it has to read."""
+    return max(0, sh.N_b - sh.n_init - sh.n_local)
+
+
 # ----------------------------------------------------------------------------- ranks
 
 
@@ -180,7 +186,7 @@ def step_config(sh, world: int) -> dict:
             "n_init": sh.n_init, "n_local": sh.n_local, "blocks_per_pair": sh.k_tot,
             "parallelism": f"replicas x{world}",
             "l2": f"inputs larger than L2: {sh.phys_layers} physical layers x {layer_gb:.2f} GB, the same layer "
-                  f"again after {sh.phys_layers * sh.pairs * (sh.k_tot * KV_BLOCK_BYTES + sh.N_b * KTIL_ROW_BYTES) / 1e9:.2f}"
+                  f"again after {sh.phys_layers * sh.pairs * (sh.k_tot * KV_BLOCK_BYTES + n_candidates(sh) * KTIL_ROW_BYTES) / 1e9:.2f}"
                   " GB of other reads"}
 
 
@@ -258,14 +264,14 @@ class DecodeStep:
     def algorithmic_bytes(self):
         sh = self.sh
         attn = sh.layers * sh.pairs * sh.k_tot * KV_BLOCK_BYTES
-        sel = (sh.layers) * sh.pairs * sh.N_b * KTIL_ROW_BYTES     # layer-0 + layers 1..79
+        sel = (sh.layers) * sh.pairs * n_candidates(sh) * KTIL_ROW_BYTES     # layer-0 + layers 1..79
         return attn, sel
 
     def attn_bytes_per_launch(self):
         return self.sh.pairs * self.sh.k_tot * KV_BLOCK_BYTES
 
     def select_bytes_per_launch(self):
-        return self.sh.pairs * self.sh.N_b * KTIL_ROW_BYTES
+        return self.sh.pairs * n_candidates(self.sh) * KTIL_ROW_BYTES
 
     def fused_bytes_per_launch(self):
         return self.attn_bytes_per_launch() + self.select_bytes_per_launch()
@@ -848,7 +854,7 @@ def run_layer_case(args, local_rank):
     assert status.item() == 0
     peak, src = measured_peaks()
     attn_bytes = sh.pairs * sh.k_tot * KV_BLOCK_BYTES
-    sel_bytes = sh.pairs * sh.N_b * KTIL_ROW_BYTES
+    sel_bytes = sh.pairs * n_candidates(sh) * KTIL_ROW_BYTES
     a, s_ = max(1e-6, statistics.median(att_ms)), statistics.median(sel_ms)
     f_ = max(1e-6, statistics.median(fus_ms)) if fus_ms else 1e-6
     h_ = statistics.median(hds_ms)
@@ -1014,7 +1020,7 @@ def run_single_layer_case(args, dev, sh, name):
     torch.cuda.synchronize()
     assert lay.status.item() == 0, f"device status {lay.status.item()}"
     kv = sh.pairs * sh.k_tot * KV_BLOCK_BYTES
-    sel = sh.pairs * sh.N_b * KTIL_ROW_BYTES
+    sel = sh.pairs * n_candidates(sh) * KTIL_ROW_BYTES
     # append: new K/V rows read and written, the touched compressed key read and written
     app = sh.pairs * (sh.n_new * 2 * 2 * D * 2 + 2 * KTIL_ROW_BYTES) if sh.n_new else 0
     gbs, frac = _rate(kv + sel + app, t["median_us"], peak)
@@ -1286,7 +1292,7 @@ def run_offload_case(args, dev):
     assert wk.status.item() == 0, f"device status {wk.status.item()}"
     ms = a.elapsed_time(b) / steps
     link_step = sh.layers * wk.link_bytes_per_layer()
-    hbm_step = sh.layers * (sh.pairs * sh.N_b * KTIL_ROW_BYTES + 2 * wk.link_bytes_per_layer())
+    hbm_step = sh.layers * (sh.pairs * n_candidates(sh) * KTIL_ROW_BYTES + 2 * wk.link_bytes_per_layer())
     line = {"case": "offload128k", "workload": sh.name, "unit_of_work": f"one decode step ({sh.layers} layers of "
             "select(l+1) -> gather(l+1) on a copy stream, beside attention(l) over the ring)",
             "steps_per_s": round(1000.0 / ms, 2), "ms_per_step": round(ms, 3), "steps_timed": steps,
