@@ -826,7 +826,7 @@ def run_layer_case(args, local_rank):
         e3.record()
         if not select_only:
             binding.sparse_decode_attn(Q, kc, vc, idx, cnt, seq, O, status=status, n_split=args.n_split,
-                                       workspace=ws)
+                                       workspace=ws, flags=attn_flags(args))
         e[2].record()
         # one fused layer: this layer's attention and the selection from the same keys
         torch.cuda.synchronize(dev)
@@ -868,7 +868,7 @@ def run_layer_case(args, local_rank):
             "heads_select_us": round(h_ * 1e3, 2), "heads_over_forecast": round(h_ / s_, 3),
             "fused_us": round(f_ * 1e3, 2), "fused_gbs": round((attn_bytes + sel_bytes) / f_ / 1e6, 1),
             "fused_frac": round((attn_bytes + sel_bytes) / f_ / 1e6 / peak, 4),
-            "peak_gbs": peak, "peak_source": src}
+            "peak_gbs": peak, "peak_source": src, "attention_contraction": contraction_name(args)}
     if select_only:   # only the selectors ran
         for key in ("attn_us", "attn_gbs", "attn_frac", "fused_us", "fused_gbs", "fused_frac"):
             line.pop(key)
@@ -942,7 +942,7 @@ def oracle_baseline(fn, budget_s, units_per_call, unit, sample, min_reps=2):
 class _Layer:
     """One decode layer on the device: cache, compressed keys, block lists, output."""
 
-    def __init__(self, sh, dev, use_workspace=False):
+    def __init__(self, sh, dev, use_workspace=False, attn_flags=0):
         import torch
         from block_sparse_long_pool_gb300 import binding
         from block_sparse_long_pool_gb300 import workloads as wl
@@ -964,6 +964,7 @@ class _Layer:
         self.O = torch.empty((B, H_q, D), dtype=torch.bfloat16, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.ws = binding.decode_workspace(B, H_q, H_kv, sh.k_tot, device=dev) if use_workspace else None
+        self.attn_flags = attn_flags
 
     def step(self):
         sh, bd = self.sh, self.binding
@@ -976,7 +977,7 @@ class _Layer:
         bd.sparse_select_topk(self.F, self.ktil, self.seq, sh.n_init, sh.n_local, sh.k, self.idx, self.cnt,
                               status=self.status, flags=bd.SPARSE_SELECT_KEYS_READY if local_only else 0)
         bd.sparse_decode_attn(self.Q, self.k_cache, self.v_cache, self.idx, self.cnt, self.seq, self.O,
-                              workspace=self.ws, status=self.status)
+                              workspace=self.ws, status=self.status, flags=self.attn_flags)
 
 
 def single_layer_oracle(lay, budget_s):
@@ -1013,7 +1014,7 @@ def single_layer_oracle(lay, budget_s):
 def run_single_layer_case(args, dev, sh, name):
     import torch
     peak, src = measured_peaks()
-    lay = _Layer(sh, dev, use_workspace=args.workspace)
+    lay = _Layer(sh, dev, use_workspace=args.workspace, attn_flags=attn_flags(args))
     evict = torch.ones(512 << 20 >> 2, dtype=torch.int32, device=dev)
     with ClockSampler(dev.index or 0) as clk:
         t = _event_times(lay.step, args.steps, args.warmup, evict)
@@ -1026,6 +1027,7 @@ def run_single_layer_case(args, dev, sh, name):
     gbs, frac = _rate(kv + sel + app, t["median_us"], peak)
     launches = 3 if sh.n_new else 2
     line = {"case": name, "workload": sh.name, "decode_path": "split (workspace)" if args.workspace else "cluster",
+            "attention_contraction": contraction_name(args),
             "unit_of_work": "one decode step (" +
             ("append + " if sh.n_new else "") + "select + attention)",
             "steps_per_s": round(1e6 / t["median_us"], 1), **t, "launches_per_step": launches,
@@ -1039,6 +1041,16 @@ def run_single_layer_case(args, dev, sh, name):
     print(json.dumps(line), flush=True)
 
 
+def contraction_name(args):
+    return "tcgen05.mma, tensor-memory accumulators" if getattr(args, "tensor_memory", False) else "mma.sync"
+
+
+def attn_flags(args):
+    """The attention calls' flag bits a case line's options ask for."""
+    from block_sparse_long_pool_gb300 import binding
+    return binding.SPARSE_ATTN_TENSOR_MEMORY if getattr(args, "tensor_memory", False) else 0
+
+
 def run_verify_case(args, dev):
     import torch
     from block_sparse_long_pool_gb300 import binding
@@ -1049,7 +1061,8 @@ def run_verify_case(args, dev):
     O = torch.empty_like(x["Q"])
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     evict = torch.ones(512 << 20 >> 2, dtype=torch.int32, device=dev)
-    out = {"case": "verify64k", "workload": sh.name, "unit_of_work": "one verification round "
+    out = {"case": "verify64k", "workload": sh.name, "attention_contraction": contraction_name(args),
+           "unit_of_work": "one verification round "
            f"({sh.N_q} queries x {sh.B * sh.H_kv} pairs)", "peak_gbs": peak, "peak_source": src,
            "l2": "512 MB read evicts L2 before each round"}
     clk = ClockSampler(dev.index or 0).__enter__()
@@ -1058,9 +1071,11 @@ def run_verify_case(args, dev):
 
         def run():
             binding.sparse_verify_attn_grouped(x["Q"], x["K"], x["V"], x["I"], C, sh.window_blocks, x["seq_len"], O,
-                                               status=status, shared=shared, n_split=args.n_split)
+                                               status=status, shared=shared, n_split=args.n_split,
+                                               flags=attn_flags(args))
         binding.sparse_verify_attn_grouped(x["Q"], x["K"], x["V"], x["I"], C, sh.window_blocks, x["seq_len"], O,
-                                           blocks_loaded=loaded, status=status, shared=shared, n_split=args.n_split)
+                                           blocks_loaded=loaded, status=status, shared=shared, n_split=args.n_split,
+                                           flags=attn_flags(args))
         t = _event_times(run, args.steps, args.warmup, evict)
         nbytes = int(loaded.item()) * KV_BLOCK_BYTES
         gbs, frac = _rate(nbytes, t["median_us"], peak)
@@ -1086,7 +1101,8 @@ def run_verify_case(args, dev):
                 # K/V stream of layer l overlap the drain of layer l - 1
                 binding.sparse_verify_attn_grouped(x["Q"], Ks[l % phys], Vs[l % phys], x["I"], sh.C, sh.window_blocks,
                                                    x["seq_len"], O, status=status, shared=shared, stream=s_,
-                                                   n_split=args.n_split, flags=binding.SPARSE_ATTN_BLOCKS_READY)
+                                                   n_split=args.n_split,
+                                                   flags=binding.SPARSE_ATTN_BLOCKS_READY | attn_flags(args))
         for _ in range(2):
             g_.replay()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -1113,7 +1129,8 @@ def run_verify_case(args, dev):
 
     def per_query():
         for q in range(sh.N_q):
-            binding.sparse_decode_attn(Qs[q], x["K"], x["V"], lists[q], cnt_q, x["seq_len"], Os[q], status=status)
+            binding.sparse_decode_attn(Qs[q], x["K"], x["V"], lists[q], cnt_q, x["seq_len"], Os[q], status=status,
+                                       flags=attn_flags(args))
     t = _event_times(per_query, args.steps, args.warmup, evict)
     out["per_query_decode"] = {"launches": sh.N_q, **t,
                                "blocks_requested": sh.N_q * sh.B * sh.H_kv * int(lists[0].shape[-1]),
@@ -1731,7 +1748,12 @@ def main():
                          "on a side stream beside sparse_decode_attn")
     ap.add_argument("--tokens", type=int, default=0, help="layer / nsa128k cases: cached tokens (default 131072)")
     ap.add_argument("--flush-mb", type=int, default=512, help="layer case: L2 flush buffer before each launch")
+    ap.add_argument("--tensor-memory", action="store_true",
+                    help="layer (with --no-workspace) / verify64k / single4k / append32k: the attention with "
+                         "SPARSE_ATTN_TENSOR_MEMORY (tcgen05.mma, tensor-memory accumulators)")
     args = ap.parse_args()
+    if args.tensor_memory and (args.workspace or (args.case == "layer" and not args.no_workspace)):
+        ap.error("--tensor-memory runs the cluster path: no workspace")
     if args.warmup < 3 and args.case == "step":
         ap.error("--warmup must be >= 3")
     rank, world, local_rank = dist_env()

@@ -31,6 +31,7 @@ SPARSE_ERR_NOT_READY = -5
 SPARSE_ERR_BAD_INDEX = -6
 SPARSE_ATTN_BLOCKS_READY = 1
 SPARSE_ATTN_STREAM_K = 2
+SPARSE_ATTN_TENSOR_MEMORY = 16
 SPARSE_NSA_BRANCH_GRID = 4
 SPARSE_SELECT_KEYS_READY = 8
 
@@ -255,7 +256,8 @@ def sparse_decode_attn(Q, k_base, v_base, blk_logical, count, seq_len, O, lse=No
     [B][H_kv][T_cap][128] or a ring slot [B][H_kv][k_tot][64][128]).  ``flags`` may be
     SPARSE_ATTN_BLOCKS_READY: the block list and K/V are not written by the previous
     kernel on ``stream`` (they are already complete while it runs), so K/V streaming may
-    start while it drains."""
+    start while it drains; SPARSE_ATTN_TENSOR_MEMORY: both contractions as tcgen05.mma
+    with tensor-memory accumulators (cluster path, no workspace)."""
     B, H_q, H_kv, k_tot, pair_stride = _decode_args(Q, k_base, v_base, blk_logical, count, seq_len, O, lse,
                                                     blk_slot)
     ws, ws_bytes = _ws(workspace)

@@ -561,11 +561,22 @@ __device__ __forceinline__ void merge_write_item4(const AttnParams &p, int b, in
         p.lse[static_cast<size_t>(b) * p.H_q + g * p.G + row] = lse_of(M, L);
 }
 
+// The CTA state's place in the ring (merge scratch): co [ROWS][128] unnormalised O,
+// cm / cl [ROWS] its row max and sum, past the 4 warp states.
+template <int NT>
+__device__ __forceinline__ float *merge_cta_state(uint8_t *base)
+{
+    constexpr int ROWS = 8 * NT;
+    return reinterpret_cast<float *>(base) + kConsumerWarps * ROWS * kWoStride + 3 * kConsumerWarps * ROWS;
+}
+
+// `cta_state_ready`: the caller has written the CTA state (merge_cta_state) itself, and
+// `st` is not read.
 template <int NT, bool VERIFY, int MAXS = kMaxSplit>
 __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uint8_t *base, bool aborted,
                                                     const AttnParams &p, int b, int g, int q0, int rows_valid,
                                                     uint32_t rank, uint32_t S, int nthreads, uint32_t ctrl_s,
-                                                    bool wait_cluster, bool allow_push)
+                                                    bool wait_cluster, bool allow_push, bool cta_state_ready = false)
 {
     constexpr int ROWS = 8 * NT;
     constexpr int SLOT = push_slot_floats<NT>();
@@ -586,13 +597,15 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
     if (push && rank == 0 && tid == 0)
         for (uint32_t r = 1; r < S; ++r)   // this CTA's ring is consumed: the peers may fill its slots
             mbar_arrive_cluster(dsmem_addr(bar_go, r));
-    if (warp < kConsumerWarps)
+    if (!cta_state_ready && warp < kConsumerWarps)
         store_warp_state<NT>(st, wo, wm, wl, warp, lane);
     if (tid == 0)
         cabort[0] = aborted ? 1 : 0;
     __syncthreads();
-    merge_warp_states<ROWS>(wo, wm, wl, wf, co, cm, cl, tid, nthreads, [] { __syncthreads(); });
-    __syncthreads();   // the CTA state (co, cm, cl, cabort) is complete
+    if (!cta_state_ready) {
+        merge_warp_states<ROWS>(wo, wm, wl, wf, co, cm, cl, tid, nthreads, [] { __syncthreads(); });
+        __syncthreads();   // the CTA state (co, cm, cl, cabort) is complete
+    }
     if (push) {
         const float *slots = reinterpret_cast<const float *>(base + kPushRecvOff);   // [S - 1][SLOT]
         if (rank != 0) {

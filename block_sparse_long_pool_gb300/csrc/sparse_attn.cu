@@ -55,15 +55,12 @@ using namespace sp;
 // the blocks (O(entries)); beyond, every entry compares itself with all others.
 constexpr int kUnionBitmapBlocks = 4096;
 static_assert(2 * (kUnionBitmapBlocks / 32) <= kMaxUnion, "union bitmap and prefix fit the entry scratch");
-template <bool VERIFY>
-__device__ __forceinline__ void build_union(const AttnParams &p, uint8_t *base, int b, int g, int q0,
-                                            int nb, int *ctrl)
+// Every thread of the CTA (NTHR of them) calls it; ulist / umask [kMaxUnion] and the
+// scratch ent_v / ent_m / ent_f [kMaxUnion] are in shared memory.
+template <int NTHR>
+__device__ __forceinline__ void build_union(const AttnParams &p, int *ulist, uint32_t *umask, int *ent_v,
+                                            uint32_t *ent_m, int *ent_f, int b, int g, int q0, int nb, int *ctrl)
 {
-    int *ulist = reinterpret_cast<int *>(base + kOffList);
-    uint32_t *umask = reinterpret_cast<uint32_t *>(base + kOffMask);
-    int *ent_v = reinterpret_cast<int *>(base + kOffEntV);
-    uint32_t *ent_m = reinterpret_cast<uint32_t *>(base + kOffEntM);
-    int *ent_f = reinterpret_cast<int *>(base + kOffEntF);
     const int tid = threadIdx.x;
     const int nq = min(p.C, p.N_q - q0);
     const int wcount = min(p.window_blocks, nb);
@@ -72,7 +69,7 @@ __device__ __forceinline__ void build_union(const AttnParams &p, uint8_t *base, 
     const int n_sel_ent = shared ? p.n_sel : nq * p.n_sel;
     const int n_ent = n_sel_ent + wcount;
     const uint32_t all_q = nq >= 32 ? 0xffffffffu : ((1u << nq) - 1u);
-    for (int e = tid; e < n_ent; e += kThreads) {
+    for (int e = tid; e < n_ent; e += NTHR) {
         int v;
         uint32_t m;
         if (e < n_sel_ent) {
@@ -90,18 +87,18 @@ __device__ __forceinline__ void build_union(const AttnParams &p, uint8_t *base, 
         ent_v[e] = v;
         ent_m[e] = m;
     }
-    for (int e = tid; e < kMaxUnion; e += kThreads)
+    for (int e = tid; e < kMaxUnion; e += NTHR)
         umask[e] = 0u;
     if (nb <= kUnionBitmapBlocks) {
         // a bitmap over the blocks: each entry sets its bit; a block's position in the
         // ascending union is the number of set bits below it
-        uint32_t *bits = reinterpret_cast<uint32_t *>(base + kOffEntF);   // [kUnionBitmapBlocks / 32]
+        uint32_t *bits = reinterpret_cast<uint32_t *>(ent_f);              // [kUnionBitmapBlocks / 32]
         uint32_t *pref = bits + kUnionBitmapBlocks / 32;                  // exclusive popcount prefix
         const int nw = (nb + 31) / 32;
-        for (int w = tid; w < nw; w += kThreads)
+        for (int w = tid; w < nw; w += NTHR)
             bits[w] = 0u;
         __syncthreads();
-        for (int e = tid; e < n_ent; e += kThreads) {
+        for (int e = tid; e < n_ent; e += NTHR) {
             const int v = ent_v[e];
             if (v != INT_MAX)
                 atomicOr(&bits[v >> 5], 1u << (v & 31));
@@ -133,7 +130,7 @@ __device__ __forceinline__ void build_union(const AttnParams &p, uint8_t *base, 
                 ctrl[kCtrlList] = incl;
         }
         __syncthreads();
-        for (int e = tid; e < n_ent; e += kThreads) {
+        for (int e = tid; e < n_ent; e += NTHR) {
             const int v = ent_v[e];
             if (v == INT_MAX)
                 continue;
@@ -145,7 +142,7 @@ __device__ __forceinline__ void build_union(const AttnParams &p, uint8_t *base, 
         return;
     }
     __syncthreads();
-    for (int e = tid; e < n_ent; e += kThreads) {
+    for (int e = tid; e < n_ent; e += NTHR) {
         const int v = ent_v[e];
         int first = v != INT_MAX;
         for (int e2 = 0; e2 < e && first; ++e2)
@@ -153,7 +150,7 @@ __device__ __forceinline__ void build_union(const AttnParams &p, uint8_t *base, 
         ent_f[e] = first;
     }
     __syncthreads();
-    for (int e = tid; e < n_ent; e += kThreads) {
+    for (int e = tid; e < n_ent; e += NTHR) {
         const int v = ent_v[e];
         if (v == INT_MAX)
             continue;
@@ -232,7 +229,9 @@ __device__ __forceinline__ void attn_cluster_cta(const CUtensorMap *kmap, const 
     if (VERIFY) {
         len = p.seq_len[b];
         const int nb = len <= 0 ? 0 : static_cast<int>((len + kBlk - 1) / kBlk);
-        build_union<VERIFY>(p, base, b, g, q0, nb, ctrl);
+        build_union<kThreads>(p, reinterpret_cast<int *>(base + kOffList), reinterpret_cast<uint32_t *>(base + kOffMask),
+                              reinterpret_cast<int *>(base + kOffEntV), reinterpret_cast<uint32_t *>(base + kOffEntM),
+                              reinterpret_cast<int *>(base + kOffEntF), b, g, q0, nb, ctrl);
         __syncthreads();
         n_list = ctrl[kCtrlList];
         const int per = (n_list + static_cast<int>(S) - 1) / static_cast<int>(S);
@@ -332,6 +331,23 @@ __global__ void __launch_bounds__(kThreads, 2)
                        const __grid_constant__ AttnParams p)
 {
     attn_cluster_cta<NT, VERIFY>(&kmap, &vmap, p, static_cast<int>(blockIdx.y));
+}
+
+}  // namespace
+
+// The tensor-memory form of the same CTA (it calls build_union above).
+#include "attn_tc.cuh"
+
+namespace {
+
+// The split-KV CTA with both contractions on the 5th-generation tensor cores: the
+// verification launches and sparse_decode_attn's cluster launch.
+template <int NT, bool VERIFY>
+__global__ void __launch_bounds__(kTcThreads, 2)
+    sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                          const __grid_constant__ AttnParams p)
+{
+    attn_tc_cta<NT, VERIFY>(&kmap, &vmap, p, static_cast<int>(blockIdx.y));
 }
 
 // ---------------------------------------------------------------- split-KV decode, workspace merge
@@ -1050,19 +1066,21 @@ size_t split_workspace_bytes(long long pairs, int G, int S)
     return counters + static_cast<size_t>(pairs) * S * part * sizeof(float);
 }
 
-template <int NT, bool VERIFY>
+// TC: the tensor-memory kernel (sparse_attn_tc_kernel, SPARSE_ATTN_TENSOR_MEMORY) instead
+// of the mma.sync one.
+template <int NT, bool VERIFY, bool TC>
 int launch(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, int S, long long units,
            int device, cudaStream_t stream)
 {
-    auto kern = sparse_attn_kernel<NT, VERIFY>;
-    const int smem = (VERIFY ? kSmemVerify : kSmemDecode) + 1024;
+    auto kern = TC ? sparse_attn_tc_kernel<NT, VERIFY> : sparse_attn_kernel<NT, VERIFY>;
+    const int smem = TC ? kTcSmem : (VERIFY ? kSmemVerify : kSmemDecode) + 1024;
     static int configured[64];
     int rc = sp_host::configure_kernel(reinterpret_cast<const void *>(kern), smem, device, configured);
     if (rc != SPARSE_OK)
         return rc;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(S), static_cast<unsigned>(units), 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(TC ? kTcThreads : kThreads, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -1113,7 +1131,7 @@ int decode_check(const uint16_t *Q, const uint16_t *k_base, const uint16_t *v_ba
     if (static_cast<long long>(B) * H_kv > 65535)
         return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn: B*H_kv=%lld > 65535",
                     static_cast<long long>(B) * H_kv);
-    if ((flags & ~(SPARSE_ATTN_BLOCKS_READY | SPARSE_ATTN_STREAM_K)) != 0u)
+    if ((flags & ~(SPARSE_ATTN_BLOCKS_READY | SPARSE_ATTN_STREAM_K | SPARSE_ATTN_TENSOR_MEMORY)) != 0u)
         return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn: unknown flags 0x%x", flags);
     if (n_split < 0)
         return fail(SPARSE_ERR_INVALID_ARG, "sparse_decode_attn: n_split < 0");
@@ -1132,6 +1150,10 @@ int decode_impl(const uint16_t *Q, const uint16_t *k_base, const uint16_t *v_bas
                           O, n_split, flags, timeout_ns);
     if (rc != SPARSE_OK)
         return rc;
+    const bool tensor_memory = (flags & SPARSE_ATTN_TENSOR_MEMORY) != 0u;
+    if (tensor_memory && workspace != nullptr)
+        return fail(SPARSE_ERR_INVALID_ARG,
+                    "sparse_decode_attn: SPARSE_ATTN_TENSOR_MEMORY runs the cluster path: pass no workspace");
     const int G = H_q / H_kv;
     const long long pairs = static_cast<long long>(B) * H_kv;
     sp_host::DeviceInfo dev;
@@ -1220,8 +1242,11 @@ int decode_impl(const uint16_t *Q, const uint16_t *k_base, const uint16_t *v_bas
         return rc;
     if ((rc = sp_host::make_kv_tensor_map(&vm, v_base, pair_stride, pairs)) != SPARSE_OK)
         return rc;
-    return G <= 8 ? launch<1, false>(p, km, vm, S, pairs, dev.device, st)
-                  : launch<2, false>(p, km, vm, S, pairs, dev.device, st);
+    if (tensor_memory)
+        return G <= 8 ? launch<1, false, true>(p, km, vm, S, pairs, dev.device, st)
+                      : launch<2, false, true>(p, km, vm, S, pairs, dev.device, st);
+    return G <= 8 ? launch<1, false, false>(p, km, vm, S, pairs, dev.device, st)
+                  : launch<2, false, false>(p, km, vm, S, pairs, dev.device, st);
 }
 
 }  // namespace
@@ -1316,6 +1341,9 @@ extern "C" SPARSE_API int sparse_decode_attn_noalloc(const uint16_t *Q, const ui
         return rc;
     if (H_q / H_kv > 8)
         return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn_noalloc: G=%d > 8", H_q / H_kv);
+    if ((flags & SPARSE_ATTN_TENSOR_MEMORY) != 0u)
+        return fail(SPARSE_ERR_INVALID_ARG,
+                    "sparse_decode_attn_noalloc: SPARSE_ATTN_TENSOR_MEMORY runs the cluster path, not this one");
     sp_host::DeviceInfo dev;
     if ((rc = sp_host::device_info(&dev)) != SPARSE_OK)
         return rc;
@@ -1373,7 +1401,7 @@ static int verify_impl(const char *name, unsigned mode, const uint16_t *Q, const
 {
     using sp_host::aligned16;
     using sp_host::fail;
-    if ((flags & ~SPARSE_ATTN_BLOCKS_READY) != 0u)
+    if ((flags & ~(SPARSE_ATTN_BLOCKS_READY | SPARSE_ATTN_TENSOR_MEMORY)) != 0u)
         return fail(SPARSE_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags);
     if (!Q || !k_cache || !v_cache || !seq_len || !O || (n_sel > 0 && !idx_q))
         return fail(SPARSE_ERR_INVALID_ARG, "%s: null pointer", name);
@@ -1429,8 +1457,11 @@ static int verify_impl(const char *name, unsigned mode, const uint16_t *Q, const
     p.flags = mode | flags;
     p.scale_log2 = scale_log2_of(scale);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return C * G <= 8 ? launch<1, true>(p, km, vm, S, units, dev.device, st)
-                      : launch<2, true>(p, km, vm, S, units, dev.device, st);
+    if ((flags & SPARSE_ATTN_TENSOR_MEMORY) != 0u)
+        return C * G <= 8 ? launch<1, true, true>(p, km, vm, S, units, dev.device, st)
+                          : launch<2, true, true>(p, km, vm, S, units, dev.device, st);
+    return C * G <= 8 ? launch<1, true, false>(p, km, vm, S, units, dev.device, st)
+                      : launch<2, true, false>(p, km, vm, S, units, dev.device, st);
 }
 
 }  // namespace

@@ -245,6 +245,22 @@ SPARSE_API int sparse_select_topk_heads(const uint16_t *Q, const float *ktil, co
 #define SPARSE_ATTN_BLOCKS_READY 1u
 /* Use the stream-K path whenever a workspace is given (see `workspace`). */
 #define SPARSE_ATTN_STREAM_K 2u
+/*
+ * Run both contractions of the cluster path on the 5th-generation tensor cores:
+ * S^T = K Q^T and O^T += V^T P^T as tcgen05.mma (bf16 operands in the 128-byte
+ * swizzled shared-memory tiles the TMA ring holds, f32 accumulators in tensor memory,
+ * one issuing thread), the softmax in 4 warps that read S^T from tensor memory and
+ * write P to shared memory, the row max updated lazily (O rescaled in tensor memory
+ * only when a row's max grows by more than 2^8).  Without it the contractions are
+ * warp-level mma.sync with the accumulators in registers.  Same results up to
+ * rounding; it runs the cluster path only, so it may not be combined with a workspace
+ * (SPARSE_ERR_INVALID_ARG).  On these memory-bound shapes (at most 16 query rows a
+ * pair) it is measured slower: every ring stage stays held while its product goes
+ * through the issuing thread, tensor memory, the softmax warps and back, and with
+ * three stages per CTA that hold time bounds the bandwidth.  The verification calls
+ * take the same flag.
+ */
+#define SPARSE_ATTN_TENSOR_MEMORY 16u
 
 SPARSE_API int sparse_decode_attn(const uint16_t *Q, const uint16_t *k_base,
                                   const uint16_t *v_base, long long pair_stride_tokens,
@@ -376,8 +392,9 @@ SPARSE_API int sparse_decode_attn_forecast(const uint16_t *Q, const uint16_t *k_
  *   blocks_loaded  optional int64 device counter: += |U| for every group (the blocks
  *            this call streams from HBM).  Without grouping the count would be
  *            sum_q |I_q ∪ W|.
- *   flags    0 or SPARSE_ATTN_BLOCKS_READY: the caller promises that idx_q, seq_len and
- *            the K/V rows are not written by the kernel preceding this one on the
+ *   flags    SPARSE_ATTN_TENSOR_MEMORY: the contractions on tcgen05 (as for
+ *            sparse_decode_attn).  SPARSE_ATTN_BLOCKS_READY: the caller promises that
+ *            idx_q, seq_len and the K/V rows are not written by the kernel preceding this one on the
  *            stream (e.g. the lists of a reuse layer, routed layers earlier; the
  *            launch-order rule of sparse_decode_attn), so the union is built and the
  *            blocks stream while that kernel drains; only Q and the outputs wait for

@@ -102,6 +102,14 @@ def test_decode_rejects_bad_arguments(lib):
     assert f(*bad) == binding.SPARSE_ERR_INVALID_ARG
     ex = lib.sparse_decode_attn_ex
     assert ex(*args[:19], None, 1, 0, None, None) == binding.SPARSE_ERR_INVALID_ARG
+    bad = list(args)
+    bad[16], bad[17], bad[18] = binding.SPARSE_ATTN_TENSOR_MEMORY, FAKE, 1 << 20   # tensor memory + workspace
+    assert f(*bad) == binding.SPARSE_ERR_INVALID_ARG
+    bad = list(args)
+    bad[16] = 64                                  # an unknown flag bit
+    assert f(*bad) == binding.SPARSE_ERR_INVALID_ARG
+    na = lib.sparse_decode_attn_noalloc
+    assert na(*args[:16], binding.SPARSE_ATTN_TENSOR_MEMORY, None, None) == binding.SPARSE_ERR_INVALID_ARG
 
 
 def test_verify_rejects_bad_arguments(lib):

@@ -232,15 +232,17 @@ def test_select_few_blocks_takes_all(lens_b):
 # ----------------------------------------------------------------------------- decode attention
 
 
-PATHS = ("cluster", "split", "stream_k")
+# "tmem": the cluster path with SPARSE_ATTN_TENSOR_MEMORY (tcgen05.mma, tensor-memory
+# accumulators) instead of mma.sync
+PATHS = ("cluster", "split", "stream_k", "tmem")
 
 
 def _decode_direct(B, H_q, H_kv, T_cap, lens_b, k_cap, seed, n_split=0, idx_np=None, cnt_np=None,
                    path="cluster"):
     """sparse_decode_attn on given (or random distinct) block lists vs oracle.attn.
     ``path``: "cluster" (no workspace), "split" (workspace: per-pair slices merged by the
-    last CTA) or "stream_k" (workspace and SPARSE_ATTN_STREAM_K); with a workspace the
-    arrival counters must end at zero."""
+    last CTA), "stream_k" (workspace and SPARSE_ATTN_STREAM_K) or "tmem" (no workspace,
+    SPARSE_ATTN_TENSOR_MEMORY); with a workspace the arrival counters must end at zero."""
     G = H_q // H_kv
     P = B * H_kv
     rng = np.random.default_rng(seed)
@@ -260,11 +262,11 @@ def _decode_direct(B, H_q, H_kv, T_cap, lens_b, k_cap, seed, n_split=0, idx_np=N
     lse = torch.zeros((B, H_q), dtype=torch.float32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     assert path in PATHS
-    ws = binding.decode_workspace(B, H_q, H_kv, k_cap, n_split) if path != "cluster" else None
+    ws = binding.decode_workspace(B, H_q, H_kv, k_cap, n_split) if path in ("split", "stream_k") else None
+    flags = {"stream_k": binding.SPARSE_ATTN_STREAM_K, "tmem": binding.SPARSE_ATTN_TENSOR_MEMORY}.get(path, 0)
     binding.sparse_decode_attn(Q, K, V, torch.from_numpy(idx_np).cuda().view(B, H_kv, k_cap),
                                torch.from_numpy(cnt_np).cuda().view(B, H_kv), _seq(lens_b), O, lse,
-                               n_split=n_split, workspace=ws, status=status,
-                               flags=binding.SPARSE_ATTN_STREAM_K if path == "stream_k" else 0)
+                               n_split=n_split, workspace=ws, status=status, flags=flags)
     torch.cuda.synchronize()
     assert status.item() == 0
     if ws is not None:
@@ -284,7 +286,8 @@ def test_decode_attn_matches_oracle_group_sizes(H_q, H_kv, path):
     _check_lse(lse, lref.reshape(2, H_q))
 
 
-@pytest.mark.parametrize("path,splits", [("cluster", (1, 2, 4, 8)), ("split", (1, 2, 3, 4, 8, 17, 64))])
+@pytest.mark.parametrize("path,splits", [("cluster", (1, 2, 4, 8)), ("split", (1, 2, 3, 4, 8, 17, 64)),
+                                         ("tmem", (1, 2, 4, 8))])
 def test_decode_attn_split_invariance(path, splits):
     outs = {}
     for n_split in splits:
@@ -353,7 +356,8 @@ def test_decode_attn_paths_agree_and_are_deterministic():
         assert torch.equal(b, c), f"{path} is not deterministic"
 
 
-def test_decode_attn_empty_and_tiny_sets():
+@pytest.mark.parametrize("path", ["cluster", "tmem"])
+def test_decode_attn_empty_and_tiny_sets(path):
     B, H_q, H_kv, T_cap, k_cap = 3, 8, 2, 4 * BLK, 5
     P = B * H_kv
     idx_np = np.full((P, k_cap), -1, np.int32)
@@ -362,7 +366,7 @@ def test_decode_attn_empty_and_tiny_sets():
     idx_np[2, :2], cnt_np[2] = [3, 1], 2
     idx_np[3, :4], cnt_np[3] = [0, 1, 2, 3], 4
     O, lse, Oref, lref = _decode_direct(B, H_q, H_kv, T_cap, [4 * BLK, 1, 3 * BLK + 7], k_cap, 5,
-                                        idx_np=idx_np, cnt_np=cnt_np)
+                                        idx_np=idx_np, cnt_np=cnt_np, path=path)
     assert_attn_close(O, Oref.reshape(B, H_q, D))
     assert not O[0, :4].any()                            # pair 0: empty set -> zeros
     assert torch.isneginf(lse[0, :4]).all()
@@ -375,10 +379,50 @@ def test_decode_attn_is_deterministic():
     assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("path", ["cluster", "split"])
+@pytest.mark.parametrize("order", ["rising", "falling", "mixed"])
+@pytest.mark.parametrize("n_split", [1, 2])
+def test_decode_attn_tensor_memory_rescales_when_the_max_jumps(order, n_split):
+    """Blocks whose keys are scaled by 1, 3, 9, 27: block maxima differ by far more than
+    the 2^8 the tensor-memory path lets a row's running max lag, so it must rescale O
+    in tensor memory (rising order), never rescale (falling), or both (mixed); the
+    output equals the oracle and the mma.sync path."""
+    B, H_q, H_kv, nb = 1, 8, 1, 8
+    T_cap = nb * BLK
+    K = wl.randn_bf16((B, H_kv, T_cap, D), 71, "cuda").float()
+    scale_of = {"rising": [1, 1, 3, 3, 9, 9, 27, 27], "falling": [27, 27, 9, 9, 3, 3, 1, 1],
+                "mixed": [1, 27, 1, 9, 3, 27, 1, 3]}[order]
+    for j, f in enumerate(scale_of):
+        K[:, :, j * BLK:(j + 1) * BLK] *= f
+    K = K.to(torch.bfloat16)
+    V = wl.randn_bf16((B, H_kv, T_cap, D), 72, "cuda")
+    Q = wl.randn_bf16((B, H_q, D), 73, "cuda")
+    idx_np = np.arange(nb, dtype=np.int32).reshape(1, nb)
+    cnt_np = np.array([nb], np.int32)
+    idx = torch.from_numpy(idx_np).cuda().view(B, H_kv, nb)
+    cnt = torch.from_numpy(cnt_np).cuda().view(B, H_kv)
+    outs = {}
+    for path, flags in (("cluster", 0), ("tmem", binding.SPARSE_ATTN_TENSOR_MEMORY)):
+        O = torch.zeros((B, H_q, D), dtype=torch.bfloat16, device="cuda")
+        lse = torch.zeros((B, H_q), dtype=torch.float32, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        binding.sparse_decode_attn(Q, K, V, idx, cnt, _seq([T_cap]), O, lse, n_split=n_split, flags=flags,
+                                   status=status)
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        outs[path] = (O, lse)
+    Oref, lref = oracle.attn(bits(Q).reshape(1, H_q, D), bits(K).reshape(1, T_cap, D), bits(V).reshape(1, T_cap, D),
+                             idx_np, cnt_np, np.array([T_cap]))
+    for path, (O, lse) in outs.items():
+        assert_attn_close(O, Oref.reshape(B, H_q, D), f"{order} {path}")
+        _check_lse(lse, lref.reshape(B, H_q))
+    assert (outs["tmem"][0].float() - outs["cluster"][0].float()).abs().max().item() <= 2 ** -6
+
+
+@pytest.mark.parametrize("path", ["cluster", "split", "tmem"])
 def test_decode_attn_reports_bad_block_ids_without_faulting(path):
     B, H_q, H_kv, T_cap, k_cap = 1, 8, 2, 8 * BLK, 3
     ws = binding.decode_workspace(B, H_q, H_kv, k_cap, 2) if path == "split" else None
+    flags = binding.SPARSE_ATTN_TENSOR_MEMORY if path == "tmem" else 0
     K = wl.randn_bf16((B, H_kv, T_cap, D), 1, "cuda")
     Q = wl.randn_bf16((B, H_q, D), 2, "cuda")
     idx = torch.tensor([[[0, 1 << 20, 2], [3, -5, 4]]], dtype=torch.int32, device="cuda")
@@ -386,7 +430,7 @@ def test_decode_attn_reports_bad_block_ids_without_faulting(path):
     O = torch.zeros((B, H_q, D), dtype=torch.bfloat16, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     binding.sparse_decode_attn(Q, K, K, idx, cnt, _seq([T_cap]), O, status=status, workspace=ws,
-                               n_split=2 if ws is not None else 0)
+                               n_split=2 if ws is not None else 0, flags=flags)
     torch.cuda.synchronize()
     assert status.item() == binding.SPARSE_ERR_BAD_INDEX
     good_idx = torch.tensor([[[0, 2, 2], [3, 4, 4]]], dtype=torch.int32, device="cuda")
@@ -567,22 +611,26 @@ def test_decode_128k_layer_all_pairs_at_full_size():
 # ----------------------------------------------------------------------------- grouped verification
 
 
-def _verify(sh, n_split=0, shared=False):
+def _verify(sh, n_split=0, shared=False, flags=0):
     inp = wl.verify_inputs(sh, device="cuda")
     O = torch.zeros((sh.B, sh.N_q, sh.H_q, D), dtype=torch.bfloat16, device="cuda")
     loaded = torch.zeros(1, dtype=torch.int64, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     binding.sparse_verify_attn_grouped(inp["Q"], inp["K"], inp["V"], inp["I"], sh.C, sh.window_blocks,
                                        inp["seq_len"], O, blocks_loaded=loaded, n_split=n_split, status=status,
-                                       shared=shared)
+                                       shared=shared, flags=flags)
     torch.cuda.synchronize()
     assert status.item() == 0
     return inp, O, int(loaded.item())
 
 
-def test_verify_64k_workload_matches_oracle_and_saves_loads():
+TM = binding.SPARSE_ATTN_TENSOR_MEMORY
+
+
+@pytest.mark.parametrize("flags", [0, TM])
+def test_verify_64k_workload_matches_oracle_and_saves_loads(flags):
     sh = wl.VERIFY_64K
-    inp, O, loaded = _verify(sh)
+    inp, O, loaded = _verify(sh, flags=flags)
     Oref, union, per_query = oracle.verify(bits(inp["Q"]), bits(inp["K"]), bits(inp["V"]), inp["I"].cpu().numpy(),
                                            sh.C, sh.window_blocks, [sh.T] * sh.B)
     assert_attn_close(O, Oref)
@@ -613,41 +661,45 @@ def test_verify_equals_per_query_decode():
         assert (Od.float() - O[:, q].float()).abs().max().item() <= 2 ** -7
 
 
+@pytest.mark.parametrize("flags", [0, TM])
 @pytest.mark.parametrize("n_split", [1, 2, 8])
-def test_verify_split_invariance(n_split):
+def test_verify_split_invariance(n_split, flags):
     sh = wl.VerifyShape("split", B=1, H_q=16, H_kv=4, T=64 * BLK, N_q=8, n_sel=16, gamma=0.75,
                         window_tokens=8 * BLK, C=4, seed=33)
-    inp, O, loaded = _verify(sh, n_split=n_split)
+    inp, O, loaded = _verify(sh, n_split=n_split, flags=flags)
     Oref, union, _ = oracle.verify(bits(inp["Q"]), bits(inp["K"]), bits(inp["V"]), inp["I"].cpu().numpy(), sh.C,
                                    sh.window_blocks, [sh.T] * sh.B)
     assert_attn_close(O, Oref)
     assert loaded == union
 
 
-def test_verify_shared_layout_64k_workload_matches_oracle():
+@pytest.mark.parametrize("flags", [0, TM])
+def test_verify_shared_layout_64k_workload_matches_oracle(flags):
     """SSV mode B on the 64K verification workload: every query over its group's first
     query's layout; each group loads n_sel + window blocks."""
     sh = wl.VERIFY_64K
-    inp, O, loaded = _verify(sh, shared=True)
+    inp, O, loaded = _verify(sh, shared=True, flags=flags)
     Oref, union, per_query = oracle.verify(bits(inp["Q"]), bits(inp["K"]), bits(inp["V"]), inp["I"].cpu().numpy(),
                                            sh.C, sh.window_blocks, [sh.T] * sh.B, shared=True)
     assert_attn_close(O, Oref)
     assert loaded == union == sh.B * sh.H_kv * (sh.N_q // sh.C) * (sh.n_sel + sh.window_blocks)
 
 
+@pytest.mark.parametrize("flags", [0, TM])
 @pytest.mark.parametrize("n_split,C", [(1, 4), (2, 3), (8, 4), (0, 1)])
-def test_verify_shared_layout_ragged_groups(n_split, C):
+def test_verify_shared_layout_ragged_groups(n_split, C, flags):
     sh = wl.VerifyShape("shared", B=2, H_q=8, H_kv=2, T=40 * BLK + 17, N_q=7, n_sel=6, gamma=0.5,
                         window_tokens=2 * BLK, C=C, seed=35)
-    inp, O, loaded = _verify(sh, n_split=n_split, shared=True)
+    inp, O, loaded = _verify(sh, n_split=n_split, shared=True, flags=flags)
     Oref, union, _ = oracle.verify(bits(inp["Q"]), bits(inp["K"]), bits(inp["V"]), inp["I"].cpu().numpy(), sh.C,
                                    sh.window_blocks, [sh.T] * sh.B, shared=True)
     assert_attn_close(O, Oref)
     assert loaded == union
 
 
+@pytest.mark.parametrize("tm", [0, TM])
 @pytest.mark.parametrize("shared", [False, True])
-def test_verify_chain_with_blocks_ready(shared):
+def test_verify_chain_with_blocks_ready(shared, tm):
     """A chain of verification launches on one stream where each launch's Q is the
     previous launch's O: with SPARSE_ATTN_BLOCKS_READY the union and the K/V stream start
     early but Q still waits, so the chain equals the one without the flag bit for bit,
@@ -665,7 +717,7 @@ def test_verify_chain_with_blocks_ready(shared):
         for l in range(4):
             binding.sparse_verify_attn_grouped(outs[l], inp["K"], inp["V"], inp["I"], sh.C, sh.window_blocks,
                                                inp["seq_len"], outs[l + 1], status=status, shared=shared,
-                                               flags=flags)
+                                               flags=flags | tm)
         torch.cuda.synchronize()
         return outs[1:]
 
