@@ -95,7 +95,7 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
 
 
-ATTN_SOURCES = ("sparse_attn.cu", "attn_core.cuh", "common.cuh")
+ATTN_SOURCES = ("sparse_attn.cu", "attn_core.cuh", "attn_tc.cuh", "common.cuh")
 FUSED_SOURCES = ("forecast.cu", "attn_core.cuh", "select_core.cuh", "select_layout.cuh", "common.cuh")
 
 
