@@ -78,9 +78,7 @@ __global__ void __launch_bounds__(kFThreads, 2)
     const uint32_t rank = blockIdx.x;   // == %cluster_ctarank
     const int pair = blockIdx.y;
     const int b = pair / p.H_kv, g = pair % p.H_kv;
-    const int per = (p.k_tot + static_cast<int>(S) - 1) / static_cast<int>(S);
-    const int i0 = min(p.k_tot, static_cast<int>(rank) * per);
-    const int cap = min(p.k_tot, i0 + per) - i0;
+    const int per = fused_slice_max(p.k_tot, static_cast<int>(S), SELG);   // the list words' layout
     int *lslot = reinterpret_cast<int *>(base + fused_off_slice());
     int *llog = lslot + fused_per_pad(per);
     uint32_t *keys = reinterpret_cast<uint32_t *>(base + fused_off_keys(per));
@@ -98,9 +96,13 @@ __global__ void __launch_bounds__(kFThreads, 2)
     const bool take_all = max(0, nb - p.n_local - p.n_init) <= p.k_sel;
     const bool score = do_sel && !take_all;
     // the top-k by CTA 0's consumer and selector warps together (else its selector warp
-    // alone, while the consumers attend)
-    const bool sel_group = SELG && rank == 0 && score && p.k_sel >= 1 &&
-                           topk_cta_regs_fits<kSelKPT>(nb - p.n_local - p.n_init, kSelThreads);
+    // alone, while the consumers attend); then CTA 0 attends over nothing and the other
+    // CTAs share this layer's list (the same decision in every CTA of the cluster)
+    const bool group = SELG && score && p.k_sel >= 1 &&
+                       topk_cta_regs_fits<kSelKPT>(nb - p.n_local - p.n_init, kSelThreads);
+    const bool sel_group = group && rank == 0;
+    int i0, cap;
+    fused_slice(p.k_tot, static_cast<int>(S), static_cast<int>(rank), group, &i0, &cap);
     // CTA r streams its slice of the candidates [n_init, nb - n_local) only: init and
     // local blocks are never scored (and the local ones may be the ones an append writes)
     const int n_cand = max(0, nb - p.n_local - p.n_init);
@@ -494,7 +496,7 @@ extern "C" SPARSE_API int sparse_decode_attn_forecast(
     if ((rc = choose_split(n_split, pairs, k_tot, dev.sm_count, &S, 16)) != SPARSE_OK)
         return rc;
     if (S > kMaxSplit && G <= 8 &&
-        !wide_clusters_fit<1>(fused_smem_bytes((k_tot + S - 1) / S, N_cap), pairs, dev.device,
+        !wide_clusters_fit<1>(fused_smem_bytes(fused_slice_max(k_tot, S, true), N_cap), pairs, dev.device,
                               static_cast<cudaStream_t>(stream))) {
         if (n_split != 0)
             return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn_forecast: clusters of 16 CTAs do not fit");
@@ -505,7 +507,12 @@ extern "C" SPARSE_API int sparse_decode_attn_forecast(
             return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn_forecast: n_split = 16 needs G <= 8");
         S = kMaxSplit;
     }
-    const int per = (k_tot + S - 1) / S;
+    // few blocks per CTA: the layer's attention is short, so the top-k is on the path to
+    // the next layer and CTA 0's consumers help with it (and leave the layer's list to the
+    // other CTAs); many blocks: the selector warp alone, hidden behind the attention
+    const bool sel_group = (k_tot + S - 1) / S <= kSelBlockMaxPer && G <= 8;
+    const bool group_kernel = S > kMaxSplit || (G <= 8 && sel_group);   // an instantiation with SELG
+    const int per = fused_slice_max(k_tot, S, group_kernel);
     if (per > kMaxListCta)
         return fail(SPARSE_ERR_UNSUPPORTED, "sparse_decode_attn_forecast: %d blocks per CTA (at most %d)", per,
                     kMaxListCta);
@@ -538,10 +545,6 @@ extern "C" SPARSE_API int sparse_decode_attn_forecast(
     p.n_local = n_local;
     p.k_sel = k;
     p.k_tot_next = k_tot_next;
-    // few blocks per CTA: the layer's attention is short, so the top-k is on the path to
-    // the next layer and CTA 0's consumers help with it before they attend; many
-    // blocks: the selector warp alone, hidden behind the attention
-    const bool sel_group = per <= kSelBlockMaxPer && G <= 8;
     CUtensorMap km, vm;
     if ((rc = sp_host::make_kv_tensor_map(&km, k_cache, T_cap, pairs)) != SPARSE_OK)
         return rc;

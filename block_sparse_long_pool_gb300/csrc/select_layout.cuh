@@ -42,6 +42,40 @@ inline size_t fused_smem_bytes(int per, int N_cap)
     return static_cast<size_t>(fused_off_keys(per)) + static_cast<size_t>(N_cap) * 4 + 1024;
 }
 
+// The slice [i0, i0 + cap) of the k_tot-long block list that CTA `rank` of a fused layer
+// attends over.  With the group top-k (`cta0_free`: CTA 0's consumer warps take the next
+// layer's top-k first) CTA 0 attends over nothing and the other S - 1 CTAs share the
+// list, the first k_tot % (S - 1) of them one block more; otherwise CTA r takes entries
+// [r * ceil(k_tot / S), ...).
+__host__ __device__ inline void fused_slice(int k_tot, int S, int rank, bool cta0_free, int *i0, int *cap)
+{
+    if (cta0_free && S > 1) {
+        if (rank == 0) {
+            *i0 = 0;
+            *cap = 0;
+            return;
+        }
+        const int n = S - 1, r = rank - 1, base = k_tot / n, rem = k_tot % n;
+        *i0 = r * base + (r < rem ? r : rem);
+        *cap = base + (r < rem ? 1 : 0);
+        return;
+    }
+    const int per = (k_tot + S - 1) / S;
+    *i0 = rank * per < k_tot ? rank * per : k_tot;
+    *cap = (*i0 + per < k_tot ? *i0 + per : k_tot) - *i0;
+}
+
+// The longest slice either way, for a kernel that may free CTA 0 (`group`); the shared
+// memory layout is sized for it.
+__host__ __device__ inline int fused_slice_max(int k_tot, int S, bool group)
+{
+    const int per = (k_tot + S - 1) / S;
+    if (!group || S < 2)
+        return per;
+    const int per1 = (k_tot + S - 2) / (S - 1);
+    return per1 > per ? per1 : per;
+}
+
 // The group top-k of CTA 0 (topk_forecast_cta): its 4 consumer warps and the selector
 // warp, on named barrier 2, with up to kSelKPT candidates per thread (2720 in all), its
 // scratch over the coarse histogram and the threshold list.
