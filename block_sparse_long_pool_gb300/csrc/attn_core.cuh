@@ -505,11 +505,17 @@ __device__ __forceinline__ int producer_fetch_slice(const AttnParams &p, int pai
 //     wait can tell from progress.
 //   pull: every CTA waits for all, then merges the S states for its slice of the dims
 //     by reading its peers' shared memory, and all wait again before leaving.
-constexpr int kPushRecvOff = 48 * 1024;   // the leader's slots: past the warp and CTA states
 constexpr int kCtrlGoBar = 10;            // ctrl[10..11]: "the leader's slots are free" (every CTA)
 constexpr int kCtrlRecvBar = 12;          // ctrl[12..13]: the peers' states have landed (leader)
-static_assert(kPushRecvOff >= (kConsumerWarps * 16 * kWoStride + 3 * kConsumerWarps * 16 + 16 * kD + 2 * 16 + 4) * 4,
-              "the slots lie past the warp and CTA states");
+
+// The leader's slots: in its ring past the merge scratch (the 4 warp states, the warp
+// weights and the CTA state, with the abort words), on a 1 KB boundary.
+template <int NT>
+__host__ __device__ constexpr int push_recv_off()
+{
+    return ((kConsumerWarps * 8 * NT * kWoStride + 3 * kConsumerWarps * 8 * NT + 8 * NT * kD + 2 * 8 * NT + 4) * 4 +
+            1023) / 1024 * 1024;
+}
 
 template <int NT>
 __host__ __device__ constexpr int push_slot_floats()
@@ -519,11 +525,16 @@ __host__ __device__ constexpr int push_slot_floats()
 static_assert(push_slot_floats<1>() % 4 == 0 && push_slot_floats<2>() % 4 == 0,
               "each slot starts 16-byte aligned, so its rows take 16-byte loads");
 
+// Whether the push form runs: at most kMaxSplit CTAs (beyond, one leader merging every
+// state for all 128 dims takes longer than the pull form, where each CTA merges its own
+// 128 / S dims: measured at 16 CTAs) and the S - 1 slots fit in the leader's ring.
 template <int NT>
 __host__ __device__ constexpr bool merge_pushes(uint32_t S)
 {
-    return S > 1 && kPushRecvOff + (S - 1) * push_slot_floats<NT>() * 4 <= kStages * kStageBytes;
+    return S > 1 && S <= static_cast<uint32_t>(kMaxSplit) &&
+           push_recv_off<NT>() + static_cast<int>(S - 1) * push_slot_floats<NT>() * 4 <= kStages * kStageBytes;
 }
+static_assert(merge_pushes<1>(8) && merge_pushes<2>(4), "the push merge serves the fused layer's clusters");
 
 // Thread 0 at kernel start, before fence_barrier_init and the cluster arrive.
 __device__ __forceinline__ void merge_barriers_init(uint32_t ctrl_s, uint32_t S, int nthreads)
@@ -570,13 +581,23 @@ __device__ __forceinline__ float *merge_cta_state(uint8_t *base)
     return reinterpret_cast<float *>(base) + kConsumerWarps * ROWS * kWoStride + 3 * kConsumerWarps * ROWS;
 }
 
+// The leader (thread 0 of CTA 0) tells each peer that its ring is consumed: the peers
+// may fill its slots.  Once per launch.
+__device__ __forceinline__ void merge_send_go(uint32_t ctrl_s, uint32_t S)
+{
+    for (uint32_t r = 1; r < S; ++r)
+        mbar_arrive_cluster(dsmem_addr(ctrl_s + 4 * kCtrlGoBar, r));
+}
+
 // `cta_state_ready`: the caller has written the CTA state (merge_cta_state) itself, and
-// `st` is not read.
+// `st` is not read.  `go_sent`: the leader's thread 0 already called merge_send_go (its
+// ring was free early).
 template <int NT, bool VERIFY, int MAXS = kMaxSplit>
 __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uint8_t *base, bool aborted,
                                                     const AttnParams &p, int b, int g, int q0, int rows_valid,
                                                     uint32_t rank, uint32_t S, int nthreads, uint32_t ctrl_s,
-                                                    bool wait_cluster, bool allow_push, bool cta_state_ready = false)
+                                                    bool wait_cluster, bool allow_push, bool cta_state_ready = false,
+                                                    bool go_sent = false)
 {
     constexpr int ROWS = 8 * NT;
     constexpr int SLOT = push_slot_floats<NT>();
@@ -594,9 +615,8 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
     const uint32_t bar_go = ctrl_s + 4 * kCtrlGoBar, bar_recv = ctrl_s + 4 * kCtrlRecvBar;
     if (wait_cluster)
         cluster_wait();   // every CTA's merge barriers are initialised
-    if (push && rank == 0 && tid == 0)
-        for (uint32_t r = 1; r < S; ++r)   // this CTA's ring is consumed: the peers may fill its slots
-            mbar_arrive_cluster(dsmem_addr(bar_go, r));
+    if (push && rank == 0 && tid == 0 && !go_sent)
+        merge_send_go(ctrl_s, S);
     if (!cta_state_ready && warp < kConsumerWarps)
         store_warp_state<NT>(st, wo, wm, wl, warp, lane);
     if (tid == 0)
@@ -607,7 +627,7 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
         __syncthreads();   // the CTA state (co, cm, cl, cabort) is complete
     }
     if (push) {
-        const float *slots = reinterpret_cast<const float *>(base + kPushRecvOff);   // [S - 1][SLOT]
+        const float *slots = reinterpret_cast<const float *>(base + push_recv_off<NT>());   // [S - 1][SLOT]
         if (rank != 0) {
             // a peer: copy the CTA state, contiguous from co, into slot rank - 1 of the leader
             const bool go = __all_sync(0xffffffffu, mbar_wait_cluster(bar_go, 0, kMergeWaitNs));
@@ -616,7 +636,7 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
                     report(p.status, SPARSE_ERR_TIMEOUT);
                 return;
             }
-            const uint32_t dst = dsmem_addr(smem_u32(base + kPushRecvOff) + (rank - 1) * SLOT * 4, 0);
+            const uint32_t dst = dsmem_addr(smem_u32(base + push_recv_off<NT>()) + (rank - 1) * SLOT * 4, 0);
             const float4 *src = reinterpret_cast<const float4 *>(co);
             for (int q4 = tid; q4 < SLOT / 4; q4 += nthreads)
                 dsmem_st_v4(dst + 16 * q4, src[q4]);

@@ -31,8 +31,9 @@
 //   * The dependent launch is allowed at once: a following launch starts streaming its
 //     key slice as SMs free up, and waits for this one before reading what it writes.
 //   * The CTAs' partial softmax states merge by push (cluster_merge_write): CTA 0 tells
-//     the others when its ring is free, they copy their states into it and leave, and
-//     CTA 0 writes O; no cluster-wide barrier at the end of the layer.
+//     the others when its ring is free (with the group top-k, where CTA 0 attends over
+//     nothing, as soon as the scores are in), they copy their states into it and leave,
+//     and CTA 0 writes O; no cluster-wide barrier at the end of the layer.
 #include <string.h>
 
 #include <mutex>
@@ -130,6 +131,7 @@ __global__ void __launch_bounds__(kFThreads, 2)
 
     WarpState<NT> st;
     st.reset();
+    bool go_sent = false;   // thread 0 of CTA 0: the push merge's "go" already sent
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
@@ -284,6 +286,13 @@ __global__ void __launch_bounds__(kFThreads, 2)
         if (sel_group) {
             // CTA 0: once every CTA has scored its slice, the top-k with the selector warp
             const bool ready = __all_sync(0xffffffffu, mbar_wait_cluster(bar_scored, 0, kWaitNs));
+            // every warp of this CTA is past its last key stage and it attends over
+            // nothing: its ring is free, so the peers may push their states into it while
+            // the top-k runs
+            if (ATTN && ready && tid == 0 && merge_pushes<NT>(S)) {
+                merge_send_go(base_s + kOffCtrl, S);
+                go_sent = true;
+            }
             topk_forecast_cta<kSelKPT, kSelThreads / 32>(
                 base_s + fused_off_keys(per), base_s + fused_off_hist(), base_s + fused_off_hist(), nb, p.n_init,
                 p.n_local, p.k_sel, tid, kSelBar, ready, p.idx_next + static_cast<size_t>(pair) * p.k_tot_next,
@@ -340,7 +349,7 @@ __global__ void __launch_bounds__(kFThreads, 2)
     if (ATTN) {
         __syncthreads();
         cluster_merge_write<NT, false, MAXS>(st, base, false, p, b, g, 0, p.G, rank, S, kFThreads,
-                                             base_s + kOffCtrl, false, true);
+                                             base_s + kOffCtrl, false, true, false, go_sent);
     }
 }
 
