@@ -597,7 +597,7 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
                                                     const AttnParams &p, int b, int g, int q0, int rows_valid,
                                                     uint32_t rank, uint32_t S, int nthreads, uint32_t ctrl_s,
                                                     bool wait_cluster, bool allow_push, bool cta_state_ready = false,
-                                                    bool go_sent = false)
+                                                    bool go_sent = false, bool skip0 = false)
 {
     constexpr int ROWS = 8 * NT;
     constexpr int SLOT = push_slot_floats<NT>();
@@ -699,48 +699,45 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
 
     // Peers' CTA states (generic pointers into distributed shared memory).  Every value
     // a thread needs for an output pair is loaded before any is used, so the remote
-    // loads of an item overlap (one round trip).
-    const int Si = static_cast<int>(S);
-    const float *pco[MAXS];
-    const float *pcm[MAXS];
-    const float *pcl[MAXS];
-    int ab[MAXS];
+    // loads of an item overlap (one round trip).  With `skip0` CTA 0 holds no state and
+    // takes no part: the states and the dims are those of CTAs 1 .. S-1.
+    const int c0 = skip0 ? 1 : 0;
+    const int Si = static_cast<int>(S) - c0;
+    // each peer's CTA state as a shared::cluster address (co; cm and cl follow it)
+    uint32_t pst[MAXS];
+    int any_abort = 0;
 #pragma unroll
     for (int c = 0; c < MAXS; ++c) {
-        const unsigned r = c < Si ? static_cast<unsigned>(c) : 0u;
-        pco[c] = static_cast<const float *>(__cluster_map_shared_rank(co, r));
-        pcm[c] = static_cast<const float *>(__cluster_map_shared_rank(cm, r));
-        pcl[c] = static_cast<const float *>(__cluster_map_shared_rank(cl, r));
-        ab[c] = c < Si ? *static_cast<const int *>(__cluster_map_shared_rank(cabort, r)) : 0;
+        const uint32_t r = c < Si ? static_cast<uint32_t>(c + c0) : static_cast<uint32_t>(c0);
+        pst[c] = dsmem_addr(smem_u32(co), r);
+        if (c < Si)
+            any_abort |= static_cast<int>(dsmem_ld_u32(pst[c] + 4u * static_cast<uint32_t>(ROWS * kD + 2 * ROWS)));
     }
-    // CTA `rank` writes dims [rank * 128 / S, (rank + 1) * 128 / S) of every row, four
-    // adjacent dims per item: with up to 16 rows and S >= 4, one item per thread, so the
-    // remote loads of the whole slice are one round trip
-    const int dims_per = kD / Si;
-    const int d0 = static_cast<int>(rank) * dims_per;
-    const int quads_per_row = dims_per / 4;
+    // CTA `rank` writes quads [qa, qb) (four adjacent dims each) of every row: with
+    // every CTA taking part, dims [rank * 128 / S, (rank + 1) * 128 / S); with up to 16
+    // rows and S >= 4, one item per thread, so the remote loads of the whole slice are
+    // one round trip
+    const int me = static_cast<int>(rank) - c0;
+    const int qa = me * (kD / 4) / Si, qb = (me + 1) * (kD / 4) / Si;
+    const int quads_per_row = qb - qa;
     const int n_items = rows_valid * quads_per_row;
     for (int item = tid; item < n_items; item += nthreads) {
         const int row = item / quads_per_row;
-        const int d = d0 + 4 * (item - row * quads_per_row);
+        const int d = 4 * (qa + item - row * quads_per_row);
         float mc[MAXS], lc[MAXS];
         float4 v[MAXS];
 #pragma unroll
         for (int c = 0; c < MAXS; ++c) {
             if (c < Si) {
-                mc[c] = pcm[c][row];
-                lc[c] = pcl[c][row];
-                v[c] = *reinterpret_cast<const float4 *>(pco[c] + row * kD + d);
+                mc[c] = dsmem_ld_f32(pst[c] + 4u * static_cast<uint32_t>(ROWS * kD + row));
+                lc[c] = dsmem_ld_f32(pst[c] + 4u * static_cast<uint32_t>(ROWS * kD + ROWS + row));
+                v[c] = dsmem_ld_v4(pst[c] + 4u * static_cast<uint32_t>(row * kD + d));
             } else {
                 mc[c] = -INFINITY;
                 lc[c] = 0.f;
                 v[c] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
-        int any_abort = 0;
-#pragma unroll
-        for (int c = 0; c < MAXS; ++c)
-            any_abort |= ab[c];
         // any CTA of the unit that failed its ready check leaves the output untouched
         if (any_abort)
             break;
@@ -759,7 +756,7 @@ __device__ __forceinline__ void cluster_merge_write(const WarpState<NT> &st, uin
             o.z = fmaf(f, v[c].z, o.z);
             o.w = fmaf(f, v[c].w, o.w);
         }
-        merge_write_item4<NT, VERIFY>(p, b, g, q0, row, d, M, L, o, rank == 0);
+        merge_write_item4<NT, VERIFY>(p, b, g, q0, row, d, M, L, o, true);   // lse with dim 0
     }
     // peers may still read this CTA's state
     cluster_sync();

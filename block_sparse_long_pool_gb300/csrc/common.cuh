@@ -362,6 +362,16 @@ __device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ float4 dsmem_ld_v4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // ---------------------------------------------------------------- selection keys
 
 // Monotone map of an fp32 score to an unsigned key (larger score -> larger key); -0

@@ -102,6 +102,11 @@ __global__ void __launch_bounds__(kFThreads, 2)
     const bool group = SELG && score && p.k_sel >= 1 &&
                        topk_cta_regs_fits<kSelKPT>(nb - p.n_local - p.n_init, kSelThreads);
     const bool sel_group = group && rank == 0;
+    // ... and with the pull merge CTA 0 (no state of its own) sits the merge out: it
+    // arrives on the merge's first cluster barrier before its top-k, so the other CTAs
+    // merge and write O while it selects
+    const bool skip0 = ATTN && group && !merge_pushes<NT>(S);
+    const bool cta0_out = skip0 && rank == 0;
     int i0, cap;
     fused_slice(p.k_tot, static_cast<int>(S), static_cast<int>(rank), group, &i0, &cap);
     // CTA r streams its slice of the candidates [n_init, nb - n_local) only: init and
@@ -188,6 +193,8 @@ __global__ void __launch_bounds__(kFThreads, 2)
             }
         }
         cluster_wait();
+        if (cta0_out)
+            cluster_arrive();   // the merge's first barrier
     } else if (warp < kConsumerWarps) {
         // ------------------------------------------------------------ consumers
         griddep_wait();   // Q and F may be written by the kernel before this one
@@ -283,6 +290,8 @@ __global__ void __launch_bounds__(kFThreads, 2)
         __syncwarp();
         if (lane == 0)
             mbar_arrive_cluster(dsmem_addr(bar_scored, 0));
+        if (cta0_out)
+            cluster_arrive();   // the merge's first barrier
         if (sel_group) {
             // CTA 0: once every CTA has scored its slice, the top-k with the selector warp
             const bool ready = __all_sync(0xffffffffu, mbar_wait_cluster(bar_scored, 0, kWaitNs));
@@ -321,6 +330,10 @@ __global__ void __launch_bounds__(kFThreads, 2)
         finish_row_sums<NT>(st);
     } else {
         // ------------------------------------------------------------ selector (CTA 0)
+        if (cta0_out) {
+            cluster_wait();
+            cluster_arrive();   // the merge's first barrier
+        }
         if (rank == 0 && do_sel) {
             if (len_bad && lane == 0)
                 report(p.status, SPARSE_ERR_BAD_INDEX);
@@ -342,14 +355,19 @@ __global__ void __launch_bounds__(kFThreads, 2)
                 report(p.status, SPARSE_ERR_TIMEOUT);
             }
         }
-        cluster_wait();
+        if (!cta0_out)
+            cluster_wait();
     }
 
     // ---------------------------------------------------------------- merge
-    if (ATTN) {
+    if (cta0_out) {
+        // the others merge without this CTA; the second barrier: they are done with the cluster
+        cluster_wait();
+        cluster_sync();
+    } else if (ATTN) {
         __syncthreads();
         cluster_merge_write<NT, false, MAXS>(st, base, false, p, b, g, 0, p.G, rank, S, kFThreads,
-                                             base_s + kOffCtrl, false, true, false, go_sent);
+                                             base_s + kOffCtrl, false, true, false, go_sent, skip0);
     }
 }
 
