@@ -360,19 +360,24 @@ __device__ __forceinline__ void topk_range_regs(uint32_t keys_s, int nb, int n_i
 
 // The coarse bin that holds the k-th largest key, from the histogram of key >> 22 at
 // coarse_s (kCoarseBins counts), by one warp: every lane sums its 32 bins [1024 - 32(l+1),
-// 1024 - 32l) read in a rotated order (lane l starts at its bin l, so the 32 lanes hit 32
-// distinct banks), a prefix sum from the top bin finds the lane that holds the k-th key,
-// and that lane alone walks its bins from the top.  Gives the bin (-1 if the histogram
-// counts fewer than k keys), the keys still needed within it and its count, on every lane.
+// 1024 - 32l) with eight 16-byte reads in a rotated order (lane l starts at its chunk
+// l mod 8, so each quarter-warp's reads cover 8 distinct 16-byte bank groups), a prefix
+// sum from the top bin finds the lane that holds the k-th key, and the warp then reads
+// that lane's 32 bins, one a lane, for a second prefix sum that finds the bin.  Gives
+// the bin (-1 if the histogram counts fewer than k keys), the keys still needed within
+// it and its count, on every lane.
 __device__ __forceinline__ void coarse_pick_warp(uint32_t coarse_s, int k, int lane, int &bsel, int &need_new,
                                                  int &cnt)
 {
     constexpr int kPer = kCoarseBins / 32;
+    static_assert(kPer == 32, "one warp, 32 bins a lane");
     const int bin0 = kCoarseBins - kPer * (lane + 1);
     int c = 0;
 #pragma unroll
-    for (int j = 0; j < kPer; ++j)
-        c += static_cast<int>(lds_u32(coarse_s + 4 * (bin0 + ((j + lane) & (kPer - 1)))));
+    for (int j = 0; j < 8; ++j) {
+        const uint4 v = lds_v4(coarse_s + 4u * static_cast<uint32_t>(bin0 + 4 * ((j + lane) & 7)));
+        c += static_cast<int>(v.x + v.y + v.z + v.w);
+    }
     int incl = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -381,33 +386,29 @@ __device__ __forceinline__ void coarse_pick_warp(uint32_t coarse_s, int k, int l
             incl += n;
     }
     const int excl = incl - c;
+    const unsigned hit = __ballot_sync(0xffffffffu, excl < k && k <= incl);
     bsel = -1;
     need_new = 0;
     cnt = 0;
-    if (excl < k && k <= incl) {
-        uint32_t cb[kPer];
-#pragma unroll
-        for (int i = 0; i < kPer; ++i)
-            cb[i] = lds_u32(coarse_s + 4 * (bin0 + i));
-        int acc = excl;
-#pragma unroll
-        for (int i = kPer - 1; i >= 0; --i) {
-            const int ci = static_cast<int>(cb[i]);
-            if (bsel < 0 && acc + ci >= k) {
-                bsel = bin0 + i;
-                need_new = k - acc;
-                cnt = ci;
-            }
-            acc += ci;
-        }
-    }
-    const unsigned hit = __ballot_sync(0xffffffffu, bsel >= 0);
-    const int src = hit != 0u ? __ffs(hit) - 1 : 0;
-    bsel = __shfl_sync(0xffffffffu, bsel, src);
-    need_new = __shfl_sync(0xffffffffu, need_new, src);
-    cnt = __shfl_sync(0xffffffffu, cnt, src);
     if (hit == 0u)
-        bsel = -1;
+        return;   // fewer than k keys counted
+    const int src = __ffs(hit) - 1;
+    const int above = __shfl_sync(0xffffffffu, excl, src);   // keys in the bins above src's
+    // src's bins, the top one on lane 0: a prefix sum from the top finds the bin
+    const int bin = kCoarseBins - kPer * src - 1 - lane;
+    const int cb = static_cast<int>(lds_u32(coarse_s + 4u * static_cast<uint32_t>(bin)));
+    int in2 = cb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, in2, o);
+        if (lane >= o)
+            in2 += n;
+    }
+    const unsigned hit2 = __ballot_sync(0xffffffffu, above + in2 - cb < k && k <= above + in2);
+    const int src2 = __ffs(hit2) - 1;   // always found: the bins of src hold the k-th key
+    bsel = kCoarseBins - kPer * src - 1 - src2;
+    need_new = k - __shfl_sync(0xffffffffu, above + in2 - cb, src2);
+    cnt = __shfl_sync(0xffffffffu, cb, src2);
 }
 
 // The exact top-k of one pair by one warp over the order keys of blocks [0, nb) (shared

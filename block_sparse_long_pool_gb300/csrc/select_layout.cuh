@@ -21,6 +21,7 @@ __host__ __device__ constexpr int fused_off_hist()
 {
     return kOffList;
 }
+static_assert(kOffList % 16 == 0, "the coarse histogram takes 16-byte reads");
 __host__ __device__ constexpr int fused_off_topk_list()
 {
     return kOffList + kCoarseBins * 4;
