@@ -107,6 +107,32 @@ def test_forecast_matches_oracle_and_the_separate_calls(H_q, H_kv, n_split):
     assert (O.float() - O_sep.float()).abs().max().item() <= 2 ** -7
 
 
+@pytest.mark.parametrize("k_cap", [7, 21, 67])
+@pytest.mark.parametrize("H_q,H_kv", [(16, 4), (64, 8)])
+def test_forecast_sixteen_cta_clusters_with_short_lists(H_q, H_kv, k_cap):
+    """Clusters of 16 CTAs with the group top-k: CTA 0 takes the next layer's top-k and
+    attends over nothing, the other 15 share the list (7 blocks: 8 of them get none) and
+    merge without CTA 0 (the pull form)."""
+    B, T_cap, N_cap = 1, 700 * BLK, 700
+    lens_b = [611 * BLK + 9]
+    n_init, n_local, k, k_tot_next = 1, 2, 32, 40
+    c = _case(B, H_q, H_kv, T_cap, lens_b, k_cap, N_cap, seed=H_q + k_cap)
+    O, lse, idx_next, cnt_next, st = _fused(c, B, H_q, H_kv, n_init, n_local, k, k_tot_next, 16)
+    assert st == 0
+    P, G = B * H_kv, H_q // H_kv
+    idx_sep = torch.full_like(idx_next, -7)
+    cnt_sep = torch.full_like(cnt_next, -7)
+    binding.sparse_select_topk(c["F"], c["ktil"], c["seq"], n_init, n_local, k, idx_sep, cnt_sep)
+    torch.cuda.synchronize()
+    assert torch.equal(idx_next, idx_sep) and torch.equal(cnt_next, cnt_sep)
+    Oref, lref = oracle.attn(bits(c["Q"]).reshape(P, G, D), bits(c["K"]).reshape(P, T_cap, D),
+                             bits(c["V"]).reshape(P, T_cap, D), c["idx_np"], c["cnt_np"], c["lens_p"])
+    assert_attn_close(O, Oref.reshape(B, H_q, D))
+    g, r = lse.cpu().double().numpy().reshape(lref.shape), lref
+    assert np.array_equal(np.isfinite(g), np.isfinite(r))
+    assert np.allclose(g[np.isfinite(r)], r[np.isfinite(r)], rtol=0, atol=2e-3)
+
+
 def test_forecast_ties_go_to_the_lower_index_exactly():
     # integer scores: fp32 and fp64 agree exactly, so the tie rule alone decides
     B, H_q, H_kv, T_cap, k_cap, N_cap = 2, 16, 2, 300 * BLK, 9, 300
