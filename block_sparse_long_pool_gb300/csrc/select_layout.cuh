@@ -46,8 +46,8 @@ inline size_t fused_smem_bytes(int per, int N_cap)
 // The slice [i0, i0 + cap) of the k_tot-long block list that CTA `rank` of a fused layer
 // attends over.  With the group top-k (`cta0_free`: CTA 0's consumer warps take the next
 // layer's top-k first) CTA 0 attends over nothing and the other S - 1 CTAs share the
-// list, the first k_tot % (S - 1) of them one block more; otherwise CTA r takes entries
-// [r * ceil(k_tot / S), ...).
+// list, the first k_tot % (S - 1) of them one block more; otherwise CTA 0 takes what is
+// left of k_tot after the other S - 1 take ceil(k_tot / S) each.
 __host__ __device__ inline void fused_slice(int k_tot, int S, int rank, bool cta0_free, int *i0, int *cap)
 {
     if (cta0_free && S > 1) {
@@ -61,8 +61,17 @@ __host__ __device__ inline void fused_slice(int k_tot, int S, int rank, bool cta
         *cap = base + (r < rem ? 1 : 0);
         return;
     }
+    // CTA 0 (the merge leader, whose selector warp shares its SM time) takes the short
+    // slice: entries [0, k_tot - (S - 1) * per), then the others ceil(k_tot / S) each
     const int per = (k_tot + S - 1) / S;
-    *i0 = rank * per < k_tot ? rank * per : k_tot;
+    const int cap0 = k_tot - (S - 1) * per > 0 ? k_tot - (S - 1) * per : 0;
+    if (rank == 0) {
+        *i0 = 0;
+        *cap = cap0;
+        return;
+    }
+    const int a = cap0 + (rank - 1) * per;
+    *i0 = a < k_tot ? a : k_tot;
     *cap = (*i0 + per < k_tot ? *i0 + per : k_tot) - *i0;
 }
 
