@@ -392,10 +392,13 @@ def kernel_breakdown(wk, dev, peak):
     L = wk.sh.layers
     reps_alone = 2 if L * 2 >= 160 else max(2, 160 // L)
 
-    def time_alone(fn, reps=reps_alone):
+    def time_alone(fn, reps=reps_alone, warmup=3):
         # synchronize, then the L2-evicting read (~85 us of GPU time), during which the
         # host enqueues the timed launch: the events bracket GPU work only, never a wait
-        # for the host to submit the launch
+        # for the host to submit the launch.  The untimed warm-up launches come first: the
+        # first launch of a kernel in the process loads its module (~0.8 ms).
+        for l in range(min(warmup, L)):
+            fn(l)
         ev = []
         for _ in range(reps):
             for l in range(L):
@@ -407,7 +410,10 @@ def kernel_breakdown(wk, dev, peak):
                 b.record()
                 ev.append((a, b))
         torch.cuda.synchronize(dev)
-        return statistics.mean(a.elapsed_time(b) for a, b in ev), len(ev)
+        t = sorted(a.elapsed_time(b) for a, b in ev)
+        dist = {"median_us": round(statistics.median(t) * 1e3, 2), "p10_us": round(t[len(t) // 10] * 1e3, 2),
+                "p90_us": round(t[(9 * len(t)) // 10] * 1e3, 2), "warmup_launches": min(warmup, L)}
+        return statistics.mean(t), len(t), dist
 
     def time_chain(fn, reps=5):
         # the L launches back to back in one graph (programmatic dependent launch
@@ -429,20 +435,20 @@ def kernel_breakdown(wk, dev, peak):
         return a.elapsed_time(b) / (reps * L)
 
     # the standalone decode attention (sparse_decode_attn, resident cache, no workspace)
-    att_alone_ms, att_n = time_alone(lambda l: wk._attend(l, cur, workspace=False))
+    att_alone_ms, att_n, att_dist = time_alone(lambda l: wk._attend(l, cur, workspace=False))
     att_chain_ms = time_chain(lambda l, st_: wk._attend(l, st_, workspace=False))
     att_bytes = wk.attn_bytes_per_launch()
     att_hash = kernel_source_hash(ATTN_SOURCES)
     # what a launch costs without streaming: the same launch with every count 0 (list
     # fetch, Q load, merge, O write), and a one-element torch kernel timed the same way
     zero_count = torch.zeros_like(wk.count[0])
-    att_empty_ms, _ = time_alone(lambda l: wk._attend(l, cur, count=zero_count, workspace=False), reps=1)
+    att_empty_ms, _, _ = time_alone(lambda l: wk._attend(l, cur, count=zero_count, workspace=False), reps=1)
     tiny = torch.zeros(1, device=dev)
-    floor_ms, _ = time_alone(lambda l: tiny.add_(1.0), reps=1)
+    floor_ms, _, _ = time_alone(lambda l: tiny.add_(1.0), reps=1)
     stream_ms = att_alone_ms - att_empty_ms
     attention = {"kernel": f"sparse_attn_kernel (sparse_decode_attn, decode, G={wk.sh.G})",
                  "algorithmic_bytes_per_launch": att_bytes,
-                 "alone": {"avg_launch_us": round(att_alone_ms * 1e3, 2), "launches_timed": att_n,
+                 "alone": {"avg_launch_us": round(att_alone_ms * 1e3, 2), "launches_timed": att_n, **att_dist,
                            "achieved": round(att_bytes / (att_alone_ms * 1e-3) / 1e9, 1),
                            "frac": round(att_bytes / (att_alone_ms * 1e-3) / 1e9 / peak, 4),
                            "empty_launch_us": round(att_empty_ms * 1e3, 2),
@@ -459,25 +465,25 @@ def kernel_breakdown(wk, dev, peak):
                              "note": f"{L} launches back to back in a CUDA graph, one per layer"},
                  "traffic": profiled_traffic(att_hash) if wk.sh.name == "decode_128k_70b_b8_80layers" else None,
                  "kernel_source_sha1": att_hash}
-    sel_alone_ms, sel_n = time_alone(lambda l: wk._select(l, wk.F[l - 1] if l else wk.F0, cur))
+    sel_alone_ms, sel_n, sel_dist = time_alone(lambda l: wk._select(l, wk.F[l - 1] if l else wk.F0, cur))
     sel_bytes = wk.select_bytes_per_launch()
     selection = {"kernel": "decode_forecast_kernel<1, false> (sparse_select_topk)",
                  "algorithmic_bytes_per_launch": sel_bytes,
-                 "alone": {"avg_launch_us": round(sel_alone_ms * 1e3, 2), "launches_timed": sel_n,
+                 "alone": {"avg_launch_us": round(sel_alone_ms * 1e3, 2), "launches_timed": sel_n, **sel_dist,
                            "achieved": round(sel_bytes / (sel_alone_ms * 1e-3) / 1e9, 1),
                            "frac": round(sel_bytes / (sel_alone_ms * 1e-3) / 1e9 / peak, 4)}}
     out = {"attention": attention, "selection": selection}
     if wk.mode == "fused":
-        dom_alone_ms, dom_n = time_alone(lambda l: wk._fused(l, cur))
+        dom_alone_ms, dom_n, dom_dist = time_alone(lambda l: wk._fused(l, cur))
         dom_bytes = wk.fused_bytes_per_launch()
         out["dominant"] = {"kernel": "decode_forecast_kernel (sparse_decode_attn_forecast: attention of layer l + "
                                      f"Forecast selection of layer l+1, G={wk.sh.G})",
                            "algorithmic_bytes_per_launch": dom_bytes, "source": FUSED_SOURCES,
-                           "alone_us": dom_alone_ms * 1e3, "alone_n": dom_n}
+                           "alone_us": dom_alone_ms * 1e3, "alone_n": dom_n, "alone_dist": dom_dist}
     else:
         out["dominant"] = {"kernel": f"sparse_attn_kernel (sparse_decode_attn, G={wk.sh.G})",
                            "algorithmic_bytes_per_launch": att_bytes, "source": ATTN_SOURCES,
-                           "alone_us": att_alone_ms * 1e3, "alone_n": att_n}
+                           "alone_us": att_alone_ms * 1e3, "alone_n": att_n, "alone_dist": att_dist}
     del flush
     return out
 
@@ -532,9 +538,10 @@ def measure_decode_step(args, sh, rank, world, local_rank, with_e2e=True):
                                          "average": round(step_bytes / launches)},
         "traffic_is": "dram__bytes_read.sum + dram__bytes_write.sum of one dominant launch (ncu), null unless "
                       "taken on the current kernel source",
-        "alone": {"avg_launch_us": round(dom["alone_us"], 2), "launches_timed": dom["alone_n"],
+        "alone": {"avg_launch_us": round(dom["alone_us"], 2), "launches_timed": dom["alone_n"], **dom["alone_dist"],
                   "achieved": round(alone_gbs, 1), "frac": round(alone_gbs / peak, 4),
-                  "note": "each launch timed by itself after a 512 MB read that evicts L2"},
+                  "note": "each launch timed by itself after a 512 MB read that evicts L2, after 3 untimed "
+                          "warm-up launches"},
         "kernel_source_sha1": dom_hash}
     line = {
         "value": round(value, 3), "unit": "steps/s", "n_gpus": world, "steps": K, "warmup": W,
