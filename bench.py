@@ -520,6 +520,8 @@ def measure_decode_step(args, sh, rank, world, local_rank, with_e2e=True):
     if sh.name == "decode_128k_70b_b8_80layers":
         dom_traffic = (profiled_traffic(dom_hash, "decode_forecast_128k_traffic.txt") if wk.mode == "fused"
                        else profiled_traffic(dom_hash))
+    elif sh.name == "decode_128k_70b_b1_80layers_resident" and wk.mode == "fused":
+        dom_traffic = profiled_traffic(dom_hash, "decode_forecast_128k_b1_traffic.txt")
     launches = wk.launches_per_step()
     achieved = step_bytes / (ms * 1e-3) / 1e9
     alone_gbs = dom["algorithmic_bytes_per_launch"] / (dom["alone_us"] * 1e-6) / 1e9
@@ -648,8 +650,12 @@ def run_ours(args, rank, world, local_rank):
 def run_b1_case(args, local_rank):
     """The literal B = 1 variant of the 128K step: all 80 layers resident (42.9 GB), 8
     pairs per layer, so a launch has 8 pairs to spread over the SMs."""
+    import dataclasses
     from block_sparse_long_pool_gb300 import workloads as wl
-    line = measure_decode_step(args, wl.DECODE_128K_B1, 0, 1, local_rank)
+    sh = wl.DECODE_128K_B1
+    if args.layers:   # fewer resident layers (the 80 launches cycle over them): small profiling captures
+        sh = dataclasses.replace(sh, name=f"{sh.name}_profiling_{args.layers}_physical", phys_layers=args.layers)
+    line = measure_decode_step(args, sh, 0, 1, local_rank)
     print(json.dumps(dict({"case": "decode128k_b1", "metric": METRIC}, **line)), flush=True)
 
 
@@ -1747,7 +1753,9 @@ def main():
                          "the other workloads, one line each")
     ap.add_argument("--case-cpu-seconds", type=float, default=3.0,
                     help="other cases: host seconds of oracle work for their cpu_baseline")
-    ap.add_argument("--layers", type=int, default=0, help="offload128k: layers (default 32; fewer for profiling)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="offload128k: layers (default 32); decode128k_b1: resident physical layers (default 80); "
+                         "fewer for profiling")
     ap.add_argument("--n-split", type=int, default=0)
     ap.add_argument("--no-workspace", action="store_true", help="layer case: attention without a workspace (cluster path)")
     ap.add_argument("--workspace", action="store_true",
