@@ -567,7 +567,7 @@ def measure_decode_step(args, sh, rank, world, local_rank, with_e2e=True):
         line["e2e"] = {"value": round(world * 1000.0 / e2e_ms, 3), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h}
     assert wk.status.item() == 0, f"device status {wk.status.item()}"
-    line["cpu_baseline"] = (cpu_baseline(wk, budget_s=args.cpu_seconds)
+    line["cpu_baseline"] = (cpu_baseline(wk, seconds=args.cpu_seconds)
                             if rank == 0 and not args.no_cpu_baseline else None)
     return line
 
@@ -712,16 +712,16 @@ def _slice_geometry(sh):
     return per_call, min(cores, per_call * sh.H_kv)
 
 
-def cpu_baseline(wk, budget_s: float = 15.0, slices: int = 4):
+def cpu_baseline(wk, seconds: float = 15.0, slices: int = 4):
     """The oracle on the host cores over a bounded sample of the decode step: layer
     slices of B_s batch elements (B_s x 8 pairs, one OpenMP thread per pair), repeated
-    until the time budget is spent, scaled to the step's layers x pairs."""
+    until that many seconds are spent, scaled to the step's layers x pairs."""
     per_call, threads = _slice_geometry(wk.sh)
     prepared = [_prepare_oracle_slice(wk, (7 * i) % wk.sh.layers,
                                       [(i * per_call + j) % wk.sh.B for j in range(per_call)])
                 for i in range(slices)]
     spent, pair_layers, reps = 0.0, 0, 0
-    while spent < budget_s or reps < len(prepared):
+    while spent < seconds or reps < len(prepared):
         dt, n = _time_oracle_slice(prepared[reps % len(prepared)], threads)
         spent += dt
         pair_layers += n
@@ -936,15 +936,15 @@ def case_roofline(kernel, nbytes, t_us, peak, peak_src, traffic=None, note=None)
     return out
 
 
-def oracle_baseline(fn, budget_s, units_per_call, unit, sample, min_reps=2):
+def oracle_baseline(fn, seconds, units_per_call, unit, sample, min_reps=2):
     """The oracle (as it stands) on the host cores: fn() runs one bounded sample of the
-    case's work in fp64, repeated until budget_s is spent; value = units per second,
+    case's work in fp64, repeated for at least `seconds` of host time; value = units per second,
     the sample scaled by units_per_call (the part of the case's unit of work it is)."""
     import oracle
     threads = len(os.sched_getaffinity(0))
     oracle.set_threads(threads)
     spent, reps = 0.0, 0
-    while spent < budget_s or reps < min_reps:
+    while spent < seconds or reps < min_reps:
         t0 = time.perf_counter()
         fn()
         spent += time.perf_counter() - t0
@@ -995,7 +995,7 @@ class _Layer:
                               workspace=self.ws, status=self.status, flags=self.attn_flags)
 
 
-def single_layer_oracle(lay, budget_s):
+def single_layer_oracle(lay, seconds):
     """The oracle on one decode step of a single-layer workload, all pairs: the
     compressed key of the block the appended token lands in (when the step appends),
     the Forecast selection and the attention, in fp64.  The compressed keys of the
@@ -1023,7 +1023,7 @@ def single_layer_oracle(lay, budget_s):
         idx, cnt, _ = oracle.select(F, ktil, lens, sh.n_init, sh.n_local, sh.k)
         oracle.attn(Q, K, V, idx, cnt, lens)
     what = ("append (the touched block's mean) + " if sh.n_new else "") + "select + attention"
-    return oracle_baseline(step, budget_s, 1.0, "steps/s", f"the whole step ({what}) of all {P} pairs in fp64")
+    return oracle_baseline(step, seconds, 1.0, "steps/s", f"the whole step ({what}) of all {P} pairs in fp64")
 
 
 def run_single_layer_case(args, dev, sh, name):
@@ -1346,7 +1346,7 @@ def run_offload_case(args, dev):
     print(json.dumps(line), flush=True)
 
 
-def offload_oracle(wk, budget_s):
+def offload_oracle(wk, seconds):
     """The oracle on one layer of the offloaded step, all pairs: the Forecast selection
     from the resident compressed keys, the staging copy of the selected blocks from the
     host cache into a ring, and the attention over the ring, in fp64; scaled to the
@@ -1371,7 +1371,7 @@ def offload_oracle(wk, budget_s):
         oracle.gather(Vh, idx, cnt, ring_v)
         # the same rows as the ring holds (a staged copy), read where the length mask is defined
         oracle.attn(Q, Kh, Vh, idx, cnt, lens)
-    return oracle_baseline(layer, budget_s, 1.0 / sh.layers, "steps/s",
+    return oracle_baseline(layer, seconds, 1.0 / sh.layers, "steps/s",
                            f"one layer of all {P} pairs (select + staging copy of K and V + attention) in fp64, "
                            f"scaled to {sh.layers} layers")
 
