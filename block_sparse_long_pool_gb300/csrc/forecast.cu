@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kFThreads, 2)
 
     WarpState<NT> st;
     st.reset();
-    bool go_sent = false;   // thread 0 of CTA 0: the push merge's "go" already sent
+    bool go_sent = false;   // warp 0 of CTA 0: the push merge's "go" already sent
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
@@ -298,8 +298,8 @@ __global__ void __launch_bounds__(kFThreads, 2)
             // every warp of this CTA is past its last key stage and it attends over
             // nothing: its ring is free, so the peers may push their states into it while
             // the top-k runs
-            if (ATTN && ready && tid == 0 && merge_pushes<NT>(S)) {
-                merge_send_go(base_s + kOffCtrl, S);
+            if (ATTN && ready && warp == 0 && merge_pushes<NT>(S)) {
+                merge_send_go(base_s + kOffCtrl, S, lane);
                 go_sent = true;
             }
             topk_forecast_cta<kSelKPT, kSelThreads / 32>(
