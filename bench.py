@@ -370,6 +370,9 @@ def time_graph_steps(graph, K, world, dev, clocks_gpu):
     with ClockSampler(clocks_gpu) as clocks:
         barrier(world)
         torch.cuda.synchronize(dev)
+        # ~1 ms of GPU spinning ahead of the start event, during which the host enqueues
+        # the replays: the timed region holds GPU work only, no wait for the host
+        torch.cuda._sleep(2_000_000)
         evs[0].record()
         for i in range(K):
             graph.replay()
